@@ -1,0 +1,456 @@
+"""Throughput of exact top-k / top-p selection on GB300: rows/s and HBM GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload 1..5] [--no-sweep]
+
+One step is one call of the whole selection pipeline (sample statistics,
+sigma-truncation, quaternary top-k / top-p pivot search, tie resolution,
+mask emission) over one batch of the workload. The headline workload is
+64 x 128256 fp32 logits with per-row top-k (workload 2); the JSON line also
+carries every workload's own number under "per_workload".
+
+Timing: W untimed steps, then exactly K steps bracketed by a barrier and a
+device synchronize, timed with CUDA events on the launching stream; inputs
+rotate over enough copies that the rotating set exceeds 3x the L2 size, so
+no step reads logits from L2. For N > 1 (torchrun) every rank processes its
+own batch (weak scaling; rows are independent, there is no collective on
+the data path) and the slowest rank's time is reported.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import WORKLOADS, assumptions, generate  # noqa: E402
+
+METRIC = "logit rows/sec and HBM GB/s (% of GB300 peak) for exact top-k/top-p masking"
+HEADLINE = 2
+KERNEL_SOURCES = [
+    os.path.join(ROOT, "top_selection_row_gb300", "csrc", f)
+    for f in ("qrita_kernel.cu", "qrita_device.cuh", "qrita_internal.h", "qrita_api.cpp")
+]
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (tested on CPU with gloo)
+# ---------------------------------------------------------------------------
+def dist_env():
+    """(rank, world, local_rank) from torchrun's environment; (0, 1, 0) alone."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate_rows_per_s(rows_per_rank: int, world: int, seconds_max: float) -> float:
+    """Whole-job throughput: every rank's rows over the slowest rank's time."""
+    return rows_per_rank * world / seconds_max
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_number: int):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    w = d.get("workloads", {}).get(str(workload_number))
+    return None if w is None else w.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
+            self.path = os.path.join(out_dir, f"clocks_{os.getpid()}.csv")
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return None
+        sms, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxes.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sms:
+            return None
+        return {"sm_mhz": float(np.median(sms)), "sm_max_mhz": float(max(maxes)),
+                "reasons": sorted(reasons), "samples": len(sms)}
+
+
+def workload_config(w, n_rot, l2_bytes):
+    return {
+        "workload": w.name,
+        "global_batch": w.B,
+        "vocab": w.V,
+        "logits_dtype": w.dtype,
+        "seed": 1000 + w.number,
+        "assumptions": assumptions(w.number),
+        "l2_defeat": f"inputs rotate over {n_rot} copies "
+                     f"({n_rot * w.B * w.V * (w.elem_bytes + 1) / 1e6:.0f} MB > 3 x L2 {l2_bytes / 1e6:.0f} MB)",
+    }
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def time_workload(number, steps, warmup, dev, world, l2_bytes, stream):
+    """Device timing of one workload; returns a dict of numbers."""
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    w = WORKLOADS[number]
+    logits, k, p = generate(number)
+    bytes_in = w.B * w.V * (w.elem_bytes + 1)
+    n_rot = max(1, math.ceil(3 * l2_bytes / bytes_in) + 1)
+    if w.dtype == "f32":
+        x0 = torch.from_numpy(logits).to(dev)
+    else:
+        x0 = torch.from_numpy(logits.view(np.int16)).to(dev).view(torch.bfloat16)
+    xs = [x0] + [x0.clone() for _ in range(n_rot - 1)]
+    outs = [torch.empty((w.B, w.V), dtype=torch.bool, device=dev) for _ in range(n_rot)]
+    kd = torch.from_numpy(k).to(dev)
+    pd = torch.from_numpy(p).to(dev)
+    k_arg = kd if w.number != 3 else kd  # k = V rows: top-k off per row
+    p_arg = pd
+    torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            q.qrita_select(xs[i % n_rot], k_arg, p_arg, out=outs[i % n_rot], stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            j = (warmup + i) % n_rot
+            ev[i][0].record(stream)
+            q.qrita_select(xs[j], k_arg, p_arg, out=outs[j], stream=stream)
+            ev[i][1].record(stream)
+        end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    total_ms = start.elapsed_time(end)
+    per_launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_s = max_over_ranks(total_ms / 1e3, world, dev)
+    del xs, outs
+    return {
+        "w": w,
+        "n_rot": n_rot,
+        "ms_per_step": total_s * 1e3 / steps,
+        "rows_per_s": aggregate_rows_per_s(w.B * steps, world, total_s),
+        "kernel_ms_mean": float(np.mean(per_launch_ms)),
+        "kernel_ms_median": float(np.median(per_launch_ms)),
+        "bytes_per_launch": w.B * w.bytes_per_row,
+        "launches": steps,
+    }
+
+
+def time_e2e(number, steps, warmup, dev, stream):
+    """End to end through qrita_select_host: pinned host logits / k / p in,
+    host mask out, copies inside the timed region."""
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    w = WORKLOADS[number]
+    logits, k, p = generate(number)
+    if w.dtype == "f32":
+        xh = torch.from_numpy(logits).pin_memory()
+    else:
+        xh = torch.from_numpy(logits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    kh = torch.from_numpy(k).pin_memory()
+    ph = torch.from_numpy(p).pin_memory()
+    out = torch.empty((w.B, w.V), dtype=torch.bool).pin_memory()
+    staging = torch.empty(q.host_staging_bytes(q.DTYPE_F32 if w.dtype == "f32" else q.DTYPE_BF16, w.B, w.V),
+                          dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        q.qrita_select_host(xh, kh, ph, out=out, staging=staging, stream=stream)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        q.qrita_select_host(xh, kh, ph, out=out, staging=staging, stream=stream)
+    dt = time.perf_counter() - t0
+    return {
+        "value": w.B * steps / dt,
+        "unit": "rows/s",
+        "h2d_bytes_per_step": w.B * w.V * w.elem_bytes + 8 * w.B,
+        "d2h_bytes_per_step": w.B * w.V,
+    }
+
+
+def oracle_rows_per_s(number, budget_s=10.0, max_rows=None):
+    """The CPU oracle as it stands, on a bounded sample of the workload's rows."""
+    from oracle import select_batch
+
+    w = WORKLOADS[number]
+    logits, k, p = generate(number)
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        r = done % w.B
+        select_batch(logits[r : r + 1], w.dtype, k[r : r + 1], p[r : r + 1])
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_rows is not None and done >= max_rows):
+            break
+    return done / el, done, el
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    import top_selection_row_gb300 as q
+
+    q.lib()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 1024 * 1024)
+    stream = torch.cuda.Stream(dev)
+    peak, peak_kind = measured_peaks()
+
+    per = {}
+    numbers = [args.workload] + ([n for n in WORKLOADS if n != args.workload] if not args.no_sweep else [])
+    for n in numbers:
+        steps = args.steps if n == args.workload else max(10, min(args.steps, 30))
+        warm = args.warmup if n == args.workload else 3
+        if n == args.workload:
+            with ClockSampler(local) as cs:
+                res = time_workload(n, steps, warm, dev, world, l2, stream)
+            res["clocks"] = cs.summary()
+        else:
+            res = time_workload(n, steps, warm, dev, world, l2, stream)
+        per[n] = res
+
+    head = per[args.workload]
+    w = head["w"]
+    achieved = head["bytes_per_launch"] / (head["kernel_ms_mean"] / 1e3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": head["rows_per_s"],
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded; shapes of the pages' workloads, no dataset)",
+        "config": dict(workload_config(w, head["n_rot"], l2), parallelism=f"rows, {world} GPU(s), no collective"),
+        "hbm_gbs": achieved,
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved,
+            "peak": peak,
+            "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json copy bandwidth)",
+            "unit": "GB/s",
+            "frac": achieved / peak,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": head["bytes_per_launch"],
+            "kernel_ms_mean": head["kernel_ms_mean"],
+        },
+        "gpu_launches": head["launches"],
+        "clocks": head.get("clocks"),
+        "per_workload": {},
+    }
+    for n, r in per.items():
+        ach = r["bytes_per_launch"] / (r["kernel_ms_median"] / 1e3) / 1e9
+        line["per_workload"][WORKLOADS[n].name] = {
+            "rows_per_s": r["rows_per_s"],
+            "kernel_ms_median": r["kernel_ms_median"],
+            "hbm_gbs": ach,
+            "frac_of_measured_peak": ach / peak,
+            "frac_of_8tbs_nominal": ach / 8000.0,
+        }
+    if rank == 0:
+        line["e2e"] = time_e2e(args.workload, max(3, min(args.steps, 20)), 2, dev, stream)
+        if not args.no_cpu_baseline:
+            v, rows, el = oracle_rows_per_s(args.workload, budget_s=args.cpu_seconds)
+            line["cpu_baseline"] = {
+                "value": v,
+                "unit": "rows/s",
+                "cores": 1,
+                "kind": "oracle",
+                "sample": f"{rows} rows of {w.name} in {el:.1f} s (numpy fp64 stable sort per row, one thread)",
+            }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    rows_per_step = 2
+    for _ in range(args.warmup):
+        oracle_rows_per_s(args.workload, budget_s=0.0, max_rows=1)
+    t0 = time.perf_counter()
+    total = 0
+    for _ in range(args.steps):
+        _, rows, _ = oracle_rows_per_s(args.workload, budget_s=1e9, max_rows=rows_per_step)
+        total += rows
+    el = time.perf_counter() - t0
+    v = total / el
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": v,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; shapes of the pages' workloads, no dataset)",
+        "config": {"workload": w.name, "global_batch": w.B, "vocab": w.V, "logits_dtype": w.dtype,
+                   "seed": 1000 + w.number, "parallelism": "CPU oracle, rank 0 only"},
+        "cpu_baseline": {"value": v, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_per_step} rows of {w.name} per step (numpy fp64 stable sort, one thread)"},
+        "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-sweep", action="store_true", help="time only the headline workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

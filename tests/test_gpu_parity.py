@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Pass rule (the oracle's): top-k masks and top-p masks of unflagged rows are
+bit-exact; rows whose boundary mass lies within 1e-6 relative of p may keep
+one token more or fewer. Workloads are the seeded synthetic batches of
+``workloads``; small cases run the oracle on every row, full-size cases on
+sampled rows plus invariants on every row.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+from oracle import select_batch, select_row
+from parity_helpers import check_against_oracle, compare_rows, invariant_failures, run_gpu, to_device, widen
+from workloads import WORKLOADS, generate
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import top_selection_row_gb300 as q
+
+    q.lib()  # must load: no fallback exists
+    return torch.device("cuda", 0)
+
+
+_cache = {}
+
+
+def workload(n, rows=None):
+    key = (n, rows)
+    if key not in _cache:
+        _cache[key] = generate(n, rows=rows)
+    return _cache[key]
+
+
+# ---------------------------------------------------------------------------
+# Workloads: leading rows at full V, every row against the oracle
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_workload_leading_rows(dev, n):
+    w = WORKLOADS[n]
+    rows = min(w.B, 24)
+    logits, k, p = workload(n, rows)
+    fails, flagged, got, st, info = check_against_oracle(logits, w.dtype, k, p, dev)
+    assert fails == [], fails[:5]
+
+
+# ---------------------------------------------------------------------------
+# Workloads at full size, launched exactly as the bench launches them
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_workload_full_size(dev, n):
+    w = WORKLOADS[n]
+    logits, k, p = workload(n)
+    got, st, info = run_gpu(logits, w.dtype, k, p, dev)
+    assert (st == 0).all()
+    # sampled rows against the oracle (evenly spaced plus seeded picks)
+    rng = np.random.default_rng(50 + n)
+    sample = sorted(set(np.linspace(0, w.B - 1, min(w.B, 16)).astype(int).tolist())
+                    | set(rng.choice(w.B, size=min(w.B, 16), replace=False).tolist()))
+    ref = select_batch(logits, w.dtype, k, p, rows=sample)
+    fails, flagged = compare_rows(got, st, ref)
+    assert fails == [], fails[:5]
+    # invariants on every row
+    bad = []
+    for r in range(w.B):
+        f = invariant_failures(widen(logits[r], w.dtype), got[r], int(k[r]), float(p[r]))
+        if f:
+            bad.append((r, f))
+    assert bad == [], bad[:5]
+    # diagnostics agree with the mask
+    assert np.array_equal(info["kept"], got.sum(axis=1).astype(np.uint32))
+
+
+# ---------------------------------------------------------------------------
+# Hand-worked rows
+# ---------------------------------------------------------------------------
+def test_golden_rows(dev, golden_rows):
+    for c in golden_rows:
+        x = np.array([c["x"]], np.float32)
+        got, st, _ = run_gpu(x, "f32", np.array([c["k"]]), np.array([c["p"]]), dev)
+        kept = sorted(np.nonzero(got[0])[0].tolist())
+        if c["status"] == "nonfinite":
+            assert st[0] == 1 and kept == [], c["name"]
+        elif c["ambiguous"]:
+            res = select_row(np.array(c["x"]), c["k"], c["p"])
+            ok = [sorted(np.nonzero(a)[0].tolist()) for a in (res.mask,) + res.alt_masks]
+            assert kept in ok, (c["name"], kept)
+        else:
+            assert st[0] == 0 and kept == c["kept"], (c["name"], kept, c["kept"])
+
+
+# ---------------------------------------------------------------------------
+# Edge cases: tiny and ragged V, every k / p corner, tie-heavy values
+# ---------------------------------------------------------------------------
+def _edge_batch(rng, V, B, dtype, kind):
+    if kind == "ties":
+        x = np.round(rng.standard_normal((B, V)) * 2) / 4
+    elif kind == "equal":
+        x = np.full((B, V), 0.5)
+    elif kind == "wide":
+        x = rng.standard_normal((B, V)) * 30
+    else:
+        x = rng.standard_normal((B, V))
+    x = x.astype(np.float32)
+    if dtype == "bf16":
+        from workloads import f32_to_bf16_bits
+
+        return f32_to_bf16_bits(x)
+    return x
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [1, 2, 3, 5, 7, 15, 16, 17, 31, 33, 100, 1000, 4097, 40000])
+def test_edge_sizes_and_parameters(dev, dtype, V):
+    rng = np.random.default_rng(V * 7 + (dtype == "bf16"))
+    ks = sorted({-3, 0, 1, 2, V // 2, V - 1, V, V + 1})
+    ps = [float("nan"), -1.0, 0.0, 1e-9, 0.3, 0.9, 0.999999, 1.0]
+    for kind in ("normal", "ties", "equal", "wide"):
+        combos = [(kk, pp) for kk in ks for pp in ps]
+        B = len(combos)
+        logits = _edge_batch(rng, V, B, dtype, kind)
+        k = np.array([c[0] for c in combos], np.int32)
+        p = np.array([c[1] for c in combos], np.float32)
+        fails, flagged, got, st, info = check_against_oracle(logits, dtype, k, p, dev)
+        assert fails == [], (kind, fails[:5])
+
+
+def test_special_values(dev):
+    V = 3000
+    rng = np.random.default_rng(5)
+    rows = []
+    base = rng.standard_normal(V).astype(np.float32)
+    r = base.copy(); r[17] = np.nan; rows.append(r)                      # NaN
+    r = base.copy(); r[2999] = np.inf; rows.append(r)                    # +inf
+    r = base.copy(); r[::3] = -np.inf; rows.append(r)                    # many -inf
+    rows.append(np.full(V, -np.inf, np.float32))                         # all -inf
+    r = np.zeros(V, np.float32); r[::2] = -0.0; rows.append(r)           # +-0 ties
+    r = (rng.integers(-3, 4, V) * np.float32(1.4e-45)).astype(np.float32); rows.append(r)  # subnormals
+    r = base.copy(); r[:5] = 1e30; rows.append(r)                        # huge finite
+    r = base.copy(); r[5:] = -3.0e38; rows.append(r)                     # float-lowest masking
+    r = np.full(V, 7.0, np.float32); rows.append(r)                      # constant
+    logits = np.stack(rows)
+    B = logits.shape[0]
+    for k_val, p_val in ((1, 1.0), (5, 1.0), (1500, 1.0), (0, 0.5), (0, 0.999), (10, 0.7), (2999, 0.2), (0, 1.0)):
+        k = np.full(B, k_val, np.int32)
+        p = np.full(B, p_val, np.float32)
+        fails, flagged, got, st, info = check_against_oracle(logits, "f32", k, p, dev)
+        assert fails == [], (k_val, p_val, fails[:5])
+        assert st[0] == 1 and st[1] == 1 and not got[0].any() and not got[1].any()
+
+
+def test_misaligned_rows(dev):
+    """Row starts off the 16-byte grid exercise the head / tail element paths."""
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    rng = np.random.default_rng(9)
+    for dtype, V in (("f32", 1001), ("f32", 4099), ("bf16", 1003), ("bf16", 8191)):
+        B = 6
+        full = _edge_batch(rng, V + 3, B, dtype, "ties")
+        k = np.array([1, 7, 100, 0, 500, 3], np.int32)
+        p = np.array([1.0, 0.8, 1.0, 0.6, 0.95, 0.3], np.float32)
+        for off in (1, 2, 3):
+            sub = np.ascontiguousarray(full[:, off : off + V])
+            # a contiguous [B, V] view starting `off` elements into a buffer
+            buf = torch.empty(B * V + off, dtype=torch.float32 if dtype == "f32" else torch.bfloat16, device=dev)
+            buf[off:] = to_device(sub.reshape(-1), dtype, dev)
+            x = buf[off:].view(B, V)
+            mask, st, _ = q.qrita_select_ex(x, torch.from_numpy(k).to(dev), torch.from_numpy(p).to(dev), row_status=True)
+            torch.cuda.synchronize()
+            got = mask.cpu().numpy().astype(np.uint8)
+            ref = select_batch(sub, dtype, k, p)
+            fails, _ = compare_rows(got, st.cpu().numpy(), ref)
+            assert fails == [], (dtype, V, off, fails[:3])
+
+
+# ---------------------------------------------------------------------------
+# Every path gives the same answer
+# ---------------------------------------------------------------------------
+def _mixed_batch():
+    parts = []
+    for n, rows in ((2, 6), (3, 6), (4, 8), (5, 8)):
+        logits, k, p = workload(n, rows)
+        parts.append((n, logits, k, p))
+    return parts
+
+
+@pytest.mark.parametrize(
+    "flags",
+    ["none", "no_trunc", "fallback", "key_pivots", "c1", "c2", "c4", "c8", "c16", "fallback_key_c16"],
+)
+def test_forced_paths_match_oracle(dev, flags):
+    import top_selection_row_gb300 as q
+
+    f = {
+        "none": 0,
+        "no_trunc": q.FLAG_NO_TRUNCATION,
+        "fallback": q.FLAG_FORCE_FALLBACK,
+        "key_pivots": q.FLAG_KEY_PIVOTS,
+        "c1": q.flag_cluster(1),
+        "c2": q.flag_cluster(2),
+        "c4": q.flag_cluster(4),
+        "c8": q.flag_cluster(8),
+        "c16": q.flag_cluster(16),
+        "fallback_key_c16": q.FLAG_FORCE_FALLBACK | q.FLAG_KEY_PIVOTS | q.flag_cluster(16),
+    }[flags]
+    for n, logits, k, p in _mixed_batch():
+        w = WORKLOADS[n]
+        if flags == "c1" and w.V * w.elem_bytes > 200 * 1024:
+            continue  # a whole row must fit one CTA's shared memory
+        if flags == "c2" and w.V * w.elem_bytes > 400 * 1024:
+            continue
+        fails, flagged, got, st, info = check_against_oracle(logits, w.dtype, k, p, dev, flags=f)
+        assert fails == [], (n, fails[:5])
+
+
+def test_deterministic_across_calls(dev):
+    logits, k, p = workload(4, 32)
+    first, _, _ = run_gpu(logits, "bf16", k, p, dev, row_info=False)
+    for _ in range(4):
+        again, _, _ = run_gpu(logits, "bf16", k, p, dev, row_info=False)
+        assert np.array_equal(first, again)
+
+
+# ---------------------------------------------------------------------------
+# Stage diagnostics against CPU restatements
+# ---------------------------------------------------------------------------
+def test_row_info_matches_cpu_restatements(dev):
+    import top_selection_row_gb300 as q
+
+    for n in (2, 3, 4):
+        w = WORKLOADS[n]
+        logits, k, p = workload(n, 16)
+        got, st, info = run_gpu(logits, w.dtype, k, p, dev)
+        ref = dict(select_batch(logits, w.dtype, k, p))
+        for r in range(logits.shape[0]):
+            x = widen(logits[r], w.dtype)
+            rec = info[r]
+            # |Z_t| is the count of logits >= t (A4), t the threshold used
+            if rec["path"] & q.PATH_TRUNC:
+                assert rec["survivors"] == int(np.count_nonzero(x >= np.float32(rec["threshold"])))
+            # m is the row max
+            assert rec["row_max"] == np.float32(x.max())
+            # the sample statistics describe the row's values
+            assert abs(rec["mu"] - x.mean()) < 0.5 * x.std() + 1e-3
+            assert 0.2 * x.std() < rec["sigma"] < 5 * x.std()
+            if not ref[r].ambiguous:
+                assert rec["kept"] == ref[r].kept
+                assert rec["boundary"] == np.float32(ref[r].boundary)
+                assert rec["n_boundary"] == ref[r].n_boundary
+
+
+def test_host_entry_point_matches_device_path(dev):
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    logits, k, p = workload(4, 12)
+    xd = to_device(logits, "bf16", dev)
+    want = q.qrita_select(xd, torch.from_numpy(k).to(dev), torch.from_numpy(p).to(dev))
+    torch.cuda.synchronize()
+    xh = xd.cpu().pin_memory()
+    out = q.qrita_select_host(xh, torch.from_numpy(k), torch.from_numpy(p))
+    assert torch.equal(out, want.cpu())
+
+
+def test_runs_on_a_side_stream(dev):
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    logits, k, p = workload(2, 8)
+    x = to_device(logits, "f32", dev)
+    kd = torch.from_numpy(k).to(dev)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        m = q.qrita_select(x, kd)
+    s.synchronize()
+    ref = select_batch(logits, "f32", k, None)
+    fails, _ = compare_rows(m.cpu().numpy().astype(np.uint8), np.zeros(8, np.int32), ref)
+    assert fails == []

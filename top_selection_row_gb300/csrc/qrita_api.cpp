@@ -1,0 +1,264 @@
+// C ABI of the selection library: argument checks, the delta tables, the
+// launch shape, and the host-buffer entry point. See include/qrita.h.
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <limits>
+
+#include <cuda_runtime.h>
+
+#include "qrita.h"
+#include "qrita_internal.h"
+
+namespace qrita {
+namespace {
+
+// ---------------------------------------------------------------------------
+// delta tables (Qrita technical summary, "Methodology", part 1: delta comes
+// from precomputed tables derived from the normal quantile function, adapted
+// to the target k or p). Phi^-1 is found by bisection on the C library's
+// erfc, Phi(z) = erfc(-z / sqrt 2) / 2, to a bracket of 1e-13.
+// ---------------------------------------------------------------------------
+double normal_cdf(double z) { return 0.5 * std::erfc(-z / std::sqrt(2.0)); }
+
+double normal_quantile(double prob) {
+  if (prob <= 0.0) return -std::numeric_limits<double>::infinity();
+  if (prob >= 1.0) return std::numeric_limits<double>::infinity();
+  double lo = -40.0, hi = 40.0;
+  for (int it = 0; it < 200 && hi - lo > 1e-13; ++it) {
+    const double mid = 0.5 * (lo + hi);
+    if (normal_cdf(mid) < prob) lo = mid;
+    else hi = mid;
+  }
+  return 0.5 * (lo + hi);
+}
+
+struct Tables {
+  float lut_k[kLutK];
+  float lut_p[kLutP];
+};
+
+Tables build_tables() {
+  Tables t;
+  for (int i = 0; i < kLutK; ++i) {
+    // Phi^-1(1 - u) = -Phi^-1(u), evaluated in the accurate lower tail
+    const double u = std::exp2(-0.5 * i);
+    t.lut_k[i] = static_cast<float>(-normal_quantile(u));
+  }
+  for (int i = 0; i < kLutP; ++i) {
+    const double q = std::exp2(-0.25 * i);
+    t.lut_p[i] = static_cast<float>(normal_quantile(q));
+  }
+  return t;
+}
+
+const Tables& tables() {
+  static const Tables t = build_tables();
+  return t;
+}
+
+// Truncation tuning (the pages give no constants; these only move speed,
+// never the result): u = alpha_k * k / V, truncation skipped above u_max.
+constexpr float kAlphaK = 2.0f;
+constexpr float kUMaxK = 0.25f;
+constexpr float kMarginP = 0.25f;
+
+// Shared memory a CTA may use while three CTAs still fit on one SM.
+constexpr size_t kSmemTarget = 74 * 1024;
+constexpr int kMinCap = 512;
+constexpr int kMaxCap = 4096;
+
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) {
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64 && n > 0) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int smem_optin() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) {
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  const int n = max_smem_per_block();
+  if (dev >= 0 && dev < 64 && n > 0) cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+int elem_bytes(int dtype) { return dtype == QRITA_DTYPE_F32 ? 4 : 2; }
+
+struct Shape {
+  int C;
+  int chunk;
+  int cap;
+  size_t smem;
+};
+
+// Launch shape: the row is split into C contiguous chunks (one CTA each, one
+// cluster per row). C grows until a chunk fits the shared-memory target, and
+// further for small batches so that more SMs share the work.
+int choose_shape(int dtype, int64_t B, int64_t V, uint32_t flags, Shape* out) {
+  const int s = elem_bytes(dtype);
+  const int optin = smem_optin();
+  if (optin <= 0) return QRITA_ECUDA;
+  int C = 1;
+  if (flags & QRITA_FLAG_CLUSTER_SET) {
+    const int shift = static_cast<int>((flags >> QRITA_FLAG_CLUSTER_SHIFT) & 7u);
+    if (shift > 4) return QRITA_EINVAL;
+    C = 1 << shift;
+  } else {
+    while (C < kMaxCluster && ((V + C - 1) / C) * s > 64 * 1024) C *= 2;
+    const int64_t sms = sm_count();
+    while (C < 8 && B * C < 2 * sms && (V + 2 * C - 1) / (2 * C) >= 2048) C *= 2;
+  }
+  int64_t chunk = (V + C - 1) / C;
+  chunk = (chunk + 15) / 16 * 16;
+  const size_t fixed_and_data = smem_bytes(dtype, static_cast<int>(chunk), 0);
+  int cap = kMinCap;
+  if (fixed_and_data + static_cast<size_t>(kMinCap) * 8 < kSmemTarget) {
+    cap = static_cast<int>((kSmemTarget - fixed_and_data) / 8);
+    cap = cap > kMaxCap ? kMaxCap : cap;
+  }
+  cap &= ~3;
+  const size_t smem = smem_bytes(dtype, static_cast<int>(chunk), cap);
+  if (smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
+  if (B * C > static_cast<int64_t>(std::numeric_limits<int32_t>::max())) return QRITA_EUNSUPPORTED;
+  out->C = C;
+  out->chunk = static_cast<int>(chunk);
+  out->cap = cap;
+  out->smem = smem;
+  return QRITA_OK;
+}
+
+int check_args(const void* logits, int dtype, int64_t B, int64_t V, const uint8_t* out_mask,
+               uint32_t flags) {
+  if (dtype != QRITA_DTYPE_F32 && dtype != QRITA_DTYPE_BF16) return QRITA_EINVAL;
+  if (B < 0 || V < 1 || V > std::numeric_limits<int32_t>::max()) return QRITA_EINVAL;
+  if (flags & ~QRITA_FLAG_KNOWN_MASK) return QRITA_EINVAL;
+  if (B == 0) return QRITA_OK;
+  if (logits == nullptr || out_mask == nullptr) return QRITA_EINVAL;
+  if (reinterpret_cast<uintptr_t>(logits) % static_cast<uintptr_t>(elem_bytes(dtype)) != 0)
+    return QRITA_EINVAL;
+  return QRITA_OK;
+}
+
+int select_impl(const void* logits, int dtype, int64_t B, int64_t V, const int32_t* k,
+                const float* p, uint8_t* out_mask, qrita_stream_t stream, uint32_t flags,
+                int32_t* row_status, qrita_row_info_t* row_info) {
+  int rc = check_args(logits, dtype, B, V, out_mask, flags);
+  if (rc != QRITA_OK || B == 0) return rc;
+  Shape sh;
+  rc = choose_shape(dtype, B, V, flags, &sh);
+  if (rc != QRITA_OK) return rc;
+  Params prm;
+  std::memset(&prm, 0, sizeof(prm));
+  prm.logits = logits;
+  prm.mask = out_mask;
+  prm.k = k;
+  prm.p = p;
+  prm.row_status = row_status;
+  prm.row_info = row_info;
+  prm.B = B;
+  prm.V = static_cast<int32_t>(V);
+  prm.C = sh.C;
+  prm.chunk = sh.chunk;
+  prm.cap = sh.cap;
+  prm.flags = flags;
+  prm.alpha_k = kAlphaK;
+  prm.margin_p = kMarginP;
+  prm.u_max_k = kUMaxK;
+  const Tables& t = tables();
+  std::memcpy(prm.lut_k, t.lut_k, sizeof(prm.lut_k));
+  std::memcpy(prm.lut_p, t.lut_p, sizeof(prm.lut_p));
+  const int e = launch_select(prm, dtype, sh.smem, stream);
+  return e == 0 ? QRITA_OK : QRITA_ECUDA;
+}
+
+size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+}  // namespace
+}  // namespace qrita
+
+extern "C" {
+
+int qrita_select(const void* logits, int dtype, int64_t B, int64_t V, const int32_t* k,
+                 const float* p, uint8_t* out_mask, qrita_stream_t stream) {
+  return qrita::select_impl(logits, dtype, B, V, k, p, out_mask, stream, 0u, nullptr, nullptr);
+}
+
+int qrita_select_ex(const void* logits, int dtype, int64_t B, int64_t V, const int32_t* k,
+                    const float* p, uint8_t* out_mask, qrita_stream_t stream, uint32_t flags,
+                    int32_t* row_status, qrita_row_info_t* row_info) {
+  return qrita::select_impl(logits, dtype, B, V, k, p, out_mask, stream, flags, row_status,
+                            row_info);
+}
+
+size_t qrita_host_staging_bytes(int dtype, int64_t B, int64_t V) {
+  if ((dtype != QRITA_DTYPE_F32 && dtype != QRITA_DTYPE_BF16) || B < 0 || V < 1 ||
+      V > std::numeric_limits<int32_t>::max())
+    return 0;
+  const size_t n = static_cast<size_t>(B) * static_cast<size_t>(V);
+  return qrita::align256(n * qrita::elem_bytes(dtype)) + qrita::align256(static_cast<size_t>(B) * 4) +
+         qrita::align256(static_cast<size_t>(B) * 4) + qrita::align256(n);
+}
+
+int qrita_select_host(const void* h_logits, int dtype, int64_t B, int64_t V, const int32_t* h_k,
+                      const float* h_p, uint8_t* h_mask, void* d_staging, size_t staging_bytes,
+                      qrita_stream_t stream) {
+  int rc = qrita::check_args(h_logits, dtype, B, V, h_mask, 0u);
+  if (rc != QRITA_OK || B == 0) return rc;
+  const size_t need = qrita_host_staging_bytes(dtype, B, V);
+  if (d_staging == nullptr || staging_bytes < need) return QRITA_EINVAL;
+  const size_t n = static_cast<size_t>(B) * static_cast<size_t>(V);
+  const size_t lb = n * qrita::elem_bytes(dtype);
+  unsigned char* base = static_cast<unsigned char*>(d_staging);
+  void* d_logits = base;
+  int32_t* d_k = reinterpret_cast<int32_t*>(base + qrita::align256(lb));
+  float* d_p = reinterpret_cast<float*>(base + qrita::align256(lb) + qrita::align256(B * 4));
+  uint8_t* d_mask = base + qrita::align256(lb) + 2 * qrita::align256(B * 4);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(d_logits, h_logits, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return QRITA_ECUDA;
+  if (h_k && cudaMemcpyAsync(d_k, h_k, B * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return QRITA_ECUDA;
+  if (h_p && cudaMemcpyAsync(d_p, h_p, B * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return QRITA_ECUDA;
+  rc = qrita::select_impl(d_logits, dtype, B, V, h_k ? d_k : nullptr, h_p ? d_p : nullptr, d_mask,
+                          stream, 0u, nullptr, nullptr);
+  if (rc != QRITA_OK) return rc;
+  if (cudaMemcpyAsync(h_mask, d_mask, n, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return QRITA_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return QRITA_ECUDA;
+  return QRITA_OK;
+}
+
+const char* qrita_strerror(int code) {
+  switch (code) {
+    case QRITA_OK:
+      return "success";
+    case QRITA_EINVAL:
+      return "invalid argument";
+    case QRITA_EUNSUPPORTED:
+      return "unsupported size: a row does not fit the shared memory of one cluster";
+    case QRITA_ECUDA:
+      return "CUDA runtime or launch error";
+    default:
+      return "unknown error code";
+  }
+}
+
+int qrita_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// Device helpers for the selection kernel: order-preserving keys, inline PTX
+// for mbarriers, TMA bulk copies and thread-block clusters (sm_90+ forms that
+// sm_103a keeps), and compensated fp32 sums.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qrita {
+namespace dev {
+
+// ---------------------------------------------------------------------------
+// Order-preserving 32-bit keys. key(a) < key(b) iff a < b for non-NaN floats,
+// with -0 mapped to the key of +0 so the two tie (the stable-sort contract
+// treats them as equal). Keys below key(-inf) or above key(+inf) are NaNs.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kKeyNegInf = 0x007FFFFFu;
+constexpr uint32_t kKeyPosInf = 0xFF800000u;
+constexpr uint32_t kKeyNegZero = 0x7FFFFFFFu;  // never produced by f2key
+
+__device__ __forceinline__ uint32_t f2key(float x) {
+  uint32_t b = __float_as_uint(x + 0.0f);  // -0 + 0 = +0; every other value unchanged
+  uint32_t m = static_cast<uint32_t>(static_cast<int32_t>(b) >> 31) | 0x80000000u;
+  return b ^ m;
+}
+
+__device__ __forceinline__ float key2f(uint32_t k) {
+  uint32_t b = (k & 0x80000000u) ? (k ^ 0x80000000u) : ~k;
+  return __uint_as_float(b);
+}
+
+// Float a pivot key compares against: "x > pivot_f(q)" counts exactly the
+// elements with key(x) > q. The one key with no canonical element, -0's raw
+// key, is moved one step down (both keys count the same set).
+__device__ __forceinline__ float pivot_f(uint32_t q) {
+  return key2f(q == kKeyNegZero ? kKeyNegZero - 1u : q);
+}
+
+// NaN-propagating max (max.NaN): a NaN anywhere makes the result NaN.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Compensated fp32 sums: a value is hi + lo with |lo| <= ulp(hi)/2.
+// two_sum is Knuth's error-free addition (6 flops, no ordering condition).
+// ---------------------------------------------------------------------------
+struct F2 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+__device__ __forceinline__ void f2_add(F2& acc, float w) {
+  float s, e;
+  two_sum(acc.hi, w, s, e);
+  acc.hi = s;
+  acc.lo += e;
+}
+
+__device__ __forceinline__ F2 f2_merge(F2 a, F2 b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  e += a.lo + b.lo;
+  F2 r;
+  r.hi = s + e;
+  r.lo = e - (r.hi - s);
+  return r;
+}
+
+__device__ __forceinline__ double f2_value(F2 a) { return static_cast<double>(a.hi) + a.lo; }
+
+// ---------------------------------------------------------------------------
+// Shared-memory addressing, mbarriers and TMA bulk copies.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+// One 1-D bulk copy global -> this CTA's shared memory, completing on bar.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(phase)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for phase `phase` of bar: gives up after `limit_ns` of wall
+// time (checked every 64 polls) and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, phase)) return true;
+    if ((it & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters and distributed shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Full cluster barrier: every thread of every CTA of the cluster arrives
+// (release) and waits (acquire). The non-.aligned forms are used so that a
+// warp need not be converged when it reaches the barrier.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile(
+      "barrier.cluster.arrive.release;\n\t"
+      "barrier.cluster.wait.acquire;" ::
+          : "memory");
+}
+
+__device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t ld_dsmem_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ double ld_dsmem_f64(uint32_t addr) {
+  double v;
+  asm volatile("ld.shared::cluster.f64 %0, [%1];" : "=d"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+}  // namespace dev
+}  // namespace qrita

@@ -1,0 +1,65 @@
+// Internal interface between the C ABI (qrita_api.cpp) and the kernel
+// translation unit (qrita_kernel.cu). Not installed; not part of the ABI.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "qrita.h"
+
+namespace qrita {
+
+// delta tables (Qrita technical summary, "Methodology", part 1: precomputed
+// tables from the normal quantile function, keyed on the target k or p).
+//   lut_k[i] = Phi^-1(1 - 2^(-i/2)),  i = 0..63   (keyed on u = alpha*k/V;
+//              the kernel takes i = floor(-2 log2 u), so 2^(-i/2) >= u)
+//   lut_p[i] = Phi^-1(2^(-i/4)),      i = 0..63   (keyed on q = 1 - p;
+//              the kernel takes i = ceil(-4 log2 q), so 2^(-i/4) <= q)
+// Rounding the key toward the larger u / smaller q lowers the threshold, so
+// the table never makes truncation less likely to hit than the exact value.
+constexpr int kLutK = 64;
+constexpr int kLutP = 64;
+
+// Threads per CTA of the selection kernel.
+constexpr int kThreads = 256;
+// Bytes of one TMA bulk piece of a row chunk (a multiple of 16 * kThreads).
+constexpr int kPieceBytes = 16 * 1024;
+// Most pieces a chunk may have (one mbarrier each).
+constexpr int kMaxPieces = 16;
+// Largest cluster the launcher uses.
+constexpr int kMaxCluster = 16;
+// Upper bound on quaternary rounds of one search (a guard: the pivot rule
+// halves the key range at least every round on average, so 32-bit keys need
+// at most 34 rounds).
+constexpr int kMaxRounds = 64;
+
+struct Params {
+  const void* logits;
+  uint8_t* mask;
+  const int32_t* k;
+  const float* p;
+  int32_t* row_status;
+  qrita_row_info_t* row_info;
+  int64_t B;
+  int32_t V;
+  int32_t C;        // CTAs per row (cluster size)
+  int32_t chunk;    // elements per CTA (multiple of 16)
+  int32_t cap;      // survivor / candidate list capacity per CTA
+  uint32_t flags;   // QRITA_FLAG_*
+  float alpha_k;    // top-k truncation safety factor (u = alpha_k * k / V)
+  float margin_p;   // subtracted from the top-p delta
+  float u_max_k;    // no truncation when alpha_k * k / V exceeds this
+  float lut_k[kLutK];
+  float lut_p[kLutP];
+};
+
+// Bytes of dynamic shared memory the kernel needs for a chunk and list size.
+size_t smem_bytes(int dtype, int chunk, int cap);
+
+// Launch the selection kernel (grid B*C, cluster C). Returns a cudaError_t.
+int launch_select(const Params& prm, int dtype, size_t smem, qrita_stream_t stream);
+
+// Largest dynamic shared memory per block on the current device.
+int max_smem_per_block();
+
+}  // namespace qrita
