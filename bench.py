@@ -190,8 +190,9 @@ def workload_config(w, n_rot, l2_bytes):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def time_workload(number, steps, warmup, dev, world, l2_bytes, stream):
-    """Device timing of one workload; returns a dict of numbers."""
+def time_workload(number, steps, warmup, dev, world, l2_bytes, stream, rotate=None):
+    """Device timing of one workload; returns a dict of numbers. ``rotate``
+    overrides the number of rotating input copies (profiling runs use 1)."""
     import torch
 
     import top_selection_row_gb300 as q
@@ -199,7 +200,7 @@ def time_workload(number, steps, warmup, dev, world, l2_bytes, stream):
     w = WORKLOADS[number]
     logits, k, p = generate(number)
     bytes_in = w.B * w.V * (w.elem_bytes + 1)
-    n_rot = max(1, math.ceil(3 * l2_bytes / bytes_in) + 1)
+    n_rot = max(1, math.ceil(3 * l2_bytes / bytes_in) + 1) if rotate is None else rotate
     if w.dtype == "f32":
         x0 = torch.from_numpy(logits).to(dev)
     else:
@@ -323,10 +324,10 @@ def run_ours(args):
         warm = args.warmup if n == args.workload else 3
         if n == args.workload:
             with ClockSampler(local) as cs:
-                res = time_workload(n, steps, warm, dev, world, l2, stream)
+                res = time_workload(n, steps, warm, dev, world, l2, stream, args.rotate)
             res["clocks"] = cs.summary()
         else:
-            res = time_workload(n, steps, warm, dev, world, l2, stream)
+            res = time_workload(n, steps, warm, dev, world, l2, stream, args.rotate)
         per[n] = res
 
     head = per[args.workload]
@@ -374,7 +375,8 @@ def run_ours(args):
             "frac_of_8tbs_nominal": ach / 8000.0,
         }
     if rank == 0:
-        line["e2e"] = time_e2e(args.workload, max(3, min(args.steps, 20)), 2, dev, stream)
+        if not args.no_e2e:
+            line["e2e"] = time_e2e(args.workload, max(3, min(args.steps, 20)), 2, dev, stream)
         if not args.no_cpu_baseline:
             v, rows, el = oracle_rows_per_s(args.workload, budget_s=args.cpu_seconds)
             line["cpu_baseline"] = {
@@ -443,6 +445,9 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true", help="time only the headline workload")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rotate", type=int, default=None,
+                    help="input copies to rotate over (default: enough to exceed 3x L2)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -60,8 +60,8 @@ enum {
   QRITA_OK = 0,
   QRITA_EINVAL = 1,       /* bad argument: null pointer, B < 0, V < 1, V > 2^31-1,
                              unknown dtype, misaligned element pointer, bad flags */
-  QRITA_EUNSUPPORTED = 2, /* valid but outside this build: a row larger than the
-                             shared memory of a 16-CTA cluster (V*elem > 3 MiB) */
+  QRITA_EUNSUPPORTED = 2, /* valid but outside this build: B*C CTAs above 2^31-1,
+                             or no launch shape fits the device */
   QRITA_ECUDA = 3         /* a CUDA runtime call or the launch failed */
 };
 
@@ -71,8 +71,8 @@ enum {
   QRITA_ROW_NONFINITE = 1,  /* NaN or +inf in the row: mask all zero */
   QRITA_ROW_SEARCH_CAP = 2, /* pivot search exceeded its round cap: mask all zero
                                (cannot happen by construction; kept as a guard) */
-  QRITA_ROW_TIMEOUT = 3     /* a bounded wait on a shared-memory copy gave up:
-                               mask all zero */
+  QRITA_ROW_TIMEOUT = 3     /* reserved for a bounded wait that gives up; this
+                               build has no such wait and never reports it */
 };
 
 /* Flags of qrita_select_ex (path forcing for tests and ablations). */
@@ -91,7 +91,7 @@ enum {
 #define QRITA_PATH_TRUNC 0x4u     /* sigma-truncation pass ran */
 #define QRITA_PATH_HIT 0x8u       /* truncation hit: the search ran on Z_t */
 #define QRITA_PATH_FALLBACK 0x10u /* the search ran on the full row */
-#define QRITA_PATH_OVERFLOW 0x20u /* Z_t did not fit the shared-memory list */
+#define QRITA_PATH_OVERFLOW 0x20u /* Z_t did not fit a CTA's shared-memory list */
 #define QRITA_PATH_KEEP_ALL 0x40u /* both filters off: every token kept */
 
 /* Diagnostics of one row (qrita_select_ex, optional). Device memory. */
@@ -109,7 +109,8 @@ typedef struct qrita_row_info {
   uint32_t kept;       /* kept tokens */
   uint32_t status;     /* QRITA_ROW_* (same as row_status[r]) */
   double z;            /* softmax denominator top-p normalised by (0 if top-p off) */
-  double reserved;
+  uint32_t passes;     /* distributed narrowing passes (fallback searches) */
+  uint32_t reserved;
 } qrita_row_info_t;
 
 /*

@@ -50,7 +50,8 @@ ROW_INFO_DTYPE = np.dtype(
         ("kept", "<u4"),
         ("status", "<u4"),
         ("z", "<f8"),
-        ("reserved", "<f8"),
+        ("passes", "<u4"),
+        ("reserved", "<u4"),
     ]
 )
 assert ROW_INFO_DTYPE.itemsize == 64

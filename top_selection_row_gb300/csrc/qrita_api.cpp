@@ -65,10 +65,16 @@ constexpr float kAlphaK = 2.0f;
 constexpr float kUMaxK = 0.25f;
 constexpr float kMarginP = 0.25f;
 
-// Shared memory a CTA may use while three CTAs still fit on one SM.
-constexpr size_t kSmemTarget = 74 * 1024;
-constexpr int kMinCap = 512;
-constexpr int kMaxCap = 4096;
+// Candidate list capacities (entries of value + index): a CTA's own list
+// and the gathered set every CTA of a row searches. Four CTAs of 256 threads
+// fit on one SM with these.
+constexpr int kOwnCap = 2048;
+constexpr int kGatherCap = 4096;
+constexpr int kCtasPerSm = 4;
+// Rows shorter than this per CTA are not split further.
+constexpr int64_t kMinChunk = 1024;
+// Chunk indices must fit below the rank bits of a gathered tag.
+constexpr int64_t kMaxChunk = int64_t(1) << 27;
 
 int sm_count() {
   static std::atomic<int> cached[64];
@@ -102,42 +108,40 @@ int elem_bytes(int dtype) { return dtype == QRITA_DTYPE_F32 ? 4 : 2; }
 struct Shape {
   int C;
   int chunk;
-  int cap;
+  int ocap;
+  int gcap;
   size_t smem;
 };
 
 // Launch shape: the row is split into C contiguous chunks (one CTA each, one
-// cluster per row). C grows until a chunk fits the shared-memory target, and
-// further for small batches so that more SMs share the work.
-int choose_shape(int dtype, int64_t B, int64_t V, uint32_t flags, Shape* out) {
-  const int s = elem_bytes(dtype);
+// cluster per row). C is the largest power of two that keeps the whole batch
+// in one wave of resident CTAs, so small batches spread over every SM while
+// large batches keep one CTA per row and stream it whole.
+int choose_shape(int64_t B, int64_t V, uint32_t flags, Shape* out) {
   const int optin = smem_optin();
   if (optin <= 0) return QRITA_ECUDA;
+  const size_t smem = smem_bytes(kOwnCap, kGatherCap);
+  if (smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
   int C = 1;
   if (flags & QRITA_FLAG_CLUSTER_SET) {
     const int shift = static_cast<int>((flags >> QRITA_FLAG_CLUSTER_SHIFT) & 7u);
     if (shift > 4) return QRITA_EINVAL;
     C = 1 << shift;
   } else {
-    while (C < kMaxCluster && ((V + C - 1) / C) * s > 64 * 1024) C *= 2;
-    const int64_t sms = sm_count();
-    while (C < 8 && B * C < 2 * sms && (V + 2 * C - 1) / (2 * C) >= 2048) C *= 2;
+    const int64_t slots = static_cast<int64_t>(sm_count()) * kCtasPerSm;
+    while (C < kMaxCluster && B * (2 * C) <= slots && (V + 2 * C - 1) / (2 * C) >= kMinChunk) C *= 2;
+  }
+  while ((V + C - 1) / C > kMaxChunk) {
+    if (C >= kMaxCluster) return QRITA_EUNSUPPORTED;
+    C *= 2;
   }
   int64_t chunk = (V + C - 1) / C;
   chunk = (chunk + 15) / 16 * 16;
-  const size_t fixed_and_data = smem_bytes(dtype, static_cast<int>(chunk), 0);
-  int cap = kMinCap;
-  if (fixed_and_data + static_cast<size_t>(kMinCap) * 8 < kSmemTarget) {
-    cap = static_cast<int>((kSmemTarget - fixed_and_data) / 8);
-    cap = cap > kMaxCap ? kMaxCap : cap;
-  }
-  cap &= ~3;
-  const size_t smem = smem_bytes(dtype, static_cast<int>(chunk), cap);
-  if (smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
   if (B * C > static_cast<int64_t>(std::numeric_limits<int32_t>::max())) return QRITA_EUNSUPPORTED;
   out->C = C;
   out->chunk = static_cast<int>(chunk);
-  out->cap = cap;
+  out->ocap = kOwnCap;
+  out->gcap = kGatherCap;
   out->smem = smem;
   return QRITA_OK;
 }
@@ -160,7 +164,7 @@ int select_impl(const void* logits, int dtype, int64_t B, int64_t V, const int32
   int rc = check_args(logits, dtype, B, V, out_mask, flags);
   if (rc != QRITA_OK || B == 0) return rc;
   Shape sh;
-  rc = choose_shape(dtype, B, V, flags, &sh);
+  rc = choose_shape(B, V, flags, &sh);
   if (rc != QRITA_OK) return rc;
   Params prm;
   std::memset(&prm, 0, sizeof(prm));
@@ -174,7 +178,8 @@ int select_impl(const void* logits, int dtype, int64_t B, int64_t V, const int32
   prm.V = static_cast<int32_t>(V);
   prm.C = sh.C;
   prm.chunk = sh.chunk;
-  prm.cap = sh.cap;
+  prm.ocap = sh.ocap;
+  prm.gcap = sh.gcap;
   prm.flags = flags;
   prm.alpha_k = kAlphaK;
   prm.margin_p = kMarginP;

@@ -22,15 +22,16 @@ constexpr int kLutP = 64;
 
 // Threads per CTA of the selection kernel.
 constexpr int kThreads = 256;
-// Bytes of one TMA bulk piece of a row chunk (a multiple of 16 * kThreads).
-constexpr int kPieceBytes = 16 * 1024;
-// Most pieces a chunk may have (one mbarrier each).
-constexpr int kMaxPieces = 16;
-// Largest cluster the launcher uses.
+// 16-byte units each thread keeps in flight while streaming a chunk.
+constexpr int kUnroll = 4;
+// Largest cluster the launcher uses (16 needs the non-portable opt-in).
 constexpr int kMaxCluster = 16;
-// Upper bound on quaternary rounds of one search (a guard: the pivot rule
-// halves the key range at least every round on average, so 32-bit keys need
-// at most 34 rounds).
+// Pivots one distributed narrowing pass evaluates: two quaternary levels,
+// the 3 quartile pivots of the range and the 3 of each of its 4 quarters.
+constexpr int kNarrowPivots = 15;
+// Upper bound on quaternary rounds of one local search and on narrowing
+// passes (guards; the pivot rule at least halves the key range every round
+// on average, so 32-bit keys need at most about 34 rounds).
 constexpr int kMaxRounds = 64;
 
 struct Params {
@@ -44,7 +45,8 @@ struct Params {
   int32_t V;
   int32_t C;        // CTAs per row (cluster size)
   int32_t chunk;    // elements per CTA (multiple of 16)
-  int32_t cap;      // survivor / candidate list capacity per CTA
+  int32_t ocap;     // own candidate list capacity per CTA (entries)
+  int32_t gcap;     // gathered candidate set capacity per CTA (entries)
   uint32_t flags;   // QRITA_FLAG_*
   float alpha_k;    // top-k truncation safety factor (u = alpha_k * k / V)
   float margin_p;   // subtracted from the top-p delta
@@ -53,8 +55,8 @@ struct Params {
   float lut_p[kLutP];
 };
 
-// Bytes of dynamic shared memory the kernel needs for a chunk and list size.
-size_t smem_bytes(int dtype, int chunk, int cap);
+// Bytes of dynamic shared memory the kernel needs for the list capacities.
+size_t smem_bytes(int ocap, int gcap);
 
 // Launch the selection kernel (grid B*C, cluster C). Returns a cudaError_t.
 int launch_select(const Params& prm, int dtype, size_t smem, qrita_stream_t stream);

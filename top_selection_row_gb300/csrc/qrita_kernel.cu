@@ -1,31 +1,34 @@
 // Fused exact top-k / top-p selection kernel for GB300 (sm_103a).
 //
 // Method: Qrita technical summary (gist.science, paper 2602.01518),
-// "Methodology" parts 1-2 and "Implementation details" (pipeline). One
-// thread-block cluster handles one row: each of its C CTAs owns a contiguous
-// chunk of the row, staged once from HBM into its shared memory with TMA bulk
-// copies and kept there for every later pass, so the logits are read from HBM
-// exactly once and the mask is written exactly once. Per-stage partial
-// results are merged across the cluster through distributed shared memory.
+// "Methodology" parts 1-2 and "Implementation details" (pipeline).
 //
-// Stages (each ends with one cluster-wide merge):
-//   A2  sample-block statistics mu, sigma (8 blocks of 64 logits per chunk)
-//   A3  delta from the normal-quantile tables, t = mu + delta*sigma
-//   A4  truncation pass: Z_t = {x >= t} compacted into a shared-memory list,
-//       row max / min, NaN / +inf detection
-//       (top-p rows without top-k: one more pass for Z = sum exp(x - m))
-//   A5  hit / fallback decision (|Z_t| >= k, or mass(Z_t) >= p Z (1 + 1e-5))
-//   A6  quaternary top-k pivot search over Z_t (hit) or the resident chunk
-//       (fallback), tracking z_mn / N_zmn per pivot
-//   A7  the same search with softmax mass in place of counts, for top-p
-//   A8  boundary ties kept by lowest token id (prefix count across the
-//       cluster ranks, then in index order inside the one straddling CTA)
-//   A9  mask emission: one coalesced pass over the resident chunk
+// One thread-block cluster of C CTAs handles one row; CTA c owns a contiguous
+// chunk of the row. The row is streamed from HBM once:
 //
-// Every decision is computed identically by every thread of the cluster
-// from merged values, so control flow, and with it every cluster barrier, is
-// uniform. The only waits are bounded mbarrier waits (an expired wait marks
-// the row QRITA_ROW_TIMEOUT) and hardware cluster barriers.
+//   A2  mu, sigma (and a reference max) from one sample block of the row,
+//       read identically by every CTA of the cluster (no exchange needed);
+//   A3  delta from the normal-quantile tables, t = mu + delta * sigma;
+//   A4  one streaming pass over the chunk keeps Z_t = {x >= t} (value and
+//       index) in a shared-memory list, and tracks max / min / NaN / +inf and,
+//       for top-p without top-k, the softmax mass of the row and of Z_t;
+//   --  one cluster merge through distributed shared memory;
+//   A5  hit: every CTA gathers the whole Z_t into its shared memory;
+//       fallback (miss, or too many candidates): distributed narrowing passes
+//       evaluate two quaternary levels (15 pivots) per cluster merge until the
+//       range that holds the boundary fits, then that range is gathered;
+//   A6  quaternary pivot search over the gathered candidates with
+//       z_mn / N_zmn duplicate tracking, inside each CTA (block barriers only);
+//   A7  the same search by softmax mass for top-p;
+//   A8  boundary duplicates kept by lowest token id: per-rank counts from the
+//       gathered set, then an index cut inside the one straddling CTA;
+//   A9  mask emission: hit rows write zeros and scatter the kept ids of the
+//       CTA's own list (no second read of the logits); fallback rows stream
+//       the chunk again.
+//
+// Every decision that steers a barrier is taken from merged values that are
+// identical in every CTA of the cluster and published through shared memory,
+// so control flow, and with it every barrier, is uniform.
 
 #include <cfloat>
 #include <cmath>
@@ -43,23 +46,13 @@ using namespace dev;
 
 constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kFull = 0xffffffffu;
-constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;  // 200 ms
-constexpr int kSampleBlocks = 8;
-constexpr int kSampleBlock = 64;  // kSampleBlocks * kSampleBlock == 2 * kThreads
-
-#ifdef QRITA_TRACE
-// Debug-only record of the search rounds of row 0 (built with -DQRITA_TRACE).
-__device__ double g_trace[4096];
-__device__ unsigned g_trace_n;
-__device__ void trace_put(double a, double b, double c, double d, double e, double f, double g, double h,
-                          double i, double j) {
-  const unsigned n = g_trace_n;
-  if (n + 10 > 4096) return;
-  const double v[10] = {a, b, c, d, e, f, g, h, i, j};
-  for (int t = 0; t < 10; ++t) g_trace[n + t] = v[t];
-  g_trace_n = n + 10;
-}
-#endif
+constexpr int kSampleBlocks = 16;
+constexpr int kSampleBlock = 64;  // 16 x 64 = 1024 sampled logits per row
+constexpr int kBins = kNarrowPivots + 1;
+constexpr int kTagShift = 28;  // gathered tag = rank << 28 | index in chunk
+// Pinned narrowing (from below only) gives up after this many passes and
+// narrows from both ends (a tie group at the boundary larger than the lists).
+constexpr int kPinnedPasses = 12;
 
 template <int DT>
 struct Elem;
@@ -97,37 +90,47 @@ __device__ __forceinline__ void unpack(const uint4 v, float (&x)[Elem<DT>::kPerU
 template <int DT>
 __device__ __forceinline__ float load_elem(const unsigned char* p) {
   if constexpr (DT == QRITA_DTYPE_F32) {
-    return *reinterpret_cast<const float*>(p);
+    return __ldg(reinterpret_cast<const float*>(p));
   } else {
-    return __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(p)) << 16);
+    return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
   }
 }
 
-template <int DT>
-__device__ __forceinline__ void copy_elem(unsigned char* dst, const unsigned char* src) {
-  if constexpr (DT == QRITA_DTYPE_F32) {
-    *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
-  } else {
-    *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(src);
-  }
+__device__ __forceinline__ uint4 ldg16(const unsigned char* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+// Read of shared state another thread wrote before a barrier. Every such read
+// goes through a volatile shared load so the compiler can neither reuse an
+// earlier load of the same word nor move the load across the barrier.
+template <typename T>
+__device__ __forceinline__ T vld(const T& r) {
+  return *reinterpret_cast<const volatile T*>(&r);
+}
+
+// Softmax weight of x for row max m. A row whose max is -inf holds only
+// -inf, and equal logits get equal weight 1.
+__device__ __forceinline__ float weight(float x, float m, bool m_neginf) {
+  return m_neginf ? 1.0f : expf(x - m);
 }
 
 // ---------------------------------------------------------------------------
 // Shared-memory layout
 // ---------------------------------------------------------------------------
-struct alignas(16) PivotPart {  // one pivot's partial (exchanged between ranks)
-  double mass;                  // softmax mass of the elements above the pivot
-  uint32_t cnt;                 // elements above the pivot
-  float z;                      // z_mn: smallest element above the pivot
-  uint32_t nz;                  // N_zmn: how many elements equal z
-  uint32_t pad;
-};
-
-struct alignas(16) Slot {  // what one CTA publishes for one merge
-  PivotPart pv[3];
-  double d[2];
+struct alignas(16) Slot {  // what one CTA publishes for one cluster merge
+  unsigned long long mass[kBins + 1];  // narrowing: per-bin fixed-point mass; [kBins] above hi
+  uint32_t cnt[kBins + 1];             // narrowing: per-bin counts; [kBins] above hi
   float f[4];
   uint32_t u[4];
+  double d[2];
+};
+
+struct alignas(16) Bcast {  // written by one thread / warp 0 before a block barrier
+  double d[8];
+  float f[12];
+  uint32_t u[24];
+  uint32_t q[16];  // pivot keys, increasing
+  float qf[16];    // pivot floats (+inf padding)
 };
 
 struct alignas(16) PAccS {  // per-warp pivot partial (block reduction scratch)
@@ -139,34 +142,36 @@ struct alignas(16) PAccS {  // per-warp pivot partial (block reduction scratch)
 };
 
 struct alignas(16) Fixed {
-  uint64_t bars[kMaxPieces];
   Slot slots[2];
-  Slot mg;  // merged result of the latest merge
+  Bcast bc;
   PAccS red[kWarps][3];
   float redf[kWarps][8];
-  uint32_t redu[kWarps][4];
-  uint32_t rank_cnt[3][kMaxCluster];  // latest round, per rank and pivot
-  float rank_z[3][kMaxCluster];
-  uint32_t rank_nz[3][kMaxCluster];
-  uint32_t rank_surv[kMaxCluster];   // survivors per rank
-  uint32_t cnt_lo[kMaxCluster];      // per-rank count above the search's lo
-  uint32_t cnt_hi[kMaxCluster];      // per-rank count above the search's hi
-  uint32_t ties[kMaxCluster];        // per-rank count of boundary-valued elements
+  uint32_t redu[kWarps][kBins];
+  uint32_t bin_cnt[kWarps][kBins];
+  unsigned long long bin_mass[kWarps][kBins];
+  uint32_t rank_bins[kMaxCluster][kBins + 1];  // latest narrowing merge, per rank
+  uint32_t rank_n[kMaxCluster];   // per-rank entries to gather
+  uint32_t rank_lo[kMaxCluster];  // per-rank count above the narrowing lo
+  uint32_t rank_hi[kMaxCluster];  // per-rank count above the narrowing hi
+  uint32_t ties[kMaxCluster];     // per-rank count of boundary-valued elements
   uint32_t scan[kWarps];
-  uint32_t list_n;
-  uint32_t err;
+  uint32_t own_n;
+  uint32_t g_n;
 };
 
-// Read of shared state another thread wrote before a barrier. Every such read
-// goes through a volatile shared load so the compiler can neither reuse an
-// earlier load of the same word nor move the load across the barrier.
-template <typename T>
-__device__ __forceinline__ T vld(const T& r) {
-  return *reinterpret_cast<const volatile T*>(&r);
-}
+// Names of the broadcast slots
+enum : int {
+  // floats
+  BF_MU = 0, BF_SIGMA, BF_MREF, BF_T, BF_MAX, BF_MIN, BF_SMIN, BF_LOF, BF_HIF,
+  // uints
+  BU_TRUNC = 0, BU_SMIN_N, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
+  BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW,
+  // doubles
+  BD_ZR = 0, BD_MR, BD_MLO, BD_MHI, BD_TARGET, BD_TOTAL,
+};
 
 // ---------------------------------------------------------------------------
-// Pivot accumulators
+// Pivot accumulators of the local search
 // ---------------------------------------------------------------------------
 struct PAcc {
   uint32_t cnt;
@@ -211,8 +216,9 @@ __device__ __forceinline__ PAcc pacc_shfl_xor(const PAcc& a, int off) {
   return o;
 }
 
-// Per-element update of the three pivots. Unused pivots are +inf (nothing
-// exceeds them). Predicated, so the warp never diverges here.
+// Per-element update of three pivots: count above, softmax mass above, and
+// z_mn / N_zmn (smallest element above the pivot and its multiplicity).
+// Unused pivots are +inf. Predicated, so the warp never diverges here.
 template <bool MASS>
 __device__ __forceinline__ void pacc_update(PAcc (&acc)[3], const float (&qf)[3], float x, float w) {
 #pragma unroll
@@ -227,12 +233,6 @@ __device__ __forceinline__ void pacc_update(PAcc (&acc)[3], const float (&qf)[3]
   }
 }
 
-// Softmax weight of x for row max m. A row whose max is -inf holds only
-// -inf, and equal logits get equal weight 1.
-__device__ __forceinline__ float weight(float x, float m, bool m_neginf) {
-  return m_neginf ? 1.0f : expf(x - m);
-}
-
 // ---------------------------------------------------------------------------
 // Warp / block helpers
 // ---------------------------------------------------------------------------
@@ -242,14 +242,25 @@ __device__ __forceinline__ float warp_sum_f(float v) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t warp_sum_u(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
 // Exclusive scan of a per-thread count over the block, in thread order.
-// Returns the exclusive prefix; *total receives the block total.
 __device__ __forceinline__ uint32_t block_excl_scan(Fixed& F, uint32_t v, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t t = __shfl_up_sync(kFull, incl, o);
+    const uint32_t t = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += t;
   }
   if (lane == 31) F.scan[warp] = incl;
@@ -266,32 +277,32 @@ __device__ __forceinline__ uint32_t block_excl_scan(Fixed& F, uint32_t v, uint32
   return wbase + incl - v;
 }
 
-// Warp-aggregated append of up to E flagged values to the shared list.
-// Every lane of the warp must call it (convergent).
+// Warp-aggregated append of the flagged values of a unit (value and index)
+// to a shared list. Every lane of the warp must call it (convergent).
 template <int E>
-__device__ __forceinline__ void warp_append(Fixed& F, float* list_x, float* list_w, uint32_t cap,
-                                            const float (&xs)[E], const float (&ws)[E],
-                                            uint32_t bits, bool with_w) {
+__device__ __forceinline__ void warp_append(uint32_t* counter, float* vals, uint32_t* idxs,
+                                            uint32_t cap, const float (&xs)[E], uint32_t idx0,
+                                            uint32_t bits) {
   const int lane = threadIdx.x & 31;
   const uint32_t c = __popc(bits);
   if (__ballot_sync(kFull, c != 0) == 0) return;
   uint32_t incl = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t t = __shfl_up_sync(kFull, incl, o);
+    const uint32_t t = __shfl_up_sync(kFull, incl, o);
     if (lane >= o) incl += t;
   }
   const uint32_t total = __shfl_sync(kFull, incl, 31);
   uint32_t base = 0;
-  if (lane == 31) base = atomicAdd(&F.list_n, total);
+  if (lane == 31) base = atomicAdd(counter, total);
   base = __shfl_sync(kFull, base, 31);
   uint32_t pos = base + incl - c;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     if ((bits >> e) & 1u) {
       if (pos < cap) {
-        list_x[pos] = xs[e];
-        if (with_w) list_w[pos] = ws[e];
+        vals[pos] = xs[e];
+        idxs[pos] = idx0 + e;
       }
       ++pos;
     }
@@ -299,408 +310,686 @@ __device__ __forceinline__ void warp_append(Fixed& F, float* list_x, float* list
 }
 
 // ---------------------------------------------------------------------------
-// Pivot choice: 25/50/75 % of the current range (lo, hi] of keys
+// Pivots: 25/50/75 % of a key range (lo, hi]
 // ---------------------------------------------------------------------------
 // Value-space quartiles (the pages' reading of "25/50/75 % of the search
-// range") when both ends are finite floats and the previous value-space
-// round shrank the key range at least by half; otherwise quartiles of the
-// 32-bit key range, which always shrink it fourfold. Returns how many
-// pivots are set (1..3); unused pivots are +inf.
-__device__ __forceinline__ int choose_pivots(uint32_t lo, uint32_t hi, bool value_ok,
-                                             uint32_t (&q)[3], float (&qf)[3], bool* used_value) {
-  const uint32_t span = hi - lo;  // >= 2
-  int np;
+// range") when value_ok and both ends are finite floats; otherwise quartiles
+// of the 32-bit key range, which always shrink it fourfold. Writes up to 3
+// strictly increasing keys inside (lo, hi) and returns how many.
+__device__ int quartile_pivots(uint32_t lo, uint32_t hi, bool value_ok, uint32_t* q, bool* used_value) {
+  const uint32_t span = hi - lo;
   *used_value = false;
+  if (span <= 1u) return 0;
   if (span <= 4u) {
-    np = static_cast<int>(span) - 1;
-    for (int j = 0; j < 3; ++j) q[j] = lo + 1u + static_cast<uint32_t>(j < np ? j : np - 1);
-  } else {
-    np = 3;
-    bool done = false;
-    if (value_ok) {
-      const float vlo = key2f(lo), vhi = key2f(hi);
-      if (isfinite(vlo) && isfinite(vhi)) {
-        const double dl = vlo, dh = vhi;
-        const uint32_t a = f2key(static_cast<float>(dl + 0.25 * (dh - dl)));
-        const uint32_t b = f2key(static_cast<float>(dl + 0.50 * (dh - dl)));
-        const uint32_t c = f2key(static_cast<float>(dl + 0.75 * (dh - dl)));
-        if (lo < a && a < b && b < c && c < hi) {
-          q[0] = a;
-          q[1] = b;
-          q[2] = c;
-          done = true;
-          *used_value = true;
-        }
+    const int np = static_cast<int>(span) - 1;
+    for (int j = 0; j < np; ++j) q[j] = lo + 1u + static_cast<uint32_t>(j);
+    return np;
+  }
+  if (value_ok) {
+    const float vlo = key2f(lo), vhi = key2f(hi);
+    if (isfinite(vlo) && isfinite(vhi)) {
+      const double dl = vlo, dh = vhi;
+      const uint32_t a = f2key(static_cast<float>(dl + 0.25 * (dh - dl)));
+      const uint32_t b = f2key(static_cast<float>(dl + 0.50 * (dh - dl)));
+      const uint32_t c = f2key(static_cast<float>(dl + 0.75 * (dh - dl)));
+      if (lo < a && a < b && b < c && c < hi) {
+        q[0] = a;
+        q[1] = b;
+        q[2] = c;
+        *used_value = true;
+        return 3;
       }
     }
-    if (!done) {
-      for (int j = 0; j < 3; ++j)
-        q[j] = lo + static_cast<uint32_t>((static_cast<uint64_t>(span) * (j + 1)) >> 2);
-    }
   }
-  for (int j = 0; j < 3; ++j) qf[j] = (j < np) ? pivot_f(q[j]) : INFINITY;
-  return np;
+  for (int j = 0; j < 3; ++j) q[j] = lo + static_cast<uint32_t>((static_cast<uint64_t>(span) * (j + 1)) >> 2);
+  return 3;
+}
+
+// Two quaternary levels at once: the quartile pivots of (lo, hi] and of each
+// of the four sub-ranges they cut. Returns the count (<= 15), keys sorted.
+__device__ int two_level_pivots(uint32_t lo, uint32_t hi, bool value_ok, uint32_t* q, bool* used_value) {
+  uint32_t l1[3];
+  const int n1 = quartile_pivots(lo, hi, value_ok, l1, used_value);
+  int n = 0;
+  uint32_t a = lo;
+  for (int s = 0; s <= n1; ++s) {
+    const uint32_t b = (s < n1) ? l1[s] : hi;
+    uint32_t l2[3];
+    bool uv = false;
+    const int n2 = quartile_pivots(a, b, value_ok, l2, &uv);
+    for (int j = 0; j < n2; ++j) q[n++] = l2[j];
+    if (s < n1) q[n++] = l1[s];
+    a = b;
+  }
+  return n;
 }
 
 // ---------------------------------------------------------------------------
-// The kernel
+// Per-CTA context
 // ---------------------------------------------------------------------------
 template <int DT>
 struct Ctx {
   static constexpr int E = Elem<DT>::kPerUnit;
   static constexpr int S = Elem<DT>::kBytes;
   Fixed* F;
-  float* list_x;
-  float* list_w;
-  const unsigned char* sbody;  // shared: first 16-byte unit of the chunk body
-  uint32_t cap;
+  float* own_val;
+  uint32_t* own_idx;
+  uint32_t ocap;
+  float* g_val;
+  uint32_t* g_tag;
+  uint32_t gcap;
+  const unsigned char* gx;     // chunk start in global memory
+  const unsigned char* gbody;  // first 16-byte aligned unit of the chunk
+  uint8_t* gmask;              // chunk start in the mask
   int n, head_n, body_units, tail_n;
   uint32_t C, crank;
-  float m;
+  int ph;           // cluster merge counter (slot parity)
+  float m;          // row max (softmax shift)
   bool m_neginf;
-  int ph;  // merge counter (slot parity)
+  float fix_scale;  // fixed-point scale of weights in [0, 1]
 };
 
-// Element e of the chunk in shared memory, by chunk-local index class.
-template <int DT>
-__device__ __forceinline__ float head_elem(const Ctx<DT>& c, int i) {
-  return load_elem<DT>(c.sbody - (c.head_n - i) * Ctx<DT>::S);
-}
-template <int DT>
-__device__ __forceinline__ float tail_elem(const Ctx<DT>& c, int j) {
-  return load_elem<DT>(c.sbody + 16 * c.body_units + j * Ctx<DT>::S);
+// Stream the chunk from global memory: kUnroll 16-byte units per thread in
+// flight, then the head / tail elements (fewer than 2E, one per thread).
+// unit_fn(xs, idx0, valid) and scalar_fn(x, idx, valid) are called by every
+// thread the same number of times (convergent), valid or not.
+template <int DT, typename UnitFn, typename ScalarFn>
+__device__ __forceinline__ void stream_chunk(const Ctx<DT>& c, UnitFn&& unit_fn, ScalarFn&& scalar_fn) {
+  constexpr int E = Ctx<DT>::E;
+  constexpr int S = Ctx<DT>::S;
+  const int tid = threadIdx.x;
+  const int nb = c.body_units;
+  for (int base = 0; base < nb; base += kThreads * kUnroll) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int u = base + j * kThreads + tid;
+      v[j] = (u < nb) ? ldg16(c.gbody + 16 * static_cast<size_t>(u)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kUnroll; ++j) {
+      const int u = base + j * kThreads + tid;
+      float xs[E];
+      unpack<DT>(v[j], xs);
+      unit_fn(xs, static_cast<uint32_t>(c.head_n + u * E), u < nb);
+    }
+  }
+  float x = 0.f;
+  uint32_t idx = 0;
+  const bool valid = tid < c.head_n + c.tail_n;
+  if (valid) {
+    if (tid < c.head_n) {
+      x = load_elem<DT>(c.gx + tid * S);
+      idx = static_cast<uint32_t>(tid);
+    } else {
+      const int j = tid - c.head_n;
+      x = load_elem<DT>(c.gbody + 16 * static_cast<size_t>(nb) + j * S);
+      idx = static_cast<uint32_t>(c.head_n + nb * E + j);
+    }
+  }
+  scalar_fn(x, idx, valid);
 }
 
-// Publish pivot partials, cluster barrier, merge all ranks (warp 0), and
-// broadcast through F->mg. above_cnt / above_mass account for this CTA's
-// elements above its list's range (list mode), which exceed every pivot.
+// ---------------------------------------------------------------------------
+// Distributed narrowing (fallback search over the lists or the chunk)
+// ---------------------------------------------------------------------------
+struct Range {
+  uint32_t lo, hi;      // count/mass(> lo) >= target > count/mass(> hi)
+  uint32_t c_lo, c_hi;  // row counts above lo / hi
+  double m_lo, m_hi;    // row masses above lo / hi (fixed-point units)
+  bool lo_all;          // lo lies below key(-inf): every element is above it
+  bool pin_hi;          // narrow from below only: gather everything above lo
+  bool fits;            // the range fits the lists: gather it
+  bool exact;           // hi - lo <= 1: the boundary value is hi
+  bool below;           // the target exceeds everything above lo: the boundary is lo itself
+  int passes;
+};
+
+// One narrowing pass: up to 15 pivots (two quaternary levels) cut (lo, hi]
+// into bins; every CTA bins its elements (from its list, or by streaming its
+// chunk again), the bins merge across the cluster in rank order, and warp 0
+// keeps the bin that holds the boundary. Counts are exact integers and
+// masses exact sums of fixed-point weights, so the merge is deterministic.
+// target < 0 means "p_frac times (the pass's total mass + extra)": the pass
+// then also measures the softmax denominator.
 template <int DT, bool MASS>
-__device__ __forceinline__ void reduce_merge_pivots(Ctx<DT>& c, PAcc (&acc)[3], uint32_t above_cnt,
-                                                    double above_mass) {
+__device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac, double extra,
+                            bool from_chunk, bool value_ok, bool* used_value_out) {
+  constexpr int E = Ctx<DT>::E;
   Fixed& F = *c.F;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int j = 0; j < 3; ++j) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      PAcc t = pacc_shfl_xor<MASS>(acc[j], o);
-      pacc_combine<MASS>(acc[j], t);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  if (tid == 0) {
+    uint32_t q[kNarrowPivots];
+    bool used_value = false;
+    const int np = two_level_pivots(R.lo, R.hi, value_ok, q, &used_value);
+    for (int j = 0; j < 16; ++j) {
+      F.bc.q[j] = (j < np) ? q[j] : R.hi;
+      F.bc.qf[j] = (j < np) ? pivot_f(q[j]) : INFINITY;
     }
-    if (lane == 0) {
-      F.red[warp][j].cnt = acc[j].cnt;
-      F.red[warp][j].z = acc[j].z;
-      F.red[warp][j].nz = acc[j].nz;
-      F.red[warp][j].mhi = acc[j].m.hi;
-      F.red[warp][j].mlo = acc[j].m.lo;
+    F.bc.u[BU_NP] = static_cast<uint32_t>(np);
+    F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
+    F.bc.f[BF_LOF] = R.lo_all ? -INFINITY : pivot_f(R.lo);
+    F.bc.f[BF_HIF] = pivot_f(R.hi);
+  }
+  for (int i = tid; i < kWarps * kBins; i += kThreads) {
+    (&F.bin_cnt[0][0])[i] = 0u;
+    (&F.bin_mass[0][0])[i] = 0ull;
+  }
+  __syncthreads();
+  const float lo_f = vld(F.bc.f[BF_LOF]);
+  const float hi_f = vld(F.bc.f[BF_HIF]);
+  const bool lo_all = R.lo_all;
+  const float scale = c.fix_scale;
+  uint32_t above_c = 0;
+  unsigned long long above_m = 0ull;
+  auto bin_one = [&](float x) {
+    if (!(lo_all || x > lo_f)) return;
+    unsigned long long wf = 0ull;
+    if (MASS) wf = __float2ull_rn(weight(x, c.m, c.m_neginf) * scale);
+    if (x > hi_f) {
+      ++above_c;
+      above_m += wf;
+      return;
     }
+    // bin = number of pivots below x (pivots increasing, +inf padded)
+    int b = 0;
+    b += (x > vld(F.bc.qf[b + 7])) ? 8 : 0;
+    b += (x > vld(F.bc.qf[b + 3])) ? 4 : 0;
+    b += (x > vld(F.bc.qf[b + 1])) ? 2 : 0;
+    b += (x > vld(F.bc.qf[b])) ? 1 : 0;
+    atomicAdd(&F.bin_cnt[warp][b], 1u);
+    if (MASS) atomicAdd(&F.bin_mass[warp][b], wf);
+  };
+  if (from_chunk) {
+    stream_chunk<DT>(
+        c,
+        [&](const float (&xs)[E], uint32_t, bool valid) {
+          if (!valid) return;
+#pragma unroll
+          for (int e = 0; e < E; ++e) bin_one(xs[e]);
+        },
+        [&](float x, uint32_t, bool valid) {
+          if (valid) bin_one(x);
+        });
+  } else {
+    const uint32_t n = min(vld(F.own_n), c.ocap);
+    for (uint32_t i = tid; i < n; i += kThreads) bin_one(c.own_val[i]);
+  }
+  above_c = warp_sum_u(above_c);
+  above_m = warp_sum_u64(above_m);
+  if (lane == 0) {
+    F.redu[warp][0] = above_c;
+    F.redu[warp][1] = static_cast<uint32_t>(above_m);
+    F.redu[warp][2] = static_cast<uint32_t>(above_m >> 32);
   }
   __syncthreads();
   Slot& my = F.slots[c.ph & 1];
-  if (warp == 0) {
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      PAcc a;
-      pacc_init(a);
-      if (lane < kWarps) {
-        a.cnt = vld(F.red[lane][j].cnt);
-        a.z = vld(F.red[lane][j].z);
-        a.nz = vld(F.red[lane][j].nz);
-        a.m.hi = vld(F.red[lane][j].mhi);
-        a.m.lo = vld(F.red[lane][j].mlo);
-      }
-#pragma unroll
-      for (int o = kWarps / 2; o > 0; o >>= 1) {
-        PAcc t = pacc_shfl_xor<MASS>(a, o);
-        pacc_combine<MASS>(a, t);
-      }
-      if (lane == 0) {
-        my.pv[j].cnt = a.cnt + above_cnt;
-        my.pv[j].z = a.z;
-        my.pv[j].nz = a.nz;
-        my.pv[j].mass = MASS ? (f2_value(a.m) + above_mass) : 0.0;
-      }
+  if (tid < kBins) {
+    uint32_t s = 0;
+    unsigned long long sm = 0ull;
+    for (int w = 0; w < kWarps; ++w) {
+      s += vld(F.bin_cnt[w][tid]);
+      sm += vld(F.bin_mass[w][tid]);
     }
+    my.cnt[tid] = s;
+    my.mass[tid] = sm;
+  } else if (tid == kBins) {
+    uint32_t s = 0;
+    unsigned long long sm = 0ull;
+    for (int w = 0; w < kWarps; ++w) {
+      s += vld(F.redu[w][0]);
+      sm += static_cast<unsigned long long>(vld(F.redu[w][1])) |
+            (static_cast<unsigned long long>(vld(F.redu[w][2])) << 32);
+    }
+    my.cnt[kBins] = s;
+    my.mass[kBins] = sm;
   }
   cluster_sync_all();
   if (warp == 0) {
-    const uint32_t base = smem_u32(&my);
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      uint32_t cnt = 0, nz = 0;
-      float z = INFINITY;
-      double mass = 0.0;
-      if (lane < static_cast<int>(c.C)) {
-        const uint32_t a = map_rank(base + j * static_cast<uint32_t>(sizeof(PivotPart)), lane);
-        mass = ld_dsmem_f64(a);
-        cnt = ld_dsmem_u32(a + 8);
-        z = ld_dsmem_f32(a + 12);
-        nz = ld_dsmem_u32(a + 16);
-        F.rank_cnt[j][lane] = cnt;
-        F.rank_z[j][lane] = z;
-        F.rank_nz[j][lane] = nz;
-      }
-#pragma unroll
-      for (int o = 8; o > 0; o >>= 1) {
-        const uint32_t cnt2 = __shfl_xor_sync(kFull, cnt, o);
-        const float z2 = __shfl_xor_sync(kFull, z, o);
-        const uint32_t nz2 = __shfl_xor_sync(kFull, nz, o);
-        const double m2 = __shfl_xor_sync(kFull, mass, o);
-        cnt += cnt2;
-        if (z2 < z) {
-          z = z2;
-          nz = nz2;
-        } else if (z2 == z) {
-          nz += nz2;
+    // lane b sums bin b over the ranks in rank order and keeps per-rank counts
+    uint32_t tot_c = 0;
+    unsigned long long tot_m = 0ull;
+    if (lane <= kBins) {
+      const uint32_t cnt_addr = smem_u32(&my.cnt[lane]);
+      const uint32_t mass_addr = smem_u32(&my.mass[lane]);
+      for (uint32_t r = 0; r < c.C; ++r) {
+        const uint32_t cr = ld_dsmem_u32(map_rank(cnt_addr, r));
+        F.rank_bins[r][lane] = cr;
+        tot_c += cr;
+        if (MASS) {
+          const uint32_t ma = map_rank(mass_addr, r);
+          tot_m += static_cast<unsigned long long>(ld_dsmem_u32(ma)) |
+                   (static_cast<unsigned long long>(ld_dsmem_u32(ma + 4)) << 32);
         }
-        mass += m2;
-      }
-      if (lane == 0) {
-        F.mg.pv[j].cnt = cnt;
-        F.mg.pv[j].z = z;
-        F.mg.pv[j].nz = nz;
-        F.mg.pv[j].mass = mass;
       }
     }
+    const int np = static_cast<int>(vld(F.bc.u[BU_NP]));
+    uint32_t bc_all[kBins + 1];
+    unsigned long long bm_all[kBins + 1];
+#pragma unroll
+    for (int b = 0; b <= kBins; ++b) {
+      bc_all[b] = __shfl_sync(kFull, tot_c, b);
+      bm_all[b] = __shfl_sync(kFull, tot_m, b);
+    }
+    __syncwarp();  // per-rank bins visible to the whole warp
+    int lo_j = -1, hi_j = -1;
+    if (lane == 0) {
+      // cum[b] = elements above pivot b-1 (cum[0]: above lo); top: above hi
+      uint32_t cum_c[kBins + 1];
+      double cum_m[kBins + 1];
+      uint32_t cc = bc_all[kBins];
+      double cm = static_cast<double>(bm_all[kBins]);
+      for (int b = np; b >= 0; --b) {
+        cc += bc_all[b];
+        cm += static_cast<double>(bm_all[b]);
+        cum_c[b] = cc;
+        cum_m[b] = cm;
+      }
+      double tgt = target;
+      if (tgt < 0.0) {
+        tgt = p_frac * (cum_m[0] + extra);
+        F.bc.d[BD_TOTAL] = cum_m[0];
+      }
+      F.bc.d[BD_TARGET] = tgt;
+      F.bc.u[BU_BELOW] = ((MASS ? cum_m[0] : static_cast<double>(cum_c[0])) < tgt) ? 1u : 0u;
+      for (int j = 0; j < np; ++j) {
+        const double above = MASS ? cum_m[j + 1] : static_cast<double>(cum_c[j + 1]);
+        if (above >= tgt) {
+          lo_j = j;
+        } else {
+          hi_j = j;
+          break;
+        }
+      }
+      if (R.pin_hi) hi_j = -1;
+      uint32_t nlo = R.lo, nhi = R.hi;
+      uint32_t nclo = cum_c[0], nchi = bc_all[kBins];
+      double nmlo = cum_m[0], nmhi = static_cast<double>(bm_all[kBins]);
+      if (lo_j >= 0) {
+        nlo = vld(F.bc.q[lo_j]);
+        nclo = cum_c[lo_j + 1];
+        nmlo = cum_m[lo_j + 1];
+      }
+      if (hi_j >= 0) {
+        nhi = vld(F.bc.q[hi_j]);
+        nchi = cum_c[hi_j + 1];
+        nmhi = cum_m[hi_j + 1];
+      }
+      F.bc.u[BU_LO] = nlo;
+      F.bc.u[BU_HI] = nhi;
+      F.bc.u[BU_CLO] = nclo;
+      F.bc.u[BU_CHI] = nchi;
+      F.bc.d[BD_MLO] = nmlo;
+      F.bc.d[BD_MHI] = nmhi;
+    }
+    lo_j = __shfl_sync(kFull, lo_j, 0);
+    hi_j = __shfl_sync(kFull, hi_j, 0);
+    // per-rank counts above the new lo / hi, from that rank's bins
+    uint32_t maxr = 0;
+    if (lane < static_cast<int>(c.C)) {
+      const uint32_t top = vld(F.rank_bins[lane][kBins]);
+      uint32_t above_lo = top, above_hi = top;
+      const int lo_first = lo_j >= 0 ? lo_j + 1 : 0;
+      for (int b = np; b >= lo_first; --b) above_lo += vld(F.rank_bins[lane][b]);
+      if (hi_j >= 0)
+        for (int b = np; b > hi_j; --b) above_hi += vld(F.rank_bins[lane][b]);
+      F.rank_lo[lane] = above_lo;
+      F.rank_hi[lane] = above_hi;
+      maxr = R.pin_hi ? above_lo : above_lo - above_hi;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) maxr = max(maxr, __shfl_xor_sync(kFull, maxr, o));
+    if (lane == 0) F.bc.u[BU_MAXR] = maxr;
   }
   __syncthreads();
   ++c.ph;
+  target = vld(F.bc.d[BD_TARGET]);
+  R.lo = vld(F.bc.u[BU_LO]);
+  R.hi = vld(F.bc.u[BU_HI]);
+  R.c_lo = vld(F.bc.u[BU_CLO]);
+  R.c_hi = vld(F.bc.u[BU_CHI]);
+  R.m_lo = vld(F.bc.d[BD_MLO]);
+  R.m_hi = vld(F.bc.d[BD_MHI]);
+  R.lo_all = R.lo < kKeyNegInf;
+  const uint32_t maxr = vld(F.bc.u[BU_MAXR]);
+  const uint32_t in_range = R.pin_hi ? R.c_lo : R.c_lo - R.c_hi;
+  R.fits = in_range <= c.gcap && maxr <= c.ocap;
+  R.exact = !R.pin_hi && (R.hi - R.lo <= 1u);
+  R.below = vld(F.bc.u[BU_BELOW]) != 0u;
+  ++R.passes;
+  *used_value_out = vld(F.bc.u[BU_USED_VALUE]) != 0u;
 }
 
-// One quaternary round's scan. List mode scans the shared list (values and,
-// for MASS, cached weights); chunk mode scans the resident chunk and, when
-// `compact` is set, also appends the elements in (clo, chi] (and their
-// weights) to the list, which then covers that range. lo_all means the lower
-// end lies below key(-inf): every element passes it (its float is a NaN).
 template <int DT, bool MASS>
-__device__ __forceinline__ void scan_round(Ctx<DT>& c, bool list_mode, uint32_t list_len,
-                                           const float (&qf)[3], PAcc (&acc)[3], bool compact,
-                                           float clo_f, float chi_f, bool lo_all = false) {
+__device__ void narrow(Ctx<DT>& c, Range& R, double& target, double p_frac, double extra, bool from_chunk) {
+  bool value_ok = true;
+  R.passes = 0;
+  R.fits = false;
+  R.exact = false;
+  R.below = false;
+  while (true) {
+    const uint32_t span_before = R.hi - R.lo;
+    bool used_value = false;
+    narrow_pass<DT, MASS>(c, R, target, p_frac, extra, from_chunk, value_ok, &used_value);
+    if (R.below || R.fits || R.exact) break;
+    if (R.passes >= kMaxRounds) break;
+    if (R.pin_hi && R.passes >= kPinnedPasses) R.pin_hi = false;
+    // a value-space split that failed to halve the key range hands the next
+    // pass to key-space quartiles
+    value_ok = !(used_value && (R.hi - R.lo) > span_before / 2u);
+  }
+}
+
+// Re-read the chunk and keep its elements in (lo, hi] in the own list.
+template <int DT>
+__device__ void extract_range(Ctx<DT>& c, const Range& R) {
   constexpr int E = Ctx<DT>::E;
   Fixed& F = *c.F;
-  const int tid = threadIdx.x;
+  if (threadIdx.x == 0) F.own_n = 0;
+  __syncthreads();
+  const float lo_f = R.lo_all ? -INFINITY : pivot_f(R.lo);
+  const float hi_f = R.pin_hi ? INFINITY : pivot_f(R.hi);
+  const bool lo_all = R.lo_all;
+  stream_chunk<DT>(
+      c,
+      [&](const float (&xs)[E], uint32_t idx0, bool valid) {
+        uint32_t bits = 0;
+        if (valid) {
 #pragma unroll
-  for (int j = 0; j < 3; ++j) pacc_init(acc[j]);
-  if (list_mode) {
-    for (uint32_t i = tid; i < list_len; i += kThreads) {
-      const float x = c.list_x[i];
-      const float w = MASS ? c.list_w[i] : 0.f;
-      pacc_update<MASS>(acc, qf, x, w);
-    }
-    return;
-  }
-  const int iters = (c.body_units + kThreads - 1) / kThreads;
-  for (int it = 0; it < iters; ++it) {
-    const int u = it * kThreads + tid;
-    float xs[E], ws[E];
-    uint32_t bits = 0;
-    if (u < c.body_units) {
-      const uint4 v = *reinterpret_cast<const uint4*>(c.sbody + 16 * u);
-      unpack<DT>(v, xs);
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        ws[e] = MASS ? weight(xs[e], c.m, c.m_neginf) : 0.f;
-        pacc_update<MASS>(acc, qf, xs[e], ws[e]);
-        if (compact && (lo_all || xs[e] > clo_f) && !(xs[e] > chi_f)) bits |= 1u << e;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < E; ++e) {
-        xs[e] = 0.f;
-        ws[e] = 0.f;
-      }
-    }
-    if (compact) warp_append<E>(F, c.list_x, c.list_w, c.cap, xs, ws, bits, MASS);
-  }
-  // head and tail elements (fewer than 2E): one element per thread
-  {
-    float xs[1], ws[1];
-    uint32_t bits = 0;
-    const int h = tid;
-    xs[0] = 0.f;
-    ws[0] = 0.f;
-    if (h < c.head_n + c.tail_n) {
-      xs[0] = (h < c.head_n) ? head_elem(c, h) : tail_elem(c, h - c.head_n);
-      ws[0] = MASS ? weight(xs[0], c.m, c.m_neginf) : 0.f;
-      pacc_update<MASS>(acc, qf, xs[0], ws[0]);
-      if (compact && (lo_all || xs[0] > clo_f) && !(xs[0] > chi_f)) bits = 1u;
-    }
-    if (compact) warp_append<1>(F, c.list_x, c.list_w, c.cap, xs, ws, bits, MASS);
-  }
+          for (int e = 0; e < E; ++e)
+            if ((lo_all || xs[e] > lo_f) && !(xs[e] > hi_f)) bits |= 1u << e;
+        }
+        warp_append<E>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx0, bits);
+      },
+      [&](float x, uint32_t idx, bool valid) {
+        const float xs[1] = {x};
+        const uint32_t bits = (valid && (lo_all || x > lo_f) && !(x > hi_f)) ? 1u : 0u;
+        warp_append<1>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx, bits);
+      });
+  __syncthreads();
 }
 
-// Search state shared by the top-k (count) and top-p (mass) searches.
-struct Search {
-  uint32_t lo, hi;     // keys: count(> lo) >= target > count(> hi) (or mass)
-  uint32_t C_lo, C_hi; // row-level counts above lo / hi
-  double M_lo, M_hi;   // row-level masses above lo / hi (MASS only)
-  double myM_hi;       // this CTA's mass above hi (MASS only)
-  // list coverage: the list holds exactly this CTA's elements in (list_lo, list_hi]
-  bool list_mode;
-  uint32_t list_len;
-  uint32_t above_cnt;  // this CTA's elements above list_hi
-  double above_mass;
+// Copy every rank's own-list entries in (lo, hi] into this CTA's gathered set
+// (value, rank << 28 | index). F.rank_n[r] holds rank r's list length.
+// sync_first: the lists were rewritten since the last cluster barrier. The
+// barrier at the end is the last access to another CTA's memory.
+template <int DT>
+__device__ void gather(Ctx<DT>& c, float lo_f, float hi_f, bool lo_all, bool sync_first) {
+  Fixed& F = *c.F;
+  if (threadIdx.x == 0) F.g_n = 0;
+  if (sync_first) cluster_sync_all();
+  __syncthreads();
+  const uint32_t val_base = smem_u32(c.own_val);
+  const uint32_t idx_base = smem_u32(c.own_idx);
+  for (uint32_t r = 0; r < c.C; ++r) {
+    const uint32_t n = min(vld(F.rank_n[r]), c.ocap);
+    const uint32_t rv = map_rank(val_base, r);
+    const uint32_t ri = map_rank(idx_base, r);
+    for (uint32_t b = 0; b < n; b += kThreads) {
+      const uint32_t i = b + threadIdx.x;
+      float xs[1] = {0.f};
+      uint32_t idx = 0, bits = 0;
+      if (i < n) {
+        xs[0] = ld_dsmem_f32(rv + 4u * i);
+        idx = ld_dsmem_u32(ri + 4u * i);
+        bits = ((lo_all || xs[0] > lo_f) && !(xs[0] > hi_f)) ? 1u : 0u;
+      }
+      warp_append<1>(&F.g_n, c.g_val, c.g_tag, c.gcap, xs, (r << kTagShift) | idx, bits);
+    }
+  }
+  cluster_sync_all();
+}
+
+// ---------------------------------------------------------------------------
+// Local quaternary search over the gathered set (block barriers only)
+// ---------------------------------------------------------------------------
+struct Local {
+  uint32_t lo, hi, c_lo, c_hi;  // row counts above lo / hi
+  double m_lo, m_hi;            // row masses above lo / hi (mass search)
+  uint32_t c_above;             // row count above the gathered range
+  double m_above;               // row mass above the gathered range
   // result
-  uint32_t tau;        // boundary key
-  uint32_t n_keep;     // boundary duplicates kept
-  uint32_t count_above;  // row-level count strictly above tau
+  uint32_t tau, n_keep, count_above;
   int rounds;
   bool capped;
 };
 
-// Quaternary pivot search (A6 for counts, A7 for mass). On return F->ties
-// holds every rank's count of elements equal to the boundary and s.tau,
-// s.n_keep, s.count_above are set. target is k (counts) or p*Z (mass).
+// Quaternary search (A6 for counts, A7 for mass) over g_val[0..g_n). The
+// search keeps count/mass(> lo) >= target > count/mass(> hi); each round
+// evaluates three pivots at 25/50/75 % of the range and stops at the first
+// pivot whose z_mn is the boundary (above(q) reaches the target and above(q)
+// minus the N_zmn copies of z_mn does not): tau = z_mn and the number of
+// kept copies follows. Thread 0 takes every decision and broadcasts it.
 template <int DT, bool MASS>
-__device__ void quaternary_search(Ctx<DT>& c, Search& s, double target, bool value_pivots) {
+__device__ void local_search(Ctx<DT>& c, Local& s, double target, bool value_pivots) {
   Fixed& F = *c.F;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  bool value_ok = value_pivots;
-  s.rounds = 0;
-  s.capped = false;
-  for (;;) {
-    __syncthreads();  // cnt_lo / cnt_hi saved by warp 0 last round are visible
-    if (s.hi - s.lo <= 1u) {
-      // (lo, hi] holds one key, so the boundary value is hi.
-      s.tau = s.hi;
-      s.count_above = s.C_hi;
-      const uint32_t N = s.C_lo - s.C_hi;
-      if (MASS) {
-        const double wz = weight(key2f(s.hi), c.m, c.m_neginf);
-        double nk = ceil((target - s.M_hi) / wz);
-        nk = fmin(fmax(nk, 1.0), static_cast<double>(N));
-        s.n_keep = static_cast<uint32_t>(nk);
-      } else {
-        s.n_keep = static_cast<uint32_t>(target) - s.C_hi;
-      }
-      if (warp == 0 && lane < static_cast<int>(c.C)) F.ties[lane] = vld(F.cnt_lo[lane]) - vld(F.cnt_hi[lane]);
-      break;
-    }
-    if (s.rounds >= kMaxRounds) {
-      s.capped = true;
-      s.tau = s.hi;
-      s.n_keep = 0;
-      s.count_above = 0;
-      if (warp == 0 && lane < static_cast<int>(c.C)) F.ties[lane] = 0;
-      break;
-    }
-    uint32_t q[3];
-    float qf[3];
-    bool used_value = false;
-    const int np = choose_pivots(s.lo, s.hi, value_ok, q, qf, &used_value);
-    const uint32_t old_span = s.hi - s.lo;
-
-    // Chunk-mode CTAs compact the current range once it fits the list.
-    bool compact = false, lo_all = false;
-    float clo_f = 0.f, chi_f = 0.f;
-    if (!s.list_mode) {
-      const uint32_t in_range = vld(F.cnt_lo[c.crank]) - vld(F.cnt_hi[c.crank]);
-      if (in_range <= c.cap) {
-        compact = true;
-        lo_all = s.lo < kKeyNegInf;
-        clo_f = lo_all ? -INFINITY : pivot_f(s.lo);
-        chi_f = pivot_f(s.hi);
-        if (threadIdx.x == 0) F.list_n = 0;
-        __syncthreads();
-      }
-    }
-    PAcc acc[3];
-    scan_round<DT, MASS>(c, s.list_mode, s.list_len, qf, acc, compact, clo_f, chi_f, lo_all);
-    const uint32_t add_cnt = s.list_mode ? s.above_cnt : 0u;
-    const double add_mass = s.list_mode ? s.above_mass : 0.0;
-    reduce_merge_pivots<DT, MASS>(c, acc, add_cnt, add_mass);
-    if (compact) {
-      s.list_mode = true;
-      s.list_len = vld(F.list_n);  // a barrier separates it from the appends
-      s.above_cnt = vld(F.cnt_hi[c.crank]);
-      s.above_mass = MASS ? s.myM_hi : 0.0;
-    }
-    ++s.rounds;
-
-#ifdef QRITA_TRACE
-    if (c.crank == 0 && threadIdx.x == 0 && blockIdx.x < c.C) {
-      for (int j = 0; j < np; ++j) {
-        const double wz = MASS ? static_cast<double>(weight(F.mg.pv[j].z, c.m, c.m_neginf)) : 1.0;
-        trace_put(static_cast<double>(s.rounds), static_cast<double>(s.lo), static_cast<double>(s.hi),
-                  static_cast<double>(q[j]), static_cast<double>(F.mg.pv[j].cnt), F.mg.pv[j].z,
-                  static_cast<double>(F.mg.pv[j].nz), F.mg.pv[j].mass, target, wz);
-      }
-    }
-#endif
-    // Walk the pivots upward: terminate at the first pivot whose z_mn is the
-    // boundary (the condition as read in the design notes: above(q) reaches
-    // the target and above(q) minus the z_mn duplicates does not), else move
-    // lo up while the pivot still reaches the target, else set hi.
-    int done_j = -1, lo_j = -1, hi_j = -1;
-    for (int j = 0; j < np; ++j) {
-      PivotPart pv;
-      pv.mass = vld(F.mg.pv[j].mass);
-      pv.cnt = vld(F.mg.pv[j].cnt);
-      pv.z = vld(F.mg.pv[j].z);
-      pv.nz = vld(F.mg.pv[j].nz);
-      const double above = MASS ? pv.mass : static_cast<double>(pv.cnt);
-      if (above >= target) {
-        const double wz = MASS ? static_cast<double>(weight(pv.z, c.m, c.m_neginf)) : 1.0;
-        const double below_z = above - static_cast<double>(pv.nz) * wz;
-        if (below_z < target) {
-          done_j = j;
-          break;
-        }
-        lo_j = j;
-      } else {
-        hi_j = j;
-        break;
-      }
-    }
-#ifdef QRITA_TRACE
-    if (c.crank == 0 && threadIdx.x == 0 && blockIdx.x < c.C)
-      trace_put(-1.0, static_cast<double>(done_j), static_cast<double>(lo_j), static_cast<double>(hi_j), 0, 0, 0, 0, 0, 0);
-#endif
-    if (done_j >= 0) {
-      PivotPart pv;
-      pv.mass = vld(F.mg.pv[done_j].mass);
-      pv.cnt = vld(F.mg.pv[done_j].cnt);
-      pv.z = vld(F.mg.pv[done_j].z);
-      pv.nz = vld(F.mg.pv[done_j].nz);
-      s.tau = f2key(pv.z);
-      s.count_above = pv.cnt - pv.nz;
-      if (MASS) {
-        const double wz = weight(pv.z, c.m, c.m_neginf);
-        double nk = ceil((target - (pv.mass - static_cast<double>(pv.nz) * wz)) / wz);
-        nk = fmin(fmax(nk, 1.0), static_cast<double>(pv.nz));
-        s.n_keep = static_cast<uint32_t>(nk);
-      } else {
-        s.n_keep = static_cast<uint32_t>(target) - s.count_above;
-      }
-      if (warp == 0 && lane < static_cast<int>(c.C))
-        F.ties[lane] = (vld(F.rank_z[done_j][lane]) == pv.z) ? vld(F.rank_nz[done_j][lane]) : 0u;
-      break;
-    }
-    if (lo_j >= 0) {
-      s.lo = q[lo_j];
-      s.C_lo = vld(F.mg.pv[lo_j].cnt);
-      s.M_lo = vld(F.mg.pv[lo_j].mass);
-      if (warp == 0 && lane < static_cast<int>(c.C)) F.cnt_lo[lane] = vld(F.rank_cnt[lo_j][lane]);
-    }
-    if (hi_j >= 0) {
-      s.hi = q[hi_j];
-      s.C_hi = vld(F.mg.pv[hi_j].cnt);
-      s.M_hi = vld(F.mg.pv[hi_j].mass);
-      if (warp == 0 && lane < static_cast<int>(c.C)) F.cnt_hi[lane] = vld(F.rank_cnt[hi_j][lane]);
-    }
-    // myM_hi needs this CTA's own mass at the new hi: it is the value this
-    // CTA published, still in its slot of the merge just done.
-    if (MASS && hi_j >= 0) s.myM_hi = vld(F.slots[(c.ph - 1) & 1].pv[hi_j].mass);
-    if (used_value) {
-      value_ok = (s.hi - s.lo) <= old_span / 2u;
-    } else {
-      value_ok = value_pivots;
-    }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t gn = min(vld(F.g_n), c.gcap);
+  if (tid == 0) {
+    F.bc.u[BU_LO] = s.lo;
+    F.bc.u[BU_HI] = s.hi;
+    F.bc.u[BU_CLO] = s.c_lo;
+    F.bc.u[BU_CHI] = s.c_hi;
+    F.bc.d[BD_MLO] = s.m_lo;
+    F.bc.d[BD_MHI] = s.m_hi;
+    F.bc.u[BU_DONE] = 0;
+    F.bc.u[BU_VMODE] = value_pivots ? 1u : 0u;
   }
-  __syncthreads();  // F.ties visible
+  int rounds = 0;
+  for (;;) {
+    // thread 0: stop when (lo, hi] holds one key, else pick the pivots
+    if (tid == 0) {
+      const uint32_t lo = F.bc.u[BU_LO], hi = F.bc.u[BU_HI];
+      if (hi - lo <= 1u) {
+        const uint32_t c_hi = F.bc.u[BU_CHI], c_lo = F.bc.u[BU_CLO];
+        const uint32_t N = c_lo - c_hi;
+        F.bc.u[BU_TAU] = hi;
+        F.bc.u[BU_CABOVE] = c_hi;
+        if (MASS) {
+          const double wz = weight(key2f(hi), c.m, c.m_neginf);
+          double nk = ceil((target - F.bc.d[BD_MHI]) / wz);
+          nk = fmin(fmax(nk, 1.0), static_cast<double>(N));
+          F.bc.u[BU_NKEEP] = static_cast<uint32_t>(nk);
+        } else {
+          F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - c_hi;
+        }
+        F.bc.u[BU_DONE] = 1;
+      } else if (rounds >= kMaxRounds) {
+        F.bc.u[BU_DONE] = 2;
+      } else {
+        uint32_t q[3];
+        bool used_value = false;
+        const int np = quartile_pivots(lo, hi, F.bc.u[BU_VMODE] != 0u, q, &used_value);
+        for (int j = 0; j < 3; ++j) {
+          F.bc.q[j] = (j < np) ? q[j] : hi;
+          F.bc.qf[j] = (j < np) ? pivot_f(q[j]) : INFINITY;
+        }
+        F.bc.u[BU_NP] = static_cast<uint32_t>(np);
+        F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
+      }
+    }
+    __syncthreads();
+    const uint32_t done0 = vld(F.bc.u[BU_DONE]);
+    if (done0 != 0u) break;
+    float qf[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) qf[j] = vld(F.bc.qf[j]);
+    PAcc acc[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) pacc_init(acc[j]);
+    for (uint32_t i = tid; i < gn; i += kThreads) {
+      const float x = c.g_val[i];
+      const float w = MASS ? weight(x, c.m, c.m_neginf) : 0.f;
+      pacc_update<MASS>(acc, qf, x, w);
+    }
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const PAcc t = pacc_shfl_xor<MASS>(acc[j], o);
+        pacc_combine<MASS>(acc[j], t);
+      }
+      if (lane == 0) {
+        F.red[warp][j].cnt = acc[j].cnt;
+        F.red[warp][j].z = acc[j].z;
+        F.red[warp][j].nz = acc[j].nz;
+        F.red[warp][j].mhi = acc[j].m.hi;
+        F.red[warp][j].mlo = acc[j].m.lo;
+      }
+    }
+    __syncthreads();
+    ++rounds;
+    if (warp == 0) {
+      PAcc tot[3];
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        PAcc a;
+        pacc_init(a);
+        if (lane < kWarps) {
+          a.cnt = vld(F.red[lane][j].cnt);
+          a.z = vld(F.red[lane][j].z);
+          a.nz = vld(F.red[lane][j].nz);
+          a.m.hi = vld(F.red[lane][j].mhi);
+          a.m.lo = vld(F.red[lane][j].mlo);
+        }
+#pragma unroll
+        for (int o = kWarps / 2; o > 0; o >>= 1) {
+          const PAcc t = pacc_shfl_xor<MASS>(a, o);
+          pacc_combine<MASS>(a, t);
+        }
+        tot[j] = a;
+      }
+      if (lane == 0) {
+        const int np = static_cast<int>(F.bc.u[BU_NP]);
+        int done_j = -1, lo_j = -1, hi_j = -1;
+        double above_j[3] = {0.0, 0.0, 0.0};
+        for (int j = 0; j < np; ++j) {
+          const double above = MASS ? (f2_value(tot[j].m) + s.m_above)
+                                    : static_cast<double>(tot[j].cnt + s.c_above);
+          above_j[j] = above;
+          if (above >= target) {
+            const double wz = MASS ? static_cast<double>(weight(tot[j].z, c.m, c.m_neginf)) : 1.0;
+            const double below_z = above - static_cast<double>(tot[j].nz) * wz;
+            if (below_z < target) {
+              done_j = j;
+              break;
+            }
+            lo_j = j;
+          } else {
+            hi_j = j;
+            break;
+          }
+        }
+        if (done_j >= 0) {
+          const PAcc& t = tot[done_j];
+          const uint32_t cnt_above = t.cnt + s.c_above - t.nz;
+          F.bc.u[BU_TAU] = f2key(t.z);
+          F.bc.u[BU_CABOVE] = cnt_above;
+          if (MASS) {
+            const double wz = weight(t.z, c.m, c.m_neginf);
+            double nk = ceil((target - (above_j[done_j] - static_cast<double>(t.nz) * wz)) / wz);
+            nk = fmin(fmax(nk, 1.0), static_cast<double>(t.nz));
+            F.bc.u[BU_NKEEP] = static_cast<uint32_t>(nk);
+          } else {
+            F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - cnt_above;
+          }
+          F.bc.u[BU_DONE] = 1;
+        } else {
+          const uint32_t old_span = F.bc.u[BU_HI] - F.bc.u[BU_LO];
+          if (lo_j >= 0) {
+            F.bc.u[BU_LO] = F.bc.q[lo_j];
+            F.bc.u[BU_CLO] = tot[lo_j].cnt + s.c_above;
+            F.bc.d[BD_MLO] = above_j[lo_j];
+          }
+          if (hi_j >= 0) {
+            F.bc.u[BU_HI] = F.bc.q[hi_j];
+            F.bc.u[BU_CHI] = tot[hi_j].cnt + s.c_above;
+            F.bc.d[BD_MHI] = above_j[hi_j];
+          }
+          // after a value-space split that failed to halve the key range,
+          // the next round splits the key range
+          const uint32_t new_span = F.bc.u[BU_HI] - F.bc.u[BU_LO];
+          const bool bad = F.bc.u[BU_USED_VALUE] != 0u && new_span > old_span / 2u;
+          F.bc.u[BU_VMODE] = (value_pivots && !bad) ? 1u : 0u;
+        }
+      }
+    }
+    __syncthreads();
+    if (vld(F.bc.u[BU_DONE]) != 0u) break;
+  }
+  s.tau = vld(F.bc.u[BU_TAU]);
+  s.n_keep = vld(F.bc.u[BU_NKEEP]);
+  s.count_above = vld(F.bc.u[BU_CABOVE]);
+  s.rounds = rounds;
+  s.capped = vld(F.bc.u[BU_DONE]) == 2u;
+  __syncthreads();
+}
+
+// Per-rank counts of gathered entries equal to tau (into F.ties).
+template <int DT>
+__device__ void count_ties_gathered(Ctx<DT>& c, float tau_f) {
+  Fixed& F = *c.F;
+  if (threadIdx.x < kMaxCluster) F.ties[threadIdx.x] = 0u;
+  __syncthreads();
+  const uint32_t gn = min(vld(F.g_n), c.gcap);
+  for (uint32_t i = threadIdx.x; i < gn; i += kThreads)
+    if (c.g_val[i] == tau_f) atomicAdd(&F.ties[c.g_tag[i] >> kTagShift], 1u);
+  __syncthreads();
+}
+
+// The index below which exactly `keep` of this CTA's own-list entries equal
+// to tau lie (the own list holds every such element of the chunk). 16-way
+// splits of the index range; invariant count(idx < lo) < keep <= count(idx < hi).
+template <int DT>
+__device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t n = min(vld(F.own_n), c.ocap);
+  uint32_t lo = 0, hi = static_cast<uint32_t>(c.n);
+  for (int round = 0; round < 32 && hi - lo > 1u; ++round) {
+    const uint32_t span = hi - lo;
+    uint32_t piv[15];
+#pragma unroll
+    for (int j = 0; j < 15; ++j) {
+      uint32_t p = (span <= 16u) ? lo + 1u + static_cast<uint32_t>(j)
+                                 : lo + static_cast<uint32_t>((static_cast<uint64_t>(span) * (j + 1)) >> 4);
+      piv[j] = p < hi ? p : hi;  // pivots at hi are inert
+    }
+    uint32_t cnt[15];
+#pragma unroll
+    for (int j = 0; j < 15; ++j) cnt[j] = 0;
+    for (uint32_t i = tid; i < n; i += kThreads) {
+      if (c.own_val[i] == tau_f) {
+        const uint32_t ix = c.own_idx[i];
+#pragma unroll
+        for (int j = 0; j < 15; ++j) cnt[j] += (ix < piv[j]) ? 1u : 0u;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 15; ++j) {
+      const uint32_t v = warp_sum_u(cnt[j]);
+      if (lane == 0) F.redu[warp][j] = v;
+    }
+    __syncthreads();
+    uint32_t nlo = lo, nhi = hi;
+#pragma unroll
+    for (int j = 0; j < 15; ++j) {
+      uint32_t s = 0;
+      for (int w = 0; w < kWarps; ++w) s += vld(F.redu[w][j]);
+      if (piv[j] <= lo || piv[j] >= hi) continue;
+      if (s < keep) nlo = max(nlo, piv[j]);
+      else nhi = min(nhi, piv[j]);
+    }
+    lo = nlo;
+    hi = nhi;
+    __syncthreads();
+  }
+  return hi;
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_constant__ Params P) {
   constexpr int E = Ctx<DT>::E;
   constexpr int S = Ctx<DT>::S;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -709,56 +998,36 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
 
   Ctx<DT> c;
   c.F = &F;
-  c.cap = static_cast<uint32_t>(P.cap);
-  c.list_x = reinterpret_cast<float*>(smem + sizeof(Fixed));
-  c.list_w = c.list_x + P.cap;
-  unsigned char* sdata = reinterpret_cast<unsigned char*>(c.list_w + P.cap);
-  unsigned char* sbody = sdata + 16;
-  c.sbody = sbody;
+  c.ocap = static_cast<uint32_t>(P.ocap);
+  c.gcap = static_cast<uint32_t>(P.gcap);
+  c.own_val = reinterpret_cast<float*>(smem + sizeof(Fixed));
+  c.own_idx = reinterpret_cast<uint32_t*>(c.own_val + P.ocap);
+  c.g_val = reinterpret_cast<float*>(c.own_idx + P.ocap);
+  c.g_tag = reinterpret_cast<uint32_t*>(c.g_val + P.gcap);
   c.C = static_cast<uint32_t>(P.C);
   c.crank = cluster_rank();
   c.ph = 0;
+  c.m = 0.f;
+  c.m_neginf = false;
+  c.fix_scale = 0.f;
 
   const int64_t r = blockIdx.x / P.C;
   const int32_t V = P.V;
   const int64_t c0 = static_cast<int64_t>(c.crank) * P.chunk;
   const int64_t rem = static_cast<int64_t>(V) - c0;
   c.n = static_cast<int>(rem <= 0 ? 0 : (rem < P.chunk ? rem : P.chunk));
-  const unsigned char* gx =
-      static_cast<const unsigned char*>(P.logits) + (static_cast<size_t>(r) * V + c0) * S;
-  uint8_t* gmask = P.mask + static_cast<size_t>(r) * V + c0;
-
-  // Chunk geometry: head elements up to the first 16-byte boundary of the
-  // global row, whole 16-byte units, tail elements.
+  const int64_t c0c = c0 < V ? c0 : V;
+  const unsigned char* grow = static_cast<const unsigned char*>(P.logits) + static_cast<size_t>(r) * V * S;
+  c.gx = grow + static_cast<size_t>(c0c) * S;
+  c.gmask = P.mask + static_cast<size_t>(r) * V + c0c;
   {
-    const uintptr_t ga = reinterpret_cast<uintptr_t>(gx);
-    int h = static_cast<int>(((16u - (ga & 15u)) & 15u) / S);
+    const uintptr_t ga = reinterpret_cast<uintptr_t>(c.gx);
+    const int h = static_cast<int>(((16u - (ga & 15u)) & 15u) / S);
     c.head_n = h < c.n ? h : c.n;
     c.body_units = (c.n - c.head_n) * S / 16;
     c.tail_n = c.n - c.head_n - c.body_units * E;
   }
-  const unsigned char* gbody = gx + c.head_n * S;
-  const int piece_units = kPieceBytes / 16;
-  const int npieces = (c.body_units + piece_units - 1) / piece_units;
-
-  // ---- stage loads: TMA bulk copies of the body, plain loads of head/tail
-  if (tid == 0) {
-    F.list_n = 0;
-    F.err = 0;
-    for (int pc = 0; pc < npieces; ++pc) mbar_init(smem_u32(&F.bars[pc]), 1);
-    fence_mbar_init();
-    for (int pc = 0; pc < npieces; ++pc) {
-      const int u0 = pc * piece_units;
-      const int nu = min(piece_units, c.body_units - u0);
-      const uint32_t bytes = static_cast<uint32_t>(nu) * 16u;
-      const uint32_t bar = smem_u32(&F.bars[pc]);
-      mbar_expect_tx(bar, bytes);
-      bulk_g2s(smem_u32(sbody + 16 * u0), gbody + 16 * u0, bytes, bar);
-    }
-  }
-  if (tid < c.head_n) copy_elem<DT>(sbody - (c.head_n - tid) * S, gx + tid * S);
-  if (tid < c.tail_n)
-    copy_elem<DT>(sbody + 16 * c.body_units + tid * S, gbody + 16 * c.body_units + tid * S);
+  c.gbody = c.gx + c.head_n * S;
 
   // ---- row parameters (uniform)
   int32_t kr = P.k ? P.k[r] : 0;
@@ -766,7 +1035,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
   bool k_on = kr >= 1 && kr < V;
   bool p_on = pr < 1.0f;  // NaN compares false: off
   if (p_on && !(pr > 0.0f)) {
-    // p <= 0 keeps exactly one token: the same set as k = 1.
+    // p <= 0 keeps exactly one token: the same set as k = 1
     p_on = false;
     if (V > 1) {
       k_on = true;
@@ -774,168 +1043,132 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
     }
   }
   const bool keep_all = !k_on && !p_on;
+  const bool p_only = p_on && !k_on;
 
-  // ---- A2: sample-block statistics (plain global loads, overlapping the copies)
+  // ---- A2: statistics of one sample block of the row (identical in every CTA)
   {
-    float sn = 0.f, sx = 0.f, sxx = 0.f;
+    float sn = 0.f, sx = 0.f, sxx = 0.f, smax = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      const int sidx = tid + j * kThreads;  // 0 .. 511
-      int idx;
-      if (c.n <= kSampleBlocks * kSampleBlock) {
-        idx = sidx;
+    for (int j = 0; j < (kSampleBlocks * kSampleBlock) / kThreads; ++j) {
+      const int sidx = tid + j * kThreads;
+      int64_t pos;
+      if (V <= kSampleBlocks * kSampleBlock) {
+        pos = sidx;
       } else {
-        idx = (sidx / kSampleBlock) * (c.n / kSampleBlocks) + (sidx % kSampleBlock);
+        pos = static_cast<int64_t>(sidx / kSampleBlock) * (V / kSampleBlocks) + (sidx % kSampleBlock);
       }
-      if (idx < c.n) {
-        const float x = load_elem<DT>(gx + static_cast<size_t>(idx) * S);
+      if (pos < V) {
+        const float x = load_elem<DT>(grow + static_cast<size_t>(pos) * S);
         if (isfinite(x)) {
           sn += 1.f;
           sx += x;
           sxx += x * x;
+          smax = fmaxf(smax, x);
         }
       }
     }
     sn = warp_sum_f(sn);
     sx = warp_sum_f(sx);
     sxx = warp_sum_f(sxx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) smax = fmaxf(smax, __shfl_xor_sync(kFull, smax, o));
     if (lane == 0) {
       F.redf[warp][0] = sn;
       F.redf[warp][1] = sx;
       F.redf[warp][2] = sxx;
+      F.redf[warp][3] = smax;
     }
-  }
-  __syncthreads();  // also: barriers initialised, head/tail stored, list_n zeroed
-  if (warp == 0) {
-    float a = lane < kWarps ? vld(F.redf[lane][0]) : 0.f;
-    float b = lane < kWarps ? vld(F.redf[lane][1]) : 0.f;
-    float d = lane < kWarps ? vld(F.redf[lane][2]) : 0.f;
-    a = warp_sum_f(a);
-    b = warp_sum_f(b);
-    d = warp_sum_f(d);
-    if (lane == 0) {
-      Slot& my = F.slots[c.ph & 1];
-      my.f[0] = a;
-      my.f[1] = b;
-      my.f[2] = d;
-    }
-  }
-  cluster_sync_all();  // first cluster barrier: every CTA of the cluster is running
-  if (warp == 0) {
-    double a = 0.0, b = 0.0, d = 0.0;
-    if (lane < static_cast<int>(c.C)) {
-      const uint32_t base = map_rank(smem_u32(&F.slots[c.ph & 1].f[0]), lane);
-      a = ld_dsmem_f32(base);
-      b = ld_dsmem_f32(base + 4);
-      d = ld_dsmem_f32(base + 8);
-    }
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) {
-      a += __shfl_xor_sync(kFull, a, o);
-      b += __shfl_xor_sync(kFull, b, o);
-      d += __shfl_xor_sync(kFull, d, o);
-    }
-    if (lane == 0) {
-      // a = finite samples, b = their sum, d = their sum of squares
-      const double mean = a > 0.0 ? b / a : 0.0;
-      const double var = a > 0.0 ? fmax(d / a - mean * mean, 0.0) : 0.0;
-      F.mg.f[1] = static_cast<float>(mean);
-      F.mg.f[2] = static_cast<float>(sqrt(var));
-      F.mg.u[0] = a > 0.0 ? 1u : 0u;
-    }
-  }
-  __syncthreads();
-  ++c.ph;
-  const float mu = vld(F.mg.f[1]);
-  const float sigma = vld(F.mg.f[2]);
-  const bool have_sample = vld(F.mg.u[0]) != 0u;
-
-  // ---- A3: delta from the normal-quantile tables, threshold t
-  bool trunc = false;
-  float t = -INFINITY;
-  if (!(P.flags & QRITA_FLAG_NO_TRUNCATION) && have_sample && !keep_all) {
-    if (k_on) {
-      const float u = P.alpha_k * static_cast<float>(kr) / static_cast<float>(V);
-      if (u <= P.u_max_k) {
-        int i = static_cast<int>(floorf(-2.0f * log2f(u)));
-        i = i < 0 ? 0 : (i > kLutK - 1 ? kLutK - 1 : i);
-        t = mu + P.lut_k[i] * sigma;
-        trunc = true;
+    if (tid == 0) F.own_n = 0;
+    __syncthreads();
+    if (tid == 0) {
+      float a = 0.f, b = 0.f, d = 0.f, mx = -INFINITY;
+      for (int w = 0; w < kWarps; ++w) {
+        a += vld(F.redf[w][0]);
+        b += vld(F.redf[w][1]);
+        d += vld(F.redf[w][2]);
+        mx = fmaxf(mx, vld(F.redf[w][3]));
       }
-    } else {
-      const float qv = 1.0f - pr;
-      int i = static_cast<int>(ceilf(-4.0f * log2f(qv)));
-      if (i <= kLutP - 1) {
-        i = i < 0 ? 0 : i;
-        t = mu + (sigma + P.lut_p[i] - P.margin_p) * sigma;
-        trunc = true;
+      const double mean = a > 0.f ? static_cast<double>(b) / a : 0.0;
+      const double var = a > 0.f ? fmax(static_cast<double>(d) / a - mean * mean, 0.0) : 0.0;
+      const float mu = static_cast<float>(mean);
+      const float sigma = static_cast<float>(sqrt(var));
+      F.bc.f[BF_MU] = mu;
+      F.bc.f[BF_SIGMA] = sigma;
+      F.bc.f[BF_MREF] = a > 0.f ? mx : 0.f;
+      // ---- A3: delta from the normal-quantile tables, threshold t
+      bool trunc = false;
+      float t = -INFINITY;
+      if (!(P.flags & QRITA_FLAG_NO_TRUNCATION) && a > 0.f && !keep_all) {
+        if (k_on) {
+          const float u = P.alpha_k * static_cast<float>(kr) / static_cast<float>(V);
+          if (u <= P.u_max_k) {
+            int i = static_cast<int>(floorf(-2.0f * log2f(u)));
+            i = i < 0 ? 0 : (i > kLutK - 1 ? kLutK - 1 : i);
+            t = mu + P.lut_k[i] * sigma;
+            trunc = true;
+          }
+        } else {
+          const float qv = 1.0f - pr;
+          int i = static_cast<int>(ceilf(-4.0f * log2f(qv)));
+          if (i <= kLutP - 1) {
+            i = i < 0 ? 0 : i;
+            t = mu + (sigma + P.lut_p[i] - P.margin_p) * sigma;
+            trunc = true;
+          }
+        }
+        if (!isfinite(t)) trunc = false;
       }
+      F.bc.f[BF_T] = trunc ? t : -INFINITY;
+      F.bc.u[BU_TRUNC] = trunc ? 1u : 0u;
     }
-    if (!isfinite(t)) trunc = false;
+    __syncthreads();
   }
+  const float mu = vld(F.bc.f[BF_MU]);
+  const float sigma = vld(F.bc.f[BF_SIGMA]);
+  const float m_ref = vld(F.bc.f[BF_MREF]);
+  const float t = vld(F.bc.f[BF_T]);
+  const bool trunc = vld(F.bc.u[BU_TRUNC]) != 0u;
 
-  // ---- A4: truncation pass over the resident chunk (waits for the copies)
+  // ---- A4: the streaming pass (the one HBM read of the row)
   {
     float vmax = -INFINITY, vmin = INFINITY, smin = INFINITY;
     uint32_t smin_n = 0;
-    bool timed_out = false;
-    const int it_per_piece = piece_units / kThreads;
-    const int iters = (c.body_units + kThreads - 1) / kThreads;
-    for (int it = 0; it < iters; ++it) {
-      if (it % it_per_piece == 0) {
-        if (!mbar_wait_bounded(smem_u32(&F.bars[it / it_per_piece]), 0, kWaitLimitNs)) timed_out = true;
+    F2 zs = {0.f, 0.f}, ms = {0.f, 0.f};
+    auto elem = [&](float x) -> bool {
+      vmax = fmax_nan(vmax, x);
+      vmin = fminf(vmin, x);
+      const bool surv = trunc && x >= t;
+      if (surv) {
+        if (x < smin) {
+          smin = x;
+          smin_n = 1;
+        } else if (x == smin) {
+          ++smin_n;
+        }
       }
-      const int u = it * kThreads + tid;
-      float xs[E], ws[E];
-      uint32_t bits = 0;
-      if (u < c.body_units) {
-        const uint4 v = *reinterpret_cast<const uint4*>(sbody + 16 * u);
-        unpack<DT>(v, xs);
+      if (p_only) {
+        const float w = expf(x - m_ref);
+        f2_add(zs, w);
+        f2_add(ms, surv ? w : 0.f);
+      }
+      return surv;
+    };
+    stream_chunk<DT>(
+        c,
+        [&](const float (&xs)[E], uint32_t idx0, bool valid) {
+          uint32_t bits = 0;
+          if (valid) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          vmax = fmax_nan(vmax, xs[e]);
-          vmin = fminf(vmin, xs[e]);
-          if (trunc && xs[e] >= t) {
-            bits |= 1u << e;
-            if (xs[e] < smin) {
-              smin = xs[e];
-              smin_n = 1;
-            } else if (xs[e] == smin) {
-              ++smin_n;
-            }
+            for (int e = 0; e < E; ++e) bits |= elem(xs[e]) ? (1u << e) : 0u;
           }
-          ws[e] = 0.f;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          xs[e] = 0.f;
-          ws[e] = 0.f;
-        }
-      }
-      if (trunc) warp_append<E>(F, c.list_x, c.list_w, c.cap, xs, ws, bits, false);
-    }
-    {
-      float xs[1] = {0.f}, ws[1] = {0.f};
-      uint32_t bits = 0;
-      if (tid < c.head_n + c.tail_n) {
-        xs[0] = (tid < c.head_n) ? head_elem(c, tid) : tail_elem(c, tid - c.head_n);
-        vmax = fmax_nan(vmax, xs[0]);
-        vmin = fminf(vmin, xs[0]);
-        if (trunc && xs[0] >= t) {
-          bits = 1u;
-          if (xs[0] < smin) {
-            smin = xs[0];
-            smin_n = 1;
-          } else if (xs[0] == smin) {
-            ++smin_n;
-          }
-        }
-      }
-      if (trunc) warp_append<1>(F, c.list_x, c.list_w, c.cap, xs, ws, bits, false);
-    }
-    if (timed_out) atomicOr(&F.err, 1u);
-    // block reduce: max (NaN-propagating), min, (smin, smin_n)
+          if (trunc) warp_append<E>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx0, bits);
+        },
+        [&](float x, uint32_t idx, bool valid) {
+          const uint32_t bits = (valid && elem(x)) ? 1u : 0u;
+          const float xs[1] = {x};
+          if (trunc) warp_append<1>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx, bits);
+        });
+    // block reduce
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       vmax = fmax_nan(vmax, __shfl_xor_sync(kFull, vmax, o));
@@ -948,57 +1181,74 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
       } else if (s2 == smin) {
         smin_n += n2;
       }
+      if (p_only) {
+        F2 a, b;
+        a.hi = __shfl_xor_sync(kFull, zs.hi, o);
+        a.lo = __shfl_xor_sync(kFull, zs.lo, o);
+        b.hi = __shfl_xor_sync(kFull, ms.hi, o);
+        b.lo = __shfl_xor_sync(kFull, ms.lo, o);
+        zs = f2_merge(zs, a);
+        ms = f2_merge(ms, b);
+      }
     }
     if (lane == 0) {
       F.redf[warp][0] = vmax;
       F.redf[warp][1] = vmin;
       F.redf[warp][2] = smin;
+      F.redf[warp][3] = zs.hi;
+      F.redf[warp][4] = zs.lo;
+      F.redf[warp][5] = ms.hi;
+      F.redf[warp][6] = ms.lo;
       F.redu[warp][0] = smin_n;
     }
     __syncthreads();
-    if (warp == 0) {
-      float a = lane < kWarps ? vld(F.redf[lane][0]) : -INFINITY;
-      float b = lane < kWarps ? vld(F.redf[lane][1]) : INFINITY;
-      float s = lane < kWarps ? vld(F.redf[lane][2]) : INFINITY;
-      uint32_t sn = lane < kWarps ? vld(F.redu[lane][0]) : 0u;
-#pragma unroll
-      for (int o = kWarps / 2; o > 0; o >>= 1) {
-        a = fmax_nan(a, __shfl_xor_sync(kFull, a, o));
-        b = fminf(b, __shfl_xor_sync(kFull, b, o));
-        const float s2 = __shfl_xor_sync(kFull, s, o);
-        const uint32_t n2 = __shfl_xor_sync(kFull, sn, o);
+    Slot& my = F.slots[c.ph & 1];
+    if (tid == 0) {
+      float a = -INFINITY, b = INFINITY, s = INFINITY;
+      uint32_t sn = 0;
+      F2 z = {0.f, 0.f}, mm = {0.f, 0.f};
+      for (int w = 0; w < kWarps; ++w) {
+        a = fmax_nan(a, vld(F.redf[w][0]));
+        b = fminf(b, vld(F.redf[w][1]));
+        const float s2 = vld(F.redf[w][2]);
+        const uint32_t n2 = vld(F.redu[w][0]);
         if (s2 < s) {
           s = s2;
           sn = n2;
         } else if (s2 == s) {
           sn += n2;
         }
+        const F2 za = {vld(F.redf[w][3]), vld(F.redf[w][4])};
+        const F2 ma = {vld(F.redf[w][5]), vld(F.redf[w][6])};
+        z = f2_merge(z, za);
+        mm = f2_merge(mm, ma);
       }
-      if (lane == 0) {
-        Slot& my = F.slots[c.ph & 1];
-        my.f[0] = a;
-        my.f[1] = b;
-        my.f[2] = s;
-        my.u[0] = sn;
-        my.u[1] = vld(F.list_n);
-        my.u[2] = F.err;
-      }
+      my.f[0] = a;
+      my.f[1] = b;
+      my.f[2] = s;
+      my.u[0] = sn;
+      my.u[1] = vld(F.own_n);
+      my.d[0] = f2_value(z);
+      my.d[1] = f2_value(mm);
     }
     cluster_sync_all();
     if (warp == 0) {
       float a = -INFINITY, b = INFINITY, s = INFINITY;
-      uint32_t sn = 0, surv = 0, err = 0, ovf = 0;
+      uint32_t sn = 0, surv = 0, ovf = 0;
+      double z = 0.0, mm = 0.0;
       if (lane < static_cast<int>(c.C)) {
-        const uint32_t base = map_rank(smem_u32(&F.slots[c.ph & 1].f[0]), lane);
-        a = ld_dsmem_f32(base);
-        b = ld_dsmem_f32(base + 4);
-        s = ld_dsmem_f32(base + 8);
-        const uint32_t ub = map_rank(smem_u32(&F.slots[c.ph & 1].u[0]), lane);
+        const uint32_t fb = map_rank(smem_u32(&my.f[0]), lane);
+        a = ld_dsmem_f32(fb);
+        b = ld_dsmem_f32(fb + 4);
+        s = ld_dsmem_f32(fb + 8);
+        const uint32_t ub = map_rank(smem_u32(&my.u[0]), lane);
         sn = ld_dsmem_u32(ub);
         surv = ld_dsmem_u32(ub + 4);
-        err = ld_dsmem_u32(ub + 8);
-        ovf = surv > c.cap ? 1u : 0u;
-        F.rank_surv[lane] = surv;
+        const uint32_t db = map_rank(smem_u32(&my.d[0]), lane);
+        z = ld_dsmem_f64(db);
+        mm = ld_dsmem_f64(db + 8);
+        ovf = surv > c.ocap ? 1u : 0u;
+        F.rank_n[lane] = surv;
       }
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) {
@@ -1013,34 +1263,37 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
           sn += n2;
         }
         surv += __shfl_xor_sync(kFull, surv, o);
-        err |= __shfl_xor_sync(kFull, err, o);
         ovf |= __shfl_xor_sync(kFull, ovf, o);
+        z += __shfl_xor_sync(kFull, z, o);
+        mm += __shfl_xor_sync(kFull, mm, o);
       }
       if (lane == 0) {
-        F.mg.f[0] = a;
-        F.mg.f[1] = b;
-        F.mg.f[2] = s;
-        F.mg.u[0] = sn;
-        F.mg.u[1] = surv;
-        F.mg.u[2] = err;
-        F.mg.u[3] = ovf;
+        F.bc.f[BF_MAX] = a;
+        F.bc.f[BF_MIN] = b;
+        F.bc.f[BF_SMIN] = s;
+        F.bc.u[BU_SMIN_N] = sn;
+        F.bc.u[BU_S] = surv;
+        F.bc.u[BU_OVF] = ovf;
+        F.bc.d[BD_ZR] = z;
+        F.bc.d[BD_MR] = mm;
       }
     }
     __syncthreads();
     ++c.ph;
   }
-  const float row_max = vld(F.mg.f[0]);
-  const float row_min = vld(F.mg.f[1]);
-  const float surv_min = vld(F.mg.f[2]);
-  const uint32_t surv_min_n = vld(F.mg.u[0]);
-  const uint32_t survivors = vld(F.mg.u[1]);
-  const bool timed_out = vld(F.mg.u[2]) != 0u;
-  const bool overflow = vld(F.mg.u[3]) != 0u;
-  const bool nonfinite = isnan(row_max) || row_max == INFINITY;
-  const bool invalid = nonfinite || timed_out;
+  const float row_max = vld(F.bc.f[BF_MAX]);
+  const float row_min = vld(F.bc.f[BF_MIN]);
+  const float surv_min = vld(F.bc.f[BF_SMIN]);
+  const uint32_t surv_min_n = vld(F.bc.u[BU_SMIN_N]);
+  const uint32_t survivors = vld(F.bc.u[BU_S]);
+  const bool overflow = vld(F.bc.u[BU_OVF]) != 0u;
+  const bool invalid = isnan(row_max) || row_max == INFINITY;
+  const double Zr = vld(F.bc.d[BD_ZR]);
+  const double Mr = vld(F.bc.d[BD_MR]);
   c.m = row_max;
   c.m_neginf = (row_max == -INFINITY);
-  const uint32_t my_surv = vld(F.list_n);
+  // weights exp(x - m) lie in [0, 1]: fixed point with headroom for V terms
+  c.fix_scale = exp2f(static_cast<float>(62 - (32 - __clz(static_cast<uint32_t>(V)))));
 
   uint32_t path = (k_on ? QRITA_PATH_TOPK : 0u) | (p_on ? QRITA_PATH_TOPP : 0u) |
                   (trunc ? QRITA_PATH_TRUNC : 0u) | (overflow ? QRITA_PATH_OVERFLOW : 0u) |
@@ -1048,172 +1301,123 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
   const bool force_fb = (P.flags & QRITA_FLAG_FORCE_FALLBACK) != 0u;
   const bool value_pivots = (P.flags & QRITA_FLAG_KEY_PIVOTS) == 0u;
 
-  // Final selection: keep key > tau, plus the n_keep lowest-id elements equal
-  // to tau. F.ties[rank] = elements equal to tau in that rank's chunk.
+  // Selection: keep key > tau, plus the n_keep lowest-id elements equal to
+  // tau; F.ties[rank] counts the elements equal to tau in each rank's chunk.
   uint32_t tau = 0, n_keep = 0, count_above = 0;
-  uint32_t rounds_k = 0, rounds_p = 0;
-  uint32_t row_status = QRITA_ROW_OK;
+  uint32_t rounds_k = 0, rounds_p = 0, passes = 0;
+  uint32_t row_status = invalid ? QRITA_ROW_NONFINITE : QRITA_ROW_OK;
   double z_used = 0.0;
-  bool sel_all = keep_all;
-  bool sel_none = false;
+  bool sel_all = keep_all && !invalid;
+  bool sel_none = invalid;
+  bool remote_done = false;   // the last access to another CTA's memory is behind a barrier
+  bool list_emit = false;     // every kept element is in this CTA's own list
+  bool ties_in_list = false;  // every element equal to tau is in this CTA's own list
+  bool ties_known = false;    // F.ties holds the per-rank tie counts
 
-  // list coverage of the survivor list: (key(t) - 1, +inf)
-  Search s;
-  s.list_mode = false;
-  s.list_len = 0;
-  s.above_cnt = 0;
-  s.above_mass = 0.0;
-  s.myM_hi = 0.0;
+  if (!invalid && !keep_all) {
+    const double pd = static_cast<double>(pr);
+    // the streaming pass summed exp(x - m_ref); shift m is exp(m_ref - m) away
+    const bool ref_ok = !c.m_neginf && isfinite(Zr) && isfinite(Mr) && Zr > 0.0 &&
+                        static_cast<double>(row_max) - m_ref < 80.0;
+    const double cf = ref_ok ? exp(static_cast<double>(m_ref) - row_max) : 0.0;
+    const double Zm = Zr * cf, Mm = Mr * cf;
 
-  double Z = 0.0, Mt = 0.0;
-  if (invalid) {
-    sel_none = true;
-    sel_all = false;
-    row_status = nonfinite ? QRITA_ROW_NONFINITE : QRITA_ROW_TIMEOUT;
-  } else if (!keep_all) {
-    // ---- top-p rows without top-k: Z = sum exp(x - m), and the survivors' mass
-    if (p_on && !k_on) {
-      F2 zs = {0.f, 0.f}, ms = {0.f, 0.f};
-      const int iters = (c.body_units + kThreads - 1) / kThreads;
-      for (int it = 0; it < iters; ++it) {
-        const int u = it * kThreads + tid;
-        if (u < c.body_units) {
-          float xs[E];
-          unpack<DT>(*reinterpret_cast<const uint4*>(sbody + 16 * u), xs);
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float w = weight(xs[e], c.m, c.m_neginf);
-            f2_add(zs, w);
-            f2_add(ms, (trunc && xs[e] >= t) ? w : 0.f);
-          }
-        }
-      }
-      if (tid < c.head_n + c.tail_n) {
-        const float x = (tid < c.head_n) ? head_elem(c, tid) : tail_elem(c, tid - c.head_n);
-        const float w = weight(x, c.m, c.m_neginf);
-        f2_add(zs, w);
-        f2_add(ms, (trunc && x >= t) ? w : 0.f);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        F2 a, b;
-        a.hi = __shfl_xor_sync(kFull, zs.hi, o);
-        a.lo = __shfl_xor_sync(kFull, zs.lo, o);
-        b.hi = __shfl_xor_sync(kFull, ms.hi, o);
-        b.lo = __shfl_xor_sync(kFull, ms.lo, o);
-        zs = f2_merge(zs, a);
-        ms = f2_merge(ms, b);
-      }
-      if (lane == 0) {
-        F.redf[warp][0] = zs.hi;
-        F.redf[warp][1] = zs.lo;
-        F.redf[warp][2] = ms.hi;
-        F.redf[warp][3] = ms.lo;
-      }
-      __syncthreads();
-      if (warp == 0) {
-        F2 a = {0.f, 0.f}, b = {0.f, 0.f};
-        if (lane < kWarps) {
-          a.hi = vld(F.redf[lane][0]);
-          a.lo = vld(F.redf[lane][1]);
-          b.hi = vld(F.redf[lane][2]);
-          b.lo = vld(F.redf[lane][3]);
-        }
-#pragma unroll
-        for (int o = kWarps / 2; o > 0; o >>= 1) {
-          F2 a2, b2;
-          a2.hi = __shfl_xor_sync(kFull, a.hi, o);
-          a2.lo = __shfl_xor_sync(kFull, a.lo, o);
-          b2.hi = __shfl_xor_sync(kFull, b.hi, o);
-          b2.lo = __shfl_xor_sync(kFull, b.lo, o);
-          a = f2_merge(a, a2);
-          b = f2_merge(b, b2);
-        }
-        if (lane == 0) {
-          F.slots[c.ph & 1].d[0] = f2_value(a);
-          F.slots[c.ph & 1].d[1] = f2_value(b);
-        }
-      }
-      cluster_sync_all();
-      if (warp == 0) {
-        double a = 0.0, b = 0.0;
-        if (lane < static_cast<int>(c.C)) {
-          const uint32_t base = map_rank(smem_u32(&F.slots[c.ph & 1].d[0]), lane);
-          a = ld_dsmem_f64(base);
-          b = ld_dsmem_f64(base + 8);
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) {
-          a += __shfl_xor_sync(kFull, a, o);
-          b += __shfl_xor_sync(kFull, b, o);
-        }
-        if (lane == 0) {
-          F.mg.d[0] = a;
-          F.mg.d[1] = b;
-        }
-      }
-      __syncthreads();
-      ++c.ph;
-      Z = vld(F.mg.d[0]);
-      Mt = vld(F.mg.d[1]);
-    }
-
-    // ---- A5 + A6: top-k search
+    bool k_full = false;  // the gathered set holds the whole top-k set S_k
     uint32_t tau_k = 0, nk_k = 0, above_k = 0;
     if (k_on) {
+      const double target = static_cast<double>(kr);
       const bool hit = trunc && !overflow && !force_fb && survivors >= static_cast<uint32_t>(kr);
       path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
-      s.rounds = 0;
-      bool done0 = false;
-      if (hit) {
-        s.list_mode = true;
-        s.list_len = my_surv;
-        s.above_cnt = 0;
+      Local s;
+      s.c_above = 0;
+      s.m_above = 0.0;
+      s.m_lo = s.m_hi = 0.0;
+      bool have_exact = false;
+      if (hit && survivors <= c.gcap) {
+        // gather Z_t whole: the candidates are (key(t) - 1, max]
+        gather<DT>(c, -INFINITY, INFINITY, true, false);
+        remote_done = true;
         s.lo = f2key(t) - 1u;
-        s.C_lo = survivors;
+        s.c_lo = survivors;
         s.hi = f2key(row_max);
-        s.C_hi = 0;
-        if (warp == 0 && lane < static_cast<int>(c.C)) {
-          F.cnt_lo[lane] = vld(F.rank_surv[lane]);
-          F.cnt_hi[lane] = 0;
-        }
-        // z_mn of the initial lo is the smallest survivor: check it first.
+        s.c_hi = 0;
+        k_full = true;
+        list_emit = true;
+        ties_in_list = true;
         if (survivors - surv_min_n < static_cast<uint32_t>(kr)) {
-          done0 = true;
+          // z_mn of the initial lo is the smallest survivor: it is the boundary
           s.tau = f2key(surv_min);
           s.count_above = survivors - surv_min_n;
           s.n_keep = static_cast<uint32_t>(kr) - s.count_above;
+          s.rounds = 0;
           s.capped = false;
-          // ties: every rank's survivors equal to surv_min; recount from the lists
+        } else {
+          local_search<DT, false>(c, s, target, value_pivots);
         }
       } else {
-        s.list_mode = false;
-        s.lo = f2key(row_min) - 1u;
-        s.C_lo = static_cast<uint32_t>(V);
-        const bool miss_with_t = trunc && survivors < static_cast<uint32_t>(kr);
-        s.hi = miss_with_t ? f2key(t) - 1u : f2key(row_max);
-        s.C_hi = miss_with_t ? survivors : 0u;
-        if (warp == 0 && lane < static_cast<int>(c.C)) {
-          const int64_t rl = static_cast<int64_t>(V) - static_cast<int64_t>(lane) * P.chunk;
-          F.cnt_lo[lane] = static_cast<uint32_t>(rl <= 0 ? 0 : (rl < P.chunk ? rl : P.chunk));
-          F.cnt_hi[lane] = miss_with_t ? vld(F.rank_surv[lane]) : 0u;
+        // narrow: over the survivor lists on a hit, over the chunk otherwise
+        Range R;
+        R.pin_hi = p_on && static_cast<uint32_t>(kr) <= c.gcap;
+        R.m_lo = R.m_hi = 0.0;
+        double tg = target;
+        if (hit) {
+          R.lo = f2key(t) - 1u;
+          R.c_lo = survivors;
+          R.hi = f2key(row_max);
+          R.c_hi = 0;
+        } else {
+          R.lo = f2key(row_min) - 1u;
+          R.c_lo = static_cast<uint32_t>(V);
+          const bool miss_t = trunc && !overflow && survivors < static_cast<uint32_t>(kr);
+          R.hi = (!R.pin_hi && miss_t) ? f2key(t) - 1u : f2key(row_max);
+          R.c_hi = (!R.pin_hi && miss_t) ? survivors : 0u;
         }
-      }
-      if (done0) {
-        // per-rank count of survivors equal to the boundary (one list scan)
-        uint32_t mine = 0;
-        for (uint32_t i = tid; i < s.list_len; i += kThreads) mine += (c.list_x[i] == surv_min) ? 1u : 0u;
-        uint32_t tot;
-        const uint32_t ex = block_excl_scan(F, mine, &tot);
-        (void)ex;
-        if (tid == 0) F.slots[c.ph & 1].u[0] = tot;
-        cluster_sync_all();
-        if (warp == 0 && lane < static_cast<int>(c.C))
-          F.ties[lane] = ld_dsmem_u32(map_rank(smem_u32(&F.slots[c.ph & 1].u[0]), lane));
-        __syncthreads();
-        ++c.ph;
-      } else {
-        quaternary_search<DT, false>(c, s, static_cast<double>(kr), value_pivots);
+        R.lo_all = R.lo < kKeyNegInf;
+        narrow<DT, false>(c, R, tg, 0.0, 0.0, !hit);
+        passes += static_cast<uint32_t>(R.passes);
+        if (R.exact) {
+          s.tau = R.hi;
+          s.count_above = R.c_hi;
+          s.n_keep = static_cast<uint32_t>(kr) - R.c_hi;
+          s.rounds = 0;
+          s.capped = false;
+          have_exact = true;
+          if (warp == 0 && lane < static_cast<int>(c.C))
+            F.ties[lane] = vld(F.rank_lo[lane]) - vld(F.rank_hi[lane]);
+          __syncthreads();
+          ties_known = true;
+        } else if (!R.fits) {
+          s.capped = true;
+          s.rounds = 0;
+        } else {
+          if (!hit) {
+            extract_range<DT>(c, R);
+            // an extraction leaves exactly each rank's range in its list
+            if (warp == 0 && lane < static_cast<int>(c.C))
+              F.rank_n[lane] = R.pin_hi ? vld(F.rank_lo[lane]) : vld(F.rank_lo[lane]) - vld(F.rank_hi[lane]);
+            __syncthreads();
+          }
+          const float glo = R.lo_all ? -INFINITY : pivot_f(R.lo);
+          const float ghi = R.pin_hi ? INFINITY : pivot_f(R.hi);
+          gather<DT>(c, glo, ghi, R.lo_all, !hit);
+          remote_done = true;
+          s.lo = R.lo;
+          s.c_lo = R.c_lo;
+          if (R.pin_hi) {
+            // everything above lo is gathered
+            s.hi = f2key(row_max);
+            s.c_hi = 0;
+            s.c_above = 0;
+          } else {
+            s.hi = R.hi;
+            s.c_hi = R.c_hi;
+            s.c_above = R.c_hi;  // elements above hi exceed every pivot
+          }
+          k_full = R.pin_hi;
+          list_emit = hit;
+          ties_in_list = true;
+          local_search<DT, false>(c, s, target, value_pivots);
+        }
       }
       rounds_k = static_cast<uint32_t>(s.rounds);
       if (s.capped) {
@@ -1226,177 +1430,290 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
       tau = tau_k;
       n_keep = nk_k;
       count_above = above_k;
+      if (!sel_none && !have_exact) {
+        count_ties_gathered<DT>(c, key2f(tau));
+        ties_known = true;
+      }
     }
 
-    // ---- A5 + A7: top-p search
     if (p_on && !sel_none) {
-      const double pd = static_cast<double>(pr);
-      if (k_on) {
-        // Z_k = mass above tau_k + n_keep_k * w(tau_k): one mass scan with a
-        // single pivot at tau_k over the list (if it covers (tau_k, max]) or
-        // the chunk (compacting x > tau_k when it fits).
-        const bool list_ok = s.list_mode && (path & QRITA_PATH_HIT);
-        if (list_ok) {
-          for (uint32_t i = tid; i < s.list_len; i += kThreads) c.list_w[i] = weight(c.list_x[i], c.m, c.m_neginf);
-          __syncthreads();
+      if (k_on && k_full) {
+        // top-p over S_k, all of it gathered: Z_k = mass(> tau_k) + n_keep_k w(tau_k)
+        const float tk = key2f(tau_k);
+        F2 acc = {0.f, 0.f};
+        const uint32_t gn = min(vld(F.g_n), c.gcap);
+        for (uint32_t i = tid; i < gn; i += kThreads) {
+          const float x = c.g_val[i];
+          f2_add(acc, x > tk ? weight(x, c.m, c.m_neginf) : 0.f);
         }
-        float qf[3] = {pivot_f(tau_k), INFINITY, INFINITY};
-        bool compact = false;
-        if (!list_ok) {
-          // compact x > tau_k while scanning; a CTA whose share does not fit
-          // the list stays in chunk mode (the append never writes past cap)
-          compact = true;
-          if (tid == 0) F.list_n = 0;
-          __syncthreads();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          F2 b;
+          b.hi = __shfl_xor_sync(kFull, acc.hi, o);
+          b.lo = __shfl_xor_sync(kFull, acc.lo, o);
+          acc = f2_merge(acc, b);
         }
-        PAcc acc[3];
-        // compaction range (tau_k, +inf]: keeps the exact top-k set minus ties
-        scan_round<DT, true>(c, list_ok, s.list_len, qf, acc, compact, pivot_f(tau_k), INFINITY);
-        reduce_merge_pivots<DT, true>(c, acc, 0u, 0.0);
-        const double M_gt = vld(F.mg.pv[0].mass);
-        const uint32_t C_gt = vld(F.mg.pv[0].cnt);
-        const double w_tau = weight(key2f(tau_k), c.m, c.m_neginf);
-        Z = M_gt + static_cast<double>(nk_k) * w_tau;
-        const double target = pd * Z;
-        z_used = Z;
+        if (lane == 0) {
+          F.redf[warp][0] = acc.hi;
+          F.redf[warp][1] = acc.lo;
+        }
+        __syncthreads();
+        if (tid == 0) {
+          F2 a = {0.f, 0.f};
+          for (int w = 0; w < kWarps; ++w) {
+            const F2 b = {vld(F.redf[w][0]), vld(F.redf[w][1])};
+            a = f2_merge(a, b);
+          }
+          F.bc.d[BD_TOTAL] = f2_value(a);
+        }
+        __syncthreads();
+        const double M_gt = vld(F.bc.d[BD_TOTAL]);
+        const double w_tau = weight(tk, c.m, c.m_neginf);
+        const double Zk = M_gt + static_cast<double>(nk_k) * w_tau;
+        const double target = pd * Zk;
+        z_used = Zk;
         if (M_gt < target) {
-          // the boundary is inside the tau_k tie group: keep fewer of them
+          // the boundary lies in the tau_k tie group: keep fewer of them
           double nk = ceil((target - M_gt) / w_tau);
           nk = fmin(fmax(nk, 1.0), static_cast<double>(nk_k));
-          tau = tau_k;
           n_keep = static_cast<uint32_t>(nk);
-          count_above = C_gt;
-          // F.ties still holds the per-rank tau_k counts from the top-k search
+          count_above = above_k;
         } else {
-          // search (tau_k, max] by mass
-          Search sp;
-          sp.lo = tau_k;
-          sp.C_lo = C_gt;
-          sp.M_lo = M_gt;
-          sp.hi = f2key(row_max);
-          sp.C_hi = 0;
-          sp.M_hi = 0.0;
-          sp.myM_hi = 0.0;
-          if (list_ok) {
-            sp.list_mode = true;
-            sp.list_len = s.list_len;
-          } else {
-            const uint32_t ln = vld(F.list_n);
-            sp.list_mode = ln <= c.cap && compact;
-            // every CTA decides for itself: a CTA whose compaction overflowed
-            // stays in chunk mode
-            sp.list_len = ln;
-          }
-          sp.above_cnt = 0;
-          sp.above_mass = 0.0;
-          if (warp == 0 && lane < static_cast<int>(c.C)) {
-            F.cnt_lo[lane] = vld(F.rank_cnt[0][lane]);
-            F.cnt_hi[lane] = 0;
-          }
-          quaternary_search<DT, true>(c, sp, target, value_pivots);
-          rounds_p = static_cast<uint32_t>(sp.rounds);
-          if (sp.capped) {
+          Local s;
+          s.lo = tau_k;
+          s.c_lo = above_k;
+          s.m_lo = M_gt;
+          s.hi = f2key(row_max);
+          s.c_hi = 0;
+          s.m_hi = 0.0;
+          s.c_above = 0;
+          s.m_above = 0.0;
+          local_search<DT, true>(c, s, target, value_pivots);
+          rounds_p = static_cast<uint32_t>(s.rounds);
+          if (s.capped) {
             sel_none = true;
             row_status = QRITA_ROW_SEARCH_CAP;
           }
-          tau = sp.tau;
-          n_keep = sp.n_keep;
-          count_above = sp.count_above;
+          tau = s.tau;
+          n_keep = s.n_keep;
+          count_above = s.count_above;
+          count_ties_gathered<DT>(c, key2f(tau));
         }
       } else {
-        const double target = pd * Z;
-        z_used = Z;
-        const bool hit = trunc && !overflow && !force_fb && Mt >= target * (1.0 + 1e-5);
-        path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
-        Search sp;
-        sp.myM_hi = 0.0;
-        sp.above_cnt = 0;
-        sp.above_mass = 0.0;
-        if (hit) {
-          for (uint32_t i = tid; i < my_surv; i += kThreads) c.list_w[i] = weight(c.list_x[i], c.m, c.m_neginf);
-          sp.list_mode = true;
-          sp.list_len = my_surv;
-          sp.lo = f2key(t) - 1u;
-          sp.C_lo = survivors;
-          sp.M_lo = Mt;
-          if (warp == 0 && lane < static_cast<int>(c.C)) F.cnt_lo[lane] = vld(F.rank_surv[lane]);
+        // top-p only, or top-p over an S_k too large to gather
+        const bool hit = !k_on && trunc && !overflow && !force_fb && ref_ok && Mm >= pd * Zm * (1.0 + 1e-5);
+        if (!k_on) path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
+        Local s;
+        s.c_above = 0;
+        s.m_above = 0.0;
+        bool have_exact = false;
+        double target = pd * Zm;
+        if (hit && survivors <= c.gcap) {
+          gather<DT>(c, -INFINITY, INFINITY, true, false);
+          remote_done = true;
+          z_used = Zm;
+          s.lo = f2key(t) - 1u;
+          s.c_lo = survivors;
+          s.m_lo = Mm;
+          s.hi = f2key(row_max);
+          s.c_hi = 0;
+          s.m_hi = 0.0;
+          list_emit = true;
+          ties_in_list = true;
+          local_search<DT, true>(c, s, target, value_pivots);
         } else {
-          sp.list_mode = false;
-          sp.list_len = 0;
-          sp.lo = f2key(row_min) - 1u;
-          sp.C_lo = static_cast<uint32_t>(V);
-          sp.M_lo = Z;
-          if (warp == 0 && lane < static_cast<int>(c.C)) {
-            const int64_t rl = static_cast<int64_t>(V) - static_cast<int64_t>(lane) * P.chunk;
-            F.cnt_lo[lane] = static_cast<uint32_t>(rl <= 0 ? 0 : (rl < P.chunk ? rl : P.chunk));
+          // narrow by mass in fixed point (shift m); a pass over the chunk
+          // measures the denominator (Z, or mass(> tau_k) for S_k) itself
+          Range R;
+          R.pin_hi = false;
+          const float scale = c.fix_scale;
+          double extra = 0.0;
+          if (k_on) {
+            R.lo = tau_k;
+            R.c_lo = above_k;
+            extra = static_cast<double>(nk_k) * static_cast<double>(weight(key2f(tau_k), c.m, c.m_neginf)) *
+                    static_cast<double>(scale);
+          } else if (hit) {
+            R.lo = f2key(t) - 1u;
+            R.c_lo = survivors;
+          } else {
+            R.lo = f2key(row_min) - 1u;
+            R.c_lo = static_cast<uint32_t>(V);
+          }
+          R.lo_all = R.lo < kKeyNegInf;
+          R.hi = f2key(row_max);
+          R.c_hi = 0;
+          R.m_lo = R.m_hi = 0.0;
+          double tg = hit ? pd * Zm * static_cast<double>(scale) : -1.0;
+          narrow<DT, true>(c, R, tg, pd, extra, !hit);
+          passes += static_cast<uint32_t>(R.passes);
+          target = tg / static_cast<double>(scale);
+          z_used = target / pd;
+          // the emission streams the chunk unless a gather below says otherwise
+          list_emit = false;
+          if (R.below) {
+            // only after top-k: mass(> tau_k) < p Z_k, so the boundary lies in
+            // the tau_k tie group (whose per-rank counts F.ties still holds)
+            const double M_gt = R.m_lo / scale;
+            const double w_tau = weight(key2f(tau_k), c.m, c.m_neginf);
+            double nk = ceil((target - M_gt) / w_tau);
+            nk = fmin(fmax(nk, 1.0), static_cast<double>(nk_k));
+            s.tau = tau_k;
+            s.n_keep = static_cast<uint32_t>(nk);
+            s.count_above = above_k;
+            s.rounds = 0;
+            s.capped = false;
+            have_exact = true;  // ties already known from top-k
+          } else if (R.exact) {
+            const double wz = weight(key2f(R.hi), c.m, c.m_neginf);
+            double nk = ceil((target - R.m_hi / scale) / wz);
+            const uint32_t N = R.c_lo - R.c_hi;
+            nk = fmin(fmax(nk, 1.0), static_cast<double>(N));
+            s.tau = R.hi;
+            s.n_keep = static_cast<uint32_t>(nk);
+            s.count_above = R.c_hi;
+            s.rounds = 0;
+            s.capped = false;
+            have_exact = true;
+            ties_in_list = false;  // the own list may not hold this tie group
+            if (warp == 0 && lane < static_cast<int>(c.C))
+              F.ties[lane] = vld(F.rank_lo[lane]) - vld(F.rank_hi[lane]);
+            __syncthreads();
+            ties_known = true;
+          } else if (!R.fits) {
+            s.capped = true;
+            s.rounds = 0;
+          } else {
+            if (!hit) {
+              extract_range<DT>(c, R);
+              if (warp == 0 && lane < static_cast<int>(c.C))
+                F.rank_n[lane] = vld(F.rank_lo[lane]) - vld(F.rank_hi[lane]);
+              __syncthreads();
+            }
+            gather<DT>(c, R.lo_all ? -INFINITY : pivot_f(R.lo), pivot_f(R.hi), R.lo_all, !hit);
+            remote_done = true;
+            s.lo = R.lo;
+            s.hi = R.hi;
+            s.c_lo = R.c_lo;
+            s.c_hi = R.c_hi;
+            s.c_above = R.c_hi;
+            s.m_lo = R.m_lo / scale;
+            s.m_hi = R.m_hi / scale;
+            s.m_above = R.m_hi / scale;
+            list_emit = hit;
+            ties_in_list = true;
+            local_search<DT, true>(c, s, target, value_pivots);
           }
         }
-        sp.hi = f2key(row_max);
-        sp.C_hi = 0;
-        sp.M_hi = 0.0;
-        if (warp == 0 && lane < static_cast<int>(c.C)) F.cnt_hi[lane] = 0;
-        quaternary_search<DT, true>(c, sp, target, value_pivots);
-        rounds_p = static_cast<uint32_t>(sp.rounds);
-        if (sp.capped) {
+        rounds_p = static_cast<uint32_t>(s.rounds);
+        if (s.capped) {
           sel_none = true;
           row_status = QRITA_ROW_SEARCH_CAP;
         }
-        tau = sp.tau;
-        n_keep = sp.n_keep;
-        count_above = sp.count_above;
+        tau = s.tau;
+        n_keep = s.n_keep;
+        count_above = s.count_above;
+        if (!sel_none && !have_exact) {
+          count_ties_gathered<DT>(c, key2f(tau));
+          ties_known = true;
+        }
       }
     }
   }
+  if (!remote_done) {
+    cluster_sync_all();  // no CTA leaves while another may read its memory
+    remote_done = true;
+  }
 
-  // ---- A8 + A9: tie resolution and mask emission
-  __syncthreads();
+  // ---- A8: boundary ties by lowest token id
+  const float tau_f = key2f(tau);
   uint32_t my_first = 0, my_ties = 0;
-  if (!sel_all && !sel_none) {
+  if (!sel_all && !sel_none && ties_known) {
     for (uint32_t l = 0; l < c.crank; ++l) my_first += vld(F.ties[l]);
     my_ties = vld(F.ties[c.crank]);
   }
-  const float tau_f = key2f(tau);
-  // 0: no ties kept, 1: all ties kept, 2: straddling (ordered pass)
+  // tie_mode 0: none kept, 1: all kept, 2: the lowest-index keep_local
   int tie_mode = 0;
   if (!sel_all && !sel_none && my_ties > 0) {
     if (my_first + my_ties <= n_keep) tie_mode = 1;
     else if (my_first < n_keep) tie_mode = 2;
   }
   const uint32_t keep_local = (tie_mode == 2) ? (n_keep - my_first) : 0u;
-  const uintptr_t mask_body = reinterpret_cast<uintptr_t>(gmask + c.head_n);
-  const bool vec_ok = (mask_body % E) == 0;
-  {
-    uint32_t running = 0;  // ties seen so far in index order (tie_mode 2)
-    // head (index order first): thread 0 walks it sequentially
-    if (tid == 0) {
-      for (int i = 0; i < c.head_n; ++i) {
-        const float x = head_elem(c, i);
-        uint8_t b;
-        if (sel_all) b = 1;
-        else if (sel_none) b = 0;
-        else if (x > tau_f) b = 1;
-        else if (x == tau_f) {
-          b = (tie_mode == 1) || (tie_mode == 2 && running < keep_local);
-          ++running;
-        } else b = 0;
-        gmask[i] = b;
+  uint32_t idx_cut = 0;
+  bool ordered_ties = false;
+  if (tie_mode == 2) {
+    if (ties_in_list) {
+      idx_cut = tie_index_cut<DT>(c, tau_f, keep_local);
+    } else {
+      ordered_ties = true;
+    }
+  }
+
+  // ---- A9: mask emission
+  if (sel_all || sel_none || list_emit) {
+    // fill the chunk's mask, then scatter the kept ids of the own list
+    const uint8_t fill = sel_all ? 1 : 0;
+    const uint32_t fill4 = sel_all ? 0x01010101u : 0u;
+    const uintptr_t ma = reinterpret_cast<uintptr_t>(c.gmask);
+    const int mh0 = static_cast<int>((16u - (ma & 15u)) & 15u);
+    const int mh = mh0 < c.n ? mh0 : c.n;
+    const int mb = (c.n - mh) / 16;
+    const int mt = c.n - mh - mb * 16;
+    if (tid < mh) c.gmask[tid] = fill;
+    for (int i = tid; i < mb; i += kThreads)
+      reinterpret_cast<uint4*>(c.gmask + mh)[i] = make_uint4(fill4, fill4, fill4, fill4);
+    if (tid < mt) c.gmask[mh + mb * 16 + tid] = fill;
+    if (list_emit && !sel_all && !sel_none) {
+      __syncthreads();  // the fill is ordered before the scatter
+      const uint32_t n = min(vld(F.own_n), c.ocap);
+      for (uint32_t i = tid; i < n; i += kThreads) {
+        const float x = c.own_val[i];
+        bool keep = x > tau_f;
+        if (x == tau_f) keep = (tie_mode == 1) || (tie_mode == 2 && c.own_idx[i] < idx_cut);
+        if (keep) c.gmask[c.own_idx[i]] = 1;
       }
     }
-    if (tie_mode == 2) {
-      // broadcast the head's tie count
+  } else {
+    // stream the chunk again: x > tau kept, ties by the rule above
+    const uintptr_t mbp = reinterpret_cast<uintptr_t>(c.gmask + c.head_n);
+    const bool vec_ok = (mbp % E) == 0;
+    uint32_t running = 0;  // ties seen so far in index order (ordered_ties)
+    auto byte_of = [&](float x, uint32_t idx, uint32_t& rank) -> uint8_t {
+      if (x > tau_f) return 1;
+      if (x == tau_f) {
+        if (tie_mode == 1) return 1;
+        if (tie_mode == 2) {
+          if (ordered_ties) return (rank++ < keep_local) ? 1 : 0;
+          return idx < idx_cut ? 1 : 0;
+        }
+      }
+      return 0;
+    };
+    if (tid == 0) {
+      for (int i = 0; i < c.head_n; ++i) {
+        const float x = load_elem<DT>(c.gx + i * S);
+        c.gmask[i] = byte_of(x, static_cast<uint32_t>(i), running);
+      }
+    }
+    if (ordered_ties) {
       if (tid == 0) F.scan[0] = running;
       __syncthreads();
       running = vld(F.scan[0]);
       __syncthreads();
     }
-    const int iters = (c.body_units + kThreads - 1) / kThreads;
-    for (int it = 0; it < iters; ++it) {
-      const int u = it * kThreads + tid;
+    const int nb = c.body_units;
+    for (int base = 0; base < nb; base += kThreads) {
+      const int u = base + tid;
+      const bool valid = u < nb;
       float xs[E];
-      bool valid = u < c.body_units;
-      if (valid) unpack<DT>(*reinterpret_cast<const uint4*>(sbody + 16 * u), xs);
-      uint32_t rank0 = 0;
-      if (tie_mode == 2) {
+      if (valid) {
+        unpack<DT>(ldg16(c.gbody + 16 * static_cast<size_t>(u)), xs);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) xs[e] = -INFINITY;
+      }
+      uint32_t rank = 0;
+      if (ordered_ties) {
         uint32_t mine = 0;
         if (valid) {
 #pragma unroll
@@ -1404,32 +1721,21 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
         }
         uint32_t tot;
         const uint32_t ex = block_excl_scan(F, mine, &tot);
-        rank0 = running + ex;
+        rank = running + ex;
         running += tot;
       }
       if (!valid) continue;
       uint8_t bytes[E];
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float x = xs[e];
-        uint8_t b;
-        if (sel_all) b = 1;
-        else if (sel_none) b = 0;
-        else if (x > tau_f) b = 1;
-        else if (x == tau_f) {
-          b = (tie_mode == 1) || (tie_mode == 2 && rank0 < keep_local);
-          ++rank0;
-        } else b = 0;
-        bytes[e] = b;
-      }
-      uint8_t* dst = gmask + c.head_n + static_cast<size_t>(u) * E;
+      for (int e = 0; e < E; ++e) bytes[e] = byte_of(xs[e], static_cast<uint32_t>(c.head_n + u * E + e), rank);
+      uint8_t* dst = c.gmask + c.head_n + static_cast<size_t>(u) * E;
       if (vec_ok) {
         if constexpr (E == 4) {
-          const uint32_t w = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
-          *reinterpret_cast<uint32_t*>(dst) = w;
+          *reinterpret_cast<uint32_t*>(dst) =
+              bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
         } else {
-          uint32_t w0 = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
-          uint32_t w1 = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (static_cast<uint32_t>(bytes[7]) << 24);
+          const uint32_t w0 = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
+          const uint32_t w1 = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (static_cast<uint32_t>(bytes[7]) << 24);
           *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
         }
       } else {
@@ -1437,20 +1743,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
         for (int e = 0; e < E; ++e) dst[e] = bytes[e];
       }
     }
-    // tail: thread 0 sequentially, after every body tie was counted
     if (tid == 0) {
-      uint8_t* tdst = gmask + c.head_n + static_cast<size_t>(c.body_units) * E;
       for (int j = 0; j < c.tail_n; ++j) {
-        const float x = tail_elem(c, j);
-        uint8_t b;
-        if (sel_all) b = 1;
-        else if (sel_none) b = 0;
-        else if (x > tau_f) b = 1;
-        else if (x == tau_f) {
-          b = (tie_mode == 1) || (tie_mode == 2 && running < keep_local);
-          ++running;
-        } else b = 0;
-        tdst[j] = b;
+        const uint32_t idx = static_cast<uint32_t>(c.head_n + nb * E + j);
+        const float x = load_elem<DT>(c.gbody + 16 * static_cast<size_t>(nb) + j * S);
+        c.gmask[idx] = byte_of(x, idx, running);
       }
     }
   }
@@ -1473,31 +1770,23 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const __grid_constant_
       else if (sel_all) kept = static_cast<uint32_t>(V);
       else kept = count_above + n_keep;
       info.boundary = sel_none ? NAN : (sel_all ? row_min : tau_f);
-      info.n_boundary = sel_none ? 0u : (sel_all ? 0u : n_keep);
+      info.n_boundary = (sel_none || sel_all) ? 0u : n_keep;
       info.kept = kept;
       info.status = row_status;
       info.z = z_used;
-      info.reserved = 0.0;
+      info.passes = passes;
+      info.reserved = 0u;
       P.row_info[r] = info;
     }
   }
-
-  // If a copy wait expired, give the copies one more bounded chance to land
-  // before the CTA's shared memory is released.
-  if (timed_out && tid == 0) {
-    for (int pc = 0; pc < npieces; ++pc) (void)mbar_wait_bounded(smem_u32(&F.bars[pc]), 0, kWaitLimitNs);
-  }
-  // No CTA leaves while another may still read its shared memory.
-  cluster_sync_all();
 }
 
 }  // namespace
 
-size_t smem_bytes(int dtype, int chunk, int cap) {
-  const int s = dtype == QRITA_DTYPE_F32 ? 4 : 2;
+size_t smem_bytes(int ocap, int gcap) {
   size_t b = sizeof(Fixed);
-  b += static_cast<size_t>(cap) * 8u;  // list values + weights
-  b += 16u + static_cast<size_t>(chunk) * s + 32u;
+  b += static_cast<size_t>(ocap) * 8u;  // own list: value + index
+  b += static_cast<size_t>(gcap) * 8u;  // gathered set: value + tag
   return (b + 127u) & ~static_cast<size_t>(127u);
 }
 
@@ -1508,21 +1797,6 @@ int max_smem_per_block() {
   cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   return v;
 }
-
-#ifdef QRITA_TRACE
-extern "C" int qrita_debug_trace(double* out, int cap, int reset) {
-  unsigned n = 0;
-  cudaDeviceSynchronize();
-  cudaMemcpyFromSymbol(&n, g_trace_n, sizeof(n));
-  if (n > static_cast<unsigned>(cap)) n = cap;
-  cudaMemcpyFromSymbol(out, g_trace, n * sizeof(double));
-  if (reset) {
-    unsigned z = 0;
-    cudaMemcpyToSymbol(g_trace_n, &z, sizeof(z));
-  }
-  return static_cast<int>(n);
-}
-#endif
 
 int launch_select(const Params& prm, int dtype, size_t smem, qrita_stream_t stream) {
   const void* fn = dtype == QRITA_DTYPE_F32 ? reinterpret_cast<const void*>(&select_kernel<QRITA_DTYPE_F32>)
