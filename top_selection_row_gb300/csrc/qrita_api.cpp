@@ -65,12 +65,14 @@ constexpr float kAlphaK = 2.0f;
 constexpr float kUMaxK = 0.25f;
 constexpr float kMarginP = 0.25f;
 
-// Candidate list capacities (entries of value + index): a CTA's own list
-// and the gathered set every CTA of a row searches. Four CTAs of 256 threads
-// fit on one SM with these.
-constexpr int kOwnCap = 2048;
-constexpr int kGatherCap = 4096;
-constexpr int kCtasPerSm = 4;
+// Candidate list capacities (entries of value + index): a CTA's own list and
+// the gathered set every CTA of a row searches; with one CTA per row the two
+// are one list. About 96 KiB either way, two CTAs per SM.
+constexpr int kOwnCap = 4096;
+constexpr int kGatherCap = 8192;
+constexpr int kSoleCap = 12288;
+// Resident CTAs per SM the kernel is built for (its register budget).
+constexpr int kCtasPerSm = 2;
 // Rows shorter than this per CTA are not split further.
 constexpr int64_t kMinChunk = 1024;
 // Chunk indices must fit below the rank bits of a gathered tag.
@@ -120,8 +122,6 @@ struct Shape {
 int choose_shape(int64_t B, int64_t V, uint32_t flags, Shape* out) {
   const int optin = smem_optin();
   if (optin <= 0) return QRITA_ECUDA;
-  const size_t smem = smem_bytes(kOwnCap, kGatherCap);
-  if (smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
   int C = 1;
   if (flags & QRITA_FLAG_CLUSTER_SET) {
     const int shift = static_cast<int>((flags >> QRITA_FLAG_CLUSTER_SHIFT) & 7u);
@@ -138,10 +138,14 @@ int choose_shape(int64_t B, int64_t V, uint32_t flags, Shape* out) {
   int64_t chunk = (V + C - 1) / C;
   chunk = (chunk + 15) / 16 * 16;
   if (B * C > static_cast<int64_t>(std::numeric_limits<int32_t>::max())) return QRITA_EUNSUPPORTED;
+  const int ocap = C == 1 ? kSoleCap : kOwnCap;
+  const int gcap = C == 1 ? kSoleCap : kGatherCap;
+  const size_t smem = smem_bytes(C, ocap, gcap);
+  if (smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
   out->C = C;
   out->chunk = static_cast<int>(chunk);
-  out->ocap = kOwnCap;
-  out->gcap = kGatherCap;
+  out->ocap = ocap;
+  out->gcap = gcap;
   out->smem = smem;
   return QRITA_OK;
 }

@@ -74,7 +74,63 @@ __device__ __forceinline__ F2 f2_merge(F2 a, F2 b) {
   return r;
 }
 
-__device__ __forceinline__ double f2_value(F2 a) { return static_cast<double>(a.hi) + a.lo; }
+__device__ __forceinline__ F2 f2_make(float hi, float lo) {
+  F2 r;
+  r.hi = hi;
+  r.lo = lo;
+  return r;
+}
+
+// a - b
+__device__ __forceinline__ F2 f2_sub(F2 a, F2 b) {
+  F2 nb;
+  nb.hi = -b.hi;
+  nb.lo = -b.lo;
+  return f2_merge(a, nb);
+}
+
+// p * a (FMA gives the exact error of the leading product)
+__device__ __forceinline__ F2 f2_mul(F2 a, float p) {
+  const float hi = p * a.hi;
+  const float e = fmaf(p, a.hi, -hi) + p * a.lo;
+  F2 r;
+  r.hi = hi + e;
+  r.lo = e - (r.hi - hi);
+  return r;
+}
+
+// n * w as a pair (exact for integers n below 2^24)
+__device__ __forceinline__ F2 f2_prod(float n, float w) {
+  F2 r;
+  r.hi = n * w;
+  r.lo = fmaf(n, w, -r.hi);
+  return r;
+}
+
+// a >= b, decided on the pair difference (sign exact to about 2^-48 relative)
+__device__ __forceinline__ bool f2_ge(F2 a, F2 b) {
+  const F2 d = f2_sub(a, b);
+  return d.hi > 0.f || (d.hi == 0.f && d.lo >= 0.f);
+}
+
+__device__ __forceinline__ float f2_float(F2 a) { return a.hi + a.lo; }
+
+// Exact conversion of a fixed-point integer (< 2^63) to a pair, and back.
+__device__ __forceinline__ F2 f2_from_u64(unsigned long long v) {
+  const float hi = __ull2float_rz(v);
+  const unsigned long long h = static_cast<unsigned long long>(hi);
+  F2 r;
+  r.hi = hi;
+  r.lo = __ull2float_rn(v - h);  // v >= h by round-toward-zero
+  return r;
+}
+
+__device__ __forceinline__ unsigned long long f2_to_u64(F2 a) {
+  if (!(a.hi > 0.f)) return 0ull;
+  const unsigned long long h = __float2ull_rz(a.hi);
+  const long long l = __float2ll_rn(a.lo + (a.hi - static_cast<float>(h)));
+  return l < 0 ? h - static_cast<unsigned long long>(-l) : h + static_cast<unsigned long long>(l);
+}
 
 // ---------------------------------------------------------------------------
 // Shared-memory addressing, mbarriers and TMA bulk copies.

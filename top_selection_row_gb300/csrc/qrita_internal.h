@@ -23,7 +23,7 @@ constexpr int kLutP = 64;
 // Threads per CTA of the selection kernel.
 constexpr int kThreads = 256;
 // 16-byte units each thread keeps in flight while streaming a chunk.
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 // Largest cluster the launcher uses (16 needs the non-portable opt-in).
 constexpr int kMaxCluster = 16;
 // Pivots one distributed narrowing pass evaluates: two quaternary levels,
@@ -46,7 +46,9 @@ struct Params {
   int32_t C;        // CTAs per row (cluster size)
   int32_t chunk;    // elements per CTA (multiple of 16)
   int32_t ocap;     // own candidate list capacity per CTA (entries)
-  int32_t gcap;     // gathered candidate set capacity per CTA (entries)
+  int32_t gcap;     // gathered candidate set capacity per CTA (entries); with
+                    // one CTA per row (C == 1) the own list is the gathered
+                    // set and ocap == gcap
   uint32_t flags;   // QRITA_FLAG_*
   float alpha_k;    // top-k truncation safety factor (u = alpha_k * k / V)
   float margin_p;   // subtracted from the top-p delta
@@ -55,8 +57,12 @@ struct Params {
   float lut_p[kLutP];
 };
 
-// Bytes of dynamic shared memory the kernel needs for the list capacities.
-size_t smem_bytes(int ocap, int gcap);
+// Smallest list region (bytes) the kernel accepts: its narrowing bins reuse it.
+constexpr int kMinListBytes = 48 * 1024;
+
+// Bytes of dynamic shared memory the kernel needs for C CTAs per row and the
+// list capacities.
+size_t smem_bytes(int C, int ocap, int gcap);
 
 // Launch the selection kernel (grid B*C, cluster C). Returns a cudaError_t.
 int launch_select(const Params& prm, int dtype, size_t smem, qrita_stream_t stream);

@@ -50,6 +50,29 @@ constexpr int kSampleBlocks = 16;
 constexpr int kSampleBlock = 64;  // 16 x 64 = 1024 sampled logits per row
 constexpr int kBins = kNarrowPivots + 1;
 constexpr int kTagShift = 28;  // gathered tag = rank << 28 | index in chunk
+// A chunk narrowing pass lays per-thread bins (counts, then fixed-point
+// masses) over the list region, which must hold them.
+constexpr int kBinBytes = kBins * kThreads * (4 + 8);
+static_assert(kBinBytes <= kMinListBytes, "the narrowing bins must fit over the lists");
+#ifdef QRITA_TRACE_TIME
+// Debug-only stage timestamps of three CTAs, and start / end of every CTA
+// (built with -DQRITA_TRACE_TIME).
+__device__ unsigned long long g_times[3][16];
+__device__ unsigned long long g_cta_times[65536][2];
+#define QRITA_T(i)                                                                              \
+  do {                                                                                          \
+    if (threadIdx.x == 0) {                                                                     \
+      const int slot_ = blockIdx.x == 0 ? 0                                                     \
+                        : (blockIdx.x == gridDim.x / 2 ? 1 : (blockIdx.x == gridDim.x - 1 ? 2 : -1)); \
+      if (slot_ >= 0) g_times[slot_][i] = globaltimer_ns();                                     \
+    }                                                                                           \
+  } while (0)
+#else
+#define QRITA_T(i) \
+  do {             \
+  } while (0)
+#endif
+
 // Pinned narrowing (from below only) gives up after this many passes and
 // narrows from both ends (a tie group at the boundary larger than the lists).
 constexpr int kPinnedPasses = 12;
@@ -122,11 +145,12 @@ struct alignas(16) Slot {  // what one CTA publishes for one cluster merge
   uint32_t cnt[kBins + 1];             // narrowing: per-bin counts; [kBins] above hi
   float f[4];
   uint32_t u[4];
-  double d[2];
+  float pr[4];  // float pairs (softmax sums of the streaming pass)
 };
 
 struct alignas(16) Bcast {  // written by one thread / warp 0 before a block barrier
-  double d[8];
+  unsigned long long x[8];  // fixed-point masses (narrowing)
+  float pr[16];             // float pairs: pair i is (pr[2i], pr[2i+1])
   float f[12];
   uint32_t u[24];
   uint32_t q[16];  // pivot keys, increasing
@@ -141,16 +165,24 @@ struct alignas(16) PAccS {  // per-warp pivot partial (block reduction scratch)
   uint32_t pad[3];
 };
 
+// Per-warp partial of one pivot of the local search.
+struct alignas(16) LPart {
+  unsigned long long mass;
+  uint32_t cnt, zmin, nz, pad;
+};
+
 struct alignas(16) Fixed {
   Slot slots[2];
   Bcast bc;
   PAccS red[kWarps][3];
+  LPart lred[kWarps][3];
   float redf[kWarps][8];
   uint32_t redu[kWarps][kBins];
   uint32_t bin_cnt[kWarps][kBins];
   unsigned long long bin_mass[kWarps][kBins];
   uint32_t rank_bins[kMaxCluster][kBins + 1];  // latest narrowing merge, per rank
   uint32_t rank_n[kMaxCluster];   // per-rank entries to gather
+  uint32_t rank_off[kMaxCluster + 1];  // their prefix offsets in the gathered set
   uint32_t rank_lo[kMaxCluster];  // per-rank count above the narrowing lo
   uint32_t rank_hi[kMaxCluster];  // per-rank count above the narrowing hi
   uint32_t ties[kMaxCluster];     // per-rank count of boundary-valued elements
@@ -165,10 +197,21 @@ enum : int {
   BF_MU = 0, BF_SIGMA, BF_MREF, BF_T, BF_MAX, BF_MIN, BF_SMIN, BF_LOF, BF_HIF,
   // uints
   BU_TRUNC = 0, BU_SMIN_N, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
-  BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW,
-  // doubles
-  BD_ZR = 0, BD_MR, BD_MLO, BD_MHI, BD_TARGET, BD_TOTAL,
+  BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS,
+  // fixed-point masses
+  BX_TARGET = 0, BX_MLO, BX_MHI,
+  // float pairs
+  BP_ZR = 0, BP_MR, BP_MLO, BP_MHI, BP_TOTAL,
 };
+
+__device__ __forceinline__ void put_pair(Bcast& b, int i, F2 v) {
+  b.pr[2 * i] = v.hi;
+  b.pr[2 * i + 1] = v.lo;
+}
+
+__device__ __forceinline__ F2 get_pair(const Bcast& b, int i) {
+  return f2_make(vld(b.pr[2 * i]), vld(b.pr[2 * i + 1]));
+}
 
 // ---------------------------------------------------------------------------
 // Pivot accumulators of the local search
@@ -316,51 +359,65 @@ __device__ __forceinline__ void warp_append(uint32_t* counter, float* vals, uint
 // range") when value_ok and both ends are finite floats; otherwise quartiles
 // of the 32-bit key range, which always shrink it fourfold. Writes up to 3
 // strictly increasing keys inside (lo, hi) and returns how many.
-__device__ int quartile_pivots(uint32_t lo, uint32_t hi, bool value_ok, uint32_t* q, bool* used_value) {
+__device__ __forceinline__ int quartile_pivots(uint32_t lo, uint32_t hi, bool value_ok, uint32_t& q0,
+                                               uint32_t& q1, uint32_t& q2, bool& used_value) {
   const uint32_t span = hi - lo;
-  *used_value = false;
+  used_value = false;
+  q0 = q1 = q2 = hi;
   if (span <= 1u) return 0;
   if (span <= 4u) {
-    const int np = static_cast<int>(span) - 1;
-    for (int j = 0; j < np; ++j) q[j] = lo + 1u + static_cast<uint32_t>(j);
-    return np;
+    q0 = lo + 1u;
+    q1 = lo + 2u;
+    q2 = lo + 3u;
+    return static_cast<int>(span) - 1;
   }
   if (value_ok) {
     const float vlo = key2f(lo), vhi = key2f(hi);
-    if (isfinite(vlo) && isfinite(vhi)) {
-      const double dl = vlo, dh = vhi;
-      const uint32_t a = f2key(static_cast<float>(dl + 0.25 * (dh - dl)));
-      const uint32_t b = f2key(static_cast<float>(dl + 0.50 * (dh - dl)));
-      const uint32_t c = f2key(static_cast<float>(dl + 0.75 * (dh - dl)));
+    const float width = vhi - vlo;
+    if (isfinite(vlo) && isfinite(vhi) && isfinite(width)) {
+      const uint32_t a = f2key(fmaf(0.25f, width, vlo));
+      const uint32_t b = f2key(fmaf(0.50f, width, vlo));
+      const uint32_t c = f2key(fmaf(0.75f, width, vlo));
       if (lo < a && a < b && b < c && c < hi) {
-        q[0] = a;
-        q[1] = b;
-        q[2] = c;
-        *used_value = true;
+        q0 = a;
+        q1 = b;
+        q2 = c;
+        used_value = true;
         return 3;
       }
     }
   }
-  for (int j = 0; j < 3; ++j) q[j] = lo + static_cast<uint32_t>((static_cast<uint64_t>(span) * (j + 1)) >> 2);
+  q0 = lo + static_cast<uint32_t>((static_cast<uint64_t>(span) * 1u) >> 2);
+  q1 = lo + static_cast<uint32_t>((static_cast<uint64_t>(span) * 2u) >> 2);
+  q2 = lo + static_cast<uint32_t>((static_cast<uint64_t>(span) * 3u) >> 2);
   return 3;
 }
 
 // Two quaternary levels at once: the quartile pivots of (lo, hi] and of each
-// of the four sub-ranges they cut. Returns the count (<= 15), keys sorted.
-__device__ int two_level_pivots(uint32_t lo, uint32_t hi, bool value_ok, uint32_t* q, bool* used_value) {
-  uint32_t l1[3];
-  const int n1 = quartile_pivots(lo, hi, value_ok, l1, used_value);
+// of the four sub-ranges they cut, written in increasing order to the
+// shared pivot arrays (keys and floats, +inf padded). Returns the count.
+__device__ int two_level_pivots(uint32_t lo, uint32_t hi, bool value_ok, volatile uint32_t* q,
+                                volatile float* qf, bool& used_value) {
+  uint32_t a0, a1, a2;
+  const int n1 = quartile_pivots(lo, hi, value_ok, a0, a1, a2, used_value);
   int n = 0;
   uint32_t a = lo;
-  for (int s = 0; s <= n1; ++s) {
-    const uint32_t b = (s < n1) ? l1[s] : hi;
-    uint32_t l2[3];
-    bool uv = false;
-    const int n2 = quartile_pivots(a, b, value_ok, l2, &uv);
-    for (int j = 0; j < n2; ++j) q[n++] = l2[j];
-    if (s < n1) q[n++] = l1[s];
-    a = b;
+#pragma unroll
+  for (int s = 0; s <= 3; ++s) {
+    if (s <= n1) {
+      const uint32_t b = (s < n1) ? (s == 0 ? a0 : (s == 1 ? a1 : a2)) : hi;
+      uint32_t b0, b1, b2;
+      bool uv = false;
+      const int n2 = quartile_pivots(a, b, value_ok, b0, b1, b2, uv);
+      if (n2 > 0) q[n++] = b0;
+      if (n2 > 1) q[n++] = b1;
+      if (n2 > 2) q[n++] = b2;
+      if (s < n1) q[n++] = b;
+      a = b;
+    }
   }
+  for (int j = 0; j < 16; ++j) qf[j] = (j < n) ? pivot_f(q[j]) : INFINITY;
+  for (int j = n; j < 16; ++j) q[j] = hi;
   return n;
 }
 
@@ -372,6 +429,8 @@ struct Ctx {
   static constexpr int E = Elem<DT>::kPerUnit;
   static constexpr int S = Elem<DT>::kBytes;
   Fixed* F;
+  unsigned char* lists;  // the list region (own list, then the gathered set)
+  bool alias;            // one CTA per row: the own list is the gathered set
   float* own_val;
   uint32_t* own_idx;
   uint32_t ocap;
@@ -436,54 +495,76 @@ __device__ __forceinline__ void stream_chunk(const Ctx<DT>& c, UnitFn&& unit_fn,
 struct Range {
   uint32_t lo, hi;      // count/mass(> lo) >= target > count/mass(> hi)
   uint32_t c_lo, c_hi;  // row counts above lo / hi
-  double m_lo, m_hi;    // row masses above lo / hi (fixed-point units)
+  unsigned long long m_lo, m_hi;  // row masses above lo / hi (fixed point)
+  unsigned long long target;      // fixed point (mass) or count
+  bool target_from_total;  // the first pass sets target = p * (mass above lo + extra)
+  float p_frac;
+  unsigned long long extra;
   bool lo_all;          // lo lies below key(-inf): every element is above it
   bool pin_hi;          // narrow from below only: gather everything above lo
   bool fits;            // the range fits the lists: gather it
   bool exact;           // hi - lo <= 1: the boundary value is hi
-  bool below;           // the target exceeds everything above lo: the boundary is lo itself
+  bool below;           // the target exceeds everything above lo: the boundary is at lo
   int passes;
 };
+
+// Bin of x among the increasing pivots (+inf padded): the number of pivots
+// below x, by a 4-step branch-free search.
+__device__ __forceinline__ int pivot_bin(const volatile float* qf, float x) {
+  int b = 0;
+  b += (x > qf[b + 7]) ? 8 : 0;
+  b += (x > qf[b + 3]) ? 4 : 0;
+  b += (x > qf[b + 1]) ? 2 : 0;
+  b += (x > qf[b]) ? 1 : 0;
+  return b;
+}
 
 // One narrowing pass: up to 15 pivots (two quaternary levels) cut (lo, hi]
 // into bins; every CTA bins its elements (from its list, or by streaming its
 // chunk again), the bins merge across the cluster in rank order, and warp 0
 // keeps the bin that holds the boundary. Counts are exact integers and
 // masses exact sums of fixed-point weights, so the merge is deterministic.
-// target < 0 means "p_frac times (the pass's total mass + extra)": the pass
-// then also measures the softmax denominator.
+// A chunk pass bins into per-thread columns of shared memory (no atomics)
+// laid over the own list and the gathered set, which it leaves undefined.
 template <int DT, bool MASS>
-__device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac, double extra,
-                            bool from_chunk, bool value_ok, bool* used_value_out) {
+__device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok, bool* used_value_out) {
   constexpr int E = Ctx<DT>::E;
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
   if (tid == 0) {
-    uint32_t q[kNarrowPivots];
     bool used_value = false;
-    const int np = two_level_pivots(R.lo, R.hi, value_ok, q, &used_value);
-    for (int j = 0; j < 16; ++j) {
-      F.bc.q[j] = (j < np) ? q[j] : R.hi;
-      F.bc.qf[j] = (j < np) ? pivot_f(q[j]) : INFINITY;
-    }
+    const int np = two_level_pivots(R.lo, R.hi, value_ok, F.bc.q, F.bc.qf, used_value);
     F.bc.u[BU_NP] = static_cast<uint32_t>(np);
     F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
     F.bc.f[BF_LOF] = R.lo_all ? -INFINITY : pivot_f(R.lo);
     F.bc.f[BF_HIF] = pivot_f(R.hi);
   }
-  for (int i = tid; i < kWarps * kBins; i += kThreads) {
-    (&F.bin_cnt[0][0])[i] = 0u;
-    (&F.bin_mass[0][0])[i] = 0ull;
+  uint32_t* lcnt = reinterpret_cast<uint32_t*>(c.lists);  // [kBins][kThreads]
+  unsigned long long* lmass =
+      reinterpret_cast<unsigned long long*>(c.lists + kBins * kThreads * 4);  // [kBins][kThreads]
+  __syncthreads();  // pivots published; earlier readers of the lists are done
+  const volatile float* qf = F.bc.qf;
+  if (from_chunk) {
+#pragma unroll
+    for (int b = 0; b < kBins; ++b) {
+      lcnt[b * kThreads + tid] = 0u;
+      if (MASS) lmass[b * kThreads + tid] = 0ull;
+    }
+  } else {
+    for (int i = tid; i < kWarps * kBins; i += kThreads) {
+      (&F.bin_cnt[0][0])[i] = 0u;
+      (&F.bin_mass[0][0])[i] = 0ull;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   const float lo_f = vld(F.bc.f[BF_LOF]);
   const float hi_f = vld(F.bc.f[BF_HIF]);
   const bool lo_all = R.lo_all;
   const float scale = c.fix_scale;
   uint32_t above_c = 0;
   unsigned long long above_m = 0ull;
-  auto bin_one = [&](float x) {
+  auto bin_one = [&](float x, bool private_bins) {
     if (!(lo_all || x > lo_f)) return;
     unsigned long long wf = 0ull;
     if (MASS) wf = __float2ull_rn(weight(x, c.m, c.m_neginf) * scale);
@@ -492,14 +573,14 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac,
       above_m += wf;
       return;
     }
-    // bin = number of pivots below x (pivots increasing, +inf padded)
-    int b = 0;
-    b += (x > vld(F.bc.qf[b + 7])) ? 8 : 0;
-    b += (x > vld(F.bc.qf[b + 3])) ? 4 : 0;
-    b += (x > vld(F.bc.qf[b + 1])) ? 2 : 0;
-    b += (x > vld(F.bc.qf[b])) ? 1 : 0;
-    atomicAdd(&F.bin_cnt[warp][b], 1u);
-    if (MASS) atomicAdd(&F.bin_mass[warp][b], wf);
+    const int b = pivot_bin(qf, x);
+    if (private_bins) {
+      lcnt[b * kThreads + tid] += 1u;
+      if (MASS) lmass[b * kThreads + tid] += wf;
+    } else {
+      atomicAdd(&F.bin_cnt[warp][b], 1u);
+      if (MASS) atomicAdd(&F.bin_mass[warp][b], wf);
+    }
   };
   if (from_chunk) {
     stream_chunk<DT>(
@@ -507,14 +588,14 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac,
         [&](const float (&xs)[E], uint32_t, bool valid) {
           if (!valid) return;
 #pragma unroll
-          for (int e = 0; e < E; ++e) bin_one(xs[e]);
+          for (int e = 0; e < E; ++e) bin_one(xs[e], true);
         },
         [&](float x, uint32_t, bool valid) {
-          if (valid) bin_one(x);
+          if (valid) bin_one(x, true);
         });
   } else {
     const uint32_t n = min(vld(F.own_n), c.ocap);
-    for (uint32_t i = tid; i < n; i += kThreads) bin_one(c.own_val[i]);
+    for (uint32_t i = tid; i < n; i += kThreads) bin_one(c.own_val[i], false);
   }
   above_c = warp_sum_u(above_c);
   above_m = warp_sum_u64(above_m);
@@ -525,7 +606,23 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac,
   }
   __syncthreads();
   Slot& my = F.slots[c.ph & 1];
-  if (tid < kBins) {
+  if (from_chunk) {
+    // warp w totals bins w and w + kWarps over the thread columns
+    for (int b = warp; b < kBins; b += kWarps) {
+      uint32_t s = 0;
+      unsigned long long sm = 0ull;
+      for (int i = lane; i < kThreads; i += 32) {
+        s += vld(lcnt[b * kThreads + i]);
+        if (MASS) sm += vld(lmass[b * kThreads + i]);
+      }
+      s = warp_sum_u(s);
+      sm = warp_sum_u64(sm);
+      if (lane == 0) {
+        my.cnt[b] = s;
+        my.mass[b] = sm;
+      }
+    }
+  } else if (tid < kBins) {
     uint32_t s = 0;
     unsigned long long sm = 0ull;
     for (int w = 0; w < kWarps; ++w) {
@@ -534,7 +631,8 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac,
     }
     my.cnt[tid] = s;
     my.mass[tid] = sm;
-  } else if (tid == kBins) {
+  }
+  if (tid == kThreads - 1) {
     uint32_t s = 0;
     unsigned long long sm = 0ull;
     for (int w = 0; w < kWarps; ++w) {
@@ -565,66 +663,55 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac,
       }
     }
     const int np = static_cast<int>(vld(F.bc.u[BU_NP]));
-    uint32_t bc_all[kBins + 1];
-    unsigned long long bm_all[kBins + 1];
+    // cumulative from the top: lane b gets the elements above pivot b-1
+    // (lane 0: above lo), lane np+1 .. kBins: above hi
+    uint32_t cc = (lane <= np || lane == kBins) ? tot_c : 0u;
+    unsigned long long cm = (lane <= np || lane == kBins) ? tot_m : 0ull;
 #pragma unroll
-    for (int b = 0; b <= kBins; ++b) {
-      bc_all[b] = __shfl_sync(kFull, tot_c, b);
-      bm_all[b] = __shfl_sync(kFull, tot_m, b);
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t c2 = __shfl_down_sync(kFull, cc, o);
+      const unsigned long long m2 = __shfl_down_sync(kFull, cm, o);
+      if (lane + o < 32) {
+        cc += c2;
+        cm += m2;
+      }
     }
     __syncwarp();  // per-rank bins visible to the whole warp
     int lo_j = -1, hi_j = -1;
-    if (lane == 0) {
-      // cum[b] = elements above pivot b-1 (cum[0]: above lo); top: above hi
-      uint32_t cum_c[kBins + 1];
-      double cum_m[kBins + 1];
-      uint32_t cc = bc_all[kBins];
-      double cm = static_cast<double>(bm_all[kBins]);
-      for (int b = np; b >= 0; --b) {
-        cc += bc_all[b];
-        cm += static_cast<double>(bm_all[b]);
-        cum_c[b] = cc;
-        cum_m[b] = cm;
-      }
-      double tgt = target;
-      if (tgt < 0.0) {
-        tgt = p_frac * (cum_m[0] + extra);
-        F.bc.d[BD_TOTAL] = cum_m[0];
-      }
-      F.bc.d[BD_TARGET] = tgt;
-      F.bc.u[BU_BELOW] = ((MASS ? cum_m[0] : static_cast<double>(cum_c[0])) < tgt) ? 1u : 0u;
-      for (int j = 0; j < np; ++j) {
-        const double above = MASS ? cum_m[j + 1] : static_cast<double>(cum_c[j + 1]);
-        if (above >= tgt) {
-          lo_j = j;
-        } else {
-          hi_j = j;
-          break;
-        }
-      }
-      if (R.pin_hi) hi_j = -1;
-      uint32_t nlo = R.lo, nhi = R.hi;
-      uint32_t nclo = cum_c[0], nchi = bc_all[kBins];
-      double nmlo = cum_m[0], nmhi = static_cast<double>(bm_all[kBins]);
-      if (lo_j >= 0) {
-        nlo = vld(F.bc.q[lo_j]);
-        nclo = cum_c[lo_j + 1];
-        nmlo = cum_m[lo_j + 1];
-      }
-      if (hi_j >= 0) {
-        nhi = vld(F.bc.q[hi_j]);
-        nchi = cum_c[hi_j + 1];
-        nmhi = cum_m[hi_j + 1];
-      }
-      F.bc.u[BU_LO] = nlo;
-      F.bc.u[BU_HI] = nhi;
-      F.bc.u[BU_CLO] = nclo;
-      F.bc.u[BU_CHI] = nchi;
-      F.bc.d[BD_MLO] = nmlo;
-      F.bc.d[BD_MHI] = nmhi;
+    const uint32_t above_hi_c = __shfl_sync(kFull, tot_c, kBins);
+    const unsigned long long above_hi_m = __shfl_sync(kFull, tot_m, kBins);
+    unsigned long long tgt = R.target;
+    if (R.target_from_total) {
+      const unsigned long long total = __shfl_sync(kFull, cm, 0) + R.extra;
+      tgt = f2_to_u64(f2_mul(f2_from_u64(total), R.p_frac));
     }
-    lo_j = __shfl_sync(kFull, lo_j, 0);
-    hi_j = __shfl_sync(kFull, hi_j, 0);
+    // walk the pivots upward (every lane, same values)
+    for (int j = 0; j < np; ++j) {
+      const uint32_t ac = __shfl_sync(kFull, cc, j + 1);
+      const unsigned long long am = __shfl_sync(kFull, cm, j + 1);
+      const bool reach = MASS ? (am >= tgt) : (static_cast<unsigned long long>(ac) >= tgt);
+      if (hi_j < 0) {
+        if (reach) lo_j = j;
+        else hi_j = j;
+      }
+    }
+    if (R.pin_hi) hi_j = -1;
+    const uint32_t c0 = __shfl_sync(kFull, cc, 0);
+    const unsigned long long m0 = __shfl_sync(kFull, cm, 0);
+    const uint32_t clo = lo_j >= 0 ? __shfl_sync(kFull, cc, lo_j + 1) : c0;
+    const unsigned long long mlo = lo_j >= 0 ? __shfl_sync(kFull, cm, lo_j + 1) : m0;
+    const uint32_t chi = hi_j >= 0 ? __shfl_sync(kFull, cc, hi_j + 1) : above_hi_c;
+    const unsigned long long mhi = hi_j >= 0 ? __shfl_sync(kFull, cm, hi_j + 1) : above_hi_m;
+    if (lane == 0) {
+      F.bc.x[BX_TARGET] = tgt;
+      F.bc.u[BU_BELOW] = (MASS ? (m0 < tgt) : (static_cast<unsigned long long>(c0) < tgt)) ? 1u : 0u;
+      F.bc.u[BU_LO] = lo_j >= 0 ? vld(F.bc.q[lo_j]) : R.lo;
+      F.bc.u[BU_HI] = hi_j >= 0 ? vld(F.bc.q[hi_j]) : R.hi;
+      F.bc.u[BU_CLO] = clo;
+      F.bc.u[BU_CHI] = chi;
+      F.bc.x[BX_MLO] = mlo;
+      F.bc.x[BX_MHI] = mhi;
+    }
     // per-rank counts above the new lo / hi, from that rank's bins
     uint32_t maxr = 0;
     if (lane < static_cast<int>(c.C)) {
@@ -644,13 +731,14 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac,
   }
   __syncthreads();
   ++c.ph;
-  target = vld(F.bc.d[BD_TARGET]);
+  R.target = vld(F.bc.x[BX_TARGET]);
+  R.target_from_total = false;
   R.lo = vld(F.bc.u[BU_LO]);
   R.hi = vld(F.bc.u[BU_HI]);
   R.c_lo = vld(F.bc.u[BU_CLO]);
   R.c_hi = vld(F.bc.u[BU_CHI]);
-  R.m_lo = vld(F.bc.d[BD_MLO]);
-  R.m_hi = vld(F.bc.d[BD_MHI]);
+  R.m_lo = vld(F.bc.x[BX_MLO]);
+  R.m_hi = vld(F.bc.x[BX_MHI]);
   R.lo_all = R.lo < kKeyNegInf;
   const uint32_t maxr = vld(F.bc.u[BU_MAXR]);
   const uint32_t in_range = R.pin_hi ? R.c_lo : R.c_lo - R.c_hi;
@@ -662,7 +750,7 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, double& target, double p_frac,
 }
 
 template <int DT, bool MASS>
-__device__ void narrow(Ctx<DT>& c, Range& R, double& target, double p_frac, double extra, bool from_chunk) {
+__device__ void narrow(Ctx<DT>& c, Range& R, bool from_chunk) {
   bool value_ok = true;
   R.passes = 0;
   R.fits = false;
@@ -671,7 +759,7 @@ __device__ void narrow(Ctx<DT>& c, Range& R, double& target, double p_frac, doub
   while (true) {
     const uint32_t span_before = R.hi - R.lo;
     bool used_value = false;
-    narrow_pass<DT, MASS>(c, R, target, p_frac, extra, from_chunk, value_ok, &used_value);
+    narrow_pass<DT, MASS>(c, R, from_chunk, value_ok, &used_value);
     if (R.below || R.fits || R.exact) break;
     if (R.passes >= kMaxRounds) break;
     if (R.pin_hi && R.passes >= kPinnedPasses) R.pin_hi = false;
@@ -717,6 +805,12 @@ __device__ void extract_range(Ctx<DT>& c, const Range& R) {
 template <int DT>
 __device__ void gather(Ctx<DT>& c, float lo_f, float hi_f, bool lo_all, bool sync_first) {
   Fixed& F = *c.F;
+  if (c.alias) {
+    // one CTA per row: the own list holds exactly the range (an extraction)
+    if (threadIdx.x == 0) F.g_n = min(vld(F.own_n), c.gcap);
+    __syncthreads();
+    return;
+  }
   if (threadIdx.x == 0) F.g_n = 0;
   if (sync_first) cluster_sync_all();
   __syncthreads();
@@ -741,183 +835,340 @@ __device__ void gather(Ctx<DT>& c, float lo_f, float hi_f, bool lo_all, bool syn
   cluster_sync_all();
 }
 
+// Copy every rank's whole own list into this CTA's gathered set at prefix
+// offsets (rank order), F.rank_n[r] entries from rank r: all loads of a
+// thread are in flight together. The cluster barrier at the end is the last
+// access to another CTA's memory.
+template <int DT>
+__device__ void gather_all(Ctx<DT>& c) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x;
+  if (c.alias) {
+    // one CTA per row: the own list is already the gathered set (tags = index)
+    if (tid == 0) F.g_n = min(vld(F.rank_n[0]), c.gcap);
+    __syncthreads();
+    return;
+  }
+  if (tid < 32) {
+    const uint32_t n = tid < static_cast<int>(c.C) ? min(vld(F.rank_n[tid]), c.ocap) : 0u;
+    uint32_t incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(kFull, incl, o);
+      if (tid >= o) incl += t;
+    }
+    if (tid < kMaxCluster) F.rank_off[tid + 1] = incl;
+    if (tid == 0) F.rank_off[0] = 0;
+  }
+  __syncthreads();
+  QRITA_T(8);
+  const uint32_t total = min(vld(F.rank_off[c.C]), c.gcap);
+  const uint32_t val_base = smem_u32(c.own_val);
+  const uint32_t idx_base = smem_u32(c.own_idx);
+  constexpr int U = 4;
+  for (uint32_t base = 0; base < total; base += kThreads * U) {
+    float v[U];
+    uint32_t ix[U], rr[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t i = base + u * kThreads + tid;
+      v[u] = 0.f;
+      ix[u] = 0u;
+      rr[u] = 0u;
+      if (i < total) {
+        uint32_t r = 0;
+        for (uint32_t k = 1; k < c.C; ++k) r += (i >= vld(F.rank_off[k])) ? 1u : 0u;
+        const uint32_t j = i - vld(F.rank_off[r]);
+        v[u] = ld_dsmem_f32(map_rank(val_base, r) + 4u * j);
+        ix[u] = ld_dsmem_u32(map_rank(idx_base, r) + 4u * j);
+        rr[u] = r;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const uint32_t i = base + u * kThreads + tid;
+      if (i < total) {
+        c.g_val[i] = v[u];
+        c.g_tag[i] = (rr[u] << kTagShift) | ix[u];
+      }
+    }
+  }
+  if (tid == 0) F.g_n = total;
+  QRITA_T(9);
+  cluster_sync_all();
+  QRITA_T(10);
+}
+
+// After an extraction of a range into the own lists: exchange the list
+// lengths and, when every list and their sum fit, gather them whole.
+// Returns whether it gathered (uniform over the cluster).
+template <int DT>
+__device__ bool gather_extracted(Ctx<DT>& c) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31;
+  cluster_sync_all();  // every rank's list is complete
+  if (tid < 32) {
+    uint32_t n = 0;
+    if (lane < static_cast<int>(c.C)) {
+      n = ld_dsmem_u32(map_rank(smem_u32(&F.own_n), lane));
+      F.rank_n[lane] = n;
+    }
+    uint32_t tot = __reduce_add_sync(kFull, n);
+    const uint32_t mx = __reduce_max_sync(kFull, n);
+    if (lane == 0) F.bc.u[BU_FITS] = (tot <= c.gcap && mx <= c.ocap) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (vld(F.bc.u[BU_FITS]) == 0u) return false;
+  gather_all<DT>(c);
+  return true;
+}
+
 // ---------------------------------------------------------------------------
 // Local quaternary search over the gathered set (block barriers only)
 // ---------------------------------------------------------------------------
 struct Local {
-  uint32_t lo, hi, c_lo, c_hi;  // row counts above lo / hi
-  double m_lo, m_hi;            // row masses above lo / hi (mass search)
-  uint32_t c_above;             // row count above the gathered range
-  double m_above;               // row mass above the gathered range
+  uint32_t lo, hi, c_lo, c_hi;   // row counts above lo / hi
+  unsigned long long m_lo, m_hi;  // row masses above lo / hi (fixed point, mass search)
+  uint32_t c_above;               // row count above the gathered range
+  unsigned long long m_above;     // row mass above the gathered range (fixed point)
   // result
   uint32_t tau, n_keep, count_above;
   int rounds;
   bool capped;
 };
 
+// Copies of a boundary value of fixed-point weight w needed when `need`
+// mass is missing above it: ceil(need / w), clamped to [1, n].
+__device__ __forceinline__ uint32_t copies_fx(unsigned long long need, unsigned long long w, uint32_t n) {
+  unsigned long long k = w > 0ull ? (need + w - 1ull) / w : 1ull;
+  k = k < 1ull ? 1ull : (k > n ? static_cast<unsigned long long>(n) : k);
+  return static_cast<uint32_t>(k);
+}
+
+// Fixed-point softmax weight: round(exp(x - m) * scale). Every place that
+// weighs a value uses this one function, so sums and boundary weights agree.
+__device__ __forceinline__ unsigned long long weight_fx(float x, float m, bool m_neginf, float scale) {
+  return __float2ull_rn(weight(x, m, m_neginf) * scale);
+}
+
+// Sum of a 64-bit value over the warp with 32-bit reductions: split into
+// 21-bit parts, so no part's sum can wrap (values below 2^63).
+__device__ __forceinline__ unsigned long long warp_sum_u64_redux(unsigned long long v) {
+  const uint32_t p0 = static_cast<uint32_t>(v & 0x1FFFFFull);
+  const uint32_t p1 = static_cast<uint32_t>((v >> 21) & 0x1FFFFFull);
+  const uint32_t p2 = static_cast<uint32_t>(v >> 42);
+  const unsigned long long s0 = __reduce_add_sync(kFull, p0);
+  const unsigned long long s1 = __reduce_add_sync(kFull, p1);
+  const unsigned long long s2 = __reduce_add_sync(kFull, p2);
+  return s0 + (s1 << 21) + (s2 << 42);
+}
+
 // Quaternary search (A6 for counts, A7 for mass) over g_val[0..g_n). The
 // search keeps count/mass(> lo) >= target > count/mass(> hi); each round
 // evaluates three pivots at 25/50/75 % of the range and stops at the first
 // pivot whose z_mn is the boundary (above(q) reaches the target and above(q)
 // minus the N_zmn copies of z_mn does not): tau = z_mn and the number of
-// kept copies follows. Thread 0 takes every decision and broadcasts it.
+// kept copies follows. Masses are exact sums of fixed-point weights, so
+// every decision is integer arithmetic; warp 0 takes it and broadcasts it.
+// target is the count (A6) or the fixed-point mass (A7) to reach.
 template <int DT, bool MASS>
-__device__ void local_search(Ctx<DT>& c, Local& s, double target, bool value_pivots) {
+__device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots,
+                             const uint32_t* first_pivots) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t gn = min(vld(F.g_n), c.gcap);
+  const float scale = c.fix_scale;
+  // state in F.bc, written by thread 0
   if (tid == 0) {
     F.bc.u[BU_LO] = s.lo;
     F.bc.u[BU_HI] = s.hi;
     F.bc.u[BU_CLO] = s.c_lo;
     F.bc.u[BU_CHI] = s.c_hi;
-    F.bc.d[BD_MLO] = s.m_lo;
-    F.bc.d[BD_MHI] = s.m_hi;
+    F.bc.x[BX_MLO] = s.m_lo;
+    F.bc.x[BX_MHI] = s.m_hi;
     F.bc.u[BU_DONE] = 0;
     F.bc.u[BU_VMODE] = value_pivots ? 1u : 0u;
-  }
-  int rounds = 0;
-  for (;;) {
-    // thread 0: stop when (lo, hi] holds one key, else pick the pivots
-    if (tid == 0) {
-      const uint32_t lo = F.bc.u[BU_LO], hi = F.bc.u[BU_HI];
-      if (hi - lo <= 1u) {
-        const uint32_t c_hi = F.bc.u[BU_CHI], c_lo = F.bc.u[BU_CLO];
-        const uint32_t N = c_lo - c_hi;
-        F.bc.u[BU_TAU] = hi;
-        F.bc.u[BU_CABOVE] = c_hi;
-        if (MASS) {
-          const double wz = weight(key2f(hi), c.m, c.m_neginf);
-          double nk = ceil((target - F.bc.d[BD_MHI]) / wz);
-          nk = fmin(fmax(nk, 1.0), static_cast<double>(N));
-          F.bc.u[BU_NKEEP] = static_cast<uint32_t>(nk);
-        } else {
-          F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - c_hi;
-        }
-        F.bc.u[BU_DONE] = 1;
-      } else if (rounds >= kMaxRounds) {
-        F.bc.u[BU_DONE] = 2;
-      } else {
-        uint32_t q[3];
-        bool used_value = false;
-        const int np = quartile_pivots(lo, hi, F.bc.u[BU_VMODE] != 0u, q, &used_value);
-        for (int j = 0; j < 3; ++j) {
-          F.bc.q[j] = (j < np) ? q[j] : hi;
-          F.bc.qf[j] = (j < np) ? pivot_f(q[j]) : INFINITY;
-        }
-        F.bc.u[BU_NP] = static_cast<uint32_t>(np);
-        F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
-      }
+    // first pivots: given (the model's guess), or quartiles of the range
+    uint32_t q0, q1, q2;
+    bool used_value = false;
+    int np;
+    if (first_pivots != nullptr && s.lo < first_pivots[0] && first_pivots[0] < first_pivots[1] &&
+        first_pivots[1] < first_pivots[2] && first_pivots[2] < s.hi) {
+      q0 = first_pivots[0];
+      q1 = first_pivots[1];
+      q2 = first_pivots[2];
+      np = 3;
+    } else {
+      np = quartile_pivots(s.lo, s.hi, value_pivots, q0, q1, q2, used_value);
     }
-    __syncthreads();
-    const uint32_t done0 = vld(F.bc.u[BU_DONE]);
-    if (done0 != 0u) break;
+    if (np == 0) {
+      // (lo, hi] holds one key already
+      F.bc.u[BU_DONE] = 3;
+    }
+    F.bc.q[0] = q0;
+    F.bc.q[1] = q1;
+    F.bc.q[2] = q2;
+    F.bc.qf[0] = np > 0 ? pivot_f(q0) : INFINITY;
+    F.bc.qf[1] = np > 1 ? pivot_f(q1) : INFINITY;
+    F.bc.qf[2] = np > 2 ? pivot_f(q2) : INFINITY;
+    F.bc.u[BU_NP] = static_cast<uint32_t>(np);
+    F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
+  }
+  __syncthreads();
+  int rounds = 0;
+  while (vld(F.bc.u[BU_DONE]) == 0u) {
     float qf[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) qf[j] = vld(F.bc.qf[j]);
-    PAcc acc[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) pacc_init(acc[j]);
+    uint32_t cnt[3] = {0u, 0u, 0u}, zk[3] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu}, nz[3] = {0u, 0u, 0u};
+    unsigned long long ms[3] = {0ull, 0ull, 0ull};
     for (uint32_t i = tid; i < gn; i += kThreads) {
       const float x = c.g_val[i];
-      const float w = MASS ? weight(x, c.m, c.m_neginf) : 0.f;
-      pacc_update<MASS>(acc, qf, x, w);
+      const uint32_t key = f2key(x);
+      const unsigned long long wf = MASS ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        const bool g = x > qf[j];
+        cnt[j] += g ? 1u : 0u;
+        if (MASS) ms[j] += g ? wf : 0ull;
+        const bool lt = g && key < zk[j];
+        nz[j] = lt ? 1u : nz[j] + ((g && key == zk[j]) ? 1u : 0u);
+        zk[j] = lt ? key : zk[j];
+      }
     }
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const PAcc t = pacc_shfl_xor<MASS>(acc[j], o);
-        pacc_combine<MASS>(acc[j], t);
-      }
+      const uint32_t cw = __reduce_add_sync(kFull, cnt[j]);
+      const uint32_t zw = __reduce_min_sync(kFull, zk[j]);
+      const uint32_t nw = __reduce_add_sync(kFull, zk[j] == zw ? nz[j] : 0u);
+      const unsigned long long mw = MASS ? warp_sum_u64_redux(ms[j]) : 0ull;
       if (lane == 0) {
-        F.red[warp][j].cnt = acc[j].cnt;
-        F.red[warp][j].z = acc[j].z;
-        F.red[warp][j].nz = acc[j].nz;
-        F.red[warp][j].mhi = acc[j].m.hi;
-        F.red[warp][j].mlo = acc[j].m.lo;
+        F.lred[warp][j].cnt = cw;
+        F.lred[warp][j].zmin = zw;
+        F.lred[warp][j].nz = nw;
+        F.lred[warp][j].mass = mw;
       }
     }
     __syncthreads();
     ++rounds;
     if (warp == 0) {
-      PAcc tot[3];
+      // lanes 0..7 hold the warps' partials; reduce each pivot over them
+      uint32_t tc[3], tz[3], tn[3];
+      unsigned long long tm[3];
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
-        PAcc a;
-        pacc_init(a);
-        if (lane < kWarps) {
-          a.cnt = vld(F.red[lane][j].cnt);
-          a.z = vld(F.red[lane][j].z);
-          a.nz = vld(F.red[lane][j].nz);
-          a.m.hi = vld(F.red[lane][j].mhi);
-          a.m.lo = vld(F.red[lane][j].mlo);
-        }
-#pragma unroll
-        for (int o = kWarps / 2; o > 0; o >>= 1) {
-          const PAcc t = pacc_shfl_xor<MASS>(a, o);
-          pacc_combine<MASS>(a, t);
-        }
-        tot[j] = a;
+        const bool own = lane < kWarps;
+        const uint32_t cw = own ? vld(F.lred[lane][j].cnt) : 0u;
+        const uint32_t zw = own ? vld(F.lred[lane][j].zmin) : 0xFFFFFFFFu;
+        const uint32_t nw = own ? vld(F.lred[lane][j].nz) : 0u;
+        const unsigned long long mw = own ? vld(F.lred[lane][j].mass) : 0ull;
+        tc[j] = __reduce_add_sync(kFull, cw);
+        tz[j] = __reduce_min_sync(kFull, zw);
+        tn[j] = __reduce_add_sync(kFull, zw == tz[j] ? nw : 0u);
+        tm[j] = MASS ? warp_sum_u64_redux(mw) : 0ull;
       }
       if (lane == 0) {
         const int np = static_cast<int>(F.bc.u[BU_NP]);
-        int done_j = -1, lo_j = -1, hi_j = -1;
-        double above_j[3] = {0.0, 0.0, 0.0};
-        for (int j = 0; j < np; ++j) {
-          const double above = MASS ? (f2_value(tot[j].m) + s.m_above)
-                                    : static_cast<double>(tot[j].cnt + s.c_above);
-          above_j[j] = above;
-          if (above >= target) {
-            const double wz = MASS ? static_cast<double>(weight(tot[j].z, c.m, c.m_neginf)) : 1.0;
-            const double below_z = above - static_cast<double>(tot[j].nz) * wz;
-            if (below_z < target) {
-              done_j = j;
-              break;
-            }
-            lo_j = j;
-          } else {
-            hi_j = j;
-            break;
-          }
+        bool reach[3], stop[3];
+        unsigned long long above[3], below[3], wz[3];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          const uint32_t ac = tc[j] + s.c_above;
+          above[j] = MASS ? tm[j] + s.m_above : static_cast<unsigned long long>(ac);
+          wz[j] = MASS ? weight_fx(key2f(tz[j]), c.m, c.m_neginf, scale) : 1ull;
+          below[j] = above[j] - static_cast<unsigned long long>(tn[j]) * wz[j];
+          reach[j] = j < np && above[j] >= target;
+          stop[j] = reach[j] && below[j] < target;
         }
+        const int done_j = stop[0] ? 0 : (reach[0] ? (stop[1] ? 1 : (reach[1] ? (stop[2] ? 2 : -1) : -1)) : -1);
+        const int lo_j = !reach[0] ? -1 : (!reach[1] || np < 2 ? 0 : (!reach[2] || np < 3 ? 1 : 2));
+        const int hi_j = !reach[0] ? 0 : (np < 2 ? -1 : (!reach[1] ? 1 : (np < 3 ? -1 : (!reach[2] ? 2 : -1))));
         if (done_j >= 0) {
-          const PAcc& t = tot[done_j];
-          const uint32_t cnt_above = t.cnt + s.c_above - t.nz;
-          F.bc.u[BU_TAU] = f2key(t.z);
-          F.bc.u[BU_CABOVE] = cnt_above;
+          const uint32_t z = done_j == 0 ? tz[0] : (done_j == 1 ? tz[1] : tz[2]);
+          const uint32_t n = done_j == 0 ? tn[0] : (done_j == 1 ? tn[1] : tn[2]);
+          const uint32_t cabove = (done_j == 0 ? tc[0] : (done_j == 1 ? tc[1] : tc[2])) + s.c_above - n;
+          F.bc.u[BU_TAU] = z;
+          F.bc.u[BU_CABOVE] = cabove;
           if (MASS) {
-            const double wz = weight(t.z, c.m, c.m_neginf);
-            double nk = ceil((target - (above_j[done_j] - static_cast<double>(t.nz) * wz)) / wz);
-            nk = fmin(fmax(nk, 1.0), static_cast<double>(t.nz));
-            F.bc.u[BU_NKEEP] = static_cast<uint32_t>(nk);
+            const unsigned long long w = done_j == 0 ? wz[0] : (done_j == 1 ? wz[1] : wz[2]);
+            const unsigned long long b = done_j == 0 ? below[0] : (done_j == 1 ? below[1] : below[2]);
+            unsigned long long k = w > 0ull ? (target - b + w - 1ull) / w : 1ull;
+            k = k < 1ull ? 1ull : (k > n ? n : k);
+            F.bc.u[BU_NKEEP] = static_cast<uint32_t>(k);
           } else {
-            F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - cnt_above;
+            F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - cabove;
           }
           F.bc.u[BU_DONE] = 1;
         } else {
           const uint32_t old_span = F.bc.u[BU_HI] - F.bc.u[BU_LO];
           if (lo_j >= 0) {
             F.bc.u[BU_LO] = F.bc.q[lo_j];
-            F.bc.u[BU_CLO] = tot[lo_j].cnt + s.c_above;
-            F.bc.d[BD_MLO] = above_j[lo_j];
+            F.bc.u[BU_CLO] = (lo_j == 0 ? tc[0] : (lo_j == 1 ? tc[1] : tc[2])) + s.c_above;
+            F.bc.x[BX_MLO] = lo_j == 0 ? above[0] : (lo_j == 1 ? above[1] : above[2]);
           }
           if (hi_j >= 0) {
             F.bc.u[BU_HI] = F.bc.q[hi_j];
-            F.bc.u[BU_CHI] = tot[hi_j].cnt + s.c_above;
-            F.bc.d[BD_MHI] = above_j[hi_j];
+            F.bc.u[BU_CHI] = (hi_j == 0 ? tc[0] : (hi_j == 1 ? tc[1] : tc[2])) + s.c_above;
+            F.bc.x[BX_MHI] = hi_j == 0 ? above[0] : (hi_j == 1 ? above[1] : above[2]);
           }
+          const uint32_t lo = F.bc.u[BU_LO], hi = F.bc.u[BU_HI];
           // after a value-space split that failed to halve the key range,
           // the next round splits the key range
-          const uint32_t new_span = F.bc.u[BU_HI] - F.bc.u[BU_LO];
-          const bool bad = F.bc.u[BU_USED_VALUE] != 0u && new_span > old_span / 2u;
-          F.bc.u[BU_VMODE] = (value_pivots && !bad) ? 1u : 0u;
+          const bool bad = F.bc.u[BU_USED_VALUE] != 0u && (hi - lo) > old_span / 2u;
+          const bool vmode = value_pivots && !bad;
+          if (hi - lo <= 1u) {
+            // (lo, hi] holds one key: the boundary value is hi
+            const uint32_t c_hi = F.bc.u[BU_CHI], c_lo = F.bc.u[BU_CLO];
+            F.bc.u[BU_TAU] = hi;
+            F.bc.u[BU_CABOVE] = c_hi;
+            if (MASS) {
+              const unsigned long long w = weight_fx(key2f(hi), c.m, c.m_neginf, scale);
+              const unsigned long long m_hi = F.bc.x[BX_MHI];
+              unsigned long long k = w > 0ull ? (target - m_hi + w - 1ull) / w : 1ull;
+              const unsigned long long n = c_lo - c_hi;
+              k = k < 1ull ? 1ull : (k > n ? n : k);
+              F.bc.u[BU_NKEEP] = static_cast<uint32_t>(k);
+            } else {
+              F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - c_hi;
+            }
+            F.bc.u[BU_DONE] = 1;
+          } else if (rounds >= kMaxRounds) {
+            F.bc.u[BU_DONE] = 2;
+          } else {
+            uint32_t q0, q1, q2;
+            bool used_value = false;
+            const int np2 = quartile_pivots(lo, hi, vmode, q0, q1, q2, used_value);
+            F.bc.q[0] = q0;
+            F.bc.q[1] = q1;
+            F.bc.q[2] = q2;
+            F.bc.qf[0] = np2 > 0 ? pivot_f(q0) : INFINITY;
+            F.bc.qf[1] = np2 > 1 ? pivot_f(q1) : INFINITY;
+            F.bc.qf[2] = np2 > 2 ? pivot_f(q2) : INFINITY;
+            F.bc.u[BU_NP] = static_cast<uint32_t>(np2);
+            F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
+          }
         }
       }
     }
     __syncthreads();
-    if (vld(F.bc.u[BU_DONE]) != 0u) break;
   }
+  if (tid == 0 && F.bc.u[BU_DONE] == 3u) {
+    // the start range held one key
+    const uint32_t hi = F.bc.u[BU_HI], c_hi = F.bc.u[BU_CHI], c_lo = F.bc.u[BU_CLO];
+    F.bc.u[BU_TAU] = hi;
+    F.bc.u[BU_CABOVE] = c_hi;
+    if (MASS) {
+      const unsigned long long w = weight_fx(key2f(hi), c.m, c.m_neginf, scale);
+      unsigned long long k = w > 0ull ? (target - F.bc.x[BX_MHI] + w - 1ull) / w : 1ull;
+      const unsigned long long n = c_lo - c_hi;
+      k = k < 1ull ? 1ull : (k > n ? n : k);
+      F.bc.u[BU_NKEEP] = static_cast<uint32_t>(k);
+    } else {
+      F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - c_hi;
+    }
+  }
+  __syncthreads();
+  QRITA_T(14);
   s.tau = vld(F.bc.u[BU_TAU]);
   s.n_keep = vld(F.bc.u[BU_NKEEP]);
   s.count_above = vld(F.bc.u[BU_CABOVE]);
@@ -989,7 +1240,7 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_constant__ Params P) {
   constexpr int E = Ctx<DT>::E;
   constexpr int S = Ctx<DT>::S;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -1000,10 +1251,17 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
   c.F = &F;
   c.ocap = static_cast<uint32_t>(P.ocap);
   c.gcap = static_cast<uint32_t>(P.gcap);
-  c.own_val = reinterpret_cast<float*>(smem + sizeof(Fixed));
+  c.lists = smem + sizeof(Fixed);
+  c.alias = P.C == 1;
+  c.own_val = reinterpret_cast<float*>(c.lists);
   c.own_idx = reinterpret_cast<uint32_t*>(c.own_val + P.ocap);
-  c.g_val = reinterpret_cast<float*>(c.own_idx + P.ocap);
-  c.g_tag = reinterpret_cast<uint32_t*>(c.g_val + P.gcap);
+  if (c.alias) {
+    c.g_val = c.own_val;
+    c.g_tag = c.own_idx;
+  } else {
+    c.g_val = reinterpret_cast<float*>(c.own_idx + P.ocap);
+    c.g_tag = reinterpret_cast<uint32_t*>(c.g_val + P.gcap);
+  }
   c.C = static_cast<uint32_t>(P.C);
   c.crank = cluster_rank();
   c.ph = 0;
@@ -1028,6 +1286,10 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
     c.tail_n = c.n - c.head_n - c.body_units * E;
   }
   c.gbody = c.gx + c.head_n * S;
+  QRITA_T(0);
+#ifdef QRITA_TRACE_TIME
+  if (tid == 0 && blockIdx.x < 65536) g_cta_times[blockIdx.x][0] = globaltimer_ns();
+#endif
 
   // ---- row parameters (uniform)
   int32_t kr = P.k ? P.k[r] : 0;
@@ -1062,7 +1324,7 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
         if (isfinite(x)) {
           sn += 1.f;
           sx += x;
-          sxx += x * x;
+          sxx = fmaf(x, x, sxx);
           smax = fmaxf(smax, x);
         }
       }
@@ -1088,10 +1350,10 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
         d += vld(F.redf[w][2]);
         mx = fmaxf(mx, vld(F.redf[w][3]));
       }
-      const double mean = a > 0.f ? static_cast<double>(b) / a : 0.0;
-      const double var = a > 0.f ? fmax(static_cast<double>(d) / a - mean * mean, 0.0) : 0.0;
-      const float mu = static_cast<float>(mean);
-      const float sigma = static_cast<float>(sqrt(var));
+      const float mean = a > 0.f ? b / a : 0.f;
+      const float var = a > 0.f ? fmaxf(d / a - mean * mean, 0.f) : 0.f;
+      const float mu = mean;
+      const float sigma = sqrtf(var);
       F.bc.f[BF_MU] = mu;
       F.bc.f[BF_SIGMA] = sigma;
       F.bc.f[BF_MREF] = a > 0.f ? mx : 0.f;
@@ -1128,46 +1390,72 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
   const float m_ref = vld(F.bc.f[BF_MREF]);
   const float t = vld(F.bc.f[BF_T]);
   const bool trunc = vld(F.bc.u[BU_TRUNC]) != 0u;
+  QRITA_T(1);
 
   // ---- A4: the streaming pass (the one HBM read of the row)
   {
     float vmax = -INFINITY, vmin = INFINITY, smin = INFINITY;
     uint32_t smin_n = 0;
     F2 zs = {0.f, 0.f}, ms = {0.f, 0.f};
-    auto elem = [&](float x) -> bool {
-      vmax = fmax_nan(vmax, x);
-      vmin = fminf(vmin, x);
-      const bool surv = trunc && x >= t;
-      if (surv) {
-        if (x < smin) {
-          smin = x;
-          smin_n = 1;
-        } else if (x == smin) {
-          ++smin_n;
-        }
-      }
-      if (p_only) {
-        const float w = expf(x - m_ref);
-        f2_add(zs, w);
-        f2_add(ms, surv ? w : 0.f);
-      }
-      return surv;
-    };
     stream_chunk<DT>(
         c,
         [&](const float (&xs)[E], uint32_t idx0, bool valid) {
           uint32_t bits = 0;
           if (valid) {
+            float zu = 0.f, mu_ = 0.f;  // this unit's softmax partials (shift m_ref)
 #pragma unroll
-            for (int e = 0; e < E; ++e) bits |= elem(xs[e]) ? (1u << e) : 0u;
+            for (int e = 0; e < E; ++e) {
+              const float x = xs[e];
+              vmax = fmax_nan(vmax, x);
+              vmin = fminf(vmin, x);
+              const bool surv = trunc && x >= t;
+              bits |= surv ? (1u << e) : 0u;
+              if (k_on && surv) {
+                if (x < smin) {
+                  smin = x;
+                  smin_n = 1;
+                } else if (x == smin) {
+                  ++smin_n;
+                }
+              }
+              if (p_only) {
+                const float w = expf(x - m_ref);
+                zu += w;
+                mu_ += surv ? w : 0.f;
+              }
+            }
+            if (p_only) {
+              f2_add(zs, zu);
+              f2_add(ms, mu_);
+            }
           }
           if (trunc) warp_append<E>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx0, bits);
         },
         [&](float x, uint32_t idx, bool valid) {
-          const uint32_t bits = (valid && elem(x)) ? 1u : 0u;
+          uint32_t bits = 0;
+          if (valid) {
+            vmax = fmax_nan(vmax, x);
+            vmin = fminf(vmin, x);
+            const bool surv = trunc && x >= t;
+            bits = surv ? 1u : 0u;
+            if (k_on && surv) {
+              if (x < smin) {
+                smin = x;
+                smin_n = 1;
+              } else if (x == smin) {
+                ++smin_n;
+              }
+            }
+            if (p_only) {
+              const float w = expf(x - m_ref);
+              f2_add(zs, w);
+              f2_add(ms, surv ? w : 0.f);
+            }
+          }
           const float xs[1] = {x};
           if (trunc) warp_append<1>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx, bits);
         });
+    QRITA_T(2);
     // block reduce
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -1182,11 +1470,8 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
         smin_n += n2;
       }
       if (p_only) {
-        F2 a, b;
-        a.hi = __shfl_xor_sync(kFull, zs.hi, o);
-        a.lo = __shfl_xor_sync(kFull, zs.lo, o);
-        b.hi = __shfl_xor_sync(kFull, ms.hi, o);
-        b.lo = __shfl_xor_sync(kFull, ms.lo, o);
+        const F2 a = f2_make(__shfl_xor_sync(kFull, zs.hi, o), __shfl_xor_sync(kFull, zs.lo, o));
+        const F2 b = f2_make(__shfl_xor_sync(kFull, ms.hi, o), __shfl_xor_sync(kFull, ms.lo, o));
         zs = f2_merge(zs, a);
         ms = f2_merge(ms, b);
       }
@@ -1204,7 +1489,7 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
     __syncthreads();
     Slot& my = F.slots[c.ph & 1];
     if (tid == 0) {
-      float a = -INFINITY, b = INFINITY, s = INFINITY;
+      float a = -INFINITY, b = INFINITY, sm = INFINITY;
       uint32_t sn = 0;
       F2 z = {0.f, 0.f}, mm = {0.f, 0.f};
       for (int w = 0; w < kWarps; ++w) {
@@ -1212,41 +1497,41 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
         b = fminf(b, vld(F.redf[w][1]));
         const float s2 = vld(F.redf[w][2]);
         const uint32_t n2 = vld(F.redu[w][0]);
-        if (s2 < s) {
-          s = s2;
+        if (s2 < sm) {
+          sm = s2;
           sn = n2;
-        } else if (s2 == s) {
+        } else if (s2 == sm) {
           sn += n2;
         }
-        const F2 za = {vld(F.redf[w][3]), vld(F.redf[w][4])};
-        const F2 ma = {vld(F.redf[w][5]), vld(F.redf[w][6])};
-        z = f2_merge(z, za);
-        mm = f2_merge(mm, ma);
+        z = f2_merge(z, f2_make(vld(F.redf[w][3]), vld(F.redf[w][4])));
+        mm = f2_merge(mm, f2_make(vld(F.redf[w][5]), vld(F.redf[w][6])));
       }
       my.f[0] = a;
       my.f[1] = b;
-      my.f[2] = s;
+      my.f[2] = sm;
       my.u[0] = sn;
       my.u[1] = vld(F.own_n);
-      my.d[0] = f2_value(z);
-      my.d[1] = f2_value(mm);
+      my.pr[0] = z.hi;
+      my.pr[1] = z.lo;
+      my.pr[2] = mm.hi;
+      my.pr[3] = mm.lo;
     }
     cluster_sync_all();
     if (warp == 0) {
-      float a = -INFINITY, b = INFINITY, s = INFINITY;
+      float a = -INFINITY, b = INFINITY, sm = INFINITY;
       uint32_t sn = 0, surv = 0, ovf = 0;
-      double z = 0.0, mm = 0.0;
+      F2 z = {0.f, 0.f}, mm = {0.f, 0.f};
       if (lane < static_cast<int>(c.C)) {
         const uint32_t fb = map_rank(smem_u32(&my.f[0]), lane);
         a = ld_dsmem_f32(fb);
         b = ld_dsmem_f32(fb + 4);
-        s = ld_dsmem_f32(fb + 8);
+        sm = ld_dsmem_f32(fb + 8);
         const uint32_t ub = map_rank(smem_u32(&my.u[0]), lane);
         sn = ld_dsmem_u32(ub);
         surv = ld_dsmem_u32(ub + 4);
-        const uint32_t db = map_rank(smem_u32(&my.d[0]), lane);
-        z = ld_dsmem_f64(db);
-        mm = ld_dsmem_f64(db + 8);
+        const uint32_t pb = map_rank(smem_u32(&my.pr[0]), lane);
+        z = f2_make(ld_dsmem_f32(pb), ld_dsmem_f32(pb + 4));
+        mm = f2_make(ld_dsmem_f32(pb + 8), ld_dsmem_f32(pb + 12));
         ovf = surv > c.ocap ? 1u : 0u;
         F.rank_n[lane] = surv;
       }
@@ -1254,33 +1539,34 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
       for (int o = 8; o > 0; o >>= 1) {
         a = fmax_nan(a, __shfl_xor_sync(kFull, a, o));
         b = fminf(b, __shfl_xor_sync(kFull, b, o));
-        const float s2 = __shfl_xor_sync(kFull, s, o);
+        const float s2 = __shfl_xor_sync(kFull, sm, o);
         const uint32_t n2 = __shfl_xor_sync(kFull, sn, o);
-        if (s2 < s) {
-          s = s2;
+        if (s2 < sm) {
+          sm = s2;
           sn = n2;
-        } else if (s2 == s) {
+        } else if (s2 == sm) {
           sn += n2;
         }
         surv += __shfl_xor_sync(kFull, surv, o);
         ovf |= __shfl_xor_sync(kFull, ovf, o);
-        z += __shfl_xor_sync(kFull, z, o);
-        mm += __shfl_xor_sync(kFull, mm, o);
+        z = f2_merge(z, f2_make(__shfl_xor_sync(kFull, z.hi, o), __shfl_xor_sync(kFull, z.lo, o)));
+        mm = f2_merge(mm, f2_make(__shfl_xor_sync(kFull, mm.hi, o), __shfl_xor_sync(kFull, mm.lo, o)));
       }
       if (lane == 0) {
         F.bc.f[BF_MAX] = a;
         F.bc.f[BF_MIN] = b;
-        F.bc.f[BF_SMIN] = s;
+        F.bc.f[BF_SMIN] = sm;
         F.bc.u[BU_SMIN_N] = sn;
         F.bc.u[BU_S] = surv;
         F.bc.u[BU_OVF] = ovf;
-        F.bc.d[BD_ZR] = z;
-        F.bc.d[BD_MR] = mm;
+        put_pair(F.bc, BP_ZR, z);
+        put_pair(F.bc, BP_MR, mm);
       }
     }
     __syncthreads();
     ++c.ph;
   }
+  QRITA_T(3);
   const float row_max = vld(F.bc.f[BF_MAX]);
   const float row_min = vld(F.bc.f[BF_MIN]);
   const float surv_min = vld(F.bc.f[BF_SMIN]);
@@ -1288,12 +1574,13 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
   const uint32_t survivors = vld(F.bc.u[BU_S]);
   const bool overflow = vld(F.bc.u[BU_OVF]) != 0u;
   const bool invalid = isnan(row_max) || row_max == INFINITY;
-  const double Zr = vld(F.bc.d[BD_ZR]);
-  const double Mr = vld(F.bc.d[BD_MR]);
+  const F2 Zr = get_pair(F.bc, BP_ZR);
+  const F2 Mr = get_pair(F.bc, BP_MR);
   c.m = row_max;
   c.m_neginf = (row_max == -INFINITY);
   // weights exp(x - m) lie in [0, 1]: fixed point with headroom for V terms
   c.fix_scale = exp2f(static_cast<float>(62 - (32 - __clz(static_cast<uint32_t>(V)))));
+  const float inv_scale = 1.0f / c.fix_scale;  // a power of two: exact
 
   uint32_t path = (k_on ? QRITA_PATH_TOPK : 0u) | (p_on ? QRITA_PATH_TOPP : 0u) |
                   (trunc ? QRITA_PATH_TRUNC : 0u) | (overflow ? QRITA_PATH_OVERFLOW : 0u) |
@@ -1306,7 +1593,7 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
   uint32_t tau = 0, n_keep = 0, count_above = 0;
   uint32_t rounds_k = 0, rounds_p = 0, passes = 0;
   uint32_t row_status = invalid ? QRITA_ROW_NONFINITE : QRITA_ROW_OK;
-  double z_used = 0.0;
+  unsigned long long z_used = 0ull;  // softmax denominator top-p used (fixed point)
   bool sel_all = keep_all && !invalid;
   bool sel_none = invalid;
   bool remote_done = false;   // the last access to another CTA's memory is behind a barrier
@@ -1315,27 +1602,26 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
   bool ties_known = false;    // F.ties holds the per-rank tie counts
 
   if (!invalid && !keep_all) {
-    const double pd = static_cast<double>(pr);
-    // the streaming pass summed exp(x - m_ref); shift m is exp(m_ref - m) away
-    const bool ref_ok = !c.m_neginf && isfinite(Zr) && isfinite(Mr) && Zr > 0.0 &&
-                        static_cast<double>(row_max) - m_ref < 80.0;
-    const double cf = ref_ok ? exp(static_cast<double>(m_ref) - row_max) : 0.0;
-    const double Zm = Zr * cf, Mm = Mr * cf;
+    // the streaming pass summed exp(x - m_ref); shift m is a factor exp(m_ref - m) away
+    const bool ref_ok = !c.m_neginf && isfinite(Zr.hi) && isfinite(Mr.hi) && Zr.hi > 0.f &&
+                        row_max - m_ref < 80.0f;
+    const float cf = ref_ok ? expf(m_ref - row_max) : 0.f;
+    const F2 Zm = f2_mul(Zr, cf), Mm = f2_mul(Mr, cf);
 
     bool k_full = false;  // the gathered set holds the whole top-k set S_k
     uint32_t tau_k = 0, nk_k = 0, above_k = 0;
     if (k_on) {
-      const double target = static_cast<double>(kr);
-      const bool hit = trunc && !overflow && !force_fb && survivors >= static_cast<uint32_t>(kr);
+      const uint32_t target = static_cast<uint32_t>(kr);
+      const bool hit = trunc && !overflow && !force_fb && survivors >= target;
       path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
       Local s;
       s.c_above = 0;
-      s.m_above = 0.0;
-      s.m_lo = s.m_hi = 0.0;
+      s.m_above = 0ull;
+      s.m_lo = s.m_hi = 0ull;
       bool have_exact = false;
       if (hit && survivors <= c.gcap) {
         // gather Z_t whole: the candidates are (key(t) - 1, max]
-        gather<DT>(c, -INFINITY, INFINITY, true, false);
+        gather_all<DT>(c);
         remote_done = true;
         s.lo = f2key(t) - 1u;
         s.c_lo = survivors;
@@ -1344,22 +1630,25 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
         k_full = true;
         list_emit = true;
         ties_in_list = true;
-        if (survivors - surv_min_n < static_cast<uint32_t>(kr)) {
+        if (survivors - surv_min_n < target) {
           // z_mn of the initial lo is the smallest survivor: it is the boundary
           s.tau = f2key(surv_min);
           s.count_above = survivors - surv_min_n;
-          s.n_keep = static_cast<uint32_t>(kr) - s.count_above;
+          s.n_keep = target - s.count_above;
           s.rounds = 0;
           s.capped = false;
         } else {
-          local_search<DT, false>(c, s, target, value_pivots);
+          local_search<DT, false>(c, s, target, value_pivots, nullptr);
         }
       } else {
         // narrow: over the survivor lists on a hit, over the chunk otherwise
         Range R;
-        R.pin_hi = p_on && static_cast<uint32_t>(kr) <= c.gcap;
-        R.m_lo = R.m_hi = 0.0;
-        double tg = target;
+        R.pin_hi = false;
+        R.m_lo = R.m_hi = 0ull;
+        R.target = target;
+        R.target_from_total = false;
+        R.p_frac = 0.f;
+        R.extra = 0ull;
         if (hit) {
           R.lo = f2key(t) - 1u;
           R.c_lo = survivors;
@@ -1368,17 +1657,17 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
         } else {
           R.lo = f2key(row_min) - 1u;
           R.c_lo = static_cast<uint32_t>(V);
-          const bool miss_t = trunc && !overflow && survivors < static_cast<uint32_t>(kr);
+          const bool miss_t = trunc && !overflow && survivors < target;
           R.hi = (!R.pin_hi && miss_t) ? f2key(t) - 1u : f2key(row_max);
           R.c_hi = (!R.pin_hi && miss_t) ? survivors : 0u;
         }
         R.lo_all = R.lo < kKeyNegInf;
-        narrow<DT, false>(c, R, tg, 0.0, 0.0, !hit);
+        narrow<DT, false>(c, R, !hit);
         passes += static_cast<uint32_t>(R.passes);
         if (R.exact) {
           s.tau = R.hi;
           s.count_above = R.c_hi;
-          s.n_keep = static_cast<uint32_t>(kr) - R.c_hi;
+          s.n_keep = target - R.c_hi;
           s.rounds = 0;
           s.capped = false;
           have_exact = true;
@@ -1413,10 +1702,10 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
             s.c_hi = R.c_hi;
             s.c_above = R.c_hi;  // elements above hi exceed every pivot
           }
-          k_full = R.pin_hi;
+          k_full = R.c_hi == 0u;  // nothing lies above the gathered range
           list_emit = hit;
           ties_in_list = true;
-          local_search<DT, false>(c, s, target, value_pivots);
+          local_search<DT, false>(c, s, target, value_pivots, nullptr);
         }
       }
       rounds_k = static_cast<uint32_t>(s.rounds);
@@ -1436,48 +1725,57 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
       }
     }
 
+    QRITA_T(4);
+    bool extracted_above_k = false;  // the own lists hold exactly {x > tau_k}
+    if (p_on && k_on && !k_full && !sel_none && above_k <= c.gcap) {
+      // S_k without its boundary copies is {x > tau_k}: extract and gather it
+      Range Rx;
+      Rx.lo = tau_k;
+      Rx.hi = kKeyPosInf;
+      Rx.lo_all = false;
+      Rx.pin_hi = true;
+      extract_range<DT>(c, Rx);
+      if (gather_extracted<DT>(c)) {
+        remote_done = true;
+        k_full = true;
+        extracted_above_k = true;
+      }
+    }
     if (p_on && !sel_none) {
       if (k_on && k_full) {
         // top-p over S_k, all of it gathered: Z_k = mass(> tau_k) + n_keep_k w(tau_k)
         const float tk = key2f(tau_k);
-        F2 acc = {0.f, 0.f};
+        const float scale = c.fix_scale;
+        unsigned long long acc = 0ull;
         const uint32_t gn = min(vld(F.g_n), c.gcap);
         for (uint32_t i = tid; i < gn; i += kThreads) {
           const float x = c.g_val[i];
-          f2_add(acc, x > tk ? weight(x, c.m, c.m_neginf) : 0.f);
+          acc += x > tk ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          F2 b;
-          b.hi = __shfl_xor_sync(kFull, acc.hi, o);
-          b.lo = __shfl_xor_sync(kFull, acc.lo, o);
-          acc = f2_merge(acc, b);
-        }
-        if (lane == 0) {
-          F.redf[warp][0] = acc.hi;
-          F.redf[warp][1] = acc.lo;
-        }
+        acc = warp_sum_u64_redux(acc);
+        if (lane == 0) F.lred[warp][0].mass = acc;
         __syncthreads();
         if (tid == 0) {
-          F2 a = {0.f, 0.f};
-          for (int w = 0; w < kWarps; ++w) {
-            const F2 b = {vld(F.redf[w][0]), vld(F.redf[w][1])};
-            a = f2_merge(a, b);
-          }
-          F.bc.d[BD_TOTAL] = f2_value(a);
+          unsigned long long a = 0ull;
+          for (int w = 0; w < kWarps; ++w) a += vld(F.lred[w][0].mass);
+          F.bc.x[BX_TARGET] = a;
         }
         __syncthreads();
-        const double M_gt = vld(F.bc.d[BD_TOTAL]);
-        const double w_tau = weight(tk, c.m, c.m_neginf);
-        const double Zk = M_gt + static_cast<double>(nk_k) * w_tau;
-        const double target = pd * Zk;
+        const unsigned long long M_gt = vld(F.bc.x[BX_TARGET]);
+        const unsigned long long w_tau = weight_fx(tk, c.m, c.m_neginf, scale);
+        const unsigned long long Zk = M_gt + static_cast<unsigned long long>(nk_k) * w_tau;
+        const unsigned long long target = f2_to_u64(f2_mul(f2_from_u64(Zk), pr));
         z_used = Zk;
+        __syncthreads();
         if (M_gt < target) {
           // the boundary lies in the tau_k tie group: keep fewer of them
-          double nk = ceil((target - M_gt) / w_tau);
-          nk = fmin(fmax(nk, 1.0), static_cast<double>(nk_k));
-          n_keep = static_cast<uint32_t>(nk);
+          n_keep = copies_fx(target - M_gt, w_tau, nk_k);
           count_above = above_k;
+          if (extracted_above_k) {
+            // the lists hold {x > tau_k} only: the tie group is not in them
+            list_emit = false;
+            ties_in_list = false;
+          }
         } else {
           Local s;
           s.lo = tau_k;
@@ -1485,10 +1783,10 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
           s.m_lo = M_gt;
           s.hi = f2key(row_max);
           s.c_hi = 0;
-          s.m_hi = 0.0;
+          s.m_hi = 0ull;
           s.c_above = 0;
-          s.m_above = 0.0;
-          local_search<DT, true>(c, s, target, value_pivots);
+          s.m_above = 0ull;
+          local_search<DT, true>(c, s, target, value_pivots, nullptr);
           rounds_p = static_cast<uint32_t>(s.rounds);
           if (s.capped) {
             sel_none = true;
@@ -1498,41 +1796,48 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
           n_keep = s.n_keep;
           count_above = s.count_above;
           count_ties_gathered<DT>(c, key2f(tau));
+          if (extracted_above_k) {
+            // tau > tau_k: the kept set and the tie group are in the lists
+            list_emit = true;
+            ties_in_list = true;
+          }
         }
       } else {
         // top-p only, or top-p over an S_k too large to gather
-        const bool hit = !k_on && trunc && !overflow && !force_fb && ref_ok && Mm >= pd * Zm * (1.0 + 1e-5);
+        const bool hit = !k_on && trunc && !overflow && !force_fb && ref_ok &&
+                         f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
         if (!k_on) path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
         Local s;
         s.c_above = 0;
-        s.m_above = 0.0;
+        s.m_above = 0ull;
         bool have_exact = false;
-        double target = pd * Zm;
+        const float scale = c.fix_scale;
         if (hit && survivors <= c.gcap) {
-          gather<DT>(c, -INFINITY, INFINITY, true, false);
+          gather_all<DT>(c);
           remote_done = true;
-          z_used = Zm;
+          z_used = f2_to_u64(f2_mul(Zm, scale));
           s.lo = f2key(t) - 1u;
           s.c_lo = survivors;
-          s.m_lo = Mm;
+          s.m_lo = f2_to_u64(f2_mul(Mm, scale));
           s.hi = f2key(row_max);
           s.c_hi = 0;
-          s.m_hi = 0.0;
+          s.m_hi = 0ull;
           list_emit = true;
           ties_in_list = true;
-          local_search<DT, true>(c, s, target, value_pivots);
+          local_search<DT, true>(c, s, f2_to_u64(f2_mul(f2_mul(Zm, pr), scale)), value_pivots, nullptr);
         } else {
           // narrow by mass in fixed point (shift m); a pass over the chunk
           // measures the denominator (Z, or mass(> tau_k) for S_k) itself
           Range R;
           R.pin_hi = false;
-          const float scale = c.fix_scale;
-          double extra = 0.0;
+          R.p_frac = pr;
+          R.extra = 0ull;
+          R.target_from_total = !hit;
+          R.target = hit ? f2_to_u64(f2_mul(f2_mul(Zm, pr), scale)) : 0ull;
           if (k_on) {
             R.lo = tau_k;
             R.c_lo = above_k;
-            extra = static_cast<double>(nk_k) * static_cast<double>(weight(key2f(tau_k), c.m, c.m_neginf)) *
-                    static_cast<double>(scale);
+            R.extra = static_cast<unsigned long long>(nk_k) * weight_fx(key2f(tau_k), c.m, c.m_neginf, scale);
           } else if (hit) {
             R.lo = f2key(t) - 1u;
             R.c_lo = survivors;
@@ -1543,34 +1848,27 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
           R.lo_all = R.lo < kKeyNegInf;
           R.hi = f2key(row_max);
           R.c_hi = 0;
-          R.m_lo = R.m_hi = 0.0;
-          double tg = hit ? pd * Zm * static_cast<double>(scale) : -1.0;
-          narrow<DT, true>(c, R, tg, pd, extra, !hit);
+          R.m_lo = R.m_hi = 0ull;
+          narrow<DT, true>(c, R, !hit);
           passes += static_cast<uint32_t>(R.passes);
-          target = tg / static_cast<double>(scale);
-          z_used = target / pd;
-          // the emission streams the chunk unless a gather below says otherwise
+          const unsigned long long target = R.target;
+          z_used = f2_to_u64(f2_mul(f2_from_u64(target), 1.0f / pr));
+          // the emission streams the chunk unless a gather below says otherwise;
+          // a chunk pass also overwrote the lists
           list_emit = false;
+          if (!hit) ties_in_list = false;
           if (R.below) {
             // only after top-k: mass(> tau_k) < p Z_k, so the boundary lies in
             // the tau_k tie group (whose per-rank counts F.ties still holds)
-            const double M_gt = R.m_lo / scale;
-            const double w_tau = weight(key2f(tau_k), c.m, c.m_neginf);
-            double nk = ceil((target - M_gt) / w_tau);
-            nk = fmin(fmax(nk, 1.0), static_cast<double>(nk_k));
             s.tau = tau_k;
-            s.n_keep = static_cast<uint32_t>(nk);
+            s.n_keep = copies_fx(target - R.m_lo, weight_fx(key2f(tau_k), c.m, c.m_neginf, scale), nk_k);
             s.count_above = above_k;
             s.rounds = 0;
             s.capped = false;
-            have_exact = true;  // ties already known from top-k
+            have_exact = true;
           } else if (R.exact) {
-            const double wz = weight(key2f(R.hi), c.m, c.m_neginf);
-            double nk = ceil((target - R.m_hi / scale) / wz);
-            const uint32_t N = R.c_lo - R.c_hi;
-            nk = fmin(fmax(nk, 1.0), static_cast<double>(N));
             s.tau = R.hi;
-            s.n_keep = static_cast<uint32_t>(nk);
+            s.n_keep = copies_fx(target - R.m_hi, weight_fx(key2f(R.hi), c.m, c.m_neginf, scale), R.c_lo - R.c_hi);
             s.count_above = R.c_hi;
             s.rounds = 0;
             s.capped = false;
@@ -1597,12 +1895,12 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
             s.c_lo = R.c_lo;
             s.c_hi = R.c_hi;
             s.c_above = R.c_hi;
-            s.m_lo = R.m_lo / scale;
-            s.m_hi = R.m_hi / scale;
-            s.m_above = R.m_hi / scale;
+            s.m_lo = R.m_lo;
+            s.m_hi = R.m_hi;
+            s.m_above = R.m_hi;
             list_emit = hit;
             ties_in_list = true;
-            local_search<DT, true>(c, s, target, value_pivots);
+            local_search<DT, true>(c, s, target, value_pivots, nullptr);
           }
         }
         rounds_p = static_cast<uint32_t>(s.rounds);
@@ -1624,6 +1922,7 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
     cluster_sync_all();  // no CTA leaves while another may read its memory
     remote_done = true;
   }
+  QRITA_T(5);
 
   // ---- A8: boundary ties by lowest token id
   const float tau_f = key2f(tau);
@@ -1648,6 +1947,7 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
       ordered_ties = true;
     }
   }
+  QRITA_T(6);
 
   // ---- A9: mask emission
   if (sel_all || sel_none || list_emit) {
@@ -1751,6 +2051,10 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
       }
     }
   }
+  QRITA_T(7);
+#ifdef QRITA_TRACE_TIME
+  if (tid == 0 && blockIdx.x < 65536) g_cta_times[blockIdx.x][1] = globaltimer_ns();
+#endif
 
   // ---- row outputs (rank 0)
   if (c.crank == 0 && tid == 0) {
@@ -1773,7 +2077,7 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
       info.n_boundary = (sel_none || sel_all) ? 0u : n_keep;
       info.kept = kept;
       info.status = row_status;
-      info.z = z_used;
+      info.z = static_cast<double>(z_used) / static_cast<double>(c.fix_scale);
       info.passes = passes;
       info.reserved = 0u;
       P.row_info[r] = info;
@@ -1783,11 +2087,11 @@ __global__ void __launch_bounds__(kThreads, 4) select_kernel(const __grid_consta
 
 }  // namespace
 
-size_t smem_bytes(int ocap, int gcap) {
-  size_t b = sizeof(Fixed);
-  b += static_cast<size_t>(ocap) * 8u;  // own list: value + index
-  b += static_cast<size_t>(gcap) * 8u;  // gathered set: value + tag
-  return (b + 127u) & ~static_cast<size_t>(127u);
+size_t smem_bytes(int C, int ocap, int gcap) {
+  size_t lists = static_cast<size_t>(ocap) * 8u;  // own list: value + index
+  if (C > 1) lists += static_cast<size_t>(gcap) * 8u;  // gathered set: value + tag
+  if (lists < static_cast<size_t>(kMinListBytes)) lists = kMinListBytes;
+  return (sizeof(Fixed) + lists + 127u) & ~static_cast<size_t>(127u);
 }
 
 int max_smem_per_block() {
@@ -1797,6 +2101,17 @@ int max_smem_per_block() {
   cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   return v;
 }
+
+#ifdef QRITA_TRACE_TIME
+extern "C" int qrita_debug_times(unsigned long long* out) {
+  cudaDeviceSynchronize();
+  return static_cast<int>(cudaMemcpyFromSymbol(out, g_times, sizeof(g_times)));
+}
+extern "C" int qrita_debug_cta_times(unsigned long long* out, int n) {
+  cudaDeviceSynchronize();
+  return static_cast<int>(cudaMemcpyFromSymbol(out, g_cta_times, sizeof(unsigned long long) * 2 * n));
+}
+#endif
 
 int launch_select(const Params& prm, int dtype, size_t smem, qrita_stream_t stream) {
   const void* fn = dtype == QRITA_DTYPE_F32 ? reinterpret_cast<const void*>(&select_kernel<QRITA_DTYPE_F32>)
