@@ -67,10 +67,10 @@ constexpr float kMarginP = 0.25f;
 
 // Candidate list capacities (entries of value + index): a CTA's own list and
 // the gathered set every CTA of a row searches; with one CTA per row the two
-// are one list. About 96 KiB either way, two CTAs per SM.
+// are one list. 104 KiB with the streaming ring either way: two CTAs per SM.
 constexpr int kOwnCap = 4096;
-constexpr int kGatherCap = 8192;
-constexpr int kSoleCap = 12288;
+constexpr int kGatherCap = 9216;
+constexpr int kSoleCap = 9216;
 // Resident CTAs per SM the kernel is built for (its register budget).
 constexpr int kCtasPerSm = 2;
 // Rows shorter than this per CTA are not split further.
@@ -141,7 +141,7 @@ int choose_shape(int64_t B, int64_t V, uint32_t flags, Shape* out) {
   const int ocap = C == 1 ? kSoleCap : kOwnCap;
   const int gcap = C == 1 ? kSoleCap : kGatherCap;
   const size_t smem = smem_bytes(C, ocap, gcap);
-  if (smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
+  if (smem == 0 || smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
   out->C = C;
   out->chunk = static_cast<int>(chunk);
   out->ocap = ocap;

@@ -57,11 +57,9 @@ struct Params {
   float lut_p[kLutP];
 };
 
-// Smallest list region (bytes) the kernel accepts: its narrowing bins reuse it.
-constexpr int kMinListBytes = 48 * 1024;
 
 // Bytes of dynamic shared memory the kernel needs for C CTAs per row and the
-// list capacities.
+// list capacities (0: the capacities leave no room for the streaming ring).
 size_t smem_bytes(int C, int ocap, int gcap);
 
 // Launch the selection kernel (grid B*C, cluster C). Returns a cudaError_t.

@@ -48,12 +48,23 @@ constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kSampleBlocks = 16;
 constexpr int kSampleBlock = 64;  // 16 x 64 = 1024 sampled logits per row
+constexpr float kClipSigmas = 4.0f;  // sample values beyond this many sigmas are outliers
+// Streaming ring: the chunk moves through shared memory in pieces of
+// kPieceBytes by 1-D bulk copies (TMA), kStages pieces in flight.
+constexpr int kStages = 4;
+constexpr int kPieceBytes = 8192;
+constexpr int kPieceUnits = kPieceBytes / 16;
+constexpr int kRingBytes = kStages * kPieceBytes;
+static_assert((kStages & (kStages - 1)) == 0, "kStages must be a power of two");
+static_assert(kPieceUnits % kThreads == 0, "a piece is whole rounds of the block");
+// Bound of one wait for a bulk copy (a copy from valid global memory lands in
+// microseconds; the bound only keeps a failing copy from hanging the kernel).
+constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
 constexpr int kBins = kNarrowPivots + 1;
 constexpr int kTagShift = 28;  // gathered tag = rank << 28 | index in chunk
 // A chunk narrowing pass lays per-thread bins (counts, then fixed-point
-// masses) over the list region, which must hold them.
+// masses) over the start of the list region, clear of the streaming ring.
 constexpr int kBinBytes = kBins * kThreads * (4 + 8);
-static_assert(kBinBytes <= kMinListBytes, "the narrowing bins must fit over the lists");
 #ifdef QRITA_TRACE_TIME
 // Debug-only stage timestamps of three CTAs, and start / end of every CTA
 // (built with -DQRITA_TRACE_TIME).
@@ -119,9 +130,6 @@ __device__ __forceinline__ float load_elem(const unsigned char* p) {
   }
 }
 
-__device__ __forceinline__ uint4 ldg16(const unsigned char* p) {
-  return __ldg(reinterpret_cast<const uint4*>(p));
-}
 
 // Read of shared state another thread wrote before a barrier. Every such read
 // goes through a volatile shared load so the compiler can neither reuse an
@@ -189,14 +197,27 @@ struct alignas(16) Fixed {
   uint32_t scan[kWarps];
   uint32_t own_n;
   uint32_t g_n;
+  uint32_t seg_n[kWarps];  // streaming pass: per-warp survivor counts
+  uint32_t seg_ovf;        // a warp's survivors exceeded its segment
+  uint32_t err;       // a bulk-copy wait of this CTA gave up
+  uint32_t err_any;   // some CTA of the row reported err (written remotely)
+  unsigned long long ring_bar[kStages];  // one mbarrier per ring stage
 };
+
+// Bytes of the list region after Fixed: the own list (value + index), then
+// the gathered set (value + tag) when C > 1. The streaming ring occupies the
+// region's last kRingBytes: inside the gathered set when C > 1 (which holds
+// nothing while the chunk streams), after the own list when C == 1.
+__host__ __device__ constexpr size_t list_region_bytes(int C, int ocap, int gcap) {
+  return C > 1 ? static_cast<size_t>(ocap + gcap) * 8u : static_cast<size_t>(ocap) * 8u + kRingBytes;
+}
 
 // Names of the broadcast slots
 enum : int {
   // floats
-  BF_MU = 0, BF_SIGMA, BF_MREF, BF_T, BF_MAX, BF_MIN, BF_SMIN, BF_LOF, BF_HIF,
+  BF_MU = 0, BF_SIGMA, BF_MREF, BF_T, BF_MAX, BF_MIN, BF_LOF, BF_HIF,
   // uints
-  BU_TRUNC = 0, BU_SMIN_N, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
+  BU_TRUNC = 0, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
   BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS,
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
@@ -223,13 +244,6 @@ struct PAcc {
   F2 m;
 };
 
-__device__ __forceinline__ void pacc_init(PAcc& a) {
-  a.cnt = 0;
-  a.z = INFINITY;
-  a.nz = 0;
-  a.m.hi = 0.f;
-  a.m.lo = 0.f;
-}
 
 template <bool MASS>
 __device__ __forceinline__ void pacc_combine(PAcc& a, const PAcc& b) {
@@ -352,6 +366,30 @@ __device__ __forceinline__ void warp_append(uint32_t* counter, float* vals, uint
   }
 }
 
+// Append the set bits' elements to this warp's segment of a list (no atomics):
+// segment `seg` = entries [seg_base, seg_base + segcap); wn is the warp's
+// running count (warp-uniform), which keeps counting past segcap.
+template <int E>
+__device__ __forceinline__ void seg_append(uint32_t& wn, float* vals, uint32_t* idxs, uint32_t seg_base,
+                                           uint32_t segcap, const float (&xs)[E], uint32_t idx0,
+                                           uint32_t bits) {
+  if (__ballot_sync(kFull, bits != 0u) == 0u) return;
+  const uint32_t lt = (1u << (threadIdx.x & 31)) - 1u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    const bool mine = (bits >> e) & 1u;
+    const uint32_t b = __ballot_sync(kFull, mine);
+    if (mine) {
+      const uint32_t pos = wn + __popc(b & lt);
+      if (pos < segcap) {
+        vals[seg_base + pos] = xs[e];
+        idxs[seg_base + pos] = idx0 + e;
+      }
+    }
+    wn += __popc(b);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Pivots: 25/50/75 % of a key range (lo, hi]
 // ---------------------------------------------------------------------------
@@ -424,6 +462,11 @@ __device__ int two_level_pivots(uint32_t lo, uint32_t hi, bool value_ok, volatil
 // ---------------------------------------------------------------------------
 // Per-CTA context
 // ---------------------------------------------------------------------------
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
+
 template <int DT>
 struct Ctx {
   static constexpr int E = Elem<DT>::kPerUnit;
@@ -442,36 +485,80 @@ struct Ctx {
   uint8_t* gmask;              // chunk start in the mask
   int n, head_n, body_units, tail_n;
   uint32_t C, crank;
+  uint32_t ring;        // shared address of the streaming ring
+  const uint4* ring_ptr;  // the same ring, generic
+  uint32_t ring_bar;    // shared address of F->ring_bar[0]
+  uint32_t ring_phase;  // bit s: parity of stage s's next completion
+  uint32_t ring_out;    // thread 0: stages with a copy not yet seen complete
   int ph;           // cluster merge counter (slot parity)
   float m;          // row max (softmax shift)
   bool m_neginf;
   float fix_scale;  // fixed-point scale of weights in [0, 1]
 };
 
-// Stream the chunk from global memory: kUnroll 16-byte units per thread in
-// flight, then the head / tail elements (fewer than 2E, one per thread).
-// unit_fn(xs, idx0, valid) and scalar_fn(x, idx, valid) are called by every
-// thread the same number of times (convergent), valid or not.
+// Issue the bulk copy of piece `piece` of the chunk body into ring stage `st`
+// (thread 0 only).
+template <int DT>
+__device__ __forceinline__ void ring_issue(Ctx<DT>& c, int piece, int st) {
+  const int u0 = piece * kPieceUnits;
+  const int n = min(kPieceUnits, c.body_units - u0);
+  const uint32_t bar = c.ring_bar + 8u * st;
+  const uint32_t bytes = static_cast<uint32_t>(n) * 16u;
+  mbar_expect_tx(bar, bytes);
+  bulk_g2s(c.ring + static_cast<uint32_t>(st) * kPieceBytes, c.gbody + 16 * static_cast<size_t>(u0), bytes, bar);
+  c.ring_out |= 1u << st;
+}
+
+// Stream the chunk: the 16-byte aligned body through the shared-memory ring
+// (kStages bulk copies in flight), then the head / tail elements (fewer than
+// 2E, one per thread). unit_fn(xs, idx0, valid) and scalar_fn(x, idx, valid)
+// are called by every thread the same number of times (convergent), valid or
+// not. prefetched: the first min(kStages, pieces) copies were issued already.
+// Every copy issued here has landed when it returns, unless a wait gave up
+// (F->err set; later calls then issue nothing).
 template <int DT, typename UnitFn, typename ScalarFn>
-__device__ __forceinline__ void stream_chunk(const Ctx<DT>& c, UnitFn&& unit_fn, ScalarFn&& scalar_fn) {
+__device__ __forceinline__ void stream_chunk(Ctx<DT>& c, UnitFn&& unit_fn, ScalarFn&& scalar_fn,
+                                             bool prefetched = false) {
   constexpr int E = Ctx<DT>::E;
   constexpr int S = Ctx<DT>::S;
+  Fixed& F = *c.F;
   const int tid = threadIdx.x;
   const int nb = c.body_units;
-  for (int base = 0; base < nb; base += kThreads * kUnroll) {
-    uint4 v[kUnroll];
+  const int npieces = (nb + kPieceUnits - 1) / kPieceUnits;
+  __syncthreads();  // earlier users of the ring's bytes are done
+  if (tid == 0 && !prefetched && npieces > 0 && vld(F.err) == 0u) {
+    fence_proxy_async_smem();  // generic writes to these bytes before the async copies
+    for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc);
+  }
+  for (int pc = 0; pc < npieces; ++pc) {
+    const int st = pc & (kStages - 1);
+    const uint32_t bar = c.ring_bar + 8u * st;
+    bool ok = false;
+    if (vld(F.err) == 0u) ok = mbar_wait_bounded(bar, (c.ring_phase >> st) & 1u, kWaitLimitNs);
+    if (ok) {
+      c.ring_phase ^= 1u << st;
+      if (tid == 0) c.ring_out &= ~(1u << st);
+    } else {
+      F.err = 1u;
+    }
+    const int u0 = pc * kPieceUnits;
+    const int n = min(kPieceUnits, nb - u0);
+    const uint4* sp = c.ring_ptr + static_cast<size_t>(st) * kPieceUnits;
+    uint4 v[kPieceUnits / kThreads];
 #pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int u = base + j * kThreads + tid;
-      v[j] = (u < nb) ? ldg16(c.gbody + 16 * static_cast<size_t>(u)) : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < kPieceUnits / kThreads; ++j) {
+      const int u = j * kThreads + tid;
+      v[j] = (u < n) ? sp[u] : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
-    for (int j = 0; j < kUnroll; ++j) {
-      const int u = base + j * kThreads + tid;
+    for (int j = 0; j < kPieceUnits / kThreads; ++j) {
+      const int u = j * kThreads + tid;
       float xs[E];
       unpack<DT>(v[j], xs);
-      unit_fn(xs, static_cast<uint32_t>(c.head_n + u * E), u < nb);
+      unit_fn(xs, static_cast<uint32_t>(c.head_n + (u0 + u) * E), u < n);
     }
+    __syncthreads();  // every thread is done with stage st
+    if (tid == 0 && pc + kStages < npieces && vld(F.err) == 0u) ring_issue(c, pc + kStages, st);
   }
   float x = 0.f;
   uint32_t idx = 0;
@@ -487,6 +574,15 @@ __device__ __forceinline__ void stream_chunk(const Ctx<DT>& c, UnitFn&& unit_fn,
     }
   }
   scalar_fn(x, idx, valid);
+}
+
+// After a wait gave up: wait (bounded) for every copy still in flight into
+// this CTA's ring, so that none lands after the CTA has exited (thread 0).
+template <int DT>
+__device__ void ring_drain(Ctx<DT>& c) {
+  for (int st = 0; st < kStages; ++st)
+    if ((c.ring_out >> st) & 1u)
+      (void)mbar_wait_bounded(c.ring_bar + 8u * st, (c.ring_phase >> st) & 1u, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------------------
@@ -923,6 +1019,69 @@ __device__ bool gather_extracted(Ctx<DT>& c) {
   return true;
 }
 
+// After the streaming pass: move the warps' segments of the own list
+// together (segment w holds its survivors at w * segcap), so the list is
+// [0, own_n). F.own_n gets the exact survivor count; F.seg_ovf is set (and
+// nothing moves) when a warp's survivors exceeded its segment.
+template <int DT>
+__device__ void compact_segments(Ctx<DT>& c, uint32_t wn) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t segcap = c.ocap / kWarps;
+  if (lane == 0) F.seg_n[warp] = wn;
+  __syncthreads();
+  uint32_t total = 0, mine_off = 0;
+  bool ovf = false;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t n = vld(F.seg_n[w]);
+    if (w < warp) mine_off += n;
+    total += n;
+    ovf = ovf || n > segcap;
+  }
+  if (!ovf) {
+    if (total <= segcap) {
+      // every destination lies below segcap: clear of every source that moves
+      if (warp > 0) {
+        const uint32_t src = static_cast<uint32_t>(warp) * segcap;
+        for (uint32_t i = lane; i < wn; i += 32) {
+          c.own_val[mine_off + i] = c.own_val[src + i];
+          c.own_idx[mine_off + i] = c.own_idx[src + i];
+        }
+      }
+    } else {
+      // segments in order, each moved down in block-wide rounds (read, barrier,
+      // write, barrier): a round's writes reach no source still to be read
+      uint32_t off = vld(F.seg_n[0]);
+      for (int w = 1; w < kWarps; ++w) {
+        const uint32_t n = vld(F.seg_n[w]);
+        const uint32_t src = static_cast<uint32_t>(w) * segcap;
+        for (uint32_t b = 0; b < n; b += kThreads) {
+          const uint32_t i = b + tid;
+          float v = 0.f;
+          uint32_t ix = 0;
+          if (i < n) {
+            v = c.own_val[src + i];
+            ix = c.own_idx[src + i];
+          }
+          __syncthreads();
+          if (i < n) {
+            c.own_val[off + i] = v;
+            c.own_idx[off + i] = ix;
+          }
+          __syncthreads();
+        }
+        off += n;
+      }
+    }
+  }
+  if (tid == 0) {
+    F.own_n = total;
+    F.seg_ovf = ovf ? 1u : 0u;
+  }
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------
 // Local quaternary search over the gathered set (block barriers only)
 // ---------------------------------------------------------------------------
@@ -1252,6 +1411,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   c.ocap = static_cast<uint32_t>(P.ocap);
   c.gcap = static_cast<uint32_t>(P.gcap);
   c.lists = smem + sizeof(Fixed);
+  {
+    unsigned char* ring = c.lists + (list_region_bytes(static_cast<int>(P.C), P.ocap, P.gcap) - kRingBytes);
+    c.ring = smem_u32(ring);
+    c.ring_ptr = reinterpret_cast<const uint4*>(ring);
+    c.ring_bar = smem_u32(&c.F->ring_bar[0]);
+    c.ring_phase = 0u;
+    c.ring_out = 0u;
+  }
   c.alias = P.C == 1;
   c.own_val = reinterpret_cast<float*>(c.lists);
   c.own_idx = reinterpret_cast<uint32_t*>(c.own_val + P.ocap);
@@ -1286,6 +1453,17 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     c.tail_n = c.n - c.head_n - c.body_units * E;
   }
   c.gbody = c.gx + c.head_n * S;
+  // the ring's first copies of the streaming pass fly while the sample
+  // statistics are taken (the chunk does not depend on them)
+  if (tid == 0) {
+    F.own_n = 0;
+    F.err = 0u;
+    F.err_any = 0u;
+    for (int st = 0; st < kStages; ++st) mbar_init(c.ring_bar + 8u * st, 1u);
+    fence_mbar_init();
+    const int npieces = (c.body_units + kPieceUnits - 1) / kPieceUnits;
+    for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc);
+  }
   QRITA_T(0);
 #ifdef QRITA_TRACE_TIME
   if (tid == 0 && blockIdx.x < 65536) g_cta_times[blockIdx.x][0] = globaltimer_ns();
@@ -1309,9 +1487,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
 
   // ---- A2: statistics of one sample block of the row (identical in every CTA)
   {
+    constexpr int kPer = (kSampleBlocks * kSampleBlock) / kThreads;
+    float sv[kPer];  // this thread's sample values (NaN: none)
     float sn = 0.f, sx = 0.f, sxx = 0.f, smax = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < (kSampleBlocks * kSampleBlock) / kThreads; ++j) {
+    for (int j = 0; j < kPer; ++j) {
       const int sidx = tid + j * kThreads;
       int64_t pos;
       if (V <= kSampleBlocks * kSampleBlock) {
@@ -1319,9 +1499,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       } else {
         pos = static_cast<int64_t>(sidx / kSampleBlock) * (V / kSampleBlocks) + (sidx % kSampleBlock);
       }
+      sv[j] = NAN;
       if (pos < V) {
         const float x = load_elem<DT>(grow + static_cast<size_t>(pos) * S);
         if (isfinite(x)) {
+          sv[j] = x;
           sn += 1.f;
           sx += x;
           sxx = fmaf(x, x, sxx);
@@ -1340,15 +1522,53 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       F.redf[warp][2] = sxx;
       F.redf[warp][3] = smax;
     }
-    if (tid == 0) F.own_n = 0;
     __syncthreads();
+    // first estimate, then the same moments over the values within
+    // kClipSigmas of it: a rare outlier in the sample would otherwise
+    // inflate sigma and push the threshold above the k-th logit
+    float a = 0.f, b = 0.f, d = 0.f, mx = -INFINITY;
+    for (int w = 0; w < kWarps; ++w) {
+      a += vld(F.redf[w][0]);
+      b += vld(F.redf[w][1]);
+      d += vld(F.redf[w][2]);
+      mx = fmaxf(mx, vld(F.redf[w][3]));
+    }
+    {
+      const float mean0 = a > 0.f ? b / a : 0.f;
+      const float sd0 = a > 0.f ? sqrtf(fmaxf(d / a - mean0 * mean0, 0.f)) : 0.f;
+      const float lim = kClipSigmas * sd0;
+      float cn = 0.f, cx = 0.f, cxx = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const float x = sv[j];
+        if (fabsf(x - mean0) <= lim) {  // false for NaN
+          cn += 1.f;
+          cx += x;
+          cxx = fmaf(x, x, cxx);
+        }
+      }
+      cn = warp_sum_f(cn);
+      cx = warp_sum_f(cx);
+      cxx = warp_sum_f(cxx);
+      __syncthreads();  // every thread has read the first partials
+      if (lane == 0) {
+        F.redf[warp][4] = cn;
+        F.redf[warp][5] = cx;
+        F.redf[warp][6] = cxx;
+      }
+      __syncthreads();
+    }
     if (tid == 0) {
-      float a = 0.f, b = 0.f, d = 0.f, mx = -INFINITY;
+      float ca = 0.f, cb = 0.f, cd = 0.f;
       for (int w = 0; w < kWarps; ++w) {
-        a += vld(F.redf[w][0]);
-        b += vld(F.redf[w][1]);
-        d += vld(F.redf[w][2]);
-        mx = fmaxf(mx, vld(F.redf[w][3]));
+        ca += vld(F.redf[w][4]);
+        cb += vld(F.redf[w][5]);
+        cd += vld(F.redf[w][6]);
+      }
+      if (ca > 0.f) {  // else keep the first estimate
+        a = ca;
+        b = cb;
+        d = cd;
       }
       const float mean = a > 0.f ? b / a : 0.f;
       const float var = a > 0.f ? fmaxf(d / a - mean * mean, 0.f) : 0.f;
@@ -1356,7 +1576,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       const float sigma = sqrtf(var);
       F.bc.f[BF_MU] = mu;
       F.bc.f[BF_SIGMA] = sigma;
-      F.bc.f[BF_MREF] = a > 0.f ? mx : 0.f;
+      F.bc.f[BF_MREF] = mx > -INFINITY ? mx : 0.f;
       // ---- A3: delta from the normal-quantile tables, threshold t
       bool trunc = false;
       float t = -INFINITY;
@@ -1394,81 +1614,68 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
 
   // ---- A4: the streaming pass (the one HBM read of the row)
   {
-    float vmax = -INFINITY, vmin = INFINITY, smin = INFINITY;
-    uint32_t smin_n = 0;
+    float vmax = -INFINITY, vmin = INFINITY;
+    uint32_t wn = 0;  // this warp's survivors (its segment of the own list)
+    const uint32_t segcap = c.ocap / kWarps;
+    const uint32_t seg_base = static_cast<uint32_t>(warp) * segcap;
     F2 zs = {0.f, 0.f}, ms = {0.f, 0.f};
-    stream_chunk<DT>(
-        c,
-        [&](const float (&xs)[E], uint32_t idx0, bool valid) {
-          uint32_t bits = 0;
-          if (valid) {
-            float zu = 0.f, mu_ = 0.f;  // this unit's softmax partials (shift m_ref)
+    // two instances: the softmax sums (one expf per element) only where
+    // top-p runs alone
+    auto streaming_pass = [&](auto po) {
+      constexpr bool PO = decltype(po)::value;
+      stream_chunk<DT>(
+          c,
+          [&](const float (&xs)[E], uint32_t idx0, bool valid) {
+            uint32_t bits = 0;
+            if (valid) {
+              float zu = 0.f, mu_ = 0.f;  // this unit's softmax partials (shift m_ref)
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-              const float x = xs[e];
+              for (int e = 0; e < E; ++e) {
+                const float x = xs[e];
+                vmax = fmax_nan(vmax, x);
+                vmin = fminf(vmin, x);
+                const bool surv = trunc && x >= t;
+                bits |= surv ? (1u << e) : 0u;
+                if constexpr (PO) {
+                  const float w = expf(x - m_ref);
+                  zu += w;
+                  mu_ += surv ? w : 0.f;
+                }
+              }
+              if constexpr (PO) {
+                f2_add(zs, zu);
+                f2_add(ms, mu_);
+              }
+            }
+            if (trunc) seg_append<E>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx0, bits);
+          },
+          [&](float x, uint32_t idx, bool valid) {
+            uint32_t bits = 0;
+            if (valid) {
               vmax = fmax_nan(vmax, x);
               vmin = fminf(vmin, x);
               const bool surv = trunc && x >= t;
-              bits |= surv ? (1u << e) : 0u;
-              if (k_on && surv) {
-                if (x < smin) {
-                  smin = x;
-                  smin_n = 1;
-                } else if (x == smin) {
-                  ++smin_n;
-                }
-              }
-              if (p_only) {
+              bits = surv ? 1u : 0u;
+              if constexpr (PO) {
                 const float w = expf(x - m_ref);
-                zu += w;
-                mu_ += surv ? w : 0.f;
+                f2_add(zs, w);
+                f2_add(ms, surv ? w : 0.f);
               }
             }
-            if (p_only) {
-              f2_add(zs, zu);
-              f2_add(ms, mu_);
-            }
-          }
-          if (trunc) warp_append<E>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx0, bits);
-        },
-        [&](float x, uint32_t idx, bool valid) {
-          uint32_t bits = 0;
-          if (valid) {
-            vmax = fmax_nan(vmax, x);
-            vmin = fminf(vmin, x);
-            const bool surv = trunc && x >= t;
-            bits = surv ? 1u : 0u;
-            if (k_on && surv) {
-              if (x < smin) {
-                smin = x;
-                smin_n = 1;
-              } else if (x == smin) {
-                ++smin_n;
-              }
-            }
-            if (p_only) {
-              const float w = expf(x - m_ref);
-              f2_add(zs, w);
-              f2_add(ms, surv ? w : 0.f);
-            }
-          }
-          const float xs[1] = {x};
-          if (trunc) warp_append<1>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx, bits);
-        });
+            const float xs[1] = {x};
+            if (trunc) seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, bits);
+          },
+          true);
+    };
+    if (p_only) streaming_pass(BoolC<true>{});
+    else streaming_pass(BoolC<false>{});
     QRITA_T(2);
+    if (trunc) compact_segments<DT>(c, wn);
     // block reduce
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       vmax = fmax_nan(vmax, __shfl_xor_sync(kFull, vmax, o));
       vmin = fminf(vmin, __shfl_xor_sync(kFull, vmin, o));
-      const float s2 = __shfl_xor_sync(kFull, smin, o);
-      const uint32_t n2 = __shfl_xor_sync(kFull, smin_n, o);
-      if (s2 < smin) {
-        smin = s2;
-        smin_n = n2;
-      } else if (s2 == smin) {
-        smin_n += n2;
-      }
       if (p_only) {
         const F2 a = f2_make(__shfl_xor_sync(kFull, zs.hi, o), __shfl_xor_sync(kFull, zs.lo, o));
         const F2 b = f2_make(__shfl_xor_sync(kFull, ms.hi, o), __shfl_xor_sync(kFull, ms.lo, o));
@@ -1479,38 +1686,26 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     if (lane == 0) {
       F.redf[warp][0] = vmax;
       F.redf[warp][1] = vmin;
-      F.redf[warp][2] = smin;
       F.redf[warp][3] = zs.hi;
       F.redf[warp][4] = zs.lo;
       F.redf[warp][5] = ms.hi;
       F.redf[warp][6] = ms.lo;
-      F.redu[warp][0] = smin_n;
     }
     __syncthreads();
     Slot& my = F.slots[c.ph & 1];
     if (tid == 0) {
-      float a = -INFINITY, b = INFINITY, sm = INFINITY;
-      uint32_t sn = 0;
+      float a = -INFINITY, b = INFINITY;
       F2 z = {0.f, 0.f}, mm = {0.f, 0.f};
       for (int w = 0; w < kWarps; ++w) {
         a = fmax_nan(a, vld(F.redf[w][0]));
         b = fminf(b, vld(F.redf[w][1]));
-        const float s2 = vld(F.redf[w][2]);
-        const uint32_t n2 = vld(F.redu[w][0]);
-        if (s2 < sm) {
-          sm = s2;
-          sn = n2;
-        } else if (s2 == sm) {
-          sn += n2;
-        }
         z = f2_merge(z, f2_make(vld(F.redf[w][3]), vld(F.redf[w][4])));
         mm = f2_merge(mm, f2_make(vld(F.redf[w][5]), vld(F.redf[w][6])));
       }
       my.f[0] = a;
       my.f[1] = b;
-      my.f[2] = sm;
-      my.u[0] = sn;
-      my.u[1] = vld(F.own_n);
+      my.u[0] = trunc ? vld(F.seg_ovf) : 0u;
+      my.u[1] = trunc ? vld(F.own_n) : 0u;
       my.pr[0] = z.hi;
       my.pr[1] = z.lo;
       my.pr[2] = mm.hi;
@@ -1518,35 +1713,26 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     }
     cluster_sync_all();
     if (warp == 0) {
-      float a = -INFINITY, b = INFINITY, sm = INFINITY;
-      uint32_t sn = 0, surv = 0, ovf = 0;
+      float a = -INFINITY, b = INFINITY;
+      uint32_t surv = 0, ovf = 0;
       F2 z = {0.f, 0.f}, mm = {0.f, 0.f};
       if (lane < static_cast<int>(c.C)) {
         const uint32_t fb = map_rank(smem_u32(&my.f[0]), lane);
         a = ld_dsmem_f32(fb);
         b = ld_dsmem_f32(fb + 4);
-        sm = ld_dsmem_f32(fb + 8);
         const uint32_t ub = map_rank(smem_u32(&my.u[0]), lane);
-        sn = ld_dsmem_u32(ub);
+        ovf = ld_dsmem_u32(ub);
         surv = ld_dsmem_u32(ub + 4);
         const uint32_t pb = map_rank(smem_u32(&my.pr[0]), lane);
         z = f2_make(ld_dsmem_f32(pb), ld_dsmem_f32(pb + 4));
         mm = f2_make(ld_dsmem_f32(pb + 8), ld_dsmem_f32(pb + 12));
-        ovf = surv > c.ocap ? 1u : 0u;
+        ovf |= surv > c.ocap ? 1u : 0u;
         F.rank_n[lane] = surv;
       }
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) {
         a = fmax_nan(a, __shfl_xor_sync(kFull, a, o));
         b = fminf(b, __shfl_xor_sync(kFull, b, o));
-        const float s2 = __shfl_xor_sync(kFull, sm, o);
-        const uint32_t n2 = __shfl_xor_sync(kFull, sn, o);
-        if (s2 < sm) {
-          sm = s2;
-          sn = n2;
-        } else if (s2 == sm) {
-          sn += n2;
-        }
         surv += __shfl_xor_sync(kFull, surv, o);
         ovf |= __shfl_xor_sync(kFull, ovf, o);
         z = f2_merge(z, f2_make(__shfl_xor_sync(kFull, z.hi, o), __shfl_xor_sync(kFull, z.lo, o)));
@@ -1555,8 +1741,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       if (lane == 0) {
         F.bc.f[BF_MAX] = a;
         F.bc.f[BF_MIN] = b;
-        F.bc.f[BF_SMIN] = sm;
-        F.bc.u[BU_SMIN_N] = sn;
         F.bc.u[BU_S] = surv;
         F.bc.u[BU_OVF] = ovf;
         put_pair(F.bc, BP_ZR, z);
@@ -1569,8 +1753,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   QRITA_T(3);
   const float row_max = vld(F.bc.f[BF_MAX]);
   const float row_min = vld(F.bc.f[BF_MIN]);
-  const float surv_min = vld(F.bc.f[BF_SMIN]);
-  const uint32_t surv_min_n = vld(F.bc.u[BU_SMIN_N]);
   const uint32_t survivors = vld(F.bc.u[BU_S]);
   const bool overflow = vld(F.bc.u[BU_OVF]) != 0u;
   const bool invalid = isnan(row_max) || row_max == INFINITY;
@@ -1596,7 +1778,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   unsigned long long z_used = 0ull;  // softmax denominator top-p used (fixed point)
   bool sel_all = keep_all && !invalid;
   bool sel_none = invalid;
-  bool remote_done = false;   // the last access to another CTA's memory is behind a barrier
   bool list_emit = false;     // every kept element is in this CTA's own list
   bool ties_in_list = false;  // every element equal to tau is in this CTA's own list
   bool ties_known = false;    // F.ties holds the per-rank tie counts
@@ -1622,7 +1803,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       if (hit && survivors <= c.gcap) {
         // gather Z_t whole: the candidates are (key(t) - 1, max]
         gather_all<DT>(c);
-        remote_done = true;
         s.lo = f2key(t) - 1u;
         s.c_lo = survivors;
         s.hi = f2key(row_max);
@@ -1630,16 +1810,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         k_full = true;
         list_emit = true;
         ties_in_list = true;
-        if (survivors - surv_min_n < target) {
-          // z_mn of the initial lo is the smallest survivor: it is the boundary
-          s.tau = f2key(surv_min);
-          s.count_above = survivors - surv_min_n;
-          s.n_keep = target - s.count_above;
-          s.rounds = 0;
-          s.capped = false;
-        } else {
-          local_search<DT, false>(c, s, target, value_pivots, nullptr);
-        }
+        local_search<DT, false>(c, s, target, value_pivots, nullptr);
       } else {
         // narrow: over the survivor lists on a hit, over the chunk otherwise
         Range R;
@@ -1689,7 +1860,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           const float glo = R.lo_all ? -INFINITY : pivot_f(R.lo);
           const float ghi = R.pin_hi ? INFINITY : pivot_f(R.hi);
           gather<DT>(c, glo, ghi, R.lo_all, !hit);
-          remote_done = true;
           s.lo = R.lo;
           s.c_lo = R.c_lo;
           if (R.pin_hi) {
@@ -1736,7 +1906,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       Rx.pin_hi = true;
       extract_range<DT>(c, Rx);
       if (gather_extracted<DT>(c)) {
-        remote_done = true;
         k_full = true;
         extracted_above_k = true;
       }
@@ -1814,7 +1983,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         const float scale = c.fix_scale;
         if (hit && survivors <= c.gcap) {
           gather_all<DT>(c);
-          remote_done = true;
           z_used = f2_to_u64(f2_mul(Zm, scale));
           s.lo = f2key(t) - 1u;
           s.c_lo = survivors;
@@ -1889,7 +2057,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               __syncthreads();
             }
             gather<DT>(c, R.lo_all ? -INFINITY : pivot_f(R.lo), pivot_f(R.hi), R.lo_all, !hit);
-            remote_done = true;
             s.lo = R.lo;
             s.hi = R.hi;
             s.c_lo = R.c_lo;
@@ -1917,10 +2084,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         }
       }
     }
-  }
-  if (!remote_done) {
-    cluster_sync_all();  // no CTA leaves while another may read its memory
-    remote_done = true;
   }
   QRITA_T(5);
 
@@ -2001,57 +2164,72 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       running = vld(F.scan[0]);
       __syncthreads();
     }
-    const int nb = c.body_units;
-    for (int base = 0; base < nb; base += kThreads) {
-      const int u = base + tid;
-      const bool valid = u < nb;
-      float xs[E];
-      if (valid) {
-        unpack<DT>(ldg16(c.gbody + 16 * static_cast<size_t>(u)), xs);
-      } else {
+    stream_chunk<DT>(
+        c,
+        [&](const float (&xs)[E], uint32_t idx0, bool valid) {
+          uint32_t rank = 0;
+          if (ordered_ties) {
+            uint32_t mine = 0;
+            if (valid) {
 #pragma unroll
-        for (int e = 0; e < E; ++e) xs[e] = -INFINITY;
-      }
-      uint32_t rank = 0;
-      if (ordered_ties) {
-        uint32_t mine = 0;
-        if (valid) {
+              for (int e = 0; e < E; ++e) mine += (xs[e] == tau_f) ? 1u : 0u;
+            }
+            uint32_t tot;
+            const uint32_t ex = block_excl_scan(F, mine, &tot);
+            rank = running + ex;
+            running += tot;
+          }
+          if (!valid) return;
+          uint8_t bytes[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) mine += (xs[e] == tau_f) ? 1u : 0u;
-        }
-        uint32_t tot;
-        const uint32_t ex = block_excl_scan(F, mine, &tot);
-        rank = running + ex;
-        running += tot;
-      }
-      if (!valid) continue;
-      uint8_t bytes[E];
+          for (int e = 0; e < E; ++e) bytes[e] = byte_of(xs[e], idx0 + e, rank);
+          uint8_t* dst = c.gmask + idx0;
+          if (vec_ok) {
+            if constexpr (E == 4) {
+              *reinterpret_cast<uint32_t*>(dst) =
+                  bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
+            } else {
+              const uint32_t w0 =
+                  bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
+              const uint32_t w1 =
+                  bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (static_cast<uint32_t>(bytes[7]) << 24);
+              *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+            }
+          } else {
 #pragma unroll
-      for (int e = 0; e < E; ++e) bytes[e] = byte_of(xs[e], static_cast<uint32_t>(c.head_n + u * E + e), rank);
-      uint8_t* dst = c.gmask + c.head_n + static_cast<size_t>(u) * E;
-      if (vec_ok) {
-        if constexpr (E == 4) {
-          *reinterpret_cast<uint32_t*>(dst) =
-              bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
-        } else {
-          const uint32_t w0 = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
-          const uint32_t w1 = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (static_cast<uint32_t>(bytes[7]) << 24);
-          *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) dst[e] = bytes[e];
-      }
-    }
-    if (tid == 0) {
-      for (int j = 0; j < c.tail_n; ++j) {
-        const uint32_t idx = static_cast<uint32_t>(c.head_n + nb * E + j);
-        const float x = load_elem<DT>(c.gbody + 16 * static_cast<size_t>(nb) + j * S);
-        c.gmask[idx] = byte_of(x, idx, running);
-      }
-    }
+            for (int e = 0; e < E; ++e) dst[e] = bytes[e];
+          }
+        },
+        [&](float x, uint32_t idx, bool valid) {
+          // the head was emitted above: only tail elements remain (index order = thread order)
+          const bool tail = valid && idx >= static_cast<uint32_t>(c.head_n);
+          uint32_t rank = 0;
+          if (ordered_ties) {
+            uint32_t tot;
+            rank = running + block_excl_scan(F, (tail && x == tau_f) ? 1u : 0u, &tot);
+            running += tot;
+          }
+          if (tail) c.gmask[idx] = byte_of(x, idx, rank);
+        });
   }
   QRITA_T(7);
+
+  // ---- a bulk-copy wait that gave up anywhere in the row voids the row.
+  // The last cluster barrier: no CTA leaves while another may still access
+  // its memory, and every CTA learns whether any CTA of the row failed.
+  __syncthreads();
+  if (tid == 0 && vld(F.err) != 0u) {
+    ring_drain<DT>(c);
+    for (uint32_t rr = 0; rr < c.C; ++rr) st_dsmem_u32(map_rank(smem_u32(&F.err_any), rr), 1u);
+  }
+  if (c.C > 1) cluster_sync_all();
+  else __syncthreads();
+  if (vld(F.err_any) != 0u) {
+    for (int i = tid; i < c.n; i += kThreads) c.gmask[i] = 0;
+    row_status = QRITA_ROW_TIMEOUT;
+    sel_none = true;
+    sel_all = false;
+  }
 #ifdef QRITA_TRACE_TIME
   if (tid == 0 && blockIdx.x < 65536) g_cta_times[blockIdx.x][1] = globaltimer_ns();
 #endif
@@ -2088,9 +2266,10 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
 }  // namespace
 
 size_t smem_bytes(int C, int ocap, int gcap) {
-  size_t lists = static_cast<size_t>(ocap) * 8u;  // own list: value + index
-  if (C > 1) lists += static_cast<size_t>(gcap) * 8u;  // gathered set: value + tag
-  if (lists < static_cast<size_t>(kMinListBytes)) lists = kMinListBytes;
+  const size_t lists = list_region_bytes(C, ocap, gcap);
+  // the ring must clear the own list and the narrowing bins laid over the region
+  const size_t ring_off = lists - kRingBytes;
+  if (ring_off < static_cast<size_t>(ocap) * 8u || ring_off < static_cast<size_t>(kBinBytes)) return 0;
   return (sizeof(Fixed) + lists + 127u) & ~static_cast<size_t>(127u);
 }
 
