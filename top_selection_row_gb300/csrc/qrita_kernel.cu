@@ -51,8 +51,8 @@ constexpr int kSampleBlock = 64;  // 16 x 64 = 1024 sampled logits per row
 constexpr float kClipSigmas = 4.0f;  // sample values beyond this many sigmas are outliers
 // Streaming ring: the chunk moves through shared memory in pieces of
 // kPieceBytes by 1-D bulk copies (TMA), kStages pieces in flight.
-constexpr int kStages = 4;
-constexpr int kPieceBytes = 8192;
+constexpr int kStages = 2;
+constexpr int kPieceBytes = 16384;
 constexpr int kPieceUnits = kPieceBytes / 16;
 constexpr int kRingBytes = kStages * kPieceBytes;
 static_assert((kStages & (kStages - 1)) == 0, "kStages must be a power of two");
@@ -66,17 +66,13 @@ constexpr int kTagShift = 28;  // gathered tag = rank << 28 | index in chunk
 // masses) over the start of the list region, clear of the streaming ring.
 constexpr int kBinBytes = kBins * kThreads * (4 + 8);
 #ifdef QRITA_TRACE_TIME
-// Debug-only stage timestamps of three CTAs, and start / end of every CTA
-// (built with -DQRITA_TRACE_TIME).
-__device__ unsigned long long g_times[3][16];
-__device__ unsigned long long g_cta_times[65536][2];
+// Debug-only stage timestamps of every CTA (built with -DQRITA_TRACE_TIME):
+// g_cta_stage[cta][i] = globaltimer at mark i (0 start, 15 end).
+constexpr int kTraceCtas = 16384;
+__device__ unsigned long long g_cta_stage[kTraceCtas][16];
 #define QRITA_T(i)                                                                              \
   do {                                                                                          \
-    if (threadIdx.x == 0) {                                                                     \
-      const int slot_ = blockIdx.x == 0 ? 0                                                     \
-                        : (blockIdx.x == gridDim.x / 2 ? 1 : (blockIdx.x == gridDim.x - 1 ? 2 : -1)); \
-      if (slot_ >= 0) g_times[slot_][i] = globaltimer_ns();                                     \
-    }                                                                                           \
+    if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_cta_stage[blockIdx.x][i] = globaltimer_ns(); \
   } while (0)
 #else
 #define QRITA_T(i) \
@@ -183,7 +179,7 @@ struct alignas(16) Fixed {
   Slot slots[2];
   Bcast bc;
   PAccS red[kWarps][3];
-  LPart lred[kWarps][3];
+  LPart lred[2][kWarps][3];  // local search: per-warp partials, double-buffered
   float redf[kWarps][8];
   uint32_t redu[kWarps][kBins];
   uint32_t bin_cnt[kWarps][kBins];
@@ -509,16 +505,22 @@ __device__ __forceinline__ void ring_issue(Ctx<DT>& c, int piece, int st) {
   c.ring_out |= 1u << st;
 }
 
+// Units of one ring piece each thread holds: unit j of a piece starting at
+// unit u0 is u0 + j * kThreads + threadIdx.x.
+constexpr int kPieceThreadUnits = kPieceUnits / kThreads;
+
 // Stream the chunk: the 16-byte aligned body through the shared-memory ring
 // (kStages bulk copies in flight), then the head / tail elements (fewer than
-// 2E, one per thread). unit_fn(xs, idx0, valid) and scalar_fn(x, idx, valid)
-// are called by every thread the same number of times (convergent), valid or
-// not. prefetched: the first min(kStages, pieces) copies were issued already.
-// Every copy issued here has landed when it returns, unless a wait gave up
-// (F->err set; later calls then issue nothing).
-template <int DT, typename UnitFn, typename ScalarFn>
-__device__ __forceinline__ void stream_chunk(Ctx<DT>& c, UnitFn&& unit_fn, ScalarFn&& scalar_fn,
-                                             bool prefetched = false) {
+// 2E, one per thread). piece_fn(v, u0, n) gets this thread's units of each
+// piece (v[j] valid when j * kThreads + tid < n); scalar_fn(x, idx, valid)
+// the head / tail element of this thread. Both are called by every thread
+// the same number of times (convergent), valid or not. prefetched: the first
+// min(kStages, pieces) copies were issued already. Every copy issued here has
+// landed when it returns, unless a wait gave up (F->err set; later calls then
+// issue nothing).
+template <int DT, typename PieceFn, typename ScalarFn>
+__device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, ScalarFn&& scalar_fn,
+                                              bool prefetched) {
   constexpr int E = Ctx<DT>::E;
   constexpr int S = Ctx<DT>::S;
   Fixed& F = *c.F;
@@ -544,21 +546,15 @@ __device__ __forceinline__ void stream_chunk(Ctx<DT>& c, UnitFn&& unit_fn, Scala
     const int u0 = pc * kPieceUnits;
     const int n = min(kPieceUnits, nb - u0);
     const uint4* sp = c.ring_ptr + static_cast<size_t>(st) * kPieceUnits;
-    uint4 v[kPieceUnits / kThreads];
+    uint4 v[kPieceThreadUnits];
 #pragma unroll
-    for (int j = 0; j < kPieceUnits / kThreads; ++j) {
+    for (int j = 0; j < kPieceThreadUnits; ++j) {
       const int u = j * kThreads + tid;
       v[j] = (u < n) ? sp[u] : make_uint4(0u, 0u, 0u, 0u);
     }
-#pragma unroll
-    for (int j = 0; j < kPieceUnits / kThreads; ++j) {
-      const int u = j * kThreads + tid;
-      float xs[E];
-      unpack<DT>(v[j], xs);
-      unit_fn(xs, static_cast<uint32_t>(c.head_n + (u0 + u) * E), u < n);
-    }
-    __syncthreads();  // every thread is done with stage st
+    __syncthreads();  // every thread holds its part of stage st: refill it now
     if (tid == 0 && pc + kStages < npieces && vld(F.err) == 0u) ring_issue(c, pc + kStages, st);
+    piece_fn(v, u0, n);
   }
   float x = 0.f;
   uint32_t idx = 0;
@@ -574,6 +570,25 @@ __device__ __forceinline__ void stream_chunk(Ctx<DT>& c, UnitFn&& unit_fn, Scala
     }
   }
   scalar_fn(x, idx, valid);
+}
+
+// stream_pieces one unit at a time: unit_fn(xs, idx0, valid) per unit.
+template <int DT, typename UnitFn, typename ScalarFn>
+__device__ __forceinline__ void stream_chunk(Ctx<DT>& c, UnitFn&& unit_fn, ScalarFn&& scalar_fn,
+                                             bool prefetched = false) {
+  constexpr int E = Ctx<DT>::E;
+  stream_pieces<DT>(
+      c,
+      [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
+#pragma unroll
+        for (int j = 0; j < kPieceThreadUnits; ++j) {
+          const int u = j * kThreads + static_cast<int>(threadIdx.x);
+          float xs[E];
+          unpack<DT>(v[j], xs);
+          unit_fn(xs, static_cast<uint32_t>(c.head_n + (u0 + u) * E), u < n);
+        }
+      },
+      scalar_fn, prefetched);
 }
 
 // After a wait gave up: wait (bounded) for every copy still in flight into
@@ -1131,54 +1146,38 @@ __device__ __forceinline__ unsigned long long warp_sum_u64_redux(unsigned long l
 // every decision is integer arithmetic; warp 0 takes it and broadcasts it.
 // target is the count (A6) or the fixed-point mass (A7) to reach.
 template <int DT, bool MASS>
-__device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots,
-                             const uint32_t* first_pivots) {
+__device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t gn = min(vld(F.g_n), c.gcap);
   const float scale = c.fix_scale;
-  // state in F.bc, written by thread 0
-  if (tid == 0) {
-    F.bc.u[BU_LO] = s.lo;
-    F.bc.u[BU_HI] = s.hi;
-    F.bc.u[BU_CLO] = s.c_lo;
-    F.bc.u[BU_CHI] = s.c_hi;
-    F.bc.x[BX_MLO] = s.m_lo;
-    F.bc.x[BX_MHI] = s.m_hi;
-    F.bc.u[BU_DONE] = 0;
-    F.bc.u[BU_VMODE] = value_pivots ? 1u : 0u;
-    // first pivots: given (the model's guess), or quartiles of the range
-    uint32_t q0, q1, q2;
-    bool used_value = false;
-    int np;
-    if (first_pivots != nullptr && s.lo < first_pivots[0] && first_pivots[0] < first_pivots[1] &&
-        first_pivots[1] < first_pivots[2] && first_pivots[2] < s.hi) {
-      q0 = first_pivots[0];
-      q1 = first_pivots[1];
-      q2 = first_pivots[2];
-      np = 3;
+  // the search state is held, identical, by every thread: one block barrier
+  // per round (the warps' partials are double-buffered)
+  uint32_t lo = s.lo, hi = s.hi, c_lo = s.c_lo, c_hi = s.c_hi;
+  unsigned long long m_lo = s.m_lo, m_hi = s.m_hi;
+  uint32_t tau = 0, n_keep = 0, cabove = 0;
+  int done = 0;  // 1: boundary found, 2: round cap
+  uint32_t q[3];
+  bool used_value = false;
+  int np = quartile_pivots(lo, hi, value_pivots, q[0], q[1], q[2], used_value);
+  // the boundary is the single key hi of (lo, hi]: keep the copies needed
+  auto one_key = [&]() {
+    tau = hi;
+    cabove = c_hi;
+    if (MASS) {
+      const unsigned long long w = weight_fx(key2f(hi), c.m, c.m_neginf, scale);
+      n_keep = copies_fx(target - m_hi, w, c_lo - c_hi);
     } else {
-      np = quartile_pivots(s.lo, s.hi, value_pivots, q0, q1, q2, used_value);
+      n_keep = static_cast<uint32_t>(target) - c_hi;
     }
-    if (np == 0) {
-      // (lo, hi] holds one key already
-      F.bc.u[BU_DONE] = 3;
-    }
-    F.bc.q[0] = q0;
-    F.bc.q[1] = q1;
-    F.bc.q[2] = q2;
-    F.bc.qf[0] = np > 0 ? pivot_f(q0) : INFINITY;
-    F.bc.qf[1] = np > 1 ? pivot_f(q1) : INFINITY;
-    F.bc.qf[2] = np > 2 ? pivot_f(q2) : INFINITY;
-    F.bc.u[BU_NP] = static_cast<uint32_t>(np);
-    F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
-  }
-  __syncthreads();
+    done = 1;
+  };
+  if (np == 0) one_key();
   int rounds = 0;
-  while (vld(F.bc.u[BU_DONE]) == 0u) {
+  while (done == 0) {
     float qf[3];
 #pragma unroll
-    for (int j = 0; j < 3; ++j) qf[j] = vld(F.bc.qf[j]);
+    for (int j = 0; j < 3; ++j) qf[j] = j < np ? pivot_f(q[j]) : INFINITY;
     uint32_t cnt[3] = {0u, 0u, 0u}, zk[3] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu}, nz[3] = {0u, 0u, 0u};
     unsigned long long ms[3] = {0ull, 0ull, 0ull};
     for (uint32_t i = tid; i < gn; i += kThreads) {
@@ -1195,6 +1194,7 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
         zk[j] = lt ? key : zk[j];
       }
     }
+    LPart(&buf)[kWarps][3] = F.lred[rounds & 1];
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
       const uint32_t cw = __reduce_add_sync(kFull, cnt[j]);
@@ -1202,138 +1202,97 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
       const uint32_t nw = __reduce_add_sync(kFull, zk[j] == zw ? nz[j] : 0u);
       const unsigned long long mw = MASS ? warp_sum_u64_redux(ms[j]) : 0ull;
       if (lane == 0) {
-        F.lred[warp][j].cnt = cw;
-        F.lred[warp][j].zmin = zw;
-        F.lred[warp][j].nz = nw;
-        F.lred[warp][j].mass = mw;
+        buf[warp][j].cnt = cw;
+        buf[warp][j].zmin = zw;
+        buf[warp][j].nz = nw;
+        buf[warp][j].mass = mw;
       }
     }
     __syncthreads();
     ++rounds;
-    if (warp == 0) {
-      // lanes 0..7 hold the warps' partials; reduce each pivot over them
-      uint32_t tc[3], tz[3], tn[3];
-      unsigned long long tm[3];
+    // every warp totals the partials (lanes 0..kWarps-1 hold one warp's each)
+    uint32_t tc[3], tz[3], tn[3];
+    unsigned long long tm[3];
 #pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        const bool own = lane < kWarps;
-        const uint32_t cw = own ? vld(F.lred[lane][j].cnt) : 0u;
-        const uint32_t zw = own ? vld(F.lred[lane][j].zmin) : 0xFFFFFFFFu;
-        const uint32_t nw = own ? vld(F.lred[lane][j].nz) : 0u;
-        const unsigned long long mw = own ? vld(F.lred[lane][j].mass) : 0ull;
-        tc[j] = __reduce_add_sync(kFull, cw);
-        tz[j] = __reduce_min_sync(kFull, zw);
-        tn[j] = __reduce_add_sync(kFull, zw == tz[j] ? nw : 0u);
-        tm[j] = MASS ? warp_sum_u64_redux(mw) : 0ull;
-      }
-      if (lane == 0) {
-        const int np = static_cast<int>(F.bc.u[BU_NP]);
-        bool reach[3], stop[3];
-        unsigned long long above[3], below[3], wz[3];
+    for (int j = 0; j < 3; ++j) {
+      const bool own = lane < kWarps;
+      const volatile LPart& pp = buf[own ? lane : 0][j];
+      const uint32_t cw = own ? pp.cnt : 0u;
+      const uint32_t zw = own ? pp.zmin : 0xFFFFFFFFu;
+      const uint32_t nw = own ? pp.nz : 0u;
+      const unsigned long long mw = (MASS && own) ? pp.mass : 0ull;
+      tc[j] = __reduce_add_sync(kFull, cw);
+      tz[j] = __reduce_min_sync(kFull, zw);
+      tn[j] = __reduce_add_sync(kFull, zw == tz[j] ? nw : 0u);
+      tm[j] = MASS ? warp_sum_u64_redux(mw) : 0ull;
+    }
+    bool reach[3], stop[3];
+    unsigned long long above[3], below[3], wz[3];
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          const uint32_t ac = tc[j] + s.c_above;
-          above[j] = MASS ? tm[j] + s.m_above : static_cast<unsigned long long>(ac);
-          wz[j] = MASS ? weight_fx(key2f(tz[j]), c.m, c.m_neginf, scale) : 1ull;
-          below[j] = above[j] - static_cast<unsigned long long>(tn[j]) * wz[j];
-          reach[j] = j < np && above[j] >= target;
-          stop[j] = reach[j] && below[j] < target;
-        }
-        const int done_j = stop[0] ? 0 : (reach[0] ? (stop[1] ? 1 : (reach[1] ? (stop[2] ? 2 : -1) : -1)) : -1);
-        const int lo_j = !reach[0] ? -1 : (!reach[1] || np < 2 ? 0 : (!reach[2] || np < 3 ? 1 : 2));
-        const int hi_j = !reach[0] ? 0 : (np < 2 ? -1 : (!reach[1] ? 1 : (np < 3 ? -1 : (!reach[2] ? 2 : -1))));
-        if (done_j >= 0) {
-          const uint32_t z = done_j == 0 ? tz[0] : (done_j == 1 ? tz[1] : tz[2]);
-          const uint32_t n = done_j == 0 ? tn[0] : (done_j == 1 ? tn[1] : tn[2]);
-          const uint32_t cabove = (done_j == 0 ? tc[0] : (done_j == 1 ? tc[1] : tc[2])) + s.c_above - n;
-          F.bc.u[BU_TAU] = z;
-          F.bc.u[BU_CABOVE] = cabove;
-          if (MASS) {
-            const unsigned long long w = done_j == 0 ? wz[0] : (done_j == 1 ? wz[1] : wz[2]);
-            const unsigned long long b = done_j == 0 ? below[0] : (done_j == 1 ? below[1] : below[2]);
-            unsigned long long k = w > 0ull ? (target - b + w - 1ull) / w : 1ull;
-            k = k < 1ull ? 1ull : (k > n ? n : k);
-            F.bc.u[BU_NKEEP] = static_cast<uint32_t>(k);
-          } else {
-            F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - cabove;
-          }
-          F.bc.u[BU_DONE] = 1;
-        } else {
-          const uint32_t old_span = F.bc.u[BU_HI] - F.bc.u[BU_LO];
-          if (lo_j >= 0) {
-            F.bc.u[BU_LO] = F.bc.q[lo_j];
-            F.bc.u[BU_CLO] = (lo_j == 0 ? tc[0] : (lo_j == 1 ? tc[1] : tc[2])) + s.c_above;
-            F.bc.x[BX_MLO] = lo_j == 0 ? above[0] : (lo_j == 1 ? above[1] : above[2]);
-          }
-          if (hi_j >= 0) {
-            F.bc.u[BU_HI] = F.bc.q[hi_j];
-            F.bc.u[BU_CHI] = (hi_j == 0 ? tc[0] : (hi_j == 1 ? tc[1] : tc[2])) + s.c_above;
-            F.bc.x[BX_MHI] = hi_j == 0 ? above[0] : (hi_j == 1 ? above[1] : above[2]);
-          }
-          const uint32_t lo = F.bc.u[BU_LO], hi = F.bc.u[BU_HI];
-          // after a value-space split that failed to halve the key range,
-          // the next round splits the key range
-          const bool bad = F.bc.u[BU_USED_VALUE] != 0u && (hi - lo) > old_span / 2u;
-          const bool vmode = value_pivots && !bad;
-          if (hi - lo <= 1u) {
-            // (lo, hi] holds one key: the boundary value is hi
-            const uint32_t c_hi = F.bc.u[BU_CHI], c_lo = F.bc.u[BU_CLO];
-            F.bc.u[BU_TAU] = hi;
-            F.bc.u[BU_CABOVE] = c_hi;
-            if (MASS) {
-              const unsigned long long w = weight_fx(key2f(hi), c.m, c.m_neginf, scale);
-              const unsigned long long m_hi = F.bc.x[BX_MHI];
-              unsigned long long k = w > 0ull ? (target - m_hi + w - 1ull) / w : 1ull;
-              const unsigned long long n = c_lo - c_hi;
-              k = k < 1ull ? 1ull : (k > n ? n : k);
-              F.bc.u[BU_NKEEP] = static_cast<uint32_t>(k);
-            } else {
-              F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - c_hi;
-            }
-            F.bc.u[BU_DONE] = 1;
-          } else if (rounds >= kMaxRounds) {
-            F.bc.u[BU_DONE] = 2;
-          } else {
-            uint32_t q0, q1, q2;
-            bool used_value = false;
-            const int np2 = quartile_pivots(lo, hi, vmode, q0, q1, q2, used_value);
-            F.bc.q[0] = q0;
-            F.bc.q[1] = q1;
-            F.bc.q[2] = q2;
-            F.bc.qf[0] = np2 > 0 ? pivot_f(q0) : INFINITY;
-            F.bc.qf[1] = np2 > 1 ? pivot_f(q1) : INFINITY;
-            F.bc.qf[2] = np2 > 2 ? pivot_f(q2) : INFINITY;
-            F.bc.u[BU_NP] = static_cast<uint32_t>(np2);
-            F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
-          }
-        }
+    for (int j = 0; j < 3; ++j) {
+      const uint32_t ac = tc[j] + s.c_above;
+      above[j] = MASS ? tm[j] + s.m_above : static_cast<unsigned long long>(ac);
+      wz[j] = MASS ? weight_fx(key2f(tz[j]), c.m, c.m_neginf, scale) : 1ull;
+      below[j] = above[j] - static_cast<unsigned long long>(tn[j]) * wz[j];
+      reach[j] = j < np && above[j] >= target;
+      stop[j] = reach[j] && below[j] < target;
+    }
+    // the first pivot (in increasing order) whose z_mn is the boundary
+    int done_j = -1;
+    if (stop[0]) done_j = 0;
+    else if (reach[0] && stop[1]) done_j = 1;
+    else if (reach[0] && reach[1] && stop[2]) done_j = 2;
+    if (done_j >= 0) {
+      const uint32_t z = done_j == 0 ? tz[0] : (done_j == 1 ? tz[1] : tz[2]);
+      const uint32_t n = done_j == 0 ? tn[0] : (done_j == 1 ? tn[1] : tn[2]);
+      tau = z;
+      cabove = (done_j == 0 ? tc[0] : (done_j == 1 ? tc[1] : tc[2])) + s.c_above - n;
+      if (MASS) {
+        const unsigned long long w = done_j == 0 ? wz[0] : (done_j == 1 ? wz[1] : wz[2]);
+        const unsigned long long b = done_j == 0 ? below[0] : (done_j == 1 ? below[1] : below[2]);
+        n_keep = copies_fx(target - b, w, n);
+      } else {
+        n_keep = static_cast<uint32_t>(target) - cabove;
       }
+      done = 1;
+      break;
     }
-    __syncthreads();
-  }
-  if (tid == 0 && F.bc.u[BU_DONE] == 3u) {
-    // the start range held one key
-    const uint32_t hi = F.bc.u[BU_HI], c_hi = F.bc.u[BU_CHI], c_lo = F.bc.u[BU_CLO];
-    F.bc.u[BU_TAU] = hi;
-    F.bc.u[BU_CABOVE] = c_hi;
-    if (MASS) {
-      const unsigned long long w = weight_fx(key2f(hi), c.m, c.m_neginf, scale);
-      unsigned long long k = w > 0ull ? (target - F.bc.x[BX_MHI] + w - 1ull) / w : 1ull;
-      const unsigned long long n = c_lo - c_hi;
-      k = k < 1ull ? 1ull : (k > n ? n : k);
-      F.bc.u[BU_NKEEP] = static_cast<uint32_t>(k);
-    } else {
-      F.bc.u[BU_NKEEP] = static_cast<uint32_t>(target) - c_hi;
+    // the highest pivot that reaches the target becomes lo, the lowest that
+    // does not becomes hi
+    const int lo_j = !reach[0] ? -1 : (!reach[1] || np < 2 ? 0 : (!reach[2] || np < 3 ? 1 : 2));
+    const int hi_j = !reach[0] ? 0 : (np < 2 ? -1 : (!reach[1] ? 1 : (np < 3 ? -1 : (!reach[2] ? 2 : -1))));
+    const uint32_t old_span = hi - lo;
+    if (lo_j >= 0) {
+      lo = lo_j == 0 ? q[0] : (lo_j == 1 ? q[1] : q[2]);
+      c_lo = (lo_j == 0 ? tc[0] : (lo_j == 1 ? tc[1] : tc[2])) + s.c_above;
+      m_lo = lo_j == 0 ? above[0] : (lo_j == 1 ? above[1] : above[2]);
     }
+    if (hi_j >= 0) {
+      hi = hi_j == 0 ? q[0] : (hi_j == 1 ? q[1] : q[2]);
+      c_hi = (hi_j == 0 ? tc[0] : (hi_j == 1 ? tc[1] : tc[2])) + s.c_above;
+      m_hi = hi_j == 0 ? above[0] : (hi_j == 1 ? above[1] : above[2]);
+    }
+    if (hi - lo <= 1u) {
+      one_key();
+      break;
+    }
+    if (rounds >= kMaxRounds) {
+      done = 2;
+      break;
+    }
+    // after a value-space split that failed to halve the key range, the next
+    // round splits the key range
+    const bool vmode = value_pivots && !(used_value && (hi - lo) > old_span / 2u);
+    np = quartile_pivots(lo, hi, vmode, q[0], q[1], q[2], used_value);
   }
-  __syncthreads();
+  (void)m_lo;
   QRITA_T(14);
-  s.tau = vld(F.bc.u[BU_TAU]);
-  s.n_keep = vld(F.bc.u[BU_NKEEP]);
-  s.count_above = vld(F.bc.u[BU_CABOVE]);
+  s.tau = tau;
+  s.n_keep = n_keep;
+  s.count_above = cabove;
   s.rounds = rounds;
-  s.capped = vld(F.bc.u[BU_DONE]) == 2u;
-  __syncthreads();
+  s.capped = done == 2;
+  __syncthreads();  // every warp has read the last round's partials
 }
 
 // Per-rank counts of gathered entries equal to tau (into F.ties).
@@ -1453,21 +1412,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     c.tail_n = c.n - c.head_n - c.body_units * E;
   }
   c.gbody = c.gx + c.head_n * S;
-  // the ring's first copies of the streaming pass fly while the sample
-  // statistics are taken (the chunk does not depend on them)
-  if (tid == 0) {
-    F.own_n = 0;
-    F.err = 0u;
-    F.err_any = 0u;
-    for (int st = 0; st < kStages; ++st) mbar_init(c.ring_bar + 8u * st, 1u);
-    fence_mbar_init();
-    const int npieces = (c.body_units + kPieceUnits - 1) / kPieceUnits;
-    for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc);
-  }
   QRITA_T(0);
-#ifdef QRITA_TRACE_TIME
-  if (tid == 0 && blockIdx.x < 65536) g_cta_times[blockIdx.x][0] = globaltimer_ns();
-#endif
 
   // ---- row parameters (uniform)
   int32_t kr = P.k ? P.k[r] : 0;
@@ -1490,6 +1435,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     constexpr int kPer = (kSampleBlocks * kSampleBlock) / kThreads;
     float sv[kPer];  // this thread's sample values (NaN: none)
     float sn = 0.f, sx = 0.f, sxx = 0.f, smax = -INFINITY;
+    float raw[kPer];
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
       const int sidx = tid + j * kThreads;
@@ -1499,9 +1445,25 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       } else {
         pos = static_cast<int64_t>(sidx / kSampleBlock) * (V / kSampleBlocks) + (sidx % kSampleBlock);
       }
+      raw[j] = pos < V ? load_elem<DT>(grow + static_cast<size_t>(pos) * S) : NAN;
+    }
+    // the ring's first copies of the streaming pass fly while the sample
+    // statistics are taken (the chunk does not depend on them); issued after
+    // the sample loads, so these are not queued behind them
+    if (tid == 0) {
+      F.own_n = 0;
+      F.err = 0u;
+      F.err_any = 0u;
+      for (int st = 0; st < kStages; ++st) mbar_init(c.ring_bar + 8u * st, 1u);
+      fence_mbar_init();
+      const int npieces = (c.body_units + kPieceUnits - 1) / kPieceUnits;
+      for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc);
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
       sv[j] = NAN;
-      if (pos < V) {
-        const float x = load_elem<DT>(grow + static_cast<size_t>(pos) * S);
+      {
+        const float x = raw[j];
         if (isfinite(x)) {
           sv[j] = x;
           sn += 1.f;
@@ -1623,31 +1585,67 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     // top-p runs alone
     auto streaming_pass = [&](auto po) {
       constexpr bool PO = decltype(po)::value;
-      stream_chunk<DT>(
+      stream_pieces<DT>(
           c,
-          [&](const float (&xs)[E], uint32_t idx0, bool valid) {
-            uint32_t bits = 0;
-            if (valid) {
-              float zu = 0.f, mu_ = 0.f;  // this unit's softmax partials (shift m_ref)
+          [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
+            float xs[kPieceThreadUnits][E];
+            uint32_t bits[kPieceThreadUnits];
+            uint32_t cnt = 0;
 #pragma unroll
-              for (int e = 0; e < E; ++e) {
-                const float x = xs[e];
-                vmax = fmax_nan(vmax, x);
-                vmin = fminf(vmin, x);
-                const bool surv = trunc && x >= t;
-                bits |= surv ? (1u << e) : 0u;
+            for (int j = 0; j < kPieceThreadUnits; ++j) {
+              unpack<DT>(v[j], xs[j]);
+              bits[j] = 0u;
+              if (j * kThreads + tid < n) {
+                float zu = 0.f, mu_ = 0.f;  // this unit's softmax partials (shift m_ref)
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                  const float x = xs[j][e];
+                  vmax = fmax_nan(vmax, x);
+                  vmin = fminf(vmin, x);
+                  const bool surv = trunc && x >= t;
+                  bits[j] |= surv ? (1u << e) : 0u;
+                  if constexpr (PO) {
+                    const float w = expf(x - m_ref);
+                    zu += w;
+                    mu_ += surv ? w : 0.f;
+                  }
+                }
                 if constexpr (PO) {
-                  const float w = expf(x - m_ref);
-                  zu += w;
-                  mu_ += surv ? w : 0.f;
+                  f2_add(zs, zu);
+                  f2_add(ms, mu_);
                 }
               }
-              if constexpr (PO) {
-                f2_add(zs, zu);
-                f2_add(ms, mu_);
+              cnt += __popc(bits[j]);
+            }
+            // this warp's survivors of the piece go to its segment at once:
+            // positions from one warp scan of the per-thread counts
+            if (__ballot_sync(kFull, cnt != 0u) == 0u) return;
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t y = __shfl_up_sync(kFull, incl, o);
+              if (lane >= o) incl += y;
+            }
+            const uint32_t tot = __shfl_sync(kFull, incl, 31);
+            uint32_t pos = wn + incl - cnt;
+            wn += tot;
+#pragma unroll
+            for (int j = 0; j < kPieceThreadUnits; ++j) {
+              uint32_t b = bits[j];
+              const uint32_t idx0 = static_cast<uint32_t>(c.head_n + (u0 + j * kThreads + tid) * E);
+              while (b != 0u) {
+                const int e = __ffs(b) - 1;
+                b &= b - 1u;
+                float x = xs[j][0];
+#pragma unroll
+                for (int q = 1; q < E; ++q) x = (q == e) ? xs[j][q] : x;
+                if (pos < segcap) {
+                  c.own_val[seg_base + pos] = x;
+                  c.own_idx[seg_base + pos] = idx0 + static_cast<uint32_t>(e);
+                }
+                ++pos;
               }
             }
-            if (trunc) seg_append<E>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx0, bits);
           },
           [&](float x, uint32_t idx, bool valid) {
             uint32_t bits = 0;
@@ -1810,7 +1808,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         k_full = true;
         list_emit = true;
         ties_in_list = true;
-        local_search<DT, false>(c, s, target, value_pivots, nullptr);
+        local_search<DT, false>(c, s, target, value_pivots);
       } else {
         // narrow: over the survivor lists on a hit, over the chunk otherwise
         Range R;
@@ -1875,7 +1873,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           k_full = R.c_hi == 0u;  // nothing lies above the gathered range
           list_emit = hit;
           ties_in_list = true;
-          local_search<DT, false>(c, s, target, value_pivots, nullptr);
+          local_search<DT, false>(c, s, target, value_pivots);
         }
       }
       rounds_k = static_cast<uint32_t>(s.rounds);
@@ -1922,11 +1920,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           acc += x > tk ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
         }
         acc = warp_sum_u64_redux(acc);
-        if (lane == 0) F.lred[warp][0].mass = acc;
+        if (lane == 0) F.lred[0][warp][0].mass = acc;
         __syncthreads();
         if (tid == 0) {
           unsigned long long a = 0ull;
-          for (int w = 0; w < kWarps; ++w) a += vld(F.lred[w][0].mass);
+          for (int w = 0; w < kWarps; ++w) a += vld(F.lred[0][w][0].mass);
           F.bc.x[BX_TARGET] = a;
         }
         __syncthreads();
@@ -1955,7 +1953,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           s.m_hi = 0ull;
           s.c_above = 0;
           s.m_above = 0ull;
-          local_search<DT, true>(c, s, target, value_pivots, nullptr);
+          local_search<DT, true>(c, s, target, value_pivots);
           rounds_p = static_cast<uint32_t>(s.rounds);
           if (s.capped) {
             sel_none = true;
@@ -1992,7 +1990,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           s.m_hi = 0ull;
           list_emit = true;
           ties_in_list = true;
-          local_search<DT, true>(c, s, f2_to_u64(f2_mul(f2_mul(Zm, pr), scale)), value_pivots, nullptr);
+          local_search<DT, true>(c, s, f2_to_u64(f2_mul(f2_mul(Zm, pr), scale)), value_pivots);
         } else {
           // narrow by mass in fixed point (shift m); a pass over the chunk
           // measures the denominator (Z, or mass(> tau_k) for S_k) itself
@@ -2067,7 +2065,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             s.m_above = R.m_hi;
             list_emit = hit;
             ties_in_list = true;
-            local_search<DT, true>(c, s, target, value_pivots, nullptr);
+            local_search<DT, true>(c, s, target, value_pivots);
           }
         }
         rounds_p = static_cast<uint32_t>(s.rounds);
@@ -2230,9 +2228,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     sel_none = true;
     sel_all = false;
   }
-#ifdef QRITA_TRACE_TIME
-  if (tid == 0 && blockIdx.x < 65536) g_cta_times[blockIdx.x][1] = globaltimer_ns();
-#endif
+  QRITA_T(15);
 
   // ---- row outputs (rank 0)
   if (c.crank == 0 && tid == 0) {
@@ -2282,13 +2278,10 @@ int max_smem_per_block() {
 }
 
 #ifdef QRITA_TRACE_TIME
-extern "C" int qrita_debug_times(unsigned long long* out) {
+extern "C" int qrita_debug_stages(unsigned long long* out, int n) {
   cudaDeviceSynchronize();
-  return static_cast<int>(cudaMemcpyFromSymbol(out, g_times, sizeof(g_times)));
-}
-extern "C" int qrita_debug_cta_times(unsigned long long* out, int n) {
-  cudaDeviceSynchronize();
-  return static_cast<int>(cudaMemcpyFromSymbol(out, g_cta_times, sizeof(unsigned long long) * 2 * n));
+  if (n > kTraceCtas) n = kTraceCtas;
+  return static_cast<int>(cudaMemcpyFromSymbol(out, g_cta_stage, sizeof(unsigned long long) * 16 * n));
 }
 #endif
 
