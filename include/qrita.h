@@ -71,15 +71,19 @@ enum {
   QRITA_ROW_NONFINITE = 1,  /* NaN or +inf in the row: mask all zero */
   QRITA_ROW_SEARCH_CAP = 2, /* pivot search exceeded its round cap: mask all zero
                                (cannot happen by construction; kept as a guard) */
-  QRITA_ROW_TIMEOUT = 3     /* reserved for a bounded wait that gives up; this
-                               build has no such wait and never reports it */
+  QRITA_ROW_TIMEOUT = 3     /* a bounded wait for a bulk copy of the row's logits
+                               gave up (not expected on a healthy device): mask
+                               all zero */
 };
 
 /* Flags of qrita_select_ex (path forcing for tests and ablations). */
 #define QRITA_FLAG_NO_TRUNCATION 0x1u  /* skip sigma-truncation: search the full row */
-#define QRITA_FLAG_FORCE_FALLBACK 0x2u /* treat every truncation as a miss */
+#define QRITA_FLAG_FORCE_FALLBACK 0x2u /* treat every truncation as a miss and search
+                                          the full row (no second truncation) */
 #define QRITA_FLAG_KEY_PIVOTS 0x4u     /* pivots at quartiles of the 32-bit key range
                                           only (no value-space quartiles) */
+#define QRITA_FLAG_FORCE_RETRY 0x8u    /* top-k rows: treat the first truncation as a
+                                          miss, so the second truncation runs */
 #define QRITA_FLAG_CLUSTER_SHIFT 8     /* bits 8..10: force 2^n CTAs per row (n in 0..4);
                                           0 in these bits and bit 11 clear = automatic */
 #define QRITA_FLAG_CLUSTER_SET 0x800u  /* bit 11: the cluster-size bits are set */
@@ -93,6 +97,9 @@ enum {
 #define QRITA_PATH_FALLBACK 0x10u /* the search ran on the full row */
 #define QRITA_PATH_OVERFLOW 0x20u /* Z_t did not fit a CTA's shared-memory list */
 #define QRITA_PATH_KEEP_ALL 0x40u /* both filters off: every token kept */
+#define QRITA_PATH_RETRY 0x80u    /* top-k: a second truncation at an order statistic
+                                     of a 4096-logit sample ran (the search ran on
+                                     its survivors unless FALLBACK is also set) */
 
 /* Diagnostics of one row (qrita_select_ex, optional). Device memory. */
 typedef struct qrita_row_info {

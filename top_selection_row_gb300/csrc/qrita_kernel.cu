@@ -4,21 +4,25 @@
 // "Methodology" parts 1-2 and "Implementation details" (pipeline).
 //
 // One thread-block cluster of C CTAs handles one row; CTA c owns a contiguous
-// chunk of the row. The row is streamed from HBM once:
+// chunk of the row. The row is read from HBM once, through a shared-memory
+// ring of 1-D bulk copies (TMA) whose first stages fly while A2 runs:
 //
 //   A2  mu, sigma (and a reference max) from one sample block of the row,
 //       read identically by every CTA of the cluster (no exchange needed);
+//       sigma is re-estimated without the sample's outliers;
 //   A3  delta from the normal-quantile tables, t = mu + delta * sigma;
 //   A4  one streaming pass over the chunk keeps Z_t = {x >= t} (value and
-//       index) in a shared-memory list, and tracks max / min / NaN / +inf and,
-//       for top-p without top-k, the softmax mass of the row and of Z_t;
+//       index) in per-warp segments of a shared-memory list, and tracks
+//       max / min / NaN / +inf and, for top-p without top-k, the softmax mass
+//       of the row and of Z_t;
 //   --  one cluster merge through distributed shared memory;
 //   A5  hit: every CTA gathers the whole Z_t into its shared memory;
 //       fallback (miss, or too many candidates): distributed narrowing passes
 //       evaluate two quaternary levels (15 pivots) per cluster merge until the
 //       range that holds the boundary fits, then that range is gathered;
 //   A6  quaternary pivot search over the gathered candidates with
-//       z_mn / N_zmn duplicate tracking, inside each CTA (block barriers only);
+//       z_mn / N_zmn duplicate tracking, inside each CTA (one block barrier
+//       per round);
 //   A7  the same search by softmax mass for top-p;
 //   A8  boundary duplicates kept by lowest token id: per-rank counts from the
 //       gathered set, then an index cut inside the one straddling CTA;
@@ -49,6 +53,11 @@ constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kSampleBlocks = 16;
 constexpr int kSampleBlock = 64;  // 16 x 64 = 1024 sampled logits per row
 constexpr float kClipSigmas = 4.0f;  // sample values beyond this many sigmas are outliers
+// Second truncation (top-k rows whose first threshold missed or overflowed):
+// the threshold is an order statistic of a larger sample of the row.
+constexpr int kRetryBlocks = 64;
+constexpr int kRetrySample = kRetryBlocks * 64;  // 4096 logits
+constexpr int kRetryPer = kRetrySample / kThreads;
 // Streaming ring: the chunk moves through shared memory in pieces of
 // kPieceBytes by 1-D bulk copies (TMA), kStages pieces in flight.
 constexpr int kStages = 2;
@@ -214,7 +223,8 @@ enum : int {
   BF_MU = 0, BF_SIGMA, BF_MREF, BF_T, BF_MAX, BF_MIN, BF_LOF, BF_HIF,
   // uints
   BU_TRUNC = 0, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
-  BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS,
+  BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS, BU_S2, BU_OVF2,
+  BU_QKEY, BU_QWANT,
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
   // float pairs
@@ -589,6 +599,48 @@ __device__ __forceinline__ void stream_chunk(Ctx<DT>& c, UnitFn&& unit_fn, Scala
         }
       },
       scalar_fn, prefetched);
+}
+
+// The survivors of one ring piece (bits[j]: the elements of this thread's unit
+// j that survive) to this warp's segment of the own list: positions from one
+// warp scan of the per-thread counts. wn is the warp's running count
+// (warp-uniform), which keeps counting past segcap.
+template <int DT>
+__device__ __forceinline__ void append_piece(Ctx<DT>& c, uint32_t& wn, uint32_t seg_base, uint32_t segcap,
+                                             const float (&xs)[kPieceThreadUnits][Ctx<DT>::E],
+                                             const uint32_t (&bits)[kPieceThreadUnits], int u0) {
+  constexpr int E = Ctx<DT>::E;
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int j = 0; j < kPieceThreadUnits; ++j) cnt += __popc(bits[j]);
+  if (__ballot_sync(kFull, cnt != 0u) == 0u) return;
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t tot = __shfl_sync(kFull, incl, 31);
+  uint32_t pos = wn + incl - cnt;
+  wn += tot;
+#pragma unroll
+  for (int j = 0; j < kPieceThreadUnits; ++j) {
+    uint32_t b = bits[j];
+    const uint32_t idx0 = static_cast<uint32_t>(c.head_n + (u0 + j * kThreads + tid) * E);
+    while (b != 0u) {
+      const int e = __ffs(b) - 1;
+      b &= b - 1u;
+      float x = xs[j][0];
+#pragma unroll
+      for (int q = 1; q < E; ++q) x = (q == e) ? xs[j][q] : x;
+      if (pos < segcap) {
+        c.own_val[seg_base + pos] = x;
+        c.own_idx[seg_base + pos] = idx0 + static_cast<uint32_t>(e);
+      }
+      ++pos;
+    }
+  }
 }
 
 // After a wait gave up: wait (bounded) for every copy still in flight into
@@ -1097,6 +1149,142 @@ __device__ void compact_segments(Ctx<DT>& c, uint32_t wn) {
   __syncthreads();
 }
 
+// Position of sample element sidx of an n-element sample spread as blocks of
+// 64 contiguous logits over the row (the whole row when V <= n).
+__device__ __forceinline__ int64_t sample_pos(int sidx, int n, int V) {
+  if (V <= n) return sidx;
+  const int blocks = n / 64;
+  return static_cast<int64_t>(sidx / 64) * (V / blocks) + (sidx % 64);
+}
+
+// Key of the j-th largest (1-based) of the kRetrySample sample logits of the
+// row (of the whole row when V <= kRetrySample), by an MSB-first radix select
+// with 8-bit digits; the histogram lives in the ring's bytes (no stream is in
+// flight). Every thread returns the same key.
+template <int DT>
+__device__ uint32_t sample_order_key(Ctx<DT>& c, const unsigned char* grow, int V, uint32_t j) {
+  constexpr int S = Ctx<DT>::S;
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr));  // 256 bins
+  uint32_t key[kRetryPer];
+  bool have[kRetryPer];
+#pragma unroll
+  for (int q = 0; q < kRetryPer; ++q) {
+    const int sidx = tid + q * kThreads;
+    const int64_t pos = sample_pos(sidx, kRetrySample, V);
+    have[q] = pos < V;
+    key[q] = have[q] ? f2key(load_elem<DT>(grow + static_cast<size_t>(pos) * S)) : 0u;
+  }
+  uint32_t prefix = 0, mask = 0, want = j;
+  __syncthreads();  // earlier users of the ring's bytes are done
+  for (int d = 3; d >= 0; --d) {
+    hist[tid] = 0u;  // kThreads == 256 bins
+    __syncthreads();
+    const int sh = 8 * d;
+#pragma unroll
+    for (int q = 0; q < kRetryPer; ++q)
+      if (have[q] && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> sh) & 255u], 1u);
+    __syncthreads();
+    if (tid < 32) {
+      // lane l holds bins 255 - 8l .. 248 - 8l (from the top)
+      uint32_t b8[8], sum = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        b8[q] = vld(hist[255 - 8 * lane - q]);
+        sum += b8[q];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const uint32_t excl = incl - sum;
+      const bool here = excl < want && want <= incl;
+      if (here) {
+        uint32_t acc = excl;
+        int bin = 255 - 8 * lane - 7;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (acc < want && want <= acc + b8[q]) {
+            bin = 255 - 8 * lane - q;
+            want -= acc;
+          }
+          acc += b8[q];
+        }
+        F.bc.u[BU_QKEY] = static_cast<uint32_t>(bin);
+        F.bc.u[BU_QWANT] = want;
+      }
+    }
+    __syncthreads();
+    prefix |= vld(F.bc.u[BU_QKEY]) << sh;
+    mask |= 255u << sh;
+    want = vld(F.bc.u[BU_QWANT]);
+    __syncthreads();
+  }
+  return prefix;
+}
+
+// Survivors (x >= t2) of the chunk into the warps' segments of the own list,
+// compacted; then one cluster merge of the counts: F.rank_n, F.bc.u[BU_S2]
+// (row survivors) and F.bc.u[BU_OVF2] (some list overflowed).
+template <int DT>
+__device__ void retry_pass(Ctx<DT>& c, float t2) {
+  constexpr int E = Ctx<DT>::E;
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t segcap = c.ocap / kWarps;
+  const uint32_t seg_base = static_cast<uint32_t>(warp) * segcap;
+  uint32_t wn = 0;
+  stream_pieces<DT>(
+      c,
+      [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
+        float xs[kPieceThreadUnits][E];
+        uint32_t bits[kPieceThreadUnits];
+#pragma unroll
+        for (int j = 0; j < kPieceThreadUnits; ++j) {
+          unpack<DT>(v[j], xs[j]);
+          bits[j] = 0u;
+          if (j * kThreads + tid < n) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) bits[j] |= (xs[j][e] >= t2) ? (1u << e) : 0u;
+          }
+        }
+        append_piece<DT>(c, wn, seg_base, segcap, xs, bits, u0);
+      },
+      [&](float x, uint32_t idx, bool valid) {
+        const float xs[1] = {x};
+        seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, (valid && x >= t2) ? 1u : 0u);
+      },
+      false);
+  compact_segments<DT>(c, wn);
+  Slot& my = F.slots[c.ph & 1];
+  if (tid == 0) {
+    my.u[0] = vld(F.seg_ovf);
+    my.u[1] = vld(F.own_n);
+  }
+  cluster_sync_all();
+  if (warp == 0) {
+    uint32_t n = 0, o = 0;
+    if (lane < static_cast<int>(c.C)) {
+      const uint32_t ub = map_rank(smem_u32(&my.u[0]), lane);
+      o = ld_dsmem_u32(ub);
+      n = ld_dsmem_u32(ub + 4);
+      o |= n > c.ocap ? 1u : 0u;
+      F.rank_n[lane] = n;
+    }
+    n = __reduce_add_sync(kFull, n);
+    o = __reduce_or_sync(kFull, o);
+    if (lane == 0) {
+      F.bc.u[BU_S2] = n;
+      F.bc.u[BU_OVF2] = o;
+    }
+  }
+  __syncthreads();
+  ++c.ph;
+}
+
 // ---------------------------------------------------------------------------
 // Local quaternary search over the gathered set (block barriers only)
 // ---------------------------------------------------------------------------
@@ -1590,7 +1778,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
             float xs[kPieceThreadUnits][E];
             uint32_t bits[kPieceThreadUnits];
-            uint32_t cnt = 0;
 #pragma unroll
             for (int j = 0; j < kPieceThreadUnits; ++j) {
               unpack<DT>(v[j], xs[j]);
@@ -1615,37 +1802,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   f2_add(ms, mu_);
                 }
               }
-              cnt += __popc(bits[j]);
             }
-            // this warp's survivors of the piece go to its segment at once:
-            // positions from one warp scan of the per-thread counts
-            if (__ballot_sync(kFull, cnt != 0u) == 0u) return;
-            uint32_t incl = cnt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-              const uint32_t y = __shfl_up_sync(kFull, incl, o);
-              if (lane >= o) incl += y;
-            }
-            const uint32_t tot = __shfl_sync(kFull, incl, 31);
-            uint32_t pos = wn + incl - cnt;
-            wn += tot;
-#pragma unroll
-            for (int j = 0; j < kPieceThreadUnits; ++j) {
-              uint32_t b = bits[j];
-              const uint32_t idx0 = static_cast<uint32_t>(c.head_n + (u0 + j * kThreads + tid) * E);
-              while (b != 0u) {
-                const int e = __ffs(b) - 1;
-                b &= b - 1u;
-                float x = xs[j][0];
-#pragma unroll
-                for (int q = 1; q < E; ++q) x = (q == e) ? xs[j][q] : x;
-                if (pos < segcap) {
-                  c.own_val[seg_base + pos] = x;
-                  c.own_idx[seg_base + pos] = idx0 + static_cast<uint32_t>(e);
-                }
-                ++pos;
-              }
-            }
+            append_piece<DT>(c, wn, seg_base, segcap, xs, bits, u0);
           },
           [&](float x, uint32_t idx, bool valid) {
             uint32_t bits = 0;
@@ -1766,6 +1924,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   (trunc ? QRITA_PATH_TRUNC : 0u) | (overflow ? QRITA_PATH_OVERFLOW : 0u) |
                   (keep_all ? QRITA_PATH_KEEP_ALL : 0u);
   const bool force_fb = (P.flags & QRITA_FLAG_FORCE_FALLBACK) != 0u;
+  const bool force_retry = (P.flags & QRITA_FLAG_FORCE_RETRY) != 0u;
   const bool value_pivots = (P.flags & QRITA_FLAG_KEY_PIVOTS) == 0u;
 
   // Selection: keep key > tau, plus the n_keep lowest-id elements equal to
@@ -1791,14 +1950,55 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     uint32_t tau_k = 0, nk_k = 0, above_k = 0;
     if (k_on) {
       const uint32_t target = static_cast<uint32_t>(kr);
-      const bool hit = trunc && !overflow && !force_fb && survivors >= target;
-      path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
+      const bool hit = trunc && !overflow && !force_fb && !force_retry && survivors >= target;
+      if (hit) path |= QRITA_PATH_HIT;
       Local s;
       s.c_above = 0;
       s.m_above = 0ull;
       s.m_lo = s.m_hi = 0ull;
       bool have_exact = false;
-      if (hit && survivors <= c.gcap) {
+      // second truncation: when the first threshold missed (or left too many
+      // candidates), an order statistic of a larger sample of the row whose
+      // expected survivors fit the gathered set
+      bool retried = false;
+      uint32_t qk = 0, S2 = 0;
+      bool ovf2 = true;
+      if (!hit && !force_fb) {
+        const int n_s = V < kRetrySample ? V : kRetrySample;
+        uint32_t jq;
+        if (V <= kRetrySample) {
+          jq = target;  // the sample is the row: t2 is the k-th logit itself
+        } else {
+          const float lam = static_cast<float>(target) * static_cast<float>(n_s) / static_cast<float>(V);
+          jq = static_cast<uint32_t>(ceilf(lam + 4.0f * sqrtf(lam) + 4.0f));
+        }
+        const float expect = static_cast<float>(jq) * static_cast<float>(V) / static_cast<float>(n_s);
+        if (jq <= static_cast<uint32_t>(n_s) && expect <= 0.7f * static_cast<float>(c.gcap) &&
+            expect <= 0.7f * static_cast<float>(c.ocap) * static_cast<float>(c.C)) {
+          path |= QRITA_PATH_RETRY;
+          qk = sample_order_key<DT>(c, grow, V, jq);
+          retry_pass<DT>(c, key2f(qk));
+          S2 = vld(F.bc.u[BU_S2]);
+          ovf2 = vld(F.bc.u[BU_OVF2]) != 0u;
+          if (!ovf2 && S2 >= target && S2 <= c.gcap) {
+            // gather Z_t2 whole: the candidates are (key(t2) - 1, max]
+            gather_all<DT>(c);
+            s.lo = qk - 1u;
+            s.c_lo = S2;
+            s.hi = f2key(row_max);
+            s.c_hi = 0;
+            k_full = true;
+            list_emit = true;
+            ties_in_list = true;
+            local_search<DT, false>(c, s, target, value_pivots);
+            retried = true;
+          }
+        }
+      }
+      if (!hit && !retried) path |= QRITA_PATH_FALLBACK;
+      if (retried) {
+        // the search above ran on Z_t2
+      } else if (hit && survivors <= c.gcap) {
         // gather Z_t whole: the candidates are (key(t) - 1, max]
         gather_all<DT>(c);
         s.lo = f2key(t) - 1u;
@@ -1827,8 +2027,17 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           R.lo = f2key(row_min) - 1u;
           R.c_lo = static_cast<uint32_t>(V);
           const bool miss_t = trunc && !overflow && survivors < target;
-          R.hi = (!R.pin_hi && miss_t) ? f2key(t) - 1u : f2key(row_max);
-          R.c_hi = (!R.pin_hi && miss_t) ? survivors : 0u;
+          const bool miss_t2 = !ovf2 && S2 < target;  // the second threshold missed too
+          R.hi = f2key(row_max);
+          R.c_hi = 0u;
+          if (miss_t) {
+            R.hi = f2key(t) - 1u;
+            R.c_hi = survivors;
+          }
+          if (miss_t2 && S2 >= R.c_hi) {
+            R.hi = qk - 1u;
+            R.c_hi = S2;
+          }
         }
         R.lo_all = R.lo < kKeyNegInf;
         narrow<DT, false>(c, R, !hit);
