@@ -912,6 +912,262 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok
   *used_value_out = vld(F.bc.u[BU_USED_VALUE]) != 0u;
 }
 
+// ---------------------------------------------------------------------------
+// Wide narrowing pass: four quaternary levels at once. The range (lo, hi] is
+// cut into 256 equal value bins (255 pivots); one pass over the chunk counts
+// (and weighs) every bin with per-warp shared-memory histograms, one cluster
+// merge totals them, and the bin holding the boundary becomes the range.
+// List-region layout while it runs: per-warp counts and masses at 0 (24 KiB),
+// pivot floats at kWideQfOff, the CTA's bin totals for the cluster at
+// kWideTotOff (clear of the narrowing bins and of the ring; remote CTAs read
+// them before the next cluster barrier, and nothing writes there before it).
+// ---------------------------------------------------------------------------
+constexpr int kWideBins = 256;
+static_assert(kWideBins == kThreads, "one thread per wide bin");
+constexpr int kWideQfOff = 24 * 1024;
+constexpr int kWideTotOff = 48 * 1024;
+static_assert(kWarps * kWideBins * 12 <= kWideQfOff, "wide histograms overlap the pivots");
+static_assert(kWideTotOff >= kBinBytes, "wide totals overlap the narrowing bins");
+
+// Block-wide inclusive suffix sum over the 256 bins (thread b holds bin b):
+// returns the sum of bins b..255 (u64; counts fit, masses are below 2^63).
+template <int DT>
+__device__ __forceinline__ unsigned long long bin_suffix_sum(Ctx<DT>& c, unsigned long long v) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // reverse order: prefix over r = 255 - b; warp w' = kWarps-1-warp holds r's block
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_down_sync(kFull, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  // incl = sum of lanes lane..31 of this warp; add the warps above
+  if (lane == 0) {
+    F.redu[warp][0] = static_cast<uint32_t>(incl);
+    F.redu[warp][1] = static_cast<uint32_t>(incl >> 32);
+  }
+  __syncthreads();
+  unsigned long long above = 0ull;
+  for (int w = warp + 1; w < kWarps; ++w)
+    above += static_cast<unsigned long long>(vld(F.redu[w][0])) |
+             (static_cast<unsigned long long>(vld(F.redu[w][1])) << 32);
+  __syncthreads();
+  return incl + above;
+}
+
+template <int DT, bool MASS>
+__device__ bool wide_pass(Ctx<DT>& c, Range& R) {
+  constexpr int E = Ctx<DT>::E;
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (R.lo_all) return false;
+  const float lo_v = pivot_f(R.lo);
+  const float hi_v = pivot_f(R.hi);
+  if (!isfinite(lo_v) || !isfinite(hi_v) || !(hi_v > lo_v)) return false;
+  const float w = (hi_v - lo_v) * (1.0f / kWideBins);
+  const float inv_w = 1.0f / w;
+  if (!(w > 0.f) || !isfinite(inv_w)) return false;
+  // pivots q_b = lo + (b + 1) w (b < 255), q_255 = hi: must increase strictly
+  const float q_prev = tid == 0 ? lo_v : fmaf(static_cast<float>(tid), w, lo_v);
+  const float q_mine = tid == kWideBins - 1 ? hi_v : fmaf(static_cast<float>(tid + 1), w, lo_v);
+  if (__syncthreads_or(!(q_mine > q_prev)) != 0) return false;
+
+  uint32_t* wcnt = reinterpret_cast<uint32_t*>(c.lists);  // [kWarps][256]
+  unsigned long long* wmass =
+      reinterpret_cast<unsigned long long*>(c.lists + kWarps * kWideBins * 4);  // [kWarps][256]
+  float* qf = reinterpret_cast<float*>(c.lists + kWideQfOff);
+  uint32_t* tot_cnt = reinterpret_cast<uint32_t*>(c.lists + kWideTotOff);  // [257]
+  unsigned long long* tot_mass =
+      reinterpret_cast<unsigned long long*>(c.lists + kWideTotOff + 2048);  // [257]
+  for (int wv = 0; wv < kWarps; ++wv) {
+    wcnt[wv * kWideBins + tid] = 0u;
+    if (MASS) wmass[wv * kWideBins + tid] = 0ull;
+  }
+  qf[tid] = q_mine;
+  __syncthreads();
+  const float scale = c.fix_scale;
+  uint32_t above_c = 0;
+  unsigned long long above_m = 0ull;
+  auto bin_one = [&](float x) {
+    if (!(x > lo_v)) return;
+    unsigned long long wf = 0ull;
+    if (MASS) wf = __float2ull_rn(weight(x, c.m, c.m_neginf) * scale);
+    if (x > hi_v) {
+      ++above_c;
+      above_m += wf;
+      return;
+    }
+    int b = static_cast<int>((x - lo_v) * inv_w);
+    b = b < 0 ? 0 : (b > kWideBins - 1 ? kWideBins - 1 : b);
+    // the estimate is within a bin of the truth: settle it on the pivots
+    if (b > 0 && x <= qf[b - 1]) --b;
+    if (b > 0 && x <= qf[b - 1]) --b;
+    if (b < kWideBins - 1 && x > qf[b]) ++b;
+    if (b < kWideBins - 1 && x > qf[b]) ++b;
+    atomicAdd(&wcnt[warp * kWideBins + b], 1u);
+    if (MASS) atomicAdd(&wmass[warp * kWideBins + b], wf);
+  };
+  stream_chunk<DT>(
+      c,
+      [&](const float (&xs)[E], uint32_t, bool valid) {
+        if (!valid) return;
+#pragma unroll
+        for (int e = 0; e < E; ++e) bin_one(xs[e]);
+      },
+      [&](float x, uint32_t, bool valid) {
+        if (valid) bin_one(x);
+      });
+  above_c = __reduce_add_sync(kFull, above_c);
+  above_m = warp_sum_u64(above_m);
+  if (lane == 0) {
+    F.redu[warp][2] = above_c;
+    F.redu[warp][3] = static_cast<uint32_t>(above_m);
+    F.redu[warp][4] = static_cast<uint32_t>(above_m >> 32);
+  }
+  __syncthreads();
+  {
+    uint32_t cb = 0;
+    unsigned long long mb = 0ull;
+    for (int wv = 0; wv < kWarps; ++wv) {
+      cb += vld(wcnt[wv * kWideBins + tid]);
+      if (MASS) mb += vld(wmass[wv * kWideBins + tid]);
+    }
+    tot_cnt[tid] = cb;
+    tot_mass[tid] = mb;
+    if (tid == 0) {
+      uint32_t ac = 0;
+      unsigned long long am = 0ull;
+      for (int wv = 0; wv < kWarps; ++wv) {
+        ac += vld(F.redu[wv][2]);
+        am += static_cast<unsigned long long>(vld(F.redu[wv][3])) |
+              (static_cast<unsigned long long>(vld(F.redu[wv][4])) << 32);
+      }
+      tot_cnt[kWideBins] = ac;
+      tot_mass[kWideBins] = am;
+    }
+  }
+  cluster_sync_all();
+  // row totals of bin tid, and above hi
+  uint32_t rc = 0;
+  unsigned long long rm = 0ull;
+  for (uint32_t r = 0; r < c.C; ++r) {
+    rc += ld_dsmem_u32(map_rank(smem_u32(&tot_cnt[tid]), r));
+    if (MASS) {
+      const uint32_t a = map_rank(smem_u32(&tot_mass[tid]), r);
+      rm += static_cast<unsigned long long>(ld_dsmem_u32(a)) |
+            (static_cast<unsigned long long>(ld_dsmem_u32(a + 4)) << 32);
+    }
+  }
+  uint32_t ac = 0;
+  unsigned long long am = 0ull;
+  for (uint32_t r = 0; r < c.C; ++r) {
+    ac += ld_dsmem_u32(map_rank(smem_u32(&tot_cnt[kWideBins]), r));
+    if (MASS) {
+      const uint32_t a = map_rank(smem_u32(&tot_mass[kWideBins]), r);
+      am += static_cast<unsigned long long>(ld_dsmem_u32(a)) |
+            (static_cast<unsigned long long>(ld_dsmem_u32(a + 4)) << 32);
+    }
+  }
+  // count / mass above the lower edge of bin tid (bins tid..255, and above hi)
+  const unsigned long long sc = bin_suffix_sum(c, rc) + ac;
+  const unsigned long long sm = MASS ? bin_suffix_sum(c, rm) + am : 0ull;
+  // the target (measured here when it is a share of this pass's total)
+  unsigned long long tgt = R.target;
+  if (R.target_from_total) {
+    if (tid == 0) {
+      F.bc.x[BX_TARGET] = f2_to_u64(f2_mul(f2_from_u64(sm + R.extra), R.p_frac));
+    }
+    __syncthreads();
+    tgt = vld(F.bc.x[BX_TARGET]);
+  }
+  // bin b holds the boundary when above(lower edge of b) reaches the target
+  // and above(upper edge) does not: the upper edge's "above" is bin b+1's
+  const unsigned long long my_above = MASS ? sm : sc;
+  const unsigned long long nxt = __shfl_down_sync(kFull, my_above, 1);
+  // above(upper edge of bin b) for lane 31 comes from the next warp's lane 0
+  if (lane == 0) {
+    F.redu[warp][5] = static_cast<uint32_t>(my_above);
+    F.redu[warp][6] = static_cast<uint32_t>(my_above >> 32);
+    F.redu[warp][7] = static_cast<uint32_t>(sc);
+  }
+  __syncthreads();
+  unsigned long long up = nxt;
+  uint32_t up_c = __shfl_down_sync(kFull, static_cast<uint32_t>(sc), 1);
+  if (lane == 31) {
+    if (warp + 1 < kWarps) {
+      up = static_cast<unsigned long long>(vld(F.redu[warp + 1][5])) |
+           (static_cast<unsigned long long>(vld(F.redu[warp + 1][6])) << 32);
+      up_c = vld(F.redu[warp + 1][7]);
+    } else {
+      up = MASS ? am : ac;
+      up_c = ac;
+    }
+  }
+  const bool below = tid == 0 && my_above < tgt;
+  const bool here = my_above >= tgt && up < tgt;
+  // (lo, hi] held the boundary on entry, so one bin claims it (or "below");
+  // should none, the range stays and the next pass narrows it
+  const bool claimed = __syncthreads_or(here || below) != 0;
+  if (!claimed && tid == 0) {
+    F.bc.u[BU_LO] = R.lo;
+    F.bc.u[BU_HI] = R.hi;
+    F.bc.u[BU_CLO] = R.c_lo;
+    F.bc.u[BU_CHI] = R.c_hi;
+    F.bc.x[BX_MLO] = R.m_lo;
+    F.bc.x[BX_MHI] = R.m_hi;
+    F.bc.u[BU_MAXR] = 0xFFFFFFFFu;
+  }
+  if (here) {
+    F.bc.u[BU_LO] = tid == 0 ? R.lo : f2key(qf[tid - 1]);
+    F.bc.u[BU_HI] = tid == kWideBins - 1 ? R.hi : f2key(qf[tid]);
+    F.bc.u[BU_CLO] = static_cast<uint32_t>(sc);
+    F.bc.u[BU_CHI] = up_c;
+    F.bc.x[BX_MLO] = MASS ? sm : 0ull;
+    F.bc.x[BX_MHI] = MASS ? up : 0ull;
+    // per-rank counts inside the bin (differences are what the callers use)
+    uint32_t maxr = 0;
+    for (uint32_t r = 0; r < c.C; ++r) {
+      const uint32_t n = ld_dsmem_u32(map_rank(smem_u32(&tot_cnt[tid]), r));
+      F.rank_lo[r] = n;
+      F.rank_hi[r] = 0u;
+      maxr = n > maxr ? n : maxr;
+    }
+    F.bc.u[BU_MAXR] = maxr;
+  }
+  if (tid == 0) {
+    F.bc.u[BU_BELOW] = below ? 1u : 0u;
+    F.bc.x[BX_TARGET] = tgt;
+  }
+  if (tid == 0 && below) {
+    // nothing narrows: keep the range, report "below"
+    F.bc.u[BU_LO] = R.lo;
+    F.bc.u[BU_HI] = R.hi;
+    F.bc.u[BU_CLO] = static_cast<uint32_t>(sc);
+    F.bc.u[BU_CHI] = R.c_hi;
+    F.bc.x[BX_MLO] = MASS ? sm : 0ull;
+    F.bc.x[BX_MHI] = R.m_hi;
+    F.bc.u[BU_MAXR] = 0xFFFFFFFFu;
+  }
+  __syncthreads();
+  R.target = vld(F.bc.x[BX_TARGET]);
+  R.target_from_total = false;
+  R.lo = vld(F.bc.u[BU_LO]);
+  R.hi = vld(F.bc.u[BU_HI]);
+  R.c_lo = vld(F.bc.u[BU_CLO]);
+  R.c_hi = vld(F.bc.u[BU_CHI]);
+  R.m_lo = vld(F.bc.x[BX_MLO]);
+  R.m_hi = vld(F.bc.x[BX_MHI]);
+  R.lo_all = R.lo < kKeyNegInf;
+  R.below = vld(F.bc.u[BU_BELOW]) != 0u;
+  const uint32_t maxr = vld(F.bc.u[BU_MAXR]);
+  R.fits = !R.below && (R.c_lo - R.c_hi) <= c.gcap && maxr <= c.ocap;
+  R.exact = !R.below && (R.hi - R.lo <= 1u);
+  ++R.passes;
+  cluster_sync_all();  // every CTA is done reading the others' bin totals
+  return true;
+}
+
 template <int DT, bool MASS>
 __device__ void narrow(Ctx<DT>& c, Range& R, bool from_chunk) {
   bool value_ok = true;
@@ -919,10 +1175,16 @@ __device__ void narrow(Ctx<DT>& c, Range& R, bool from_chunk) {
   R.fits = false;
   R.exact = false;
   R.below = false;
+  bool wide_done = false;
   while (true) {
     const uint32_t span_before = R.hi - R.lo;
     bool used_value = false;
-    narrow_pass<DT, MASS>(c, R, from_chunk, value_ok, &used_value);
+    if (from_chunk && !wide_done && wide_pass<DT, MASS>(c, R)) {
+      wide_done = true;
+      used_value = true;
+    } else {
+      narrow_pass<DT, MASS>(c, R, from_chunk, value_ok, &used_value);
+    }
     if (R.below || R.fits || R.exact) break;
     if (R.passes >= kMaxRounds) break;
     if (R.pin_hi && R.passes >= kPinnedPasses) R.pin_hi = false;
