@@ -202,6 +202,8 @@ struct alignas(16) Fixed {
   uint32_t scan[kWarps];
   uint32_t own_n;
   uint32_t g_n;
+  float tail_val[32 * 4];  // local search tail: the last range's elements
+  uint32_t tail_n;
   uint32_t seg_n[kWarps];  // streaming pass: per-warp survivor counts
   uint32_t seg_ovf;        // a warp's survivors exceeded its segment
   uint32_t err;       // a bulk-copy wait of this CTA gave up
@@ -1182,6 +1184,7 @@ __device__ void narrow(Ctx<DT>& c, Range& R, bool from_chunk) {
     if (from_chunk && !wide_done && wide_pass<DT, MASS>(c, R)) {
       wide_done = true;
       used_value = true;
+      QRITA_T(11);
     } else {
       narrow_pass<DT, MASS>(c, R, from_chunk, value_ok, &used_value);
     }
@@ -1221,6 +1224,7 @@ __device__ void extract_range(Ctx<DT>& c, const Range& R) {
         warp_append<1>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx, bits);
       });
   __syncthreads();
+  QRITA_T(12);
 }
 
 // Copy every rank's own-list entries in (lo, hi] into this CTA's gathered set
@@ -1258,6 +1262,7 @@ __device__ void gather(Ctx<DT>& c, float lo_f, float hi_f, bool lo_all, bool syn
     }
   }
   cluster_sync_all();
+  QRITA_T(13);
 }
 
 // Copy every rank's whole own list into this CTA's gathered set at prefix
@@ -1552,6 +1557,10 @@ __device__ void retry_pass(Ctx<DT>& c, float t2) {
 // ---------------------------------------------------------------------------
 struct Local {
   uint32_t lo, hi, c_lo, c_hi;   // row counts above lo / hi
+  // count search: the Gaussian model of the row for the first pivots
+  // (model_sigma <= 0: none)
+  float model_mu, model_sigma;
+  int model_V;
   unsigned long long m_lo, m_hi;  // row masses above lo / hi (fixed point, mass search)
   uint32_t c_above;               // row count above the gathered range
   unsigned long long m_above;     // row mass above the gathered range (fixed point)
@@ -1595,21 +1604,82 @@ __device__ __forceinline__ unsigned long long warp_sum_u64_redux(unsigned long l
 // kept copies follows. Masses are exact sums of fixed-point weights, so
 // every decision is integer arithmetic; warp 0 takes it and broadcasts it.
 // target is the count (A6) or the fixed-point mass (A7) to reach.
+// Three increasing pivot keys strictly inside (lo, hi) at the floats v0 < v1
+// < v2; false when they collapse or leave the range.
+__device__ __forceinline__ bool pivots_at(uint32_t lo, uint32_t hi, float v0, float v1, float v2, uint32_t (&q)[3]) {
+  if (!(v0 < v1 && v1 < v2) || !isfinite(v0) || !isfinite(v2)) return false;
+  q[0] = f2key(v0);
+  q[1] = f2key(v1);
+  q[2] = f2key(v2);
+  return lo < q[0] && q[0] < q[1] && q[1] < q[2] && q[2] < hi;
+}
+
+// Count search pivots placed where the count above them is expected to cross
+// the target. First round: the Gaussian tail anchored at the range's lower
+// end, where the count is known (count(> v) = c_lo Q((v - mu)/sigma) /
+// Q((v_lo - mu)/sigma)), solved for 1.25, 1 and 0.8 times the target. Later
+// rounds: interpolation of log(count) in value between the range ends (a
+// Gaussian tail is close to exponential), with pivots an eighth of the range
+// apart around the estimate. The quaternary search stays exact whatever the
+// pivots; these only save rounds.
+__device__ __forceinline__ bool count_model_pivots(const Local& s, uint32_t target, uint32_t (&q)[3]) {
+  const float v_lo = pivot_f(s.lo);
+  if (!isfinite(v_lo) || s.c_lo == 0u) return false;
+  const float q_lo = normcdff((s.model_mu - v_lo) / s.model_sigma);  // upper tail at v_lo
+  float v[3];
+  const float f[3] = {1.25f, 1.0f, 0.8f};
+#pragma unroll
+  for (int j = 0; j < 3; ++j) {
+    const float u = q_lo * fminf(static_cast<float>(target) * f[j] / static_cast<float>(s.c_lo), 1.0f);
+    v[j] = s.model_mu - s.model_sigma * normcdfinvf(u);
+  }
+  return pivots_at(s.lo, s.hi, v[0], v[1], v[2], q);
+}
+
+__device__ __forceinline__ bool count_interp_pivots(uint32_t lo, uint32_t hi, uint32_t c_lo, uint32_t c_hi,
+                                                    uint32_t target, uint32_t (&q)[3]) {
+  const float v_lo = pivot_f(lo), v_hi = pivot_f(hi);
+  if (!isfinite(v_lo) || !isfinite(v_hi) || !(v_hi > v_lo) || c_lo <= c_hi) return false;
+  const float l_lo = logf(static_cast<float>(c_lo));
+  const float l_hi = logf(static_cast<float>(c_hi) + 0.5f);
+  const float l_t = logf(static_cast<float>(target) - 0.5f);
+  float f = (l_lo - l_t) / (l_lo - l_hi);
+  f = fminf(fmaxf(f, 0.125f), 0.875f);
+  const float width = v_hi - v_lo;
+  const float mid = fmaf(f, width, v_lo);
+  const float d = 0.125f * width;
+  return pivots_at(lo, hi, mid - d, mid, mid + d, q);
+}
+
+// Tail of the search: once the range holds at most kTail elements they are
+// copied out and one warp finishes the rounds with warp reductions only.
+constexpr int kTailPer = 4;
+constexpr int kTail = 32 * kTailPer;
+
 template <int DT, bool MASS>
 __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t gn = min(vld(F.g_n), c.gcap);
   const float scale = c.fix_scale;
-  // the search state is held, identical, by every thread: one block barrier
-  // per round (the warps' partials are double-buffered)
+  // the search state is held, identical, by every thread (by warp 0 alone in
+  // the tail): one block barrier per block round, the warps' partials
+  // double-buffered
   uint32_t lo = s.lo, hi = s.hi, c_lo = s.c_lo, c_hi = s.c_hi;
   unsigned long long m_lo = s.m_lo, m_hi = s.m_hi;
   uint32_t tau = 0, n_keep = 0, cabove = 0;
   int done = 0;  // 1: boundary found, 2: round cap
   uint32_t q[3];
   bool used_value = false;
-  int np = quartile_pivots(lo, hi, value_pivots, q[0], q[1], q[2], used_value);
+  const bool model = !MASS && value_pivots && s.model_sigma > 0.f;
+  bool interp = false;  // this round's pivots came from the model / interpolation
+  int np;
+  if (model && hi - lo > 4u && count_model_pivots(s, static_cast<uint32_t>(target), q)) {
+    np = 3;
+    interp = true;
+  } else {
+    np = quartile_pivots(lo, hi, value_pivots, q[0], q[1], q[2], used_value);
+  }
   // the boundary is the single key hi of (lo, hi]: keep the copies needed
   auto one_key = [&]() {
     tau = hi;
@@ -1622,9 +1692,84 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
     }
     done = 1;
   };
-  if (np == 0) one_key();
+  // One round's decision from the totals above the pivots (counts and
+  // masses over the whole row): stop at the first pivot whose z_mn is the
+  // boundary, else move lo / hi and choose the next pivots.
   int rounds = 0;
-  while (done == 0) {
+  auto decide = [&](const uint32_t (&tc)[3], const uint32_t (&tz)[3], const uint32_t (&tn)[3],
+                    const unsigned long long (&tm)[3]) {
+    bool reach[3], stop[3];
+    unsigned long long above[3], below[3], wz[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      above[j] = MASS ? tm[j] : static_cast<unsigned long long>(tc[j]);
+      wz[j] = MASS ? weight_fx(key2f(tz[j]), c.m, c.m_neginf, scale) : 1ull;
+      below[j] = above[j] - static_cast<unsigned long long>(tn[j]) * wz[j];
+      reach[j] = j < np && above[j] >= target;
+      stop[j] = reach[j] && below[j] < target;
+    }
+    // the first pivot (in increasing order) whose z_mn is the boundary
+    int done_j = -1;
+    if (stop[0]) done_j = 0;
+    else if (reach[0] && stop[1]) done_j = 1;
+    else if (reach[0] && reach[1] && stop[2]) done_j = 2;
+    if (done_j >= 0) {
+      const uint32_t z = done_j == 0 ? tz[0] : (done_j == 1 ? tz[1] : tz[2]);
+      const uint32_t n = done_j == 0 ? tn[0] : (done_j == 1 ? tn[1] : tn[2]);
+      tau = z;
+      cabove = (done_j == 0 ? tc[0] : (done_j == 1 ? tc[1] : tc[2])) - n;
+      if (MASS) {
+        const unsigned long long w = done_j == 0 ? wz[0] : (done_j == 1 ? wz[1] : wz[2]);
+        const unsigned long long b = done_j == 0 ? below[0] : (done_j == 1 ? below[1] : below[2]);
+        n_keep = copies_fx(target - b, w, n);
+      } else {
+        n_keep = static_cast<uint32_t>(target) - cabove;
+      }
+      done = 1;
+      return;
+    }
+    // the highest pivot that reaches the target becomes lo, the lowest that
+    // does not becomes hi
+    const int lo_j = !reach[0] ? -1 : (!reach[1] || np < 2 ? 0 : (!reach[2] || np < 3 ? 1 : 2));
+    const int hi_j = !reach[0] ? 0 : (np < 2 ? -1 : (!reach[1] ? 1 : (np < 3 ? -1 : (!reach[2] ? 2 : -1))));
+    const uint32_t old_span = hi - lo;
+    if (lo_j >= 0) {
+      lo = lo_j == 0 ? q[0] : (lo_j == 1 ? q[1] : q[2]);
+      c_lo = lo_j == 0 ? tc[0] : (lo_j == 1 ? tc[1] : tc[2]);
+      m_lo = lo_j == 0 ? above[0] : (lo_j == 1 ? above[1] : above[2]);
+    }
+    if (hi_j >= 0) {
+      hi = hi_j == 0 ? q[0] : (hi_j == 1 ? q[1] : q[2]);
+      c_hi = hi_j == 0 ? tc[0] : (hi_j == 1 ? tc[1] : tc[2]);
+      m_hi = hi_j == 0 ? above[0] : (hi_j == 1 ? above[1] : above[2]);
+    }
+    if (hi - lo <= 1u) {
+      one_key();
+      return;
+    }
+    if (rounds >= kMaxRounds) {
+      done = 2;
+      return;
+    }
+    // after a value-space split that failed to halve the key range, the next
+    // round splits the key range
+    const bool vmode = value_pivots && !(used_value && (hi - lo) > old_span / 2u);
+    // interpolated pivots again only after a round that cut the key range at
+    // least fourfold (else plain quartiles guarantee progress)
+    const bool good = (hi - lo) <= old_span / 4u;
+    if (model && (good || !interp) && hi - lo > 4u &&
+        count_interp_pivots(lo, hi, c_lo, c_hi, static_cast<uint32_t>(target), q)) {
+      np = 3;
+      interp = true;
+      used_value = true;
+    } else {
+      np = quartile_pivots(lo, hi, vmode, q[0], q[1], q[2], used_value);
+      interp = false;
+    }
+  };
+  if (np == 0) one_key();
+  // block rounds over the gathered set while the range is large
+  while (done == 0 && c_lo - c_hi > static_cast<uint32_t>(kTail)) {
     float qf[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) qf[j] = j < np ? pivot_f(q[j]) : INFINITY;
@@ -1671,69 +1816,91 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
       const uint32_t zw = own ? pp.zmin : 0xFFFFFFFFu;
       const uint32_t nw = own ? pp.nz : 0u;
       const unsigned long long mw = (MASS && own) ? pp.mass : 0ull;
-      tc[j] = __reduce_add_sync(kFull, cw);
+      tc[j] = __reduce_add_sync(kFull, cw) + s.c_above;
       tz[j] = __reduce_min_sync(kFull, zw);
       tn[j] = __reduce_add_sync(kFull, zw == tz[j] ? nw : 0u);
-      tm[j] = MASS ? warp_sum_u64_redux(mw) : 0ull;
+      tm[j] = MASS ? warp_sum_u64_redux(mw) + s.m_above : 0ull;
     }
-    bool reach[3], stop[3];
-    unsigned long long above[3], below[3], wz[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const uint32_t ac = tc[j] + s.c_above;
-      above[j] = MASS ? tm[j] + s.m_above : static_cast<unsigned long long>(ac);
-      wz[j] = MASS ? weight_fx(key2f(tz[j]), c.m, c.m_neginf, scale) : 1ull;
-      below[j] = above[j] - static_cast<unsigned long long>(tn[j]) * wz[j];
-      reach[j] = j < np && above[j] >= target;
-      stop[j] = reach[j] && below[j] < target;
-    }
-    // the first pivot (in increasing order) whose z_mn is the boundary
-    int done_j = -1;
-    if (stop[0]) done_j = 0;
-    else if (reach[0] && stop[1]) done_j = 1;
-    else if (reach[0] && reach[1] && stop[2]) done_j = 2;
-    if (done_j >= 0) {
-      const uint32_t z = done_j == 0 ? tz[0] : (done_j == 1 ? tz[1] : tz[2]);
-      const uint32_t n = done_j == 0 ? tn[0] : (done_j == 1 ? tn[1] : tn[2]);
-      tau = z;
-      cabove = (done_j == 0 ? tc[0] : (done_j == 1 ? tc[1] : tc[2])) + s.c_above - n;
-      if (MASS) {
-        const unsigned long long w = done_j == 0 ? wz[0] : (done_j == 1 ? wz[1] : wz[2]);
-        const unsigned long long b = done_j == 0 ? below[0] : (done_j == 1 ? below[1] : below[2]);
-        n_keep = copies_fx(target - b, w, n);
-      } else {
-        n_keep = static_cast<uint32_t>(target) - cabove;
+    decide(tc, tz, tn, tm);
+  }
+  __syncthreads();  // every warp has read the last block round's partials
+  if (done == 0) {
+    // tail: the (lo, hi] elements of the gathered set (c_lo - c_hi of them)
+    // to shared memory; warp 0 finishes the search
+    if (tid == 0) F.tail_n = 0u;
+    __syncthreads();
+    for (uint32_t b = 0; b < gn; b += kThreads) {
+      const uint32_t i = b + tid;
+      const float x = i < gn ? c.g_val[i] : -INFINITY;
+      const uint32_t key = f2key(x);  // keys: lo may lie below key(-inf)
+      const bool in = i < gn && key > lo && key <= hi;
+      const uint32_t bal = __ballot_sync(kFull, in);
+      uint32_t base = 0;
+      if (lane == 0 && bal != 0u) base = atomicAdd(&F.tail_n, static_cast<uint32_t>(__popc(bal)));
+      base = __shfl_sync(kFull, base, 0);
+      if (in) {
+        const uint32_t pos = base + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
+        if (pos < static_cast<uint32_t>(kTail)) F.tail_val[pos] = x;
       }
-      done = 1;
-      break;
     }
-    // the highest pivot that reaches the target becomes lo, the lowest that
-    // does not becomes hi
-    const int lo_j = !reach[0] ? -1 : (!reach[1] || np < 2 ? 0 : (!reach[2] || np < 3 ? 1 : 2));
-    const int hi_j = !reach[0] ? 0 : (np < 2 ? -1 : (!reach[1] ? 1 : (np < 3 ? -1 : (!reach[2] ? 2 : -1))));
-    const uint32_t old_span = hi - lo;
-    if (lo_j >= 0) {
-      lo = lo_j == 0 ? q[0] : (lo_j == 1 ? q[1] : q[2]);
-      c_lo = (lo_j == 0 ? tc[0] : (lo_j == 1 ? tc[1] : tc[2])) + s.c_above;
-      m_lo = lo_j == 0 ? above[0] : (lo_j == 1 ? above[1] : above[2]);
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t tn_all = min(vld(F.tail_n), static_cast<uint32_t>(kTail));
+      float tx[kTailPer];
+      unsigned long long tw[kTailPer];
+#pragma unroll
+      for (int e = 0; e < kTailPer; ++e) {
+        const uint32_t i = static_cast<uint32_t>(lane + 32 * e);
+        tx[e] = i < tn_all ? vld(F.tail_val[i]) : -INFINITY;
+        tw[e] = (MASS && i < tn_all) ? weight_fx(tx[e], c.m, c.m_neginf, scale) : 0ull;
+      }
+      // everything above the tail range is already counted in c_hi / m_hi
+      const uint32_t base_c = c_hi;
+      const unsigned long long base_m = m_hi;
+      while (done == 0) {
+        float qf[3];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) qf[j] = j < np ? pivot_f(q[j]) : INFINITY;
+        uint32_t tc[3], tz[3], tn[3];
+        unsigned long long tm[3];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          uint32_t cnt = 0, zk = 0xFFFFFFFFu;
+          unsigned long long ms = 0ull;
+#pragma unroll
+          for (int e = 0; e < kTailPer; ++e) {
+            const bool g = tx[e] > qf[j];
+            cnt += g ? 1u : 0u;
+            if (MASS) ms += g ? tw[e] : 0ull;
+            const uint32_t key = f2key(tx[e]);
+            zk = (g && key < zk) ? key : zk;
+          }
+          tz[j] = __reduce_min_sync(kFull, zk);
+          uint32_t nz = 0;
+#pragma unroll
+          for (int e = 0; e < kTailPer; ++e) nz += (tx[e] > qf[j] && f2key(tx[e]) == tz[j]) ? 1u : 0u;
+          tc[j] = __reduce_add_sync(kFull, cnt) + base_c;
+          tn[j] = __reduce_add_sync(kFull, nz);
+          tm[j] = MASS ? warp_sum_u64_redux(ms) + base_m : 0ull;
+        }
+        ++rounds;
+        decide(tc, tz, tn, tm);
+      }
+      if (lane == 0) {
+        F.bc.u[BU_TAU] = tau;
+        F.bc.u[BU_NKEEP] = n_keep;
+        F.bc.u[BU_CABOVE] = cabove;
+        F.bc.u[BU_DONE] = static_cast<uint32_t>(done);
+        F.bc.u[BU_NP] = static_cast<uint32_t>(rounds);
+      }
     }
-    if (hi_j >= 0) {
-      hi = hi_j == 0 ? q[0] : (hi_j == 1 ? q[1] : q[2]);
-      c_hi = (hi_j == 0 ? tc[0] : (hi_j == 1 ? tc[1] : tc[2])) + s.c_above;
-      m_hi = hi_j == 0 ? above[0] : (hi_j == 1 ? above[1] : above[2]);
-    }
-    if (hi - lo <= 1u) {
-      one_key();
-      break;
-    }
-    if (rounds >= kMaxRounds) {
-      done = 2;
-      break;
-    }
-    // after a value-space split that failed to halve the key range, the next
-    // round splits the key range
-    const bool vmode = value_pivots && !(used_value && (hi - lo) > old_span / 2u);
-    np = quartile_pivots(lo, hi, vmode, q[0], q[1], q[2], used_value);
+    __syncthreads();
+    tau = vld(F.bc.u[BU_TAU]);
+    n_keep = vld(F.bc.u[BU_NKEEP]);
+    cabove = vld(F.bc.u[BU_CABOVE]);
+    done = static_cast<int>(vld(F.bc.u[BU_DONE]));
+    rounds = static_cast<int>(vld(F.bc.u[BU_NP]));
+    __syncthreads();
   }
   (void)m_lo;
   QRITA_T(14);
@@ -1742,7 +1909,6 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
   s.count_above = cabove;
   s.rounds = rounds;
   s.capped = done == 2;
-  __syncthreads();  // every warp has read the last round's partials
 }
 
 // Per-rank counts of gathered entries equal to tau (into F.ties).
@@ -2215,6 +2381,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       const bool hit = trunc && !overflow && !force_fb && !force_retry && survivors >= target;
       if (hit) path |= QRITA_PATH_HIT;
       Local s;
+      s.model_mu = mu;
+      s.model_sigma = (sigma > 0.f && isfinite(sigma) && isfinite(mu)) ? sigma : 0.f;
+      s.model_V = V;
       s.c_above = 0;
       s.m_above = 0ull;
       s.m_lo = s.m_hi = 0ull;
@@ -2416,6 +2585,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           }
         } else {
           Local s;
+          s.model_mu = 0.f;
+          s.model_sigma = 0.f;
+          s.model_V = V;
           s.lo = tau_k;
           s.c_lo = above_k;
           s.m_lo = M_gt;
@@ -2446,6 +2618,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                          f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
         if (!k_on) path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
         Local s;
+        s.model_mu = 0.f;
+        s.model_sigma = 0.f;
+        s.model_V = V;
         s.c_above = 0;
         s.m_above = 0ull;
         bool have_exact = false;
