@@ -65,13 +65,6 @@ constexpr float kAlphaK = 2.0f;
 constexpr float kUMaxK = 0.25f;
 constexpr float kMarginP = 0.25f;
 
-// Candidate list capacities (entries of value + index): a CTA's own list and
-// the gathered set every CTA of a row searches; with one CTA per row the two
-// are one list. 104 KiB with the streaming ring either way: two CTAs per SM.
-constexpr int kOwnCap = 4096;
-constexpr int kGatherCap = 9216;
-constexpr int kSoleCap = 9216;
-// Resident CTAs per SM the kernel is built for (its register budget).
 constexpr int kCtasPerSm = 2;
 // Rows shorter than this per CTA are not split further.
 constexpr int64_t kMinChunk = 1024;

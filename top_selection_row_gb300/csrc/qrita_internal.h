@@ -34,6 +34,17 @@ constexpr int kNarrowPivots = 15;
 // on average, so 32-bit keys need at most about 34 rounds).
 constexpr int kMaxRounds = 64;
 
+// Candidate list capacities (entries of value + index): a CTA's own list and
+// the gathered set every CTA of a row searches; with one CTA per row the two
+// are one list. 103 KiB with the streaming ring either way: two CTAs per SM.
+constexpr int kOwnCap = 4096;
+constexpr int kGatherCap = 9088;
+constexpr int kSoleCap = 9088;
+// Shared memory of one SM on GB300 and what the runtime reserves per CTA: two
+// CTAs must fit.
+constexpr int kSmemPerSm = 228 * 1024;
+constexpr int kSmemReservedPerCta = 1024;
+
 struct Params {
   const void* logits;
   uint8_t* mask;

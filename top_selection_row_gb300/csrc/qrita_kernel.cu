@@ -170,13 +170,6 @@ struct alignas(16) Bcast {  // written by one thread / warp 0 before a block bar
   float qf[16];    // pivot floats (+inf padding)
 };
 
-struct alignas(16) PAccS {  // per-warp pivot partial (block reduction scratch)
-  uint32_t cnt;
-  float z;
-  uint32_t nz;
-  float mhi, mlo;
-  uint32_t pad[3];
-};
 
 // Per-warp partial of one pivot of the local search.
 struct alignas(16) LPart {
@@ -187,7 +180,6 @@ struct alignas(16) LPart {
 struct alignas(16) Fixed {
   Slot slots[2];
   Bcast bc;
-  PAccS red[kWarps][3];
   LPart lred[2][kWarps][3];  // local search: per-warp partials, double-buffered
   float redf[kWarps][8];
   uint32_t redu[kWarps][kBins];
@@ -202,7 +194,8 @@ struct alignas(16) Fixed {
   uint32_t scan[kWarps];
   uint32_t own_n;
   uint32_t g_n;
-  float tail_val[32 * 4];  // local search tail: the last range's elements
+  float tail_val[kThreads];  // local search tail: the last range's elements
+  unsigned long long tail_w[kThreads];  // and their fixed-point weights (mass search)
   uint32_t tail_n;
   uint32_t seg_n[kWarps];  // streaming pass: per-warp survivor counts
   uint32_t seg_ovf;        // a warp's survivors exceeded its segment
@@ -240,62 +233,6 @@ __device__ __forceinline__ void put_pair(Bcast& b, int i, F2 v) {
 
 __device__ __forceinline__ F2 get_pair(const Bcast& b, int i) {
   return f2_make(vld(b.pr[2 * i]), vld(b.pr[2 * i + 1]));
-}
-
-// ---------------------------------------------------------------------------
-// Pivot accumulators of the local search
-// ---------------------------------------------------------------------------
-struct PAcc {
-  uint32_t cnt;
-  float z;
-  uint32_t nz;
-  F2 m;
-};
-
-
-template <bool MASS>
-__device__ __forceinline__ void pacc_combine(PAcc& a, const PAcc& b) {
-  a.cnt += b.cnt;
-  if (b.z < a.z) {
-    a.z = b.z;
-    a.nz = b.nz;
-  } else if (b.z == a.z) {
-    a.nz += b.nz;
-  }
-  if (MASS) a.m = f2_merge(a.m, b.m);
-}
-
-template <bool MASS>
-__device__ __forceinline__ PAcc pacc_shfl_xor(const PAcc& a, int off) {
-  PAcc o;
-  o.cnt = __shfl_xor_sync(kFull, a.cnt, off);
-  o.z = __shfl_xor_sync(kFull, a.z, off);
-  o.nz = __shfl_xor_sync(kFull, a.nz, off);
-  if (MASS) {
-    o.m.hi = __shfl_xor_sync(kFull, a.m.hi, off);
-    o.m.lo = __shfl_xor_sync(kFull, a.m.lo, off);
-  } else {
-    o.m.hi = 0.f;
-    o.m.lo = 0.f;
-  }
-  return o;
-}
-
-// Per-element update of three pivots: count above, softmax mass above, and
-// z_mn / N_zmn (smallest element above the pivot and its multiplicity).
-// Unused pivots are +inf. Predicated, so the warp never diverges here.
-template <bool MASS>
-__device__ __forceinline__ void pacc_update(PAcc (&acc)[3], const float (&qf)[3], float x, float w) {
-#pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    const bool g = x > qf[j];
-    acc[j].cnt += g ? 1u : 0u;
-    if (MASS) f2_add(acc[j].m, g ? w : 0.f);
-    const bool lt = g && (x < acc[j].z);
-    const bool eq = (x == acc[j].z);
-    acc[j].nz = lt ? 1u : (acc[j].nz + (eq ? 1u : 0u));
-    acc[j].z = lt ? x : acc[j].z;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1652,9 +1589,8 @@ __device__ __forceinline__ bool count_interp_pivots(uint32_t lo, uint32_t hi, ui
 }
 
 // Tail of the search: once the range holds at most kTail elements they are
-// copied out and one warp finishes the rounds with warp reductions only.
-constexpr int kTailPer = 4;
-constexpr int kTail = 32 * kTailPer;
+// copied out and each tests itself as the boundary (one thread each).
+constexpr int kTail = kThreads;
 
 template <int DT, bool MASS>
 __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots) {
@@ -1824,10 +1760,14 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
     decide(tc, tz, tn, tm);
   }
   __syncthreads();  // every warp has read the last block round's partials
+  QRITA_T(12);
   if (done == 0) {
     // tail: the (lo, hi] elements of the gathered set (c_lo - c_hi of them)
-    // to shared memory; warp 0 finishes the search
-    if (tid == 0) F.tail_n = 0u;
+    // to shared memory; each tests itself as the boundary
+    if (tid == 0) {
+      F.tail_n = 0u;
+      F.bc.u[BU_DONE] = 2u;  // unless a candidate answers (it always does)
+    }
     __syncthreads();
     for (uint32_t b = 0; b < gn; b += kThreads) {
       const uint32_t i = b + tid;
@@ -1840,60 +1780,57 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
       base = __shfl_sync(kFull, base, 0);
       if (in) {
         const uint32_t pos = base + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
-        if (pos < static_cast<uint32_t>(kTail)) F.tail_val[pos] = x;
+        if (pos < static_cast<uint32_t>(kTail)) {
+          F.tail_val[pos] = x;
+          if (MASS) F.tail_w[pos] = weight_fx(x, c.m, c.m_neginf, scale);
+        }
       }
     }
     __syncthreads();
-    if (warp == 0) {
-      const uint32_t tn_all = min(vld(F.tail_n), static_cast<uint32_t>(kTail));
-      float tx[kTailPer];
-      unsigned long long tw[kTailPer];
+    QRITA_T(13);
+    // every candidate v of the range tests itself: it is the boundary when
+    // count(> v) < target <= count(>= v) (masses likewise), which is where
+    // further quaternary rounds would stop (tau = v = z_mn, N_zmn = N(v))
+    const uint32_t tn_all = min(vld(F.tail_n), static_cast<uint32_t>(kTail));
+    if (tid < static_cast<int>(tn_all)) {
+      // the buffer is complete (barrier above) and unchanged from here on:
+      // plain loads, eight in flight
+      const float* tv = F.tail_val;
+      const unsigned long long* tw = F.tail_w;
+      const float v = tv[tid];
+      uint32_t gt = 0, eq = 0;
+      unsigned long long mgt = 0ull;
+      uint32_t i = 0;
+      for (; i + 8u <= tn_all; i += 8u) {
+        float x[8];
 #pragma unroll
-      for (int e = 0; e < kTailPer; ++e) {
-        const uint32_t i = static_cast<uint32_t>(lane + 32 * e);
-        tx[e] = i < tn_all ? vld(F.tail_val[i]) : -INFINITY;
-        tw[e] = (MASS && i < tn_all) ? weight_fx(tx[e], c.m, c.m_neginf, scale) : 0ull;
-      }
-      // everything above the tail range is already counted in c_hi / m_hi
-      const uint32_t base_c = c_hi;
-      const unsigned long long base_m = m_hi;
-      while (done == 0) {
-        float qf[3];
+        for (int u = 0; u < 8; ++u) x[u] = tv[i + u];
 #pragma unroll
-        for (int j = 0; j < 3; ++j) qf[j] = j < np ? pivot_f(q[j]) : INFINITY;
-        uint32_t tc[3], tz[3], tn[3];
-        unsigned long long tm[3];
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          uint32_t cnt = 0, zk = 0xFFFFFFFFu;
-          unsigned long long ms = 0ull;
-#pragma unroll
-          for (int e = 0; e < kTailPer; ++e) {
-            const bool g = tx[e] > qf[j];
-            cnt += g ? 1u : 0u;
-            if (MASS) ms += g ? tw[e] : 0ull;
-            const uint32_t key = f2key(tx[e]);
-            zk = (g && key < zk) ? key : zk;
-          }
-          tz[j] = __reduce_min_sync(kFull, zk);
-          uint32_t nz = 0;
-#pragma unroll
-          for (int e = 0; e < kTailPer; ++e) nz += (tx[e] > qf[j] && f2key(tx[e]) == tz[j]) ? 1u : 0u;
-          tc[j] = __reduce_add_sync(kFull, cnt) + base_c;
-          tn[j] = __reduce_add_sync(kFull, nz);
-          tm[j] = MASS ? warp_sum_u64_redux(ms) + base_m : 0ull;
+        for (int u = 0; u < 8; ++u) {
+          gt += x[u] > v ? 1u : 0u;
+          eq += x[u] == v ? 1u : 0u;
+          if (MASS) mgt += x[u] > v ? tw[i + u] : 0ull;
         }
-        ++rounds;
-        decide(tc, tz, tn, tm);
       }
-      if (lane == 0) {
-        F.bc.u[BU_TAU] = tau;
-        F.bc.u[BU_NKEEP] = n_keep;
-        F.bc.u[BU_CABOVE] = cabove;
-        F.bc.u[BU_DONE] = static_cast<uint32_t>(done);
-        F.bc.u[BU_NP] = static_cast<uint32_t>(rounds);
+      for (; i < tn_all; ++i) {
+        const float x = tv[i];
+        gt += x > v ? 1u : 0u;
+        eq += x == v ? 1u : 0u;
+        if (MASS) mgt += x > v ? tw[i] : 0ull;
+      }
+      const unsigned long long above_gt = MASS ? mgt + m_hi : static_cast<unsigned long long>(gt + c_hi);
+      const unsigned long long wv = MASS ? tw[tid] : 1ull;
+      const unsigned long long above_ge = above_gt + static_cast<unsigned long long>(eq) * wv;
+      // every copy of the boundary value answers, with the same values
+      if (above_gt < target && target <= above_ge) {
+        F.bc.u[BU_TAU] = f2key(v);
+        const uint32_t ca = gt + c_hi;
+        F.bc.u[BU_CABOVE] = ca;
+        F.bc.u[BU_NKEEP] = MASS ? copies_fx(target - above_gt, wv, eq) : static_cast<uint32_t>(target) - ca;
+        F.bc.u[BU_DONE] = 1u;
       }
     }
+    if (tid == 0) F.bc.u[BU_NP] = static_cast<uint32_t>(rounds + 1);
     __syncthreads();
     tau = vld(F.bc.u[BU_TAU]);
     n_keep = vld(F.bc.u[BU_NKEEP]);
@@ -2906,6 +2843,13 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
 }
 
 }  // namespace
+
+static_assert(2 * (sizeof(Fixed) + list_region_bytes(2, kOwnCap, kGatherCap) + 128 + kSmemReservedPerCta) <=
+                  static_cast<size_t>(kSmemPerSm),
+              "two CTAs of a cluster shape must fit one SM");
+static_assert(2 * (sizeof(Fixed) + list_region_bytes(1, kSoleCap, kSoleCap) + 128 + kSmemReservedPerCta) <=
+                  static_cast<size_t>(kSmemPerSm),
+              "two CTAs of the one-CTA shape must fit one SM");
 
 size_t smem_bytes(int C, int ocap, int gcap) {
   const size_t lists = list_region_bytes(C, ocap, gcap);
