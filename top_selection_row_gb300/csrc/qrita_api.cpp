@@ -104,7 +104,6 @@ struct Shape {
   int C;
   int chunk;
   int ocap;
-  int gcap;
   size_t smem;
 };
 
@@ -131,14 +130,12 @@ int choose_shape(int64_t B, int64_t V, uint32_t flags, Shape* out) {
   int64_t chunk = (V + C - 1) / C;
   chunk = (chunk + 15) / 16 * 16;
   if (B * C > static_cast<int64_t>(std::numeric_limits<int32_t>::max())) return QRITA_EUNSUPPORTED;
-  const int ocap = C == 1 ? kSoleCap : kOwnCap;
-  const int gcap = C == 1 ? kSoleCap : kGatherCap;
-  const size_t smem = smem_bytes(C, ocap, gcap);
+  const int ocap = kOwnCap;
+  const size_t smem = smem_bytes(ocap);
   if (smem == 0 || smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
   out->C = C;
   out->chunk = static_cast<int>(chunk);
   out->ocap = ocap;
-  out->gcap = gcap;
   out->smem = smem;
   return QRITA_OK;
 }
@@ -176,7 +173,6 @@ int select_impl(const void* logits, int dtype, int64_t B, int64_t V, const int32
   prm.C = sh.C;
   prm.chunk = sh.chunk;
   prm.ocap = sh.ocap;
-  prm.gcap = sh.gcap;
   prm.flags = flags;
   prm.alpha_k = kAlphaK;
   prm.margin_p = kMarginP;

@@ -34,12 +34,9 @@ constexpr int kNarrowPivots = 15;
 // on average, so 32-bit keys need at most about 34 rounds).
 constexpr int kMaxRounds = 64;
 
-// Candidate list capacities (entries of value + index): a CTA's own list and
-// the gathered set every CTA of a row searches; with one CTA per row the two
-// are one list. 103 KiB with the streaming ring either way: two CTAs per SM.
-constexpr int kOwnCap = 4096;
-constexpr int kGatherCap = 9088;
-constexpr int kSoleCap = 9088;
+// Capacity of a CTA's own candidate list (entries of value + index): 72 KiB,
+// plus the 32 KiB streaming ring: two CTAs per SM.
+constexpr int kOwnCap = 9216;
 // Shared memory of one SM on GB300 and what the runtime reserves per CTA: two
 // CTAs must fit.
 constexpr int kSmemPerSm = 228 * 1024;
@@ -57,9 +54,6 @@ struct Params {
   int32_t C;        // CTAs per row (cluster size)
   int32_t chunk;    // elements per CTA (multiple of 16)
   int32_t ocap;     // own candidate list capacity per CTA (entries)
-  int32_t gcap;     // gathered candidate set capacity per CTA (entries); with
-                    // one CTA per row (C == 1) the own list is the gathered
-                    // set and ocap == gcap
   uint32_t flags;   // QRITA_FLAG_*
   float alpha_k;    // top-k truncation safety factor (u = alpha_k * k / V)
   float margin_p;   // subtracted from the top-p delta
@@ -69,9 +63,9 @@ struct Params {
 };
 
 
-// Bytes of dynamic shared memory the kernel needs for C CTAs per row and the
-// list capacities (0: the capacities leave no room for the streaming ring).
-size_t smem_bytes(int C, int ocap, int gcap);
+// Bytes of dynamic shared memory the kernel needs for an own-list capacity
+// (0: the capacity leaves no room for the streaming ring).
+size_t smem_bytes(int ocap);
 
 // Launch the selection kernel (grid B*C, cluster C). Returns a cudaError_t.
 int launch_select(const Params& prm, int dtype, size_t smem, qrita_stream_t stream);

@@ -16,16 +16,20 @@
 //       max / min / NaN / +inf and, for top-p without top-k, the softmax mass
 //       of the row and of Z_t;
 //   --  one cluster merge through distributed shared memory;
-//   A5  hit: every CTA gathers the whole Z_t into its shared memory;
-//       fallback (miss, or too many candidates): distributed narrowing passes
-//       evaluate two quaternary levels (15 pivots) per cluster merge until the
-//       range that holds the boundary fits, then that range is gathered;
-//   A6  quaternary pivot search over the gathered candidates with
-//       z_mn / N_zmn duplicate tracking, inside each CTA (one block barrier
-//       per round);
+//   A5  hit: the survivors stay in the CTAs' own lists; fallback (miss, or
+//       too many candidates): a second truncation at an order statistic of
+//       a larger sample (top-k), else distributed narrowing passes over the
+//       chunk (one 256-bin pass, then two quaternary levels per cluster
+//       merge) until the range that holds the boundary fits the own lists,
+//       from which it is extracted;
+//   A6  quaternary pivot search over the own lists of the cluster with
+//       z_mn / N_zmn duplicate tracking: every CTA counts its own list, the
+//       counts are merged through distributed shared memory each round, and
+//       the last few hundred candidates are copied to every CTA and tested
+//       directly;
 //   A7  the same search by softmax mass for top-p;
 //   A8  boundary duplicates kept by lowest token id: per-rank counts from the
-//       gathered set, then an index cut inside the one straddling CTA;
+//       search, then an index cut inside the one straddling CTA;
 //   A9  mask emission: hit rows write zeros and scatter the kept ids of the
 //       CTA's own list (no second read of the logits); fallback rows stream
 //       the chunk again.
@@ -70,7 +74,6 @@ static_assert(kPieceUnits % kThreads == 0, "a piece is whole rounds of the block
 // microseconds; the bound only keeps a failing copy from hanging the kernel).
 constexpr uint64_t kWaitLimitNs = 200ull * 1000ull * 1000ull;
 constexpr int kBins = kNarrowPivots + 1;
-constexpr int kTagShift = 28;  // gathered tag = rank << 28 | index in chunk
 // A chunk narrowing pass lays per-thread bins (counts, then fixed-point
 // masses) over the start of the list region, clear of the streaming ring.
 constexpr int kBinBytes = kBins * kThreads * (4 + 8);
@@ -180,21 +183,24 @@ struct alignas(16) LPart {
 struct alignas(16) Fixed {
   Slot slots[2];
   Bcast bc;
-  LPart lred[2][kWarps][3];  // local search: per-warp partials, double-buffered
+  LPart lred[2][kWarps][3];  // quaternary search: per-warp partials, double-buffered
   float redf[kWarps][8];
   uint32_t redu[kWarps][kBins];
-  uint32_t bin_cnt[kWarps][kBins];
-  unsigned long long bin_mass[kWarps][kBins];
   uint32_t rank_bins[kMaxCluster][kBins + 1];  // latest narrowing merge, per rank
-  uint32_t rank_n[kMaxCluster];   // per-rank entries to gather
-  uint32_t rank_off[kMaxCluster + 1];  // their prefix offsets in the gathered set
-  uint32_t rank_lo[kMaxCluster];  // per-rank count above the narrowing lo
-  uint32_t rank_hi[kMaxCluster];  // per-rank count above the narrowing hi
+  uint32_t rank_n[kMaxCluster];   // per-rank own-list entries (survivors)
+  uint32_t rank_lo[kMaxCluster];  // per-rank count above lo (narrowing: chunk; search: own list)
+  uint32_t rank_hi[kMaxCluster];  // per-rank count above hi
   uint32_t ties[kMaxCluster];     // per-rank count of boundary-valued elements
+  uint32_t pr_cnt[kMaxCluster][3];  // search round: per-rank counts above the pivots
+  uint32_t pr_nz[kMaxCluster][3];   // search round: per-rank copies of the row's z_mn
+  uint32_t dtot[3][3];              // search round: row count, z_mn, N_zmn per pivot
+  unsigned long long dmass[3];      // search round: row mass above each pivot
   uint32_t scan[kWarps];
   uint32_t own_n;
-  uint32_t g_n;
-  float tail_val[kThreads];  // local search tail: the last range's elements
+  uint32_t seg_base[kWarps];  // own list: warp w's entries are [seg_base[w], + seg_cnt[w])
+  uint32_t seg_cnt[kWarps];
+  float tail_val[kThreads];  // search tail: the last range's elements (cluster-wide)
+  uint8_t tail_rank[kThreads];  // and the cluster rank each came from
   unsigned long long tail_w[kThreads];  // and their fixed-point weights (mass search)
   uint32_t tail_n;
   uint32_t seg_n[kWarps];  // streaming pass: per-warp survivor counts
@@ -205,11 +211,9 @@ struct alignas(16) Fixed {
 };
 
 // Bytes of the list region after Fixed: the own list (value + index), then
-// the gathered set (value + tag) when C > 1. The streaming ring occupies the
-// region's last kRingBytes: inside the gathered set when C > 1 (which holds
-// nothing while the chunk streams), after the own list when C == 1.
-__host__ __device__ constexpr size_t list_region_bytes(int C, int ocap, int gcap) {
-  return C > 1 ? static_cast<size_t>(ocap + gcap) * 8u : static_cast<size_t>(ocap) * 8u + kRingBytes;
+// the streaming ring.
+__host__ __device__ constexpr size_t list_region_bytes(int ocap) {
+  return static_cast<size_t>(ocap) * 8u + kRingBytes;
 }
 
 // Names of the broadcast slots
@@ -417,14 +421,10 @@ struct Ctx {
   static constexpr int E = Elem<DT>::kPerUnit;
   static constexpr int S = Elem<DT>::kBytes;
   Fixed* F;
-  unsigned char* lists;  // the list region (own list, then the gathered set)
-  bool alias;            // one CTA per row: the own list is the gathered set
+  unsigned char* lists;  // the list region (own list, then the ring)
   float* own_val;
   uint32_t* own_idx;
   uint32_t ocap;
-  float* g_val;
-  uint32_t* g_tag;
-  uint32_t gcap;
   const unsigned char* gx;     // chunk start in global memory
   const unsigned char* gbody;  // first 16-byte aligned unit of the chunk
   uint8_t* gmask;              // chunk start in the mask
@@ -603,8 +603,8 @@ struct Range {
   float p_frac;
   unsigned long long extra;
   bool lo_all;          // lo lies below key(-inf): every element is above it
-  bool pin_hi;          // narrow from below only: gather everything above lo
-  bool fits;            // the range fits the lists: gather it
+  bool pin_hi;          // extraction: keep everything above lo
+  bool fits;            // every rank's part of the range fits its own list
   bool exact;           // hi - lo <= 1: the boundary value is hi
   bool below;           // the target exceeds everything above lo: the boundary is at lo
   int passes;
@@ -627,9 +627,9 @@ __device__ __forceinline__ int pivot_bin(const volatile float* qf, float x) {
 // keeps the bin that holds the boundary. Counts are exact integers and
 // masses exact sums of fixed-point weights, so the merge is deterministic.
 // A chunk pass bins into per-thread columns of shared memory (no atomics)
-// laid over the own list and the gathered set, which it leaves undefined.
+// laid over the own list, which it leaves undefined.
 template <int DT, bool MASS>
-__device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok, bool* used_value_out) {
+__device__ void narrow_pass(Ctx<DT>& c, Range& R, bool value_ok, bool* used_value_out) {
   constexpr int E = Ctx<DT>::E;
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -647,18 +647,10 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok
       reinterpret_cast<unsigned long long*>(c.lists + kBins * kThreads * 4);  // [kBins][kThreads]
   __syncthreads();  // pivots published; earlier readers of the lists are done
   const volatile float* qf = F.bc.qf;
-  if (from_chunk) {
 #pragma unroll
-    for (int b = 0; b < kBins; ++b) {
-      lcnt[b * kThreads + tid] = 0u;
-      if (MASS) lmass[b * kThreads + tid] = 0ull;
-    }
-  } else {
-    for (int i = tid; i < kWarps * kBins; i += kThreads) {
-      (&F.bin_cnt[0][0])[i] = 0u;
-      (&F.bin_mass[0][0])[i] = 0ull;
-    }
-    __syncthreads();
+  for (int b = 0; b < kBins; ++b) {
+    lcnt[b * kThreads + tid] = 0u;
+    if (MASS) lmass[b * kThreads + tid] = 0ull;
   }
   const float lo_f = vld(F.bc.f[BF_LOF]);
   const float hi_f = vld(F.bc.f[BF_HIF]);
@@ -666,7 +658,7 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok
   const float scale = c.fix_scale;
   uint32_t above_c = 0;
   unsigned long long above_m = 0ull;
-  auto bin_one = [&](float x, bool private_bins) {
+  auto bin_one = [&](float x) {
     if (!(lo_all || x > lo_f)) return;
     unsigned long long wf = 0ull;
     if (MASS) wf = __float2ull_rn(weight(x, c.m, c.m_neginf) * scale);
@@ -676,29 +668,19 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok
       return;
     }
     const int b = pivot_bin(qf, x);
-    if (private_bins) {
-      lcnt[b * kThreads + tid] += 1u;
-      if (MASS) lmass[b * kThreads + tid] += wf;
-    } else {
-      atomicAdd(&F.bin_cnt[warp][b], 1u);
-      if (MASS) atomicAdd(&F.bin_mass[warp][b], wf);
-    }
+    lcnt[b * kThreads + tid] += 1u;
+    if (MASS) lmass[b * kThreads + tid] += wf;
   };
-  if (from_chunk) {
-    stream_chunk<DT>(
-        c,
-        [&](const float (&xs)[E], uint32_t, bool valid) {
-          if (!valid) return;
+  stream_chunk<DT>(
+      c,
+      [&](const float (&xs)[E], uint32_t, bool valid) {
+        if (!valid) return;
 #pragma unroll
-          for (int e = 0; e < E; ++e) bin_one(xs[e], true);
-        },
-        [&](float x, uint32_t, bool valid) {
-          if (valid) bin_one(x, true);
-        });
-  } else {
-    const uint32_t n = min(vld(F.own_n), c.ocap);
-    for (uint32_t i = tid; i < n; i += kThreads) bin_one(c.own_val[i], false);
-  }
+        for (int e = 0; e < E; ++e) bin_one(xs[e]);
+      },
+      [&](float x, uint32_t, bool valid) {
+        if (valid) bin_one(x);
+      });
   above_c = warp_sum_u(above_c);
   above_m = warp_sum_u64(above_m);
   if (lane == 0) {
@@ -708,7 +690,7 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok
   }
   __syncthreads();
   Slot& my = F.slots[c.ph & 1];
-  if (from_chunk) {
+  {
     // warp w totals bins w and w + kWarps over the thread columns
     for (int b = warp; b < kBins; b += kWarps) {
       uint32_t s = 0;
@@ -724,15 +706,6 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok
         my.mass[b] = sm;
       }
     }
-  } else if (tid < kBins) {
-    uint32_t s = 0;
-    unsigned long long sm = 0ull;
-    for (int w = 0; w < kWarps; ++w) {
-      s += vld(F.bin_cnt[w][tid]);
-      sm += vld(F.bin_mass[w][tid]);
-    }
-    my.cnt[tid] = s;
-    my.mass[tid] = sm;
   }
   if (tid == kThreads - 1) {
     uint32_t s = 0;
@@ -843,8 +816,7 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool from_chunk, bool value_ok
   R.m_hi = vld(F.bc.x[BX_MHI]);
   R.lo_all = R.lo < kKeyNegInf;
   const uint32_t maxr = vld(F.bc.u[BU_MAXR]);
-  const uint32_t in_range = R.pin_hi ? R.c_lo : R.c_lo - R.c_hi;
-  R.fits = in_range <= c.gcap && maxr <= c.ocap;
+  R.fits = maxr <= c.ocap;
   R.exact = !R.pin_hi && (R.hi - R.lo <= 1u);
   R.below = vld(F.bc.u[BU_BELOW]) != 0u;
   ++R.passes;
@@ -1100,7 +1072,7 @@ __device__ bool wide_pass(Ctx<DT>& c, Range& R) {
   R.lo_all = R.lo < kKeyNegInf;
   R.below = vld(F.bc.u[BU_BELOW]) != 0u;
   const uint32_t maxr = vld(F.bc.u[BU_MAXR]);
-  R.fits = !R.below && (R.c_lo - R.c_hi) <= c.gcap && maxr <= c.ocap;
+  R.fits = !R.below && maxr <= c.ocap;
   R.exact = !R.below && (R.hi - R.lo <= 1u);
   ++R.passes;
   cluster_sync_all();  // every CTA is done reading the others' bin totals
@@ -1108,7 +1080,7 @@ __device__ bool wide_pass(Ctx<DT>& c, Range& R) {
 }
 
 template <int DT, bool MASS>
-__device__ void narrow(Ctx<DT>& c, Range& R, bool from_chunk) {
+__device__ void narrow(Ctx<DT>& c, Range& R) {
   bool value_ok = true;
   R.passes = 0;
   R.fits = false;
@@ -1118,12 +1090,12 @@ __device__ void narrow(Ctx<DT>& c, Range& R, bool from_chunk) {
   while (true) {
     const uint32_t span_before = R.hi - R.lo;
     bool used_value = false;
-    if (from_chunk && !wide_done && wide_pass<DT, MASS>(c, R)) {
+    if (!wide_done && wide_pass<DT, MASS>(c, R)) {
       wide_done = true;
       used_value = true;
       QRITA_T(11);
     } else {
-      narrow_pass<DT, MASS>(c, R, from_chunk, value_ok, &used_value);
+      narrow_pass<DT, MASS>(c, R, value_ok, &used_value);
     }
     if (R.below || R.fits || R.exact) break;
     if (R.passes >= kMaxRounds) break;
@@ -1164,191 +1136,74 @@ __device__ void extract_range(Ctx<DT>& c, const Range& R) {
   QRITA_T(12);
 }
 
-// Copy every rank's own-list entries in (lo, hi] into this CTA's gathered set
-// (value, rank << 28 | index). F.rank_n[r] holds rank r's list length.
-// sync_first: the lists were rewritten since the last cluster barrier. The
-// barrier at the end is the last access to another CTA's memory.
+// The own list as kWarps segments: warp w owns entries [seg_base[w],
+// seg_base[w] + seg_cnt[w]). After the streaming pass (and the second
+// truncation) segment w holds warp w's survivors at w * segcap: publish the
+// counts; F.own_n gets the exact survivor count and F.seg_ovf whether a
+// warp's survivors exceeded its segment.
 template <int DT>
-__device__ void gather(Ctx<DT>& c, float lo_f, float hi_f, bool lo_all, bool sync_first) {
-  Fixed& F = *c.F;
-  if (c.alias) {
-    // one CTA per row: the own list holds exactly the range (an extraction)
-    if (threadIdx.x == 0) F.g_n = min(vld(F.own_n), c.gcap);
-    __syncthreads();
-    return;
-  }
-  if (threadIdx.x == 0) F.g_n = 0;
-  if (sync_first) cluster_sync_all();
-  __syncthreads();
-  const uint32_t val_base = smem_u32(c.own_val);
-  const uint32_t idx_base = smem_u32(c.own_idx);
-  for (uint32_t r = 0; r < c.C; ++r) {
-    const uint32_t n = min(vld(F.rank_n[r]), c.ocap);
-    const uint32_t rv = map_rank(val_base, r);
-    const uint32_t ri = map_rank(idx_base, r);
-    for (uint32_t b = 0; b < n; b += kThreads) {
-      const uint32_t i = b + threadIdx.x;
-      float xs[1] = {0.f};
-      uint32_t idx = 0, bits = 0;
-      if (i < n) {
-        xs[0] = ld_dsmem_f32(rv + 4u * i);
-        idx = ld_dsmem_u32(ri + 4u * i);
-        bits = ((lo_all || xs[0] > lo_f) && !(xs[0] > hi_f)) ? 1u : 0u;
-      }
-      warp_append<1>(&F.g_n, c.g_val, c.g_tag, c.gcap, xs, (r << kTagShift) | idx, bits);
-    }
-  }
-  cluster_sync_all();
-  QRITA_T(13);
-}
-
-// Copy every rank's whole own list into this CTA's gathered set at prefix
-// offsets (rank order), F.rank_n[r] entries from rank r: all loads of a
-// thread are in flight together. The cluster barrier at the end is the last
-// access to another CTA's memory.
-template <int DT>
-__device__ void gather_all(Ctx<DT>& c) {
-  Fixed& F = *c.F;
-  const int tid = threadIdx.x;
-  if (c.alias) {
-    // one CTA per row: the own list is already the gathered set (tags = index)
-    if (tid == 0) F.g_n = min(vld(F.rank_n[0]), c.gcap);
-    __syncthreads();
-    return;
-  }
-  if (tid < 32) {
-    const uint32_t n = tid < static_cast<int>(c.C) ? min(vld(F.rank_n[tid]), c.ocap) : 0u;
-    uint32_t incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(kFull, incl, o);
-      if (tid >= o) incl += t;
-    }
-    if (tid < kMaxCluster) F.rank_off[tid + 1] = incl;
-    if (tid == 0) F.rank_off[0] = 0;
-  }
-  __syncthreads();
-  QRITA_T(8);
-  const uint32_t total = min(vld(F.rank_off[c.C]), c.gcap);
-  const uint32_t val_base = smem_u32(c.own_val);
-  const uint32_t idx_base = smem_u32(c.own_idx);
-  constexpr int U = 4;
-  for (uint32_t base = 0; base < total; base += kThreads * U) {
-    float v[U];
-    uint32_t ix[U], rr[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t i = base + u * kThreads + tid;
-      v[u] = 0.f;
-      ix[u] = 0u;
-      rr[u] = 0u;
-      if (i < total) {
-        uint32_t r = 0;
-        for (uint32_t k = 1; k < c.C; ++k) r += (i >= vld(F.rank_off[k])) ? 1u : 0u;
-        const uint32_t j = i - vld(F.rank_off[r]);
-        v[u] = ld_dsmem_f32(map_rank(val_base, r) + 4u * j);
-        ix[u] = ld_dsmem_u32(map_rank(idx_base, r) + 4u * j);
-        rr[u] = r;
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const uint32_t i = base + u * kThreads + tid;
-      if (i < total) {
-        c.g_val[i] = v[u];
-        c.g_tag[i] = (rr[u] << kTagShift) | ix[u];
-      }
-    }
-  }
-  if (tid == 0) F.g_n = total;
-  QRITA_T(9);
-  cluster_sync_all();
-  QRITA_T(10);
-}
-
-// After an extraction of a range into the own lists: exchange the list
-// lengths and, when every list and their sum fit, gather them whole.
-// Returns whether it gathered (uniform over the cluster).
-template <int DT>
-__device__ bool gather_extracted(Ctx<DT>& c) {
-  Fixed& F = *c.F;
-  const int tid = threadIdx.x, lane = tid & 31;
-  cluster_sync_all();  // every rank's list is complete
-  if (tid < 32) {
-    uint32_t n = 0;
-    if (lane < static_cast<int>(c.C)) {
-      n = ld_dsmem_u32(map_rank(smem_u32(&F.own_n), lane));
-      F.rank_n[lane] = n;
-    }
-    uint32_t tot = __reduce_add_sync(kFull, n);
-    const uint32_t mx = __reduce_max_sync(kFull, n);
-    if (lane == 0) F.bc.u[BU_FITS] = (tot <= c.gcap && mx <= c.ocap) ? 1u : 0u;
-  }
-  __syncthreads();
-  if (vld(F.bc.u[BU_FITS]) == 0u) return false;
-  gather_all<DT>(c);
-  return true;
-}
-
-// After the streaming pass: move the warps' segments of the own list
-// together (segment w holds its survivors at w * segcap), so the list is
-// [0, own_n). F.own_n gets the exact survivor count; F.seg_ovf is set (and
-// nothing moves) when a warp's survivors exceeded its segment.
-template <int DT>
-__device__ void compact_segments(Ctx<DT>& c, uint32_t wn) {
+__device__ void own_segments_streamed(Ctx<DT>& c, uint32_t wn) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t segcap = c.ocap / kWarps;
-  if (lane == 0) F.seg_n[warp] = wn;
+  if (lane == 0) {
+    F.seg_n[warp] = wn;
+    F.seg_base[warp] = static_cast<uint32_t>(warp) * segcap;
+    F.seg_cnt[warp] = min(wn, segcap);
+  }
   __syncthreads();
-  uint32_t total = 0, mine_off = 0;
-  bool ovf = false;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const uint32_t n = vld(F.seg_n[w]);
-    if (w < warp) mine_off += n;
-    total += n;
-    ovf = ovf || n > segcap;
-  }
-  if (!ovf) {
-    if (total <= segcap) {
-      // every destination lies below segcap: clear of every source that moves
-      if (warp > 0) {
-        const uint32_t src = static_cast<uint32_t>(warp) * segcap;
-        for (uint32_t i = lane; i < wn; i += 32) {
-          c.own_val[mine_off + i] = c.own_val[src + i];
-          c.own_idx[mine_off + i] = c.own_idx[src + i];
-        }
-      }
-    } else {
-      // segments in order, each moved down in block-wide rounds (read, barrier,
-      // write, barrier): a round's writes reach no source still to be read
-      uint32_t off = vld(F.seg_n[0]);
-      for (int w = 1; w < kWarps; ++w) {
-        const uint32_t n = vld(F.seg_n[w]);
-        const uint32_t src = static_cast<uint32_t>(w) * segcap;
-        for (uint32_t b = 0; b < n; b += kThreads) {
-          const uint32_t i = b + tid;
-          float v = 0.f;
-          uint32_t ix = 0;
-          if (i < n) {
-            v = c.own_val[src + i];
-            ix = c.own_idx[src + i];
-          }
-          __syncthreads();
-          if (i < n) {
-            c.own_val[off + i] = v;
-            c.own_idx[off + i] = ix;
-          }
-          __syncthreads();
-        }
-        off += n;
-      }
-    }
-  }
   if (tid == 0) {
+    uint32_t total = 0;
+    bool ovf = false;
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t n = vld(F.seg_n[w]);
+      total += n;
+      ovf = ovf || n > segcap;
+    }
     F.own_n = total;
     F.seg_ovf = ovf ? 1u : 0u;
+  }
+  __syncthreads();
+}
+
+// After an extraction (entries [0, own_n) of the own list): eight equal
+// slices, one per warp.
+template <int DT>
+__device__ void own_segments_contiguous(Ctx<DT>& c) {
+  Fixed& F = *c.F;
+  if (threadIdx.x == 0) {
+    const uint32_t total = vld(F.own_n);
+    const uint32_t n = min(total, c.ocap);
+    const uint32_t slice = (n + kWarps - 1u) / kWarps;
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t b = min(static_cast<uint32_t>(w) * slice, n);
+      F.seg_base[w] = b;
+      F.seg_cnt[w] = min(slice, n - b);
+    }
+    F.seg_ovf = total > c.ocap ? 1u : 0u;
+  }
+  __syncthreads();
+}
+
+// fn(value, index) over this warp's segment of the own list (lanes stride;
+// no collective operations inside fn).
+template <int DT, typename Fn>
+__device__ __forceinline__ void own_for(Ctx<DT>& c, Fn&& fn) {
+  Fixed& F = *c.F;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t base = vld(F.seg_base[warp]), n = vld(F.seg_cnt[warp]);
+  for (uint32_t i = static_cast<uint32_t>(lane); i < n; i += 32u) fn(c.own_val[base + i], c.own_idx[base + i]);
+}
+
+// Per-rank own-list counts above the search's lo and hi (F.rank_lo,
+// F.rank_hi): n[r] entries of rank r lie above lo, none above hi.
+template <int DT>
+__device__ void rank_counts_from(Ctx<DT>& c, const uint32_t* n) {
+  Fixed& F = *c.F;
+  if (threadIdx.x < static_cast<int>(c.C)) {
+    const uint32_t v = vld(n[threadIdx.x]);
+    F.rank_lo[threadIdx.x] = v;
+    F.rank_hi[threadIdx.x] = 0u;
   }
   __syncthreads();
 }
@@ -1462,7 +1317,7 @@ __device__ void retry_pass(Ctx<DT>& c, float t2) {
         seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, (valid && x >= t2) ? 1u : 0u);
       },
       false);
-  compact_segments<DT>(c, wn);
+  own_segments_streamed<DT>(c, wn);
   Slot& my = F.slots[c.ph & 1];
   if (tid == 0) {
     my.u[0] = vld(F.seg_ovf);
@@ -1588,19 +1443,73 @@ __device__ __forceinline__ bool count_interp_pivots(uint32_t lo, uint32_t hi, ui
   return pivots_at(lo, hi, mid - d, mid, mid + d, q);
 }
 
-// Tail of the search: once the range holds at most kTail elements they are
-// copied out and each tests itself as the boundary (one thread each).
-constexpr int kTail = kThreads;
-
-template <int DT, bool MASS>
-__device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots) {
+// One cluster merge of a per-CTA count, mass and overflow flag (thread 0's
+// arguments are what this CTA publishes): afterwards F.rank_n[r] is rank r's
+// count, F.bc.u[BU_S2] the row total, F.bc.u[BU_MAXR] the largest count,
+// F.bc.u[BU_OVF2] whether any rank flagged (or exceeded the list capacity)
+// and F.bc.x[BX_MLO] the row's mass.
+template <int DT>
+__device__ void merge_count_mass(Ctx<DT>& c, uint32_t n, unsigned long long m, uint32_t ovf) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t gn = min(vld(F.g_n), c.gcap);
+  Slot& my = F.slots[c.ph & 1];
+  if (tid == 0) {
+    my.u[0] = n;
+    my.u[1] = ovf;
+    my.mass[0] = m;
+  }
+  cluster_sync_all();
+  if (warp == 0) {
+    uint32_t rn = 0, ro = 0;
+    unsigned long long rm = 0ull;
+    if (lane < static_cast<int>(c.C)) {
+      const uint32_t ub = map_rank(smem_u32(&my.u[0]), static_cast<uint32_t>(lane));
+      rn = ld_dsmem_u32(ub);
+      ro = ld_dsmem_u32(ub + 4u);
+      const uint32_t mb = map_rank(smem_u32(&my.mass[0]), static_cast<uint32_t>(lane));
+      rm = static_cast<unsigned long long>(ld_dsmem_u32(mb)) |
+           (static_cast<unsigned long long>(ld_dsmem_u32(mb + 4u)) << 32);
+      ro |= rn > c.ocap ? 1u : 0u;
+      F.rank_n[lane] = rn;
+    }
+    const uint32_t tot = __reduce_add_sync(kFull, rn);
+    const uint32_t mx = __reduce_max_sync(kFull, rn);
+    const uint32_t o = __reduce_or_sync(kFull, ro);
+    const unsigned long long tm = warp_sum_u64_redux(rm);
+    if (lane == 0) {
+      F.bc.u[BU_S2] = tot;
+      F.bc.u[BU_MAXR] = mx;
+      F.bc.u[BU_OVF2] = o;
+      F.bc.x[BX_MLO] = tm;
+    }
+  }
+  __syncthreads();
+  ++c.ph;
+}
+
+// Tail of the search: once the range holds at most kTail elements (over the
+// whole row) they are copied to every CTA and each tests itself as the
+// boundary (one thread each).
+constexpr int kTail = kThreads;
+
+// Quaternary search (A6 for counts, A7 for mass) over the own lists of the
+// cluster. The search keeps count/mass(> lo) >= target > count/mass(> hi);
+// each round evaluates three pivots: every CTA counts (and weighs) its own
+// list, the CTAs' partials are merged through distributed shared memory, and
+// every CTA takes the same decision: stop at the first pivot whose z_mn is
+// the boundary (above(q) reaches the target and above(q) minus the N_zmn
+// copies of z_mn does not), else move lo / hi. Masses are exact sums of
+// fixed-point weights, so every decision is integer arithmetic.
+// On entry F.rank_lo / F.rank_hi hold each rank's own-list counts above lo /
+// hi; s.c_above / s.m_above count what lies above the lists' range. On exit
+// F.ties holds each rank's count of the boundary value.
+template <int DT, bool MASS>
+__device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float scale = c.fix_scale;
-  // the search state is held, identical, by every thread (by warp 0 alone in
-  // the tail): one block barrier per block round, the warps' partials
-  // double-buffered
+  const int C = static_cast<int>(c.C);
+  // the search state is held, identical, by every thread of every CTA
   uint32_t lo = s.lo, hi = s.hi, c_lo = s.c_lo, c_hi = s.c_hi;
   unsigned long long m_lo = s.m_lo, m_hi = s.m_hi;
   uint32_t tau = 0, n_keep = 0, cabove = 0;
@@ -1616,6 +1525,8 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
   } else {
     np = quartile_pivots(lo, hi, value_pivots, q[0], q[1], q[2], used_value);
   }
+  int done_j = -1, lo_j = -1, hi_j = -1;
+  bool collapsed = false;  // (lo, hi] holds one key: the boundary is hi
   // the boundary is the single key hi of (lo, hi]: keep the copies needed
   auto one_key = [&]() {
     tau = hi;
@@ -1627,10 +1538,8 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
       n_keep = static_cast<uint32_t>(target) - c_hi;
     }
     done = 1;
+    collapsed = true;
   };
-  // One round's decision from the totals above the pivots (counts and
-  // masses over the whole row): stop at the first pivot whose z_mn is the
-  // boundary, else move lo / hi and choose the next pivots.
   int rounds = 0;
   auto decide = [&](const uint32_t (&tc)[3], const uint32_t (&tz)[3], const uint32_t (&tn)[3],
                     const unsigned long long (&tm)[3]) {
@@ -1645,10 +1554,11 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
       stop[j] = reach[j] && below[j] < target;
     }
     // the first pivot (in increasing order) whose z_mn is the boundary
-    int done_j = -1;
+    done_j = -1;
     if (stop[0]) done_j = 0;
     else if (reach[0] && stop[1]) done_j = 1;
     else if (reach[0] && reach[1] && stop[2]) done_j = 2;
+    lo_j = hi_j = -1;
     if (done_j >= 0) {
       const uint32_t z = done_j == 0 ? tz[0] : (done_j == 1 ? tz[1] : tz[2]);
       const uint32_t n = done_j == 0 ? tn[0] : (done_j == 1 ? tn[1] : tn[2]);
@@ -1666,8 +1576,8 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
     }
     // the highest pivot that reaches the target becomes lo, the lowest that
     // does not becomes hi
-    const int lo_j = !reach[0] ? -1 : (!reach[1] || np < 2 ? 0 : (!reach[2] || np < 3 ? 1 : 2));
-    const int hi_j = !reach[0] ? 0 : (np < 2 ? -1 : (!reach[1] ? 1 : (np < 3 ? -1 : (!reach[2] ? 2 : -1))));
+    lo_j = !reach[0] ? -1 : (!reach[1] || np < 2 ? 0 : (!reach[2] || np < 3 ? 1 : 2));
+    hi_j = !reach[0] ? 0 : (np < 2 ? -1 : (!reach[1] ? 1 : (np < 3 ? -1 : (!reach[2] ? 2 : -1))));
     const uint32_t old_span = hi - lo;
     if (lo_j >= 0) {
       lo = lo_j == 0 ? q[0] : (lo_j == 1 ? q[1] : q[2]);
@@ -1704,15 +1614,14 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
     }
   };
   if (np == 0) one_key();
-  // block rounds over the gathered set while the range is large
+  // rounds over the own lists while the range is large
   while (done == 0 && c_lo - c_hi > static_cast<uint32_t>(kTail)) {
     float qf[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) qf[j] = j < np ? pivot_f(q[j]) : INFINITY;
     uint32_t cnt[3] = {0u, 0u, 0u}, zk[3] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu}, nz[3] = {0u, 0u, 0u};
     unsigned long long ms[3] = {0ull, 0ull, 0ull};
-    for (uint32_t i = tid; i < gn; i += kThreads) {
-      const float x = c.g_val[i];
+    own_for(c, [&](float x, uint32_t) {
       const uint32_t key = f2key(x);
       const unsigned long long wf = MASS ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
 #pragma unroll
@@ -1724,7 +1633,7 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
         nz[j] = lt ? 1u : nz[j] + ((g && key == zk[j]) ? 1u : 0u);
         zk[j] = lt ? key : zk[j];
       }
-    }
+    });
     LPart(&buf)[kWarps][3] = F.lred[rounds & 1];
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
@@ -1740,59 +1649,132 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
       }
     }
     __syncthreads();
-    ++rounds;
-    // every warp totals the partials (lanes 0..kWarps-1 hold one warp's each)
-    uint32_t tc[3], tz[3], tn[3];
-    unsigned long long tm[3];
+    Slot& my = F.slots[c.ph & 1];
+    if (warp == 0) {
+      // this CTA's totals over its warps, published for the cluster
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const bool own = lane < kWarps;
-      const volatile LPart& pp = buf[own ? lane : 0][j];
-      const uint32_t cw = own ? pp.cnt : 0u;
-      const uint32_t zw = own ? pp.zmin : 0xFFFFFFFFu;
-      const uint32_t nw = own ? pp.nz : 0u;
-      const unsigned long long mw = (MASS && own) ? pp.mass : 0ull;
-      tc[j] = __reduce_add_sync(kFull, cw) + s.c_above;
-      tz[j] = __reduce_min_sync(kFull, zw);
-      tn[j] = __reduce_add_sync(kFull, zw == tz[j] ? nw : 0u);
-      tm[j] = MASS ? warp_sum_u64_redux(mw) + s.m_above : 0ull;
+      for (int j = 0; j < 3; ++j) {
+        const bool own = lane < kWarps;
+        const volatile LPart& pp = buf[own ? lane : 0][j];
+        const uint32_t cw = own ? pp.cnt : 0u;
+        const uint32_t zw = own ? pp.zmin : 0xFFFFFFFFu;
+        const uint32_t nw = own ? pp.nz : 0u;
+        const unsigned long long mw = (MASS && own) ? pp.mass : 0ull;
+        const uint32_t lc = __reduce_add_sync(kFull, cw);
+        const uint32_t lz = __reduce_min_sync(kFull, zw);
+        const uint32_t ln = __reduce_add_sync(kFull, zw == lz ? nw : 0u);
+        const unsigned long long lm = MASS ? warp_sum_u64_redux(mw) : 0ull;
+        if (lane == 0) {
+          my.cnt[j] = lc;
+          my.cnt[3 + j] = lz;
+          my.cnt[6 + j] = ln;
+          my.mass[j] = lm;
+        }
+      }
     }
-    decide(tc, tz, tn, tm);
-  }
-  __syncthreads();  // every warp has read the last block round's partials
-  QRITA_T(12);
-  if (done == 0) {
-    // tail: the (lo, hi] elements of the gathered set (c_lo - c_hi of them)
-    // to shared memory; each tests itself as the boundary
-    if (tid == 0) {
-      F.tail_n = 0u;
-      F.bc.u[BU_DONE] = 2u;  // unless a candidate answers (it always does)
-    }
-    __syncthreads();
-    for (uint32_t b = 0; b < gn; b += kThreads) {
-      const uint32_t i = b + tid;
-      const float x = i < gn ? c.g_val[i] : -INFINITY;
-      const uint32_t key = f2key(x);  // keys: lo may lie below key(-inf)
-      const bool in = i < gn && key > lo && key <= hi;
-      const uint32_t bal = __ballot_sync(kFull, in);
-      uint32_t base = 0;
-      if (lane == 0 && bal != 0u) base = atomicAdd(&F.tail_n, static_cast<uint32_t>(__popc(bal)));
-      base = __shfl_sync(kFull, base, 0);
-      if (in) {
-        const uint32_t pos = base + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
-        if (pos < static_cast<uint32_t>(kTail)) {
-          F.tail_val[pos] = x;
-          if (MASS) F.tail_w[pos] = weight_fx(x, c.m, c.m_neginf, scale);
+    cluster_sync_all();
+    if (warp == 0) {
+      // lane r reads rank r's totals; the row's totals and per-rank shares
+#pragma unroll
+      for (int j = 0; j < 3; ++j) {
+        uint32_t rc = 0, rz = 0xFFFFFFFFu, rn = 0;
+        unsigned long long rm = 0ull;
+        if (lane < C) {
+          const uint32_t cb = map_rank(smem_u32(&my.cnt[0]), static_cast<uint32_t>(lane));
+          rc = ld_dsmem_u32(cb + 4u * j);
+          rz = ld_dsmem_u32(cb + 4u * (3 + j));
+          rn = ld_dsmem_u32(cb + 4u * (6 + j));
+          if (MASS) {
+            const uint32_t mb = map_rank(smem_u32(&my.mass[j]), static_cast<uint32_t>(lane));
+            rm = static_cast<unsigned long long>(ld_dsmem_u32(mb)) |
+                 (static_cast<unsigned long long>(ld_dsmem_u32(mb + 4)) << 32);
+          }
+        }
+        const uint32_t gz = __reduce_min_sync(kFull, rz);
+        const uint32_t gc = __reduce_add_sync(kFull, rc);
+        const uint32_t gn = __reduce_add_sync(kFull, rz == gz ? rn : 0u);
+        const unsigned long long gm = MASS ? warp_sum_u64_redux(rm) : 0ull;
+        if (lane < C) {
+          F.pr_cnt[lane][j] = rc;
+          F.pr_nz[lane][j] = rz == gz ? rn : 0u;
+        }
+        if (lane == 0) {
+          F.dtot[0][j] = gc;
+          F.dtot[1][j] = gz;
+          F.dtot[2][j] = gn;
+          F.dmass[j] = gm;
         }
       }
     }
     __syncthreads();
+    ++c.ph;
+    ++rounds;
+    uint32_t tc[3], tz[3], tn[3];
+    unsigned long long tm[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      tc[j] = vld(F.dtot[0][j]) + s.c_above;
+      tz[j] = vld(F.dtot[1][j]);
+      tn[j] = vld(F.dtot[2][j]);
+      tm[j] = MASS ? vld(F.dmass[j]) + s.m_above : 0ull;
+    }
+    decide(tc, tz, tn, tm);
+    // per-rank bookkeeping of the decision (identical in every thread)
+    if (tid < C) {
+      if (done_j >= 0) {
+        F.ties[tid] = vld(F.pr_nz[tid][done_j]);
+      } else {
+        if (lo_j >= 0) F.rank_lo[tid] = vld(F.pr_cnt[tid][lo_j]);
+        if (hi_j >= 0) F.rank_hi[tid] = vld(F.pr_cnt[tid][hi_j]);
+        if (collapsed) F.ties[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
+      }
+    }
+    __syncthreads();
+  }
+  if (done == 1 && collapsed && rounds == 0) {
+    // the start range held one key
+    if (tid < C) F.ties[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
+    __syncthreads();
+  }
+  if (done == 0) {
+    // tail: every CTA's (lo, hi] elements (rank_lo - rank_hi of them) are
+    // stored into every CTA's tail buffer at the rank's offset
+    uint32_t off = 0;
+    for (int r = 0; r < static_cast<int>(c.crank); ++r) off += vld(F.rank_lo[r]) - vld(F.rank_hi[r]);
+    uint32_t total = 0;
+    for (int r = 0; r < C; ++r) total += vld(F.rank_lo[r]) - vld(F.rank_hi[r]);
+    total = min(total, static_cast<uint32_t>(kTail));
+    if (tid == 0) {
+      F.tail_n = 0u;
+      F.bc.u[BU_DONE] = 2u;  // unless a candidate answers (one always does)
+    }
+    __syncthreads();
+    own_for(c, [&](float x, uint32_t) {
+      const uint32_t key = f2key(x);  // keys: lo may lie below key(-inf)
+      if (key > lo && key <= hi) {
+        const uint32_t dst = off + atomicAdd(&F.tail_n, 1u);
+        if (dst < static_cast<uint32_t>(kTail)) {
+          const unsigned long long w = MASS ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
+          for (int r = 0; r < C; ++r) {
+            const uint32_t rr = static_cast<uint32_t>(r);
+            st_dsmem_u32(map_rank(smem_u32(&F.tail_val[dst]), rr), __float_as_uint(x));
+            st_dsmem_u8(map_rank(smem_u32(&F.tail_rank[dst]), rr), c.crank);
+            if (MASS) {
+              const uint32_t a = map_rank(smem_u32(&F.tail_w[dst]), rr);
+              st_dsmem_u32(a, static_cast<uint32_t>(w));
+              st_dsmem_u32(a + 4u, static_cast<uint32_t>(w >> 32));
+            }
+          }
+        }
+      }
+    });
+    cluster_sync_all();  // every CTA's tail buffer is complete
     QRITA_T(13);
-    // every candidate v of the range tests itself: it is the boundary when
-    // count(> v) < target <= count(>= v) (masses likewise), which is where
-    // further quaternary rounds would stop (tau = v = z_mn, N_zmn = N(v))
-    const uint32_t tn_all = min(vld(F.tail_n), static_cast<uint32_t>(kTail));
-    if (tid < static_cast<int>(tn_all)) {
+    // every candidate v tests itself: it is the boundary when count(> v) <
+    // target <= count(>= v) (masses likewise), where further quaternary
+    // rounds would stop (tau = v = z_mn, N_zmn = N(v))
+    if (tid < C) F.ties[tid] = 0u;
+    if (tid < static_cast<int>(total)) {
       // the buffer is complete (barrier above) and unchanged from here on:
       // plain loads, eight in flight
       const float* tv = F.tail_val;
@@ -1801,22 +1783,22 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
       uint32_t gt = 0, eq = 0;
       unsigned long long mgt = 0ull;
       uint32_t i = 0;
-      for (; i + 8u <= tn_all; i += 8u) {
-        float x[8];
+      for (; i + 8u <= total; i += 8u) {
+        float xv[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = tv[i + u];
+        for (int u = 0; u < 8; ++u) xv[u] = tv[i + u];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          gt += x[u] > v ? 1u : 0u;
-          eq += x[u] == v ? 1u : 0u;
-          if (MASS) mgt += x[u] > v ? tw[i + u] : 0ull;
+          gt += xv[u] > v ? 1u : 0u;
+          eq += xv[u] == v ? 1u : 0u;
+          if (MASS) mgt += xv[u] > v ? tw[i + u] : 0ull;
         }
       }
-      for (; i < tn_all; ++i) {
-        const float x = tv[i];
-        gt += x > v ? 1u : 0u;
-        eq += x == v ? 1u : 0u;
-        if (MASS) mgt += x > v ? tw[i] : 0ull;
+      for (; i < total; ++i) {
+        const float xv = tv[i];
+        gt += xv > v ? 1u : 0u;
+        eq += xv == v ? 1u : 0u;
+        if (MASS) mgt += xv > v ? tw[i] : 0ull;
       }
       const unsigned long long above_gt = MASS ? mgt + m_hi : static_cast<unsigned long long>(gt + c_hi);
       const unsigned long long wv = MASS ? tw[tid] : 1ull;
@@ -1830,13 +1812,14 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
         F.bc.u[BU_DONE] = 1u;
       }
     }
-    if (tid == 0) F.bc.u[BU_NP] = static_cast<uint32_t>(rounds + 1);
     __syncthreads();
     tau = vld(F.bc.u[BU_TAU]);
     n_keep = vld(F.bc.u[BU_NKEEP]);
     cabove = vld(F.bc.u[BU_CABOVE]);
     done = static_cast<int>(vld(F.bc.u[BU_DONE]));
-    rounds = static_cast<int>(vld(F.bc.u[BU_NP]));
+    ++rounds;
+    // per-rank copies of the boundary value
+    if (tid < static_cast<int>(total) && F.tail_val[tid] == key2f(tau)) atomicAdd(&F.ties[F.tail_rank[tid]], 1u);
     __syncthreads();
   }
   (void)m_lo;
@@ -1848,18 +1831,6 @@ __device__ void local_search(Ctx<DT>& c, Local& s, unsigned long long target, bo
   s.capped = done == 2;
 }
 
-// Per-rank counts of gathered entries equal to tau (into F.ties).
-template <int DT>
-__device__ void count_ties_gathered(Ctx<DT>& c, float tau_f) {
-  Fixed& F = *c.F;
-  if (threadIdx.x < kMaxCluster) F.ties[threadIdx.x] = 0u;
-  __syncthreads();
-  const uint32_t gn = min(vld(F.g_n), c.gcap);
-  for (uint32_t i = threadIdx.x; i < gn; i += kThreads)
-    if (c.g_val[i] == tau_f) atomicAdd(&F.ties[c.g_tag[i] >> kTagShift], 1u);
-  __syncthreads();
-}
-
 // The index below which exactly `keep` of this CTA's own-list entries equal
 // to tau lie (the own list holds every such element of the chunk). 16-way
 // splits of the index range; invariant count(idx < lo) < keep <= count(idx < hi).
@@ -1867,7 +1838,6 @@ template <int DT>
 __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t n = min(vld(F.own_n), c.ocap);
   uint32_t lo = 0, hi = static_cast<uint32_t>(c.n);
   for (int round = 0; round < 32 && hi - lo > 1u; ++round) {
     const uint32_t span = hi - lo;
@@ -1881,13 +1851,12 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
     uint32_t cnt[15];
 #pragma unroll
     for (int j = 0; j < 15; ++j) cnt[j] = 0;
-    for (uint32_t i = tid; i < n; i += kThreads) {
-      if (c.own_val[i] == tau_f) {
-        const uint32_t ix = c.own_idx[i];
+    own_for(c, [&](float x, uint32_t ix) {
+      if (x == tau_f) {
 #pragma unroll
         for (int j = 0; j < 15; ++j) cnt[j] += (ix < piv[j]) ? 1u : 0u;
       }
-    }
+    });
 #pragma unroll
     for (int j = 0; j < 15; ++j) {
       const uint32_t v = warp_sum_u(cnt[j]);
@@ -1921,26 +1890,17 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   Ctx<DT> c;
   c.F = &F;
   c.ocap = static_cast<uint32_t>(P.ocap);
-  c.gcap = static_cast<uint32_t>(P.gcap);
   c.lists = smem + sizeof(Fixed);
   {
-    unsigned char* ring = c.lists + (list_region_bytes(static_cast<int>(P.C), P.ocap, P.gcap) - kRingBytes);
+    unsigned char* ring = c.lists + (list_region_bytes(P.ocap) - kRingBytes);
     c.ring = smem_u32(ring);
     c.ring_ptr = reinterpret_cast<const uint4*>(ring);
     c.ring_bar = smem_u32(&c.F->ring_bar[0]);
     c.ring_phase = 0u;
     c.ring_out = 0u;
   }
-  c.alias = P.C == 1;
   c.own_val = reinterpret_cast<float*>(c.lists);
   c.own_idx = reinterpret_cast<uint32_t*>(c.own_val + P.ocap);
-  if (c.alias) {
-    c.g_val = c.own_val;
-    c.g_tag = c.own_idx;
-  } else {
-    c.g_val = reinterpret_cast<float*>(c.own_idx + P.ocap);
-    c.g_tag = reinterpret_cast<uint32_t*>(c.g_val + P.gcap);
-  }
   c.C = static_cast<uint32_t>(P.C);
   c.crank = cluster_rank();
   c.ph = 0;
@@ -2191,7 +2151,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     if (p_only) streaming_pass(BoolC<true>{});
     else streaming_pass(BoolC<false>{});
     QRITA_T(2);
-    if (trunc) compact_segments<DT>(c, wn);
+    own_segments_streamed<DT>(c, trunc ? wn : 0u);
     // block reduce
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -2311,7 +2271,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     const float cf = ref_ok ? expf(m_ref - row_max) : 0.f;
     const F2 Zm = f2_mul(Zr, cf), Mm = f2_mul(Mr, cf);
 
-    bool k_full = false;  // the gathered set holds the whole top-k set S_k
+    bool k_full = false;  // the own lists hold every element of S_k above tau_k
     uint32_t tau_k = 0, nk_k = 0, above_k = 0;
     if (k_on) {
       const uint32_t target = static_cast<uint32_t>(kr);
@@ -2325,13 +2285,22 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       s.m_above = 0ull;
       s.m_lo = s.m_hi = 0ull;
       bool have_exact = false;
-      // second truncation: when the first threshold missed (or left too many
-      // candidates), an order statistic of a larger sample of the row whose
-      // expected survivors fit the gathered set
-      bool retried = false;
+      bool searched = false;  // the search ran on the own lists' survivors
       uint32_t qk = 0, S2 = 0;
       bool ovf2 = true;
-      if (!hit && !force_fb) {
+      if (hit) {
+        // Z_t is in the own lists: the candidates are (key(t) - 1, max]
+        rank_counts_from<DT>(c, F.rank_n);
+        s.lo = f2key(t) - 1u;
+        s.c_lo = survivors;
+        s.hi = f2key(row_max);
+        s.c_hi = 0;
+        dsearch<DT, false>(c, s, target, value_pivots);
+        searched = true;
+      } else if (!force_fb) {
+        // second truncation: when the first threshold missed (or left too many
+        // candidates), an order statistic of a larger sample of the row whose
+        // expected survivors fit the own lists
         const int n_s = V < kRetrySample ? V : kRetrySample;
         uint32_t jq;
         if (V <= kRetrySample) {
@@ -2341,44 +2310,32 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           jq = static_cast<uint32_t>(ceilf(lam + 4.0f * sqrtf(lam) + 4.0f));
         }
         const float expect = static_cast<float>(jq) * static_cast<float>(V) / static_cast<float>(n_s);
-        if (jq <= static_cast<uint32_t>(n_s) && expect <= 0.7f * static_cast<float>(c.gcap) &&
-            expect <= 0.7f * static_cast<float>(c.ocap) * static_cast<float>(c.C)) {
+        if (jq <= static_cast<uint32_t>(n_s) &&
+            expect <= 0.75f * static_cast<float>(c.ocap) * static_cast<float>(c.C)) {
           path |= QRITA_PATH_RETRY;
           qk = sample_order_key<DT>(c, grow, V, jq);
           retry_pass<DT>(c, key2f(qk));
           S2 = vld(F.bc.u[BU_S2]);
           ovf2 = vld(F.bc.u[BU_OVF2]) != 0u;
-          if (!ovf2 && S2 >= target && S2 <= c.gcap) {
-            // gather Z_t2 whole: the candidates are (key(t2) - 1, max]
-            gather_all<DT>(c);
+          if (!ovf2 && S2 >= target) {
+            // Z_t2 is in the own lists: the candidates are (key(t2) - 1, max]
+            rank_counts_from<DT>(c, F.rank_n);
             s.lo = qk - 1u;
             s.c_lo = S2;
             s.hi = f2key(row_max);
             s.c_hi = 0;
-            k_full = true;
-            list_emit = true;
-            ties_in_list = true;
-            local_search<DT, false>(c, s, target, value_pivots);
-            retried = true;
+            dsearch<DT, false>(c, s, target, value_pivots);
+            searched = true;
           }
         }
       }
-      if (!hit && !retried) path |= QRITA_PATH_FALLBACK;
-      if (retried) {
-        // the search above ran on Z_t2
-      } else if (hit && survivors <= c.gcap) {
-        // gather Z_t whole: the candidates are (key(t) - 1, max]
-        gather_all<DT>(c);
-        s.lo = f2key(t) - 1u;
-        s.c_lo = survivors;
-        s.hi = f2key(row_max);
-        s.c_hi = 0;
+      if (searched) {
         k_full = true;
         list_emit = true;
         ties_in_list = true;
-        local_search<DT, false>(c, s, target, value_pivots);
       } else {
-        // narrow: over the survivor lists on a hit, over the chunk otherwise
+        // narrow over the chunk, then search the extracted range
+        path |= QRITA_PATH_FALLBACK;
         Range R;
         R.pin_hi = false;
         R.m_lo = R.m_hi = 0ull;
@@ -2386,29 +2343,22 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         R.target_from_total = false;
         R.p_frac = 0.f;
         R.extra = 0ull;
-        if (hit) {
-          R.lo = f2key(t) - 1u;
-          R.c_lo = survivors;
-          R.hi = f2key(row_max);
-          R.c_hi = 0;
-        } else {
-          R.lo = f2key(row_min) - 1u;
-          R.c_lo = static_cast<uint32_t>(V);
-          const bool miss_t = trunc && !overflow && survivors < target;
-          const bool miss_t2 = !ovf2 && S2 < target;  // the second threshold missed too
-          R.hi = f2key(row_max);
-          R.c_hi = 0u;
-          if (miss_t) {
-            R.hi = f2key(t) - 1u;
-            R.c_hi = survivors;
-          }
-          if (miss_t2 && S2 >= R.c_hi) {
-            R.hi = qk - 1u;
-            R.c_hi = S2;
-          }
+        R.lo = f2key(row_min) - 1u;
+        R.c_lo = static_cast<uint32_t>(V);
+        const bool miss_t = trunc && !overflow && survivors < target;
+        const bool miss_t2 = !ovf2 && S2 < target;  // the second threshold missed too
+        R.hi = f2key(row_max);
+        R.c_hi = 0u;
+        if (miss_t) {
+          R.hi = f2key(t) - 1u;
+          R.c_hi = survivors;
+        }
+        if (miss_t2 && S2 >= R.c_hi) {
+          R.hi = qk - 1u;
+          R.c_hi = S2;
         }
         R.lo_all = R.lo < kKeyNegInf;
-        narrow<DT, false>(c, R, !hit);
+        narrow<DT, false>(c, R);
         passes += static_cast<uint32_t>(R.passes);
         if (R.exact) {
           s.tau = R.hi;
@@ -2417,42 +2367,32 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           s.rounds = 0;
           s.capped = false;
           have_exact = true;
-          if (warp == 0 && lane < static_cast<int>(c.C))
-            F.ties[lane] = vld(F.rank_lo[lane]) - vld(F.rank_hi[lane]);
+          if (tid < static_cast<int>(c.C)) F.ties[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
           __syncthreads();
-          ties_known = true;
         } else if (!R.fits) {
           s.capped = true;
           s.rounds = 0;
         } else {
-          if (!hit) {
-            extract_range<DT>(c, R);
-            // an extraction leaves exactly each rank's range in its list
-            if (warp == 0 && lane < static_cast<int>(c.C))
-              F.rank_n[lane] = R.pin_hi ? vld(F.rank_lo[lane]) : vld(F.rank_lo[lane]) - vld(F.rank_hi[lane]);
-            __syncthreads();
+          extract_range<DT>(c, R);
+          own_segments_contiguous<DT>(c);
+          // each rank's list holds exactly its part of the range
+          if (tid < static_cast<int>(c.C)) {
+            F.rank_lo[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
+            F.rank_hi[tid] = 0u;
           }
-          const float glo = R.lo_all ? -INFINITY : pivot_f(R.lo);
-          const float ghi = R.pin_hi ? INFINITY : pivot_f(R.hi);
-          gather<DT>(c, glo, ghi, R.lo_all, !hit);
+          __syncthreads();
           s.lo = R.lo;
           s.c_lo = R.c_lo;
-          if (R.pin_hi) {
-            // everything above lo is gathered
-            s.hi = f2key(row_max);
-            s.c_hi = 0;
-            s.c_above = 0;
-          } else {
-            s.hi = R.hi;
-            s.c_hi = R.c_hi;
-            s.c_above = R.c_hi;  // elements above hi exceed every pivot
-          }
-          k_full = R.c_hi == 0u;  // nothing lies above the gathered range
-          list_emit = hit;
+          s.hi = R.hi;
+          s.c_hi = R.c_hi;
+          s.c_above = R.c_hi;  // elements above hi exceed every pivot
+          dsearch<DT, false>(c, s, target, value_pivots);
+          k_full = R.c_hi == 0u;  // nothing lies above the extracted range
+          list_emit = false;
           ties_in_list = true;
-          local_search<DT, false>(c, s, target, value_pivots);
         }
       }
+      (void)have_exact;
       rounds_k = static_cast<uint32_t>(s.rounds);
       if (s.capped) {
         sel_none = true;
@@ -2464,53 +2404,61 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       tau = tau_k;
       n_keep = nk_k;
       count_above = above_k;
-      if (!sel_none && !have_exact) {
-        count_ties_gathered<DT>(c, key2f(tau));
-        ties_known = true;
-      }
+      ties_known = !sel_none;
     }
 
     QRITA_T(4);
     bool extracted_above_k = false;  // the own lists hold exactly {x > tau_k}
-    if (p_on && k_on && !k_full && !sel_none && above_k <= c.gcap) {
-      // S_k without its boundary copies is {x > tau_k}: extract and gather it
+    if (p_on && k_on && !k_full && !sel_none) {
+      // S_k without its boundary copies is {x > tau_k}: extract it
       Range Rx;
       Rx.lo = tau_k;
       Rx.hi = kKeyPosInf;
       Rx.lo_all = false;
       Rx.pin_hi = true;
       extract_range<DT>(c, Rx);
-      if (gather_extracted<DT>(c)) {
+      own_segments_contiguous<DT>(c);
+      merge_count_mass<DT>(c, vld(F.own_n), 0ull, vld(F.seg_ovf));
+      if (vld(F.bc.u[BU_OVF2]) == 0u) {
         k_full = true;
         extracted_above_k = true;
       }
     }
     if (p_on && !sel_none) {
+      const float scale = c.fix_scale;
       if (k_on && k_full) {
-        // top-p over S_k, all of it gathered: Z_k = mass(> tau_k) + n_keep_k w(tau_k)
+        // top-p over S_k, all of it in the own lists:
+        // Z_k = mass(> tau_k) + n_keep_k w(tau_k)
         const float tk = key2f(tau_k);
-        const float scale = c.fix_scale;
+        uint32_t cnt = 0;
         unsigned long long acc = 0ull;
-        const uint32_t gn = min(vld(F.g_n), c.gcap);
-        for (uint32_t i = tid; i < gn; i += kThreads) {
-          const float x = c.g_val[i];
-          acc += x > tk ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
-        }
+        own_for(c, [&](float x, uint32_t) {
+          if (x > tk) {
+            ++cnt;
+            acc += weight_fx(x, c.m, c.m_neginf, scale);
+          }
+        });
+        cnt = __reduce_add_sync(kFull, cnt);
         acc = warp_sum_u64_redux(acc);
-        if (lane == 0) F.lred[0][warp][0].mass = acc;
-        __syncthreads();
-        if (tid == 0) {
-          unsigned long long a = 0ull;
-          for (int w = 0; w < kWarps; ++w) a += vld(F.lred[0][w][0].mass);
-          F.bc.x[BX_TARGET] = a;
+        if (lane == 0) {
+          F.lred[0][warp][0].mass = acc;
+          F.lred[0][warp][0].cnt = cnt;
         }
         __syncthreads();
-        const unsigned long long M_gt = vld(F.bc.x[BX_TARGET]);
+        uint32_t cta_n = 0;
+        unsigned long long cta_m = 0ull;
+        if (tid == 0) {
+          for (int w = 0; w < kWarps; ++w) {
+            cta_n += vld(F.lred[0][w][0].cnt);
+            cta_m += vld(F.lred[0][w][0].mass);
+          }
+        }
+        merge_count_mass<DT>(c, cta_n, cta_m, 0u);
+        const unsigned long long M_gt = vld(F.bc.x[BX_MLO]);
         const unsigned long long w_tau = weight_fx(tk, c.m, c.m_neginf, scale);
         const unsigned long long Zk = M_gt + static_cast<unsigned long long>(nk_k) * w_tau;
         const unsigned long long target = f2_to_u64(f2_mul(f2_from_u64(Zk), pr));
         z_used = Zk;
-        __syncthreads();
         if (M_gt < target) {
           // the boundary lies in the tau_k tie group: keep fewer of them
           n_keep = copies_fx(target - M_gt, w_tau, nk_k);
@@ -2521,6 +2469,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             ties_in_list = false;
           }
         } else {
+          rank_counts_from<DT>(c, F.rank_n);
           Local s;
           s.model_mu = 0.f;
           s.model_sigma = 0.f;
@@ -2533,7 +2482,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           s.m_hi = 0ull;
           s.c_above = 0;
           s.m_above = 0ull;
-          local_search<DT, true>(c, s, target, value_pivots);
+          dsearch<DT, true>(c, s, target, value_pivots);
           rounds_p = static_cast<uint32_t>(s.rounds);
           if (s.capped) {
             sel_none = true;
@@ -2542,7 +2491,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           tau = s.tau;
           n_keep = s.n_keep;
           count_above = s.count_above;
-          count_ties_gathered<DT>(c, key2f(tau));
           if (extracted_above_k) {
             // tau > tau_k: the kept set and the tie group are in the lists
             list_emit = true;
@@ -2550,7 +2498,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           }
         }
       } else {
-        // top-p only, or top-p over an S_k too large to gather
+        // top-p only, or top-p over an S_k too large for the lists
         const bool hit = !k_on && trunc && !overflow && !force_fb && ref_ok &&
                          f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
         if (!k_on) path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
@@ -2561,9 +2509,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         s.c_above = 0;
         s.m_above = 0ull;
         bool have_exact = false;
-        const float scale = c.fix_scale;
-        if (hit && survivors <= c.gcap) {
-          gather_all<DT>(c);
+        if (hit) {
+          // Z_t is in the own lists: the candidates are (key(t) - 1, max]
+          rank_counts_from<DT>(c, F.rank_n);
           z_used = f2_to_u64(f2_mul(Zm, scale));
           s.lo = f2key(t) - 1u;
           s.c_lo = survivors;
@@ -2573,7 +2521,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           s.m_hi = 0ull;
           list_emit = true;
           ties_in_list = true;
-          local_search<DT, true>(c, s, f2_to_u64(f2_mul(f2_mul(Zm, pr), scale)), value_pivots);
+          dsearch<DT, true>(c, s, f2_to_u64(f2_mul(f2_mul(Zm, pr), scale)), value_pivots);
         } else {
           // narrow by mass in fixed point (shift m); a pass over the chunk
           // measures the denominator (Z, or mass(> tau_k) for S_k) itself
@@ -2581,15 +2529,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           R.pin_hi = false;
           R.p_frac = pr;
           R.extra = 0ull;
-          R.target_from_total = !hit;
-          R.target = hit ? f2_to_u64(f2_mul(f2_mul(Zm, pr), scale)) : 0ull;
+          R.target_from_total = true;
+          R.target = 0ull;
           if (k_on) {
             R.lo = tau_k;
             R.c_lo = above_k;
             R.extra = static_cast<unsigned long long>(nk_k) * weight_fx(key2f(tau_k), c.m, c.m_neginf, scale);
-          } else if (hit) {
-            R.lo = f2key(t) - 1u;
-            R.c_lo = survivors;
           } else {
             R.lo = f2key(row_min) - 1u;
             R.c_lo = static_cast<uint32_t>(V);
@@ -2598,14 +2543,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           R.hi = f2key(row_max);
           R.c_hi = 0;
           R.m_lo = R.m_hi = 0ull;
-          narrow<DT, true>(c, R, !hit);
+          narrow<DT, true>(c, R);
           passes += static_cast<uint32_t>(R.passes);
           const unsigned long long target = R.target;
           z_used = f2_to_u64(f2_mul(f2_from_u64(target), 1.0f / pr));
-          // the emission streams the chunk unless a gather below says otherwise;
-          // a chunk pass also overwrote the lists
+          // the chunk passes overwrote the lists: the emission streams the
+          // chunk unless an extraction below refills them
           list_emit = false;
-          if (!hit) ties_in_list = false;
+          ties_in_list = false;
           if (R.below) {
             // only after top-k: mass(> tau_k) < p Z_k, so the boundary lies in
             // the tau_k tie group (whose per-rank counts F.ties still holds)
@@ -2622,22 +2567,20 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             s.rounds = 0;
             s.capped = false;
             have_exact = true;
-            ties_in_list = false;  // the own list may not hold this tie group
-            if (warp == 0 && lane < static_cast<int>(c.C))
-              F.ties[lane] = vld(F.rank_lo[lane]) - vld(F.rank_hi[lane]);
+            if (tid < static_cast<int>(c.C)) F.ties[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
             __syncthreads();
             ties_known = true;
           } else if (!R.fits) {
             s.capped = true;
             s.rounds = 0;
           } else {
-            if (!hit) {
-              extract_range<DT>(c, R);
-              if (warp == 0 && lane < static_cast<int>(c.C))
-                F.rank_n[lane] = vld(F.rank_lo[lane]) - vld(F.rank_hi[lane]);
-              __syncthreads();
+            extract_range<DT>(c, R);
+            own_segments_contiguous<DT>(c);
+            if (tid < static_cast<int>(c.C)) {
+              F.rank_lo[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
+              F.rank_hi[tid] = 0u;
             }
-            gather<DT>(c, R.lo_all ? -INFINITY : pivot_f(R.lo), pivot_f(R.hi), R.lo_all, !hit);
+            __syncthreads();
             s.lo = R.lo;
             s.hi = R.hi;
             s.c_lo = R.c_lo;
@@ -2646,9 +2589,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             s.m_lo = R.m_lo;
             s.m_hi = R.m_hi;
             s.m_above = R.m_hi;
-            list_emit = hit;
             ties_in_list = true;
-            local_search<DT, true>(c, s, target, value_pivots);
+            dsearch<DT, true>(c, s, target, value_pivots);
           }
         }
         rounds_p = static_cast<uint32_t>(s.rounds);
@@ -2659,10 +2601,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         tau = s.tau;
         n_keep = s.n_keep;
         count_above = s.count_above;
-        if (!sel_none && !have_exact) {
-          count_ties_gathered<DT>(c, key2f(tau));
-          ties_known = true;
-        }
+        if (!sel_none && !have_exact) ties_known = true;
       }
     }
   }
@@ -2709,13 +2648,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     if (tid < mt) c.gmask[mh + mb * 16 + tid] = fill;
     if (list_emit && !sel_all && !sel_none) {
       __syncthreads();  // the fill is ordered before the scatter
-      const uint32_t n = min(vld(F.own_n), c.ocap);
-      for (uint32_t i = tid; i < n; i += kThreads) {
-        const float x = c.own_val[i];
+      own_for(c, [&](float x, uint32_t ix) {
         bool keep = x > tau_f;
-        if (x == tau_f) keep = (tie_mode == 1) || (tie_mode == 2 && c.own_idx[i] < idx_cut);
-        if (keep) c.gmask[c.own_idx[i]] = 1;
-      }
+        if (x == tau_f) keep = (tie_mode == 1) || (tie_mode == 2 && ix < idx_cut);
+        if (keep) c.gmask[ix] = 1;
+      });
     }
   } else {
     // stream the chunk again: x > tau kept, ties by the rule above
@@ -2844,18 +2781,15 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
 
 }  // namespace
 
-static_assert(2 * (sizeof(Fixed) + list_region_bytes(2, kOwnCap, kGatherCap) + 128 + kSmemReservedPerCta) <=
+static_assert(2 * (sizeof(Fixed) + list_region_bytes(kOwnCap) + 128 + kSmemReservedPerCta) <=
                   static_cast<size_t>(kSmemPerSm),
-              "two CTAs of a cluster shape must fit one SM");
-static_assert(2 * (sizeof(Fixed) + list_region_bytes(1, kSoleCap, kSoleCap) + 128 + kSmemReservedPerCta) <=
-                  static_cast<size_t>(kSmemPerSm),
-              "two CTAs of the one-CTA shape must fit one SM");
+              "two CTAs must fit one SM");
 
-size_t smem_bytes(int C, int ocap, int gcap) {
-  const size_t lists = list_region_bytes(C, ocap, gcap);
+size_t smem_bytes(int ocap) {
+  const size_t lists = list_region_bytes(ocap);
   // the ring must clear the own list and the narrowing bins laid over the region
   const size_t ring_off = lists - kRingBytes;
-  if (ring_off < static_cast<size_t>(ocap) * 8u || ring_off < static_cast<size_t>(kBinBytes)) return 0;
+  if (ring_off < static_cast<size_t>(kBinBytes) || ring_off < static_cast<size_t>(kWideTotOff) + 4096u) return 0;
   return (sizeof(Fixed) + lists + 127u) & ~static_cast<size_t>(127u);
 }
 
