@@ -68,7 +68,7 @@ constexpr int kStages = 2;
 constexpr int kPieceBytes = 16384;
 constexpr int kPieceUnits = kPieceBytes / 16;
 constexpr int kRingBytes = kStages * kPieceBytes;
-static_assert((kStages & (kStages - 1)) == 0, "kStages must be a power of two");
+
 static_assert(kPieceUnits % kThreads == 0, "a piece is whole rounds of the block");
 // Bound of one wait for a bulk copy (a copy from valid global memory lands in
 // microseconds; the bound only keeps a failing copy from hanging the kernel).
@@ -482,7 +482,7 @@ __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, Sc
     for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc);
   }
   for (int pc = 0; pc < npieces; ++pc) {
-    const int st = pc & (kStages - 1);
+    const int st = pc % kStages;
     const uint32_t bar = c.ring_bar + 8u * st;
     bool ok = false;
     if (vld(F.err) == 0u) ok = mbar_wait_bounded(bar, (c.ring_phase >> st) & 1u, kWaitLimitNs);
@@ -1887,6 +1887,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   Fixed& F = *reinterpret_cast<Fixed*>(smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+  // the previous kernel of the stream (which may have written the logits,
+  // k or p) has completed and its writes are visible past this point; the
+  // next kernel may be scheduled from now on (it waits the same way)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   Ctx<DT> c;
   c.F = &F;
   c.ocap = static_cast<uint32_t>(P.ocap);
@@ -2823,13 +2829,18 @@ int launch_select(const Params& prm, int dtype, size_t smem, qrita_stream_t stre
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = reinterpret_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(prm.C);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the CTAs may be scheduled while the
+  // previous kernel of the stream drains; they wait for it (griddepcontrol)
+  // before touching memory
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (dtype == QRITA_DTYPE_F32) {
     e = cudaLaunchKernelEx(&cfg, select_kernel<QRITA_DTYPE_F32>, prm);
   } else {
