@@ -554,14 +554,18 @@ __device__ __forceinline__ void append_piece(Ctx<DT>& c, uint32_t& wn, uint32_t 
 #pragma unroll
   for (int j = 0; j < kPieceThreadUnits; ++j) cnt += __popc(bits[j]);
   if (__ballot_sync(kFull, cnt != 0u) == 0u) return;
-  uint32_t incl = cnt;
+  // warp prefix of the counts by bit planes: independent ballots instead of
+  // a chain of shuffles (cnt < 2^kPlanes)
+  constexpr int kPlanes = 32 - __builtin_clz(static_cast<unsigned>(kPieceThreadUnits * E));
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t excl = 0, tot = 0;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
+  for (int b = 0; b < kPlanes; ++b) {
+    const uint32_t plane = __ballot_sync(kFull, (cnt >> b) & 1u);
+    excl += static_cast<uint32_t>(__popc(plane & lt)) << b;
+    tot += static_cast<uint32_t>(__popc(plane)) << b;
   }
-  const uint32_t tot = __shfl_sync(kFull, incl, 31);
-  uint32_t pos = wn + incl - cnt;
+  uint32_t pos = wn + excl;
   wn += tot;
 #pragma unroll
   for (int j = 0; j < kPieceThreadUnits; ++j) {
@@ -1819,7 +1823,10 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     done = static_cast<int>(vld(F.bc.u[BU_DONE]));
     ++rounds;
     // per-rank copies of the boundary value
-    if (tid < static_cast<int>(total) && F.tail_val[tid] == key2f(tau)) atomicAdd(&F.ties[F.tail_rank[tid]], 1u);
+    if (tid < static_cast<int>(total) && F.tail_val[tid] == key2f(tau)) {
+      const uint32_t rk = F.tail_rank[tid];
+      if (rk < c.C) atomicAdd(&F.ties[rk], 1u);  // a rank index from shared memory: bounded
+    }
     __syncthreads();
   }
   (void)m_lo;
