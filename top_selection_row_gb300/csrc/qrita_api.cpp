@@ -44,7 +44,7 @@ Tables build_tables() {
   Tables t;
   for (int i = 0; i < kLutK; ++i) {
     // Phi^-1(1 - u) = -Phi^-1(u), evaluated in the accurate lower tail
-    const double u = std::exp2(-0.5 * i);
+    const double u = std::exp2(-0.25 * i);
     t.lut_k[i] = static_cast<float>(-normal_quantile(u));
   }
   for (int i = 0; i < kLutP; ++i) {
@@ -60,8 +60,11 @@ const Tables& tables() {
 }
 
 // Truncation tuning (the pages give no constants; these only move speed,
-// never the result): u = alpha_k * k / V, truncation skipped above u_max.
+// never the result): u = alpha_k * k / V, truncation skipped above u_max;
+// alpha shrinks toward kAlphaMinK when alpha * k survivors would not fit the
+// own lists.
 constexpr float kAlphaK = 2.0f;
+constexpr float kAlphaMinK = 1.25f;
 constexpr float kUMaxK = 0.25f;
 constexpr float kMarginP = 0.25f;
 
@@ -175,6 +178,7 @@ int select_impl(const void* logits, int dtype, int64_t B, int64_t V, const int32
   prm.ocap = sh.ocap;
   prm.flags = flags;
   prm.alpha_k = kAlphaK;
+  prm.alpha_min_k = kAlphaMinK;
   prm.margin_p = kMarginP;
   prm.u_max_k = kUMaxK;
   const Tables& t = tables();

@@ -11,13 +11,13 @@ namespace qrita {
 
 // delta tables (Qrita technical summary, "Methodology", part 1: precomputed
 // tables from the normal quantile function, keyed on the target k or p).
-//   lut_k[i] = Phi^-1(1 - 2^(-i/2)),  i = 0..63   (keyed on u = alpha*k/V;
-//              the kernel takes i = floor(-2 log2 u), so 2^(-i/2) >= u)
+//   lut_k[i] = Phi^-1(1 - 2^(-i/4)),  i = 0..127  (keyed on u = alpha*k/V;
+//              the kernel takes i = floor(-4 log2 u), so 2^(-i/4) >= u)
 //   lut_p[i] = Phi^-1(2^(-i/4)),      i = 0..63   (keyed on q = 1 - p;
 //              the kernel takes i = ceil(-4 log2 q), so 2^(-i/4) <= q)
 // Rounding the key toward the larger u / smaller q lowers the threshold, so
 // the table never makes truncation less likely to hit than the exact value.
-constexpr int kLutK = 64;
+constexpr int kLutK = 128;
 constexpr int kLutP = 64;
 
 // Threads per CTA of the selection kernel.
@@ -56,6 +56,7 @@ struct Params {
   int32_t ocap;     // own candidate list capacity per CTA (entries)
   uint32_t flags;   // QRITA_FLAG_*
   float alpha_k;    // top-k truncation safety factor (u = alpha_k * k / V)
+  float alpha_min_k;  // the smallest factor used to keep the survivors within the lists
   float margin_p;   // subtracted from the top-p delta
   float u_max_k;    // no truncation when alpha_k * k / V exceeds this
   float lut_k[kLutK];

@@ -1505,8 +1505,9 @@ constexpr int kTail = kThreads;
 // copies of z_mn does not), else move lo / hi. Masses are exact sums of
 // fixed-point weights, so every decision is integer arithmetic.
 // On entry F.rank_lo / F.rank_hi hold each rank's own-list counts above lo /
-// hi; s.c_above / s.m_above count what lies above the lists' range. On exit
-// F.ties holds each rank's count of the boundary value.
+// hi, and s.c_hi / s.m_hi the row's count and mass above hi (including what
+// lies above the lists' range). Each round scans only the lists' (lo, hi].
+// On exit F.ties holds each rank's count of the boundary value.
 template <int DT, bool MASS>
 __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots) {
   Fixed& F = *c.F;
@@ -1625,8 +1626,11 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     for (int j = 0; j < 3; ++j) qf[j] = j < np ? pivot_f(q[j]) : INFINITY;
     uint32_t cnt[3] = {0u, 0u, 0u}, zk[3] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu}, nz[3] = {0u, 0u, 0u};
     unsigned long long ms[3] = {0ull, 0ull, 0ull};
+    // only the range (lo, hi] is scanned: what lies above hi is counted in
+    // c_hi / m_hi (and per rank in F.rank_hi) already
     own_for(c, [&](float x, uint32_t) {
       const uint32_t key = f2key(x);
+      if (key <= lo || key > hi) return;
       const unsigned long long wf = MASS ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
 #pragma unroll
       for (int j = 0; j < 3; ++j) {
@@ -1699,7 +1703,7 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
         const uint32_t gn = __reduce_add_sync(kFull, rz == gz ? rn : 0u);
         const unsigned long long gm = MASS ? warp_sum_u64_redux(rm) : 0ull;
         if (lane < C) {
-          F.pr_cnt[lane][j] = rc;
+          F.pr_cnt[lane][j] = rc + vld(F.rank_hi[lane]);  // the rank's list count above the pivot
           F.pr_nz[lane][j] = rz == gz ? rn : 0u;
         }
         if (lane == 0) {
@@ -1717,10 +1721,10 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     unsigned long long tm[3];
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
-      tc[j] = vld(F.dtot[0][j]) + s.c_above;
+      tc[j] = vld(F.dtot[0][j]) + c_hi;  // row counts above the pivots
       tz[j] = vld(F.dtot[1][j]);
       tn[j] = vld(F.dtot[2][j]);
-      tm[j] = MASS ? vld(F.dmass[j]) + s.m_above : 0ull;
+      tm[j] = MASS ? vld(F.dmass[j]) + m_hi : 0ull;
     }
     decide(tc, tz, tn, tm);
     // per-rank bookkeeping of the decision (identical in every thread)
@@ -1845,6 +1849,22 @@ template <int DT>
 __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the tie group's indices, compacted into the ring's bytes (no stream is in
+  // flight); a group too large for them is scanned in the own list
+  uint32_t* tix = reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr));
+  constexpr uint32_t kTieCap = kRingBytes / 4;
+  __syncthreads();  // earlier users of the ring's bytes are done
+  if (tid == 0) F.tail_n = 0u;
+  __syncthreads();
+  own_for(c, [&](float x, uint32_t ix) {
+    if (x == tau_f) {
+      const uint32_t pos = atomicAdd(&F.tail_n, 1u);
+      if (pos < kTieCap) tix[pos] = ix;
+    }
+  });
+  __syncthreads();
+  const uint32_t nt = vld(F.tail_n);
+  const bool compact = nt <= kTieCap;
   uint32_t lo = 0, hi = static_cast<uint32_t>(c.n);
   for (int round = 0; round < 32 && hi - lo > 1u; ++round) {
     const uint32_t span = hi - lo;
@@ -1858,12 +1878,17 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
     uint32_t cnt[15];
 #pragma unroll
     for (int j = 0; j < 15; ++j) cnt[j] = 0;
-    own_for(c, [&](float x, uint32_t ix) {
-      if (x == tau_f) {
+    auto count_one = [&](uint32_t ix) {
 #pragma unroll
-        for (int j = 0; j < 15; ++j) cnt[j] += (ix < piv[j]) ? 1u : 0u;
-      }
-    });
+      for (int j = 0; j < 15; ++j) cnt[j] += (ix < piv[j]) ? 1u : 0u;
+    };
+    if (compact) {
+      for (uint32_t i = tid; i < nt; i += kThreads) count_one(tix[i]);
+    } else {
+      own_for(c, [&](float x, uint32_t ix) {
+        if (x == tau_f) count_one(ix);
+      });
+    }
 #pragma unroll
     for (int j = 0; j < 15; ++j) {
       const uint32_t v = warp_sum_u(cnt[j]);
@@ -2070,9 +2095,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       float t = -INFINITY;
       if (!(P.flags & QRITA_FLAG_NO_TRUNCATION) && a > 0.f && !keep_all) {
         if (k_on) {
-          const float u = P.alpha_k * static_cast<float>(kr) / static_cast<float>(V);
+          // alpha * k expected survivors (up to 2^(1/4) more from the table's
+          // rounding) should fit 80 % of the row's own lists
+          const float room = 0.8f * static_cast<float>(P.ocap) * static_cast<float>(P.C) /
+                             (1.19f * static_cast<float>(kr));
+          const float alpha = fmaxf(fminf(P.alpha_k, room), P.alpha_min_k);
+          const float u = alpha * static_cast<float>(kr) / static_cast<float>(V);
           if (u <= P.u_max_k) {
-            int i = static_cast<int>(floorf(-2.0f * log2f(u)));
+            int i = static_cast<int>(floorf(-4.0f * log2f(u)));
             i = i < 0 ? 0 : (i > kLutK - 1 ? kLutK - 1 : i);
             t = mu + P.lut_k[i] * sigma;
             trunc = true;
