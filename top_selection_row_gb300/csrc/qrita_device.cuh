@@ -210,6 +210,16 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 // Full cluster barrier: every thread of every CTA of the cluster arrives
 // (release) and waits (acquire). The non-.aligned forms are used so that a
 // warp need not be converged when it reaches the barrier.
+// The two halves of a cluster barrier, for work between them that touches
+// no other CTA's memory.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile(
       "barrier.cluster.arrive.release;\n\t"

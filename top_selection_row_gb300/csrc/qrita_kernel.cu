@@ -2650,6 +2650,21 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   }
   QRITA_T(5);
 
+  // The last cluster barrier (see the end of the row) is entered here when
+  // nothing below touches another CTA's memory or streams the chunk: its
+  // arrive now, its wait at the end. A bulk-copy wait that gave up is
+  // reported to every CTA before the arrive.
+  const bool early_arrive = c.C > 1 && (sel_all || sel_none || list_emit);
+  if (early_arrive) {
+    __syncthreads();
+    if (tid == 0 && vld(F.err) != 0u) {
+      ring_drain<DT>(c);
+      for (uint32_t rr = 0; rr < c.C; ++rr) st_dsmem_u32(map_rank(smem_u32(&F.err_any), rr), 1u);
+    }
+    __syncthreads();
+    cluster_arrive();
+  }
+
   // ---- A8: boundary ties by lowest token id
   const float tau_f = key2f(tau);
   uint32_t my_first = 0, my_ties = 0;
@@ -2678,17 +2693,19 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   // ---- A9: mask emission
   if (sel_all || sel_none || list_emit) {
     // fill the chunk's mask, then scatter the kept ids of the own list
-    const uint8_t fill = sel_all ? 1 : 0;
-    const uint32_t fill4 = sel_all ? 0x01010101u : 0u;
-    const uintptr_t ma = reinterpret_cast<uintptr_t>(c.gmask);
-    const int mh0 = static_cast<int>((16u - (ma & 15u)) & 15u);
-    const int mh = mh0 < c.n ? mh0 : c.n;
-    const int mb = (c.n - mh) / 16;
-    const int mt = c.n - mh - mb * 16;
-    if (tid < mh) c.gmask[tid] = fill;
-    for (int i = tid; i < mb; i += kThreads)
-      reinterpret_cast<uint4*>(c.gmask + mh)[i] = make_uint4(fill4, fill4, fill4, fill4);
-    if (tid < mt) c.gmask[mh + mb * 16 + tid] = fill;
+    {
+      const uint8_t fill = sel_all ? 1 : 0;
+      const uint32_t fill4 = sel_all ? 0x01010101u : 0u;
+      const uintptr_t ma = reinterpret_cast<uintptr_t>(c.gmask);
+      const int mh0 = static_cast<int>((16u - (ma & 15u)) & 15u);
+      const int mh = mh0 < c.n ? mh0 : c.n;
+      const int mb = (c.n - mh) / 16;
+      const int mt = c.n - mh - mb * 16;
+      if (tid < mh) c.gmask[tid] = fill;
+      for (int i = tid; i < mb; i += kThreads)
+        reinterpret_cast<uint4*>(c.gmask + mh)[i] = make_uint4(fill4, fill4, fill4, fill4);
+      if (tid < mt) c.gmask[mh + mb * 16 + tid] = fill;
+    }
     if (list_emit && !sel_all && !sel_none) {
       __syncthreads();  // the fill is ordered before the scatter
       own_for(c, [&](float x, uint32_t ix) {
@@ -2779,12 +2796,16 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   // The last cluster barrier: no CTA leaves while another may still access
   // its memory, and every CTA learns whether any CTA of the row failed.
   __syncthreads();
-  if (tid == 0 && vld(F.err) != 0u) {
-    ring_drain<DT>(c);
-    for (uint32_t rr = 0; rr < c.C; ++rr) st_dsmem_u32(map_rank(smem_u32(&F.err_any), rr), 1u);
+  if (early_arrive) {
+    cluster_wait();
+  } else {
+    if (tid == 0 && vld(F.err) != 0u) {
+      ring_drain<DT>(c);
+      for (uint32_t rr = 0; rr < c.C; ++rr) st_dsmem_u32(map_rank(smem_u32(&F.err_any), rr), 1u);
+    }
+    if (c.C > 1) cluster_sync_all();
+    else __syncthreads();
   }
-  if (c.C > 1) cluster_sync_all();
-  else __syncthreads();
   if (vld(F.err_any) != 0u) {
     for (int i = tid; i < c.n; i += kThreads) c.gmask[i] = 0;
     row_status = QRITA_ROW_TIMEOUT;
