@@ -199,6 +199,8 @@ struct alignas(16) Fixed {
   uint32_t own_n;
   uint32_t seg_base[kWarps];  // own list: warp w's entries are [seg_base[w], + seg_cnt[w])
   uint32_t seg_cnt[kWarps];
+  uint32_t col_mode;            // own list in per-thread columns instead:
+  uint8_t col_n[kThreads];      // thread t's entries are t + j * kThreads, j < col_n[t]
   float tail_val[kThreads];  // search tail: the last range's elements (cluster-wide)
   uint8_t tail_rank[kThreads];  // and the cluster rank each came from
   unsigned long long tail_w[kThreads];  // and their fixed-point weights (mass search)
@@ -1155,6 +1157,7 @@ __device__ void own_segments_streamed(Ctx<DT>& c, uint32_t wn) {
     F.seg_base[warp] = static_cast<uint32_t>(warp) * segcap;
     F.seg_cnt[warp] = min(wn, segcap);
   }
+  if (tid == 0) F.col_mode = 0u;
   __syncthreads();
   if (tid == 0) {
     uint32_t total = 0;
@@ -1185,16 +1188,88 @@ __device__ void own_segments_contiguous(Ctx<DT>& c) {
       F.seg_cnt[w] = min(slice, n - b);
     }
     F.seg_ovf = total > c.ocap ? 1u : 0u;
+    F.col_mode = 0u;
   }
   __syncthreads();
 }
 
-// fn(value, index) over this warp's segment of the own list (lanes stride;
-// no collective operations inside fn).
+// After a streaming pass in column mode: thread t kept its survivors at
+// t + j * kThreads (cn of them counted, at most ocap / kThreads stored).
+template <int DT>
+__device__ void own_columns_streamed(Ctx<DT>& c, uint32_t cn) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t colcap = c.ocap / kThreads;
+  F.col_n[tid] = static_cast<uint8_t>(min(cn, colcap));
+  const uint32_t ws = __reduce_add_sync(kFull, cn);
+  if (lane == 0) F.seg_n[warp] = ws;
+  const bool ovf = __syncthreads_or(cn > colcap) != 0;
+  if (tid == 0) {
+    uint32_t total = 0;
+    for (int w = 0; w < kWarps; ++w) total += vld(F.seg_n[w]);
+    F.own_n = total;
+    F.seg_ovf = ovf ? 1u : 0u;
+    F.col_mode = 1u;
+  }
+  __syncthreads();
+}
+
+// Columns to warp segments (the form the search and the emission scan
+// fastest): each warp's column entries are staged densely in the ring's bytes
+// (no stream is in flight) and copied back to the warp's segment. Left in
+// columns when a warp holds more than the staging gives it.
+template <int DT>
+__device__ void own_columns_to_segments(Ctx<DT>& c, uint32_t cn) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr uint32_t kStage = kRingBytes / 8 / kWarps;  // entries per warp
+  const uint32_t colcap = c.ocap / kThreads;
+  const uint32_t segcap = c.ocap / kWarps;
+  const uint32_t n = min(cn, colcap);
+  uint32_t incl = n;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t tot = __shfl_sync(kFull, incl, 31);
+  if (__syncthreads_or(tot > kStage || vld(F.seg_ovf) != 0u) != 0) return;
+  float* sv = reinterpret_cast<float*>(const_cast<uint4*>(c.ring_ptr));
+  uint32_t* si = reinterpret_cast<uint32_t*>(sv + kStage * kWarps);
+  const uint32_t base = static_cast<uint32_t>(warp) * kStage + (incl - n);
+  for (uint32_t j = 0; j < n; ++j) {
+    sv[base + j] = c.own_val[j * kThreads + tid];
+    si[base + j] = c.own_idx[j * kThreads + tid];
+  }
+  __syncthreads();  // every column is staged: the list region is free
+  const uint32_t dst = static_cast<uint32_t>(warp) * segcap, src = static_cast<uint32_t>(warp) * kStage;
+  for (uint32_t i = lane; i < tot; i += 32u) {
+    c.own_val[dst + i] = sv[src + i];
+    c.own_idx[dst + i] = si[src + i];
+  }
+  if (lane == 0) {
+    F.seg_base[warp] = dst;
+    F.seg_cnt[warp] = tot;
+  }
+  __syncthreads();
+  if (tid == 0) F.col_mode = 0u;
+  __syncthreads();
+}
+
+// fn(value, index) over this thread's share of the own list: its column, or
+// its lane's stride of its warp's segment (no collective operations inside fn).
 template <int DT, typename Fn>
 __device__ __forceinline__ void own_for(Ctx<DT>& c, Fn&& fn) {
   Fixed& F = *c.F;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (vld(F.col_mode) != 0u) {
+    const uint32_t n = vld(F.col_n[threadIdx.x]);
+    for (uint32_t j = 0; j < n; ++j) {
+      const uint32_t i = j * kThreads + threadIdx.x;
+      fn(c.own_val[i], c.own_idx[i]);
+    }
+    return;
+  }
   const uint32_t base = vld(F.seg_base[warp]), n = vld(F.seg_cnt[warp]);
   for (uint32_t i = static_cast<uint32_t>(lane); i < n; i += 32u) fn(c.own_val[base + i], c.own_idx[base + i]);
 }
@@ -2139,8 +2214,22 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     F2 zs = {0.f, 0.f}, ms = {0.f, 0.f};
     // two instances: the softmax sums (one expf per element) only where
     // top-p runs alone
-    auto streaming_pass = [&](auto po) {
+    // top-k rows expecting few survivors per CTA keep them in per-thread
+    // columns of the own list (no warp communication per piece)
+    uint32_t cn = 0;
+    const uint32_t colcap = c.ocap / kThreads;
+    const bool col = !p_only && trunc && k_on &&
+                     2.4f * static_cast<float>(kr) <= static_cast<float>(c.ocap / 8u) * static_cast<float>(c.C);
+    auto col_put = [&](float x, uint32_t idx) {
+      if (cn < colcap) {
+        c.own_val[cn * kThreads + tid] = x;
+        c.own_idx[cn * kThreads + tid] = idx;
+      }
+      ++cn;
+    };
+    auto streaming_pass = [&](auto po, auto cm) {
       constexpr bool PO = decltype(po)::value;
+      constexpr bool COL = decltype(cm)::value;
       stream_pieces<DT>(
           c,
           [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
@@ -2171,7 +2260,23 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                 }
               }
             }
-            append_piece<DT>(c, wn, seg_base, segcap, xs, bits, u0);
+            if constexpr (COL) {
+#pragma unroll
+              for (int j = 0; j < kPieceThreadUnits; ++j) {
+                uint32_t b = bits[j];
+                const uint32_t idx0 = static_cast<uint32_t>(c.head_n + (u0 + j * kThreads + tid) * E);
+                while (b != 0u) {
+                  const int e = __ffs(b) - 1;
+                  b &= b - 1u;
+                  float x = xs[j][0];
+#pragma unroll
+                  for (int q = 1; q < E; ++q) x = (q == e) ? xs[j][q] : x;
+                  col_put(x, idx0 + static_cast<uint32_t>(e));
+                }
+              }
+            } else {
+              append_piece<DT>(c, wn, seg_base, segcap, xs, bits, u0);
+            }
           },
           [&](float x, uint32_t idx, bool valid) {
             uint32_t bits = 0;
@@ -2187,14 +2292,24 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               }
             }
             const float xs[1] = {x};
-            if (trunc) seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, bits);
+            if constexpr (COL) {
+              if (bits) col_put(x, idx);
+            } else {
+              if (trunc) seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, bits);
+            }
           },
           true);
     };
-    if (p_only) streaming_pass(BoolC<true>{});
-    else streaming_pass(BoolC<false>{});
+    if (p_only) streaming_pass(BoolC<true>{}, BoolC<false>{});
+    else if (col) streaming_pass(BoolC<false>{}, BoolC<true>{});
+    else streaming_pass(BoolC<false>{}, BoolC<false>{});
     QRITA_T(2);
-    own_segments_streamed<DT>(c, trunc ? wn : 0u);
+    if (col) {
+      own_columns_streamed<DT>(c, cn);
+      own_columns_to_segments<DT>(c, cn);
+    } else {
+      own_segments_streamed<DT>(c, trunc ? wn : 0u);
+    }
     // block reduce
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -2574,10 +2689,21 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           R.extra = 0ull;
           R.target_from_total = true;
           R.target = 0ull;
+          R.m_lo = R.m_hi = 0ull;
+          // top-p alone, truncation hit by mass but too many survivors: the
+          // boundary lies above t, and the target is p Z from the streaming pass
+          const bool mass_hit = !k_on && trunc && !force_fb && ref_ok &&
+                                f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
           if (k_on) {
             R.lo = tau_k;
             R.c_lo = above_k;
             R.extra = static_cast<unsigned long long>(nk_k) * weight_fx(key2f(tau_k), c.m, c.m_neginf, scale);
+          } else if (mass_hit) {
+            R.lo = f2key(t) - 1u;
+            R.c_lo = survivors;
+            R.target_from_total = false;
+            R.target = f2_to_u64(f2_mul(f2_mul(Zm, pr), scale));
+            R.m_lo = f2_to_u64(f2_mul(Mm, scale));
           } else {
             R.lo = f2key(row_min) - 1u;
             R.c_lo = static_cast<uint32_t>(V);
@@ -2585,7 +2711,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           R.lo_all = R.lo < kKeyNegInf;
           R.hi = f2key(row_max);
           R.c_hi = 0;
-          R.m_lo = R.m_hi = 0ull;
           narrow<DT, true>(c, R);
           passes += static_cast<uint32_t>(R.passes);
           const unsigned long long target = R.target;
