@@ -205,6 +205,10 @@ struct alignas(16) Fixed {
   uint8_t tail_rank[kThreads];  // and the cluster rank each came from
   unsigned long long tail_w[kThreads];  // and their fixed-point weights (mass search)
   uint32_t tail_n;
+  uint32_t tbin_c[16];               // search tail: counts and masses of its 16 bins
+  unsigned long long tbin_m[16];
+  uint32_t tsel[2];                  // the bin holding the boundary, count above it
+  unsigned long long tsel_m;         // and mass above it
   uint32_t seg_n[kWarps];  // streaming pass: per-warp survivor counts
   uint32_t seg_ovf;        // a warp's survivors exceeded its segment
   uint32_t err;       // a bulk-copy wait of this CTA gave up
@@ -1853,43 +1857,113 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     });
     cluster_sync_all();  // every CTA's tail buffer is complete
     QRITA_T(13);
+    // the candidates: first a split of (lo, hi] into 16 equal value bins
+    // (one pass over the tail, counts and masses per bin); the bin where the
+    // count (mass) from the top reaches the target holds the boundary, and
+    // only its elements are candidates
+    if (tid < C) F.ties[tid] = 0u;
+    const float* tv = F.tail_val;
+    const unsigned long long* tw = F.tail_w;
+    const float lo_f = pivot_f(lo), hi_f = pivot_f(hi);
+    const float bw = (hi_f - lo_f) * (1.0f / 16.0f);
+    const bool split = total > 32u && isfinite(lo_f) && isfinite(hi_f) && bw > 0.f &&
+                       fmaf(15.0f, bw, lo_f) < hi_f && fmaf(1.0f, bw, lo_f) > lo_f;
+    // bin b = (edge(b-1), edge(b)], edge(-1) = lo, edge(15) = hi
+    auto edge = [&](int b) -> float {
+      return b < 0 ? lo_f : (b >= 15 ? hi_f : fmaf(static_cast<float>(b + 1), bw, lo_f));
+    };
+    uint32_t ckl = lo, ckh = hi;  // the candidates' key range (ckl, ckh]
+    uint32_t base_c = c_hi;       // count / mass above ckh
+    unsigned long long base_m = m_hi;
+    if (split) {
+      if (tid < 16) {
+        F.tbin_c[tid] = 0u;
+        F.tbin_m[tid] = 0ull;
+      }
+      __syncthreads();
+      if (tid < static_cast<int>(total)) {
+        const float x = tv[tid];
+        int b = static_cast<int>((x - lo_f) / bw);
+        b = b < 0 ? 0 : (b > 15 ? 15 : b);
+        if (b > 0 && x <= edge(b - 1)) --b;
+        if (b < 15 && x > edge(b)) ++b;
+        atomicAdd(&F.tbin_c[b], 1u);
+        if (MASS) atomicAdd(&F.tbin_m[b], tw[tid]);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t ac = c_hi;
+        unsigned long long am = m_hi;
+        int bs = 0;
+        for (int b = 15; b >= 0; --b) {
+          const uint32_t nc = ac + vld(F.tbin_c[b]);
+          const unsigned long long nm = am + vld(F.tbin_m[b]);
+          if ((MASS ? nm : static_cast<unsigned long long>(nc)) >= target) {
+            bs = b;
+            break;
+          }
+          ac = nc;
+          am = nm;
+        }
+        F.tsel[0] = static_cast<uint32_t>(bs);
+        F.tsel[1] = ac;
+        F.tsel_m = am;
+      }
+      __syncthreads();
+      const int bs = static_cast<int>(vld(F.tsel[0]));
+      if (bs > 0) ckl = f2key(edge(bs - 1));
+      if (bs < 15) ckh = f2key(edge(bs));
+      base_c = vld(F.tsel[1]);
+      base_m = vld(F.tsel_m);
+    }
+    // the candidates, compacted into the ring's bytes (no stream is in flight)
+    float* cv = reinterpret_cast<float*>(const_cast<uint4*>(c.ring_ptr));
+    unsigned long long* cw = reinterpret_cast<unsigned long long*>(cv + kTail);
+    if (tid == 0) F.tail_n = 0u;
+    __syncthreads();
+    if (tid < static_cast<int>(total)) {
+      const float x = tv[tid];
+      const uint32_t key = f2key(x);  // keys: lo may lie below key(-inf)
+      if (key > ckl && key <= ckh) {
+        const uint32_t pos = atomicAdd(&F.tail_n, 1u);
+        cv[pos] = x;
+        if (MASS) cw[pos] = tw[tid];
+      }
+    }
+    __syncthreads();
+    const uint32_t nc = min(vld(F.tail_n), static_cast<uint32_t>(kTail));
     // every candidate v tests itself: it is the boundary when count(> v) <
     // target <= count(>= v) (masses likewise), where further quaternary
     // rounds would stop (tau = v = z_mn, N_zmn = N(v))
-    if (tid < C) F.ties[tid] = 0u;
-    if (tid < static_cast<int>(total)) {
-      // the buffer is complete (barrier above) and unchanged from here on:
-      // plain loads, eight in flight
-      const float* tv = F.tail_val;
-      const unsigned long long* tw = F.tail_w;
-      const float v = tv[tid];
+    if (tid < static_cast<int>(nc)) {
+      const float v = cv[tid];
       uint32_t gt = 0, eq = 0;
       unsigned long long mgt = 0ull;
       uint32_t i = 0;
-      for (; i + 8u <= total; i += 8u) {
+      for (; i + 8u <= nc; i += 8u) {
         float xv[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) xv[u] = tv[i + u];
+        for (int u = 0; u < 8; ++u) xv[u] = cv[i + u];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           gt += xv[u] > v ? 1u : 0u;
           eq += xv[u] == v ? 1u : 0u;
-          if (MASS) mgt += xv[u] > v ? tw[i + u] : 0ull;
+          if (MASS) mgt += xv[u] > v ? cw[i + u] : 0ull;
         }
       }
-      for (; i < total; ++i) {
-        const float xv = tv[i];
+      for (; i < nc; ++i) {
+        const float xv = cv[i];
         gt += xv > v ? 1u : 0u;
         eq += xv == v ? 1u : 0u;
-        if (MASS) mgt += xv > v ? tw[i] : 0ull;
+        if (MASS) mgt += xv > v ? cw[i] : 0ull;
       }
-      const unsigned long long above_gt = MASS ? mgt + m_hi : static_cast<unsigned long long>(gt + c_hi);
-      const unsigned long long wv = MASS ? tw[tid] : 1ull;
+      const unsigned long long above_gt = MASS ? mgt + base_m : static_cast<unsigned long long>(gt + base_c);
+      const unsigned long long wv = MASS ? cw[tid] : 1ull;
       const unsigned long long above_ge = above_gt + static_cast<unsigned long long>(eq) * wv;
       // every copy of the boundary value answers, with the same values
       if (above_gt < target && target <= above_ge) {
         F.bc.u[BU_TAU] = f2key(v);
-        const uint32_t ca = gt + c_hi;
+        const uint32_t ca = gt + base_c;
         F.bc.u[BU_CABOVE] = ca;
         F.bc.u[BU_NKEEP] = MASS ? copies_fx(target - above_gt, wv, eq) : static_cast<uint32_t>(target) - ca;
         F.bc.u[BU_DONE] = 1u;
