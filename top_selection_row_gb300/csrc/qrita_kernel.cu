@@ -839,16 +839,25 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool value_ok, bool* used_valu
 // (and weighs) every bin with per-warp shared-memory histograms, one cluster
 // merge totals them, and the bin holding the boundary becomes the range.
 // List-region layout while it runs: per-warp counts and masses at 0 (24 KiB),
-// pivot floats at kWideQfOff, the CTA's bin totals for the cluster at
-// kWideTotOff (clear of the narrowing bins and of the ring; remote CTAs read
+// the CTA's bin totals for the cluster at kWideTotOff (clear of the narrowing bins and of the ring; remote CTAs read
 // them before the next cluster barrier, and nothing writes there before it).
 // ---------------------------------------------------------------------------
 constexpr int kWideBins = 256;
 static_assert(kWideBins == kThreads, "one thread per wide bin");
-constexpr int kWideQfOff = 24 * 1024;
 constexpr int kWideTotOff = 48 * 1024;
-static_assert(kWarps * kWideBins * 12 <= kWideQfOff, "wide histograms overlap the pivots");
+static_assert(kWarps * kWideBins * 12 <= kWideTotOff, "wide histograms overlap the totals");
 static_assert(kWideTotOff >= kBinBytes, "wide totals overlap the narrowing bins");
+
+// Exact 64-bit shared-memory accumulation by two 32-bit atomics: the low
+// word's carry (seen in the value the first atomic returns) goes into the
+// high word with the high half. Much cheaper than a 64-bit shared atomic.
+__device__ __forceinline__ void add_u64_halves(unsigned long long* p, unsigned long long v) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(p);  // little-endian: w[0] low, w[1] high
+  const uint32_t l = static_cast<uint32_t>(v);
+  const uint32_t old = atomicAdd(w, l);
+  const uint32_t h = static_cast<uint32_t>(v >> 32) + ((old + l) < old ? 1u : 0u);
+  if (h != 0u) atomicAdd(w + 1, h);
+}
 
 // Block-wide inclusive suffix sum over the 256 bins (thread b holds bin b):
 // returns the sum of bins b..255 (u64; counts fit, masses are below 2^63).
@@ -889,15 +898,18 @@ __device__ bool wide_pass(Ctx<DT>& c, Range& R) {
   const float w = (hi_v - lo_v) * (1.0f / kWideBins);
   const float inv_w = 1.0f / w;
   if (!(w > 0.f) || !isfinite(inv_w)) return false;
-  // pivots q_b = lo + (b + 1) w (b < 255), q_255 = hi: must increase strictly
-  const float q_prev = tid == 0 ? lo_v : fmaf(static_cast<float>(tid), w, lo_v);
-  const float q_mine = tid == kWideBins - 1 ? hi_v : fmaf(static_cast<float>(tid + 1), w, lo_v);
+  // pivots q_b = lo + (b + 1) w (b < 255), q_255 = hi: must increase strictly;
+  // recomputed wherever needed (the same expression gives the same float)
+  auto edge = [&](int b) -> float {
+    return b >= kWideBins - 1 ? hi_v : fmaf(static_cast<float>(b + 1), w, lo_v);
+  };
+  const float q_prev = tid == 0 ? lo_v : edge(tid - 1);
+  const float q_mine = edge(tid);
   if (__syncthreads_or(!(q_mine > q_prev)) != 0) return false;
 
   uint32_t* wcnt = reinterpret_cast<uint32_t*>(c.lists);  // [kWarps][256]
   unsigned long long* wmass =
       reinterpret_cast<unsigned long long*>(c.lists + kWarps * kWideBins * 4);  // [kWarps][256]
-  float* qf = reinterpret_cast<float*>(c.lists + kWideQfOff);
   uint32_t* tot_cnt = reinterpret_cast<uint32_t*>(c.lists + kWideTotOff);  // [257]
   unsigned long long* tot_mass =
       reinterpret_cast<unsigned long long*>(c.lists + kWideTotOff + 2048);  // [257]
@@ -905,7 +917,6 @@ __device__ bool wide_pass(Ctx<DT>& c, Range& R) {
     wcnt[wv * kWideBins + tid] = 0u;
     if (MASS) wmass[wv * kWideBins + tid] = 0ull;
   }
-  qf[tid] = q_mine;
   __syncthreads();
   const float scale = c.fix_scale;
   uint32_t above_c = 0;
@@ -922,12 +933,12 @@ __device__ bool wide_pass(Ctx<DT>& c, Range& R) {
     int b = static_cast<int>((x - lo_v) * inv_w);
     b = b < 0 ? 0 : (b > kWideBins - 1 ? kWideBins - 1 : b);
     // the estimate is within a bin of the truth: settle it on the pivots
-    if (b > 0 && x <= qf[b - 1]) --b;
-    if (b > 0 && x <= qf[b - 1]) --b;
-    if (b < kWideBins - 1 && x > qf[b]) ++b;
-    if (b < kWideBins - 1 && x > qf[b]) ++b;
+    if (b > 0 && x <= edge(b - 1)) --b;
+    if (b > 0 && x <= edge(b - 1)) --b;
+    if (b < kWideBins - 1 && x > edge(b)) ++b;
+    if (b < kWideBins - 1 && x > edge(b)) ++b;
     atomicAdd(&wcnt[warp * kWideBins + b], 1u);
-    if (MASS) atomicAdd(&wmass[warp * kWideBins + b], wf);
+    if (MASS) add_u64_halves(&wmass[warp * kWideBins + b], wf);
   };
   stream_chunk<DT>(
       c,
@@ -1040,8 +1051,8 @@ __device__ bool wide_pass(Ctx<DT>& c, Range& R) {
     F.bc.u[BU_MAXR] = 0xFFFFFFFFu;
   }
   if (here) {
-    F.bc.u[BU_LO] = tid == 0 ? R.lo : f2key(qf[tid - 1]);
-    F.bc.u[BU_HI] = tid == kWideBins - 1 ? R.hi : f2key(qf[tid]);
+    F.bc.u[BU_LO] = tid == 0 ? R.lo : f2key(q_prev);
+    F.bc.u[BU_HI] = tid == kWideBins - 1 ? R.hi : f2key(q_mine);
     F.bc.u[BU_CLO] = static_cast<uint32_t>(sc);
     F.bc.u[BU_CHI] = up_c;
     F.bc.x[BX_MLO] = MASS ? sm : 0ull;
