@@ -115,6 +115,17 @@ __device__ __forceinline__ bool f2_ge(F2 a, F2 b) {
 
 __device__ __forceinline__ float f2_float(F2 a) { return a.hi + a.lo; }
 
+// round(v), ties to even, for a float 0 <= v < 2^63: the value a 64-bit
+// round-to-nearest conversion gives, from two 32-bit conversions (64-bit
+// conversions issue on this GPU's narrow fp64 pipe). With h = floor(v / 2^32),
+// r = v - h 2^32 is exact in fp32 (v mod 2^32 keeps at most v's 24
+// significant bits), so round(v) = h 2^32 + round(r), and round(r) < 2^32.
+__device__ __forceinline__ unsigned long long round_u64(float v) {
+  const float hf = truncf(v * 0x1p-32f);
+  const float r = fmaf(-hf, 0x1p32f, v);
+  return (static_cast<unsigned long long>(static_cast<uint32_t>(hf)) << 32) | __float2uint_rn(r);
+}
+
 // Exact conversion of a fixed-point integer (< 2^63) to a pair, and back.
 __device__ __forceinline__ F2 f2_from_u64(unsigned long long v) {
   const float hi = __ull2float_rz(v);

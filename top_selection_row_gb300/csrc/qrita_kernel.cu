@@ -68,6 +68,10 @@ constexpr int kStages = 2;
 constexpr int kPieceBytes = 16384;
 constexpr int kPieceUnits = kPieceBytes / 16;
 constexpr int kRingBytes = kStages * kPieceBytes;
+// Passes that leave (part of) the own list unused stream through a deeper
+// ring: up to kMaxStages stages, the extra ones laid below the standard ring
+// over the list's unused bytes.
+constexpr int kMaxStages = 6;
 
 static_assert(kPieceUnits % kThreads == 0, "a piece is whole rounds of the block");
 // Bound of one wait for a bulk copy (a copy from valid global memory lands in
@@ -153,6 +157,23 @@ __device__ __forceinline__ float weight(float x, float m, bool m_neginf) {
   return m_neginf ? 1.0f : expf(x - m);
 }
 
+// Fixed-point softmax weight: round(exp(x - m) * scale). Every place that
+// weighs a value uses this one function, so sums and boundary weights agree.
+__device__ __forceinline__ unsigned long long weight_fx(float x, float m, bool m_neginf, float scale) {
+  return round_u64(weight(x, m, m_neginf) * scale);
+}
+
+// Bin of x among the increasing pivots (+inf padded): the number of pivots
+// below x, by a 4-step branch-free search.
+__device__ __forceinline__ int pivot_bin(const volatile float* qf, float x) {
+  int b = 0;
+  b += (x > qf[b + 7]) ? 8 : 0;
+  b += (x > qf[b + 3]) ? 4 : 0;
+  b += (x > qf[b + 1]) ? 2 : 0;
+  b += (x > qf[b]) ? 1 : 0;
+  return b;
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory layout
 // ---------------------------------------------------------------------------
@@ -201,19 +222,19 @@ struct alignas(16) Fixed {
   uint32_t seg_cnt[kWarps];
   uint32_t col_mode;            // own list in per-thread columns instead:
   uint8_t col_n[kThreads];      // thread t's entries are t + j * kThreads, j < col_n[t]
-  float tail_val[kThreads];  // search tail: the last range's elements (cluster-wide)
-  uint8_t tail_rank[kThreads];  // and the cluster rank each came from
-  unsigned long long tail_w[kThreads];  // and their fixed-point weights (mass search)
   uint32_t tail_n;
-  uint32_t tbin_c[16];               // search tail: counts and masses of its 16 bins
-  unsigned long long tbin_m[16];
+  uint32_t tbin_c[64];               // search tail: counts and masses of its bins
+  unsigned long long tbin_m[64];
   uint32_t tsel[2];                  // the bin holding the boundary, count above it
   unsigned long long tsel_m;         // and mass above it
+  uint32_t tkey[2];                  // the smallest and largest key of its members
+  float bp[16];                      // bracket pivots of the top-k search (+inf padded)
+  uint32_t bp_bins[16];              // own-list survivors between consecutive bracket pivots
   uint32_t seg_n[kWarps];  // streaming pass: per-warp survivor counts
   uint32_t seg_ovf;        // a warp's survivors exceeded its segment
   uint32_t err;       // a bulk-copy wait of this CTA gave up
   uint32_t err_any;   // some CTA of the row reported err (written remotely)
-  unsigned long long ring_bar[kStages];  // one mbarrier per ring stage
+  unsigned long long ring_bar[kMaxStages];  // one mbarrier per ring stage
 };
 
 // Bytes of the list region after Fixed: the own list (value + index), then
@@ -449,15 +470,26 @@ struct Ctx {
 
 // Issue the bulk copy of piece `piece` of the chunk body into ring stage `st`
 // (thread 0 only).
+// base: shared address of stage 0 of the ring the current pass uses.
 template <int DT>
-__device__ __forceinline__ void ring_issue(Ctx<DT>& c, int piece, int st) {
+__device__ __forceinline__ void ring_issue(Ctx<DT>& c, int piece, int st, uint32_t base) {
   const int u0 = piece * kPieceUnits;
   const int n = min(kPieceUnits, c.body_units - u0);
   const uint32_t bar = c.ring_bar + 8u * st;
   const uint32_t bytes = static_cast<uint32_t>(n) * 16u;
   mbar_expect_tx(bar, bytes);
-  bulk_g2s(c.ring + static_cast<uint32_t>(st) * kPieceBytes, c.gbody + 16 * static_cast<size_t>(u0), bytes, bar);
+  bulk_g2s(base + static_cast<uint32_t>(st) * kPieceBytes, c.gbody + 16 * static_cast<size_t>(u0), bytes, bar);
   c.ring_out |= 1u << st;
+}
+
+// Stages a pass may stream through when the first `used` bytes of the list
+// region must stay intact (the ring grows down from the end of the region).
+__host__ __device__ constexpr int ring_stages(size_t region, size_t used) {
+  return region < used + static_cast<size_t>(kRingBytes)
+             ? kStages
+             : ((region - used) / kPieceBytes > static_cast<size_t>(kMaxStages)
+                    ? kMaxStages
+                    : static_cast<int>((region - used) / kPieceBytes));
 }
 
 // Units of one ring piece each thread holds: unit j of a piece starting at
@@ -470,25 +502,29 @@ constexpr int kPieceThreadUnits = kPieceUnits / kThreads;
 // piece (v[j] valid when j * kThreads + tid < n); scalar_fn(x, idx, valid)
 // the head / tail element of this thread. Both are called by every thread
 // the same number of times (convergent), valid or not. prefetched: the first
-// min(kStages, pieces) copies were issued already. Every copy issued here has
+// min(kStages, pieces) copies were issued already (into the standard ring).
+// nst: ring stages (kStages: the standard ring; more reach down into the own
+// list, which the caller leaves unused there). Every copy issued here has
 // landed when it returns, unless a wait gave up (F->err set; later calls then
 // issue nothing).
 template <int DT, typename PieceFn, typename ScalarFn>
 __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, ScalarFn&& scalar_fn,
-                                              bool prefetched) {
+                                              bool prefetched, int nst = kStages) {
   constexpr int E = Ctx<DT>::E;
   constexpr int S = Ctx<DT>::S;
   Fixed& F = *c.F;
   const int tid = threadIdx.x;
   const int nb = c.body_units;
   const int npieces = (nb + kPieceUnits - 1) / kPieceUnits;
+  const uint32_t base = c.ring - static_cast<uint32_t>(nst - kStages) * kPieceBytes;
+  const uint4* base_ptr = c.ring_ptr - static_cast<size_t>(nst - kStages) * kPieceUnits;
+  if (!prefetched) fence_proxy_async_smem();  // generic writes to these bytes before the async copies
   __syncthreads();  // earlier users of the ring's bytes are done
   if (tid == 0 && !prefetched && npieces > 0 && vld(F.err) == 0u) {
-    fence_proxy_async_smem();  // generic writes to these bytes before the async copies
-    for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc);
+    for (int pc = 0; pc < npieces && pc < nst; ++pc) ring_issue(c, pc, pc, base);
   }
-  for (int pc = 0; pc < npieces; ++pc) {
-    const int st = pc % kStages;
+  int st = 0;
+  for (int pc = 0; pc < npieces; ++pc, st = (st + 1 == nst) ? 0 : st + 1) {
     const uint32_t bar = c.ring_bar + 8u * st;
     bool ok = false;
     if (vld(F.err) == 0u) ok = mbar_wait_bounded(bar, (c.ring_phase >> st) & 1u, kWaitLimitNs);
@@ -500,7 +536,7 @@ __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, Sc
     }
     const int u0 = pc * kPieceUnits;
     const int n = min(kPieceUnits, nb - u0);
-    const uint4* sp = c.ring_ptr + static_cast<size_t>(st) * kPieceUnits;
+    const uint4* sp = base_ptr + static_cast<size_t>(st) * kPieceUnits;
     uint4 v[kPieceThreadUnits];
 #pragma unroll
     for (int j = 0; j < kPieceThreadUnits; ++j) {
@@ -508,7 +544,7 @@ __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, Sc
       v[j] = (u < n) ? sp[u] : make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();  // every thread holds its part of stage st: refill it now
-    if (tid == 0 && pc + kStages < npieces && vld(F.err) == 0u) ring_issue(c, pc + kStages, st);
+    if (tid == 0 && pc + nst < npieces && vld(F.err) == 0u) ring_issue(c, pc + nst, st, base);
     piece_fn(v, u0, n);
   }
   float x = 0.f;
@@ -530,7 +566,7 @@ __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, Sc
 // stream_pieces one unit at a time: unit_fn(xs, idx0, valid) per unit.
 template <int DT, typename UnitFn, typename ScalarFn>
 __device__ __forceinline__ void stream_chunk(Ctx<DT>& c, UnitFn&& unit_fn, ScalarFn&& scalar_fn,
-                                             bool prefetched = false) {
+                                             bool prefetched = false, int nst = kStages) {
   constexpr int E = Ctx<DT>::E;
   stream_pieces<DT>(
       c,
@@ -543,7 +579,7 @@ __device__ __forceinline__ void stream_chunk(Ctx<DT>& c, UnitFn&& unit_fn, Scala
           unit_fn(xs, static_cast<uint32_t>(c.head_n + (u0 + u) * E), u < n);
         }
       },
-      scalar_fn, prefetched);
+      scalar_fn, prefetched, nst);
 }
 
 // The survivors of one ring piece (bits[j]: the elements of this thread's unit
@@ -596,7 +632,7 @@ __device__ __forceinline__ void append_piece(Ctx<DT>& c, uint32_t& wn, uint32_t 
 // this CTA's ring, so that none lands after the CTA has exited (thread 0).
 template <int DT>
 __device__ void ring_drain(Ctx<DT>& c) {
-  for (int st = 0; st < kStages; ++st)
+  for (int st = 0; st < kMaxStages; ++st)
     if ((c.ring_out >> st) & 1u)
       (void)mbar_wait_bounded(c.ring_bar + 8u * st, (c.ring_phase >> st) & 1u, kWaitLimitNs);
 }
@@ -619,17 +655,6 @@ struct Range {
   bool below;           // the target exceeds everything above lo: the boundary is at lo
   int passes;
 };
-
-// Bin of x among the increasing pivots (+inf padded): the number of pivots
-// below x, by a 4-step branch-free search.
-__device__ __forceinline__ int pivot_bin(const volatile float* qf, float x) {
-  int b = 0;
-  b += (x > qf[b + 7]) ? 8 : 0;
-  b += (x > qf[b + 3]) ? 4 : 0;
-  b += (x > qf[b + 1]) ? 2 : 0;
-  b += (x > qf[b]) ? 1 : 0;
-  return b;
-}
 
 // One narrowing pass: up to 15 pivots (two quaternary levels) cut (lo, hi]
 // into bins; every CTA bins its elements (from its list, or by streaming its
@@ -671,7 +696,7 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool value_ok, bool* used_valu
   auto bin_one = [&](float x) {
     if (!(lo_all || x > lo_f)) return;
     unsigned long long wf = 0ull;
-    if (MASS) wf = __float2ull_rn(weight(x, c.m, c.m_neginf) * scale);
+    if (MASS) wf = weight_fx(x, c.m, c.m_neginf, scale);
     if (x > hi_f) {
       ++above_c;
       above_m += wf;
@@ -690,7 +715,8 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool value_ok, bool* used_valu
       },
       [&](float x, uint32_t, bool valid) {
         if (valid) bin_one(x);
-      });
+      },
+      false, ring_stages(list_region_bytes(static_cast<int>(c.ocap)), kBinBytes));
   above_c = warp_sum_u(above_c);
   above_m = warp_sum_u64(above_m);
   if (lane == 0) {
@@ -839,14 +865,14 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool value_ok, bool* used_valu
 // (and weighs) every bin with per-warp shared-memory histograms, one cluster
 // merge totals them, and the bin holding the boundary becomes the range.
 // List-region layout while it runs: per-warp counts and masses at 0 (24 KiB),
-// the CTA's bin totals for the cluster at kWideTotOff (clear of the narrowing bins and of the ring; remote CTAs read
-// them before the next cluster barrier, and nothing writes there before it).
+// the CTA's bin totals for the cluster at kWideTotOff, the ring above them.
+// Remote CTAs read the totals between the pass's two cluster barriers.
 // ---------------------------------------------------------------------------
 constexpr int kWideBins = 256;
 static_assert(kWideBins == kThreads, "one thread per wide bin");
-constexpr int kWideTotOff = 48 * 1024;
-static_assert(kWarps * kWideBins * 12 <= kWideTotOff, "wide histograms overlap the totals");
-static_assert(kWideTotOff >= kBinBytes, "wide totals overlap the narrowing bins");
+constexpr int kWideTotOff = kWarps * kWideBins * 12;
+// bytes of the list region the wide pass keeps: histograms, then the totals
+constexpr int kWideUsed = kWideTotOff + 2048 + (kWideBins + 1) * 8;
 
 // Exact 64-bit shared-memory accumulation by two 32-bit atomics: the low
 // word's carry (seen in the value the first atomic returns) goes into the
@@ -924,7 +950,7 @@ __device__ bool wide_pass(Ctx<DT>& c, Range& R) {
   auto bin_one = [&](float x) {
     if (!(x > lo_v)) return;
     unsigned long long wf = 0ull;
-    if (MASS) wf = __float2ull_rn(weight(x, c.m, c.m_neginf) * scale);
+    if (MASS) wf = weight_fx(x, c.m, c.m_neginf, scale);
     if (x > hi_v) {
       ++above_c;
       above_m += wf;
@@ -949,7 +975,8 @@ __device__ bool wide_pass(Ctx<DT>& c, Range& R) {
       },
       [&](float x, uint32_t, bool valid) {
         if (valid) bin_one(x);
-      });
+      },
+      false, ring_stages(list_region_bytes(static_cast<int>(c.ocap)), kWideUsed));
   above_c = __reduce_add_sync(kFull, above_c);
   above_m = warp_sum_u64(above_m);
   if (lane == 0) {
@@ -1464,11 +1491,6 @@ __device__ __forceinline__ uint32_t copies_fx(unsigned long long need, unsigned 
   return static_cast<uint32_t>(k);
 }
 
-// Fixed-point softmax weight: round(exp(x - m) * scale). Every place that
-// weighs a value uses this one function, so sums and boundary weights agree.
-__device__ __forceinline__ unsigned long long weight_fx(float x, float m, bool m_neginf, float scale) {
-  return __float2ull_rn(weight(x, m, m_neginf) * scale);
-}
 
 // Sum of a 64-bit value over the warp with 32-bit reductions: split into
 // 21-bit parts, so no part's sum can wrap (values below 2^63).
@@ -1582,9 +1604,28 @@ __device__ void merge_count_mass(Ctx<DT>& c, uint32_t n, unsigned long long m, u
 }
 
 // Tail of the search: once the range holds at most kTail elements (over the
-// whole row) they are copied to every CTA and each tests itself as the
-// boundary (one thread each).
-constexpr int kTail = kThreads;
+// whole row) they are copied to every CTA, split into kTailBins value bins,
+// and the elements of the bin holding the boundary each test themselves.
+// Layout in the ring's bytes: values, weights, ranks, then the compacted
+// candidates' values and weights.
+constexpr int kTail = 1024;
+// Bracket pivots: before the streaming pass, the Gaussian model places
+// kBracket pivots where the count above is expected to be m_j k, m_j =
+// 2^((7 - j) / 5) (2.6 k down to 0.38 k); each CTA counts its survivors
+// above them and the first cluster merge totals the counts, so the top-k
+// search starts from the bracket that holds the boundary.
+constexpr int kBracket = 15;
+constexpr int kTailBins = 64;
+constexpr int kTailLevels = 3;   // bin splits of the tail at most
+constexpr int kTailDirect = 64;  // sets this small are tested directly
+constexpr int kTailValOff = 0;
+constexpr int kTailWOff = kTailValOff + kTail * 4;
+constexpr int kTailRankOff = kTailWOff + kTail * 8;
+constexpr int kCandValOff = kTailRankOff + kTail;
+constexpr int kCandWOff = kCandValOff + kTail * 4;
+static_assert(kCandWOff + kTail * 8 <= kRingBytes, "the search tail exceeds the ring's bytes");
+static_assert(kCandWOff % 8 == 0 && kTailWOff % 8 == 0, "tail weights are 8-byte aligned");
+static_assert(kTailBins == 64, "the bin scan gives each lane of one warp two bins");
 
 // Quaternary search (A6 for counts, A7 for mass) over the own lists of the
 // cluster. The search keeps count/mass(> lo) >= target > count/mass(> hi);
@@ -1598,8 +1639,10 @@ constexpr int kTail = kThreads;
 // hi, and s.c_hi / s.m_hi the row's count and mass above hi (including what
 // lies above the lists' range). Each round scans only the lists' (lo, hi].
 // On exit F.ties holds each rank's count of the boundary value.
+// synced: a cluster barrier passed since any CTA of the row last used its
+// ring (the tail is stored into the other CTAs' rings).
 template <int DT, bool MASS>
-__device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots) {
+__device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots, bool synced = true) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float scale = c.fix_scale;
@@ -1747,6 +1790,7 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
       }
     }
     __syncthreads();
+    QRITA_T(8);
     Slot& my = F.slots[c.ph & 1];
     if (warp == 0) {
       // this CTA's totals over its warps, published for the cluster
@@ -1771,6 +1815,7 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
       }
     }
     cluster_sync_all();
+    QRITA_T(9);
     if (warp == 0) {
       // lane r reads rank r's totals; the row's totals and per-rank shares
 #pragma unroll
@@ -1828,6 +1873,7 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
       }
     }
     __syncthreads();
+    QRITA_T(10);
   }
   if (done == 1 && collapsed && rounds == 0) {
     // the start range held one key
@@ -1836,7 +1882,16 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
   }
   if (done == 0) {
     // tail: every CTA's (lo, hi] elements (rank_lo - rank_hi of them) are
-    // stored into every CTA's tail buffer at the rank's offset
+    // stored into every CTA's tail buffer (the ring's bytes, idle during the
+    // search) at the rank's offset. A CTA may still be streaming into its ring
+    // unless a cluster barrier passed since: one is taken here if none did.
+    if (!synced && rounds == 0) cluster_sync_all();
+    unsigned char* rb = reinterpret_cast<unsigned char*>(const_cast<uint4*>(c.ring_ptr));
+    float* tv = reinterpret_cast<float*>(rb + kTailValOff);
+    unsigned long long* tw = reinterpret_cast<unsigned long long*>(rb + kTailWOff);
+    uint8_t* tr = rb + kTailRankOff;
+    float* cv = reinterpret_cast<float*>(rb + kCandValOff);
+    unsigned long long* cw = reinterpret_cast<unsigned long long*>(rb + kCandWOff);
     uint32_t off = 0;
     for (int r = 0; r < static_cast<int>(c.crank); ++r) off += vld(F.rank_lo[r]) - vld(F.rank_hi[r]);
     uint32_t total = 0;
@@ -1849,16 +1904,24 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     __syncthreads();
     own_for(c, [&](float x, uint32_t) {
       const uint32_t key = f2key(x);  // keys: lo may lie below key(-inf)
-      if (key > lo && key <= hi) {
-        const uint32_t dst = off + atomicAdd(&F.tail_n, 1u);
+      const bool in = key > lo && key <= hi;
+      // positions: one shared atomic per warp step
+      const uint32_t am = __activemask();
+      const uint32_t bal = __ballot_sync(am, in);
+      const int leader = __ffs(bal) - 1;
+      uint32_t wbase = 0;
+      if (lane == leader) wbase = atomicAdd(&F.tail_n, static_cast<uint32_t>(__popc(bal)));
+      wbase = __shfl_sync(am, wbase, leader < 0 ? 0 : leader);
+      if (in) {
+        const uint32_t dst = off + wbase + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
         if (dst < static_cast<uint32_t>(kTail)) {
           const unsigned long long w = MASS ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
           for (int r = 0; r < C; ++r) {
             const uint32_t rr = static_cast<uint32_t>(r);
-            st_dsmem_u32(map_rank(smem_u32(&F.tail_val[dst]), rr), __float_as_uint(x));
-            st_dsmem_u8(map_rank(smem_u32(&F.tail_rank[dst]), rr), c.crank);
+            st_dsmem_u32(map_rank(smem_u32(&tv[dst]), rr), __float_as_uint(x));
+            st_dsmem_u8(map_rank(smem_u32(&tr[dst]), rr), c.crank);
             if (MASS) {
-              const uint32_t a = map_rank(smem_u32(&F.tail_w[dst]), rr);
+              const uint32_t a = map_rank(smem_u32(&tw[dst]), rr);
               st_dsmem_u32(a, static_cast<uint32_t>(w));
               st_dsmem_u32(a + 4u, static_cast<uint32_t>(w >> 32));
             }
@@ -1866,118 +1929,176 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
         }
       }
     });
+    QRITA_T(12);
     cluster_sync_all();  // every CTA's tail buffer is complete
     QRITA_T(13);
-    // the candidates: first a split of (lo, hi] into 16 equal value bins
-    // (one pass over the tail, counts and masses per bin); the bin where the
-    // count (mass) from the top reaches the target holds the boundary, and
-    // only its elements are candidates
+    // the candidates: up to kTailLevels splits of the candidate set into
+    // kTailBins bins by a monotone function of the value over the set's value
+    // range [v0, v1], bin(x) = trunc((x - v0) nb / (v1 - v0)) (so bins are
+    // value intervals in increasing order). The bin where the count (mass)
+    // from the top reaches the target holds the boundary; its members become
+    // the set. A set of one value is the boundary itself; a small set is
+    // tested directly.
     if (tid < C) F.ties[tid] = 0u;
-    const float* tv = F.tail_val;
-    const unsigned long long* tw = F.tail_w;
-    const float lo_f = pivot_f(lo), hi_f = pivot_f(hi);
-    const float bw = (hi_f - lo_f) * (1.0f / 16.0f);
-    const bool split = total > 32u && isfinite(lo_f) && isfinite(hi_f) && bw > 0.f &&
-                       fmaf(15.0f, bw, lo_f) < hi_f && fmaf(1.0f, bw, lo_f) > lo_f;
-    // bin b = (edge(b-1), edge(b)], edge(-1) = lo, edge(15) = hi
-    auto edge = [&](int b) -> float {
-      return b < 0 ? lo_f : (b >= 15 ? hi_f : fmaf(static_cast<float>(b + 1), bw, lo_f));
-    };
-    uint32_t ckl = lo, ckh = hi;  // the candidates' key range (ckl, ckh]
-    uint32_t base_c = c_hi;       // count / mass above ckh
+    uint32_t base_c = c_hi;  // count / mass above the set
     unsigned long long base_m = m_hi;
-    if (split) {
-      if (tid < 16) {
+    const float* sv = tv;  // the set's values and weights
+    const unsigned long long* sw = tw;
+    uint32_t ns = total;
+    float v0 = pivot_f(lo), v1 = pivot_f(hi);  // level 0: the range (lo, hi]
+    bool one_value = false;
+    for (int level = 0; level < kTailLevels && ns > static_cast<uint32_t>(kTailDirect); ++level) {
+      const float inv_bw = static_cast<float>(kTailBins) / (v1 - v0);
+      if (!(isfinite(v0) && isfinite(v1) && v1 > v0 && isfinite(inv_bw) && inv_bw > 0.f)) break;
+      // members satisfy x > v0 (level 0) or x >= v0 (later): never negative
+      auto tbin = [&](float x) -> int {
+        const int b = static_cast<int>((x - v0) * inv_bw);
+        return b < 0 ? 0 : (b > kTailBins - 1 ? kTailBins - 1 : b);
+      };
+      if (tid < kTailBins) {
         F.tbin_c[tid] = 0u;
         F.tbin_m[tid] = 0ull;
       }
       __syncthreads();
-      if (tid < static_cast<int>(total)) {
-        const float x = tv[tid];
-        int b = static_cast<int>((x - lo_f) / bw);
-        b = b < 0 ? 0 : (b > 15 ? 15 : b);
-        if (b > 0 && x <= edge(b - 1)) --b;
-        if (b < 15 && x > edge(b)) ++b;
+      for (uint32_t i = tid; i < ns; i += kThreads) {
+        const int b = tbin(sv[i]);
         atomicAdd(&F.tbin_c[b], 1u);
-        if (MASS) atomicAdd(&F.tbin_m[b], tw[tid]);
+        if (MASS) add_u64_halves(&F.tbin_m[b], sw[i]);
       }
       __syncthreads();
-      if (tid == 0) {
-        uint32_t ac = c_hi;
-        unsigned long long am = m_hi;
-        int bs = 0;
-        for (int b = 15; b >= 0; --b) {
-          const uint32_t nc = ac + vld(F.tbin_c[b]);
-          const unsigned long long nm = am + vld(F.tbin_m[b]);
-          if ((MASS ? nm : static_cast<unsigned long long>(nc)) >= target) {
-            bs = b;
-            break;
+      if (warp == 0) {
+        // lane l holds bins 63 - 2l and 62 - 2l; prefix sums from the top
+        // find the first bin whose cumulative total reaches the target
+        const int b0 = kTailBins - 1 - 2 * lane, b1 = b0 - 1;
+        const uint32_t n0 = vld(F.tbin_c[b0]), n1 = vld(F.tbin_c[b1]);
+        const unsigned long long v0w = MASS ? vld(F.tbin_m[b0]) : static_cast<unsigned long long>(n0);
+        const unsigned long long v1w = MASS ? vld(F.tbin_m[b1]) : static_cast<unsigned long long>(n1);
+        unsigned long long incl = v0w + v1w;
+        uint32_t incl_n = n0 + n1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+          const uint32_t yn = __shfl_up_sync(kFull, incl_n, o);
+          if (lane >= o) {
+            incl += y;
+            incl_n += yn;
           }
-          ac = nc;
-          am = nm;
         }
-        F.tsel[0] = static_cast<uint32_t>(bs);
-        F.tsel[1] = ac;
-        F.tsel_m = am;
+        const unsigned long long top = MASS ? base_m : static_cast<unsigned long long>(base_c);
+        const unsigned long long ex = top + incl - (v0w + v1w);
+        const uint32_t ex_n = base_c + incl_n - (n0 + n1);
+        const bool r0 = ex + v0w >= target, r1 = ex + v0w + v1w >= target;
+        const uint32_t hit = __ballot_sync(kFull, r1);
+        const int L = hit != 0u ? __ffs(hit) - 1 : -1;
+        if (lane == (L < 0 ? 0 : L)) {
+          F.tsel[0] = L < 0 ? 0xFFFFFFFFu : static_cast<uint32_t>(r0 ? b0 : b1);
+          F.tsel[1] = r0 ? ex_n : ex_n + n0;
+          F.tsel_m = MASS ? (r0 ? ex : ex + v0w) : 0ull;
+          F.tkey[0] = 0xFFFFFFFFu;
+          F.tkey[1] = 0u;
+          F.tail_n = 0u;
+        }
       }
       __syncthreads();
-      const int bs = static_cast<int>(vld(F.tsel[0]));
-      if (bs > 0) ckl = f2key(edge(bs - 1));
-      if (bs < 15) ckh = f2key(edge(bs));
+      const uint32_t sel = vld(F.tsel[0]);
+      if (sel == 0xFFFFFFFFu) break;  // cannot happen while the set holds the boundary
+      const int bs = static_cast<int>(sel);
       base_c = vld(F.tsel[1]);
       base_m = vld(F.tsel_m);
-    }
-    // the candidates, compacted into the ring's bytes (no stream is in flight)
-    float* cv = reinterpret_cast<float*>(const_cast<uint4*>(c.ring_ptr));
-    unsigned long long* cw = reinterpret_cast<unsigned long long*>(cv + kTail);
-    if (tid == 0) F.tail_n = 0u;
-    __syncthreads();
-    if (tid < static_cast<int>(total)) {
-      const float x = tv[tid];
-      const uint32_t key = f2key(x);  // keys: lo may lie below key(-inf)
-      if (key > ckl && key <= ckh) {
-        const uint32_t pos = atomicAdd(&F.tail_n, 1u);
-        cv[pos] = x;
-        if (MASS) cw[pos] = tw[tid];
-      }
-    }
-    __syncthreads();
-    const uint32_t nc = min(vld(F.tail_n), static_cast<uint32_t>(kTail));
-    // every candidate v tests itself: it is the boundary when count(> v) <
-    // target <= count(>= v) (masses likewise), where further quaternary
-    // rounds would stop (tau = v = z_mn, N_zmn = N(v))
-    if (tid < static_cast<int>(nc)) {
-      const float v = cv[tid];
-      uint32_t gt = 0, eq = 0;
-      unsigned long long mgt = 0ull;
-      uint32_t i = 0;
-      for (; i + 8u <= nc; i += 8u) {
-        float xv[8];
+      // the members of bin bs become the set (compacted into cv / cw, in place
+      // when the set is there already: every thread reads before any writes)
+      float xr[kTail / kThreads];
+      unsigned long long wr[kTail / kThreads];
+      bool mem[kTail / kThreads];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) xv[u] = cv[i + u];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          gt += xv[u] > v ? 1u : 0u;
-          eq += xv[u] == v ? 1u : 0u;
-          if (MASS) mgt += xv[u] > v ? cw[i + u] : 0ull;
+      for (int j = 0; j < kTail / kThreads; ++j) {
+        const uint32_t i = tid + static_cast<uint32_t>(j) * kThreads;
+        mem[j] = false;
+        xr[j] = 0.f;
+        wr[j] = 0ull;
+        if (i < ns) {
+          xr[j] = sv[i];
+          wr[j] = MASS ? sw[i] : 0ull;
+          mem[j] = tbin(xr[j]) == bs;
         }
       }
-      for (; i < nc; ++i) {
-        const float xv = cv[i];
-        gt += xv > v ? 1u : 0u;
-        eq += xv == v ? 1u : 0u;
-        if (MASS) mgt += xv > v ? cw[i] : 0ull;
+      __syncthreads();
+      uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+      for (int j = 0; j < kTail / kThreads; ++j) {
+        if (mem[j]) {
+          const uint32_t pos = atomicAdd(&F.tail_n, 1u);
+          cv[pos] = xr[j];
+          if (MASS) cw[pos] = wr[j];
+          const uint32_t k = f2key(xr[j]);
+          kmin = min(kmin, k);
+          kmax = max(kmax, k);
+        }
       }
-      const unsigned long long above_gt = MASS ? mgt + base_m : static_cast<unsigned long long>(gt + base_c);
-      const unsigned long long wv = MASS ? cw[tid] : 1ull;
-      const unsigned long long above_ge = above_gt + static_cast<unsigned long long>(eq) * wv;
-      // every copy of the boundary value answers, with the same values
-      if (above_gt < target && target <= above_ge) {
-        F.bc.u[BU_TAU] = f2key(v);
-        const uint32_t ca = gt + base_c;
-        F.bc.u[BU_CABOVE] = ca;
-        F.bc.u[BU_NKEEP] = MASS ? copies_fx(target - above_gt, wv, eq) : static_cast<uint32_t>(target) - ca;
+      kmin = __reduce_min_sync(kFull, kmin);
+      kmax = __reduce_max_sync(kFull, kmax);
+      if (lane == 0) {
+        atomicMin(&F.tkey[0], kmin);
+        atomicMax(&F.tkey[1], kmax);
+      }
+      __syncthreads();
+      ns = vld(F.tail_n);
+      sv = cv;
+      sw = cw;
+      const uint32_t kmn = vld(F.tkey[0]), kmx = vld(F.tkey[1]);
+      v0 = key2f(kmn);
+      v1 = key2f(kmx);
+      if (kmn == kmx) {
+        one_value = true;
+        break;
+      }
+    }
+    if (one_value) {
+      // every member equals v0: it is the boundary, with ns copies
+      if (tid == 0) {
+        const unsigned long long wv = MASS ? sw[0] : 1ull;
+        F.bc.u[BU_TAU] = f2key(v0);
+        F.bc.u[BU_CABOVE] = base_c;
+        F.bc.u[BU_NKEEP] = MASS ? copies_fx(target - base_m, wv, ns) : static_cast<uint32_t>(target) - base_c;
         F.bc.u[BU_DONE] = 1u;
+      }
+    } else {
+      // every member v tests itself: it is the boundary when count(> v) <
+      // target <= count(>= v) (masses likewise), where further quaternary
+      // rounds would stop (tau = v = z_mn, N_zmn = N(v))
+      for (uint32_t ci = tid; ci < ns; ci += kThreads) {
+        const float v = sv[ci];
+        uint32_t gt = 0, eq = 0;
+        unsigned long long mgt = 0ull;
+        uint32_t i = 0;
+        for (; i + 8u <= ns; i += 8u) {
+          float xv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) xv[u] = sv[i + u];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            gt += xv[u] > v ? 1u : 0u;
+            eq += xv[u] == v ? 1u : 0u;
+            if (MASS) mgt += xv[u] > v ? sw[i + u] : 0ull;
+          }
+        }
+        for (; i < ns; ++i) {
+          const float xv = sv[i];
+          gt += xv > v ? 1u : 0u;
+          eq += xv == v ? 1u : 0u;
+          if (MASS) mgt += xv > v ? sw[i] : 0ull;
+        }
+        const unsigned long long above_gt = MASS ? mgt + base_m : static_cast<unsigned long long>(gt + base_c);
+        const unsigned long long wv = MASS ? sw[ci] : 1ull;
+        const unsigned long long above_ge = above_gt + static_cast<unsigned long long>(eq) * wv;
+        // every copy of the boundary value answers, with the same values
+        if (above_gt < target && target <= above_ge) {
+          F.bc.u[BU_TAU] = f2key(v);
+          const uint32_t ca = gt + base_c;
+          F.bc.u[BU_CABOVE] = ca;
+          F.bc.u[BU_NKEEP] = MASS ? copies_fx(target - above_gt, wv, eq) : static_cast<uint32_t>(target) - ca;
+          F.bc.u[BU_DONE] = 1u;
+        }
       }
     }
     __syncthreads();
@@ -1987,9 +2108,12 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     done = static_cast<int>(vld(F.bc.u[BU_DONE]));
     ++rounds;
     // per-rank copies of the boundary value
-    if (tid < static_cast<int>(total) && F.tail_val[tid] == key2f(tau)) {
-      const uint32_t rk = F.tail_rank[tid];
-      if (rk < c.C) atomicAdd(&F.ties[rk], 1u);  // a rank index from shared memory: bounded
+    const float tau_v = key2f(tau);
+    for (uint32_t i = tid; i < total; i += kThreads) {
+      if (tv[i] == tau_v) {
+        const uint32_t rk = tr[i];
+        if (rk < c.C) atomicAdd(&F.ties[rk], 1u);  // a rank index from shared memory: bounded
+      }
     }
     __syncthreads();
   }
@@ -2165,10 +2289,10 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       F.own_n = 0;
       F.err = 0u;
       F.err_any = 0u;
-      for (int st = 0; st < kStages; ++st) mbar_init(c.ring_bar + 8u * st, 1u);
+      for (int st = 0; st < kMaxStages; ++st) mbar_init(c.ring_bar + 8u * st, 1u);
       fence_mbar_init();
       const int npieces = (c.body_units + kPieceUnits - 1) / kPieceUnits;
-      for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc);
+      for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc, c.ring);
     }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -2289,6 +2413,22 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   const float t = vld(F.bc.f[BF_T]);
   const bool trunc = vld(F.bc.u[BU_TRUNC]) != 0u;
   QRITA_T(1);
+  const bool value_pivots = (P.flags & QRITA_FLAG_KEY_PIVOTS) == 0u;
+  // bracket pivots for a top-k search over the survivors (identical in every
+  // CTA of the row: they come from the shared sample); never below t, so the
+  // own lists' counts above them are the row's
+  const bool bracket = trunc && k_on && !p_only && value_pivots && sigma > 0.f && isfinite(sigma) &&
+                       isfinite(mu) && (P.flags & QRITA_FLAG_FORCE_FALLBACK) == 0u;
+  if (bracket && tid < 16) {
+    float q = INFINITY;
+    if (tid < kBracket) {
+      const float mj = exp2f(static_cast<float>(7 - tid) * 0.2f);
+      const float u = fminf(mj * static_cast<float>(kr) / static_cast<float>(V), 0.5f);
+      q = fmaxf(mu - sigma * normcdfinvf(u), t);
+    }
+    F.bp[tid] = q;  // published by the streaming pass's first block barrier
+    F.bp_bins[tid] = 0u;
+  }
 
   // ---- A4: the streaming pass (the one HBM read of the row)
   {
@@ -2395,6 +2535,24 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     } else {
       own_segments_streamed<DT>(c, trunc ? wn : 0u);
     }
+    if (bracket) {
+      // survivors between consecutive bracket pivots (bin b: b pivots below)
+      const volatile float* bq = F.bp;
+      own_for(c, [&](float x, uint32_t) { atomicAdd(&F.bp_bins[pivot_bin(bq, x)], 1u); });
+      __syncthreads();
+    }
+    if (bracket && warp == 0) {
+      // this CTA's count above each bracket pivot (the bins above it), for
+      // the merge
+      uint32_t v = lane < 16 ? vld(F.bp_bins[lane]) : 0u;
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(kFull, v, o);
+        if (lane + o < 16) v += y;
+      }
+      const uint32_t above = __shfl_down_sync(kFull, v, 1);  // bins lane + 1 .. 15
+      if (lane < kBracket) F.slots[c.ph & 1].cnt[lane] = above;
+    }
     // block reduce
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -2436,6 +2594,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       my.pr[3] = mm.lo;
     }
     cluster_sync_all();
+    if (bracket) {
+      // rank r's count above bracket pivot j (thread 16 r + j)
+      const uint32_t r = static_cast<uint32_t>(tid) >> 4, j = static_cast<uint32_t>(tid) & 15u;
+      if (r < c.C && j < static_cast<uint32_t>(kBracket))
+        F.rank_bins[r][j] = ld_dsmem_u32(map_rank(smem_u32(&my.cnt[j]), r));
+    }
     if (warp == 0) {
       float a = -INFINITY, b = INFINITY;
       uint32_t surv = 0, ovf = 0;
@@ -2493,7 +2657,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   (keep_all ? QRITA_PATH_KEEP_ALL : 0u);
   const bool force_fb = (P.flags & QRITA_FLAG_FORCE_FALLBACK) != 0u;
   const bool force_retry = (P.flags & QRITA_FLAG_FORCE_RETRY) != 0u;
-  const bool value_pivots = (P.flags & QRITA_FLAG_KEY_PIVOTS) == 0u;
 
   // Selection: keep key > tau, plus the n_keep lowest-id elements equal to
   // tau; F.ties[rank] counts the elements equal to tau in each rank's chunk.
@@ -2531,7 +2694,30 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       bool searched = false;  // the search ran on the own lists' survivors
       uint32_t qk = 0, S2 = 0;
       bool ovf2 = true;
-      if (hit) {
+      if (hit && bracket) {
+        // Z_t is in the own lists, and the merged bracket counts place the
+        // boundary: lane j totals pivot j over the ranks; the largest j whose
+        // count reaches k is lo, the next pivot hi (counts fall with j)
+        uint32_t tj = 0;
+        if (lane < kBracket)
+          for (uint32_t r = 0; r < c.C; ++r) tj += vld(F.rank_bins[r][lane]);
+        const uint32_t reach = __ballot_sync(kFull, lane < kBracket && tj >= target);
+        const int js = reach != 0u ? 31 - __clz(reach) : -1;
+        const uint32_t t_lo = __shfl_sync(kFull, tj, js < 0 ? 0 : js);
+        const bool hi_piv = js + 1 < kBracket;
+        const uint32_t t_hi = __shfl_sync(kFull, tj, hi_piv ? js + 1 : 0);
+        s.lo = js >= 0 ? f2key(vld(F.bp[js])) : f2key(t) - 1u;
+        s.c_lo = js >= 0 ? t_lo : survivors;
+        s.hi = hi_piv ? f2key(vld(F.bp[js + 1])) : f2key(row_max);
+        s.c_hi = hi_piv ? t_hi : 0u;
+        if (tid < static_cast<int>(c.C)) {
+          F.rank_lo[tid] = js >= 0 ? vld(F.rank_bins[tid][js]) : vld(F.rank_n[tid]);
+          F.rank_hi[tid] = hi_piv ? vld(F.rank_bins[tid][js + 1]) : 0u;
+        }
+        __syncthreads();
+        dsearch<DT, false>(c, s, target, value_pivots);
+        searched = true;
+      } else if (hit) {
         // Z_t is in the own lists: the candidates are (key(t) - 1, max]
         rank_counts_from<DT>(c, F.rank_n);
         s.lo = f2key(t) - 1u;
@@ -2629,7 +2815,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           s.hi = R.hi;
           s.c_hi = R.c_hi;
           s.c_above = R.c_hi;  // elements above hi exceed every pivot
-          dsearch<DT, false>(c, s, target, value_pivots);
+          dsearch<DT, false>(c, s, target, value_pivots, false);
           k_full = R.c_hi == 0u;  // nothing lies above the extracted range
           list_emit = false;
           ties_in_list = true;
@@ -2843,7 +3029,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             s.m_hi = R.m_hi;
             s.m_above = R.m_hi;
             ties_in_list = true;
-            dsearch<DT, true>(c, s, target, value_pivots);
+            dsearch<DT, true>(c, s, target, value_pivots, false);
           }
         }
         rounds_p = static_cast<uint32_t>(s.rounds);
@@ -2998,7 +3184,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             running += tot;
           }
           if (tail) c.gmask[idx] = byte_of(x, idx, rank);
-        });
+        },
+        false, ring_stages(list_region_bytes(static_cast<int>(c.ocap)), 0));
   }
   QRITA_T(7);
 
