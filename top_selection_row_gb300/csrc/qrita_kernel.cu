@@ -466,7 +466,25 @@ struct Ctx {
   float m;          // row max (softmax shift)
   bool m_neginf;
   float fix_scale;  // fixed-point scale of weights in [0, 1]
+  bool zero_fill;       // the chunk's mask is to be zeroed early (by the search tail)
+  bool zero_fill_done;  // and it was
 };
+
+// Fill the chunk's mask with one byte value (16-byte stores where aligned).
+template <int DT>
+__device__ __forceinline__ void fill_mask(Ctx<DT>& c, uint8_t fill) {
+  const int tid = threadIdx.x;
+  const uint32_t fill4 = fill ? 0x01010101u : 0u;
+  const uintptr_t ma = reinterpret_cast<uintptr_t>(c.gmask);
+  const int mh0 = static_cast<int>((16u - (ma & 15u)) & 15u);
+  const int mh = mh0 < c.n ? mh0 : c.n;
+  const int mb = (c.n - mh) / 16;
+  const int mt = c.n - mh - mb * 16;
+  if (tid < mh) c.gmask[tid] = fill;
+  for (int i = tid; i < mb; i += kThreads)
+    reinterpret_cast<uint4*>(c.gmask + mh)[i] = make_uint4(fill4, fill4, fill4, fill4);
+  if (tid < mt) c.gmask[mh + mb * 16 + tid] = fill;
+}
 
 // Issue the bulk copy of piece `piece` of the chunk body into ring stage `st`
 // (thread 0 only).
@@ -1299,7 +1317,8 @@ __device__ void own_columns_to_segments(Ctx<DT>& c, uint32_t cn) {
 }
 
 // fn(value, index) over this thread's share of the own list: its column, or
-// its lane's stride of its warp's segment (no collective operations inside fn).
+// its lane's stride of its warp's segment. Warp collectives inside fn must use
+// the active mask (the lanes' trip counts differ).
 template <int DT, typename Fn>
 __device__ __forceinline__ void own_for(Ctx<DT>& c, Fn&& fn) {
   Fixed& F = *c.F;
@@ -1932,6 +1951,13 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     QRITA_T(12);
     cluster_sync_all();  // every CTA's tail buffer is complete
     QRITA_T(13);
+    if (c.zero_fill) {
+      // the mask's zeros go out while the tail is tested (no cluster barrier
+      // with release ordering follows before the emission)
+      fill_mask<DT>(c, 0);
+      c.zero_fill = false;
+      c.zero_fill_done = true;
+    }
     // the candidates: up to kTailLevels splits of the candidate set into
     // kTailBins bins by a monotone function of the value over the set's value
     // range [v0, v1], bin(x) = trunc((x - v0) nb / (v1 - v0)) (so bins are
@@ -2229,6 +2255,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   c.m = 0.f;
   c.m_neginf = false;
   c.fix_scale = 0.f;
+  c.zero_fill = false;
+  c.zero_fill_done = false;
 
   const int64_t r = blockIdx.x / P.C;
   const int32_t V = P.V;
@@ -2715,6 +2743,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           F.rank_hi[tid] = hi_piv ? vld(F.rank_bins[tid][js + 1]) : 0u;
         }
         __syncthreads();
+        c.zero_fill = true;  // the mask is all zeros but for the scattered kept ids
         dsearch<DT, false>(c, s, target, value_pivots);
         searched = true;
       } else if (hit) {
@@ -3051,14 +3080,19 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   // arrive now, its wait at the end. A bulk-copy wait that gave up is
   // reported to every CTA before the arrive.
   const bool early_arrive = c.C > 1 && (sel_all || sel_none || list_emit);
+  const bool zero_filled = c.zero_fill_done;
   if (early_arrive) {
-    __syncthreads();
-    if (tid == 0 && vld(F.err) != 0u) {
-      ring_drain<DT>(c);
-      for (uint32_t rr = 0; rr < c.C; ++rr) st_dsmem_u32(map_rank(smem_u32(&F.err_any), rr), 1u);
+    if (__syncthreads_or(vld(F.err) != 0u) != 0) {
+      if (tid == 0) {
+        ring_drain<DT>(c);
+        for (uint32_t rr = 0; rr < c.C; ++rr) st_dsmem_u32(map_rank(smem_u32(&F.err_any), rr), 1u);
+      }
+      __syncthreads();
+      cluster_arrive();  // release: the flags are seen after the wait
+    } else {
+      // this CTA's accesses to other CTAs' memory were loads already used
+      cluster_arrive_relaxed();
     }
-    __syncthreads();
-    cluster_arrive();
   }
 
   // ---- A8: boundary ties by lowest token id
@@ -3088,20 +3122,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
 
   // ---- A9: mask emission
   if (sel_all || sel_none || list_emit) {
-    // fill the chunk's mask, then scatter the kept ids of the own list
-    {
-      const uint8_t fill = sel_all ? 1 : 0;
-      const uint32_t fill4 = sel_all ? 0x01010101u : 0u;
-      const uintptr_t ma = reinterpret_cast<uintptr_t>(c.gmask);
-      const int mh0 = static_cast<int>((16u - (ma & 15u)) & 15u);
-      const int mh = mh0 < c.n ? mh0 : c.n;
-      const int mb = (c.n - mh) / 16;
-      const int mt = c.n - mh - mb * 16;
-      if (tid < mh) c.gmask[tid] = fill;
-      for (int i = tid; i < mb; i += kThreads)
-        reinterpret_cast<uint4*>(c.gmask + mh)[i] = make_uint4(fill4, fill4, fill4, fill4);
-      if (tid < mt) c.gmask[mh + mb * 16 + tid] = fill;
-    }
+    // fill the chunk's mask (unless the search tail zeroed it already), then
+    // scatter the kept ids of the own list
+    if (sel_all || !zero_filled) fill_mask<DT>(c, sel_all ? 1 : 0);
     if (list_emit && !sel_all && !sel_none) {
       __syncthreads();  // the fill is ordered before the scatter
       own_for(c, [&](float x, uint32_t ix) {
