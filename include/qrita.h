@@ -84,6 +84,9 @@ enum {
                                           only (no value-space quartiles) */
 #define QRITA_FLAG_FORCE_RETRY 0x8u    /* top-k rows: treat the first truncation as a
                                           miss, so the second truncation runs */
+#define QRITA_FLAG_HIST_MISS 0x10u     /* top-p rows binned by the streaming pass: treat
+                                          the bins' bracket as missed, so the narrowing
+                                          passes run instead */
 #define QRITA_FLAG_CLUSTER_SHIFT 8     /* bits 8..10: force 2^n CTAs per row (n in 0..4);
                                           0 in these bits and bit 11 clear = automatic */
 #define QRITA_FLAG_CLUSTER_SET 0x800u  /* bit 11: the cluster-size bits are set */
@@ -100,6 +103,9 @@ enum {
 #define QRITA_PATH_RETRY 0x80u    /* top-k: a second truncation at an order statistic
                                      of a 4096-logit sample ran (the search ran on
                                      its survivors unless FALLBACK is also set) */
+#define QRITA_PATH_HIST 0x100u    /* top-p alone: value bins counted by the streaming
+                                     pass placed the boundary, and one more pass
+                                     extracted those bins for the search */
 
 /* Diagnostics of one row (qrita_select_ex, optional). Device memory. */
 typedef struct qrita_row_info {

@@ -197,7 +197,7 @@ def _mixed_batch():
 @pytest.mark.parametrize(
     "flags",
     ["none", "no_trunc", "fallback", "key_pivots", "c1", "c2", "c4", "c8", "c16", "fallback_key_c16",
-     "retry", "retry_c1", "retry_c16", "retry_key"],
+     "retry", "retry_c1", "retry_c16", "retry_key", "hist_miss", "hist_miss_c16"],
 )
 def test_forced_paths_match_oracle(dev, flags):
     import top_selection_row_gb300 as q
@@ -217,6 +217,8 @@ def test_forced_paths_match_oracle(dev, flags):
         "retry_c1": q.FLAG_FORCE_RETRY | q.flag_cluster(1),
         "retry_c16": q.FLAG_FORCE_RETRY | q.flag_cluster(16),
         "retry_key": q.FLAG_FORCE_RETRY | q.FLAG_KEY_PIVOTS,
+        "hist_miss": q.FLAG_HIST_MISS,
+        "hist_miss_c16": q.FLAG_HIST_MISS | q.flag_cluster(16),
     }[flags]
     for n, logits, k, p in _mixed_batch():
         w = WORKLOADS[n]
@@ -225,6 +227,24 @@ def test_forced_paths_match_oracle(dev, flags):
         if flags.startswith("retry"):
             top_k = (k >= 1) & (k < w.V)
             assert ((info["path"][top_k] & q.PATH_RETRY) != 0).all()
+        if flags.startswith("hist_miss"):
+            assert ((info["path"] & q.PATH_HIST) == 0).all()
+
+
+def test_first_pass_bins_place_flat_top_p_rows(dev):
+    """Top-p rows whose survivors far exceed the lists (flat rows: high
+    temperature) take their boundary's bins from the streaming pass, so one
+    more pass extracts them and no narrowing pass runs."""
+    import top_selection_row_gb300 as q
+
+    w = WORKLOADS[3]
+    logits, k, p = workload(3, 48)
+    for flags in (0, q.flag_cluster(1), q.flag_cluster(8)):
+        fails, flagged, got, st, info = check_against_oracle(logits, w.dtype, k, p, dev, flags=flags)
+        assert fails == [], (flags, fails[:5])
+        hist = (info["path"] & q.PATH_HIST) != 0
+        assert hist.sum() >= 8, (flags, int(hist.sum()))
+        assert (info["passes"][hist] == 1).all()
 
 
 def test_second_truncation_rescues_uniform_rows(dev):

@@ -227,6 +227,12 @@ __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");
 }
 
+// Shared-memory add without a returned value.
+__device__ __forceinline__ void red_add_shared_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(v)
+               : "memory");
+}
+
 // Arrive without release ordering: for a CTA whose earlier accesses to other
 // CTAs' memory were loads whose values it has used already.
 __device__ __forceinline__ void cluster_arrive_relaxed() {

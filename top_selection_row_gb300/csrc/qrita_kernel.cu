@@ -246,11 +246,11 @@ __host__ __device__ constexpr size_t list_region_bytes(int ocap) {
 // Names of the broadcast slots
 enum : int {
   // floats
-  BF_MU = 0, BF_SIGMA, BF_MREF, BF_T, BF_MAX, BF_MIN, BF_LOF, BF_HIF,
+  BF_MU = 0, BF_SIGMA, BF_MREF, BF_T, BF_MAX, BF_MIN, BF_LOF, BF_HIF, BF_PHAM,
   // uints
   BU_TRUNC = 0, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
   BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS, BU_S2, BU_OVF2,
-  BU_QKEY, BU_QWANT,
+  BU_QKEY, BU_QWANT, BU_PHAC,
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
   // float pairs
@@ -1200,6 +1200,208 @@ __device__ void extract_range(Ctx<DT>& c, const Range& R) {
       });
   __syncthreads();
   QRITA_T(12);
+}
+
+// ---------------------------------------------------------------------------
+// Top-p rows binned by the streaming pass (top-p alone, far more survivors
+// than the lists hold): the streaming pass also counts and weighs the
+// survivors in kHistBins value bins of [t, m_ref] (bin(x) = trunc((x - t) nb /
+// (m_ref - t)), a monotone function of x, so bins are value intervals; the
+// survivors above m_ref are totalled apart). The weights there are fp32
+// exp(x - m_ref) in 32-bit fixed point: approximate, they only choose the
+// bins around the boundary. One more pass (split_pass) then keeps every
+// element above the chosen bins, extracts the bins' elements to the own
+// list and weighs both exactly in the search's fixed point; the search runs
+// on the list when the exact masses confirm the bracket.
+// List-region layout while the streaming pass runs: per-warp counts at 0,
+// per-warp masses at kWarps * kHistBins * 4; the CTA's totals at kPhTotOff
+// (counts, 64-bit masses, then the count and fp32 mass above m_ref).
+// ---------------------------------------------------------------------------
+constexpr int kHistBins = 256;
+static_assert(kHistBins == kThreads, "one thread per histogram bin");
+constexpr int kPhTotOff = 2 * kWarps * kHistBins * 4;
+constexpr int kPhAboveOff = kPhTotOff + kHistBins * 4 + kHistBins * 8;
+
+// Block-wide inclusive suffix sum of one float per thread (thread b, bin b).
+template <int DT>
+__device__ __forceinline__ float bin_suffix_sum_f(Ctx<DT>& c, float v) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_down_sync(kFull, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  if (lane == 0) F.redf[warp][2] = incl;
+  __syncthreads();
+  float above = 0.f;
+  for (int w = warp + 1; w < kWarps; ++w) above += vld(F.redf[w][2]);
+  __syncthreads();
+  return incl + above;
+}
+
+// Largest key k in [a, b] with bin(k) <= g, given bin(a) <= g; bin is
+// monotone in the key. A 32-way search by each warp (every lane returns it).
+template <typename BinFn>
+__device__ __forceinline__ uint32_t last_key_in_bins(uint32_t a, uint32_t b, int g, BinFn&& bin) {
+  const int lane = threadIdx.x & 31;
+  if (bin(b) <= g) return b;
+  uint32_t lo = a, hi = b;  // bin(lo) <= g < bin(hi)
+  for (int it = 0; it < 40 && hi - lo > 1u; ++it) {
+    const uint32_t span = hi - lo;
+    const uint32_t probe = lo + static_cast<uint32_t>((static_cast<uint64_t>(span) * (lane + 1)) >> 5);
+    const uint32_t bal = __ballot_sync(kFull, lane < 31 && bin(probe) <= g);
+    const int L = __popc(bal);  // probes 0 .. L-1 are in, probe L (or hi) is out
+    const uint32_t nlo = __shfl_sync(kFull, probe, L > 0 ? L - 1 : 0);
+    const uint32_t nhi = __shfl_sync(kFull, probe, L < 31 ? L : 31);
+    if (L > 0) lo = nlo;
+    hi = L < 31 ? nhi : hi;
+  }
+  return lo;
+}
+
+// The pass after the first-pass histogram: elements above hi (keys) are kept
+// (mask 1), those in (lo, hi] go to the own list (mask 0 until the search
+// decides), the rest are dropped; the kept and the listed are weighed
+// exactly. Returns this CTA's count and mass above hi and the list's mass
+// (every thread); F.own_n counts the list.
+template <int DT>
+__device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_above,
+                           unsigned long long& m_above, unsigned long long& m_in) {
+  constexpr int E = Ctx<DT>::E;
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) F.own_n = 0;
+  const float scale = c.fix_scale;
+  uint32_t ca = 0;
+  unsigned long long ma = 0ull, mi = 0ull;
+  const uintptr_t mbp = reinterpret_cast<uintptr_t>(c.gmask + c.head_n);
+  const bool vec_ok = (mbp % E) == 0;
+  auto classify = [&](float x, uint8_t& byte) -> bool {
+    const uint32_t k = f2key(x);
+    const bool above = k > hi;
+    const bool in = !above && k > lo;
+    if (above || in) {
+      const unsigned long long w = weight_fx(x, c.m, c.m_neginf, scale);
+      if (above) {
+        ++ca;
+        ma += w;
+      } else {
+        mi += w;
+      }
+    }
+    byte = above ? 1 : 0;
+    return in;
+  };
+  stream_chunk<DT>(
+      c,
+      [&](const float (&xs)[E], uint32_t idx0, bool valid) {
+        uint32_t bits = 0;
+        if (valid) {
+          uint8_t bytes[E];
+#pragma unroll
+          for (int e = 0; e < E; ++e) bits |= classify(xs[e], bytes[e]) ? (1u << e) : 0u;
+          uint8_t* dst = c.gmask + idx0;
+          if (vec_ok) {
+            if constexpr (E == 4) {
+              *reinterpret_cast<uint32_t*>(dst) =
+                  bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
+            } else {
+              const uint32_t w0 =
+                  bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
+              const uint32_t w1 =
+                  bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (static_cast<uint32_t>(bytes[7]) << 24);
+              *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) dst[e] = bytes[e];
+          }
+        }
+        warp_append<E>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx0, bits);
+      },
+      [&](float x, uint32_t idx, bool valid) {
+        uint32_t bits = 0;
+        if (valid) {
+          uint8_t byte;
+          bits = classify(x, byte) ? 1u : 0u;
+          c.gmask[idx] = byte;
+        }
+        const float xs[1] = {x};
+        warp_append<1>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx, bits);
+      });
+  ca = __reduce_add_sync(kFull, ca);
+  ma = warp_sum_u64(ma);
+  mi = warp_sum_u64(mi);
+  if (lane == 0) {
+    F.lred[0][warp][0].cnt = ca;
+    F.lred[0][warp][0].mass = ma;
+    F.lred[0][warp][1].mass = mi;
+  }
+  __syncthreads();
+  uint32_t tc = 0;
+  unsigned long long tma = 0ull, tmi = 0ull;
+  for (int w = 0; w < kWarps; ++w) {
+    tc += vld(F.lred[0][w][0].cnt);
+    tma += vld(F.lred[0][w][0].mass);
+    tmi += vld(F.lred[0][w][1].mass);
+  }
+  c_above = tc;
+  m_above = tma;
+  m_in = tmi;
+  __syncthreads();
+}
+
+// Cluster merge after split_pass: F.rank_n[r] (list entries of rank r),
+// F.bc.u[BU_S2] (row list entries), F.bc.u[BU_OVF2] (a list overflowed),
+// F.bc.u[BU_CHI] (row count above hi), F.bc.x[BX_MHI] / [BX_MLO] (row mass
+// above hi / of the lists).
+template <int DT>
+__device__ void merge_split(Ctx<DT>& c, uint32_t n, uint32_t ovf, uint32_t ca, unsigned long long ma,
+                            unsigned long long mi) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  Slot& my = F.slots[c.ph & 1];
+  if (tid == 0) {
+    my.u[0] = n;
+    my.u[1] = ovf;
+    my.u[2] = ca;
+    my.mass[0] = ma;
+    my.mass[1] = mi;
+  }
+  cluster_sync_all();
+  if (warp == 0) {
+    uint32_t rn = 0, ro = 0, rc = 0;
+    unsigned long long rma = 0ull, rmi = 0ull;
+    if (lane < static_cast<int>(c.C)) {
+      const uint32_t ub = map_rank(smem_u32(&my.u[0]), static_cast<uint32_t>(lane));
+      const uint32_t mb = map_rank(smem_u32(&my.mass[0]), static_cast<uint32_t>(lane));
+      rn = ld_dsmem_u32(ub);
+      ro = ld_dsmem_u32(ub + 4u);
+      rc = ld_dsmem_u32(ub + 8u);
+      rma = static_cast<unsigned long long>(ld_dsmem_u32(mb)) |
+            (static_cast<unsigned long long>(ld_dsmem_u32(mb + 4u)) << 32);
+      rmi = static_cast<unsigned long long>(ld_dsmem_u32(mb + 8u)) |
+            (static_cast<unsigned long long>(ld_dsmem_u32(mb + 12u)) << 32);
+      ro |= rn > c.ocap ? 1u : 0u;
+      F.rank_n[lane] = rn;
+    }
+    const uint32_t tn = __reduce_add_sync(kFull, rn);
+    const uint32_t to = __reduce_or_sync(kFull, ro);
+    const uint32_t tcn = __reduce_add_sync(kFull, rc);
+    const unsigned long long tma = warp_sum_u64(rma);
+    const unsigned long long tmi = warp_sum_u64(rmi);
+    if (lane == 0) {
+      F.bc.u[BU_S2] = tn;
+      F.bc.u[BU_OVF2] = to;
+      F.bc.u[BU_CHI] = tcn;
+      F.bc.x[BX_MHI] = tma;
+      F.bc.x[BX_MLO] = tmi;
+    }
+  }
+  __syncthreads();
+  ++c.ph;
 }
 
 // The own list as kWarps segments: warp w owns entries [seg_base[w],
@@ -2457,6 +2659,28 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     F.bp[tid] = q;  // published by the streaming pass's first block barrier
     F.bp_bins[tid] = 0u;
   }
+  // top-p alone with far more expected survivors than the lists hold: the
+  // streaming pass also bins the survivors in [t, m_ref] (see split_pass)
+  // (bins over [t, ph_hi]; ph_hi = min(m_ref, mu + 4 sigma), so an outlier in
+  // the sample does not widen them; weights there are at most 1)
+  float ph_inv_w = 0.f, ph_scale = 0.f, ph_hi = 0.f;
+  bool ph = false;
+  if (p_only && trunc && sigma > 0.f && isfinite(m_ref) && (P.flags & QRITA_FLAG_FORCE_FALLBACK) == 0u) {
+    const float expect = static_cast<float>(V) * normcdff((mu - t) / sigma);
+    ph_hi = fminf(m_ref, fmaf(kClipSigmas, sigma, mu));
+    ph_inv_w = static_cast<float>(kHistBins) / (ph_hi - t);
+    ph = ph_hi > t && expect > 0.9f * static_cast<float>(c.ocap) * static_cast<float>(c.C) && isfinite(ph_inv_w) &&
+         ph_inv_w > 0.f;
+    // 32-bit bin masses per warp: a warp bins at most chunk / kWarps + 32
+    // elements (the same scale in every CTA of the row)
+    const uint32_t per_warp = static_cast<uint32_t>(P.chunk) / kWarps + 32u;
+    ph_scale = exp2f(static_cast<float>(__clz(per_warp)));
+  }
+  if (ph) {
+    uint32_t* h = reinterpret_cast<uint32_t*>(c.lists);
+    for (int i = tid; i < 2 * kWarps * kHistBins; i += kThreads) h[i] = 0u;
+    // published by the streaming pass's first block barrier
+  }
 
   // ---- A4: the streaming pass (the one HBM read of the row)
   {
@@ -2480,9 +2704,26 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       }
       ++cn;
     };
-    auto streaming_pass = [&](auto po, auto cm) {
+    uint32_t* ph_cnt = reinterpret_cast<uint32_t*>(c.lists) + warp * kHistBins;
+    uint32_t* ph_mass = ph_cnt + kWarps * kHistBins;
+    uint32_t ph_n = 0, ph_ac = 0;  // survivors; those above ph_hi
+    float ph_am = 0.f;             // and the latter's weight (shift m_ref)
+    auto ph_bin = [&](float x, float w) {
+      ++ph_n;
+      if (x <= ph_hi) {
+        int b = static_cast<int>((x - t) * ph_inv_w);
+        b = b > kHistBins - 1 ? kHistBins - 1 : b;
+        red_add_shared_u32(&ph_cnt[b], 1u);
+        red_add_shared_u32(&ph_mass[b], __float2uint_rn(w * ph_scale));
+      } else {
+        ++ph_ac;
+        ph_am += w;
+      }
+    };
+    auto streaming_pass = [&](auto po, auto cm, auto hc) {
       constexpr bool PO = decltype(po)::value;
       constexpr bool COL = decltype(cm)::value;
+      constexpr bool PH = decltype(hc)::value;
       stream_pieces<DT>(
           c,
           [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
@@ -2505,6 +2746,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                     const float w = expf(x - m_ref);
                     zu += w;
                     mu_ += surv ? w : 0.f;
+                    if constexpr (PH) {
+                      if (surv) ph_bin(x, w);
+                    }
                   }
                 }
                 if constexpr (PO) {
@@ -2527,7 +2771,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   col_put(x, idx0 + static_cast<uint32_t>(e));
                 }
               }
-            } else {
+            } else if constexpr (!PH) {
               append_piece<DT>(c, wn, seg_base, segcap, xs, bits, u0);
             }
           },
@@ -2542,20 +2786,24 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                 const float w = expf(x - m_ref);
                 f2_add(zs, w);
                 f2_add(ms, surv ? w : 0.f);
+                if constexpr (PH) {
+                  if (surv) ph_bin(x, w);
+                }
               }
             }
             const float xs[1] = {x};
             if constexpr (COL) {
               if (bits) col_put(x, idx);
-            } else {
+            } else if constexpr (!PH) {
               if (trunc) seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, bits);
             }
           },
           true);
     };
-    if (p_only) streaming_pass(BoolC<true>{}, BoolC<false>{});
-    else if (col) streaming_pass(BoolC<false>{}, BoolC<true>{});
-    else streaming_pass(BoolC<false>{}, BoolC<false>{});
+    if (ph) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<true>{});
+    else if (p_only) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<false>{});
+    else if (col) streaming_pass(BoolC<false>{}, BoolC<true>{}, BoolC<false>{});
+    else streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{});
     QRITA_T(2);
     if (col) {
       own_columns_streamed<DT>(c, cn);
@@ -2580,6 +2828,45 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       }
       const uint32_t above = __shfl_down_sync(kFull, v, 1);  // bins lane + 1 .. 15
       if (lane < kBracket) F.slots[c.ph & 1].cnt[lane] = above;
+    }
+    if (ph) {
+      // this CTA's bin totals and its survivors above m_ref, read by the
+      // other CTAs of the row after the merge; the survivors are counted
+      // (none is in the own list: the merge sees an overflow)
+      uint32_t* tc = reinterpret_cast<uint32_t*>(c.lists + kPhTotOff);
+      unsigned long long* tm = reinterpret_cast<unsigned long long*>(c.lists + kPhTotOff + kHistBins * 4);
+      uint32_t* ta = reinterpret_cast<uint32_t*>(c.lists + kPhAboveOff);
+      const uint32_t* h = reinterpret_cast<const uint32_t*>(c.lists);
+      uint32_t sc = 0;
+      unsigned long long sm = 0ull;
+      for (int w = 0; w < kWarps; ++w) {
+        sc += vld(h[w * kHistBins + tid]);
+        sm += vld(h[(kWarps + w) * kHistBins + tid]);
+      }
+      tc[tid] = sc;
+      tm[tid] = sm;
+      const uint32_t wnn = __reduce_add_sync(kFull, ph_n), wac = __reduce_add_sync(kFull, ph_ac);
+      const float wam = warp_sum_f(ph_am);
+      if (lane == 0) {
+        F.redu[warp][0] = wnn;
+        F.redu[warp][1] = wac;
+        F.redf[warp][7] = wam;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t a = 0, b = 0;
+        float m2 = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          a += vld(F.redu[w][0]);
+          b += vld(F.redu[w][1]);
+          m2 += vld(F.redf[w][7]);
+        }
+        F.own_n = a;
+        F.seg_ovf = 1u;
+        ta[0] = b;
+        ta[1] = __float_as_uint(m2);
+      }
+      __syncthreads();
     }
     // block reduce
 #pragma unroll
@@ -2697,6 +2984,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   bool list_emit = false;     // every kept element is in this CTA's own list
   bool ties_in_list = false;  // every element equal to tau is in this CTA's own list
   bool ties_known = false;    // F.ties holds the per-rank tie counts
+  bool ph_mask = false;       // the mask holds 1 above the own lists' range, 0 elsewhere
 
   if (!invalid && !keep_all) {
     // the streaming pass summed exp(x - m_ref); shift m is a factor exp(m_ref - m) away
@@ -2994,71 +3282,174 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           // boundary lies above t, and the target is p Z from the streaming pass
           const bool mass_hit = !k_on && trunc && !force_fb && ref_ok &&
                                 f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
-          if (k_on) {
-            R.lo = tau_k;
-            R.c_lo = above_k;
-            R.extra = static_cast<unsigned long long>(nk_k) * weight_fx(key2f(tau_k), c.m, c.m_neginf, scale);
-          } else if (mass_hit) {
-            R.lo = f2key(t) - 1u;
-            R.c_lo = survivors;
-            R.target_from_total = false;
-            R.target = f2_to_u64(f2_mul(f2_mul(Zm, pr), scale));
-            R.m_lo = f2_to_u64(f2_mul(Mm, scale));
-          } else {
-            R.lo = f2key(row_min) - 1u;
-            R.c_lo = static_cast<uint32_t>(V);
-          }
-          R.lo_all = R.lo < kKeyNegInf;
-          R.hi = f2key(row_max);
-          R.c_hi = 0;
-          narrow<DT, true>(c, R);
-          passes += static_cast<uint32_t>(R.passes);
-          const unsigned long long target = R.target;
-          z_used = f2_to_u64(f2_mul(f2_from_u64(target), 1.0f / pr));
-          // the chunk passes overwrote the lists: the emission streams the
-          // chunk unless an extraction below refills them
-          list_emit = false;
-          ties_in_list = false;
-          if (R.below) {
-            // only after top-k: mass(> tau_k) < p Z_k, so the boundary lies in
-            // the tau_k tie group (whose per-rank counts F.ties still holds)
-            s.tau = tau_k;
-            s.n_keep = copies_fx(target - R.m_lo, weight_fx(key2f(tau_k), c.m, c.m_neginf, scale), nk_k);
-            s.count_above = above_k;
-            s.rounds = 0;
-            s.capped = false;
-            have_exact = true;
-          } else if (R.exact) {
-            s.tau = R.hi;
-            s.n_keep = copies_fx(target - R.m_hi, weight_fx(key2f(R.hi), c.m, c.m_neginf, scale), R.c_lo - R.c_hi);
-            s.count_above = R.c_hi;
-            s.rounds = 0;
-            s.capped = false;
-            have_exact = true;
-            if (tid < static_cast<int>(c.C)) F.ties[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
-            __syncthreads();
-            ties_known = true;
-          } else if (!R.fits) {
-            s.capped = true;
-            s.rounds = 0;
-          } else {
-            extract_range<DT>(c, R);
-            own_segments_contiguous<DT>(c);
-            if (tid < static_cast<int>(c.C)) {
-              F.rank_lo[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
-              F.rank_hi[tid] = 0u;
+          bool ph_done = false;
+          if (ph && mass_hit && (P.flags & QRITA_FLAG_HIST_MISS) == 0u) {
+            // the first pass's bins: row totals of bin tid (approximate mass,
+            // shift m_ref) and of the survivors above m_ref
+            const uint32_t* tc = reinterpret_cast<const uint32_t*>(c.lists + kPhTotOff);
+            const unsigned long long* tm =
+                reinterpret_cast<const unsigned long long*>(c.lists + kPhTotOff + kHistBins * 4);
+            const uint32_t* ta = reinterpret_cast<const uint32_t*>(c.lists + kPhAboveOff);
+            float mf = 0.f;
+            for (uint32_t r = 0; r < c.C; ++r) {
+              const uint32_t ab = map_rank(smem_u32(&tm[tid]), r);
+              const unsigned long long v = static_cast<unsigned long long>(ld_dsmem_u32(ab)) |
+                                           (static_cast<unsigned long long>(ld_dsmem_u32(ab + 4u)) << 32);
+              mf += __ull2float_rn(v);
             }
-            __syncthreads();
-            s.lo = R.lo;
-            s.hi = R.hi;
-            s.c_lo = R.c_lo;
-            s.c_hi = R.c_hi;
-            s.c_above = R.c_hi;
-            s.m_lo = R.m_lo;
-            s.m_hi = R.m_hi;
-            s.m_above = R.m_hi;
-            ties_in_list = true;
-            dsearch<DT, true>(c, s, target, value_pivots, false);
+            mf *= 1.0f / ph_scale;
+            if (warp == 0) {
+              uint32_t ac = 0;
+              float am = 0.f;
+              if (lane < static_cast<int>(c.C)) {
+                ac = ld_dsmem_u32(map_rank(smem_u32(&ta[0]), static_cast<uint32_t>(lane)));
+                am = __uint_as_float(ld_dsmem_u32(map_rank(smem_u32(&ta[1]), static_cast<uint32_t>(lane))));
+              }
+              ac = __reduce_add_sync(kFull, ac);
+              am = warp_sum_f(am);
+              if (lane == 0) {
+                F.bc.u[BU_PHAC] = ac;
+                F.bc.f[BF_PHAM] = am;
+              }
+            }
+            const float sfx = bin_suffix_sum_f<DT>(c, mf);  // block barriers inside
+            const float am_row = vld(F.bc.f[BF_PHAM]);
+            const float cum = sfx + am_row;  // mass of bins tid.. and above m_ref
+            const float T = f2_float(f2_mul(Zr, pr));
+            // the largest bin whose mass from the top reaches p Z (approximately),
+            // with one bin of margin on either side
+            const int nb = __syncthreads_count(cum >= T);
+            const int bstar = am_row >= T ? kHistBins : nb - 1;
+            // rank tid's elements in bins [b0, b1] (bin kHistBins: above ph_hi)
+            auto rank_count = [&](int b0, int b1) -> uint32_t {
+              uint32_t cr = 0;
+              const int top = b1 < kHistBins - 1 ? b1 : kHistBins - 1;
+              for (int b = b0; b <= top; ++b) cr += ld_dsmem_u32(map_rank(smem_u32(&tc[b]), static_cast<uint32_t>(tid)));
+              if (b1 >= kHistBins) cr += ld_dsmem_u32(map_rank(smem_u32(&ta[0]), static_cast<uint32_t>(tid)));
+              return cr;
+            };
+            int bl = bstar - 1 < 0 ? 0 : bstar - 1;
+            int bh = bstar + 1;  // >= kHistBins: the range reaches above ph_hi
+            bool fits = __syncthreads_and(tid >= static_cast<int>(c.C) || rank_count(bl, bh) <= c.ocap) != 0;
+            if (!fits && bstar < kHistBins) {
+              // without the margin bins
+              bl = bstar;
+              bh = bstar;
+              fits = __syncthreads_and(tid >= static_cast<int>(c.C) || rank_count(bl, bh) <= c.ocap) != 0;
+            }
+            cluster_sync_all();  // every CTA has read the others' totals
+            if (nb > 0 && fits) {
+              // the bins' key range: bin(x) as the streaming pass computed it
+              auto bfun = [&](uint32_t k) -> int {
+                const float x = key2f(k);
+                if (!(x >= t)) return -1;
+                if (x > ph_hi) return kHistBins;
+                const int b = static_cast<int>((x - t) * ph_inv_w);
+                return b > kHistBins - 1 ? kHistBins - 1 : b;
+              };
+              const uint32_t kt = f2key(t), km = f2key(ph_hi);
+              const uint32_t lo_key = bl == 0 ? kt - 1u : last_key_in_bins(kt, km, bl - 1, bfun);
+              const bool to_top = bh >= kHistBins;
+              const uint32_t hi_key = to_top ? kKeyPosInf : last_key_in_bins(kt, km, bh, bfun);
+              uint32_t ca = 0;
+              unsigned long long ma = 0ull, mi = 0ull;
+              split_pass<DT>(c, lo_key, hi_key, ca, ma, mi);
+              passes += 1u;
+              own_segments_contiguous<DT>(c);
+              merge_split<DT>(c, vld(F.own_n), vld(F.seg_ovf), ca, ma, mi);
+              const uint32_t n_in = vld(F.bc.u[BU_S2]);
+              const bool ovf_in = vld(F.bc.u[BU_OVF2]) != 0u;
+              const uint32_t c_above = vld(F.bc.u[BU_CHI]);
+              const unsigned long long m_above = vld(F.bc.x[BX_MHI]), m_in = vld(F.bc.x[BX_MLO]);
+              const unsigned long long target = f2_to_u64(f2_mul(f2_mul(Zm, pr), scale));
+              // the exact masses confirm the bracket: search the lists
+              if (!ovf_in && m_above < target && target <= m_above + m_in) {
+                rank_counts_from<DT>(c, F.rank_n);
+                s.lo = lo_key;
+                s.hi = to_top ? f2key(row_max) : hi_key;
+                s.c_lo = c_above + n_in;
+                s.c_hi = c_above;
+                s.m_lo = m_above + m_in;
+                s.m_hi = m_above;
+                s.c_above = c_above;
+                s.m_above = m_above;
+                z_used = f2_to_u64(f2_mul(Zm, scale));
+                list_emit = true;
+                ties_in_list = true;
+                ph_mask = true;
+                path |= QRITA_PATH_HIST;
+                dsearch<DT, true>(c, s, target, value_pivots);
+                ph_done = true;
+              }
+            }
+          }
+          if (!ph_done) {
+            if (k_on) {
+              R.lo = tau_k;
+              R.c_lo = above_k;
+              R.extra = static_cast<unsigned long long>(nk_k) * weight_fx(key2f(tau_k), c.m, c.m_neginf, scale);
+            } else if (mass_hit) {
+              R.lo = f2key(t) - 1u;
+              R.c_lo = survivors;
+              R.target_from_total = false;
+              R.target = f2_to_u64(f2_mul(f2_mul(Zm, pr), scale));
+              R.m_lo = f2_to_u64(f2_mul(Mm, scale));
+            } else {
+              R.lo = f2key(row_min) - 1u;
+              R.c_lo = static_cast<uint32_t>(V);
+            }
+            R.lo_all = R.lo < kKeyNegInf;
+            R.hi = f2key(row_max);
+            R.c_hi = 0;
+            narrow<DT, true>(c, R);
+            passes += static_cast<uint32_t>(R.passes);
+            const unsigned long long target = R.target;
+            z_used = f2_to_u64(f2_mul(f2_from_u64(target), 1.0f / pr));
+            // the chunk passes overwrote the lists: the emission streams the
+            // chunk unless an extraction below refills them
+            list_emit = false;
+            ties_in_list = false;
+            if (R.below) {
+              // only after top-k: mass(> tau_k) < p Z_k, so the boundary lies in
+              // the tau_k tie group (whose per-rank counts F.ties still holds)
+              s.tau = tau_k;
+              s.n_keep = copies_fx(target - R.m_lo, weight_fx(key2f(tau_k), c.m, c.m_neginf, scale), nk_k);
+              s.count_above = above_k;
+              s.rounds = 0;
+              s.capped = false;
+              have_exact = true;
+            } else if (R.exact) {
+              s.tau = R.hi;
+              s.n_keep = copies_fx(target - R.m_hi, weight_fx(key2f(R.hi), c.m, c.m_neginf, scale), R.c_lo - R.c_hi);
+              s.count_above = R.c_hi;
+              s.rounds = 0;
+              s.capped = false;
+              have_exact = true;
+              if (tid < static_cast<int>(c.C)) F.ties[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
+              __syncthreads();
+              ties_known = true;
+            } else if (!R.fits) {
+              s.capped = true;
+              s.rounds = 0;
+            } else {
+              extract_range<DT>(c, R);
+              own_segments_contiguous<DT>(c);
+              if (tid < static_cast<int>(c.C)) {
+                F.rank_lo[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
+                F.rank_hi[tid] = 0u;
+              }
+              __syncthreads();
+              s.lo = R.lo;
+              s.hi = R.hi;
+              s.c_lo = R.c_lo;
+              s.c_hi = R.c_hi;
+              s.c_above = R.c_hi;
+              s.m_lo = R.m_lo;
+              s.m_hi = R.m_hi;
+              s.m_above = R.m_hi;
+              ties_in_list = true;
+              dsearch<DT, true>(c, s, target, value_pivots, false);
+            }
           }
         }
         rounds_p = static_cast<uint32_t>(s.rounds);
@@ -3124,7 +3515,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   if (sel_all || sel_none || list_emit) {
     // fill the chunk's mask (unless the search tail zeroed it already), then
     // scatter the kept ids of the own list
-    if (sel_all || !zero_filled) fill_mask<DT>(c, sel_all ? 1 : 0);
+    if (sel_all || sel_none || !(zero_filled || ph_mask)) fill_mask<DT>(c, sel_all ? 1 : 0);
     if (list_emit && !sel_all && !sel_none) {
       __syncthreads();  // the fill is ordered before the scatter
       own_for(c, [&](float x, uint32_t ix) {
