@@ -1261,76 +1261,89 @@ __device__ __forceinline__ uint32_t last_key_in_bins(uint32_t a, uint32_t b, int
   return lo;
 }
 
+template <int DT>
+__device__ void own_segments_streamed(Ctx<DT>& c, uint32_t wn);
+
 // The pass after the first-pass histogram: elements above hi (keys) are kept
-// (mask 1), those in (lo, hi] go to the own list (mask 0 until the search
-// decides), the rest are dropped; the kept and the listed are weighed
-// exactly. Returns this CTA's count and mass above hi and the list's mass
-// (every thread); F.own_n counts the list.
+// (mask 1), those in (lo, hi] go to this warp's segment of the own list (mask
+// 0 until the search decides), the rest are dropped; the kept and the listed
+// are weighed exactly. Returns this CTA's count and mass above hi and the
+// list's mass (every thread); the own list's segments are published.
 template <int DT>
 __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_above,
                            unsigned long long& m_above, unsigned long long& m_in) {
   constexpr int E = Ctx<DT>::E;
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) F.own_n = 0;
   const float scale = c.fix_scale;
+  const uint32_t segcap = c.ocap / kWarps;
+  const uint32_t seg_base = static_cast<uint32_t>(warp) * segcap;
+  uint32_t wn = 0;
   uint32_t ca = 0;
   unsigned long long ma = 0ull, mi = 0ull;
   const uintptr_t mbp = reinterpret_cast<uintptr_t>(c.gmask + c.head_n);
   const bool vec_ok = (mbp % E) == 0;
-  auto classify = [&](float x, uint8_t& byte) -> bool {
-    const uint32_t k = f2key(x);
-    const bool above = k > hi;
-    const bool in = !above && k > lo;
-    if (above || in) {
-      const unsigned long long w = weight_fx(x, c.m, c.m_neginf, scale);
-      if (above) {
-        ++ca;
-        ma += w;
-      } else {
-        mi += w;
-      }
-    }
-    byte = above ? 1 : 0;
-    return in;
-  };
-  stream_chunk<DT>(
+  stream_pieces<DT>(
       c,
-      [&](const float (&xs)[E], uint32_t idx0, bool valid) {
-        uint32_t bits = 0;
-        if (valid) {
-          uint8_t bytes[E];
+      [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
+        float xs[kPieceThreadUnits][E];
+        uint32_t bits[kPieceThreadUnits];
 #pragma unroll
-          for (int e = 0; e < E; ++e) bits |= classify(xs[e], bytes[e]) ? (1u << e) : 0u;
-          uint8_t* dst = c.gmask + idx0;
-          if (vec_ok) {
-            if constexpr (E == 4) {
-              *reinterpret_cast<uint32_t*>(dst) =
-                  bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
-            } else {
-              const uint32_t w0 =
-                  bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (static_cast<uint32_t>(bytes[3]) << 24);
-              const uint32_t w1 =
-                  bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (static_cast<uint32_t>(bytes[7]) << 24);
-              *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+        for (int j = 0; j < kPieceThreadUnits; ++j) {
+          unpack<DT>(v[j], xs[j]);
+          bits[j] = 0u;
+          if (j * kThreads + tid < n) {
+            uint32_t keep = 0u;  // bit e: element e is above hi
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+              const float x = xs[j][e];
+              const uint32_t k = f2key(x);
+              const bool above = k > hi;
+              const bool in = !above && k > lo;
+              const unsigned long long w = weight_fx(x, c.m, c.m_neginf, scale);
+              ca += above ? 1u : 0u;
+              ma += above ? w : 0ull;
+              mi += in ? w : 0ull;
+              keep |= above ? (1u << e) : 0u;
+              bits[j] |= in ? (1u << e) : 0u;
             }
-          } else {
+            // one mask byte per element (bit e of keep -> byte e)
+            uint8_t* dst = c.gmask + c.head_n + static_cast<size_t>(u0 + j * kThreads + tid) * E;
+            const uint32_t w0 = (keep & 1u) | ((keep & 2u) << 7) | ((keep & 4u) << 14) | ((keep & 8u) << 21);
+            if (vec_ok) {
+              if constexpr (E == 4) {
+                *reinterpret_cast<uint32_t*>(dst) = w0;
+              } else {
+                const uint32_t k1 = keep >> 4;
+                const uint32_t w1 = (k1 & 1u) | ((k1 & 2u) << 7) | ((k1 & 4u) << 14) | ((k1 & 8u) << 21);
+                *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+              }
+            } else {
 #pragma unroll
-            for (int e = 0; e < E; ++e) dst[e] = bytes[e];
+              for (int e = 0; e < E; ++e) dst[e] = static_cast<uint8_t>((keep >> e) & 1u);
+            }
           }
         }
-        warp_append<E>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx0, bits);
+        append_piece<DT>(c, wn, seg_base, segcap, xs, bits, u0);
       },
       [&](float x, uint32_t idx, bool valid) {
         uint32_t bits = 0;
         if (valid) {
-          uint8_t byte;
-          bits = classify(x, byte) ? 1u : 0u;
-          c.gmask[idx] = byte;
+          const uint32_t k = f2key(x);
+          const bool above = k > hi;
+          const bool in = !above && k > lo;
+          const unsigned long long w = weight_fx(x, c.m, c.m_neginf, scale);
+          ca += above ? 1u : 0u;
+          ma += above ? w : 0ull;
+          mi += in ? w : 0ull;
+          bits = in ? 1u : 0u;
+          c.gmask[idx] = above ? 1 : 0;
         }
         const float xs[1] = {x};
-        warp_append<1>(&F.own_n, c.own_val, c.own_idx, c.ocap, xs, idx, bits);
-      });
+        seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, bits);
+      },
+      false);
+  own_segments_streamed<DT>(c, wn);
   ca = __reduce_add_sync(kFull, ca);
   ma = warp_sum_u64(ma);
   mi = warp_sum_u64(mi);
@@ -3355,7 +3368,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               unsigned long long ma = 0ull, mi = 0ull;
               split_pass<DT>(c, lo_key, hi_key, ca, ma, mi);
               passes += 1u;
-              own_segments_contiguous<DT>(c);
               merge_split<DT>(c, vld(F.own_n), vld(F.seg_ovf), ca, ma, mi);
               const uint32_t n_in = vld(F.bc.u[BU_S2]);
               const bool ovf_in = vld(F.bc.u[BU_OVF2]) != 0u;
