@@ -108,7 +108,12 @@ struct Shape {
   int chunk;
   int ocap;
   size_t smem;
+  bool multi_wave;  // more CTAs than the device holds at once
 };
+
+// Rows are reordered (heavy first) only for batches this small: every CTA
+// reads all k and p to find its row.
+constexpr int64_t kMaxReorderRows = 8192;
 
 // Launch shape: the row is split into C contiguous chunks (one CTA each, one
 // cluster per row). C is the largest power of two that keeps the whole batch
@@ -136,6 +141,7 @@ int choose_shape(int64_t B, int64_t V, uint32_t flags, Shape* out) {
   const int ocap = kOwnCap;
   const size_t smem = smem_bytes(ocap);
   if (smem == 0 || smem > static_cast<size_t>(optin)) return QRITA_EUNSUPPORTED;
+  out->multi_wave = B * C > static_cast<int64_t>(sm_count()) * kCtasPerSm;
   out->C = C;
   out->chunk = static_cast<int>(chunk);
   out->ocap = ocap;
@@ -177,6 +183,7 @@ int select_impl(const void* logits, int dtype, int64_t B, int64_t V, const int32
   prm.chunk = sh.chunk;
   prm.ocap = sh.ocap;
   prm.flags = flags;
+  prm.heavy_first = (sh.multi_wave && B <= kMaxReorderRows && p != nullptr) ? 1 : 0;
   prm.alpha_k = kAlphaK;
   prm.alpha_min_k = kAlphaMinK;
   prm.margin_p = kMarginP;

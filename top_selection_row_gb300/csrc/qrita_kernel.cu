@@ -250,7 +250,7 @@ enum : int {
   // uints
   BU_TRUNC = 0, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
   BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS, BU_S2, BU_OVF2,
-  BU_QKEY, BU_QWANT, BU_PHAC,
+  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW,
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
   // float pairs
@@ -2436,6 +2436,46 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
   return hi;
 }
 
+// Row of cluster slot `slot` when heavy rows go first: rows whose top-p runs
+// alone (their streaming pass weighs every logit, and most take more passes)
+// take the first slots, then the others, each group in row order, so the
+// longest rows start in the first wave. Every thread returns the row.
+__device__ int64_t heavy_first_row(const Params& P, Fixed& F, int64_t slot) {
+  const int tid = threadIdx.x;
+  const int64_t B = P.B;
+  const int64_t per = (B + kThreads - 1) / kThreads;
+  const int64_t r0 = min(B, static_cast<int64_t>(tid) * per), r1 = min(B, r0 + per);
+  auto heavy = [&](int64_t r) -> bool {
+    const int32_t k = P.k ? P.k[r] : 0;
+    const float p = P.p ? P.p[r] : 1.0f;
+    const bool k_on = k >= 1 && k < P.V;
+    return p < 1.0f && p > 0.0f && !k_on;
+  };
+  uint32_t mine = 0;
+  for (int64_t r = r0; r < r1; ++r) mine += heavy(r) ? 1u : 0u;
+  uint32_t tot = 0;
+  const uint32_t before = block_excl_scan(F, mine, &tot);  // heavy rows below r0
+  const bool want_heavy = slot < static_cast<int64_t>(tot);
+  const int64_t want = want_heavy ? slot : slot - tot;
+  const int64_t have_before = want_heavy ? static_cast<int64_t>(before) : r0 - before;
+  const int64_t have = want_heavy ? static_cast<int64_t>(mine) : (r1 - r0) - mine;
+  if (tid == 0) F.bc.u[BU_ROW] = static_cast<uint32_t>(slot);  // unless a block holds it
+  __syncthreads();
+  if (want >= have_before && want < have_before + have) {
+    int64_t seen = have_before;
+    for (int64_t r = r0; r < r1; ++r) {
+      if (heavy(r) == want_heavy) {
+        if (seen == want) F.bc.u[BU_ROW] = static_cast<uint32_t>(r);
+        ++seen;
+      }
+    }
+  }
+  __syncthreads();
+  const int64_t row = vld(F.bc.u[BU_ROW]);
+  __syncthreads();
+  return row;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_constant__ Params P) {
   constexpr int E = Ctx<DT>::E;
@@ -2473,7 +2513,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   c.zero_fill = false;
   c.zero_fill_done = false;
 
-  const int64_t r = blockIdx.x / P.C;
+  const int64_t r = P.heavy_first ? heavy_first_row(P, F, blockIdx.x / P.C) : blockIdx.x / P.C;
   const int32_t V = P.V;
   const int64_t c0 = static_cast<int64_t>(c.crank) * P.chunk;
   const int64_t rem = static_cast<int64_t>(V) - c0;
