@@ -1704,10 +1704,6 @@ __device__ void retry_pass(Ctx<DT>& c, float t2) {
 // ---------------------------------------------------------------------------
 struct Local {
   uint32_t lo, hi, c_lo, c_hi;   // row counts above lo / hi
-  // count search: the Gaussian model of the row for the first pivots
-  // (model_sigma <= 0: none)
-  float model_mu, model_sigma;
-  int model_V;
   unsigned long long m_lo, m_hi;  // row masses above lo / hi (fixed point, mass search)
   uint32_t c_above;               // row count above the gathered range
   unsigned long long m_above;     // row mass above the gathered range (fixed point)
@@ -1736,61 +1732,6 @@ __device__ __forceinline__ unsigned long long warp_sum_u64_redux(unsigned long l
   const unsigned long long s1 = __reduce_add_sync(kFull, p1);
   const unsigned long long s2 = __reduce_add_sync(kFull, p2);
   return s0 + (s1 << 21) + (s2 << 42);
-}
-
-// Quaternary search (A6 for counts, A7 for mass) over g_val[0..g_n). The
-// search keeps count/mass(> lo) >= target > count/mass(> hi); each round
-// evaluates three pivots at 25/50/75 % of the range and stops at the first
-// pivot whose z_mn is the boundary (above(q) reaches the target and above(q)
-// minus the N_zmn copies of z_mn does not): tau = z_mn and the number of
-// kept copies follows. Masses are exact sums of fixed-point weights, so
-// every decision is integer arithmetic; warp 0 takes it and broadcasts it.
-// target is the count (A6) or the fixed-point mass (A7) to reach.
-// Three increasing pivot keys strictly inside (lo, hi) at the floats v0 < v1
-// < v2; false when they collapse or leave the range.
-__device__ __forceinline__ bool pivots_at(uint32_t lo, uint32_t hi, float v0, float v1, float v2, uint32_t (&q)[3]) {
-  if (!(v0 < v1 && v1 < v2) || !isfinite(v0) || !isfinite(v2)) return false;
-  q[0] = f2key(v0);
-  q[1] = f2key(v1);
-  q[2] = f2key(v2);
-  return lo < q[0] && q[0] < q[1] && q[1] < q[2] && q[2] < hi;
-}
-
-// Count search pivots placed where the count above them is expected to cross
-// the target. First round: the Gaussian tail anchored at the range's lower
-// end, where the count is known (count(> v) = c_lo Q((v - mu)/sigma) /
-// Q((v_lo - mu)/sigma)), solved for 1.25, 1 and 0.8 times the target. Later
-// rounds: interpolation of log(count) in value between the range ends (a
-// Gaussian tail is close to exponential), with pivots an eighth of the range
-// apart around the estimate. The quaternary search stays exact whatever the
-// pivots; these only save rounds.
-__device__ __forceinline__ bool count_model_pivots(const Local& s, uint32_t target, uint32_t (&q)[3]) {
-  const float v_lo = pivot_f(s.lo);
-  if (!isfinite(v_lo) || s.c_lo == 0u) return false;
-  const float q_lo = normcdff((s.model_mu - v_lo) / s.model_sigma);  // upper tail at v_lo
-  float v[3];
-  const float f[3] = {1.25f, 1.0f, 0.8f};
-#pragma unroll
-  for (int j = 0; j < 3; ++j) {
-    const float u = q_lo * fminf(static_cast<float>(target) * f[j] / static_cast<float>(s.c_lo), 1.0f);
-    v[j] = s.model_mu - s.model_sigma * normcdfinvf(u);
-  }
-  return pivots_at(s.lo, s.hi, v[0], v[1], v[2], q);
-}
-
-__device__ __forceinline__ bool count_interp_pivots(uint32_t lo, uint32_t hi, uint32_t c_lo, uint32_t c_hi,
-                                                    uint32_t target, uint32_t (&q)[3]) {
-  const float v_lo = pivot_f(lo), v_hi = pivot_f(hi);
-  if (!isfinite(v_lo) || !isfinite(v_hi) || !(v_hi > v_lo) || c_lo <= c_hi) return false;
-  const float l_lo = logf(static_cast<float>(c_lo));
-  const float l_hi = logf(static_cast<float>(c_hi) + 0.5f);
-  const float l_t = logf(static_cast<float>(target) - 0.5f);
-  float f = (l_lo - l_t) / (l_lo - l_hi);
-  f = fminf(fmaxf(f, 0.125f), 0.875f);
-  const float width = v_hi - v_lo;
-  const float mid = fmaf(f, width, v_lo);
-  const float d = 0.125f * width;
-  return pivots_at(lo, hi, mid - d, mid, mid + d, q);
 }
 
 // One cluster merge of a per-CTA count, mass and overflow flag (thread 0's
@@ -1861,13 +1802,16 @@ static_assert(kCandWOff + kTail * 8 <= kRingBytes, "the search tail exceeds the 
 static_assert(kCandWOff % 8 == 0 && kTailWOff % 8 == 0, "tail weights are 8-byte aligned");
 static_assert(kTailBins == 64, "the bin scan gives each lane of one warp two bins");
 
-// Quaternary search (A6 for counts, A7 for mass) over the own lists of the
-// cluster. The search keeps count/mass(> lo) >= target > count/mass(> hi);
-// each round evaluates three pivots: every CTA counts (and weighs) its own
-// list, the CTAs' partials are merged through distributed shared memory, and
-// every CTA takes the same decision: stop at the first pivot whose z_mn is
-// the boundary (above(q) reaches the target and above(q) minus the N_zmn
-// copies of z_mn does not), else move lo / hi. Masses are exact sums of
+// Distributed search (A6 for counts, A7 for mass) over the own lists of the
+// cluster: the pages' quaternary search, generalised to kSplit-way rounds.
+// The search keeps count/mass(> lo) >= target > count/mass(> hi). Each round
+// cuts (lo, hi] into kSplit bins by a monotone function of the value (equal
+// value widths; equal key widths after a value split that kept more than half
+// of the range), every CTA counts (and weighs) its own list into them, the
+// bins merge through distributed shared memory, and every CTA keeps the bin
+// where the count (mass) from the top reaches the target. Once the range
+// holds at most kTail elements they are gathered and tested directly (the
+// tail, where the pages' z_mn / N_zmn test decides). Masses are exact sums of
 // fixed-point weights, so every decision is integer arithmetic.
 // On entry F.rank_lo / F.rank_hi hold each rank's own-list counts above lo /
 // hi, and s.c_hi / s.m_hi the row's count and mass above hi (including what
@@ -1875,6 +1819,16 @@ static_assert(kTailBins == 64, "the bin scan gives each lane of one warp two bin
 // On exit F.ties holds each rank's count of the boundary value.
 // synced: a cluster barrier passed since any CTA of the row last used its
 // ring (the tail is stored into the other CTAs' rings).
+constexpr int kSplit = kTailBins;
+struct RoundBin {  // one bin of one CTA's round, published for the cluster
+  uint32_t cnt, above;  // elements in the bin, in the bins above it
+  unsigned long long mass;
+};
+constexpr int kRoundPubOff = 26 * 1024;  // two alternating areas in the ring's bytes
+static_assert(kRoundPubOff >= kCandWOff + kTail * 8, "round bins overlap the tail");
+static_assert(kRoundPubOff + 2 * kSplit * static_cast<int>(sizeof(RoundBin)) <= kRingBytes,
+              "round bins exceed the ring's bytes");
+
 template <int DT, bool MASS>
 __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool value_pivots, bool synced = true) {
   Fixed& F = *c.F;
@@ -1886,18 +1840,6 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
   unsigned long long m_lo = s.m_lo, m_hi = s.m_hi;
   uint32_t tau = 0, n_keep = 0, cabove = 0;
   int done = 0;  // 1: boundary found, 2: round cap
-  uint32_t q[3];
-  bool used_value = false;
-  const bool model = !MASS && value_pivots && s.model_sigma > 0.f;
-  bool interp = false;  // this round's pivots came from the model / interpolation
-  int np;
-  if (model && hi - lo > 4u && count_model_pivots(s, static_cast<uint32_t>(target), q)) {
-    np = 3;
-    interp = true;
-  } else {
-    np = quartile_pivots(lo, hi, value_pivots, q[0], q[1], q[2], used_value);
-  }
-  int done_j = -1, lo_j = -1, hi_j = -1;
   bool collapsed = false;  // (lo, hi] holds one key: the boundary is hi
   // the boundary is the single key hi of (lo, hi]: keep the copies needed
   auto one_key = [&]() {
@@ -1913,204 +1855,141 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     collapsed = true;
   };
   int rounds = 0;
-  auto decide = [&](const uint32_t (&tc)[3], const uint32_t (&tz)[3], const uint32_t (&tn)[3],
-                    const unsigned long long (&tm)[3]) {
-    bool reach[3], stop[3];
-    unsigned long long above[3], below[3], wz[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      above[j] = MASS ? tm[j] : static_cast<unsigned long long>(tc[j]);
-      wz[j] = MASS ? weight_fx(key2f(tz[j]), c.m, c.m_neginf, scale) : 1ull;
-      below[j] = above[j] - static_cast<unsigned long long>(tn[j]) * wz[j];
-      reach[j] = j < np && above[j] >= target;
-      stop[j] = reach[j] && below[j] < target;
-    }
-    // the first pivot (in increasing order) whose z_mn is the boundary
-    done_j = -1;
-    if (stop[0]) done_j = 0;
-    else if (reach[0] && stop[1]) done_j = 1;
-    else if (reach[0] && reach[1] && stop[2]) done_j = 2;
-    lo_j = hi_j = -1;
-    if (done_j >= 0) {
-      const uint32_t z = done_j == 0 ? tz[0] : (done_j == 1 ? tz[1] : tz[2]);
-      const uint32_t n = done_j == 0 ? tn[0] : (done_j == 1 ? tn[1] : tn[2]);
-      tau = z;
-      cabove = (done_j == 0 ? tc[0] : (done_j == 1 ? tc[1] : tc[2])) - n;
-      if (MASS) {
-        const unsigned long long w = done_j == 0 ? wz[0] : (done_j == 1 ? wz[1] : wz[2]);
-        const unsigned long long b = done_j == 0 ? below[0] : (done_j == 1 ? below[1] : below[2]);
-        n_keep = copies_fx(target - b, w, n);
-      } else {
-        n_keep = static_cast<uint32_t>(target) - cabove;
-      }
-      done = 1;
-      return;
-    }
-    // the highest pivot that reaches the target becomes lo, the lowest that
-    // does not becomes hi
-    lo_j = !reach[0] ? -1 : (!reach[1] || np < 2 ? 0 : (!reach[2] || np < 3 ? 1 : 2));
-    hi_j = !reach[0] ? 0 : (np < 2 ? -1 : (!reach[1] ? 1 : (np < 3 ? -1 : (!reach[2] ? 2 : -1))));
-    const uint32_t old_span = hi - lo;
-    if (lo_j >= 0) {
-      lo = lo_j == 0 ? q[0] : (lo_j == 1 ? q[1] : q[2]);
-      c_lo = lo_j == 0 ? tc[0] : (lo_j == 1 ? tc[1] : tc[2]);
-      m_lo = lo_j == 0 ? above[0] : (lo_j == 1 ? above[1] : above[2]);
-    }
-    if (hi_j >= 0) {
-      hi = hi_j == 0 ? q[0] : (hi_j == 1 ? q[1] : q[2]);
-      c_hi = hi_j == 0 ? tc[0] : (hi_j == 1 ? tc[1] : tc[2]);
-      m_hi = hi_j == 0 ? above[0] : (hi_j == 1 ? above[1] : above[2]);
-    }
-    if (hi - lo <= 1u) {
-      one_key();
-      return;
-    }
-    if (rounds >= kMaxRounds) {
-      done = 2;
-      return;
-    }
-    // after a value-space split that failed to halve the key range, the next
-    // round splits the key range
-    const bool vmode = value_pivots && !(used_value && (hi - lo) > old_span / 2u);
-    // interpolated pivots again only after a round that cut the key range at
-    // least fourfold (else plain quartiles guarantee progress)
-    const bool good = (hi - lo) <= old_span / 4u;
-    if (model && (good || !interp) && hi - lo > 4u &&
-        count_interp_pivots(lo, hi, c_lo, c_hi, static_cast<uint32_t>(target), q)) {
-      np = 3;
-      interp = true;
-      used_value = true;
-    } else {
-      np = quartile_pivots(lo, hi, vmode, q[0], q[1], q[2], used_value);
-      interp = false;
-    }
-  };
-  if (np == 0) one_key();
+  bool vmode = value_pivots;
+  if (hi - lo <= 1u) one_key();
+  RoundBin* pub = reinterpret_cast<RoundBin*>(reinterpret_cast<unsigned char*>(const_cast<uint4*>(c.ring_ptr)) +
+                                              kRoundPubOff);
   // rounds over the own lists while the range is large
   while (done == 0 && c_lo - c_hi > static_cast<uint32_t>(kTail)) {
-    float qf[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) qf[j] = j < np ? pivot_f(q[j]) : INFINITY;
-    uint32_t cnt[3] = {0u, 0u, 0u}, zk[3] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu}, nz[3] = {0u, 0u, 0u};
-    unsigned long long ms[3] = {0ull, 0ull, 0ull};
+    if (rounds >= kMaxRounds) {
+      done = 2;
+      break;
+    }
+    const float lo_f = pivot_f(lo), hi_f = pivot_f(hi);
+    const float inv = static_cast<float>(kSplit) / (hi_f - lo_f);
+    const bool val = vmode && isfinite(lo_f) && isfinite(hi_f) && hi_f > lo_f && isfinite(inv) && inv > 0.f;
+    const uint32_t span = hi - lo;
+    // bin of a key in (lo, hi]: monotone in the key
+    auto bin_of_key = [&](uint32_t k) -> int {
+      if (val) {
+        const int b = static_cast<int>((key2f(k) - lo_f) * inv);
+        return b < 0 ? 0 : (b > kSplit - 1 ? kSplit - 1 : b);
+      }
+      return static_cast<int>((static_cast<uint64_t>(k - lo - 1u) * kSplit) / span);
+    };
+    if (tid < kSplit) {
+      F.tbin_c[tid] = 0u;
+      F.tbin_m[tid] = 0ull;
+    }
+    __syncthreads();
     // only the range (lo, hi] is scanned: what lies above hi is counted in
     // c_hi / m_hi (and per rank in F.rank_hi) already
     own_for(c, [&](float x, uint32_t) {
       const uint32_t key = f2key(x);
       if (key <= lo || key > hi) return;
-      const unsigned long long wf = MASS ? weight_fx(x, c.m, c.m_neginf, scale) : 0ull;
-#pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        const bool g = x > qf[j];
-        cnt[j] += g ? 1u : 0u;
-        if (MASS) ms[j] += g ? wf : 0ull;
-        const bool lt = g && key < zk[j];
-        nz[j] = lt ? 1u : nz[j] + ((g && key == zk[j]) ? 1u : 0u);
-        zk[j] = lt ? key : zk[j];
-      }
+      const int b = bin_of_key(key);
+      atomicAdd(&F.tbin_c[b], 1u);
+      if (MASS) add_u64_halves(&F.tbin_m[b], weight_fx(x, c.m, c.m_neginf, scale));
     });
-    LPart(&buf)[kWarps][3] = F.lred[rounds & 1];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      const uint32_t cw = __reduce_add_sync(kFull, cnt[j]);
-      const uint32_t zw = __reduce_min_sync(kFull, zk[j]);
-      const uint32_t nw = __reduce_add_sync(kFull, zk[j] == zw ? nz[j] : 0u);
-      const unsigned long long mw = MASS ? warp_sum_u64_redux(ms[j]) : 0ull;
-      if (lane == 0) {
-        buf[warp][j].cnt = cw;
-        buf[warp][j].zmin = zw;
-        buf[warp][j].nz = nw;
-        buf[warp][j].mass = mw;
-      }
-    }
     __syncthreads();
     QRITA_T(8);
-    Slot& my = F.slots[c.ph & 1];
+    RoundBin* my = pub + (rounds & 1) * kSplit;
     if (warp == 0) {
-      // this CTA's totals over its warps, published for the cluster
+      // this CTA's bins, with the count above each, for the cluster (lane l:
+      // bins 2l, 2l + 1)
+      const uint32_t n0 = vld(F.tbin_c[2 * lane]), n1 = vld(F.tbin_c[2 * lane + 1]);
+      uint32_t incl = n0 + n1;  // bins 2l .. 63 after the scan
 #pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        const bool own = lane < kWarps;
-        const volatile LPart& pp = buf[own ? lane : 0][j];
-        const uint32_t cw = own ? pp.cnt : 0u;
-        const uint32_t zw = own ? pp.zmin : 0xFFFFFFFFu;
-        const uint32_t nw = own ? pp.nz : 0u;
-        const unsigned long long mw = (MASS && own) ? pp.mass : 0ull;
-        const uint32_t lc = __reduce_add_sync(kFull, cw);
-        const uint32_t lz = __reduce_min_sync(kFull, zw);
-        const uint32_t ln = __reduce_add_sync(kFull, zw == lz ? nw : 0u);
-        const unsigned long long lm = MASS ? warp_sum_u64_redux(mw) : 0ull;
-        if (lane == 0) {
-          my.cnt[j] = lc;
-          my.cnt[3 + j] = lz;
-          my.cnt[6 + j] = ln;
-          my.mass[j] = lm;
-        }
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(kFull, incl, o);
+        if (lane + o < 32) incl += y;
       }
+      const uint32_t above1 = incl - n0 - n1;
+      my[2 * lane] = RoundBin{n0, above1 + n1, MASS ? vld(F.tbin_m[2 * lane]) : 0ull};
+      my[2 * lane + 1] = RoundBin{n1, above1, MASS ? vld(F.tbin_m[2 * lane + 1]) : 0ull};
     }
     cluster_sync_all();
     QRITA_T(9);
+    if (tid < kSplit) {
+      // the row's bin tid
+      uint32_t rc = 0;
+      unsigned long long rm = 0ull;
+      for (int r = 0; r < C; ++r) {
+        const uint32_t ab = map_rank(smem_u32(&my[tid]), static_cast<uint32_t>(r));
+        rc += ld_dsmem_u32(ab);
+        if (MASS)
+          rm += static_cast<unsigned long long>(ld_dsmem_u32(ab + 8u)) |
+                (static_cast<unsigned long long>(ld_dsmem_u32(ab + 12u)) << 32);
+      }
+      F.tbin_c[tid] = rc;
+      F.tbin_m[tid] = rm;
+    }
+    __syncthreads();
     if (warp == 0) {
-      // lane r reads rank r's totals; the row's totals and per-rank shares
+      // lane l holds bins 63 - 2l and 62 - 2l; prefix sums from the top find
+      // the first bin whose cumulative total reaches the target
+      const int b0 = kSplit - 1 - 2 * lane, b1 = b0 - 1;
+      const uint32_t n0 = vld(F.tbin_c[b0]), n1 = vld(F.tbin_c[b1]);
+      const unsigned long long v0w = MASS ? vld(F.tbin_m[b0]) : static_cast<unsigned long long>(n0);
+      const unsigned long long v1w = MASS ? vld(F.tbin_m[b1]) : static_cast<unsigned long long>(n1);
+      unsigned long long inc = v0w + v1w;
+      uint32_t inc_n = n0 + n1;
 #pragma unroll
-      for (int j = 0; j < 3; ++j) {
-        uint32_t rc = 0, rz = 0xFFFFFFFFu, rn = 0;
-        unsigned long long rm = 0ull;
-        if (lane < C) {
-          const uint32_t cb = map_rank(smem_u32(&my.cnt[0]), static_cast<uint32_t>(lane));
-          rc = ld_dsmem_u32(cb + 4u * j);
-          rz = ld_dsmem_u32(cb + 4u * (3 + j));
-          rn = ld_dsmem_u32(cb + 4u * (6 + j));
-          if (MASS) {
-            const uint32_t mb = map_rank(smem_u32(&my.mass[j]), static_cast<uint32_t>(lane));
-            rm = static_cast<unsigned long long>(ld_dsmem_u32(mb)) |
-                 (static_cast<unsigned long long>(ld_dsmem_u32(mb + 4)) << 32);
-          }
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, inc, o);
+        const uint32_t yn = __shfl_up_sync(kFull, inc_n, o);
+        if (lane >= o) {
+          inc += y;
+          inc_n += yn;
         }
-        const uint32_t gz = __reduce_min_sync(kFull, rz);
-        const uint32_t gc = __reduce_add_sync(kFull, rc);
-        const uint32_t gn = __reduce_add_sync(kFull, rz == gz ? rn : 0u);
-        const unsigned long long gm = MASS ? warp_sum_u64_redux(rm) : 0ull;
-        if (lane < C) {
-          F.pr_cnt[lane][j] = rc + vld(F.rank_hi[lane]);  // the rank's list count above the pivot
-          F.pr_nz[lane][j] = rz == gz ? rn : 0u;
-        }
-        if (lane == 0) {
-          F.dtot[0][j] = gc;
-          F.dtot[1][j] = gz;
-          F.dtot[2][j] = gn;
-          F.dmass[j] = gm;
-        }
+      }
+      const unsigned long long top = MASS ? m_hi : static_cast<unsigned long long>(c_hi);
+      const unsigned long long ex = top + inc - (v0w + v1w);
+      const uint32_t ex_n = c_hi + inc_n - (n0 + n1);
+      const bool r0 = ex + v0w >= target, r1 = ex + v0w + v1w >= target;
+      const uint32_t hit = __ballot_sync(kFull, r1);
+      // (lo, hi] holds the boundary, so some bin reaches the target
+      const int L = hit != 0u ? __ffs(hit) - 1 : 31;
+      if (lane == L) {
+        const bool first = r0;  // (no lane reached: lane 31 takes bin 0)
+        const int bs = first ? b0 : b1;
+        const uint32_t an = first ? ex_n : ex_n + n0;
+        const unsigned long long am = first ? ex : ex + v0w;
+        F.bc.u[BU_NP] = static_cast<uint32_t>(bs);
+        F.bc.u[BU_CHI] = an;
+        F.bc.u[BU_CLO] = an + (first ? n0 : n1);
+        F.bc.x[BX_MHI] = MASS ? am : 0ull;
+        F.bc.x[BX_MLO] = MASS ? am + (first ? v0w : v1w) : 0ull;
       }
     }
     __syncthreads();
-    ++c.ph;
-    ++rounds;
-    uint32_t tc[3], tz[3], tn[3];
-    unsigned long long tm[3];
-#pragma unroll
-    for (int j = 0; j < 3; ++j) {
-      tc[j] = vld(F.dtot[0][j]) + c_hi;  // row counts above the pivots
-      tz[j] = vld(F.dtot[1][j]);
-      tn[j] = vld(F.dtot[2][j]);
-      tm[j] = MASS ? vld(F.dmass[j]) + m_hi : 0ull;
-    }
-    decide(tc, tz, tn, tm);
-    // per-rank bookkeeping of the decision (identical in every thread)
+    const int bs = static_cast<int>(vld(F.bc.u[BU_NP]));
     if (tid < C) {
-      if (done_j >= 0) {
-        F.ties[tid] = vld(F.pr_nz[tid][done_j]);
-      } else {
-        if (lo_j >= 0) F.rank_lo[tid] = vld(F.pr_cnt[tid][lo_j]);
-        if (hi_j >= 0) F.rank_hi[tid] = vld(F.pr_cnt[tid][hi_j]);
-        if (collapsed) F.ties[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
-      }
+      // rank tid's list counts above the new hi and lo
+      const uint32_t ab = map_rank(smem_u32(&my[bs]), static_cast<uint32_t>(tid));
+      const uint32_t in_bin = ld_dsmem_u32(ab), above = ld_dsmem_u32(ab + 4u);
+      const uint32_t nh = vld(F.rank_hi[tid]) + above;
+      F.rank_hi[tid] = nh;
+      F.rank_lo[tid] = nh + in_bin;
     }
-    __syncthreads();
+    const uint32_t old_n = c_lo - c_hi;
+    c_hi = vld(F.bc.u[BU_CHI]);
+    c_lo = vld(F.bc.u[BU_CLO]);
+    m_hi = vld(F.bc.x[BX_MHI]);
+    m_lo = vld(F.bc.x[BX_MLO]);
+    const uint32_t nlo = bs == 0 ? lo : last_key_in_bins(lo + 1u, hi, bs - 1, bin_of_key);
+    const uint32_t nhi = bs == kSplit - 1 ? hi : last_key_in_bins(lo + 1u, hi, bs, bin_of_key);
+    lo = nlo;
+    hi = nhi;
+    ++rounds;
+    // a value split that kept more than half of the range: key ranges next
+    if (val && c_lo - c_hi > old_n / 2u) vmode = false;
+    __syncthreads();  // F.rank_* and the broadcast read before the next round
+    if (hi - lo <= 1u) one_key();
     QRITA_T(10);
   }
-  if (done == 1 && collapsed && rounds == 0) {
-    // the start range held one key
+  if (done == 1 && collapsed) {
+    // the range held one key: every copy of it is the boundary's
     if (tid < C) F.ties[tid] = vld(F.rank_lo[tid]) - vld(F.rank_hi[tid]);
     __syncthreads();
   }
@@ -2368,8 +2247,10 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
 }
 
 // The index below which exactly `keep` of this CTA's own-list entries equal
-// to tau lie (the own list holds every such element of the chunk). 16-way
-// splits of the index range; invariant count(idx < lo) < keep <= count(idx < hi).
+// to tau lie (the own list holds every such element of the chunk). A small
+// group ranks its indices directly; a large one takes 16-way splits of the
+// index range, invariant count(idx < lo) < keep <= count(idx < hi).
+constexpr uint32_t kTieDirect = 512;
 template <int DT>
 __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
   Fixed& F = *c.F;
@@ -2389,6 +2270,21 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
   });
   __syncthreads();
   const uint32_t nt = vld(F.tail_n);
+  if (nt <= kTieDirect) {
+    // a small group: the keep-th smallest index, by each index's rank
+    if (tid == 0) F.bc.u[BU_QKEY] = static_cast<uint32_t>(c.n);
+    __syncthreads();
+    for (uint32_t i = tid; i < nt; i += kThreads) {
+      const uint32_t v = tix[i];
+      uint32_t below = 0;
+      for (uint32_t j = 0; j < nt; ++j) below += tix[j] < v ? 1u : 0u;
+      if (below + 1u == keep) F.bc.u[BU_QKEY] = v + 1u;
+    }
+    __syncthreads();
+    const uint32_t cut = vld(F.bc.u[BU_QKEY]);
+    __syncthreads();
+    return cut;
+  }
   const bool compact = nt <= kTieCap;
   uint32_t lo = 0, hi = static_cast<uint32_t>(c.n);
   for (int round = 0; round < 32 && hi - lo > 1u; ++round) {
@@ -3053,9 +2949,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       const bool hit = trunc && !overflow && !force_fb && !force_retry && survivors >= target;
       if (hit) path |= QRITA_PATH_HIT;
       Local s;
-      s.model_mu = mu;
-      s.model_sigma = (sigma > 0.f && isfinite(sigma) && isfinite(mu)) ? sigma : 0.f;
-      s.model_V = V;
       s.c_above = 0;
       s.m_above = 0ull;
       s.m_lo = s.m_hi = 0ull;
@@ -3270,9 +3163,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         } else {
           rank_counts_from<DT>(c, F.rank_n);
           Local s;
-          s.model_mu = 0.f;
-          s.model_sigma = 0.f;
-          s.model_V = V;
           s.lo = tau_k;
           s.c_lo = above_k;
           s.m_lo = M_gt;
@@ -3302,9 +3192,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                          f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
         if (!k_on) path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
         Local s;
-        s.model_mu = 0.f;
-        s.model_sigma = 0.f;
-        s.model_V = V;
         s.c_above = 0;
         s.m_above = 0ull;
         bool have_exact = false;
