@@ -103,6 +103,9 @@ enum {
 #define QRITA_PATH_RETRY 0x80u    /* top-k: a second truncation at an order statistic
                                      of a 4096-logit sample ran (the search ran on
                                      its survivors unless FALLBACK is also set) */
+#define QRITA_PATH_SAMPLE_T 0x200u /* top-k: the sample contradicted the Gaussian
+                                     threshold; an order statistic of the sample
+                                     was the threshold */
 #define QRITA_PATH_HIST 0x100u    /* top-p alone: value bins counted by the streaming
                                      pass placed the boundary, and one more pass
                                      extracted those bins for the search */

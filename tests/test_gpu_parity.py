@@ -247,10 +247,10 @@ def test_first_pass_bins_place_flat_top_p_rows(dev):
         assert (info["passes"][hist] == 1).all()
 
 
-def test_second_truncation_rescues_uniform_rows(dev):
-    """Uniform rows defeat the Gaussian threshold (it lies above their max);
-    the second truncation at a sample order statistic finds the candidates
-    without a full-row search."""
+def test_sample_threshold_rescues_uniform_rows(dev):
+    """Uniform rows defeat the Gaussian threshold (it lies above their max):
+    the sample contradicts it, and an order statistic of the sample becomes
+    the threshold, so the first pass keeps the candidates."""
     import top_selection_row_gb300 as q
 
     w = WORKLOADS[4]
@@ -259,6 +259,24 @@ def test_second_truncation_rescues_uniform_rows(dev):
     uniform = np.abs(x).max(axis=1) <= 1.0
     assert uniform.any()
     fails, flagged, got, st, info = check_against_oracle(logits, w.dtype, k, p, dev)
+    assert fails == [], fails[:5]
+    path = info["path"][uniform]
+    assert ((path & q.PATH_SAMPLE_T) != 0).mean() >= 0.75
+    assert ((path & (q.PATH_FALLBACK | q.PATH_RETRY)) == 0).mean() >= 0.75
+
+
+def test_second_truncation_rescues_uniform_rows(dev):
+    """With the first threshold forced to miss, the second truncation at an
+    order statistic of a larger sample finds the uniform rows' candidates
+    without a full-row search."""
+    import top_selection_row_gb300 as q
+
+    w = WORKLOADS[4]
+    logits, k, p = workload(4, 64)
+    x = widen(logits, w.dtype)
+    uniform = np.abs(x).max(axis=1) <= 1.0
+    assert uniform.any()
+    fails, flagged, got, st, info = check_against_oracle(logits, w.dtype, k, p, dev, flags=q.FLAG_FORCE_RETRY)
     assert fails == [], fails[:5]
     path = info["path"][uniform]
     assert ((path & q.PATH_RETRY) != 0).all()

@@ -36,6 +36,7 @@ def flag_cluster(n_ctas: int) -> int:
 PATH_TOPK, PATH_TOPP, PATH_TRUNC, PATH_HIT = 0x1, 0x2, 0x4, 0x8
 PATH_FALLBACK, PATH_OVERFLOW, PATH_KEEP_ALL, PATH_RETRY = 0x10, 0x20, 0x40, 0x80
 PATH_HIST = 0x100
+PATH_SAMPLE_T = 0x200
 
 # Layout of qrita_row_info_t (64 bytes).
 ROW_INFO_DTYPE = np.dtype(

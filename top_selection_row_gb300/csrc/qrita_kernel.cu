@@ -189,7 +189,7 @@ struct alignas(16) Bcast {  // written by one thread / warp 0 before a block bar
   unsigned long long x[8];  // fixed-point masses (narrowing)
   float pr[16];             // float pairs: pair i is (pr[2i], pr[2i+1])
   float f[12];
-  uint32_t u[24];
+  uint32_t u[28];
   uint32_t q[16];  // pivot keys, increasing
   float qf[16];    // pivot floats (+inf padding)
 };
@@ -250,7 +250,7 @@ enum : int {
   // uints
   BU_TRUNC = 0, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
   BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS, BU_S2, BU_OVF2,
-  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW,
+  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW, BU_SAMPLE_T,
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
   // float pairs
@@ -1571,33 +1571,22 @@ __device__ __forceinline__ int64_t sample_pos(int sidx, int n, int V) {
   return static_cast<int64_t>(sidx / 64) * (V / blocks) + (sidx % 64);
 }
 
-// Key of the j-th largest (1-based) of the kRetrySample sample logits of the
-// row (of the whole row when V <= kRetrySample), by an MSB-first radix select
-// with 8-bit digits; the histogram lives in the ring's bytes (no stream is in
-// flight). Every thread returns the same key.
-template <int DT>
-__device__ uint32_t sample_order_key(Ctx<DT>& c, const unsigned char* grow, int V, uint32_t j) {
-  constexpr int S = Ctx<DT>::S;
+// The key of the j-th largest (j >= 1) of the keys the threads hold (have[q]
+// marks the valid ones), by an MSB-first radix select with 8-bit digits over
+// a 256-bin histogram in shared memory. Every thread returns the same key.
+template <int DT, int N>
+__device__ uint32_t radix_select(Ctx<DT>& c, const uint32_t (&key)[N], const bool (&have)[N], uint32_t j,
+                                 uint32_t* hist) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr));  // 256 bins
-  uint32_t key[kRetryPer];
-  bool have[kRetryPer];
-#pragma unroll
-  for (int q = 0; q < kRetryPer; ++q) {
-    const int sidx = tid + q * kThreads;
-    const int64_t pos = sample_pos(sidx, kRetrySample, V);
-    have[q] = pos < V;
-    key[q] = have[q] ? f2key(load_elem<DT>(grow + static_cast<size_t>(pos) * S)) : 0u;
-  }
   uint32_t prefix = 0, mask = 0, want = j;
-  __syncthreads();  // earlier users of the ring's bytes are done
+  __syncthreads();  // earlier users of the histogram's bytes are done
   for (int d = 3; d >= 0; --d) {
     hist[tid] = 0u;  // kThreads == 256 bins
     __syncthreads();
     const int sh = 8 * d;
 #pragma unroll
-    for (int q = 0; q < kRetryPer; ++q)
+    for (int q = 0; q < N; ++q)
       if (have[q] && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> sh) & 255u], 1u);
     __syncthreads();
     if (tid < 32) {
@@ -1638,6 +1627,25 @@ __device__ uint32_t sample_order_key(Ctx<DT>& c, const unsigned char* grow, int 
     __syncthreads();
   }
   return prefix;
+}
+
+// The key of the j-th largest logit of a kRetrySample-logit sample of the
+// row (of the whole row when V <= kRetrySample); the histogram lives in the
+// ring's bytes (no stream is in flight).
+template <int DT>
+__device__ uint32_t sample_order_key(Ctx<DT>& c, const unsigned char* grow, int V, uint32_t j) {
+  constexpr int S = Ctx<DT>::S;
+  const int tid = threadIdx.x;
+  uint32_t key[kRetryPer];
+  bool have[kRetryPer];
+#pragma unroll
+  for (int q = 0; q < kRetryPer; ++q) {
+    const int sidx = tid + q * kThreads;
+    const int64_t pos = sample_pos(sidx, kRetrySample, V);
+    have[q] = pos < V;
+    key[q] = have[q] ? f2key(load_elem<DT>(grow + static_cast<size_t>(pos) * S)) : 0u;
+  }
+  return radix_select<DT, kRetryPer>(c, key, have, j, reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr)));
 }
 
 // Survivors (x >= t2) of the chunk into the warps' segments of the own list,
@@ -2583,8 +2591,45 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       }
       F.bc.f[BF_T] = trunc ? t : -INFINITY;
       F.bc.u[BU_TRUNC] = trunc ? 1u : 0u;
+      F.bc.u[BU_SAMPLE_T] = 0u;
     }
     __syncthreads();
+    // A top-k threshold the sample contradicts (a quarter or less of the
+    // sample values expected above the k-th logit lie above it, as on rows
+    // bounded below the Gaussian tail): an order statistic of the sample with
+    // a margin is the threshold instead, when its expected survivors fit.
+    if (k_on && vld(F.bc.u[BU_TRUNC]) != 0u &&
+        (P.flags & (QRITA_FLAG_FORCE_FALLBACK | QRITA_FLAG_FORCE_RETRY)) == 0u) {
+      const float tt = vld(F.bc.f[BF_T]);
+      int n_ge = 0, n_f = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        n_ge += __syncthreads_count(sv[j] >= tt);
+        n_f += __syncthreads_count(!isnan(sv[j]));
+      }
+      const float lam = static_cast<float>(kr) * static_cast<float>(n_f) / static_cast<float>(V);
+      const int jq = static_cast<int>(ceilf(lam + 3.0f * sqrtf(lam) + 3.0f));
+      const float expect = static_cast<float>(jq) * static_cast<float>(V) / static_cast<float>(n_f > 0 ? n_f : 1);
+      if (n_f >= 256 && lam >= 2.0f && 4.0f * static_cast<float>(n_ge) < lam && jq <= n_f &&
+          expect <= 0.85f * static_cast<float>(P.ocap) * static_cast<float>(P.C)) {
+        // the jq-th largest sample value (histogram in the list region, free
+        // here: the ring's first copies are in flight)
+        uint32_t key[kPer];
+        bool have[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+          have[j] = !isnan(sv[j]);
+          key[j] = have[j] ? f2key(sv[j]) : 0u;
+        }
+        const uint32_t kq = radix_select<DT, kPer>(c, key, have, static_cast<uint32_t>(jq),
+                                                   reinterpret_cast<uint32_t*>(c.lists));
+        if (tid == 0) {
+          F.bc.f[BF_T] = key2f(kq);
+          F.bc.u[BU_SAMPLE_T] = 1u;
+        }
+        __syncthreads();
+      }
+    }
   }
   const float mu = vld(F.bc.f[BF_MU]);
   const float sigma = vld(F.bc.f[BF_SIGMA]);
@@ -2918,7 +2963,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
 
   uint32_t path = (k_on ? QRITA_PATH_TOPK : 0u) | (p_on ? QRITA_PATH_TOPP : 0u) |
                   (trunc ? QRITA_PATH_TRUNC : 0u) | (overflow ? QRITA_PATH_OVERFLOW : 0u) |
-                  (keep_all ? QRITA_PATH_KEEP_ALL : 0u);
+                  (keep_all ? QRITA_PATH_KEEP_ALL : 0u) |
+                  (vld(F.bc.u[BU_SAMPLE_T]) != 0u ? QRITA_PATH_SAMPLE_T : 0u);
   const bool force_fb = (P.flags & QRITA_FLAG_FORCE_FALLBACK) != 0u;
   const bool force_retry = (P.flags & QRITA_FLAG_FORCE_RETRY) != 0u;
 
