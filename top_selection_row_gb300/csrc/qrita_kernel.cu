@@ -2723,12 +2723,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
             float xs[kPieceThreadUnits][E];
             uint32_t bits[kPieceThreadUnits];
+            float zu = 0.f, mu_ = 0.f;  // this piece's softmax partials (shift m_ref)
 #pragma unroll
             for (int j = 0; j < kPieceThreadUnits; ++j) {
               unpack<DT>(v[j], xs[j]);
               bits[j] = 0u;
               if (j * kThreads + tid < n) {
-                float zu = 0.f, mu_ = 0.f;  // this unit's softmax partials (shift m_ref)
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                   const float x = xs[j][e];
@@ -2745,11 +2745,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                     }
                   }
                 }
-                if constexpr (PO) {
-                  f2_add(zs, zu);
-                  f2_add(ms, mu_);
-                }
               }
+            }
+            if constexpr (PO) {
+              f2_add(zs, zu);
+              f2_add(ms, mu_);
             }
             if constexpr (COL) {
 #pragma unroll
