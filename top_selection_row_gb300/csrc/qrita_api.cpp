@@ -70,7 +70,7 @@ constexpr float kMarginP = 0.25f;
 
 constexpr int kCtasPerSm = 2;
 // Rows shorter than this per CTA are not split further.
-constexpr int64_t kMinChunk = 1024;
+constexpr int64_t kMinChunk = 3072;
 // Chunk indices must fit below the rank bits of a gathered tag.
 constexpr int64_t kMaxChunk = int64_t(1) << 27;
 
