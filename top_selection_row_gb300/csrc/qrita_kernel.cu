@@ -90,9 +90,16 @@ __device__ unsigned long long g_cta_stage[kTraceCtas][16];
   do {                                                                                          \
     if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_cta_stage[blockIdx.x][i] = globaltimer_ns(); \
   } while (0)
+#define QRITA_V(i, v)                                                                           \
+  do {                                                                                          \
+    if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_cta_stage[blockIdx.x][i] = (v);         \
+  } while (0)
 #else
 #define QRITA_T(i) \
   do {             \
+  } while (0)
+#define QRITA_V(i, v) \
+  do {                \
   } while (0)
 #endif
 
@@ -2255,10 +2262,11 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
 }
 
 // The index below which exactly `keep` of this CTA's own-list entries equal
-// to tau lie (the own list holds every such element of the chunk). A small
-// group ranks its indices directly; a large one takes 16-way splits of the
-// index range, invariant count(idx < lo) < keep <= count(idx < hi).
-constexpr uint32_t kTieDirect = 512;
+// to tau lie (the own list holds every such element of the chunk). A group
+// of at most kTieDirect radix-selects its keep-th smallest index; a larger
+// one takes 16-way splits of the index range, invariant count(idx < lo) <
+// keep <= count(idx < hi).
+constexpr uint32_t kTieDirect = 1024;
 template <int DT>
 __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
   Fixed& F = *c.F;
@@ -2267,31 +2275,40 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
   // flight); a group too large for them is scanned in the own list
   uint32_t* tix = reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr));
   constexpr uint32_t kTieCap = kRingBytes / 4;
+  static_assert(kTieDirect + kThreads <= kTieCap, "the index histogram fits after a small group");
   __syncthreads();  // earlier users of the ring's bytes are done
   if (tid == 0) F.tail_n = 0u;
   __syncthreads();
   own_for(c, [&](float x, uint32_t ix) {
-    if (x == tau_f) {
-      const uint32_t pos = atomicAdd(&F.tail_n, 1u);
+    const bool eq = x == tau_f;
+    // positions: one shared atomic per warp step
+    const uint32_t am = __activemask();
+    const uint32_t bal = __ballot_sync(am, eq);
+    const int leader = __ffs(bal) - 1;
+    uint32_t wbase = 0;
+    if (lane == leader) wbase = atomicAdd(&F.tail_n, static_cast<uint32_t>(__popc(bal)));
+    wbase = __shfl_sync(am, wbase, leader < 0 ? 0 : leader);
+    if (eq) {
+      const uint32_t pos = wbase + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
       if (pos < kTieCap) tix[pos] = ix;
     }
   });
   __syncthreads();
   const uint32_t nt = vld(F.tail_n);
   if (nt <= kTieDirect) {
-    // a small group: the keep-th smallest index, by each index's rank
-    if (tid == 0) F.bc.u[BU_QKEY] = static_cast<uint32_t>(c.n);
-    __syncthreads();
-    for (uint32_t i = tid; i < nt; i += kThreads) {
-      const uint32_t v = tix[i];
-      uint32_t below = 0;
-      for (uint32_t j = 0; j < nt; ++j) below += tix[j] < v ? 1u : 0u;
-      if (below + 1u == keep) F.bc.u[BU_QKEY] = v + 1u;
+    // a small group: the keep-th smallest index (the (nt + 1 - keep)-th
+    // largest) by a radix select over the indices, the histogram after them
+    constexpr int kPerT = kTieDirect / kThreads;
+    uint32_t key[kPerT];
+    bool have[kPerT];
+#pragma unroll
+    for (int q = 0; q < kPerT; ++q) {
+      const uint32_t i = static_cast<uint32_t>(tid + q * kThreads);
+      have[q] = i < nt;
+      key[q] = have[q] ? tix[i] : 0u;
     }
-    __syncthreads();
-    const uint32_t cut = vld(F.bc.u[BU_QKEY]);
-    __syncthreads();
-    return cut;
+    const uint32_t kth = radix_select<DT, kPerT>(c, key, have, nt + 1u - keep, tix + kTieDirect);
+    return kth + 1u;
   }
   const bool compact = nt <= kTieCap;
   uint32_t lo = 0, hi = static_cast<uint32_t>(c.n);
