@@ -2265,21 +2265,25 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
 // to tau lie (the own list holds every such element of the chunk). A group
 // of at most kTieDirect radix-selects its keep-th smallest index; a larger
 // one takes 16-way splits of the index range, invariant count(idx < lo) <
-// keep <= count(idx < hi).
+// keep <= count(idx < hi). mark_above: the scan over the own list also
+// writes the mask's 1 for every entry above tau (the mask is filled already);
+// the compacted group (F.tail_n indices in the ring's bytes, when they fit)
+// stays for the emission.
 constexpr uint32_t kTieDirect = 1024;
+constexpr uint32_t kTieCap = kRingBytes / 4;
 template <int DT>
-__device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep) {
+__device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep, bool mark_above) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the tie group's indices, compacted into the ring's bytes (no stream is in
   // flight); a group too large for them is scanned in the own list
   uint32_t* tix = reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr));
-  constexpr uint32_t kTieCap = kRingBytes / 4;
   static_assert(kTieDirect + kThreads <= kTieCap, "the index histogram fits after a small group");
   __syncthreads();  // earlier users of the ring's bytes are done
   if (tid == 0) F.tail_n = 0u;
   __syncthreads();
   own_for(c, [&](float x, uint32_t ix) {
+    if (mark_above && x > tau_f) c.gmask[ix] = 1;
     const bool eq = x == tau_f;
     // positions: one shared atomic per warp step
     const uint32_t am = __activemask();
@@ -3504,9 +3508,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   const uint32_t keep_local = (tie_mode == 2) ? (n_keep - my_first) : 0u;
   uint32_t idx_cut = 0;
   bool ordered_ties = false;
+  // the cut's scan over the own list also writes the kept entries above tau
+  // when the mask is filled already (the emission then writes only the ties)
+  const bool fused_ties = tie_mode == 2 && ties_in_list && list_emit && (zero_filled || ph_mask);
   if (tie_mode == 2) {
     if (ties_in_list) {
-      idx_cut = tie_index_cut<DT>(c, tau_f, keep_local);
+      idx_cut = tie_index_cut<DT>(c, tau_f, keep_local, fused_ties);
     } else {
       ordered_ties = true;
     }
@@ -3520,11 +3527,27 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     if (sel_all || sel_none || !(zero_filled || ph_mask)) fill_mask<DT>(c, sel_all ? 1 : 0);
     if (list_emit && !sel_all && !sel_none) {
       __syncthreads();  // the fill is ordered before the scatter
-      own_for(c, [&](float x, uint32_t ix) {
-        bool keep = x > tau_f;
-        if (x == tau_f) keep = (tie_mode == 1) || (tie_mode == 2 && ix < idx_cut);
-        if (keep) c.gmask[ix] = 1;
-      });
+      if (fused_ties) {
+        // the entries above tau are written: the ties below the cut remain
+        const uint32_t nt = vld(F.tail_n);
+        if (nt <= kTieCap) {
+          const uint32_t* tix = reinterpret_cast<const uint32_t*>(c.ring_ptr);
+          for (uint32_t i = tid; i < nt; i += kThreads) {
+            const uint32_t ix = tix[i];
+            if (ix < idx_cut) c.gmask[ix] = 1;
+          }
+        } else {
+          own_for(c, [&](float x, uint32_t ix) {
+            if (x == tau_f && ix < idx_cut) c.gmask[ix] = 1;
+          });
+        }
+      } else {
+        own_for(c, [&](float x, uint32_t ix) {
+          bool keep = x > tau_f;
+          if (x == tau_f) keep = (tie_mode == 1) || (tie_mode == 2 && ix < idx_cut);
+          if (keep) c.gmask[ix] = 1;
+        });
+      }
     }
   } else {
     // stream the chunk again: x > tau kept, ties by the rule above
