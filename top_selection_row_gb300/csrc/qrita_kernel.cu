@@ -2662,14 +2662,21 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   // bracket pivots for a top-k search over the survivors (identical in every
   // CTA of the row: they come from the shared sample); never below t, so the
   // own lists' counts above them are the row's
+  // (a threshold the sample chose: the pivots split [t, m_ref] evenly, the
+  // Gaussian model having failed for the row)
+  const bool sample_t = vld(F.bc.u[BU_SAMPLE_T]) != 0u;
   const bool bracket = trunc && k_on && !p_only && value_pivots && sigma > 0.f && isfinite(sigma) &&
-                       isfinite(mu) && (P.flags & QRITA_FLAG_FORCE_FALLBACK) == 0u;
+                       isfinite(mu) && isfinite(m_ref) && (P.flags & QRITA_FLAG_FORCE_FALLBACK) == 0u;
   if (bracket && tid < 16) {
     float q = INFINITY;
     if (tid < kBracket) {
-      const float mj = exp2f(static_cast<float>(7 - tid) * 0.2f);
-      const float u = fminf(mj * static_cast<float>(kr) / static_cast<float>(V), 0.5f);
-      q = fmaxf(mu - sigma * normcdfinvf(u), t);
+      if (sample_t) {
+        q = fmaxf(fmaf(static_cast<float>(tid + 1) * (1.0f / 16.0f), m_ref - t, t), t);
+      } else {
+        const float mj = exp2f(static_cast<float>(7 - tid) * 0.2f);
+        const float u = fminf(mj * static_cast<float>(kr) / static_cast<float>(V), 0.5f);
+        q = fmaxf(mu - sigma * normcdfinvf(u), t);
+      }
     }
     F.bp[tid] = q;  // published by the streaming pass's first block barrier
     F.bp_bins[tid] = 0u;
