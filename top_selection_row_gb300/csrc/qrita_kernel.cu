@@ -3297,7 +3297,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           const bool mass_hit = !k_on && trunc && !force_fb && ref_ok &&
                                 f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
           bool ph_done = false;
-          if (ph && mass_hit && (P.flags & QRITA_FLAG_HIST_MISS) == 0u) {
+          if (ph && mass_hit) {
             // the first pass's bins: row totals of bin tid (approximate mass,
             // shift m_ref) and of the survivors above m_ref
             const uint32_t* tc = reinterpret_cast<const uint32_t*>(c.lists + kPhTotOff);
@@ -3375,8 +3375,10 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               const uint32_t c_above = vld(F.bc.u[BU_CHI]);
               const unsigned long long m_above = vld(F.bc.x[BX_MHI]), m_in = vld(F.bc.x[BX_MLO]);
               const unsigned long long target = f2_to_u64(f2_mul(f2_mul(Zm, pr), scale));
-              // the exact masses confirm the bracket: search the lists
-              if (!ovf_in && m_above < target && target <= m_above + m_in) {
+              // the exact masses confirm the bracket: search the lists (a
+              // test flag treats the bracket as missed)
+              if (!ovf_in && m_above < target && target <= m_above + m_in &&
+                  (P.flags & QRITA_FLAG_HIST_MISS) == 0u) {
                 rank_counts_from<DT>(c, F.rank_n);
                 s.lo = lo_key;
                 s.hi = to_top ? f2key(row_max) : hi_key;
