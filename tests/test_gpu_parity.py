@@ -333,6 +333,25 @@ def test_host_entry_point_matches_device_path(dev):
     assert torch.equal(out, want.cpu())
 
 
+@pytest.mark.parametrize("n,rows", [(2, 64), (2, 13), (4, 3), (1, 4)])
+def test_host_entry_sizes_match_device_path(dev, n, rows):
+    """The host entry (copies in, selection, copy out) gives the device
+    path's masks for batches of several sizes and row counts, call after call."""
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    w = WORKLOADS[n]
+    logits, k, p = workload(n, rows)
+    xd = to_device(logits, w.dtype, dev)
+    want = q.qrita_select(xd, torch.from_numpy(k).to(dev), torch.from_numpy(p).to(dev))
+    torch.cuda.synchronize()
+    xh = xd.cpu().pin_memory()
+    for _ in range(2):
+        out = q.qrita_select_host(xh, torch.from_numpy(k), torch.from_numpy(p))
+        assert torch.equal(out, want.cpu())
+
+
 def test_runs_on_a_side_stream(dev):
     import torch
 
