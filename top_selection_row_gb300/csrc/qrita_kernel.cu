@@ -10,23 +10,24 @@
 //   A2  mu, sigma (and a reference max) from one sample block of the row,
 //       read identically by every CTA of the cluster (no exchange needed);
 //       sigma is re-estimated without the sample's outliers;
-//   A3  delta from the normal-quantile tables, t = mu + delta * sigma;
+//   A3  delta from the normal-quantile tables, t = mu + delta * sigma; a
+//       top-k threshold the sample contradicts becomes an order statistic of
+//       the sample; top-k rows get bracket pivots from the model;
 //   A4  one streaming pass over the chunk keeps Z_t = {x >= t} (value and
-//       index) in per-warp segments of a shared-memory list, and tracks
-//       max / min / NaN / +inf and, for top-p without top-k, the softmax mass
-//       of the row and of Z_t;
+//       index) in a shared-memory list, and tracks max / min / NaN / +inf
+//       and, for top-p without top-k, the softmax mass of the row and of Z_t
+//       (rows whose Z_t cannot fit the lists bin it by value instead);
 //   --  one cluster merge through distributed shared memory;
-//   A5  hit: the survivors stay in the CTAs' own lists; fallback (miss, or
-//       too many candidates): a second truncation at an order statistic of
-//       a larger sample (top-k), else distributed narrowing passes over the
-//       chunk (one 256-bin pass, then two quaternary levels per cluster
-//       merge) until the range that holds the boundary fits the own lists,
-//       from which it is extracted;
-//   A6  quaternary pivot search over the own lists of the cluster with
-//       z_mn / N_zmn duplicate tracking: every CTA counts its own list, the
-//       counts are merged through distributed shared memory each round, and
-//       the last few hundred candidates are copied to every CTA and tested
-//       directly;
+//   A5  hit: the survivors stay in the CTAs' own lists; else a second
+//       truncation at an order statistic of a larger sample (top-k), one
+//       pass that extracts the bins around the boundary (binned top-p rows),
+//       or distributed narrowing passes over the chunk (one 256-bin pass,
+//       then two quaternary levels per cluster merge) until the range that
+//       holds the boundary fits the own lists, from which it is extracted;
+//   A6  the pivot search over the own lists of the cluster (64 bins a round,
+//       merged through distributed shared memory), then the last candidates
+//       are copied to every CTA, split again locally, and tested directly
+//       (the z_mn / N_zmn test);
 //   A7  the same search by softmax mass for top-p;
 //   A8  boundary duplicates kept by lowest token id: per-rank counts from the
 //       search, then an index cut inside the one straddling CTA;
