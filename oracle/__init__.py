@@ -9,6 +9,7 @@ imports it and shares no code with it.
 from .qrita_oracle import (  # noqa: F401
     AMBIGUITY_REL,
     RowResult,
+    accepts,
     bf16_bits_to_f64,
     select_batch,
     select_row,

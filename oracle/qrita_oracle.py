@@ -29,8 +29,13 @@ name both filters but not their order, and this is the reading taken.
 A row holding NaN or +inf is invalid: its mask is all zero.
 
 Boundary-band flag: when top-p is active the row is flagged ambiguous if
-|c_{j*} - p| <= 1e-6 * p or |c_{j*-1} - p| <= 1e-6 * p; on such rows a GPU
-result one token shorter or longer than the oracle's prefix is accepted.
+|c_{j*} - p| <= 1e-6 * p or |c_{j*-1} - p| <= 1e-6 * p. On such rows any
+prefix of the stable order is accepted whose end the band cannot tell from
+the boundary: the count n with c_{n-1} >= p - 1e-6 p (it reaches p within
+the band) and c_{n-2} < p + 1e-6 p (one token fewer falls short within the
+band). On short rows that is the oracle's prefix or one token more or less;
+on rows of millions of logits, whose tokens each carry far less than 1e-6 of
+the mass, it can be several.
 
 Pins (tests/test_oracle_pins.py, tests/golden/): brute-force permutation
 enumeration on tiny rows with exact rational weights, hand-worked tie-heavy
@@ -63,6 +68,8 @@ class RowResult:
     n_boundary how many tokens equal to ``boundary`` are kept
     ambiguous  top-p boundary within the relative band of p
     alt_masks  masks of the neighbouring prefixes (only when ambiguous)
+    band_kept  (smallest, largest) accepted count of kept tokens
+    band_order the order of S_k (only when ambiguous), for accepts()
     """
 
     mask: np.ndarray
@@ -72,6 +79,8 @@ class RowResult:
     n_boundary: int
     ambiguous: bool
     alt_masks: tuple
+    band_kept: tuple = (0, 0)
+    band_order: np.ndarray | None = None
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
@@ -128,6 +137,7 @@ def select_row(x, k: int | None, p: float | None) -> RowResult:
     top_p = p is not None and not np.isnan(p) and p < 1.0
     ambiguous = False
     alts: tuple = ()
+    band_kept = None
     if not top_p:
         n_keep = s_k.shape[0]
     else:
@@ -151,12 +161,34 @@ def select_row(x, k: int | None, p: float | None) -> RowResult:
                 for n in (n_keep - 1, n_keep + 1)
                 if 1 <= n <= s_k.shape[0]
             )
+            # every count whose prefix end the band cannot tell apart
+            n_lo = _first_reaching(c, p - band) + 1
+            n_hi = _first_reaching(c, p + band) + 1
+            band_kept = (min(n_lo, n_keep - 1 if n_keep > 1 else 1), max(n_hi, n_keep + 1))
 
     mask = _mask_from_prefix(V, s_k, n_keep)
     boundary = float(x[s_k[n_keep - 1]])
     kept_vals = x[s_k[:n_keep]]
     n_boundary = int(np.count_nonzero(kept_vals == boundary))
-    return RowResult(mask, STATUS_OK, int(n_keep), boundary, n_boundary, ambiguous, alts)
+    if band_kept is None:
+        return RowResult(mask, STATUS_OK, int(n_keep), boundary, n_boundary, ambiguous, alts, (int(n_keep), int(n_keep)))
+    return RowResult(mask, STATUS_OK, int(n_keep), boundary, n_boundary, ambiguous, alts,
+                     (int(band_kept[0]), int(min(band_kept[1], s_k.shape[0]))), s_k)
+
+
+def accepts(res: RowResult, got: np.ndarray) -> bool:
+    """Whether a mask ``got`` (uint8 / bool [V]) is an accepted result for
+    the row: the definition's mask, or on a flagged row any prefix of the
+    stable order whose count lies in ``band_kept``."""
+    g = np.asarray(got).astype(np.uint8)
+    if np.array_equal(g, res.mask):
+        return True
+    if not res.ambiguous or res.band_order is None:
+        return False
+    n = int(g.sum())
+    if not (res.band_kept[0] <= n <= res.band_kept[1]):
+        return False
+    return np.array_equal(g, _mask_from_prefix(g.shape[0], res.band_order, n))
 
 
 def select_batch(logits: np.ndarray, dtype: str, k=None, p=None, rows=None):

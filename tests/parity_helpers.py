@@ -5,7 +5,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from oracle import select_batch
+from oracle import accepts, select_batch
 from oracle.qrita_oracle import STATUS_NONFINITE
 
 
@@ -50,8 +50,8 @@ def compare_rows(got_mask, got_status, oracle_rows):
             continue
         if res.ambiguous:
             flagged += 1
-            if not (np.array_equal(g, res.mask) or any(np.array_equal(g, a) for a in res.alt_masks)):
-                fails.append((r, "flagged row outside the band", int(g.sum()), res.kept))
+            if not accepts(res, g):
+                fails.append((r, "flagged row outside the band", int(g.sum()), res.kept, res.band_kept))
         elif not np.array_equal(g, res.mask):
             diff = np.nonzero(g != res.mask)[0]
             fails.append((r, "mismatch", int(g.sum()), res.kept, diff[:8].tolist()))

@@ -117,6 +117,28 @@ def _edge_batch(rng, V, B, dtype, kind):
     return x
 
 
+@pytest.mark.parametrize("dtype,V,kind", [("f32", 3_000_017, "normal"), ("bf16", (1 << 24) + 3, "normal"),
+                                          ("f32", 3_000_017, "flat")])
+def test_very_long_rows(dev, dtype, V, kind):
+    """Rows of millions of logits (up to 2^24 + 3): the launch spreads a row
+    over up to 16 CTAs; top-k small and large, top-p over flat and peaked
+    rows."""
+    rng = np.random.default_rng(V + (dtype == "bf16"))
+    x = rng.standard_normal((4, V)).astype(np.float32)
+    if kind == "flat":
+        x *= np.float32(0.3)
+    if dtype == "bf16":
+        from workloads import f32_to_bf16_bits
+
+        logits = f32_to_bf16_bits(x)
+    else:
+        logits = x
+    k = np.array([1, 5000, V, V], np.int32)
+    p = np.array([1.0, 0.9, 0.95, 0.5], np.float32)
+    fails, flagged, got, st, info = check_against_oracle(logits, dtype, k, p, dev)
+    assert fails == [], fails[:5]
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("V", [1, 2, 3, 5, 7, 15, 16, 17, 31, 33, 100, 1000, 4097, 40000])
 def test_edge_sizes_and_parameters(dev, dtype, V):

@@ -269,3 +269,33 @@ def _pin_failures(golden_rows):
 def test_planted_mistakes_are_caught(monkeypatch, golden_rows, name, attr, mutant):
     monkeypatch.setattr(O, attr, mutant)
     assert _pin_failures(golden_rows), f"mutant {name} slipped through every pin"
+
+
+def test_band_accepts_every_prefix_the_band_cannot_tell_apart():
+    """On a row of millions of equal logits each token carries 1/V of the
+    mass, so the 1e-6 relative band around p covers several prefix ends:
+    c_n = n / V exactly, and for p = 1/2 the band holds counts
+    V/2 - 3 .. V/2 + 3 (1e-6 * 0.5 * 6e6 = 3). Exactly those prefixes are
+    accepted; a longer or shorter one, or a non-prefix of an accepted count,
+    is not."""
+    from oracle import accepts, select_row
+
+    V = 6_000_000
+    res = select_row(np.zeros(V), None, 0.5)
+    half = V // 2
+    assert res.ambiguous and res.kept == half
+    assert res.band_kept == (half - 3, half + 3)
+
+    def prefix(n):
+        m = np.zeros(V, np.uint8)
+        m[:n] = 1
+        return m
+
+    for n in range(half - 3, half + 4):
+        assert accepts(res, prefix(n)), n
+    for n in (half - 4, half + 4):
+        assert not accepts(res, prefix(n)), n
+    bad = prefix(half + 1)
+    bad[half] = 0
+    bad[V - 1] = 1
+    assert not accepts(res, bad)
