@@ -3346,7 +3346,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             int bl = bstar - 1 < 0 ? 0 : bstar - 1;
             int bh = bstar + 1;  // >= kHistBins: the range reaches above ph_hi
             bool fits = __syncthreads_and(tid >= static_cast<int>(c.C) || rank_count(bl, bh) <= c.ocap) != 0;
-            if (!fits && bstar < kHistBins) {
+            if (!fits && bstar >= 0 && bstar < kHistBins) {
               // without the margin bins
               bl = bstar;
               bh = bstar;
