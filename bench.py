@@ -26,6 +26,7 @@ import math
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -128,7 +129,10 @@ class ClockSampler:
 
     def __enter__(self):
         try:
-            out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp"
+            # the raw samples go to QRITA_CLOCKS_DIR when set (kept for
+            # inspection), else to the temp directory
+            out_dir = os.environ.get("QRITA_CLOCKS_DIR") or tempfile.gettempdir()
+            os.makedirs(out_dir, exist_ok=True)
             self.path = os.path.join(out_dir, f"clocks_{os.getpid()}.csv")
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
