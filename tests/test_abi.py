@@ -100,3 +100,84 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(bind, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         bind.lib()
+
+
+def _header_probe(tmp_path):
+    """Compile a C program against include/qrita.h that prints the row-info
+    layout and every constant; returns {name: int}."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    fields = ["mu", "sigma", "threshold", "row_max", "survivors", "path", "rounds_k", "rounds_p", "boundary",
+              "n_boundary", "kept", "status", "z", "passes", "reserved"]
+    consts = ["QRITA_DTYPE_F32", "QRITA_DTYPE_BF16", "QRITA_OK", "QRITA_EINVAL", "QRITA_EUNSUPPORTED",
+              "QRITA_ECUDA", "QRITA_ROW_OK", "QRITA_ROW_NONFINITE", "QRITA_ROW_SEARCH_CAP", "QRITA_ROW_TIMEOUT",
+              "QRITA_FLAG_NO_TRUNCATION", "QRITA_FLAG_FORCE_FALLBACK", "QRITA_FLAG_KEY_PIVOTS",
+              "QRITA_FLAG_FORCE_RETRY", "QRITA_FLAG_HIST_MISS", "QRITA_FLAG_CLUSTER_SHIFT", "QRITA_FLAG_CLUSTER_SET",
+              "QRITA_PATH_TOPK", "QRITA_PATH_TOPP", "QRITA_PATH_TRUNC", "QRITA_PATH_HIT", "QRITA_PATH_FALLBACK",
+              "QRITA_PATH_OVERFLOW", "QRITA_PATH_KEEP_ALL", "QRITA_PATH_RETRY", "QRITA_PATH_HIST",
+              "QRITA_PATH_SAMPLE_T"]
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "qrita.h"', "int main(void) {",
+             '  printf("sizeof %zu\\n", sizeof(qrita_row_info_t));']
+    lines += [f'  printf("off_{f} %zu\\n", offsetof(qrita_row_info_t, {f}));' for f in fields]
+    lines += [f'  printf("size_{f} %zu\\n", sizeof(((qrita_row_info_t*)0)->{f}));' for f in fields]
+    lines += [f'  printf("{c} %lld\\n", (long long)({c}));' for c in consts]
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "probe"
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(root, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True, timeout=120)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True, timeout=60).stdout
+    return {k: int(v) for k, v in (ln.split() for ln in out.splitlines())}
+
+
+def test_row_info_layout_matches_the_header(tmp_path):
+    import top_selection_row_gb300 as q
+
+    h = _header_probe(tmp_path)
+    dt = q.ROW_INFO_DTYPE
+    assert h["sizeof"] == dt.itemsize == 64
+    assert list(dt.names) == [k[4:] for k in h if k.startswith("off_")]
+    for name in dt.names:
+        ftype, off = dt.fields[name][:2]
+        assert h[f"off_{name}"] == off, name
+        assert h[f"size_{name}"] == ftype.itemsize, name
+
+
+def test_binding_constants_match_the_header(tmp_path):
+    import top_selection_row_gb300 as q
+
+    h = _header_probe(tmp_path)
+    for name, v in h.items():
+        if not name.startswith("QRITA_") or name == "QRITA_FLAG_CLUSTER_SHIFT":
+            continue
+        attr = name[len("QRITA_"):]
+        assert getattr(q, attr) == v, name
+    assert q.flag_cluster(1) == h["QRITA_FLAG_CLUSTER_SET"]
+    assert q.flag_cluster(16) == h["QRITA_FLAG_CLUSTER_SET"] | (4 << h["QRITA_FLAG_CLUSTER_SHIFT"])
+
+
+def test_binding_rejects_bad_host_arguments_before_any_device_work():
+    torch = pytest.importorskip("torch")
+    import top_selection_row_gb300 as q
+
+    x = torch.zeros(3, 10)
+    with pytest.raises(ValueError):
+        q.qrita_select(x)  # device entry point: host tensors are refused
+    with pytest.raises(ValueError):
+        q.qrita_select_host(torch.zeros(10))  # not [B, V]
+    with pytest.raises(TypeError):
+        q.qrita_select_host(torch.zeros(3, 10, dtype=torch.float16))
+    with pytest.raises(ValueError):
+        q.qrita_select_host(torch.zeros(10, 3).t())  # not row-major
+    with pytest.raises(ValueError):
+        q.qrita_select_host(x, k=torch.ones(3, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        q.qrita_select_host(x, k=torch.ones(2, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        q.qrita_select_host(x, p=torch.ones(3, dtype=torch.float64))
