@@ -5,9 +5,13 @@
 
 One step is one call of the whole selection pipeline (sample statistics,
 sigma-truncation, quaternary top-k / top-p pivot search, tie resolution,
-mask emission) over one batch of the workload. The headline workload is
-64 x 128256 fp32 logits with per-row top-k (workload 2); the JSON line also
-carries every workload's own number under "per_workload".
+mask emission) over one batch of the workload. The headline workload is the
+largest one: 1024 x 262144 bf16 logits with mixed per-row top-k / top-p
+(workload 5); the JSON line also carries every workload's own number under
+"per_workload", with the count of rows each path of the kernel took (from
+the per-row diagnostics of one untimed call) and the oracle's count of
+flagged top-p rows (tests/golden/flagged_counts.json, written from the
+oracle alone by tests/golden/make_flagged_counts.py).
 
 Timing: W untimed steps, then exactly K steps bracketed by a barrier and a
 device synchronize, timed with CUDA events on the launching stream; inputs
@@ -38,7 +42,7 @@ if ROOT not in sys.path:
 from workloads import WORKLOADS, assumptions, generate  # noqa: E402
 
 METRIC = "logit rows/sec and HBM GB/s (% of GB300 peak) for exact top-k/top-p masking"
-HEADLINE = 2
+HEADLINE = 5
 KERNEL_SOURCES = [
     os.path.join(ROOT, "top_selection_row_gb300", "csrc", f)
     for f in ("qrita_kernel.cu", "qrita_device.cuh", "qrita_internal.h", "qrita_api.cpp")
@@ -178,6 +182,33 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sms)}
 
 
+def oracle_flagged_counts():
+    """Per-workload top-p rows and the oracle's flagged rows, as stored by
+    tests/golden/make_flagged_counts.py (None when the file is missing)."""
+    path = os.path.join(ROOT, "tests", "golden", "flagged_counts.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        return json.load(f).get("workloads")
+
+
+PATH_BITS = {
+    "top_k": 0x1, "top_p": 0x2, "truncated": 0x4, "hit": 0x8, "fallback": 0x10, "overflow": 0x20,
+    "keep_all": 0x40, "retry": 0x80, "hist": 0x100, "sample_threshold": 0x200,
+}
+
+
+def path_counts(info) -> dict:
+    """Rows per path bit of qrita_row_info_t.path, plus rows that searched
+    their truncation survivors (hit, retry or hist without the fallback)."""
+    path = info["path"].astype(np.int64)
+    out = {name: int(((path & bit) != 0).sum()) for name, bit in PATH_BITS.items()}
+    searched = (path & (0x8 | 0x80 | 0x100)) != 0
+    out["searched_survivors"] = int((searched & ((path & 0x10) == 0)).sum())
+    out["narrowing_passes_total"] = int(info["passes"].astype(np.int64).sum())
+    return out
+
+
 def workload_config(w, n_rot, l2_bytes):
     return {
         "workload": w.name,
@@ -269,8 +300,14 @@ def time_workload(number, steps, warmup, dev, world, l2_bytes, stream, rotate=No
     except Exception as e:  # capture is optional: report why it is missing
         print(f"bench: CUDA-graph timing skipped ({type(e).__name__}: {e})", file=sys.stderr)
         torch.cuda.synchronize(dev)
+    # one untimed call with the per-row diagnostics: rows per path
+    with torch.cuda.stream(stream):
+        _, _, info = q.qrita_select_ex(xs[0], k_arg, p_arg, out=outs[0], stream=stream, row_info=True)
+    torch.cuda.synchronize(dev)
+    paths = path_counts(q.decode_row_info(info))
     del xs, outs
     return {
+        "paths": paths,
         "w": w,
         "n_rot": n_rot,
         "ms_per_step": total_s * 1e3 / steps,
@@ -441,10 +478,13 @@ def run_ours(args):
         "clocks": head.get("clocks"),
         "per_workload": {},
     }
+    flagged = oracle_flagged_counts() or {}
     for n, r in per.items():
         ach = r["bytes_per_launch"] / (r["kernel_ms_mean"] / 1e3) / 1e9
         gms = r["graph_ms_per_step"]
         line["per_workload"][WORKLOADS[n].name] = {
+            "paths": r["paths"],
+            "oracle_flagged": flagged.get(WORKLOADS[n].name),
             "rows_per_s": r["rows_per_s"],
             "ms_per_step": r["ms_per_step"],
             "kernel_ms_isolated_median": r["kernel_ms_isolated_median"],

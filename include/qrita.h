@@ -26,10 +26,18 @@
  * or +inf gets an all-zero mask and a non-zero row status. At least one token
  * is kept in every valid row.
  *
- * Top-k masks are bit-exact. Top-p masks are bit-exact except where the
- * cumulative mass at the boundary lies within 1e-6 (relative) of p, where the
- * prefix may be one token shorter or longer (the kernel sums fp32 softmax
- * weights with compensated arithmetic; the definition is fp64).
+ * Top-k masks are bit-exact. Top-p masks are bit-exact except on rows whose
+ * cumulative mass at the boundary lies within 1e-6 * p of p. On such a row
+ * the kept set is still a prefix of the stable descending order of S_k, of
+ * n tokens, where n is the definition's count, one more or one fewer, or any
+ * count the band cannot tell from it: c(n) >= p - 1e-6 p and
+ * c(n - 1) < p + 1e-6 p, c(n) being the renormalised mass of the first n
+ * tokens. On short rows that is one token either way; on rows of millions of
+ * logits, where one token carries far less than 1e-6 of the mass, it can be
+ * several. Arithmetic: every softmax weight is fp32 exp(x - m) rounded to an
+ * unsigned 64-bit fixed-point integer, and all masses are exact integer sums
+ * of those weights (so every decision is deterministic and independent of
+ * summation order); the definition is fp64.
  *
  * Threading: every entry point is reentrant and thread-safe, keeps no state
  * between calls and allocates no memory. Launches are stream-ordered; the
@@ -91,7 +99,12 @@ enum {
 #define QRITA_FLAG_CLUSTER_SHIFT 8     /* bits 8..10: force 2^n CTAs per row (n in 0..4);
                                           0 in these bits and bit 11 clear = automatic */
 #define QRITA_FLAG_CLUSTER_SET 0x800u  /* bit 11: the cluster-size bits are set */
-#define QRITA_FLAG_KNOWN_MASK 0xFFFu
+#define QRITA_FLAG_TEST_GIVE_UP 0x1000u /* tests only: the first bounded wait for a bulk
+                                           copy in the first CTA of row 0 reports that it
+                                           gave up (without waiting), so that row takes the
+                                           QRITA_ROW_TIMEOUT path; the copy still lands and is
+                                           waited for before the CTA exits */
+#define QRITA_FLAG_KNOWN_MASK 0x1FFFu
 
 /* Bits of qrita_row_info_t.path. */
 #define QRITA_PATH_TOPK 0x1u      /* top-k active for the row */
@@ -188,6 +201,20 @@ size_t qrita_host_staging_bytes(int dtype, int64_t B, int64_t V);
 int qrita_select_host(const void* h_logits, int dtype, int64_t B, int64_t V, const int32_t* h_k,
                       const float* h_p, uint8_t* h_mask, void* d_staging, size_t staging_bytes,
                       qrita_stream_t stream);
+
+/*
+ * qrita_delta_table: copy one of the host-built truncation tables the kernel
+ * receives (Qrita technical summary, "Methodology", part 1: delta comes from
+ * precomputed tables of the normal quantile function keyed on k or p).
+ *
+ *   which  0: the top-k table, entry i = Phi^-1(1 - 2^(-i/4));
+ *          1: the top-p table, entry i = Phi^-1(2^(-i/4)).
+ *   out    host float[n] or NULL; receives min(n, length) entries.
+ *
+ * Returns the table's length (entries), or -1 when `which` is unknown.
+ * Touches no device; for tests and diagnostics.
+ */
+int qrita_delta_table(int which, float* out, int n);
 
 /* Static, human-readable text for a QRITA_* return code. */
 const char* qrita_strerror(int code);

@@ -43,6 +43,29 @@ def load_golden(path):
     return cases
 
 
+# flagged top-p rows per workload, reported at the end of the run
+_FLAGGED = {}
+
+
+@pytest.fixture(scope="session")
+def record_flagged():
+    """record_flagged(name, flagged, rows): the oracle's count of top-p rows
+    whose boundary mass lies within 1e-6 * p of p, for the run summary."""
+
+    def rec(name, flagged, rows):
+        _FLAGGED[name] = (int(flagged), int(rows))
+
+    return rec
+
+
+def pytest_terminal_summary(terminalreporter):
+    if _FLAGGED:
+        terminalreporter.write_line("rows compared with the oracle, and the flagged top-p rows among them:")
+        for name in sorted(_FLAGGED):
+            f, n = _FLAGGED[name]
+            terminalreporter.write_line(f"  {name}: {n} rows, {f} flagged")
+
+
 @pytest.fixture(scope="session")
 def golden_rows():
     return load_golden(os.path.join(ROOT, "tests", "golden", "handworked_rows.txt"))

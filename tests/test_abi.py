@@ -59,7 +59,7 @@ FAKE = ctypes.c_void_p(0x1000)  # never dereferenced: every case fails validatio
         (FAKE, 0, 1, 10, NULL, 0),             # null mask
         (ctypes.c_void_p(0x1002), 0, 1, 10, FAKE, 0),  # fp32 pointer not 4-byte aligned
         (ctypes.c_void_p(0x1001), 1, 1, 10, FAKE, 0),  # bf16 pointer not 2-byte aligned
-        (FAKE, 0, 1, 10, FAKE, 0x1000),        # unknown flag bit
+        (FAKE, 0, 1, 10, FAKE, 0x80000000),    # unknown flag bit
     ],
 )
 def test_invalid_arguments_are_rejected(L, logits, dtype, B, V, mask, flags):
@@ -84,6 +84,9 @@ def test_host_staging_bytes(L):
             assert L.qrita_host_staging_bytes(dt, B, V) == up(B * V * s) + 2 * up(B * 4) + up(B * V)
     assert L.qrita_host_staging_bytes(5, 1, 1) == 0
     assert L.qrita_host_staging_bytes(0, 1, 0) == 0
+    # sizes whose byte count would overflow size_t are refused, not wrapped
+    assert L.qrita_host_staging_bytes(0, 2**62, 2**31 - 1) == 0
+    assert L.qrita_host_staging_bytes(1, 2**40, 2**30) == 0
 
 
 def test_host_entry_rejects_short_staging(L):
@@ -118,6 +121,7 @@ def _header_probe(tmp_path):
               "QRITA_ECUDA", "QRITA_ROW_OK", "QRITA_ROW_NONFINITE", "QRITA_ROW_SEARCH_CAP", "QRITA_ROW_TIMEOUT",
               "QRITA_FLAG_NO_TRUNCATION", "QRITA_FLAG_FORCE_FALLBACK", "QRITA_FLAG_KEY_PIVOTS",
               "QRITA_FLAG_FORCE_RETRY", "QRITA_FLAG_HIST_MISS", "QRITA_FLAG_CLUSTER_SHIFT", "QRITA_FLAG_CLUSTER_SET",
+              "QRITA_FLAG_TEST_GIVE_UP",
               "QRITA_PATH_TOPK", "QRITA_PATH_TOPP", "QRITA_PATH_TRUNC", "QRITA_PATH_HIT", "QRITA_PATH_FALLBACK",
               "QRITA_PATH_OVERFLOW", "QRITA_PATH_KEEP_ALL", "QRITA_PATH_RETRY", "QRITA_PATH_HIST",
               "QRITA_PATH_SAMPLE_T"]

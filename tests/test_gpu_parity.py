@@ -13,7 +13,8 @@ import numpy as np
 import pytest
 
 from oracle import select_batch, select_row
-from parity_helpers import check_against_oracle, compare_rows, invariant_failures, run_gpu, to_device, widen
+from parity_helpers import (check_against_oracle, compare_rows, compare_rows_pooled, invariant_failures, run_gpu,
+                            to_device, widen)
 from workloads import WORKLOADS, generate
 
 pytestmark = pytest.mark.gpu
@@ -53,30 +54,73 @@ def test_workload_leading_rows(dev, n):
 
 
 # ---------------------------------------------------------------------------
-# Workloads at full size, launched exactly as the bench launches them
+# Workloads at full size, launched exactly as the bench launches them: every
+# row against the oracle (spread over the host cores) and the invariants
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
-def test_workload_full_size(dev, n):
+def test_workload_full_size(dev, n, record_flagged):
     w = WORKLOADS[n]
     logits, k, p = workload(n)
     got, st, info = run_gpu(logits, w.dtype, k, p, dev)
     assert (st == 0).all()
-    # sampled rows against the oracle (evenly spaced plus seeded picks)
-    rng = np.random.default_rng(50 + n)
-    sample = sorted(set(np.linspace(0, w.B - 1, min(w.B, 16)).astype(int).tolist())
-                    | set(rng.choice(w.B, size=min(w.B, 16), replace=False).tolist()))
-    ref = select_batch(logits, w.dtype, k, p, rows=sample)
-    fails, flagged = compare_rows(got, st, ref)
+    fails, flagged, bad = compare_rows_pooled(logits, w.dtype, k, p, got, st)
+    record_flagged(f"workload {n} {w.name}", flagged, w.B)
     assert fails == [], fails[:5]
-    # invariants on every row
-    bad = []
-    for r in range(w.B):
-        f = invariant_failures(widen(logits[r], w.dtype), got[r], int(k[r]), float(p[r]))
-        if f:
-            bad.append((r, f))
     assert bad == [], bad[:5]
     # diagnostics agree with the mask
     assert np.array_equal(info["kept"], got.sum(axis=1).astype(np.uint32))
+
+
+def test_multi_wave_batch_every_row(dev, record_flagged):
+    """A batch of 700 one-CTA rows (more than the device holds at once), half
+    of them top-p only, so the launch reorders rows heavy-first across waves;
+    every row is compared with the oracle."""
+    import top_selection_row_gb300 as q
+
+    rng = np.random.default_rng(700)
+    B, V = 700, 32000
+    T = rng.uniform(0.5, 1.5, size=(B, 1))
+    x = (rng.standard_normal((B, V)) / T).astype(np.float32)
+    for r in range(B):
+        pos = rng.choice(V, size=16, replace=False)
+        x[r, pos] = (rng.uniform(4.0, 10.0, size=16) / T[r, 0]).astype(np.float32)
+    p_only = rng.permutation(B) < B // 2
+    k = np.where(p_only, V, rng.integers(1, 1000, size=B)).astype(np.int32)
+    p = np.where(p_only, rng.uniform(0.5, 0.99, size=B),
+                 np.where(rng.random(B) < 0.5, 1.0, rng.uniform(0.8, 1.0, size=B))).astype(np.float32)
+    got, st, info = run_gpu(x, "f32", k, p, dev)
+    assert (st == 0).all()
+    fails, flagged, bad = compare_rows_pooled(x, "f32", k, p, got, st)
+    record_flagged("multi-wave b700_v32000_f32_mixed", flagged, B)
+    assert fails == [], fails[:5]
+    assert bad == [], bad[:5]
+    assert ((info["path"] & q.PATH_TOPP) != 0).sum() >= B // 2
+
+
+@pytest.mark.parametrize("case", ["w2_c16", "w5_c16", "w2_c1", "w3_c2", "w4_c1"])
+def test_copy_wait_give_up_voids_only_its_row(dev, case):
+    """A bounded wait for a bulk copy that gives up (forced by a test flag on
+    the first wait of row 0's first CTA) voids that row: status
+    QRITA_ROW_TIMEOUT and an all-zero mask. The copy it gave up on still
+    lands and is waited for before the CTA exits, and every other row of the
+    batch is still exact against the oracle."""
+    import top_selection_row_gb300 as q
+
+    n = int(case[1])
+    cl = {"c16": 0, "c1": q.flag_cluster(1), "c2": q.flag_cluster(2)}[case.split("_")[1]]
+    w = WORKLOADS[n]
+    logits, k, p = workload(n, 8)
+    got, st, info = run_gpu(logits, w.dtype, k, p, dev, flags=q.FLAG_TEST_GIVE_UP | cl)
+    assert st[0] == q.ROW_TIMEOUT
+    assert not got[0].any()
+    assert info["status"][0] == q.ROW_TIMEOUT and info["kept"][0] == 0
+    ref = select_batch(logits, w.dtype, k, p, rows=list(range(1, 8)))
+    fails, _ = compare_rows(got, st, ref)
+    assert fails == [], fails[:5]
+    # the flag leaves a batch without row 0's CTA untouched: the next call is clean
+    again, st2, _ = run_gpu(logits, w.dtype, k, p, dev, flags=cl)
+    assert (st2 == 0).all()
+    assert np.array_equal(again[1:], got[1:])
 
 
 # ---------------------------------------------------------------------------

@@ -25,6 +25,7 @@ FLAG_KEY_PIVOTS = 0x4
 FLAG_FORCE_RETRY = 0x8
 FLAG_HIST_MISS = 0x10
 FLAG_CLUSTER_SET = 0x800
+FLAG_TEST_GIVE_UP = 0x1000
 
 
 def flag_cluster(n_ctas: int) -> int:
@@ -171,6 +172,18 @@ def decode_row_info(info) -> np.ndarray:
     """qrita_row_info_t records (CUDA uint8 [B, 64]) as a numpy structured array."""
     raw = info.detach().cpu().numpy()
     return np.ascontiguousarray(raw).view(ROW_INFO_DTYPE).reshape(-1)
+
+
+def delta_table(which: int) -> np.ndarray:
+    """The host-built truncation table the kernel receives: ``which`` 0 is the
+    top-k table (entry i = Phi^-1(1 - 2^(-i/4))), 1 the top-p table (entry
+    i = Phi^-1(2^(-i/4))). Returns float32 [length]."""
+    n = int(lib().qrita_delta_table(int(which), None, 0))
+    if n < 0:
+        raise ValueError(f"unknown delta table {which}")
+    out = np.zeros(n, np.float32)
+    lib().qrita_delta_table(int(which), out.ctypes.data_as(ctypes.c_void_p), n)
+    return out
 
 
 def host_staging_bytes(dtype_code: int, B: int, V: int) -> int:

@@ -17,6 +17,7 @@ EXPORTED = (
     "qrita_select_ex",
     "qrita_host_staging_bytes",
     "qrita_select_host",
+    "qrita_delta_table",
     "qrita_strerror",
     "qrita_version",
 )
@@ -43,6 +44,8 @@ def lib() -> ctypes.CDLL:
     L.qrita_host_staging_bytes.restype = sz
     L.qrita_select_host.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, sz, vp]
     L.qrita_select_host.restype = i32
+    L.qrita_delta_table.argtypes = [i32, vp, i32]
+    L.qrita_delta_table.restype = i32
     L.qrita_strerror.argtypes = [i32]
     L.qrita_strerror.restype = ctypes.c_char_p
     L.qrita_version.argtypes = []

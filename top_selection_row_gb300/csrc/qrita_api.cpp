@@ -218,9 +218,13 @@ size_t qrita_host_staging_bytes(int dtype, int64_t B, int64_t V) {
   if ((dtype != QRITA_DTYPE_F32 && dtype != QRITA_DTYPE_BF16) || B < 0 || V < 1 ||
       V > std::numeric_limits<int32_t>::max())
     return 0;
-  const size_t n = static_cast<size_t>(B) * static_cast<size_t>(V);
-  return qrita::align256(n * qrita::elem_bytes(dtype)) + qrita::align256(static_cast<size_t>(B) * 4) +
-         qrita::align256(static_cast<size_t>(B) * 4) + qrita::align256(n);
+  // every section and the sum must fit size_t (0 = invalid, as above)
+  constexpr size_t kMax = std::numeric_limits<size_t>::max();
+  const size_t b = static_cast<size_t>(B), v = static_cast<size_t>(V);
+  const size_t eb = static_cast<size_t>(qrita::elem_bytes(dtype));
+  if (b != 0 && v > (kMax / 8u) / b) return 0;  // B*V*eb and the 256-byte roundings stay far below kMax
+  const size_t n = b * v;
+  return qrita::align256(n * eb) + qrita::align256(b * 4) + qrita::align256(b * 4) + qrita::align256(n);
 }
 
 int qrita_select_host(const void* h_logits, int dtype, int64_t B, int64_t V, const int32_t* h_k,
@@ -238,19 +242,42 @@ int qrita_select_host(const void* h_logits, int dtype, int64_t B, int64_t V, con
   float* d_p = reinterpret_cast<float*>(base + qrita::align256(lb) + qrita::align256(B * 4));
   uint8_t* d_mask = base + qrita::align256(lb) + 2 * qrita::align256(B * 4);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // once a copy is enqueued, every return waits for the stream first: the
+  // caller may free or reuse its host buffers as soon as the call returns
+  auto fail_after_enqueue = [st](int code) {
+    (void)cudaStreamSynchronize(st);
+    return code;
+  };
   if (cudaMemcpyAsync(d_logits, h_logits, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return QRITA_ECUDA;
+    return fail_after_enqueue(QRITA_ECUDA);
   if (h_k && cudaMemcpyAsync(d_k, h_k, B * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return QRITA_ECUDA;
+    return fail_after_enqueue(QRITA_ECUDA);
   if (h_p && cudaMemcpyAsync(d_p, h_p, B * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
-    return QRITA_ECUDA;
+    return fail_after_enqueue(QRITA_ECUDA);
   rc = qrita::select_impl(d_logits, dtype, B, V, h_k ? d_k : nullptr, h_p ? d_p : nullptr, d_mask,
                           stream, 0u, nullptr, nullptr);
-  if (rc != QRITA_OK) return rc;
+  if (rc != QRITA_OK) return fail_after_enqueue(rc);
   if (cudaMemcpyAsync(h_mask, d_mask, n, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return QRITA_ECUDA;
+    return fail_after_enqueue(QRITA_ECUDA);
   if (cudaStreamSynchronize(st) != cudaSuccess) return QRITA_ECUDA;
   return QRITA_OK;
+}
+
+int qrita_delta_table(int which, float* out, int n) {
+  const qrita::Tables& t = qrita::tables();
+  const float* src = nullptr;
+  int len = 0;
+  if (which == 0) {
+    src = t.lut_k;
+    len = qrita::kLutK;
+  } else if (which == 1) {
+    src = t.lut_p;
+    len = qrita::kLutP;
+  } else {
+    return -1;
+  }
+  if (out != nullptr && n > 0) std::memcpy(out, src, sizeof(float) * static_cast<size_t>(n < len ? n : len));
+  return len;
 }
 
 const char* qrita_strerror(int code) {

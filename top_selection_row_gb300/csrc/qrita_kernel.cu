@@ -476,6 +476,7 @@ struct Ctx {
   float fix_scale;  // fixed-point scale of weights in [0, 1]
   bool zero_fill;       // the chunk's mask is to be zeroed early (by the search tail)
   bool zero_fill_done;  // and it was
+  bool give_up_once;    // test flag: the next bounded copy wait reports that it gave up
 };
 
 // Fill the chunk's mask with one byte value (16-byte stores where aligned).
@@ -553,7 +554,15 @@ __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, Sc
   for (int pc = 0; pc < npieces; ++pc, st = (st + 1 == nst) ? 0 : st + 1) {
     const uint32_t bar = c.ring_bar + 8u * st;
     bool ok = false;
-    if (vld(F.err) == 0u) ok = mbar_wait_bounded(bar, (c.ring_phase >> st) & 1u, kWaitLimitNs);
+    if (vld(F.err) == 0u) {
+      if (c.give_up_once) {
+        // QRITA_FLAG_TEST_GIVE_UP: this wait reports a timeout without waiting
+        // (the copy itself still lands; the drain below waits for it)
+        c.give_up_once = false;
+      } else {
+        ok = mbar_wait_bounded(bar, (c.ring_phase >> st) & 1u, kWaitLimitNs);
+      }
+    }
     if (ok) {
       c.ring_phase ^= 1u << st;
       if (tid == 0) c.ring_out &= ~(1u << st);
@@ -2456,6 +2465,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     c.tail_n = c.n - c.head_n - c.body_units * E;
   }
   c.gbody = c.gx + c.head_n * S;
+  // the test flag voids row 0 from its first CTA: uniform over that CTA
+  c.give_up_once = (P.flags & QRITA_FLAG_TEST_GIVE_UP) != 0u && r == 0 && c.crank == 0u;
   QRITA_T(0);
 
   // ---- row parameters (uniform)
