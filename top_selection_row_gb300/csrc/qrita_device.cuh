@@ -44,6 +44,39 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
 }
 
 // ---------------------------------------------------------------------------
+// Packed bf16 pairs (one 32-bit word holds elements 2i (low half) and 2i+1).
+// ---------------------------------------------------------------------------
+// Per-half NaN-propagating max and NaN-ignoring min.
+__device__ __forceinline__ uint32_t bf2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf2_min(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// 0xFFFF in each half where a >= b (false for NaN), else 0.
+__device__ __forceinline__ uint32_t bf2_ge_mask(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.ge.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// The smallest bf16 value c >= t (t finite fp32), as raw bits: for bf16 x,
+// x >= t exactly when x >= c. Truncating t's low half moves it toward zero:
+// up for negative t, down for positive t, so only a positive inexact t steps
+// to the next bf16.
+__device__ __forceinline__ uint32_t bf16_ceil_bits(float t) {
+  uint32_t tb = __float_as_uint(t) >> 16;
+  if (__uint_as_float(tb << 16) < t) tb += 1u;
+  return tb;
+}
+
+// ---------------------------------------------------------------------------
 // Compensated fp32 sums: a value is hi + lo with |lo| <= ulp(hi)/2.
 // two_sum is Knuth's error-free addition (6 flops, no ordering condition).
 // ---------------------------------------------------------------------------

@@ -159,10 +159,22 @@ __device__ __forceinline__ T vld(const T& r) {
   return *reinterpret_cast<const volatile T*>(&r);
 }
 
+// exp(d) as 2^(d log2 e) by the hardware base-2 exponential (ex2.approx,
+// subnormal results flushed to zero). d = x - s is formed first, so the
+// argument's rounding error scales with |x - s| and not with the shift s:
+// weights near the shift, which carry the mass, are within a few ulp of
+// exp, and a row's weights all come from this one function.
+constexpr float kLog2e = 1.4426950408889634f;
+__device__ __forceinline__ float exp_shifted(float x, float s) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"((x - s) * kLog2e));
+  return r;
+}
+
 // Softmax weight of x for row max m. A row whose max is -inf holds only
 // -inf, and equal logits get equal weight 1.
 __device__ __forceinline__ float weight(float x, float m, bool m_neginf) {
-  return m_neginf ? 1.0f : expf(x - m);
+  return m_neginf ? 1.0f : exp_shifted(x, m);
 }
 
 // Fixed-point softmax weight: round(exp(x - m) * scale). Every place that
@@ -657,6 +669,62 @@ __device__ __forceinline__ void append_piece(Ctx<DT>& c, uint32_t& wn, uint32_t 
       if (pos < segcap) {
         c.own_val[seg_base + pos] = x;
         c.own_idx[seg_base + pos] = idx0 + static_cast<uint32_t>(e);
+      }
+      ++pos;
+    }
+  }
+}
+
+// bf16 unit (8 elements, four packed words) survivor bits in the packed
+// layout: bit i is element 2i (word i's low half), bit 16 + i element 2i + 1.
+__device__ __forceinline__ uint32_t bf16_unit_bits(const uint4 v, uint32_t t2) {
+  uint32_t b = bf2_ge_mask(v.x, t2) & 0x00010001u;
+  b |= bf2_ge_mask(v.y, t2) & 0x00020002u;
+  b |= bf2_ge_mask(v.z, t2) & 0x00040004u;
+  b |= bf2_ge_mask(v.w, t2) & 0x00080008u;
+  return b;
+}
+
+// Element (index within the unit) and value of packed bit p of a bf16 unit.
+__device__ __forceinline__ int bf16_bit_elem(int p) { return ((p & 15) << 1) | (p >> 4); }
+__device__ __forceinline__ float bf16_bit_value(const uint4 v, int p) {
+  const int i = p & 15;
+  const uint32_t w = i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+  return __uint_as_float((p >> 4) ? (w & 0xFFFF0000u) : (w << 16));
+}
+
+// append_piece for bf16 units in the packed bit layout: the values come
+// straight from the raw units (only survivors are widened).
+template <int DT>
+__device__ __forceinline__ void append_piece_bf16(Ctx<DT>& c, uint32_t& wn, uint32_t seg_base, uint32_t segcap,
+                                                  const uint4 (&v)[kPieceThreadUnits],
+                                                  const uint32_t (&bits)[kPieceThreadUnits], int u0) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int j = 0; j < kPieceThreadUnits; ++j) cnt += __popc(bits[j]);
+  if (__ballot_sync(kFull, cnt != 0u) == 0u) return;
+  constexpr int kPlanes = 32 - __builtin_clz(static_cast<unsigned>(kPieceThreadUnits * 8));
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t excl = 0, tot = 0;
+#pragma unroll
+  for (int b = 0; b < kPlanes; ++b) {
+    const uint32_t plane = __ballot_sync(kFull, (cnt >> b) & 1u);
+    excl += static_cast<uint32_t>(__popc(plane & lt)) << b;
+    tot += static_cast<uint32_t>(__popc(plane)) << b;
+  }
+  uint32_t pos = wn + excl;
+  wn += tot;
+#pragma unroll
+  for (int j = 0; j < kPieceThreadUnits; ++j) {
+    uint32_t b = bits[j];
+    const uint32_t idx0 = static_cast<uint32_t>(c.head_n + (u0 + j * kThreads + tid) * 8);
+    while (b != 0u) {
+      const int p = __ffs(b) - 1;
+      b &= b - 1u;
+      if (pos < segcap) {
+        c.own_val[seg_base + pos] = bf16_bit_value(v[j], p);
+        c.own_idx[seg_base + pos] = idx0 + static_cast<uint32_t>(bf16_bit_elem(p));
       }
       ++pos;
     }
@@ -1297,7 +1365,11 @@ __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_abo
   const uint32_t seg_base = static_cast<uint32_t>(warp) * segcap;
   uint32_t wn = 0;
   uint32_t ca = 0;
-  unsigned long long ma = 0ull, mi = 0ull;
+  // the mass above hi is one constant offset of the search that follows, so
+  // it is summed in compensated fp32 (a unit's partial at a time); the list's
+  // mass must equal what the search sums over the list: exact fixed point
+  F2 ma = {0.f, 0.f};
+  unsigned long long mi = 0ull;
   const uintptr_t mbp = reinterpret_cast<uintptr_t>(c.gmask + c.head_n);
   const bool vec_ok = (mbp % E) == 0;
   stream_pieces<DT>(
@@ -1311,19 +1383,21 @@ __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_abo
           bits[j] = 0u;
           if (j * kThreads + tid < n) {
             uint32_t keep = 0u;  // bit e: element e is above hi
+            float pa = 0.f;
 #pragma unroll
             for (int e = 0; e < E; ++e) {
               const float x = xs[j][e];
               const uint32_t k = f2key(x);
               const bool above = k > hi;
               const bool in = !above && k > lo;
-              const unsigned long long w = weight_fx(x, c.m, c.m_neginf, scale);
+              const float w = weight(x, c.m, c.m_neginf);
               ca += above ? 1u : 0u;
-              ma += above ? w : 0ull;
-              mi += in ? w : 0ull;
+              pa += above ? w : 0.f;
+              if (in) mi += round_u64(w * scale);
               keep |= above ? (1u << e) : 0u;
               bits[j] |= in ? (1u << e) : 0u;
             }
+            f2_add(ma, pa);
             // one mask byte per element (bit e of keep -> byte e)
             uint8_t* dst = c.gmask + c.head_n + static_cast<size_t>(u0 + j * kThreads + tid) * E;
             const uint32_t w0 = (keep & 1u) | ((keep & 2u) << 7) | ((keep & 4u) << 14) | ((keep & 8u) << 21);
@@ -1349,10 +1423,10 @@ __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_abo
           const uint32_t k = f2key(x);
           const bool above = k > hi;
           const bool in = !above && k > lo;
-          const unsigned long long w = weight_fx(x, c.m, c.m_neginf, scale);
+          const float w = weight(x, c.m, c.m_neginf);
           ca += above ? 1u : 0u;
-          ma += above ? w : 0ull;
-          mi += in ? w : 0ull;
+          if (above) f2_add(ma, w);
+          if (in) mi += round_u64(w * scale);
           bits = in ? 1u : 0u;
           c.gmask[idx] = above ? 1 : 0;
         }
@@ -1362,23 +1436,27 @@ __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_abo
       false);
   own_segments_streamed<DT>(c, wn);
   ca = __reduce_add_sync(kFull, ca);
-  ma = warp_sum_u64(ma);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    ma = f2_merge(ma, f2_make(__shfl_xor_sync(kFull, ma.hi, o), __shfl_xor_sync(kFull, ma.lo, o)));
   mi = warp_sum_u64(mi);
   if (lane == 0) {
     F.lred[0][warp][0].cnt = ca;
-    F.lred[0][warp][0].mass = ma;
+    F.redf[warp][6] = ma.hi;
+    F.redf[warp][7] = ma.lo;
     F.lred[0][warp][1].mass = mi;
   }
   __syncthreads();
   uint32_t tc = 0;
-  unsigned long long tma = 0ull, tmi = 0ull;
+  F2 tma = {0.f, 0.f};
+  unsigned long long tmi = 0ull;
   for (int w = 0; w < kWarps; ++w) {
     tc += vld(F.lred[0][w][0].cnt);
-    tma += vld(F.lred[0][w][0].mass);
+    tma = f2_merge(tma, f2_make(vld(F.redf[w][6]), vld(F.redf[w][7])));
     tmi += vld(F.lred[0][w][1].mass);
   }
   c_above = tc;
-  m_above = tma;
+  m_above = f2_to_u64(f2_mul(tma, scale));
   m_in = tmi;
   __syncthreads();
 }
@@ -2719,11 +2797,18 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   // ---- A4: the streaming pass (the one HBM read of the row)
   {
     float vmax = -INFINITY, vmin = INFINITY;
+    // bf16 rows without top-p alone: packed running max / min (-inf, +inf
+    // pairs) and the threshold as the smallest bf16 >= t, in both halves
+    uint32_t vmax2 = 0xFF80FF80u, vmin2 = 0x7F807F80u, t2 = 0u;
+    if (DT == QRITA_DTYPE_BF16 && trunc) {
+      const uint32_t tb = bf16_ceil_bits(t);
+      t2 = tb | (tb << 16);
+    }
     uint32_t wn = 0;  // this warp's survivors (its segment of the own list)
     const uint32_t segcap = c.ocap / kWarps;
     const uint32_t seg_base = static_cast<uint32_t>(warp) * segcap;
     F2 zs = {0.f, 0.f}, ms = {0.f, 0.f};
-    // two instances: the softmax sums (one expf per element) only where
+    // two instances: the softmax sums (one exponential per element) only where
     // top-p runs alone
     // top-k rows expecting few survivors per CTA keep them in per-thread
     // columns of the own list (no warp communication per piece)
@@ -2761,6 +2846,36 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       stream_pieces<DT>(
           c,
           [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
+            if constexpr (DT == QRITA_DTYPE_BF16 && !PO) {
+              // packed bf16: max / min and the survivor test on pairs; only
+              // survivors are widened
+              uint32_t bits[kPieceThreadUnits];
+#pragma unroll
+              for (int j = 0; j < kPieceThreadUnits; ++j) {
+                bits[j] = 0u;
+                if (j * kThreads + tid < n) {
+                  const uint4 u = v[j];
+                  vmax2 = bf2_max_nan(vmax2, bf2_max_nan(bf2_max_nan(u.x, u.y), bf2_max_nan(u.z, u.w)));
+                  vmin2 = bf2_min(vmin2, bf2_min(bf2_min(u.x, u.y), bf2_min(u.z, u.w)));
+                  if (trunc) bits[j] = bf16_unit_bits(u, t2);
+                }
+              }
+              if constexpr (COL) {
+#pragma unroll
+                for (int j = 0; j < kPieceThreadUnits; ++j) {
+                  uint32_t b = bits[j];
+                  const uint32_t idx0 = static_cast<uint32_t>(c.head_n + (u0 + j * kThreads + tid) * E);
+                  while (b != 0u) {
+                    const int q = __ffs(b) - 1;
+                    b &= b - 1u;
+                    col_put(bf16_bit_value(v[j], q), idx0 + static_cast<uint32_t>(bf16_bit_elem(q)));
+                  }
+                }
+              } else {
+                append_piece_bf16<DT>(c, wn, seg_base, segcap, v, bits, u0);
+              }
+              return;
+            }
             float xs[kPieceThreadUnits][E];
             uint32_t bits[kPieceThreadUnits];
             float zu = 0.f, mu_ = 0.f;  // this piece's softmax partials (shift m_ref)
@@ -2777,7 +2892,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   const bool surv = trunc && x >= t;
                   bits[j] |= surv ? (1u << e) : 0u;
                   if constexpr (PO) {
-                    const float w = expf(x - m_ref);
+                    const float w = exp_shifted(x, m_ref);
                     zu += w;
                     mu_ += surv ? w : 0.f;
                     if constexpr (PH) {
@@ -2817,7 +2932,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               const bool surv = trunc && x >= t;
               bits = surv ? 1u : 0u;
               if constexpr (PO) {
-                const float w = expf(x - m_ref);
+                const float w = exp_shifted(x, m_ref);
                 f2_add(zs, w);
                 f2_add(ms, surv ? w : 0.f);
                 if constexpr (PH) {
@@ -2901,6 +3016,10 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         ta[1] = __float_as_uint(m2);
       }
       __syncthreads();
+    }
+    if (DT == QRITA_DTYPE_BF16 && !p_only) {
+      vmax = fmax_nan(vmax, fmax_nan(__uint_as_float(vmax2 << 16), __uint_as_float(vmax2 & 0xFFFF0000u)));
+      vmin = fminf(vmin, fminf(__uint_as_float(vmin2 << 16), __uint_as_float(vmin2 & 0xFFFF0000u)));
     }
     // block reduce
 #pragma unroll
