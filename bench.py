@@ -194,7 +194,7 @@ def oracle_flagged_counts():
 
 PATH_BITS = {
     "top_k": 0x1, "top_p": 0x2, "truncated": 0x4, "hit": 0x8, "fallback": 0x10, "overflow": 0x20,
-    "keep_all": 0x40, "retry": 0x80, "hist": 0x100, "sample_threshold": 0x200,
+    "keep_all": 0x40, "retry": 0x80, "hist": 0x100, "sample_threshold": 0x200, "key_histogram": 0x400,
 }
 
 
@@ -203,7 +203,7 @@ def path_counts(info) -> dict:
     their truncation survivors (hit, retry or hist without the fallback)."""
     path = info["path"].astype(np.int64)
     out = {name: int(((path & bit) != 0).sum()) for name, bit in PATH_BITS.items()}
-    searched = (path & (0x8 | 0x80 | 0x100)) != 0
+    searched = (path & (0x8 | 0x80 | 0x100 | 0x400)) != 0
     out["searched_survivors"] = int((searched & ((path & 0x10) == 0)).sum())
     out["narrowing_passes_total"] = int(info["passes"].astype(np.int64).sum())
     return out

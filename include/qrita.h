@@ -104,7 +104,10 @@ enum {
                                            gave up (without waiting), so that row takes the
                                            QRITA_ROW_TIMEOUT path; the copy still lands and is
                                            waited for before the CTA exits */
-#define QRITA_FLAG_KNOWN_MASK 0x1FFFu
+#define QRITA_FLAG_NO_KEY_HIST 0x2000u /* bf16 rows: search with pivot rounds even where the
+                                           survivors span few enough 16-bit keys for the
+                                           key histogram */
+#define QRITA_FLAG_KNOWN_MASK 0x3FFFu
 
 /* Bits of qrita_row_info_t.path. */
 #define QRITA_PATH_TOPK 0x1u      /* top-k active for the row */
@@ -123,6 +126,9 @@ enum {
 #define QRITA_PATH_HIST 0x100u    /* top-p alone: value bins counted by the streaming
                                      pass placed the boundary, and one more pass
                                      extracted those bins for the search */
+#define QRITA_PATH_KEYHIST 0x400u /* bf16 truncation hit: one histogram of the survivors'
+                                     16-bit keys placed the top-k boundary (and the
+                                     top-p boundary over S_k) */
 
 /* Diagnostics of one row (qrita_select_ex, optional). Device memory. */
 typedef struct qrita_row_info {

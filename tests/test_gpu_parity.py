@@ -263,7 +263,8 @@ def _mixed_batch():
 @pytest.mark.parametrize(
     "flags",
     ["none", "no_trunc", "fallback", "key_pivots", "c1", "c2", "c4", "c8", "c16", "fallback_key_c16",
-     "retry", "retry_c1", "retry_c16", "retry_key", "hist_miss", "hist_miss_c16"],
+     "retry", "retry_c1", "retry_c16", "retry_key", "hist_miss", "hist_miss_c16", "no_key_hist",
+     "no_key_hist_c1", "no_key_hist_c4"],
 )
 def test_forced_paths_match_oracle(dev, flags):
     import top_selection_row_gb300 as q
@@ -285,6 +286,9 @@ def test_forced_paths_match_oracle(dev, flags):
         "retry_key": q.FLAG_FORCE_RETRY | q.FLAG_KEY_PIVOTS,
         "hist_miss": q.FLAG_HIST_MISS,
         "hist_miss_c16": q.FLAG_HIST_MISS | q.flag_cluster(16),
+        "no_key_hist": q.FLAG_NO_KEY_HIST,
+        "no_key_hist_c1": q.FLAG_NO_KEY_HIST | q.flag_cluster(1),
+        "no_key_hist_c4": q.FLAG_NO_KEY_HIST | q.flag_cluster(4),
     }[flags]
     for n, logits, k, p in _mixed_batch():
         w = WORKLOADS[n]
@@ -295,6 +299,45 @@ def test_forced_paths_match_oracle(dev, flags):
             assert ((info["path"][top_k] & q.PATH_RETRY) != 0).all()
         if flags.startswith("hist_miss"):
             assert ((info["path"] & q.PATH_HIST) == 0).all()
+        if flags.startswith("no_key_hist"):
+            assert ((info["path"] & q.PATH_KEYHIST) == 0).all()
+
+
+@pytest.mark.parametrize("n,cl", [(4, 0), (5, 0), (4, 16), (5, 2)])
+def test_key_histogram_places_bf16_boundaries(dev, n, cl):
+    """bf16 rows whose truncation hit place both boundaries with one
+    histogram of the survivors' 16-bit keys (merged over the cluster when a
+    row spans several CTAs)."""
+    import top_selection_row_gb300 as q
+
+    w = WORKLOADS[n]
+    logits, k, p = workload(n, 32)
+    flags = q.flag_cluster(cl) if cl else 0
+    fails, flagged, got, st, info = check_against_oracle(logits, w.dtype, k, p, dev, flags=flags)
+    assert fails == [], fails[:5]
+    hit = ((info["path"] & q.PATH_HIT) != 0) & ((info["path"] & q.PATH_TOPK) != 0)
+    kh = (info["path"] & q.PATH_KEYHIST) != 0
+    assert hit.sum() >= 8
+    assert (kh == hit).all()
+
+
+def test_key_histogram_gives_way_on_wide_bf16_rows(dev):
+    """A far outlier widens the survivors' key range beyond the histogram:
+    those rows take the pivot rounds, with the same results."""
+    import top_selection_row_gb300 as q
+    from workloads import f32_to_bf16_bits
+
+    rng = np.random.default_rng(17)
+    B, V = 12, 50000
+    x = rng.standard_normal((B, V)).astype(np.float32)
+    x[:, 123] = np.float32(3e30)     # far above: tens of thousands of keys away
+    x[::2, 4567] = np.float32(-1e25)
+    logits = f32_to_bf16_bits(x)
+    k = np.array([1, 2, 10, 100, 1000, 5000, 1, 50, 700, 3, 20000, 60], np.int32)
+    p = np.array([1.0, 0.5, 0.9, 1.0, 0.99, 1.0, 0.3, 1.0, 0.95, 1.0, 0.7, 1.0], np.float32)
+    fails, flagged, got, st, info = check_against_oracle(logits, "bf16", k, p, dev)
+    assert fails == [], fails[:5]
+    assert ((info["path"] & q.PATH_KEYHIST) == 0).all()
 
 
 def test_first_pass_bins_place_flat_top_p_rows(dev):

@@ -26,6 +26,7 @@ FLAG_FORCE_RETRY = 0x8
 FLAG_HIST_MISS = 0x10
 FLAG_CLUSTER_SET = 0x800
 FLAG_TEST_GIVE_UP = 0x1000
+FLAG_NO_KEY_HIST = 0x2000
 
 
 def flag_cluster(n_ctas: int) -> int:
@@ -38,6 +39,7 @@ PATH_TOPK, PATH_TOPP, PATH_TRUNC, PATH_HIT = 0x1, 0x2, 0x4, 0x8
 PATH_FALLBACK, PATH_OVERFLOW, PATH_KEEP_ALL, PATH_RETRY = 0x10, 0x20, 0x40, 0x80
 PATH_HIST = 0x100
 PATH_SAMPLE_T = 0x200
+PATH_KEYHIST = 0x400
 
 # Layout of qrita_row_info_t (64 bytes).
 ROW_INFO_DTYPE = np.dtype(

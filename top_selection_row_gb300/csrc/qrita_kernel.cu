@@ -2449,6 +2449,165 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep, bool m
   return hi;
 }
 
+// ---------------------------------------------------------------------------
+// Key histogram search (bf16 rows whose truncation hit): a bf16 logit has a
+// 16-bit order key, and the survivors [t, max] of a row span few of them
+// (a few hundred on Gaussian rows). One pass over the own lists counts every
+// key; the row's counts (merged over the cluster through distributed shared
+// memory) then give the top-k boundary directly: the bin where the count
+// from the top reaches k is z_mn, its count N_zmn, and k - count(above) of
+// its copies are kept. It is the quaternary search with a pivot at every
+// key of the range, which ends in one round. Top-p over S_k follows from the
+// same counts: a bin's mass is its count times the fixed-point weight of its
+// one value (the boundary bin counts only the copies top-k keeps).
+// Layout in the ring's bytes (idle after the streaming pass): this CTA's
+// counts, then the row's counts (C > 1).
+// ---------------------------------------------------------------------------
+constexpr int kKeyHistBins = 2048;
+static_assert(2 * kKeyHistBins * 4 <= kRingBytes, "the key histograms fit the ring's bytes");
+
+// 16-bit order key of a logit widened from bf16 (the top half of its 32-bit
+// key), and back to the value.
+__device__ __forceinline__ uint32_t key16_of(float x) { return f2key(x) >> 16; }
+__device__ __forceinline__ float value_of_key16(uint32_t k16) {
+  const uint32_t b = (k16 & 0x8000u) ? (k16 ^ 0x8000u) : (~k16 & 0xFFFFu);
+  return __uint_as_float(b << 16);
+}
+
+// Exclusive scan of a per-thread 64-bit value over the block, in thread order.
+__device__ __forceinline__ unsigned long long block_excl_scan_u64(Fixed& F, unsigned long long v,
+                                                                  unsigned long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) F.lred[1][warp][0].mass = incl;
+  __syncthreads();
+  unsigned long long wbase = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const unsigned long long s = vld(F.lred[1][w][0].mass);
+    wbase += (w < warp) ? s : 0ull;
+    tot += s;
+  }
+  __syncthreads();
+  *total = tot;
+  return wbase + incl - v;
+}
+
+struct KeyHist {
+  uint32_t tau_k, nk_k, above_k;     // top-k boundary key, copies kept, count above
+  uint32_t tau, n_keep, count_above;  // the final boundary (after top-p)
+  unsigned long long z;               // Z_k (fixed point) when top-p ran
+};
+
+// base16: the 16-bit key of the smallest bf16 >= t (every own-list entry is
+// at or above it); span: keys base16 .. key16(row max). Every thread of every
+// CTA of the row returns the same result; F.ties holds each rank's count of
+// the final boundary value.
+template <int DT>
+__device__ KeyHist keyhist_select(Ctx<DT>& c, uint32_t kk, bool p_on, float pr, uint32_t base16, uint32_t span) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t* lh = reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr));
+  uint32_t* rh = c.C > 1 ? lh + kKeyHistBins : lh;
+  __syncthreads();  // earlier users of the ring's bytes are done
+  for (uint32_t i = tid; i < span; i += kThreads) lh[i] = 0u;
+  __syncthreads();
+  own_for(c, [&](float x, uint32_t) {
+    const uint32_t b = key16_of(x) - base16;
+    // lanes holding the same key add once (ties are common in bf16 rows)
+    const uint32_t am = __activemask();
+    const uint32_t peers = __match_any_sync(am, b);
+    if (lane == __ffs(peers) - 1 && b < span) atomicAdd(&lh[b], static_cast<uint32_t>(__popc(peers)));
+  });
+  if (c.C > 1) {
+    cluster_sync_all();  // every CTA's counts are complete
+    for (uint32_t i = tid; i < span; i += kThreads) {
+      uint32_t sum = 0;
+      for (uint32_t r = 0; r < c.C; ++r) sum += ld_dsmem_u32(map_rank(smem_u32(&lh[i]), r));
+      rh[i] = sum;
+    }
+  }
+  __syncthreads();
+  // bins from the top: j = span - 1 - b; thread t holds j in [t P, t P + P)
+  const uint32_t P = (span + kThreads - 1) / kThreads;
+  const uint32_t j0 = min(static_cast<uint32_t>(tid) * P, span), j1 = min(j0 + P, span);
+  uint32_t mine = 0;
+  for (uint32_t j = j0; j < j1; ++j) mine += vld(rh[span - 1 - j]);
+  uint32_t tot = 0;
+  const uint32_t excl = block_excl_scan(F, mine, &tot);
+  {
+    uint32_t above = excl;
+    for (uint32_t j = j0; j < j1; ++j) {
+      const uint32_t n = vld(rh[span - 1 - j]);
+      if (above < kk && kk <= above + n) {
+        F.bc.u[BU_TAU] = j;
+        F.bc.u[BU_CABOVE] = above;
+      }
+      above += n;
+    }
+  }
+  __syncthreads();
+  const uint32_t jk = vld(F.bc.u[BU_TAU]);
+  KeyHist h;
+  h.above_k = vld(F.bc.u[BU_CABOVE]);
+  h.nk_k = kk - h.above_k;
+  h.tau_k = f2key(value_of_key16(base16 + (span - 1 - jk)));
+  h.tau = h.tau_k;
+  h.n_keep = h.nk_k;
+  h.count_above = h.above_k;
+  h.z = 0ull;
+  uint32_t jf = jk;  // the final boundary's bin (from the top)
+  if (p_on) {
+    // masses of the bins of S_k: count x weight of the bin's value
+    const float scale = c.fix_scale;
+    unsigned long long mm = 0ull;
+    for (uint32_t j = j0; j < j1 && j <= jk; ++j) {
+      const uint32_t n = j < jk ? vld(rh[span - 1 - j]) : h.nk_k;
+      if (n != 0u) mm += static_cast<unsigned long long>(n) *
+                         weight_fx(value_of_key16(base16 + (span - 1 - j)), c.m, c.m_neginf, scale);
+    }
+    unsigned long long zk = 0ull;
+    const unsigned long long excl_m = block_excl_scan_u64(F, mm, &zk);
+    const unsigned long long target = f2_to_u64(f2_mul(f2_from_u64(zk), pr));
+    {
+      unsigned long long am = excl_m;
+      uint32_t ac = excl;
+      for (uint32_t j = j0; j < j1 && j <= jk; ++j) {
+        const uint32_t n = j < jk ? vld(rh[span - 1 - j]) : h.nk_k;
+        if (n == 0u) continue;
+        const unsigned long long w = weight_fx(value_of_key16(base16 + (span - 1 - j)), c.m, c.m_neginf, scale);
+        const unsigned long long mj = static_cast<unsigned long long>(n) * w;
+        if (am < target && target <= am + mj) {
+          F.bc.u[BU_NP] = j;
+          F.bc.u[BU_CHI] = ac;
+          F.bc.u[BU_NKEEP] = copies_fx(target - am, w, n);
+        }
+        am += mj;
+        ac += n;
+      }
+    }
+    __syncthreads();
+    jf = vld(F.bc.u[BU_NP]);
+    h.tau = f2key(value_of_key16(base16 + (span - 1 - jf)));
+    h.count_above = vld(F.bc.u[BU_CHI]);
+    h.n_keep = vld(F.bc.u[BU_NKEEP]);
+    h.z = zk;
+  }
+  // each rank's copies of the final boundary value
+  const uint32_t bf = span - 1 - jf;
+  if (tid < static_cast<int>(c.C)) {
+    F.ties[tid] = c.C > 1 ? ld_dsmem_u32(map_rank(smem_u32(&lh[bf]), static_cast<uint32_t>(tid))) : vld(lh[bf]);
+  }
+  if (c.C > 1) cluster_sync_all();  // no CTA reuses its counts while another may read them
+  else __syncthreads();
+  return h;
+}
+
 // Row of cluster slot `slot` when heavy rows go first: rows whose top-p runs
 // alone (their streaming pass weighs every logit, and most take more passes)
 // take the first slots, then the others, each group in row order, so the
@@ -2755,8 +2914,10 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   // (a threshold the sample chose: the pivots split [t, m_ref] evenly, the
   // Gaussian model having failed for the row)
   const bool sample_t = vld(F.bc.u[BU_SAMPLE_T]) != 0u;
+  // (bf16 rows place the boundary with the key histogram instead)
   const bool bracket = trunc && k_on && !p_only && value_pivots && sigma > 0.f && isfinite(sigma) &&
-                       isfinite(mu) && isfinite(m_ref) && (P.flags & QRITA_FLAG_FORCE_FALLBACK) == 0u;
+                       isfinite(mu) && isfinite(m_ref) && (P.flags & QRITA_FLAG_FORCE_FALLBACK) == 0u &&
+                       !(DT == QRITA_DTYPE_BF16 && (P.flags & QRITA_FLAG_NO_KEY_HIST) == 0u);
   if (bracket && tid < 16) {
     float q = INFINITY;
     if (tid < kBracket) {
@@ -3149,6 +3310,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
 
     bool k_full = false;  // the own lists hold every element of S_k above tau_k
     uint32_t tau_k = 0, nk_k = 0, above_k = 0;
+    bool kh_done = false;  // the key histogram placed both boundaries
+    uint32_t kh_final_tau = 0, kh_final_keep = 0, kh_final_above = 0;
     if (k_on) {
       const uint32_t target = static_cast<uint32_t>(kr);
       const bool hit = trunc && !overflow && !force_fb && !force_retry && survivors >= target;
@@ -3161,7 +3324,27 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       bool searched = false;  // the search ran on the own lists' survivors
       uint32_t qk = 0, S2 = 0;
       bool ovf2 = true;
-      if (hit && bracket) {
+      // bf16 rows whose survivors span at most kKeyHistBins keys: one
+      // histogram of the keys replaces the pivot rounds (and top-p over S_k)
+      const uint32_t kh_base = DT == QRITA_DTYPE_BF16 && trunc ? key16_of(__uint_as_float(bf16_ceil_bits(t) << 16)) : 0u;
+      const uint32_t kh_top = DT == QRITA_DTYPE_BF16 ? key16_of(row_max) : 0u;
+      const bool kh = DT == QRITA_DTYPE_BF16 && hit && (P.flags & QRITA_FLAG_NO_KEY_HIST) == 0u &&
+                      kh_top >= kh_base && kh_top - kh_base < static_cast<uint32_t>(kKeyHistBins);
+      if (kh) {
+        const KeyHist h = keyhist_select<DT>(c, target, p_on, pr, kh_base, kh_top - kh_base + 1u);
+        path |= QRITA_PATH_KEYHIST;
+        s.tau = h.tau_k;
+        s.n_keep = h.nk_k;
+        s.count_above = h.above_k;
+        s.rounds = 1;
+        s.capped = false;
+        kh_final_tau = h.tau;
+        kh_final_keep = h.n_keep;
+        kh_final_above = h.count_above;
+        z_used = h.z;
+        kh_done = true;
+        searched = true;
+      } else if (hit && bracket) {
         // Z_t is in the own lists, and the merged bracket counts place the
         // boundary: lane j totals pivot j over the ranks; the largest j whose
         // count reaches k is lo, the next pivot hi (counts fall with j)
@@ -3302,6 +3485,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       n_keep = nk_k;
       count_above = above_k;
       ties_known = !sel_none;
+      if (kh_done) {
+        tau = kh_final_tau;
+        n_keep = kh_final_keep;
+        count_above = kh_final_above;
+        if (p_on) rounds_p = 1u;
+      }
     }
 
     QRITA_T(4);
@@ -3321,7 +3510,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         extracted_above_k = true;
       }
     }
-    if (p_on && !sel_none) {
+    if (p_on && !sel_none && !kh_done) {
       const float scale = c.fix_scale;
       if (k_on && k_full) {
         // top-p over S_k, all of it in the own lists:
