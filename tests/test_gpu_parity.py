@@ -315,10 +315,58 @@ def test_key_histogram_places_bf16_boundaries(dev, n, cl):
     flags = q.flag_cluster(cl) if cl else 0
     fails, flagged, got, st, info = check_against_oracle(logits, w.dtype, k, p, dev, flags=flags)
     assert fails == [], fails[:5]
-    hit = ((info["path"] & q.PATH_HIT) != 0) & ((info["path"] & q.PATH_TOPK) != 0)
+    topk = (info["path"] & q.PATH_TOPK) != 0
+    hit = ((info["path"] & q.PATH_HIT) != 0) & topk
     kh = (info["path"] & q.PATH_KEYHIST) != 0
     assert hit.sum() >= 8
-    assert (kh == hit).all()
+    assert (kh[topk] == hit[topk]).all()
+
+
+@pytest.mark.parametrize("cl", [0, 1, 2, 4])
+def test_key_window_places_bf16_top_p_rows(dev, cl):
+    """bf16 rows whose top-p runs alone over far more survivors than the lists
+    hold count a window of 16-bit keys in the streaming pass and place the
+    boundary from those exact bins (no extraction pass, no search rounds)."""
+    import top_selection_row_gb300 as q
+
+    w = WORKLOADS[5]
+    logits, k, p = workload(5, 48)
+    flags = q.flag_cluster(cl) if cl else 0
+    fails, flagged, got, st, info = check_against_oracle(logits, w.dtype, k, p, dev, flags=flags)
+    assert fails == [], fails[:5]
+    p_only = (k >= w.V) & (p < 1.0)
+    assert p_only.sum() >= 4
+    kw = (info["path"] & q.PATH_KEYHIST) != 0
+    assert kw[p_only].all()
+    assert (info["passes"][p_only] == 1).all()
+
+
+@pytest.mark.parametrize("case", ["above_window", "huge_tie_group", "negative_logits"])
+def test_key_window_gives_way(dev, case):
+    """Rows the key window cannot settle are still exact: a boundary among
+    outliers far above the window, a tie group at the boundary larger than
+    the emission collects, rows of negative logits only."""
+    import top_selection_row_gb300 as q
+    from workloads import f32_to_bf16_bits
+
+    rng = np.random.default_rng({"above_window": 1, "huge_tie_group": 2, "negative_logits": 3}[case])
+    B, V = 6, 60000
+    if case == "above_window":
+        x = rng.standard_normal((B, V)).astype(np.float32)
+        for r in range(B):
+            x[r, rng.choice(V, 4, replace=False)] = np.float32(60.0 + r)
+        p = np.array([0.3, 0.5, 0.9, 0.99, 0.2, 0.7], np.float32)
+    elif case == "huge_tie_group":
+        x = (np.round(rng.standard_normal((B, V)) * 2) / 2).astype(np.float32)
+        p = np.array([0.3, 0.5, 0.6, 0.7, 0.8, 0.95], np.float32)
+    else:
+        x = (rng.standard_normal((B, V)) - 40.0).astype(np.float32)
+        p = np.array([0.5, 0.8, 0.9, 0.95, 0.99, 0.6], np.float32)
+    logits = f32_to_bf16_bits(x)
+    k = np.full(B, V, np.int32)
+    for flags in (q.flag_cluster(1), q.flag_cluster(2)):
+        fails, flagged, got, st, info = check_against_oracle(logits, "bf16", k, p, dev, flags=flags)
+        assert fails == [], (case, flags, fails[:5])
 
 
 def test_key_histogram_gives_way_on_wide_bf16_rows(dev):

@@ -66,6 +66,18 @@ __device__ __forceinline__ uint32_t bf2_ge_mask(uint32_t a, uint32_t b) {
   return r;
 }
 
+__device__ __forceinline__ uint32_t bf2_gt_mask(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t bf2_eq_mask(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("set.eq.u32.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // The smallest bf16 value c >= t (t finite fp32), as raw bits: for bf16 x,
 // x >= t exactly when x >= c. Truncating t's low half moves it toward zero:
 // up for negative t, down for positive t, so only a positive inexact t steps

@@ -270,11 +270,11 @@ enum : int {
   // uints
   BU_TRUNC = 0, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
   BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS, BU_S2, BU_OVF2,
-  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW, BU_SAMPLE_T,
+  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW, BU_SAMPLE_T, BU_KWCA, BU_KWCB,
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
   // float pairs
-  BP_ZR = 0, BP_MR, BP_MLO, BP_MHI, BP_TOTAL,
+  BP_ZR = 0, BP_MR, BP_MLO, BP_MHI, BP_TOTAL, BP_GAP,
 };
 
 __device__ __forceinline__ void put_pair(Bcast& b, int i, F2 v) {
@@ -2608,6 +2608,283 @@ __device__ KeyHist keyhist_select(Ctx<DT>& c, uint32_t kk, bool p_on, float pr, 
   return h;
 }
 
+// ---------------------------------------------------------------------------
+// Key window for bf16 rows whose top-p runs alone over far more survivors than
+// the lists hold. The streaming pass counts the logits of a window of 16-bit
+// keys (from the bulk's top down to kKwBins keys, not below t) in a histogram
+// of the CTA's own; a window bin holds one value, so its mass is its count
+// times the fixed-point weight of that value, exact. The logits outside the
+// window are weighed one by one (their sum, and apart the sum above the
+// window, are constant offsets of the search). After the pass the bin where
+// the mass from the top reaches p Z is the boundary (z_mn, its count N_zmn)
+// with no extraction and no further search, and one emission pass writes the
+// mask: everything above the boundary value, the boundary's copies
+// provisionally, the ties beyond the lowest-index ones cleared afterwards.
+// A boundary outside the window falls back to the narrowing passes.
+// Layout in the list region while it runs: this CTA's counts, then (C > 1)
+// the row's counts; during the emission the tie indices and a radix histogram.
+// ---------------------------------------------------------------------------
+constexpr int kKwBins = 4096;
+constexpr uint32_t kKwHeadroom = 256;   // keys of the window above the bulk's top
+constexpr uint32_t kKwTieCap = 4096;    // tie indices the emission collects
+static_assert(2 * kKwBins * 4 <= kOwnCap * 8, "the key window's histograms fit the list region");
+// |x| < 2^-8 holds most of the 16-bit keys (every small binade): a window
+// that straddles zero leaves those keys out as a gap, weighed one by one
+constexpr uint32_t kKeyPosGap = 0xBB80u;  // key of +2^-8
+constexpr uint32_t kKeyNegGap = 0x447Fu;  // key of -2^-8
+
+// The window: keys lo0 .. lo0 + bot_span - 1 (bottom part), a gap of
+// blob_len keys, then top_span keys (top part). Bins hold the bottom part,
+// then the top part, each in increasing key order.
+struct KeyWindow {
+  uint32_t lo0, bot_span, blob_len, top_span;
+};
+
+// The window for keys k_t (smallest bf16 >= t) .. k_hi; false when it cannot
+// be placed (its top inside the gap).
+__device__ __forceinline__ bool key_window(uint32_t k_t, uint32_t k_hi, KeyWindow& w) {
+  const uint32_t nb = static_cast<uint32_t>(kKwBins);
+  if (k_hi < k_t || (k_hi > kKeyNegGap && k_hi < kKeyPosGap)) return false;
+  w.bot_span = 0u;
+  w.blob_len = 0u;
+  if (k_hi <= kKeyNegGap || k_t >= kKeyPosGap) {
+    w.lo0 = k_hi - k_t >= nb ? k_hi - (nb - 1u) : k_t;
+    w.top_span = k_hi - w.lo0 + 1u;
+    return true;
+  }
+  // the top part from +2^-8 (or less when the budget runs out), then below
+  // the gap as many negative keys as the budget leaves, not below t
+  const uint32_t top_lo = k_hi - kKeyPosGap >= nb ? k_hi - (nb - 1u) : kKeyPosGap;
+  w.top_span = k_hi - top_lo + 1u;
+  w.lo0 = top_lo;
+  const uint32_t room = nb - w.top_span;
+  if (k_t <= kKeyNegGap && room > 0u && top_lo == kKeyPosGap) {
+    const uint32_t bot_lo = kKeyNegGap - k_t >= room ? kKeyNegGap - (room - 1u) : k_t;
+    w.bot_span = kKeyNegGap - bot_lo + 1u;
+    w.blob_len = top_lo - kKeyNegGap - 1u;
+    w.lo0 = bot_lo;
+  }
+  return true;
+}
+
+// Key of bin b of the window.
+__device__ __forceinline__ uint32_t window_key(const KeyWindow& w, uint32_t b) {
+  return w.lo0 + (b < w.bot_span ? b : b + w.blob_len);
+}
+
+// Boundary of a top-p-alone bf16 row from the key window. Zo: softmax sum
+// (shift m_ref) of the logits outside the window bins; Ma / ca: mass and count
+// of those above the window; Mb / cb: of those in the gap; cf = exp(m_ref -
+// m). Returns false (uniformly) when the boundary lies outside the bins. On
+// success h holds the boundary and F.ties each rank's count of its value.
+template <int DT>
+__device__ bool kw_select(Ctx<DT>& c, float pr, const KeyWindow& kw, F2 Zo, F2 Ma, uint32_t ca, F2 Mb, uint32_t cb,
+                          float cf, KeyHist& h) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x;
+  const uint32_t nb = kw.bot_span + kw.top_span;
+  uint32_t* lh = reinterpret_cast<uint32_t*>(c.lists);
+  uint32_t* rh = c.C > 1 ? lh + kKwBins : lh;
+  // -0 and +0 are one value: their keys (0x7FFF, 0x8000) share one bin
+  // (both lie in one part only when that part spans zero without a gap)
+  if (tid == 0 && kw.bot_span == 0u && kw.lo0 <= 0x7FFFu && 0x8000u - kw.lo0 < kw.top_span) {
+    lh[0x8000u - kw.lo0] += lh[0x7FFFu - kw.lo0];
+    lh[0x7FFFu - kw.lo0] = 0u;
+  }
+  if (c.C > 1) {
+    cluster_sync_all();  // every CTA's counts are complete
+    for (uint32_t i = tid; i < nb; i += kThreads) {
+      uint32_t sum = 0;
+      for (uint32_t r = 0; r < c.C; ++r) sum += ld_dsmem_u32(map_rank(smem_u32(&lh[i]), r));
+      rh[i] = sum;
+    }
+  }
+  __syncthreads();
+  const float scale = c.fix_scale;
+  const unsigned long long z_out = f2_to_u64(f2_mul(f2_mul(Zo, cf), scale));
+  const unsigned long long m_top = f2_to_u64(f2_mul(f2_mul(Ma, cf), scale));
+  const unsigned long long m_gap = f2_to_u64(f2_mul(f2_mul(Mb, cf), scale));
+  // bins from the top: j = nb - 1 - b (the top part first, then past the gap
+  // the bottom part); thread t holds j in [t P, t P + P)
+  const uint32_t P = (nb + kThreads - 1) / kThreads;
+  const uint32_t j0 = min(static_cast<uint32_t>(tid) * P, nb), j1 = min(j0 + P, nb);
+  auto bin_w = [&](uint32_t j) -> unsigned long long {
+    return weight_fx(value_of_key16(window_key(kw, nb - 1 - j)), c.m, c.m_neginf, scale);
+  };
+  unsigned long long mm = 0ull, mm_top = 0ull;
+  uint32_t cc = 0;
+  for (uint32_t j = j0; j < j1; ++j) {
+    const uint32_t n = vld(rh[nb - 1 - j]);
+    if (n != 0u) {
+      const unsigned long long mj = static_cast<unsigned long long>(n) * bin_w(j);
+      mm += mj;
+      mm_top += j < kw.top_span ? mj : 0ull;
+      cc += n;
+    }
+  }
+  unsigned long long wtot = 0ull, wtop = 0ull;
+  const unsigned long long excl_m = block_excl_scan_u64(F, mm, &wtot);
+  (void)block_excl_scan_u64(F, mm_top, &wtop);
+  uint32_t ctot = 0;
+  const uint32_t excl_c = block_excl_scan(F, cc, &ctot);
+  const unsigned long long target = f2_to_u64(f2_mul(f2_from_u64(z_out + wtot), pr));
+  // the boundary must lie in the bins: above the window the mass stays below
+  // the target; the top part, or past the gap the bottom part, reaches it
+  const bool in_top = m_top < target && target <= m_top + wtop;
+  const bool in_bot = kw.bot_span > 0u && m_top + wtop + m_gap < target && target <= m_top + wtot + m_gap;
+  if (!(in_top || in_bot)) return false;
+  {
+    unsigned long long am = m_top + excl_m + (j0 >= kw.top_span ? m_gap : 0ull);
+    uint32_t ac = ca + excl_c + (j0 >= kw.top_span ? cb : 0u);
+    for (uint32_t j = j0; j < j1; ++j) {
+      if (j == kw.top_span && j != j0) {  // crossing the gap inside this thread's bins
+        am += m_gap;
+        ac += cb;
+      }
+      const uint32_t n = vld(rh[nb - 1 - j]);
+      if (n == 0u) continue;
+      const unsigned long long w = bin_w(j);
+      const unsigned long long mj = static_cast<unsigned long long>(n) * w;
+      if (am < target && target <= am + mj) {
+        F.bc.u[BU_NP] = j;
+        F.bc.u[BU_CHI] = ac;
+        F.bc.u[BU_NKEEP] = copies_fx(target - am, w, n);
+      }
+      am += mj;
+      ac += n;
+    }
+  }
+  __syncthreads();
+  const uint32_t jf = vld(F.bc.u[BU_NP]);
+  const uint32_t bf = nb - 1 - jf;
+  h.tau = f2key(value_of_key16(window_key(kw, bf)));
+  h.count_above = vld(F.bc.u[BU_CHI]);
+  h.n_keep = vld(F.bc.u[BU_NKEEP]);
+  h.z = z_out + wtot;
+  h.tau_k = h.tau;
+  h.nk_k = h.n_keep;
+  h.above_k = h.count_above;
+  if (tid < static_cast<int>(c.C)) {
+    F.ties[tid] = c.C > 1 ? ld_dsmem_u32(map_rank(smem_u32(&lh[bf]), static_cast<uint32_t>(tid))) : vld(lh[bf]);
+  }
+  if (c.C > 1) cluster_sync_all();  // no CTA reuses its counts while another may read them
+  else __syncthreads();
+  return true;
+}
+
+// Mask emission of a key-window row (bf16): one pass over the chunk writes 1
+// above tau and, when some of the boundary's copies are kept here, 1 for
+// every copy while collecting their indices; then the copies from the
+// keep_local-th lowest index on are cleared. Returns false (uniformly, and
+// before any clearing) when the copies exceed what it can collect: the caller
+// then writes the whole chunk again with the ties ranked in index order.
+template <int DT>
+__device__ bool kw_emit(Ctx<DT>& c, float tau_f, int tie_mode, uint32_t keep_local) {
+  Fixed& F = *c.F;
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t* tix = reinterpret_cast<uint32_t*>(c.lists);
+  uint32_t* rhist = tix + kKwTieCap;
+  const uint32_t tb = __float_as_uint(tau_f) >> 16;  // tau is a bf16 value
+  const uint32_t tau2 = tb | (tb << 16);
+  const bool want_eq = tie_mode != 0, collect = tie_mode == 2;
+  const uintptr_t mbp = reinterpret_cast<uintptr_t>(c.gmask + c.head_n);
+  const bool vec_ok = (mbp % 8u) == 0u;
+  if (tid == 0) F.tail_n = 0u;
+  // (stream_pieces opens with a block barrier: the reset is seen)
+  auto push_ties = [&](uint32_t eqbits, uint32_t idx0) {
+    // lanes with copies append their indices (rare: one value of the row)
+    const uint32_t cnt = __popc(eqbits);
+    const uint32_t am = __activemask();
+    uint32_t incl = cnt;
+    const uint32_t bal = __ballot_sync(am, cnt != 0u);
+    if (bal == 0u) return;
+    const int leader = __ffs(bal) - 1;
+    // positions: an exclusive prefix over the active lanes by shuffles
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(am, incl, o);
+      if (lane >= o && ((am >> (lane - o)) & 1u)) incl += y;
+    }
+    const uint32_t tot = __shfl_sync(am, incl, 31 - __clz(am));
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(&F.tail_n, tot);
+    base = __shfl_sync(am, base, leader);
+    uint32_t pos = base + incl - cnt;
+    uint32_t b = eqbits;
+    while (b != 0u) {
+      const int q = __ffs(b) - 1;
+      b &= b - 1u;
+      if (pos < kKwTieCap) tix[pos] = idx0 + static_cast<uint32_t>(bf16_bit_elem(q));
+      ++pos;
+    }
+  };
+  stream_pieces<DT>(
+      c,
+      [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
+#pragma unroll
+        for (int j = 0; j < kPieceThreadUnits; ++j) {
+          uint32_t eqbits = 0u;
+          const uint32_t idx0 = static_cast<uint32_t>(c.head_n + (u0 + j * kThreads + tid) * 8);
+          if (j * kThreads + tid < n) {
+            const uint4 u = v[j];
+            uint32_t e0 = 0u, e1 = 0u, e2 = 0u, e3 = 0u;
+            if (want_eq) {
+              e0 = bf2_eq_mask(u.x, tau2);
+              e1 = bf2_eq_mask(u.y, tau2);
+              e2 = bf2_eq_mask(u.z, tau2);
+              e3 = bf2_eq_mask(u.w, tau2);
+            }
+            const uint32_t m0 = bf2_gt_mask(u.x, tau2) | e0, m1 = bf2_gt_mask(u.y, tau2) | e1;
+            const uint32_t m2 = bf2_gt_mask(u.z, tau2) | e2, m3 = bf2_gt_mask(u.w, tau2) | e3;
+            // element 2i is word i's low half, 2i + 1 its high half: bytes in order
+            const uint32_t lo4 = __byte_perm(m0, m1, 0x6420) & 0x01010101u;
+            const uint32_t hi4 = __byte_perm(m2, m3, 0x6420) & 0x01010101u;
+            uint8_t* dst = c.gmask + idx0;
+            if (vec_ok) {
+              *reinterpret_cast<uint2*>(dst) = make_uint2(lo4, hi4);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                dst[e] = static_cast<uint8_t>((lo4 >> (8 * e)) & 1u);
+                dst[4 + e] = static_cast<uint8_t>((hi4 >> (8 * e)) & 1u);
+              }
+            }
+            if (collect)
+              eqbits = (e0 & 0x00010001u) | (e1 & 0x00020002u) | (e2 & 0x00040004u) | (e3 & 0x00080008u);
+          }
+          if (collect) push_ties(eqbits, idx0);
+        }
+      },
+      [&](float x, uint32_t idx, bool valid) {
+        uint32_t eqb = 0u;
+        if (valid) {
+          c.gmask[idx] = (x > tau_f || (want_eq && x == tau_f)) ? 1 : 0;
+          eqb = (collect && x == tau_f) ? 1u : 0u;
+        }
+        if (collect) push_ties(eqb, idx);  // bit 0 decodes to element 0: the index itself
+      },
+      false, ring_stages(list_region_bytes(static_cast<int>(c.ocap)), (kKwTieCap + kThreads) * 4));
+  if (!collect) return true;
+  __syncthreads();
+  const uint32_t nt = vld(F.tail_n);
+  if (nt > kKwTieCap) return false;  // uniform: every thread read the same count
+  if (keep_local >= nt) return true;
+  // the keep_local-th lowest index is the (nt + 1 - keep_local)-th largest
+  constexpr int kPer = kKwTieCap / kThreads;
+  uint32_t key[kPer];
+  bool have[kPer];
+#pragma unroll
+  for (int q = 0; q < kPer; ++q) {
+    const uint32_t i = static_cast<uint32_t>(tid + q * kThreads);
+    have[q] = i < nt;
+    key[q] = have[q] ? tix[i] : 0u;
+  }
+  const uint32_t kth = radix_select<DT, kPer>(c, key, have, nt + 1u - keep_local, rhist);
+#pragma unroll
+  for (int q = 0; q < kPer; ++q)
+    if (have[q] && key[q] > kth) c.gmask[key[q]] = 0;
+  return true;
+}
+
 // Row of cluster slot `slot` when heavy rows go first: rows whose top-p runs
 // alone (their streaming pass weighs every logit, and most take more passes)
 // take the first slots, then the others, each group in row order, so the
@@ -2949,10 +3226,28 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     const uint32_t per_warp = static_cast<uint32_t>(P.chunk) / kWarps + 32u;
     ph_scale = exp2f(static_cast<float>(__clz(per_warp)));
   }
+  // bf16 rows of that kind count a window of 16-bit keys instead (exact
+  // bins: see kw_select); the window reaches kKwHeadroom keys above the
+  // bulk's top and at most kKwBins keys down, never below t
+  bool kw = false;
+  KeyWindow kwin = {0u, 0u, 0u, 0u};
+  if (DT == QRITA_DTYPE_BF16 && ph && c.C <= 4u && (P.flags & QRITA_FLAG_NO_KEY_HIST) == 0u) {
+    const uint32_t k_t = key16_of(__uint_as_float(bf16_ceil_bits(t) << 16));
+    const uint32_t k_hi = min(key16_of(__uint_as_float(bf16_ceil_bits(ph_hi) << 16)) + kKwHeadroom, 0xFF7Fu);
+    if (key_window(k_t, k_hi, kwin)) {
+      kw = true;
+      ph = false;
+    }
+  }
+  const uint32_t kw_nb = kwin.bot_span + kwin.top_span;
   if (ph) {
     uint32_t* h = reinterpret_cast<uint32_t*>(c.lists);
     for (int i = tid; i < 2 * kWarps * kHistBins; i += kThreads) h[i] = 0u;
     // published by the streaming pass's first block barrier
+  }
+  if (kw) {
+    uint32_t* h = reinterpret_cast<uint32_t*>(c.lists);
+    for (uint32_t i = tid; i < kw_nb; i += kThreads) h[i] = 0u;
   }
 
   // ---- A4: the streaming pass (the one HBM read of the row)
@@ -3110,7 +3405,74 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           },
           true);
     };
-    if (ph) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<true>{});
+    // key-window rows: counts of the window's keys; every other logit weighed
+    // (shift m_ref) into the sum outside the window, and apart above it
+    F2 kw_out = {0.f, 0.f}, kw_top = {0.f, 0.f}, kw_gap = {0.f, 0.f};
+    uint32_t kw_ca = 0, kw_cb = 0, kw_ge_t = 0;
+    if constexpr (DT == QRITA_DTYPE_BF16) {
+      if (kw) {
+        uint32_t* kwh = reinterpret_cast<uint32_t*>(c.lists);
+        const uint32_t top_off = kwin.bot_span + kwin.blob_len;
+        const uint32_t top_end = top_off + kwin.top_span;
+        float pg = 0.f;  // the gap's partial of the current unit
+        auto kw_one = [&](float x, float& po, float& pa) {
+          const uint32_t k16 = key16_of(x);
+          const uint32_t d = k16 - kwin.lo0;  // wraps for keys below the window
+          const float w = exp_shifted(x, m_ref);
+          const bool in_bot = d < kwin.bot_span;
+          const bool in_top = d - top_off < kwin.top_span;
+          const bool gap = d >= kwin.bot_span && d < top_off;
+          const bool above = d >= top_end && k16 >= kwin.lo0;
+          if (in_bot || in_top) red_add_shared_u32(&kwh[in_bot ? d : d - kwin.blob_len], 1u);
+          po += (in_bot || in_top) ? 0.f : w;
+          pa += above ? w : 0.f;
+          pg += gap ? w : 0.f;
+          kw_ca += above ? 1u : 0u;
+          kw_cb += gap ? 1u : 0u;
+        };
+        stream_pieces<DT>(
+            c,
+            [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
+#pragma unroll
+              for (int j = 0; j < kPieceThreadUnits; ++j) {
+                if (j * kThreads + tid < n) {
+                  const uint4 u = v[j];
+                  vmax2 = bf2_max_nan(vmax2, bf2_max_nan(bf2_max_nan(u.x, u.y), bf2_max_nan(u.z, u.w)));
+                  vmin2 = bf2_min(vmin2, bf2_min(bf2_min(u.x, u.y), bf2_min(u.z, u.w)));
+                  kw_ge_t += __popc(bf16_unit_bits(u, t2));
+                  float xs[8];
+                  unpack<DT>(u, xs);
+                  float po = 0.f, pa = 0.f;
+                  pg = 0.f;
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) kw_one(xs[e], po, pa);
+                  f2_add(kw_out, po);
+                  f2_add(kw_top, pa);
+                  f2_add(kw_gap, pg);
+                }
+              }
+            },
+            [&](float x, uint32_t, bool valid) {
+              if (valid) {
+                vmax = fmax_nan(vmax, x);
+                vmin = fminf(vmin, x);
+                kw_ge_t += x >= t ? 1u : 0u;
+                float po = 0.f, pa = 0.f;
+                pg = 0.f;
+                kw_one(x, po, pa);
+                f2_add(kw_out, po);
+                f2_add(kw_top, pa);
+                f2_add(kw_gap, pg);
+              }
+            },
+            true);
+        zs = kw_out;
+        ms = kw_top;
+      }
+    }
+    if (kw) {
+      // handled above
+    } else if (ph) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<true>{});
     else if (p_only) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<false>{});
     else if (col) streaming_pass(BoolC<false>{}, BoolC<true>{}, BoolC<false>{});
     else streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{});
@@ -3138,6 +3500,40 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       }
       const uint32_t above = __shfl_down_sync(kFull, v, 1);  // bins lane + 1 .. 15
       if (lane < kBracket) F.slots[c.ph & 1].cnt[lane] = above;
+    }
+    uint32_t kw_ca_cta = 0, kw_cb_cta = 0;
+    if (kw) {
+      // survivors (x >= t) are counted, none is in the own list (the merge
+      // sees an overflow); the count above the window goes to the merge
+      const uint32_t wg = __reduce_add_sync(kFull, kw_ge_t), wa = __reduce_add_sync(kFull, kw_ca);
+      const uint32_t wb = __reduce_add_sync(kFull, kw_cb);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        kw_gap = f2_merge(kw_gap, f2_make(__shfl_xor_sync(kFull, kw_gap.hi, o), __shfl_xor_sync(kFull, kw_gap.lo, o)));
+      if (lane == 0) {
+        F.redu[warp][0] = wg;
+        F.redu[warp][1] = wa;
+        F.redu[warp][2] = wb;
+        F.redf[warp][6] = kw_gap.hi;
+        F.redf[warp][7] = kw_gap.lo;
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t a = 0, b = 0, g = 0;
+        F2 mg = {0.f, 0.f};
+        for (int w = 0; w < kWarps; ++w) {
+          a += vld(F.redu[w][0]);
+          b += vld(F.redu[w][1]);
+          g += vld(F.redu[w][2]);
+          mg = f2_merge(mg, f2_make(vld(F.redf[w][6]), vld(F.redf[w][7])));
+        }
+        F.own_n = a;
+        F.seg_ovf = 1u;
+        kw_ca_cta = b;
+        kw_cb_cta = g;
+        kw_gap = mg;
+      }
+      __syncthreads();
     }
     if (ph) {
       // this CTA's bin totals and its survivors above m_ref, read by the
@@ -3178,7 +3574,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       }
       __syncthreads();
     }
-    if (DT == QRITA_DTYPE_BF16 && !p_only) {
+    if (DT == QRITA_DTYPE_BF16 && (!p_only || kw)) {
       vmax = fmax_nan(vmax, fmax_nan(__uint_as_float(vmax2 << 16), __uint_as_float(vmax2 & 0xFFFF0000u)));
       vmin = fminf(vmin, fminf(__uint_as_float(vmin2 << 16), __uint_as_float(vmin2 & 0xFFFF0000u)));
     }
@@ -3217,6 +3613,10 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       my.f[1] = b;
       my.u[0] = trunc ? vld(F.seg_ovf) : 0u;
       my.u[1] = trunc ? vld(F.own_n) : 0u;
+      my.u[2] = kw_ca_cta;
+      my.u[3] = kw_cb_cta;
+      my.f[2] = kw_gap.hi;  // (thread 0 holds the CTA's gap mass)
+      my.f[3] = kw_gap.lo;
       my.pr[0] = z.hi;
       my.pr[1] = z.lo;
       my.pr[2] = mm.hi;
@@ -3231,8 +3631,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     }
     if (warp == 0) {
       float a = -INFINITY, b = INFINITY;
-      uint32_t surv = 0, ovf = 0;
-      F2 z = {0.f, 0.f}, mm = {0.f, 0.f};
+      uint32_t surv = 0, ovf = 0, kwc = 0, kwb = 0;
+      F2 z = {0.f, 0.f}, mm = {0.f, 0.f}, mg = {0.f, 0.f};
       if (lane < static_cast<int>(c.C)) {
         const uint32_t fb = map_rank(smem_u32(&my.f[0]), lane);
         a = ld_dsmem_f32(fb);
@@ -3240,6 +3640,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         const uint32_t ub = map_rank(smem_u32(&my.u[0]), lane);
         ovf = ld_dsmem_u32(ub);
         surv = ld_dsmem_u32(ub + 4);
+        kwc = ld_dsmem_u32(ub + 8);
+        kwb = ld_dsmem_u32(ub + 12);
+        mg = f2_make(ld_dsmem_f32(fb + 8), ld_dsmem_f32(fb + 12));
         const uint32_t pb = map_rank(smem_u32(&my.pr[0]), lane);
         z = f2_make(ld_dsmem_f32(pb), ld_dsmem_f32(pb + 4));
         mm = f2_make(ld_dsmem_f32(pb + 8), ld_dsmem_f32(pb + 12));
@@ -3251,6 +3654,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         a = fmax_nan(a, __shfl_xor_sync(kFull, a, o));
         b = fminf(b, __shfl_xor_sync(kFull, b, o));
         surv += __shfl_xor_sync(kFull, surv, o);
+        kwc += __shfl_xor_sync(kFull, kwc, o);
+        kwb += __shfl_xor_sync(kFull, kwb, o);
+        mg = f2_merge(mg, f2_make(__shfl_xor_sync(kFull, mg.hi, o), __shfl_xor_sync(kFull, mg.lo, o)));
         ovf |= __shfl_xor_sync(kFull, ovf, o);
         z = f2_merge(z, f2_make(__shfl_xor_sync(kFull, z.hi, o), __shfl_xor_sync(kFull, z.lo, o)));
         mm = f2_merge(mm, f2_make(__shfl_xor_sync(kFull, mm.hi, o), __shfl_xor_sync(kFull, mm.lo, o)));
@@ -3259,6 +3665,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         F.bc.f[BF_MAX] = a;
         F.bc.f[BF_MIN] = b;
         F.bc.u[BU_S] = surv;
+        F.bc.u[BU_KWCA] = kwc;
+        F.bc.u[BU_KWCB] = kwb;
+        put_pair(F.bc, BP_GAP, mg);
         F.bc.u[BU_OVF] = ovf;
         put_pair(F.bc, BP_ZR, z);
         put_pair(F.bc, BP_MR, mm);
@@ -3300,6 +3709,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   bool ties_in_list = false;  // every element equal to tau is in this CTA's own list
   bool ties_known = false;    // F.ties holds the per-rank tie counts
   bool ph_mask = false;       // the mask holds 1 above the own lists' range, 0 elsewhere
+  bool kw_done = false;       // the key window placed the top-p boundary (kw_emit writes the mask)
 
   if (!invalid && !keep_all) {
     // the streaming pass summed exp(x - m_ref); shift m is a factor exp(m_ref - m) away
@@ -3311,6 +3721,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     bool k_full = false;  // the own lists hold every element of S_k above tau_k
     uint32_t tau_k = 0, nk_k = 0, above_k = 0;
     bool kh_done = false;  // the key histogram placed both boundaries
+    kw_done = false;
     uint32_t kh_final_tau = 0, kh_final_keep = 0, kh_final_above = 0;
     if (k_on) {
       const uint32_t target = static_cast<uint32_t>(kr);
@@ -3582,7 +3993,26 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         }
       } else {
         // top-p only, or top-p over an S_k too large for the lists
-        const bool hit = !k_on && trunc && !overflow && !force_fb && ref_ok &&
+        // (key-window rows first: see kw_select)
+        if (kw && !k_on && ref_ok) {
+          KeyHist h;
+          if (kw_select<DT>(c, pr, kwin, Zr, Mr, vld(F.bc.u[BU_KWCA]), get_pair(F.bc, BP_GAP),
+                            vld(F.bc.u[BU_KWCB]), cf, h)) {
+            path |= QRITA_PATH_KEYHIST | QRITA_PATH_HIT;
+            tau = h.tau;
+            n_keep = h.n_keep;
+            count_above = h.count_above;
+            z_used = h.z;
+            rounds_p = 1u;
+            passes = 1u;  // the emission pass
+            ties_known = true;
+            kw_done = true;
+          }
+        }
+      }
+      if (!kw_done && !(k_on && k_full)) {
+        // top-p only, or top-p over an S_k too large for the lists
+        const bool hit = !k_on && trunc && !overflow && !force_fb && ref_ok && !kw &&
                          f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
         if (!k_on) path |= hit ? QRITA_PATH_HIT : QRITA_PATH_FALLBACK;
         Local s;
@@ -3614,7 +4044,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           R.m_lo = R.m_hi = 0ull;
           // top-p alone, truncation hit by mass but too many survivors: the
           // boundary lies above t, and the target is p Z from the streaming pass
-          const bool mass_hit = !k_on && trunc && !force_fb && ref_ok &&
+          // (key-window rows summed other quantities: narrow from the whole row)
+          const bool mass_hit = !k_on && trunc && !force_fb && ref_ok && !kw &&
                                 f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
           bool ph_done = false;
           if (ph && mass_hit) {
@@ -3850,7 +4281,13 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   QRITA_T(6);
 
   // ---- A9: mask emission
-  if (sel_all || sel_none || list_emit) {
+  bool kw_emitted = false;
+  if constexpr (DT == QRITA_DTYPE_BF16) {
+    if (kw_done && !sel_all && !sel_none) kw_emitted = kw_emit<DT>(c, tau_f, tie_mode, keep_local);
+  }
+  if (kw_emitted) {
+    // written
+  } else if (sel_all || sel_none || list_emit) {
     // fill the chunk's mask (unless the search tail zeroed it already), then
     // scatter the kept ids of the own list
     if (sel_all || sel_none || !(zero_filled || ph_mask)) fill_mask<DT>(c, sel_all ? 1 : 0);
