@@ -272,6 +272,15 @@ __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");
 }
 
+// Shared-memory add of 1, predicated in the instruction itself (no branch).
+__device__ __forceinline__ void red_inc_shared_if(uint32_t* p, bool cond) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q red.shared.add.u32 [%0], 1;\n\t}" ::"r"(
+          static_cast<uint32_t>(__cvta_generic_to_shared(p))),
+      "r"(cond ? 1u : 0u)
+      : "memory");
+}
+
 // Shared-memory add without a returned value.
 __device__ __forceinline__ void red_add_shared_u32(uint32_t* p, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(v)

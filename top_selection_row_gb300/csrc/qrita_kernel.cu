@@ -2640,26 +2640,27 @@ struct KeyWindow {
   uint32_t lo0, bot_span, blob_len, top_span;
 };
 
-// The window for keys k_t (smallest bf16 >= t) .. k_hi; false when it cannot
-// be placed (its top inside the gap).
-__device__ __forceinline__ bool key_window(uint32_t k_t, uint32_t k_hi, KeyWindow& w) {
+// The window below key k_hi: kKwBins keys down from it, leaving out the gap
+// when it straddles zero; false when it cannot be placed (its top inside the
+// gap). Logits below it are weighed one by one like those of the gap.
+__device__ __forceinline__ bool key_window(uint32_t k_hi, KeyWindow& w) {
   const uint32_t nb = static_cast<uint32_t>(kKwBins);
-  if (k_hi < k_t || (k_hi > kKeyNegGap && k_hi < kKeyPosGap)) return false;
+  if (k_hi > kKeyNegGap && k_hi < kKeyPosGap) return false;
   w.bot_span = 0u;
   w.blob_len = 0u;
-  if (k_hi <= kKeyNegGap || k_t >= kKeyPosGap) {
-    w.lo0 = k_hi - k_t >= nb ? k_hi - (nb - 1u) : k_t;
+  if (k_hi <= kKeyNegGap) {
+    w.lo0 = k_hi >= nb - 1u ? k_hi - (nb - 1u) : 0u;
     w.top_span = k_hi - w.lo0 + 1u;
     return true;
   }
   // the top part from +2^-8 (or less when the budget runs out), then below
-  // the gap as many negative keys as the budget leaves, not below t
+  // the gap as many negative keys as the budget leaves
   const uint32_t top_lo = k_hi - kKeyPosGap >= nb ? k_hi - (nb - 1u) : kKeyPosGap;
   w.top_span = k_hi - top_lo + 1u;
   w.lo0 = top_lo;
   const uint32_t room = nb - w.top_span;
-  if (k_t <= kKeyNegGap && room > 0u && top_lo == kKeyPosGap) {
-    const uint32_t bot_lo = kKeyNegGap - k_t >= room ? kKeyNegGap - (room - 1u) : k_t;
+  if (room > 0u && top_lo == kKeyPosGap) {
+    const uint32_t bot_lo = kKeyNegGap >= room - 1u ? kKeyNegGap - (room - 1u) : 0u;
     w.bot_span = kKeyNegGap - bot_lo + 1u;
     w.blob_len = top_lo - kKeyNegGap - 1u;
     w.lo0 = bot_lo;
@@ -3232,9 +3233,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   bool kw = false;
   KeyWindow kwin = {0u, 0u, 0u, 0u};
   if (DT == QRITA_DTYPE_BF16 && ph && c.C <= 4u && (P.flags & QRITA_FLAG_NO_KEY_HIST) == 0u) {
-    const uint32_t k_t = key16_of(__uint_as_float(bf16_ceil_bits(t) << 16));
     const uint32_t k_hi = min(key16_of(__uint_as_float(bf16_ceil_bits(ph_hi) << 16)) + kKwHeadroom, 0xFF7Fu);
-    if (key_window(k_t, k_hi, kwin)) {
+    if (key_window(k_hi, kwin)) {
       kw = true;
       ph = false;
     }
@@ -3414,25 +3414,59 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         uint32_t* kwh = reinterpret_cast<uint32_t*>(c.lists);
         const uint32_t top_off = kwin.bot_span + kwin.blob_len;
         const uint32_t top_end = top_off + kwin.top_span;
-        float pg = 0.f;  // the gap's partial of the current unit
-        auto kw_one = [&](float x, float& po, float& pa) {
-          const uint32_t k16 = key16_of(x);
-          const uint32_t d = k16 - kwin.lo0;  // wraps for keys below the window
-          const float w = exp_shifted(x, m_ref);
+        float po = 0.f, pa = 0.f, pg = 0.f;  // partials of the current piece
+        // logits outside the bins (below the window, in the gap, above it:
+        // rare) are weighed one by one; k: the 16-bit order key of raw h
+        auto kw_rare = [&](uint32_t k, uint32_t h) {
+          const uint32_t d = k - kwin.lo0;  // wraps for keys below the window
+          const float w = exp_shifted(__uint_as_float(h << 16), m_ref);
+          po += w;
+          if (k >= kwin.lo0) {
+            if (d >= top_end) {
+              pa += w;
+              ++kw_ca;
+            } else {
+              pg += w;
+              ++kw_cb;
+            }
+          }
+        };
+        // order keys of both halves of a packed word: x ^ 0xFFFF for negative
+        // halves, x ^ 0x8000 for the others (-0 keeps its own key; zeros lie
+        // in the gap)
+        auto keys2 = [](uint32_t w) -> uint32_t {
+          const uint32_t sgn = (w >> 15) & 0x00010001u;
+          return w ^ ((sgn * 0x7FFFu) | 0x80008000u);
+        };
+        // one key: counted in its bin (predicated, no branch), or marked rare
+        auto kw_key = [&](uint32_t k) -> bool {
+          const uint32_t d = k - kwin.lo0;
           const bool in_bot = d < kwin.bot_span;
-          const bool in_top = d - top_off < kwin.top_span;
-          const bool gap = d >= kwin.bot_span && d < top_off;
-          const bool above = d >= top_end && k16 >= kwin.lo0;
-          if (in_bot || in_top) red_add_shared_u32(&kwh[in_bot ? d : d - kwin.blob_len], 1u);
-          po += (in_bot || in_top) ? 0.f : w;
-          pa += above ? w : 0.f;
-          pg += gap ? w : 0.f;
-          kw_ca += above ? 1u : 0u;
-          kw_cb += gap ? 1u : 0u;
+          const bool in = in_bot || d - top_off < kwin.top_span;
+          red_inc_shared_if(&kwh[in_bot ? d : (in ? d - kwin.blob_len : 0u)], in);
+          return in;
+        };
+        auto kw_unit = [&](const uint4 u) {
+          const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
+          uint32_t rare = 0u;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t k2 = keys2(wv[i]);
+            rare |= kw_key(k2 & 0xFFFFu) ? 0u : (1u << (2 * i));
+            rare |= kw_key(k2 >> 16) ? 0u : (2u << (2 * i));
+          }
+          while (rare != 0u) {
+            const int e = __ffs(rare) - 1;
+            rare &= rare - 1u;
+            const uint32_t w = e < 2 ? u.x : (e < 4 ? u.y : (e < 6 ? u.z : u.w));
+            const uint32_t h = (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+            kw_rare(keys2(h) & 0xFFFFu, h);
+          }
         };
         stream_pieces<DT>(
             c,
             [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
+              po = pa = pg = 0.f;
 #pragma unroll
               for (int j = 0; j < kPieceThreadUnits; ++j) {
                 if (j * kThreads + tid < n) {
@@ -3440,30 +3474,26 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   vmax2 = bf2_max_nan(vmax2, bf2_max_nan(bf2_max_nan(u.x, u.y), bf2_max_nan(u.z, u.w)));
                   vmin2 = bf2_min(vmin2, bf2_min(bf2_min(u.x, u.y), bf2_min(u.z, u.w)));
                   kw_ge_t += __popc(bf16_unit_bits(u, t2));
-                  float xs[8];
-                  unpack<DT>(u, xs);
-                  float po = 0.f, pa = 0.f;
-                  pg = 0.f;
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) kw_one(xs[e], po, pa);
-                  f2_add(kw_out, po);
-                  f2_add(kw_top, pa);
-                  f2_add(kw_gap, pg);
+                  kw_unit(u);
                 }
               }
+              f2_add(kw_out, po);
+              f2_add(kw_top, pa);
+              f2_add(kw_gap, pg);
             },
             [&](float x, uint32_t, bool valid) {
+              po = pa = pg = 0.f;
               if (valid) {
                 vmax = fmax_nan(vmax, x);
                 vmin = fminf(vmin, x);
                 kw_ge_t += x >= t ? 1u : 0u;
-                float po = 0.f, pa = 0.f;
-                pg = 0.f;
-                kw_one(x, po, pa);
-                f2_add(kw_out, po);
-                f2_add(kw_top, pa);
-                f2_add(kw_gap, pg);
+                const uint32_t h = __float_as_uint(x) >> 16;
+                const uint32_t k = keys2(h) & 0xFFFFu;
+                if (!kw_key(k)) kw_rare(k, h);
               }
+              f2_add(kw_out, po);
+              f2_add(kw_top, pa);
+              f2_add(kw_gap, pg);
             },
             true);
         zs = kw_out;
