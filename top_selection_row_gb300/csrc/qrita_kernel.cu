@@ -507,17 +507,23 @@ __device__ __forceinline__ void fill_mask(Ctx<DT>& c, uint8_t fill) {
   if (tid < mt) c.gmask[mh + mb * 16 + tid] = fill;
 }
 
+// Byte offset of ring stage st from the standard ring: stages 0 .. kStages-1
+// are the standard ring; deeper rings add stages below it, stage kStages
+// right below, the next below that, and so on.
+__device__ __forceinline__ int stage_off(int st) {
+  return st < kStages ? st * kPieceBytes : -(st - kStages + 1) * kPieceBytes;
+}
+
 // Issue the bulk copy of piece `piece` of the chunk body into ring stage `st`
 // (thread 0 only).
-// base: shared address of stage 0 of the ring the current pass uses.
 template <int DT>
-__device__ __forceinline__ void ring_issue(Ctx<DT>& c, int piece, int st, uint32_t base) {
+__device__ __forceinline__ void ring_issue(Ctx<DT>& c, int piece, int st) {
   const int u0 = piece * kPieceUnits;
   const int n = min(kPieceUnits, c.body_units - u0);
   const uint32_t bar = c.ring_bar + 8u * st;
   const uint32_t bytes = static_cast<uint32_t>(n) * 16u;
   mbar_expect_tx(bar, bytes);
-  bulk_g2s(base + static_cast<uint32_t>(st) * kPieceBytes, c.gbody + 16 * static_cast<size_t>(u0), bytes, bar);
+  bulk_g2s(c.ring + static_cast<uint32_t>(stage_off(st)), c.gbody + 16 * static_cast<size_t>(u0), bytes, bar);
   c.ring_out |= 1u << st;
 }
 
@@ -555,12 +561,12 @@ __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, Sc
   const int tid = threadIdx.x;
   const int nb = c.body_units;
   const int npieces = (nb + kPieceUnits - 1) / kPieceUnits;
-  const uint32_t base = c.ring - static_cast<uint32_t>(nst - kStages) * kPieceBytes;
-  const uint4* base_ptr = c.ring_ptr - static_cast<size_t>(nst - kStages) * kPieceUnits;
-  if (!prefetched) fence_proxy_async_smem();  // generic writes to these bytes before the async copies
+  // generic writes to these bytes before the async copies (a prefetched pass
+  // still issues its stages below the standard ring here)
+  if (!prefetched || nst > kStages) fence_proxy_async_smem();
   __syncthreads();  // earlier users of the ring's bytes are done
-  if (tid == 0 && !prefetched && npieces > 0 && vld(F.err) == 0u) {
-    for (int pc = 0; pc < npieces && pc < nst; ++pc) ring_issue(c, pc, pc, base);
+  if (tid == 0 && npieces > 0 && vld(F.err) == 0u) {
+    for (int pc = prefetched ? kStages : 0; pc < npieces && pc < nst; ++pc) ring_issue(c, pc, pc);
   }
   int st = 0;
   for (int pc = 0; pc < npieces; ++pc, st = (st + 1 == nst) ? 0 : st + 1) {
@@ -583,7 +589,7 @@ __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, Sc
     }
     const int u0 = pc * kPieceUnits;
     const int n = min(kPieceUnits, nb - u0);
-    const uint4* sp = base_ptr + static_cast<size_t>(st) * kPieceUnits;
+    const uint4* sp = c.ring_ptr + stage_off(st) / 16;
     uint4 v[kPieceThreadUnits];
 #pragma unroll
     for (int j = 0; j < kPieceThreadUnits; ++j) {
@@ -591,7 +597,7 @@ __device__ __forceinline__ void stream_pieces(Ctx<DT>& c, PieceFn&& piece_fn, Sc
       v[j] = (u < n) ? sp[u] : make_uint4(0u, 0u, 0u, 0u);
     }
     __syncthreads();  // every thread holds its part of stage st: refill it now
-    if (tid == 0 && pc + nst < npieces && vld(F.err) == 0u) ring_issue(c, pc + nst, st, base);
+    if (tid == 0 && pc + nst < npieces && vld(F.err) == 0u) ring_issue(c, pc + nst, st);
     piece_fn(v, u0, n);
   }
   float x = 0.f;
@@ -3027,7 +3033,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       for (int st = 0; st < kMaxStages; ++st) mbar_init(c.ring_bar + 8u * st, 1u);
       fence_mbar_init();
       const int npieces = (c.body_units + kPieceUnits - 1) / kPieceUnits;
-      for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc, c.ring);
+      for (int pc = 0; pc < npieces && pc < kStages; ++pc) ring_issue(c, pc, pc);
     }
 #pragma unroll
     for (int j = 0; j < kPer; ++j) {
@@ -3272,6 +3278,24 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     const uint32_t colcap = c.ocap / kThreads;
     const bool col = !p_only && trunc && k_on &&
                      2.4f * static_cast<float>(kr) <= static_cast<float>(c.ocap / 8u) * static_cast<float>(c.C);
+    const int stream_nst = kStages;  // (deeper rings here measured no gain)
+    // top-k rows with truncation on one CTA write their mask's zeros during
+    // the pass (a lone CTA's stream is latency-bound, so the stores cost
+    // nothing there; rows split over a cluster stream at full bandwidth and
+    // zero the mask later): the emission then only scatters the kept ids from
+    // the lists; a row that ends on another path rewrites every byte
+    const bool zfill = !p_only && trunc && k_on && c.C == 1u;
+    const bool zvec = (reinterpret_cast<uintptr_t>(c.gmask + c.head_n) % E) == 0u;
+    auto zero_unit = [&](int u) {
+      uint8_t* dst = c.gmask + c.head_n + static_cast<size_t>(u) * E;
+      if (zvec) {
+        if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = 0u;
+        else *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) dst[e] = 0;
+      }
+    };
     auto col_put = [&](float x, uint32_t idx) {
       if (cn < colcap) {
         c.own_val[cn * kThreads + tid] = x;
@@ -3314,6 +3338,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   vmax2 = bf2_max_nan(vmax2, bf2_max_nan(bf2_max_nan(u.x, u.y), bf2_max_nan(u.z, u.w)));
                   vmin2 = bf2_min(vmin2, bf2_min(bf2_min(u.x, u.y), bf2_min(u.z, u.w)));
                   if (trunc) bits[j] = bf16_unit_bits(u, t2);
+                  if (zfill) zero_unit(u0 + j * kThreads + tid);
                 }
               }
               if constexpr (COL) {
@@ -3340,6 +3365,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               unpack<DT>(v[j], xs[j]);
               bits[j] = 0u;
               if (j * kThreads + tid < n) {
+                if (!PO && zfill) zero_unit(u0 + j * kThreads + tid);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                   const float x = xs[j][e];
@@ -3387,6 +3413,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               vmin = fminf(vmin, x);
               const bool surv = trunc && x >= t;
               bits = surv ? 1u : 0u;
+              if (!PO && zfill) c.gmask[idx] = 0;
               if constexpr (PO) {
                 const float w = exp_shifted(x, m_ref);
                 f2_add(zs, w);
@@ -3403,7 +3430,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               if (trunc) seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, bits);
             }
           },
-          true);
+          true, stream_nst);
     };
     // key-window rows: counts of the window's keys; every other logit weighed
     // (shift m_ref) into the sum outside the window, and apart above it
@@ -3495,7 +3522,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               f2_add(kw_top, pa);
               f2_add(kw_gap, pg);
             },
-            true);
+            true, stream_nst);
         zs = kw_out;
         ms = kw_top;
       }
@@ -3507,6 +3534,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     else if (col) streaming_pass(BoolC<false>{}, BoolC<true>{}, BoolC<false>{});
     else streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{});
     QRITA_T(2);
+    c.zero_fill_done = zfill;
     if (col) {
       own_columns_streamed<DT>(c, cn);
       own_columns_to_segments<DT>(c, cn);
@@ -3806,7 +3834,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           F.rank_hi[tid] = hi_piv ? vld(F.rank_bins[tid][js + 1]) : 0u;
         }
         __syncthreads();
-        c.zero_fill = true;  // the mask is all zeros but for the scattered kept ids
+        c.zero_fill = !c.zero_fill_done;  // the mask is all zeros but for the scattered kept ids
         dsearch<DT, false>(c, s, target, value_pivots);
         searched = true;
       } else if (hit) {
