@@ -2365,6 +2365,21 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
 // stays for the emission.
 constexpr uint32_t kTieDirect = 1024;
 constexpr uint32_t kTieCap = kRingBytes / 4;
+
+// The keep-th smallest of nt <= kThreads distinct indices tix[0 .. nt), plus
+// one: thread i ranks index i by counting the smaller ones (every thread
+// reads the same entry at each step, so the loads broadcast).
+__device__ __forceinline__ uint32_t small_index_cut(Fixed& F, const uint32_t* tix, uint32_t nt, uint32_t keep) {
+  const int tid = threadIdx.x;
+  const uint32_t mine = static_cast<uint32_t>(tid) < nt ? tix[tid] : 0xFFFFFFFFu;
+  uint32_t r = 0;
+  for (uint32_t j = 0; j < nt; ++j) r += tix[j] < mine ? 1u : 0u;
+  if (static_cast<uint32_t>(tid) < nt && r + 1u == keep) F.bc.u[BU_QKEY] = mine + 1u;
+  __syncthreads();
+  const uint32_t cut = vld(F.bc.u[BU_QKEY]);
+  __syncthreads();
+  return cut;
+}
 template <int DT>
 __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep, bool mark_above) {
   Fixed& F = *c.F;
@@ -2393,6 +2408,7 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep, bool m
   });
   __syncthreads();
   const uint32_t nt = vld(F.tail_n);
+  if (nt <= static_cast<uint32_t>(kThreads)) return small_index_cut(F, tix, nt, keep);
   if (nt <= kTieDirect) {
     // a small group: the keep-th smallest index (the (nt + 1 - keep)-th
     // largest) by a radix select over the indices, the histogram after them
@@ -2517,7 +2533,7 @@ struct KeyHist {
 template <int DT>
 __device__ KeyHist keyhist_select(Ctx<DT>& c, uint32_t kk, bool p_on, float pr, uint32_t base16, uint32_t span) {
   Fixed& F = *c.F;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   uint32_t* lh = reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr));
   uint32_t* rh = c.C > 1 ? lh + kKeyHistBins : lh;
   __syncthreads();  // earlier users of the ring's bytes are done
@@ -2525,10 +2541,7 @@ __device__ KeyHist keyhist_select(Ctx<DT>& c, uint32_t kk, bool p_on, float pr, 
   __syncthreads();
   own_for(c, [&](float x, uint32_t) {
     const uint32_t b = key16_of(x) - base16;
-    // lanes holding the same key add once (ties are common in bf16 rows)
-    const uint32_t am = __activemask();
-    const uint32_t peers = __match_any_sync(am, b);
-    if (lane == __ffs(peers) - 1 && b < span) atomicAdd(&lh[b], static_cast<uint32_t>(__popc(peers)));
+    red_inc_shared_if(&lh[b < span ? b : 0u], b < span);
   });
   if (c.C > 1) {
     cluster_sync_all();  // every CTA's counts are complete
@@ -2875,6 +2888,11 @@ __device__ bool kw_emit(Ctx<DT>& c, float tau_f, int tie_mode, uint32_t keep_loc
   const uint32_t nt = vld(F.tail_n);
   if (nt > kKwTieCap) return false;  // uniform: every thread read the same count
   if (keep_local >= nt) return true;
+  if (nt <= static_cast<uint32_t>(kThreads)) {
+    const uint32_t cut = small_index_cut(F, tix, nt, keep_local);
+    if (static_cast<uint32_t>(tid) < nt && tix[tid] >= cut) c.gmask[tix[tid]] = 0;
+    return true;
+  }
   // the keep_local-th lowest index is the (nt + 1 - keep_local)-th largest
   constexpr int kPer = kKwTieCap / kThreads;
   uint32_t key[kPer];
