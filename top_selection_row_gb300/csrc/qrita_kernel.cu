@@ -2756,7 +2756,10 @@ __device__ bool kw_select(Ctx<DT>& c, float pr, const KeyWindow& kw, F2 Zo, F2 M
   {
     unsigned long long am = m_top + excl_m + (j0 >= kw.top_span ? m_gap : 0ull);
     uint32_t ac = ca + excl_c + (j0 >= kw.top_span ? cb : 0u);
-    for (uint32_t j = j0; j < j1; ++j) {
+    // only the thread whose bins hold the target walks them
+    const unsigned long long end = am + mm + (j0 < kw.top_span && j1 > kw.top_span ? m_gap : 0ull);
+    const uint32_t jend = (am < target && target <= end) ? j1 : j0;
+    for (uint32_t j = j0; j < jend; ++j) {
       if (j == kw.top_span && j != j0) {  // crossing the gap inside this thread's bins
         am += m_gap;
         ac += cb;
@@ -2810,6 +2813,7 @@ __device__ bool kw_emit(Ctx<DT>& c, float tau_f, int tie_mode, uint32_t keep_loc
   const uintptr_t mbp = reinterpret_cast<uintptr_t>(c.gmask + c.head_n);
   const bool vec_ok = (mbp % 8u) == 0u;
   if (tid == 0) F.tail_n = 0u;
+  QRITA_T(11);
   // (stream_pieces opens with a block barrier: the reset is seen)
   auto push_ties = [&](uint32_t eqbits, uint32_t idx0) {
     // lanes with copies append their indices (rare: one value of the row)
@@ -2883,6 +2887,7 @@ __device__ bool kw_emit(Ctx<DT>& c, float tau_f, int tie_mode, uint32_t keep_loc
         if (collect) push_ties(eqb, idx);  // bit 0 decodes to element 0: the index itself
       },
       false, ring_stages(list_region_bytes(static_cast<int>(c.ocap)), (kKwTieCap + kThreads) * 4));
+  QRITA_T(12);
   if (!collect) return true;
   __syncthreads();
   const uint32_t nt = vld(F.tail_n);
@@ -3337,10 +3342,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
         ph_am += w;
       }
     };
-    auto streaming_pass = [&](auto po, auto cm, auto hc) {
+    auto streaming_pass = [&](auto po, auto cm, auto hc, auto zf) {
       constexpr bool PO = decltype(po)::value;
       constexpr bool COL = decltype(cm)::value;
       constexpr bool PH = decltype(hc)::value;
+      constexpr bool ZF = decltype(zf)::value;  // zero the mask while streaming
       stream_pieces<DT>(
           c,
           [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
@@ -3356,7 +3362,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   vmax2 = bf2_max_nan(vmax2, bf2_max_nan(bf2_max_nan(u.x, u.y), bf2_max_nan(u.z, u.w)));
                   vmin2 = bf2_min(vmin2, bf2_min(bf2_min(u.x, u.y), bf2_min(u.z, u.w)));
                   if (trunc) bits[j] = bf16_unit_bits(u, t2);
-                  if (zfill) zero_unit(u0 + j * kThreads + tid);
+                  if constexpr (ZF) zero_unit(u0 + j * kThreads + tid);
                 }
               }
               if constexpr (COL) {
@@ -3383,7 +3389,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               unpack<DT>(v[j], xs[j]);
               bits[j] = 0u;
               if (j * kThreads + tid < n) {
-                if (!PO && zfill) zero_unit(u0 + j * kThreads + tid);
+                if constexpr (!PO && ZF) zero_unit(u0 + j * kThreads + tid);
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                   const float x = xs[j][e];
@@ -3431,7 +3437,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               vmin = fminf(vmin, x);
               const bool surv = trunc && x >= t;
               bits = surv ? 1u : 0u;
-              if (!PO && zfill) c.gmask[idx] = 0;
+              if constexpr (!PO && ZF) c.gmask[idx] = 0;
               if constexpr (PO) {
                 const float w = exp_shifted(x, m_ref);
                 f2_add(zs, w);
@@ -3547,10 +3553,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     }
     if (kw) {
       // handled above
-    } else if (ph) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<true>{});
-    else if (p_only) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<false>{});
-    else if (col) streaming_pass(BoolC<false>{}, BoolC<true>{}, BoolC<false>{});
-    else streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{});
+    } else if (ph) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<true>{}, BoolC<false>{});
+    else if (p_only) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<false>{}, BoolC<false>{});
+    else if (col && zfill) streaming_pass(BoolC<false>{}, BoolC<true>{}, BoolC<false>{}, BoolC<true>{});
+    else if (col) streaming_pass(BoolC<false>{}, BoolC<true>{}, BoolC<false>{}, BoolC<false>{});
+    else if (zfill) streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{}, BoolC<true>{});
+    else streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{}, BoolC<false>{});
     QRITA_T(2);
     c.zero_fill_done = zfill;
     if (col) {
