@@ -320,6 +320,68 @@ def time_workload(number, steps, warmup, dev, world, l2_bytes, stream, rotate=No
     }
 
 
+def sort_mask(x, kd, pd):
+    """The sort-based comparator the pages measure against (Qrita summary,
+    "Problem statement" and "Results"): a stable descending sort of each row,
+    the top-k prefix, softmax and cumulative sum over it, the first prefix
+    reaching p, scattered back into a keep-mask. Plain PyTorch on the GPU,
+    in fp32: a timing and memory comparator, not an exact reference."""
+    import torch
+
+    xf = x.float()
+    B, V = xf.shape
+    vals, idx = torch.sort(xf, dim=1, descending=True, stable=True)
+    pos = torch.arange(V, device=xf.device).unsqueeze(0)
+    k_on = ((kd >= 1) & (kd < V)).unsqueeze(1)
+    keep = torch.where(k_on, pos < kd.unsqueeze(1), torch.ones_like(pos, dtype=torch.bool))
+    p_on = (pd < 1.0).unsqueeze(1)
+    wts = torch.exp(vals - vals[:, :1]) * keep
+    z = wts.sum(dim=1, keepdim=True)
+    before = (torch.cumsum(wts, dim=1) - wts) / z  # mass of the tokens ranked before
+    keep = keep & torch.where(p_on, (before < pd.unsqueeze(1)) | (pos == 0), torch.ones_like(keep))
+    return torch.zeros_like(keep).scatter_(1, idx, keep)
+
+
+def time_sort_baseline(number, steps, warmup, dev, stream):
+    """Time and peak extra device memory of the sort-based comparator on the
+    workload, beside the library's (which allocates nothing)."""
+    import torch
+
+    w = WORKLOADS[number]
+    logits, k, p = generate(number)
+    if w.dtype == "f32":
+        x = torch.from_numpy(logits).to(dev)
+    else:
+        x = torch.from_numpy(logits.view(np.int16)).to(dev).view(torch.bfloat16)
+    kd = torch.from_numpy(k).to(dev)
+    pd = torch.from_numpy(p).to(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            sort_mask(x, kd, pd)
+    torch.cuda.synchronize(dev)
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        s.record(stream)
+        for _ in range(steps):
+            sort_mask(x, kd, pd)
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    ms = s.elapsed_time(e) / steps
+    del x, kd, pd
+    return {
+        "impl": "torch.sort(stable=True) + softmax/cumsum over the sorted row + scatter (fp32, PyTorch on the GPU)",
+        "workload": w.name,
+        "ms_per_step": ms,
+        "rows_per_s": w.B / (ms / 1e3),
+        "peak_extra_device_bytes": int(peak),
+        "ours_extra_device_bytes": 0,
+        "note": "the library allocates nothing per call; the comparator's bytes are its sort and scan temporaries",
+    }
+
+
 def time_e2e(number, steps, warmup, dev, stream):
     """End to end through qrita_select_host: pinned host logits / k / p in,
     host mask out, copies inside the timed region."""
@@ -495,6 +557,11 @@ def run_ours(args):
             "graph_rows_per_s": (r["w"].B / (gms / 1e3)) if gms else None,
         }
     if rank == 0:
+        if not args.no_sort_baseline:
+            sb = time_sort_baseline(args.workload, max(3, min(args.steps, 10)), 2, dev, stream)
+            ours_ms = head["kernel_ms_mean"]
+            sb["speedup_of_ours"] = sb["ms_per_step"] / ours_ms
+            line["sort_baseline"] = sb
         if not args.no_e2e:
             line["e2e"] = time_e2e(args.workload, max(3, min(args.steps, 20)), 2, dev, stream)
         if not args.no_cpu_baseline:
@@ -515,6 +582,84 @@ def run_ours(args):
         import torch.distributed as dist
 
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# ablations (python bench.py --ablation): the pages' ablation switches
+# reproduced with this build's flags, each timed beside the default
+# ---------------------------------------------------------------------------
+ABLATIONS = [
+    ("default", 0),
+    ("no truncation (search the full row)", 0x1),
+    ("list search: quaternary (3 pivots a round)", 0x4000 | 0x2000),
+    ("list search: binary (1 pivot a round)", 0x8000 | 0x2000),
+    ("list search: 64 bins a round, no key histogram", 0x2000),
+    ("fallback: this build (256-bin pass, then 15 pivots a pass)", 0x2 | 0x2000),
+    ("fallback: quaternary (3 pivots a pass)", 0x2 | 0x4000 | 0x2000),
+    ("fallback: binary (1 pivot a pass)", 0x2 | 0x8000 | 0x2000),
+    ("launch: 1 CTA per row", 0x800 | (0 << 8)),
+    ("launch: 2 CTAs per row", 0x800 | (1 << 8)),
+    ("launch: 4 CTAs per row", 0x800 | (2 << 8)),
+    ("launch: 8 CTAs per row", 0x800 | (3 << 8)),
+]
+
+PAGES_ABLATIONS = {
+    "truncation": "Gaussian truncation cuts latency by about 74% against searching the full logits",
+    "quaternary": "quaternary search is slightly slower than binary on truncation hits and about 2.3 ms faster "
+                  "on fallbacks over the whole vocabulary",
+    "duplicates": "duplicate handling adds about 3.5% latency (not switchable here: the result would not be exact)",
+    "autotune": "tiered block-size autotuning cuts latency by almost 30% against one fixed block size "
+                "(here: the launch-shape rule against fixed CTAs per row)",
+    "source": "Qrita technical summary (gist.science, paper 2602.01518), \"Results\", ablation studies; "
+              "other hardware (H100, RTX4090, MI355X), not a target",
+}
+
+
+def run_ablation(args):
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    q.lib()
+    stream = torch.cuda.Stream(dev)
+    numbers = [int(t) for t in args.ablation_workloads.split(",")]
+    out = {}
+    for n in numbers:
+        w = WORKLOADS[n]
+        logits, k, p = generate(n)
+        if w.dtype == "f32":
+            x = torch.from_numpy(logits).to(dev)
+        else:
+            x = torch.from_numpy(logits.view(np.int16)).to(dev).view(torch.bfloat16)
+        # inputs rotate over enough copies to exceed 3x the L2 size (126 MB)
+        n_rot = max(2, math.ceil(3 * 126e6 / (w.B * w.V * (w.elem_bytes + 1))) + 1)
+        xs = [x] + [x.clone() for _ in range(n_rot - 1)]
+        outs = [torch.empty((w.B, w.V), dtype=torch.bool, device=dev) for _ in xs]
+        kd = torch.from_numpy(k).to(dev)
+        pd = torch.from_numpy(p).to(dev)
+        res = {}
+        for name, flags in ABLATIONS:
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    q.qrita_select_ex(xs[i % n_rot], kd, pd, out=outs[i % n_rot], stream=stream, flags=flags)
+            torch.cuda.synchronize(dev)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            steps = max(3, args.steps // 5)
+            with torch.cuda.stream(stream):
+                s.record(stream)
+                for i in range(steps):
+                    q.qrita_select_ex(xs[i % n_rot], kd, pd, out=outs[i % n_rot], stream=stream, flags=flags)
+                e.record(stream)
+            torch.cuda.synchronize(dev)
+            res[name] = {"flags": flags, "ms_per_call": s.elapsed_time(e) / steps}
+        base = res["default"]["ms_per_call"]
+        for r in res.values():
+            r["vs_default"] = r["ms_per_call"] / base
+        out[w.name] = res
+        del xs, outs
+    print(json.dumps({"ablation": out, "pages": PAGES_ABLATIONS}), flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -571,12 +716,19 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ablation", action="store_true",
+                    help="time the ablation switches (truncation, search width, launch shape) instead")
+    ap.add_argument("--ablation-workloads", default="2,3,4,5")
+    ap.add_argument("--no-sort-baseline", action="store_true",
+                    help="skip the torch.sort-based comparator (time and peak memory)")
     ap.add_argument("--rotate", type=int, default=None,
                     help="input copies to rotate over (default: enough to exceed 3x L2)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.ablation:
+        run_ablation(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

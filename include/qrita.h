@@ -107,7 +107,13 @@ enum {
 #define QRITA_FLAG_NO_KEY_HIST 0x2000u /* bf16 rows: search with pivot rounds even where the
                                            survivors span few enough 16-bit keys for the
                                            key histogram */
-#define QRITA_FLAG_KNOWN_MASK 0x3FFFu
+#define QRITA_FLAG_SEARCH_QUATERNARY 0x4000u /* ablation: the pages' literal search form, three
+                                                 pivots (25/50/75 %) a round or narrowing pass,
+                                                 four bins per tail split, no 256-bin first pass */
+#define QRITA_FLAG_SEARCH_BINARY 0x8000u     /* ablation: one pivot (the middle) a round or pass,
+                                                 two bins per tail split, no 256-bin first pass
+                                                 (wins over QRITA_FLAG_SEARCH_QUATERNARY) */
+#define QRITA_FLAG_KNOWN_MASK 0xFFFFu
 
 /* Bits of qrita_row_info_t.path. */
 #define QRITA_PATH_TOPK 0x1u      /* top-k active for the row */

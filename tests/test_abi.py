@@ -122,6 +122,7 @@ def _header_probe(tmp_path):
               "QRITA_FLAG_NO_TRUNCATION", "QRITA_FLAG_FORCE_FALLBACK", "QRITA_FLAG_KEY_PIVOTS",
               "QRITA_FLAG_FORCE_RETRY", "QRITA_FLAG_HIST_MISS", "QRITA_FLAG_CLUSTER_SHIFT", "QRITA_FLAG_CLUSTER_SET",
               "QRITA_FLAG_TEST_GIVE_UP", "QRITA_FLAG_NO_KEY_HIST", "QRITA_PATH_KEYHIST",
+              "QRITA_FLAG_SEARCH_QUATERNARY", "QRITA_FLAG_SEARCH_BINARY",
               "QRITA_PATH_TOPK", "QRITA_PATH_TOPP", "QRITA_PATH_TRUNC", "QRITA_PATH_HIT", "QRITA_PATH_FALLBACK",
               "QRITA_PATH_OVERFLOW", "QRITA_PATH_KEEP_ALL", "QRITA_PATH_RETRY", "QRITA_PATH_HIST",
               "QRITA_PATH_SAMPLE_T"]

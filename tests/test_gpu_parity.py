@@ -264,7 +264,8 @@ def _mixed_batch():
     "flags",
     ["none", "no_trunc", "fallback", "key_pivots", "c1", "c2", "c4", "c8", "c16", "fallback_key_c16",
      "retry", "retry_c1", "retry_c16", "retry_key", "hist_miss", "hist_miss_c16", "no_key_hist",
-     "no_key_hist_c1", "no_key_hist_c4"],
+     "no_key_hist_c1", "no_key_hist_c4", "quaternary", "binary", "fallback_quaternary", "fallback_binary_c4",
+     "no_trunc_quaternary_c1", "key_pivots_binary"],
 )
 def test_forced_paths_match_oracle(dev, flags):
     import top_selection_row_gb300 as q
@@ -289,6 +290,12 @@ def test_forced_paths_match_oracle(dev, flags):
         "no_key_hist": q.FLAG_NO_KEY_HIST,
         "no_key_hist_c1": q.FLAG_NO_KEY_HIST | q.flag_cluster(1),
         "no_key_hist_c4": q.FLAG_NO_KEY_HIST | q.flag_cluster(4),
+        "quaternary": q.FLAG_SEARCH_QUATERNARY | q.FLAG_NO_KEY_HIST,
+        "binary": q.FLAG_SEARCH_BINARY | q.FLAG_NO_KEY_HIST,
+        "fallback_quaternary": q.FLAG_FORCE_FALLBACK | q.FLAG_SEARCH_QUATERNARY | q.FLAG_NO_KEY_HIST,
+        "fallback_binary_c4": q.FLAG_FORCE_FALLBACK | q.FLAG_SEARCH_BINARY | q.FLAG_NO_KEY_HIST | q.flag_cluster(4),
+        "no_trunc_quaternary_c1": q.FLAG_NO_TRUNCATION | q.FLAG_SEARCH_QUATERNARY | q.flag_cluster(1),
+        "key_pivots_binary": q.FLAG_KEY_PIVOTS | q.FLAG_SEARCH_BINARY | q.FLAG_NO_KEY_HIST,
     }[flags]
     for n, logits, k, p in _mixed_batch():
         w = WORKLOADS[n]

@@ -27,6 +27,8 @@ FLAG_HIST_MISS = 0x10
 FLAG_CLUSTER_SET = 0x800
 FLAG_TEST_GIVE_UP = 0x1000
 FLAG_NO_KEY_HIST = 0x2000
+FLAG_SEARCH_QUATERNARY = 0x4000
+FLAG_SEARCH_BINARY = 0x8000
 
 
 def flag_cluster(n_ctas: int) -> int:

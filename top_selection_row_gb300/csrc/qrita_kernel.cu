@@ -270,7 +270,7 @@ enum : int {
   // uints
   BU_TRUNC = 0, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
   BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS, BU_S2, BU_OVF2,
-  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW, BU_SAMPLE_T, BU_KWCA, BU_KWCB,
+  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW, BU_SAMPLE_T, BU_KWCA, BU_KWCB, BU_SGE,
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
   // float pairs
@@ -489,6 +489,9 @@ struct Ctx {
   bool zero_fill;       // the chunk's mask is to be zeroed early (by the search tail)
   bool zero_fill_done;  // and it was
   bool give_up_once;    // test flag: the next bounded copy wait reports that it gave up
+  int split;            // bins of a list-search round and of a tail split (64; 4 or 2 by flag)
+  int npiv;             // pivots of a narrowing pass (15; 3 or 1 by flag)
+  bool wide_ok;         // the 256-bin first narrowing pass may run
 };
 
 // Fill the chunk's mask with one byte value (16-byte stores where aligned).
@@ -780,7 +783,24 @@ __device__ void narrow_pass(Ctx<DT>& c, Range& R, bool value_ok, bool* used_valu
 
   if (tid == 0) {
     bool used_value = false;
-    const int np = two_level_pivots(R.lo, R.hi, value_ok, F.bc.q, F.bc.qf, used_value);
+    int np;
+    if (c.npiv >= kNarrowPivots) {
+      np = two_level_pivots(R.lo, R.hi, value_ok, F.bc.q, F.bc.qf, used_value);
+    } else {
+      // one quaternary level (3 pivots) or a binary split (the middle one)
+      uint32_t q0, q1, q2;
+      const int n1 = quartile_pivots(R.lo, R.hi, value_ok, q0, q1, q2, used_value);
+      np = 0;
+      if (c.npiv == 1) {
+        if (n1 > 0) F.bc.q[np++] = n1 == 3 ? q1 : q0;
+      } else {
+        if (n1 > 0) F.bc.q[np++] = q0;
+        if (n1 > 1) F.bc.q[np++] = q1;
+        if (n1 > 2) F.bc.q[np++] = q2;
+      }
+      for (int j = 0; j < 16; ++j) F.bc.qf[j] = (j < np) ? pivot_f(F.bc.q[j]) : INFINITY;
+      for (int j = np; j < 16; ++j) F.bc.q[j] = R.hi;
+    }
     F.bc.u[BU_NP] = static_cast<uint32_t>(np);
     F.bc.u[BU_USED_VALUE] = used_value ? 1u : 0u;
     F.bc.f[BF_LOF] = R.lo_all ? -INFINITY : pivot_f(R.lo);
@@ -1247,7 +1267,7 @@ __device__ void narrow(Ctx<DT>& c, Range& R) {
   while (true) {
     const uint32_t span_before = R.hi - R.lo;
     bool used_value = false;
-    if (!wide_done && wide_pass<DT, MASS>(c, R)) {
+    if (!wide_done && c.wide_ok && wide_pass<DT, MASS>(c, R)) {
       wide_done = true;
       used_value = true;
       QRITA_T(11);
@@ -1975,16 +1995,17 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
       break;
     }
     const float lo_f = pivot_f(lo), hi_f = pivot_f(hi);
-    const float inv = static_cast<float>(kSplit) / (hi_f - lo_f);
+    const int ns = c.split;  // bins this round (kSplit unless a flag narrows it)
+    const float inv = static_cast<float>(ns) / (hi_f - lo_f);
     const bool val = vmode && isfinite(lo_f) && isfinite(hi_f) && hi_f > lo_f && isfinite(inv) && inv > 0.f;
     const uint32_t span = hi - lo;
     // bin of a key in (lo, hi]: monotone in the key
     auto bin_of_key = [&](uint32_t k) -> int {
       if (val) {
         const int b = static_cast<int>((key2f(k) - lo_f) * inv);
-        return b < 0 ? 0 : (b > kSplit - 1 ? kSplit - 1 : b);
+        return b < 0 ? 0 : (b > ns - 1 ? ns - 1 : b);
       }
-      return static_cast<int>((static_cast<uint64_t>(k - lo - 1u) * kSplit) / span);
+      return static_cast<int>((static_cast<uint64_t>(k - lo - 1u) * static_cast<uint64_t>(ns)) / span);
     };
     if (tid < kSplit) {
       F.tbin_c[tid] = 0u;
@@ -2087,7 +2108,7 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     m_hi = vld(F.bc.x[BX_MHI]);
     m_lo = vld(F.bc.x[BX_MLO]);
     const uint32_t nlo = bs == 0 ? lo : last_key_in_bins(lo + 1u, hi, bs - 1, bin_of_key);
-    const uint32_t nhi = bs == kSplit - 1 ? hi : last_key_in_bins(lo + 1u, hi, bs, bin_of_key);
+    const uint32_t nhi = bs == ns - 1 ? hi : last_key_in_bins(lo + 1u, hi, bs, bin_of_key);
     lo = nlo;
     hi = nhi;
     ++rounds;
@@ -2177,12 +2198,13 @@ __device__ void dsearch(Ctx<DT>& c, Local& s, unsigned long long target, bool va
     float v0 = pivot_f(lo), v1 = pivot_f(hi);  // level 0: the range (lo, hi]
     bool one_value = false;
     for (int level = 0; level < kTailLevels && ns > static_cast<uint32_t>(kTailDirect); ++level) {
-      const float inv_bw = static_cast<float>(kTailBins) / (v1 - v0);
+      const int tb = c.split;  // bins of this split
+      const float inv_bw = static_cast<float>(tb) / (v1 - v0);
       if (!(isfinite(v0) && isfinite(v1) && v1 > v0 && isfinite(inv_bw) && inv_bw > 0.f)) break;
       // members satisfy x > v0 (level 0) or x >= v0 (later): never negative
       auto tbin = [&](float x) -> int {
         const int b = static_cast<int>((x - v0) * inv_bw);
-        return b < 0 ? 0 : (b > kTailBins - 1 ? kTailBins - 1 : b);
+        return b < 0 ? 0 : (b > tb - 1 ? tb - 1 : b);
       };
       if (tid < kTailBins) {
         F.tbin_c[tid] = 0u;
@@ -3011,6 +3033,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   c.gbody = c.gx + c.head_n * S;
   // the test flag voids row 0 from its first CTA: uniform over that CTA
   c.give_up_once = (P.flags & QRITA_FLAG_TEST_GIVE_UP) != 0u && r == 0 && c.crank == 0u;
+  // search width: the pages' quaternary form (3 pivots) or a binary split
+  // for ablations; by default 64-bin rounds and two quaternary levels a pass
+  c.split = (P.flags & QRITA_FLAG_SEARCH_BINARY) ? 2 : ((P.flags & QRITA_FLAG_SEARCH_QUATERNARY) ? 4 : kSplit);
+  c.npiv = (P.flags & QRITA_FLAG_SEARCH_BINARY) ? 1 : ((P.flags & QRITA_FLAG_SEARCH_QUATERNARY) ? 3 : kNarrowPivots);
+  c.wide_ok = (P.flags & (QRITA_FLAG_SEARCH_BINARY | QRITA_FLAG_SEARCH_QUATERNARY)) == 0u;
   QRITA_T(0);
 
   // ---- row parameters (uniform)
@@ -3111,8 +3138,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       cn = warp_sum_f(cn);
       cx = warp_sum_f(cx);
       cxx = warp_sum_f(cxx);
-      __syncthreads();  // every thread has read the first partials
-      if (lane == 0) {
+      if (lane == 0) {  // (slots apart from the first partials)
         F.redf[warp][4] = cn;
         F.redf[warp][5] = cx;
         F.redf[warp][6] = cxx;
@@ -3169,6 +3195,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       F.bc.f[BF_T] = trunc ? t : -INFINITY;
       F.bc.u[BU_TRUNC] = trunc ? 1u : 0u;
       F.bc.u[BU_SAMPLE_T] = 0u;
+      F.bc.u[BU_SGE] = 0u;
     }
     __syncthreads();
     // A top-k threshold the sample contradicts (a quarter or less of the
@@ -3178,12 +3205,16 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     if (k_on && vld(F.bc.u[BU_TRUNC]) != 0u &&
         (P.flags & (QRITA_FLAG_FORCE_FALLBACK | QRITA_FLAG_FORCE_RETRY)) == 0u) {
       const float tt = vld(F.bc.f[BF_T]);
-      int n_ge = 0, n_f = 0;
+      // the sample's count at or above t (high half) and of finite values
+      // (low half; at most kSampleBlocks * kSampleBlock), one block reduction
+      uint32_t ge_f = 0;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        n_ge += __syncthreads_count(sv[j] >= tt);
-        n_f += __syncthreads_count(!isnan(sv[j]));
-      }
+      for (int j = 0; j < kPer; ++j) ge_f += (sv[j] >= tt ? 0x10000u : 0u) + (isnan(sv[j]) ? 0u : 1u);
+      ge_f = __reduce_add_sync(kFull, ge_f);
+      if (lane == 0) atomicAdd(&F.bc.u[BU_SGE], ge_f);
+      __syncthreads();
+      const uint32_t tot_ge_f = vld(F.bc.u[BU_SGE]);
+      const int n_ge = static_cast<int>(tot_ge_f >> 16), n_f = static_cast<int>(tot_ge_f & 0xFFFFu);
       const float lam = static_cast<float>(kr) * static_cast<float>(n_f) / static_cast<float>(V);
       const int jq = static_cast<int>(ceilf(lam + 3.0f * sqrtf(lam) + 3.0f));
       const float expect = static_cast<float>(jq) * static_cast<float>(V) / static_cast<float>(n_f > 0 ? n_f : 1);
