@@ -14,3 +14,4 @@ from .qrita_oracle import (  # noqa: F401
     select_batch,
     select_row,
 )
+from .qrita_outputs import SAMPLE_BAND, candidates, sample, topk_ids  # noqa: F401
