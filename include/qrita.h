@@ -215,6 +215,57 @@ int qrita_select_host(const void* h_logits, int dtype, int64_t B, int64_t V, con
                       qrita_stream_t stream);
 
 /*
+ * qrita_topk_ids: the top-k token ids of every row in stable order (logit
+ * descending, equal logits by lower id), as a drafter keeps them (Qrita
+ * technical summary, "Problem statement": the full candidate set with the
+ * exact sort-based semantics, here in rank order).
+ *
+ *   logits, dtype, B, V   as qrita_select.
+ *   k        device int32[B] (required): row r gets the first k_r ids of its
+ *            stable descending order when 1 <= k_r <= kmax (and min(k_r, V)
+ *            when k_r >= V); other rows get none.
+ *   kmax     1 .. 8192: the length of each row of out_ids.
+ *   out_mask device uint8[B, V]: the top-k keep-mask (also an output; the
+ *            ids are read back from it).
+ *   out_ids  device int32[B, kmax]: the ids in rank order, then -1.
+ *
+ * Two kernels on stream (the selection, then the ids); allocates nothing.
+ * Errors as qrita_select; QRITA_EINVAL also for k == NULL, out_ids == NULL
+ * or kmax outside 1 .. 8192.
+ */
+int qrita_topk_ids(const void* logits, int dtype, int64_t B, int64_t V, const int32_t* k, int32_t kmax,
+                   uint8_t* out_mask, int32_t* out_ids, qrita_stream_t stream);
+
+/*
+ * qrita_candidates: the candidate lists a verifier or a sampler consumes
+ * after the mask, and one token drawn from each (Qrita technical summary,
+ * "Problem statement": the complete candidate set, beside the single sampled
+ * token stochastic samplers return).
+ *
+ *   logits, dtype, B, V   as qrita_select.
+ *   mask       device uint8[B, V], e.g. qrita_select's output (nonzero = kept).
+ *   cap        >= 1: the length of each row of out_ids / out_probs.
+ *   out_ids    device int32[B, cap]: the kept ids in increasing id order; a
+ *              row keeping more than cap writes its first cap.
+ *   out_probs  device float[B, cap]: their probabilities renormalised over
+ *              the row's kept set, p_i = exp(x_i - m) / sum over kept of
+ *              exp(x_j - m), m the largest kept logit (fp32, from 64-bit
+ *              fixed-point weights; within a few 1e-7 relative of fp64).
+ *   out_count  device int32[B]: the row's kept count (may exceed cap).
+ *   u          device float[B] or NULL: one uniform in [0, 1) per row.
+ *   out_sample device int32[B] or NULL (NULL exactly when u is): the first
+ *              kept id, in id order, whose cumulative probability exceeds
+ *              u_r; -1 for a row that keeps nothing.
+ *
+ * Entries past a row's count are left as they were. Two kernels at most on
+ * stream; allocates nothing. Errors as qrita_select; QRITA_EINVAL also for
+ * cap < 1, a NULL output, or exactly one of u / out_sample NULL.
+ */
+int qrita_candidates(const void* logits, int dtype, int64_t B, int64_t V, const uint8_t* mask, int32_t cap,
+                     int32_t* out_ids, float* out_probs, int32_t* out_count, const float* u, int32_t* out_sample,
+                     qrita_stream_t stream);
+
+/*
  * qrita_delta_table: copy one of the host-built truncation tables the kernel
  * receives (Qrita technical summary, "Methodology", part 1: delta comes from
  * precomputed tables of the normal quantile function keyed on k or p).

@@ -178,6 +178,60 @@ def decode_row_info(info) -> np.ndarray:
     return np.ascontiguousarray(raw).view(ROW_INFO_DTYPE).reshape(-1)
 
 
+def qrita_topk_ids(logits, k, kmax, out_mask=None, out_ids=None, stream=None):
+    """Top-k ids of every row in stable order (logit descending, lower id
+    first among equals) through qrita_topk_ids.
+
+    logits: CUDA [B, V] float32 / bfloat16; k: CUDA int32 [B]; kmax: 1..8192.
+    Returns (ids int32 [B, kmax], padded with -1; mask bool [B, V]).
+    """
+    torch = _torch()
+    B, V = _check_rows(logits)
+    dev = logits.device
+    kk = _vec(k, B, torch.int32, "k", dev)
+    if kk is None:
+        raise ValueError("k is required")
+    if out_mask is None:
+        out_mask = torch.empty((B, V), dtype=torch.bool, device=dev)
+    if out_ids is None:
+        out_ids = torch.empty((B, int(kmax)), dtype=torch.int32, device=dev)
+    elif out_ids.shape != (B, int(kmax)) or out_ids.dtype != torch.int32 or not out_ids.is_contiguous():
+        raise ValueError("out_ids must be a contiguous int32 [B, kmax] tensor")
+    rc = lib().qrita_topk_ids(
+        ctypes.c_void_p(logits.data_ptr() if B else 0), _dtype_code(logits), B, V,
+        ctypes.c_void_p(kk.data_ptr()), int(kmax), ctypes.c_void_p(out_mask.data_ptr() if B else 0),
+        ctypes.c_void_p(out_ids.data_ptr() if B else 0), _stream_ptr(dev, stream))
+    if rc != OK:
+        raise QritaError(rc)
+    return out_ids, out_mask
+
+
+def qrita_candidates(logits, mask, cap, u=None, stream=None):
+    """Kept ids in id order with probabilities renormalised over the kept set,
+    the kept count, and (with u: CUDA float32 [B]) one token drawn per row,
+    through qrita_candidates. Returns (ids [B, cap], probs [B, cap], count [B],
+    sample [B] or None); entries past a row's count are -1 / 0."""
+    torch = _torch()
+    B, V = _check_rows(logits)
+    dev = logits.device
+    if mask.shape != (B, V) or mask.dtype not in (torch.bool, torch.uint8) or not mask.is_contiguous():
+        raise ValueError("mask must be a contiguous bool/uint8 [B, V] tensor")
+    uu = _vec(u, B, torch.float32, "u", dev)
+    ids = torch.full((B, int(cap)), -1, dtype=torch.int32, device=dev)
+    probs = torch.zeros((B, int(cap)), dtype=torch.float32, device=dev)
+    count = torch.empty(B, dtype=torch.int32, device=dev)
+    sample = torch.empty(B, dtype=torch.int32, device=dev) if uu is not None else None
+    rc = lib().qrita_candidates(
+        ctypes.c_void_p(logits.data_ptr() if B else 0), _dtype_code(logits), B, V,
+        ctypes.c_void_p(mask.data_ptr() if B else 0), int(cap), ctypes.c_void_p(ids.data_ptr() if B else 0),
+        ctypes.c_void_p(probs.data_ptr() if B else 0), ctypes.c_void_p(count.data_ptr() if B else 0),
+        ctypes.c_void_p(uu.data_ptr() if uu is not None else 0),
+        ctypes.c_void_p(sample.data_ptr() if sample is not None else 0), _stream_ptr(dev, stream))
+    if rc != OK:
+        raise QritaError(rc)
+    return ids, probs, count, sample
+
+
 def delta_table(which: int) -> np.ndarray:
     """The host-built truncation table the kernel receives: ``which`` 0 is the
     top-k table (entry i = Phi^-1(1 - 2^(-i/4))), 1 the top-p table (entry

@@ -17,6 +17,8 @@ EXPORTED = (
     "qrita_select_ex",
     "qrita_host_staging_bytes",
     "qrita_select_host",
+    "qrita_topk_ids",
+    "qrita_candidates",
     "qrita_delta_table",
     "qrita_strerror",
     "qrita_version",
@@ -44,6 +46,10 @@ def lib() -> ctypes.CDLL:
     L.qrita_host_staging_bytes.restype = sz
     L.qrita_select_host.argtypes = [vp, i32, i64, i64, vp, vp, vp, vp, sz, vp]
     L.qrita_select_host.restype = i32
+    L.qrita_topk_ids.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp, vp]
+    L.qrita_topk_ids.restype = i32
+    L.qrita_candidates.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp, vp, vp, vp, vp]
+    L.qrita_candidates.restype = i32
     L.qrita_delta_table.argtypes = [i32, vp, i32]
     L.qrita_delta_table.restype = i32
     L.qrita_strerror.argtypes = [i32]

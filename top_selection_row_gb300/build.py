@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libqrita.so")
 
-SOURCES = ["qrita_kernel.cu", "qrita_api.cpp"]
+SOURCES = ["qrita_kernel.cu", "qrita_outputs.cu", "qrita_api.cpp"]
 HEADERS = ["qrita_device.cuh", "qrita_internal.h"]
 
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -49,27 +49,29 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=None) 
     """Compile libqrita.so for sm_103a; returns its path."""
     if not force and up_to_date():
         return LIB_PATH
-    tmp = LIB_PATH + ".tmp"
-    cmd = [
-        nvcc_path(),
-        *GENCODE,
-        "-lineinfo",
-        "-O3",
-        "-std=c++17",
-        "-Xcompiler",
-        "-fPIC",
-        "-shared",
-        "-I",
-        INCLUDE,
-        "-o",
-        tmp,
-        *[os.path.join(CSRC, s) for s in SOURCES],
-    ]
+    import tempfile
+
+    base = [nvcc_path(), *GENCODE, "-lineinfo", "-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
     if extra_flags:
-        cmd[1:1] = list(extra_flags)
-    if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
+        base[1:1] = list(extra_flags)
+    tmp = LIB_PATH + ".tmp"
+    with tempfile.TemporaryDirectory(prefix="qrita_build_") as td:
+        # every translation unit compiles at once, then one link
+        objs, procs = [], []
+        for src in SOURCES:
+            obj = os.path.join(td, os.path.splitext(src)[0] + ".o")
+            cmd = [*base, "-c", os.path.join(CSRC, src), "-o", obj]
+            if verbose:
+                print(" ".join(cmd), file=sys.stderr)
+            procs.append((cmd, subprocess.Popen(cmd)))
+            objs.append(obj)
+        for cmd, pr in procs:
+            if pr.wait() != 0:
+                raise subprocess.CalledProcessError(pr.returncode, cmd)
+        link = [nvcc_path(), *GENCODE, "-shared", "-o", tmp, *objs]
+        if verbose:
+            print(" ".join(link), file=sys.stderr)
+        subprocess.run(link, check=True)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

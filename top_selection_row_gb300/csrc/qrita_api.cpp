@@ -263,6 +263,31 @@ int qrita_select_host(const void* h_logits, int dtype, int64_t B, int64_t V, con
   return QRITA_OK;
 }
 
+int qrita_topk_ids(const void* logits, int dtype, int64_t B, int64_t V, const int32_t* k, int32_t kmax,
+                   uint8_t* out_mask, int32_t* out_ids, qrita_stream_t stream) {
+  int rc = qrita::check_args(logits, dtype, B, V, out_mask, 0u);
+  if (rc != QRITA_OK || B == 0) return rc;
+  if (k == nullptr || out_ids == nullptr || kmax < 1 || kmax > qrita::kMaxIds) return QRITA_EINVAL;
+  if (B > static_cast<int64_t>(std::numeric_limits<int32_t>::max())) return QRITA_EUNSUPPORTED;
+  rc = qrita::select_impl(logits, dtype, B, V, k, nullptr, out_mask, stream, 0u, nullptr, nullptr);
+  if (rc != QRITA_OK) return rc;
+  return qrita::launch_ids(logits, dtype, B, V, k, kmax, out_mask, out_ids, stream) == 0 ? QRITA_OK : QRITA_ECUDA;
+}
+
+int qrita_candidates(const void* logits, int dtype, int64_t B, int64_t V, const uint8_t* mask, int32_t cap,
+                     int32_t* out_ids, float* out_probs, int32_t* out_count, const float* u, int32_t* out_sample,
+                     qrita_stream_t stream) {
+  int rc = qrita::check_args(logits, dtype, B, V, mask, 0u);
+  if (rc != QRITA_OK || B == 0) return rc;
+  if (cap < 1 || out_ids == nullptr || out_probs == nullptr || out_count == nullptr) return QRITA_EINVAL;
+  if ((u == nullptr) != (out_sample == nullptr)) return QRITA_EINVAL;
+  if (B > static_cast<int64_t>(std::numeric_limits<int32_t>::max())) return QRITA_EUNSUPPORTED;
+  return qrita::launch_candidates(logits, dtype, B, V, mask, cap, out_ids, out_probs, out_count, u, out_sample,
+                                  stream) == 0
+             ? QRITA_OK
+             : QRITA_ECUDA;
+}
+
 int qrita_delta_table(int which, float* out, int n) {
   const qrita::Tables& t = qrita::tables();
   const float* src = nullptr;

@@ -75,4 +75,13 @@ int launch_select(const Params& prm, int dtype, size_t smem, qrita_stream_t stre
 // Largest dynamic shared memory per block on the current device.
 int max_smem_per_block();
 
+// Outputs beyond the mask (qrita_outputs.cu). Both return a cudaError_t.
+constexpr int32_t kMaxIds = 8192;  // largest kmax of qrita_topk_ids
+size_t ids_smem_bytes(int32_t kmax);
+int launch_ids(const void* logits, int dtype, int64_t B, int64_t V, const int32_t* k, int32_t kmax,
+               const uint8_t* mask, int32_t* out_ids, qrita_stream_t stream);
+int launch_candidates(const void* logits, int dtype, int64_t B, int64_t V, const uint8_t* mask, int32_t cap,
+                      int32_t* out_ids, float* out_probs, int32_t* out_count, const float* u, int32_t* out_sample,
+                      qrita_stream_t stream);
+
 }  // namespace qrita
