@@ -382,6 +382,84 @@ def time_sort_baseline(number, steps, warmup, dev, stream):
     }
 
 
+def time_outputs(number, steps, warmup, dev, stream, peak, kmax=2048, cap=2048):
+    """The outputs after the mask on the workload, inputs resident: the top-k
+    ids in rank order (qrita_topk_ids: the selection with top-p off, then the
+    ids kernel) beside the selection alone, and the candidate lists with one
+    draw per row (qrita_candidates over the workload's mask). Algorithmic
+    bytes: ids: the mask read, the kept logits and the id rows written;
+    candidates: the mask read, the kept logits, the ids and probabilities
+    written (up to cap per row), the count, the uniform and the draw."""
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    w = WORKLOADS[number]
+    logits, k, p = generate(number)
+    if w.dtype == "f32":
+        x = torch.from_numpy(logits).to(dev)
+    else:
+        x = torch.from_numpy(logits.view(np.int16)).to(dev).view(torch.bfloat16)
+    kd = torch.from_numpy(k).to(dev)
+    pd = torch.from_numpy(p).to(dev)
+    mask = q.qrita_select(x, kd, pd, stream=stream)
+    torch.cuda.synchronize(dev)
+    kept = mask.sum(dim=1).cpu().numpy().astype(np.int64)
+    rng = np.random.default_rng(7)
+    ud = torch.from_numpy(rng.random(w.B).astype(np.float32)).to(dev)
+    ids = torch.empty((w.B, cap), dtype=torch.int32, device=dev)
+    probs = torch.empty((w.B, cap), dtype=torch.float32, device=dev)
+    count = torch.empty(w.B, dtype=torch.int32, device=dev)
+    sample = torch.empty(w.B, dtype=torch.int32, device=dev)
+    kmask = torch.empty((w.B, w.V), dtype=torch.bool, device=dev)
+    kids = torch.empty((w.B, kmax), dtype=torch.int32, device=dev)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.synchronize(dev)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            s.record(stream)
+            for _ in range(steps):
+                fn()
+            e.record(stream)
+        torch.cuda.synchronize(dev)
+        return s.elapsed_time(e) / steps
+
+    cand_ms = timed(lambda: q.qrita_candidates(x, mask, cap, u=ud, stream=stream, out=(ids, probs, count, sample)))
+    ids_ms = timed(lambda: q.qrita_topk_ids(x, kd, kmax, out_mask=kmask, out_ids=kids, stream=stream))
+    sel_k_ms = timed(lambda: q.qrita_select(x, kd, None, out=kmask, stream=stream))
+    kk = np.where((k >= 1) & (k <= kmax), np.minimum(k, w.V), 0).astype(np.int64)
+    ids_bytes = int(w.B * w.V + kk.sum() * w.elem_bytes + w.B * kmax * 4)
+    cand_bytes = int(w.B * w.V + kept.sum() * w.elem_bytes + np.minimum(kept, cap).sum() * 8 + w.B * 12)
+    ids_extra = max(ids_ms - sel_k_ms, 1e-9)
+    del x, mask, kmask
+    return {
+        "workload": w.name,
+        "candidates": {
+            "call": "qrita_candidates (cap %d, one draw per row)" % cap,
+            "ms_per_call": cand_ms,
+            "rows_per_s": w.B / (cand_ms / 1e3),
+            "algorithmic_bytes": cand_bytes,
+            "hbm_gbs": cand_bytes / (cand_ms / 1e3) / 1e9,
+            "frac_of_measured_peak": cand_bytes / (cand_ms / 1e3) / 1e9 / peak,
+            "kept_per_row_mean": float(kept.mean()),
+        },
+        "topk_ids": {
+            "call": "qrita_topk_ids (kmax %d): the selection with top-p off, then the ids" % kmax,
+            "ms_per_call": ids_ms,
+            "rows_per_s": w.B / (ids_ms / 1e3),
+            "selection_alone_ms": sel_k_ms,
+            "ids_kernel_ms_estimate": ids_extra,
+            "ids_algorithmic_bytes": ids_bytes,
+            "ids_frac_of_measured_peak": ids_bytes / (ids_extra / 1e3) / 1e9 / peak,
+            "rows_with_ids": int((kk > 0).sum()),
+        },
+    }
+
+
 def time_e2e(number, steps, warmup, dev, stream):
     """End to end through qrita_select_host: pinned host logits / k / p in,
     host mask out, copies inside the timed region."""
@@ -564,6 +642,8 @@ def run_ours(args):
             line["sort_baseline"] = sb
         if not args.no_e2e:
             line["e2e"] = time_e2e(args.workload, max(3, min(args.steps, 20)), 2, dev, stream)
+        if not args.no_outputs:
+            line["outputs"] = time_outputs(args.workload, max(3, min(args.steps, 20)), 3, dev, stream, peak)
         if not args.no_cpu_baseline:
             v1, rows1, el1 = oracle_rows_per_s(args.workload, budget_s=args.cpu_seconds / 2)
             vn, rowsn, cores = oracle_rows_per_s_pooled(args.workload, budget_s=args.cpu_seconds / 2)
@@ -640,21 +720,22 @@ def run_ablation(args):
         kd = torch.from_numpy(k).to(dev)
         pd = torch.from_numpy(p).to(dev)
         res = {}
-        for name, flags in ABLATIONS:
+        # the default is timed first and again last; the ratios divide by
+        # the mean of the two (the spread shows the run-to-run noise)
+        for name, flags in ABLATIONS + [("default (timed again, last)", 0)]:
             with torch.cuda.stream(stream):
-                for i in range(3):
+                for i in range(args.warmup):
                     q.qrita_select_ex(xs[i % n_rot], kd, pd, out=outs[i % n_rot], stream=stream, flags=flags)
             torch.cuda.synchronize(dev)
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            steps = max(3, args.steps // 5)
             with torch.cuda.stream(stream):
                 s.record(stream)
-                for i in range(steps):
+                for i in range(args.steps):
                     q.qrita_select_ex(xs[i % n_rot], kd, pd, out=outs[i % n_rot], stream=stream, flags=flags)
                 e.record(stream)
             torch.cuda.synchronize(dev)
-            res[name] = {"flags": flags, "ms_per_call": s.elapsed_time(e) / steps}
-        base = res["default"]["ms_per_call"]
+            res[name] = {"flags": flags, "ms_per_call": s.elapsed_time(e) / args.steps}
+        base = 0.5 * (res["default"]["ms_per_call"] + res["default (timed again, last)"]["ms_per_call"])
         for r in res.values():
             r["vs_default"] = r["ms_per_call"] / base
         out[w.name] = res
@@ -719,6 +800,8 @@ def main(argv=None):
     ap.add_argument("--ablation", action="store_true",
                     help="time the ablation switches (truncation, search width, launch shape) instead")
     ap.add_argument("--ablation-workloads", default="2,3,4,5")
+    ap.add_argument("--no-outputs", action="store_true",
+                    help="skip timing the outputs after the mask (top-k ids, candidate lists)")
     ap.add_argument("--no-sort-baseline", action="store_true",
                     help="skip the torch.sort-based comparator (time and peak memory)")
     ap.add_argument("--rotate", type=int, default=None,

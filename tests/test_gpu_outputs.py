@@ -135,6 +135,48 @@ def test_candidates_edges(dev):
     _cand_case(dev, f32_to_bf16_bits(x), "bf16", mask, 64, us)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_vector_and_scalar_forms(dev, dtype):
+    """Rows whose mask and logits start on 16-byte boundaries (V a multiple of
+    16) take the vector kernels; the same rows with V off by a few elements,
+    or shifted one element off the boundary, take the scalar ones. Both must
+    match the oracle."""
+    import torch
+
+    import top_selection_row_gb300 as q
+
+    rng = np.random.default_rng(17)
+    for V in (4096, 4099, 5008):
+        x = (np.round(rng.standard_normal((6, V)) * 8) / 8).astype(np.float32)  # ties
+        x[2, :] = 0.75
+        logits = f32_to_bf16_bits(x) if dtype == "bf16" else x
+        k = np.array([1, 33, 700, 4096, 0, 2047], np.int32)
+        _ids_case(dev, logits, dtype, k, 4096)
+        mask = (rng.random((6, V)) < np.array([0.002, 0.05, 0.5, 1.0, 0.0, 0.9])[:, None]).astype(np.uint8)
+        us = rng.random(6).astype(np.float32)
+        _cand_case(dev, logits, dtype, mask, V, us)
+        _cand_case(dev, logits, dtype, mask, 40, us)
+        # one element off the 16-byte boundary: the logits and the mask live
+        # at offset 1 of larger buffers
+        xd = to_device(logits, dtype, dev).reshape(-1)
+        xs = torch.empty(xd.numel() + 8, dtype=xd.dtype, device=dev)
+        xs[1:1 + xd.numel()] = xd
+        xo = xs[1:1 + xd.numel()].view(6, V)
+        ms = torch.zeros(6 * V + 16, dtype=torch.uint8, device=dev)
+        ms[1:1 + 6 * V] = torch.from_numpy(mask.reshape(-1)).to(dev)
+        mo = ms[1:1 + 6 * V].view(6, V)
+        ud = torch.from_numpy(us).to(dev)
+        ids_o, probs_o, count_o, smp_o = q.qrita_candidates(xo, mo, V, u=ud)
+        ids_a, probs_a, count_a, smp_a = q.qrita_candidates(to_device(logits, dtype, dev),
+                                                            torch.from_numpy(mask).to(dev), V, u=ud)
+        assert torch.equal(count_o, count_a) and torch.equal(ids_o, ids_a) and torch.equal(smp_o, smp_a)
+        assert torch.allclose(probs_o, probs_a, rtol=4e-6, atol=0)
+        kd = torch.from_numpy(k).to(dev)
+        tid_o, _ = q.qrita_topk_ids(xo, kd, 4096)
+        tid_a, _ = q.qrita_topk_ids(to_device(logits, dtype, dev), kd, 4096)
+        assert torch.equal(tid_o, tid_a)
+
+
 def test_draws_follow_the_probabilities(dev):
     """Stratified uniforms over one row: each kept id is drawn in proportion
     to its probability (the draw is the inverse distribution function)."""

@@ -15,7 +15,7 @@ import pytest
 from oracle import select_batch, select_row
 from parity_helpers import (check_against_oracle, compare_rows, compare_rows_pooled, invariant_failures, run_gpu,
                             to_device, widen)
-from workloads import WORKLOADS, generate
+from workloads import WORKLOADS, f32_to_bf16_bits, generate
 
 pytestmark = pytest.mark.gpu
 
@@ -427,6 +427,32 @@ def test_sample_threshold_rescues_uniform_rows(dev):
     path = info["path"][uniform]
     assert ((path & q.PATH_SAMPLE_T) != 0).mean() >= 0.75
     assert ((path & (q.PATH_FALLBACK | q.PATH_RETRY)) == 0).mean() >= 0.75
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_light_tails_take_the_sample_threshold_at_small_k(dev, dtype):
+    """Small k on rows bounded below the Gaussian tail: the sample expects
+    fewer than two values above the k-th logit, so it cannot test the
+    Gaussian threshold itself; its tail lighter than the Gaussian's
+    (hardly any value above mu + 2 sigma) sends the row to the sample's
+    order statistic, not to a second pass. Gaussian rows keep their
+    threshold."""
+    import top_selection_row_gb300 as q
+
+    rng = np.random.default_rng(41)
+    B, V = 24, 201088
+    x = rng.uniform(-1.0, 1.0, (B, V)).astype(np.float32)
+    x[B // 2:] = rng.standard_normal((B - B // 2, V)).astype(np.float32)
+    k = np.array([1, 2, 5, 20, 50, 97, 113, 200, 300, 1, 60, 150] * 2, np.int32)
+    p = np.where(np.arange(B) % 3 == 0, np.float32(0.9), np.float32(1.0)).astype(np.float32)
+    logits = f32_to_bf16_bits(x) if dtype == "bf16" else x
+    fails, flagged, got, st, info = check_against_oracle(logits, dtype, k, p, dev)
+    assert fails == [], fails[:5]
+    path = info["path"].astype(np.int64)
+    uni, gau = path[: B // 2], path[B // 2:]
+    assert ((uni & q.PATH_SAMPLE_T) != 0).all(), [hex(v) for v in uni]
+    assert ((uni & (q.PATH_RETRY | q.PATH_FALLBACK)) == 0).all(), [hex(v) for v in uni]
+    assert ((gau & q.PATH_SAMPLE_T) == 0).all(), [hex(v) for v in gau]
 
 
 def test_second_truncation_rescues_uniform_rows(dev):

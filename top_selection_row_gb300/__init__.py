@@ -206,21 +206,37 @@ def qrita_topk_ids(logits, k, kmax, out_mask=None, out_ids=None, stream=None):
     return out_ids, out_mask
 
 
-def qrita_candidates(logits, mask, cap, u=None, stream=None):
+def qrita_candidates(logits, mask, cap, u=None, stream=None, out=None):
     """Kept ids in id order with probabilities renormalised over the kept set,
     the kept count, and (with u: CUDA float32 [B]) one token drawn per row,
     through qrita_candidates. Returns (ids [B, cap], probs [B, cap], count [B],
-    sample [B] or None); entries past a row's count are -1 / 0."""
+    sample [B] or None). Without ``out`` the entries past a row's count are
+    -1 / 0; ``out`` = (ids, probs, count, sample) reuses the caller's buffers
+    (contiguous int32 [B, cap], float32 [B, cap], int32 [B], int32 [B] or
+    None exactly when u is), whose entries past a row's count are left as
+    they were."""
     torch = _torch()
     B, V = _check_rows(logits)
     dev = logits.device
     if mask.shape != (B, V) or mask.dtype not in (torch.bool, torch.uint8) or not mask.is_contiguous():
         raise ValueError("mask must be a contiguous bool/uint8 [B, V] tensor")
     uu = _vec(u, B, torch.float32, "u", dev)
-    ids = torch.full((B, int(cap)), -1, dtype=torch.int32, device=dev)
-    probs = torch.zeros((B, int(cap)), dtype=torch.float32, device=dev)
-    count = torch.empty(B, dtype=torch.int32, device=dev)
-    sample = torch.empty(B, dtype=torch.int32, device=dev) if uu is not None else None
+    if out is None:
+        ids = torch.full((B, int(cap)), -1, dtype=torch.int32, device=dev)
+        probs = torch.zeros((B, int(cap)), dtype=torch.float32, device=dev)
+        count = torch.empty(B, dtype=torch.int32, device=dev)
+        sample = torch.empty(B, dtype=torch.int32, device=dev) if uu is not None else None
+    else:
+        ids, probs, count, sample = out
+        for t, shape, dt, name in ((ids, (B, int(cap)), torch.int32, "ids"), (probs, (B, int(cap)), torch.float32, "probs"),
+                                   (count, (B,), torch.int32, "count")):
+            if t.shape != shape or t.dtype != dt or not t.is_contiguous() or t.device != dev:
+                raise ValueError(f"out {name} must be a contiguous {dt} {list(shape)} tensor on {dev}")
+        if (sample is None) != (uu is None):
+            raise ValueError("out sample must be given exactly when u is")
+        if sample is not None and (sample.shape != (B,) or sample.dtype != torch.int32 or not sample.is_contiguous()
+                                   or sample.device != dev):
+            raise ValueError(f"out sample must be a contiguous int32 [{B}] tensor on {dev}")
     rc = lib().qrita_candidates(
         ctypes.c_void_p(logits.data_ptr() if B else 0), _dtype_code(logits), B, V,
         ctypes.c_void_p(mask.data_ptr() if B else 0), int(cap), ctypes.c_void_p(ids.data_ptr() if B else 0),

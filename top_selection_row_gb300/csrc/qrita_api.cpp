@@ -183,7 +183,7 @@ int select_impl(const void* logits, int dtype, int64_t B, int64_t V, const int32
   prm.chunk = sh.chunk;
   prm.ocap = sh.ocap;
   prm.flags = flags;
-  prm.heavy_first = (sh.multi_wave && B <= kMaxReorderRows && p != nullptr) ? 1 : 0;
+  prm.heavy_first = (sh.multi_wave && B <= kMaxReorderRows && (p != nullptr || k != nullptr)) ? 1 : 0;
   prm.alpha_k = kAlphaK;
   prm.alpha_min_k = kAlphaMinK;
   prm.margin_p = kMarginP;

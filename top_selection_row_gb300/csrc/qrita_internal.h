@@ -55,7 +55,7 @@ struct Params {
   int32_t chunk;    // elements per CTA (multiple of 16)
   int32_t ocap;     // own candidate list capacity per CTA (entries)
   uint32_t flags;   // QRITA_FLAG_*
-  int32_t heavy_first;  // more CTAs than fit at once: rows whose top-p runs alone start first
+  int32_t heavy_first;  // more CTAs than fit at once: the rows expected to run longest start first
   float alpha_k;    // top-k truncation safety factor (u = alpha_k * k / V)
   float alpha_min_k;  // the smallest factor used to keep the survivors within the lists
   float margin_p;   // subtracted from the top-p delta

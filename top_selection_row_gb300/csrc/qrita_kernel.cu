@@ -87,6 +87,11 @@ constexpr int kBinBytes = kBins * kThreads * (4 + 8);
 // g_cta_stage[cta][i] = globaltimer at mark i (0 start, 15 end).
 constexpr int kTraceCtas = 16384;
 __device__ unsigned long long g_cta_stage[kTraceCtas][16];
+__device__ long long g_cta_row[kTraceCtas];  // the row each CTA handled
+#define QRITA_ROWID(r)                                                                          \
+  do {                                                                                          \
+    if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_cta_row[blockIdx.x] = (r);               \
+  } while (0)
 #define QRITA_T(i)                                                                              \
   do {                                                                                          \
     if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_cta_stage[blockIdx.x][i] = globaltimer_ns(); \
@@ -96,6 +101,9 @@ __device__ unsigned long long g_cta_stage[kTraceCtas][16];
     if (threadIdx.x == 0 && blockIdx.x < kTraceCtas) g_cta_stage[blockIdx.x][i] = (v);         \
   } while (0)
 #else
+#define QRITA_ROWID(r) \
+  do {                 \
+  } while (0)
 #define QRITA_T(i) \
   do {             \
   } while (0)
@@ -270,12 +278,14 @@ enum : int {
   // uints
   BU_TRUNC = 0, BU_S, BU_OVF, BU_LO, BU_HI, BU_CLO, BU_CHI, BU_DONE, BU_TAU,
   BU_NKEEP, BU_CABOVE, BU_NP, BU_USED_VALUE, BU_VMODE, BU_MAXR, BU_BELOW, BU_FITS, BU_S2, BU_OVF2,
-  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW, BU_SAMPLE_T, BU_KWCA, BU_KWCB, BU_SGE,
+  BU_QKEY, BU_QWANT, BU_PHAC, BU_ROW, BU_SAMPLE_T, BU_KWCA, BU_KWCB, BU_SGE, BU_S2S,
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
   // float pairs
   BP_ZR = 0, BP_MR, BP_MLO, BP_MHI, BP_TOTAL, BP_GAP,
 };
+static_assert(BU_S2S < static_cast<int>(sizeof(Bcast::u) / sizeof(uint32_t)), "every uint slot fits the broadcast block");
+static_assert(BP_GAP < static_cast<int>(sizeof(Bcast::pr) / sizeof(float) / 2), "every pair slot fits the broadcast block");
 
 __device__ __forceinline__ void put_pair(Bcast& b, int i, F2 v) {
   b.pr[2 * i] = v.hi;
@@ -1393,11 +1403,16 @@ __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_abo
   uint32_t ca = 0;
   // the mass above hi is one constant offset of the search that follows, so
   // it is summed in compensated fp32 (a unit's partial at a time); the list's
-  // mass must equal what the search sums over the list: exact fixed point
+  // mass must equal what the search sums over the list: exact fixed point,
+  // summed over the list once it is complete
   F2 ma = {0.f, 0.f};
   unsigned long long mi = 0ull;
   const uintptr_t mbp = reinterpret_cast<uintptr_t>(c.gmask + c.head_n);
   const bool vec_ok = (mbp % E) == 0;
+  // key(x) > q as a float comparison, x > pivot_f(q), for keys at or above
+  // -inf's; a bound below it holds every element
+  const bool lo_all = lo < kKeyNegInf, hi_all = hi < kKeyNegInf;
+  const float lo_f = lo_all ? -INFINITY : pivot_f(lo), hi_f = hi_all ? -INFINITY : pivot_f(hi);
   stream_pieces<DT>(
       c,
       [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
@@ -1413,13 +1428,11 @@ __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_abo
 #pragma unroll
             for (int e = 0; e < E; ++e) {
               const float x = xs[j][e];
-              const uint32_t k = f2key(x);
-              const bool above = k > hi;
-              const bool in = !above && k > lo;
+              const bool above = hi_all || x > hi_f;
+              const bool in = !above && (lo_all || x > lo_f);
               const float w = weight(x, c.m, c.m_neginf);
               ca += above ? 1u : 0u;
               pa += above ? w : 0.f;
-              if (in) mi += round_u64(w * scale);
               keep |= above ? (1u << e) : 0u;
               bits[j] |= in ? (1u << e) : 0u;
             }
@@ -1449,10 +1462,8 @@ __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_abo
           const uint32_t k = f2key(x);
           const bool above = k > hi;
           const bool in = !above && k > lo;
-          const float w = weight(x, c.m, c.m_neginf);
           ca += above ? 1u : 0u;
-          if (above) f2_add(ma, w);
-          if (in) mi += round_u64(w * scale);
+          if (above) f2_add(ma, weight(x, c.m, c.m_neginf));
           bits = in ? 1u : 0u;
           c.gmask[idx] = above ? 1 : 0;
         }
@@ -1461,6 +1472,9 @@ __device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_abo
       },
       false);
   own_segments_streamed<DT>(c, wn);
+  // the list's exact mass (entries past a full segment are lost: the caller
+  // then does not use it)
+  own_for(c, [&](float x, uint32_t) { mi += round_u64(weight(x, c.m, c.m_neginf) * scale); });
   ca = __reduce_add_sync(kFull, ca);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
@@ -2937,35 +2951,59 @@ __device__ bool kw_emit(Ctx<DT>& c, float tau_f, int tie_mode, uint32_t keep_loc
   return true;
 }
 
-// Row of cluster slot `slot` when heavy rows go first: rows whose top-p runs
-// alone (their streaming pass weighs every logit, and most take more passes)
-// take the first slots, then the others, each group in row order, so the
-// longest rows start in the first wave. Every thread returns the row.
+// Row of cluster slot `slot` when the longest rows go first. Rows fall in
+// four cost classes, taken in this order, each in row order:
+//   3  top-p alone (the streaming pass weighs every logit; most take a
+//      second pass);
+//   2  top-k expecting more survivors than per-thread columns hold (every
+//      warp appends survivors piece by piece);
+//   1  the other top-k rows;
+//   0  rows that keep everything (one pass that writes ones).
+// So the longest rows start in the first wave and the shortest fill the
+// last. Every thread returns the row.
 __device__ int64_t heavy_first_row(const Params& P, Fixed& F, int64_t slot) {
   const int tid = threadIdx.x;
   const int64_t B = P.B;
   const int64_t per = (B + kThreads - 1) / kThreads;
   const int64_t r0 = min(B, static_cast<int64_t>(tid) * per), r1 = min(B, r0 + per);
-  auto heavy = [&](int64_t r) -> bool {
-    const int32_t k = P.k ? P.k[r] : 0;
+  const float col_rows = static_cast<float>(P.ocap / 8) * static_cast<float>(P.C);
+  auto cost_class = [&](int64_t r) -> int {
+    int32_t k = P.k ? P.k[r] : 0;
     const float p = P.p ? P.p[r] : 1.0f;
-    const bool k_on = k >= 1 && k < P.V;
-    return p < 1.0f && p > 0.0f && !k_on;
+    bool k_on = k >= 1 && k < P.V;
+    bool p_on = p < 1.0f;  // NaN: off
+    if (p_on && !(p > 0.0f)) {  // p <= 0 keeps one token, as k = 1
+      p_on = false;
+      k_on = P.V > 1;
+      k = 1;
+    }
+    if (!k_on && !p_on) return 0;
+    if (!k_on) return 3;
+    return 2.4f * static_cast<float>(k) > col_rows ? 2 : 1;
   };
-  uint32_t mine = 0;
-  for (int64_t r = r0; r < r1; ++r) mine += heavy(r) ? 1u : 0u;
-  uint32_t tot = 0;
-  const uint32_t before = block_excl_scan(F, mine, &tot);  // heavy rows below r0
-  const bool want_heavy = slot < static_cast<int64_t>(tot);
-  const int64_t want = want_heavy ? slot : slot - tot;
-  const int64_t have_before = want_heavy ? static_cast<int64_t>(before) : r0 - before;
-  const int64_t have = want_heavy ? static_cast<int64_t>(mine) : (r1 - r0) - mine;
+  // per-class counts, four 16-bit fields (B <= 65535 rows reorder)
+  unsigned long long mine = 0ull;
+  for (int64_t r = r0; r < r1; ++r) mine += 1ull << (16 * cost_class(r));
+  unsigned long long tot = 0ull;
+  const unsigned long long before = block_excl_scan_u64(F, mine, &tot);
+  auto field = [](unsigned long long v, int c) -> int64_t { return static_cast<int64_t>((v >> (16 * c)) & 0xFFFFull); };
+  // the slot's class and its rank within the class
+  int want_c = 0;
+  int64_t want = slot;
+  for (int c = 3; c >= 0; --c) {
+    if (want < field(tot, c)) {
+      want_c = c;
+      break;
+    }
+    want -= field(tot, c);
+  }
   if (tid == 0) F.bc.u[BU_ROW] = static_cast<uint32_t>(slot);  // unless a block holds it
   __syncthreads();
+  const int64_t have_before = field(before, want_c), have = field(mine, want_c);
   if (want >= have_before && want < have_before + have) {
     int64_t seen = have_before;
     for (int64_t r = r0; r < r1; ++r) {
-      if (heavy(r) == want_heavy) {
+      if (cost_class(r) == want_c) {
         if (seen == want) F.bc.u[BU_ROW] = static_cast<uint32_t>(r);
         ++seen;
       }
@@ -3039,6 +3077,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   c.npiv = (P.flags & QRITA_FLAG_SEARCH_BINARY) ? 1 : ((P.flags & QRITA_FLAG_SEARCH_QUATERNARY) ? 3 : kNarrowPivots);
   c.wide_ok = (P.flags & (QRITA_FLAG_SEARCH_BINARY | QRITA_FLAG_SEARCH_QUATERNARY)) == 0u;
   QRITA_T(0);
+  QRITA_ROWID(r);
 
   // ---- row parameters (uniform)
   int32_t kr = P.k ? P.k[r] : 0;
@@ -3196,29 +3235,46 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       F.bc.u[BU_TRUNC] = trunc ? 1u : 0u;
       F.bc.u[BU_SAMPLE_T] = 0u;
       F.bc.u[BU_SGE] = 0u;
+      F.bc.u[BU_S2S] = 0u;
     }
     __syncthreads();
     // A top-k threshold the sample contradicts (a quarter or less of the
     // sample values expected above the k-th logit lie above it, as on rows
     // bounded below the Gaussian tail): an order statistic of the sample with
     // a margin is the threshold instead, when its expected survivors fit.
+    // When fewer than two sample values are expected above the k-th logit,
+    // the sample cannot test t itself; there a tail much lighter than the
+    // Gaussian's (a quarter or less of the sample values it puts above
+    // mu + 2 sigma) and no sample value at or above t decide instead.
     if (k_on && vld(F.bc.u[BU_TRUNC]) != 0u &&
         (P.flags & (QRITA_FLAG_FORCE_FALLBACK | QRITA_FLAG_FORCE_RETRY)) == 0u) {
       const float tt = vld(F.bc.f[BF_T]);
+      const float t2s = fmaf(2.0f, vld(F.bc.f[BF_SIGMA]), vld(F.bc.f[BF_MU]));
       // the sample's count at or above t (high half) and of finite values
-      // (low half; at most kSampleBlocks * kSampleBlock), one block reduction
-      uint32_t ge_f = 0;
+      // (low half; at most kSampleBlocks * kSampleBlock), and its count at or
+      // above mu + 2 sigma, one block reduction
+      uint32_t ge_f = 0, ge_2s = 0;
 #pragma unroll
-      for (int j = 0; j < kPer; ++j) ge_f += (sv[j] >= tt ? 0x10000u : 0u) + (isnan(sv[j]) ? 0u : 1u);
+      for (int j = 0; j < kPer; ++j) {
+        ge_f += (sv[j] >= tt ? 0x10000u : 0u) + (isnan(sv[j]) ? 0u : 1u);
+        ge_2s += sv[j] >= t2s ? 1u : 0u;
+      }
       ge_f = __reduce_add_sync(kFull, ge_f);
-      if (lane == 0) atomicAdd(&F.bc.u[BU_SGE], ge_f);
+      ge_2s = __reduce_add_sync(kFull, ge_2s);
+      if (lane == 0) {
+        atomicAdd(&F.bc.u[BU_SGE], ge_f);
+        atomicAdd(&F.bc.u[BU_S2S], ge_2s);
+      }
       __syncthreads();
       const uint32_t tot_ge_f = vld(F.bc.u[BU_SGE]);
       const int n_ge = static_cast<int>(tot_ge_f >> 16), n_f = static_cast<int>(tot_ge_f & 0xFFFFu);
+      const int n_2s = static_cast<int>(vld(F.bc.u[BU_S2S]));
       const float lam = static_cast<float>(kr) * static_cast<float>(n_f) / static_cast<float>(V);
       const int jq = static_cast<int>(ceilf(lam + 3.0f * sqrtf(lam) + 3.0f));
       const float expect = static_cast<float>(jq) * static_cast<float>(V) / static_cast<float>(n_f > 0 ? n_f : 1);
-      if (n_f >= 256 && lam >= 2.0f && 4.0f * static_cast<float>(n_ge) < lam && jq <= n_f &&
+      // (P(X >= mu + 2 sigma) = 0.02275 for a Gaussian)
+      const bool light = 4.0f * static_cast<float>(n_2s) < 0.02275f * static_cast<float>(n_f);
+      if (n_f >= 256 && (lam >= 2.0f || light) && 4.0f * static_cast<float>(n_ge) < lam && jq <= n_f &&
           expect <= 0.85f * static_cast<float>(P.ocap) * static_cast<float>(P.C)) {
         // the jq-th largest sample value (histogram in the list region, free
         // here: the ring's first copies are in flight)
@@ -4587,6 +4643,11 @@ extern "C" int qrita_debug_stages(unsigned long long* out, int n) {
   cudaDeviceSynchronize();
   if (n > kTraceCtas) n = kTraceCtas;
   return static_cast<int>(cudaMemcpyFromSymbol(out, g_cta_stage, sizeof(unsigned long long) * 16 * n));
+}
+extern "C" int qrita_debug_rows(long long* out, int n) {
+  cudaDeviceSynchronize();
+  if (n > kTraceCtas) n = kTraceCtas;
+  return static_cast<int>(cudaMemcpyFromSymbol(out, g_cta_row, sizeof(long long) * n));
 }
 #endif
 

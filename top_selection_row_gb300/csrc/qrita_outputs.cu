@@ -230,6 +230,356 @@ __global__ void __launch_bounds__(kOutThreads) cand_kernel(const void* logits, i
   if (!draw && out_sample != nullptr && tid == 0) out_sample[r] = -1;
 }
 
+// ---------------------------------------------------------------------------
+// Vector forms of both kernels, for rows whose mask and logits start on a
+// 16-byte boundary (V a multiple of 16 and aligned base pointers): the row is
+// read in units of 16 elements (16 mask bytes, 64 or 32 logit bytes), warp w
+// owning a contiguous run of units and its lanes taking 32 consecutive units
+// a step, so every load is coalesced. Kept ids keep their order: a warp's
+// positions come from a warp scan per step and the warps' totals from one
+// block scan.
+// ---------------------------------------------------------------------------
+constexpr int kUnit = 16;  // elements per unit
+
+// Kept bits of one unit of 16 mask bytes: bit e for byte e nonzero.
+__device__ __forceinline__ uint32_t unit_kept_bits(const uint4 m) {
+  const uint32_t w[4] = {m.x, m.y, m.z, m.w};
+  uint32_t bits = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    // one bit per nonzero byte (bytes 0..3 to bits 0..3)
+    const uint32_t nz = __vcmpne4(w[i], 0u) & 0x01010101u;
+    bits |= ((nz * 0x01020408u) >> 24) << (4 * i);
+  }
+  return bits;
+}
+
+// The 16 logits of unit u of the row, widened to fp32.
+template <int DT>
+__device__ __forceinline__ void unit_logits(const void* lrow, int64_t u, float (&x)[kUnit]) {
+  if constexpr (DT == QRITA_DTYPE_F32) {
+    const uint4* p = static_cast<const uint4*>(lrow) + u * 4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = __ldg(p + q);
+      x[4 * q] = __uint_as_float(v.x);
+      x[4 * q + 1] = __uint_as_float(v.y);
+      x[4 * q + 2] = __uint_as_float(v.z);
+      x[4 * q + 3] = __uint_as_float(v.w);
+    }
+  } else {
+    const uint4* p = static_cast<const uint4*>(lrow) + u * 2;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 v = __ldg(p + q);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+        x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
+// Warp w's run of units [u_lo, u_hi) of a row of nu units.
+__device__ __forceinline__ void warp_units(int64_t nu, int64_t& u_lo, int64_t& u_hi) {
+  const int64_t per = (nu + kOutWarps - 1) / kOutWarps;
+  u_lo = min(nu, static_cast<int64_t>(threadIdx.x >> 5) * per);
+  u_hi = min(nu, u_lo + per);
+}
+
+// Exclusive warp scans (lane order) of a 32-bit and a 64-bit value; the
+// inclusive total comes back in *tot.
+__device__ __forceinline__ uint32_t warp_excl_u32(uint32_t v, uint32_t* tot) {
+  const int lane = threadIdx.x & 31;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += y;
+  }
+  *tot = __shfl_sync(kFullMask, incl, 31);
+  return incl - v;
+}
+
+__device__ __forceinline__ unsigned long long warp_excl_u64(unsigned long long v, unsigned long long* tot) {
+  const int lane = threadIdx.x & 31;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long y = __shfl_up_sync(kFullMask, incl, o);
+    if (lane >= o) incl += y;
+  }
+  *tot = __shfl_sync(kFullMask, incl, 31);
+  return incl - v;
+}
+
+// Exclusive scan over the warps of one value per warp (lane 0's), and the
+// block total; every thread gets its warp's base.
+template <typename T>
+__device__ __forceinline__ T warps_excl(T v, T* slots, T* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) slots[warp] = v;
+  __syncthreads();
+  T base = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kOutWarps; ++w) {
+    const T s = *reinterpret_cast<volatile T*>(&slots[w]);
+    base += w < warp ? s : T(0);
+    tot += s;
+  }
+  __syncthreads();
+  *total = tot;
+  return base;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kOutThreads) ids_kernel_vec(const void* logits, int64_t V, const int32_t* k,
+                                                              int32_t kmax, const uint8_t* mask, int32_t* out_ids) {
+  extern __shared__ __align__(16) unsigned long long keys[];  // [pow2 >= kmax]
+  __shared__ uint32_t warp_slots[kOutWarps];
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int32_t kr = k[r];
+  int32_t* orow = out_ids + r * static_cast<int64_t>(kmax);
+  const bool ok = kr >= 1 && kr <= kmax;
+  const int64_t nu = V / kUnit;
+  const uint4* mrow = reinterpret_cast<const uint4*>(mask + r * V);
+  const void* lrow = static_cast<const unsigned char*>(logits) + r * V * (DT == QRITA_DTYPE_F32 ? 4 : 2);
+  int64_t u_lo, u_hi;
+  warp_units(nu, u_lo, u_hi);
+  // pass 1: this warp's kept count (four units a lane in flight)
+  uint32_t cnt = 0;
+  if (ok) {
+    for (int64_t ub = u_lo + lane; ub < u_hi; ub += 128) {
+      uint4 mv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mv[j] = ub + 32 * j < u_hi ? __ldg(mrow + ub + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cnt += __popc(unit_kept_bits(mv[j]));
+    }
+  }
+  cnt = __reduce_add_sync(kFullMask, cnt);
+  uint32_t total = 0;
+  const uint32_t wbase = warps_excl<uint32_t>(cnt, warp_slots, &total);
+  const uint32_t n = ok ? min(total, static_cast<uint32_t>(kmax)) : 0u;
+  uint32_t np2 = 1;
+  while (np2 < n) np2 <<= 1;
+  // pass 2: the first n kept ids with their order keys, in id order
+  if (ok && wbase < n) {
+    uint32_t run = wbase;
+    for (int64_t ub = u_lo; ub < u_hi && run < n; ub += 32) {
+      const int64_t u = ub + lane;
+      const uint32_t bits = u < u_hi ? unit_kept_bits(__ldg(mrow + u)) : 0u;
+      uint32_t step = 0;
+      uint32_t pos = run + warp_excl_u32(__popc(bits), &step);
+      if (bits != 0u && pos < n) {
+        float x[kUnit];
+        unit_logits<DT>(lrow, u, x);
+        uint32_t b = bits;
+        while (b != 0u && pos < n) {
+          const int e = __ffs(b) - 1;
+          b &= b - 1u;
+          float xe = x[0];
+#pragma unroll
+          for (int q = 1; q < kUnit; ++q) xe = (q == e) ? x[q] : xe;
+          const uint32_t key = f2key(xe);
+          keys[pos++] = (static_cast<unsigned long long>(~key) << 32) | static_cast<uint32_t>(u * kUnit + e);
+        }
+      }
+      run += step;
+    }
+  }
+  for (uint32_t i = n + tid; i < np2; i += kOutThreads) keys[i] = ~0ull;  // padding sorts last
+  __syncthreads();
+  // bitonic sort, ascending
+  for (uint32_t size = 2; size <= np2; size <<= 1) {
+    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+      for (uint32_t t = tid; t < np2 / 2; t += kOutThreads) {
+        const uint32_t a = 2 * stride * (t / stride) + (t % stride);
+        const uint32_t b = a + stride;
+        const bool up = (a & size) == 0;
+        const unsigned long long ka = keys[a], kb = keys[b];
+        if ((ka > kb) == up) {
+          keys[a] = kb;
+          keys[b] = ka;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int32_t i = tid; i < kmax; i += kOutThreads)
+    orow[i] = static_cast<uint32_t>(i) < n ? static_cast<int32_t>(keys[i] & 0xFFFFFFFFull) : -1;
+}
+
+constexpr int kLaneUnits = 4;  // units a lane takes per step (loads in flight)
+
+// Candidate lists, vector form, in two passes over the row: (1) the kept
+// count and the largest kept logit; (2) in id order, the ids and their
+// fixed-point weights (written as floats up to cap), and each warp's mass.
+// Then the one warp whose mass range holds the draw's target walks its run
+// again to find the token, and the written weights are divided by the total.
+template <int DT>
+__global__ void __launch_bounds__(kOutThreads, 4) cand_kernel_vec(const void* logits, int64_t V, const uint8_t* mask,
+                                                                  int32_t cap, int32_t* out_ids, float* out_probs,
+                                                                  int32_t* out_count, const float* u,
+                                                                  int32_t* out_sample) {
+  __shared__ uint32_t warp_slots[kOutWarps];
+  __shared__ unsigned long long warp_slots64[kOutWarps];
+  __shared__ float warp_max[kOutWarps];
+  __shared__ int32_t sample_at;
+  const int64_t r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t nu = V / kUnit;
+  const uint4* mrow = reinterpret_cast<const uint4*>(mask + r * V);
+  const void* lrow = static_cast<const unsigned char*>(logits) + r * V * (DT == QRITA_DTYPE_F32 ? 4 : 2);
+  int64_t u_lo, u_hi;
+  warp_units(nu, u_lo, u_hi);
+  // pass 1: kept count and largest kept logit (units u_lo + lane + 32 j)
+  uint32_t cnt = 0;
+  float m = -INFINITY;
+  for (int64_t ub = u_lo; ub < u_hi; ub += 32 * kLaneUnits) {
+    uint32_t bits[kLaneUnits];
+#pragma unroll
+    for (int j = 0; j < kLaneUnits; ++j) {
+      const int64_t uu = ub + lane + 32 * j;
+      bits[j] = uu < u_hi ? unit_kept_bits(__ldg(mrow + uu)) : 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < kLaneUnits; ++j) {
+      if (bits[j] != 0u) {
+        cnt += __popc(bits[j]);
+        float x[kUnit];
+        unit_logits<DT>(lrow, ub + lane + 32 * j, x);
+#pragma unroll
+        for (int e = 0; e < kUnit; ++e) m = ((bits[j] >> e) & 1u) ? fmaxf(m, x[e]) : m;
+      }
+    }
+  }
+  cnt = __reduce_add_sync(kFullMask, cnt);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
+  if (lane == 0) warp_max[warp] = m;
+  uint32_t total = 0;
+  const uint32_t wbase = warps_excl<uint32_t>(cnt, warp_slots, &total);  // (its barriers publish warp_max)
+  float rm = -INFINITY;
+  for (int w = 0; w < kOutWarps; ++w) rm = fmaxf(rm, *reinterpret_cast<volatile float*>(&warp_max[w]));
+  if (tid == 0) {
+    out_count[r] = static_cast<int32_t>(total);
+    sample_at = -1;
+  }
+  const bool m_neginf = rm == -INFINITY;  // every kept logit is -inf: equal weights
+  const float scale = exp2f(static_cast<float>(62 - (32 - __clz(static_cast<uint32_t>(V)))));
+  auto wfx = [&](float x) -> unsigned long long {
+    float w = 1.0f;
+    if (!m_neginf) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(w) : "f"((x - rm) * 1.4426950408889634f));
+    return round_u64(w * scale);
+  };
+  // the kept weights of lane-contiguous units ub + kLaneUnits * lane + j, in
+  // id order; fn(id, w) per kept id
+  auto lane_units = [&](int64_t ub, uint32_t (&bits)[kLaneUnits]) {
+#pragma unroll
+    for (int j = 0; j < kLaneUnits; ++j) {
+      const int64_t uu = ub + kLaneUnits * lane + j;
+      bits[j] = uu < u_hi ? unit_kept_bits(__ldg(mrow + uu)) : 0u;
+    }
+  };
+  // pass 2: ids and weights in id order, this warp's mass
+  unsigned long long wmass = 0ull;
+  {
+    uint32_t run = wbase;
+    for (int64_t ub = u_lo; ub < u_hi; ub += 32 * kLaneUnits) {
+      uint32_t bits[kLaneUnits];
+      lane_units(ub, bits);
+      uint32_t c = 0;
+#pragma unroll
+      for (int j = 0; j < kLaneUnits; ++j) c += __popc(bits[j]);
+      uint32_t step_n = 0;
+      uint32_t pos = run + warp_excl_u32(c, &step_n);
+#pragma unroll
+      for (int j = 0; j < kLaneUnits; ++j) {
+        if (bits[j] != 0u) {
+          const int64_t uu = ub + kLaneUnits * lane + j;
+          float x[kUnit];
+          unit_logits<DT>(lrow, uu, x);
+#pragma unroll
+          for (int e = 0; e < kUnit; ++e) {
+            if ((bits[j] >> e) & 1u) {
+              const unsigned long long w = wfx(x[e]);
+              wmass += w;
+              if (pos < static_cast<uint32_t>(cap)) {
+                out_ids[r * cap + pos] = static_cast<int32_t>(uu * kUnit + e);
+                out_probs[r * cap + pos] = static_cast<float>(w);
+              }
+              ++pos;
+            }
+          }
+        }
+      }
+      run += step_n;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wmass += __shfl_xor_sync(kFullMask, wmass, o);
+  unsigned long long z = 0ull;
+  const unsigned long long mbase = warps_excl<unsigned long long>(wmass, warp_slots64, &z);
+  // (the barriers inside also order pass 2's writes before the division)
+  const bool draw = u != nullptr && out_sample != nullptr && total > 0u;
+  if (draw) {
+    const float uf = u[r];
+    const F2 t = f2_mul(f2_from_u64(z), uf);
+    const unsigned long long target = uf > 0.f ? f2_to_u64(t) : 0ull;
+    // the warp whose mass range holds the target walks its run again
+    if (mbase <= target && target < mbase + wmass) {
+      unsigned long long acc = mbase;
+      for (int64_t ub = u_lo; ub < u_hi; ub += 32 * kLaneUnits) {
+        uint32_t bits[kLaneUnits];
+        lane_units(ub, bits);
+        unsigned long long lm = 0ull;
+#pragma unroll
+        for (int j = 0; j < kLaneUnits; ++j) {
+          if (bits[j] != 0u) {
+            float x[kUnit];
+            unit_logits<DT>(lrow, ub + kLaneUnits * lane + j, x);
+#pragma unroll
+            for (int e = 0; e < kUnit; ++e)
+              if ((bits[j] >> e) & 1u) lm += wfx(x[e]);
+          }
+        }
+        unsigned long long step_m = 0ull;
+        unsigned long long a = acc + warp_excl_u64(lm, &step_m);
+        if (a <= target && target < a + lm) {
+#pragma unroll
+          for (int j = 0; j < kLaneUnits; ++j) {
+            if (bits[j] != 0u) {
+              const int64_t uu = ub + kLaneUnits * lane + j;
+              float x[kUnit];
+              unit_logits<DT>(lrow, uu, x);
+#pragma unroll
+              for (int e = 0; e < kUnit; ++e) {
+                if ((bits[j] >> e) & 1u) {
+                  const unsigned long long w = wfx(x[e]);
+                  if (a <= target && target < a + w) sample_at = static_cast<int32_t>(uu * kUnit + e);
+                  a += w;
+                }
+              }
+            }
+          }
+        }
+        acc += step_m;
+        if (acc > target) break;  // (warp-uniform)
+      }
+    }
+  }
+  const float zf = static_cast<float>(z);
+  const uint32_t nw = min(total, static_cast<uint32_t>(cap));
+  for (uint32_t i = tid; i < nw; i += kOutThreads) out_probs[r * cap + i] = out_probs[r * cap + i] / zf;
+  __syncthreads();
+  if (draw && tid == 0) out_sample[r] = *reinterpret_cast<volatile int32_t*>(&sample_at);
+  if (!draw && out_sample != nullptr && tid == 0) out_sample[r] = -1;
+}
+
 // The last kept id of the row (for a target past every cumulative sum).
 __global__ void __launch_bounds__(kOutThreads) last_kept_kernel(int64_t V, const uint8_t* mask, int32_t* out_sample) {
   const int64_t r = blockIdx.x;
@@ -261,33 +611,55 @@ size_t ids_smem_bytes(int32_t kmax) {
   return np2 * sizeof(unsigned long long);
 }
 
+// The vector kernels' condition: every row of the mask and of the logits
+// starts on a 16-byte boundary.
+static bool vec_rows(const void* logits, const uint8_t* mask, int64_t V) {
+  return V % kUnit == 0 && reinterpret_cast<uintptr_t>(logits) % 16u == 0u &&
+         reinterpret_cast<uintptr_t>(mask) % 16u == 0u;
+}
+
+template <int DT>
+static cudaError_t launch_ids_t(const void* logits, int64_t B, int64_t V, const int32_t* k, int32_t kmax, const uint8_t* mask,
+                         int32_t* out_ids, size_t smem, cudaStream_t st) {
+  const bool vec = vec_rows(logits, mask, V);
+  const void* fn = vec ? reinterpret_cast<const void*>(&ids_kernel_vec<DT>) : reinterpret_cast<const void*>(&ids_kernel<DT>);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  if (vec) ids_kernel_vec<DT><<<static_cast<unsigned>(B), kOutThreads, smem, st>>>(logits, V, k, kmax, mask, out_ids);
+  else ids_kernel<DT><<<static_cast<unsigned>(B), kOutThreads, smem, st>>>(logits, V, k, kmax, mask, out_ids);
+  return cudaGetLastError();
+}
+
 int launch_ids(const void* logits, int dtype, int64_t B, int64_t V, const int32_t* k, int32_t kmax,
                const uint8_t* mask, int32_t* out_ids, qrita_stream_t stream) {
   const size_t smem = ids_smem_bytes(kmax);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e;
-  if (dtype == QRITA_DTYPE_F32) {
-    e = cudaFuncSetAttribute(ids_kernel<QRITA_DTYPE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return static_cast<int>(e);
-    ids_kernel<QRITA_DTYPE_F32><<<static_cast<unsigned>(B), kOutThreads, smem, st>>>(logits, V, k, kmax, mask, out_ids);
-  } else {
-    e = cudaFuncSetAttribute(ids_kernel<QRITA_DTYPE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return static_cast<int>(e);
-    ids_kernel<QRITA_DTYPE_BF16><<<static_cast<unsigned>(B), kOutThreads, smem, st>>>(logits, V, k, kmax, mask, out_ids);
-  }
-  return static_cast<int>(cudaGetLastError());
+  const cudaError_t e = dtype == QRITA_DTYPE_F32
+                            ? launch_ids_t<QRITA_DTYPE_F32>(logits, B, V, k, kmax, mask, out_ids, smem, st)
+                            : launch_ids_t<QRITA_DTYPE_BF16>(logits, B, V, k, kmax, mask, out_ids, smem, st);
+  return static_cast<int>(e);
 }
 
 int launch_candidates(const void* logits, int dtype, int64_t B, int64_t V, const uint8_t* mask, int32_t cap,
                       int32_t* out_ids, float* out_probs, int32_t* out_count, const float* u, int32_t* out_sample,
                       qrita_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const bool vec = vec_rows(logits, mask, V);
+  const unsigned g = static_cast<unsigned>(B);
   if (dtype == QRITA_DTYPE_F32) {
-    cand_kernel<QRITA_DTYPE_F32><<<static_cast<unsigned>(B), kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids,
-                                                                                   out_probs, out_count, u, out_sample);
+    if (vec)
+      cand_kernel_vec<QRITA_DTYPE_F32><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count, u,
+                                                                  out_sample);
+    else
+      cand_kernel<QRITA_DTYPE_F32><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count, u,
+                                                              out_sample);
   } else {
-    cand_kernel<QRITA_DTYPE_BF16><<<static_cast<unsigned>(B), kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids,
-                                                                                    out_probs, out_count, u, out_sample);
+    if (vec)
+      cand_kernel_vec<QRITA_DTYPE_BF16><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count,
+                                                                   u, out_sample);
+    else
+      cand_kernel<QRITA_DTYPE_BF16><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count, u,
+                                                               out_sample);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
