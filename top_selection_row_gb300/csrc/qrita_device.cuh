@@ -281,6 +281,18 @@ __device__ __forceinline__ void red_inc_shared_if(uint32_t* p, bool cond) {
       : "memory");
 }
 
+// The same two on a 32-bit shared-window address (a base from smem_u32 plus
+// a byte offset), so hot loops form no 64-bit generic address per update.
+__device__ __forceinline__ void red_inc_shared_at_if(uint32_t saddr, bool cond) {
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t@q red.shared.add.u32 [%0], 1;\n\t}" ::"r"(saddr),
+               "r"(cond ? 1u : 0u)
+               : "memory");
+}
+
+__device__ __forceinline__ void red_add_shared_at(uint32_t saddr, uint32_t v) {
+  asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+
 // Shared-memory add without a returned value.
 __device__ __forceinline__ void red_add_shared_u32(uint32_t* p, uint32_t v) {
   asm volatile("red.shared.add.u32 [%0], %1;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(p))), "r"(v)

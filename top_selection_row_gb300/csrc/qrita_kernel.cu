@@ -713,27 +713,20 @@ __device__ __forceinline__ float bf16_bit_value(const uint4 v, int p) {
 }
 
 // append_piece for bf16 units in the packed bit layout: the values come
-// straight from the raw units (only survivors are widened).
+// straight from the raw units (only survivors are widened). A lane with
+// survivors claims its slots of the warp's segment with one shared atomic on
+// the warp's running count (F.seg_n[warp], zeroed before the pass): the
+// segment is unordered, so no warp scan is needed.
 template <int DT>
-__device__ __forceinline__ void append_piece_bf16(Ctx<DT>& c, uint32_t& wn, uint32_t seg_base, uint32_t segcap,
+__device__ __forceinline__ void append_piece_bf16(Ctx<DT>& c, uint32_t seg_base, uint32_t segcap,
                                                   const uint4 (&v)[kPieceThreadUnits],
                                                   const uint32_t (&bits)[kPieceThreadUnits], int u0) {
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   uint32_t cnt = 0;
 #pragma unroll
   for (int j = 0; j < kPieceThreadUnits; ++j) cnt += __popc(bits[j]);
-  if (__ballot_sync(kFull, cnt != 0u) == 0u) return;
-  constexpr int kPlanes = 32 - __builtin_clz(static_cast<unsigned>(kPieceThreadUnits * 8));
-  const uint32_t lt = (1u << lane) - 1u;
-  uint32_t excl = 0, tot = 0;
-#pragma unroll
-  for (int b = 0; b < kPlanes; ++b) {
-    const uint32_t plane = __ballot_sync(kFull, (cnt >> b) & 1u);
-    excl += static_cast<uint32_t>(__popc(plane & lt)) << b;
-    tot += static_cast<uint32_t>(__popc(plane)) << b;
-  }
-  uint32_t pos = wn + excl;
-  wn += tot;
+  if (cnt == 0u) return;
+  uint32_t pos = atomicAdd(&c.F->seg_n[warp], cnt);
 #pragma unroll
   for (int j = 0; j < kPieceThreadUnits; ++j) {
     uint32_t b = bits[j];
@@ -2575,9 +2568,10 @@ __device__ KeyHist keyhist_select(Ctx<DT>& c, uint32_t kk, bool p_on, float pr, 
   __syncthreads();  // earlier users of the ring's bytes are done
   for (uint32_t i = tid; i < span; i += kThreads) lh[i] = 0u;
   __syncthreads();
+  const uint32_t lh_s = smem_u32(lh);
   own_for(c, [&](float x, uint32_t) {
     const uint32_t b = key16_of(x) - base16;
-    red_inc_shared_if(&lh[b < span ? b : 0u], b < span);
+    red_inc_shared_at_if(lh_s + 4u * (b < span ? b : 0u), b < span);
   });
   if (c.C > 1) {
     cluster_sync_all();  // every CTA's counts are complete
@@ -3377,6 +3371,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       t2 = tb | (tb << 16);
     }
     uint32_t wn = 0;  // this warp's survivors (its segment of the own list)
+    if (lane == 0) F.seg_n[warp] = 0u;  // (the bf16 pieces count there; stream_pieces opens with a barrier)
     const uint32_t segcap = c.ocap / kWarps;
     const uint32_t seg_base = static_cast<uint32_t>(warp) * segcap;
     F2 zs = {0.f, 0.f}, ms = {0.f, 0.f};
@@ -3415,6 +3410,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     };
     uint32_t* ph_cnt = reinterpret_cast<uint32_t*>(c.lists) + warp * kHistBins;
     uint32_t* ph_mass = ph_cnt + kWarps * kHistBins;
+    const uint32_t ph_cnt_s = smem_u32(ph_cnt), ph_mass_s = smem_u32(ph_mass);
     uint32_t ph_n = 0, ph_ac = 0;  // survivors; those above ph_hi
     float ph_am = 0.f;             // and the latter's weight (shift m_ref)
     auto ph_bin = [&](float x, float w) {
@@ -3422,8 +3418,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       if (x <= ph_hi) {
         int b = static_cast<int>((x - t) * ph_inv_w);
         b = b > kHistBins - 1 ? kHistBins - 1 : b;
-        red_add_shared_u32(&ph_cnt[b], 1u);
-        red_add_shared_u32(&ph_mass[b], __float2uint_rn(w * ph_scale));
+        red_add_shared_at(ph_cnt_s + 4u * static_cast<uint32_t>(b), 1u);
+        red_add_shared_at(ph_mass_s + 4u * static_cast<uint32_t>(b), __float2uint_rn(w * ph_scale));
       } else {
         ++ph_ac;
         ph_am += w;
@@ -3464,7 +3460,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   }
                 }
               } else {
-                append_piece_bf16<DT>(c, wn, seg_base, segcap, v, bits, u0);
+                append_piece_bf16<DT>(c, seg_base, segcap, v, bits, u0);
               }
               return;
             }
@@ -3518,6 +3514,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             }
           },
           [&](float x, uint32_t idx, bool valid) {
+            if constexpr (DT == QRITA_DTYPE_BF16 && !PO && !COL) {
+              // the pieces counted this warp's survivors in F.seg_n[warp]
+              __syncwarp();
+              wn = vld(F.seg_n[warp]);
+              __syncwarp();
+            }
             uint32_t bits = 0;
             if (valid) {
               vmax = fmax_nan(vmax, x);
@@ -3577,11 +3579,12 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
           return w ^ ((sgn * 0x7FFFu) | 0x80008000u);
         };
         // one key: counted in its bin (predicated, no branch), or marked rare
+        const uint32_t kwh_s = smem_u32(kwh);
         auto kw_key = [&](uint32_t k) -> bool {
           const uint32_t d = k - kwin.lo0;
           const bool in_bot = d < kwin.bot_span;
           const bool in = in_bot || d - top_off < kwin.top_span;
-          red_inc_shared_if(&kwh[in_bot ? d : (in ? d - kwin.blob_len : 0u)], in);
+          red_inc_shared_at_if(kwh_s + 4u * (in_bot ? d : (in ? d - kwin.blob_len : 0u)), in);
           return in;
         };
         auto kw_unit = [&](const uint4 u) {

@@ -6,6 +6,7 @@
 // verification and reinforcement learning consume. Both kernels read a row's
 // keep-mask (from the selection kernel) and its logits; one CTA per row.
 
+#include <cstddef>
 #include <cstdint>
 
 #include <cuda_runtime.h>
@@ -334,6 +335,61 @@ __device__ __forceinline__ T warps_excl(T v, T* slots, T* total) {
   return base;
 }
 
+// Units a lane takes per step, and the 16-byte words of one unit's logits:
+// every load of a step (its masks, then the logits of its units that keep
+// anything, predicated) is issued before any result is used.
+template <int DT>
+struct StepShape {
+  static constexpr int kWords = DT == QRITA_DTYPE_F32 ? 4 : 2;
+  static constexpr int kUnits = DT == QRITA_DTYPE_F32 ? 2 : 4;
+};
+
+// Units u_first + j * stride (j < kUnits, below u_hi): kept bits and raw logits.
+template <int DT>
+__device__ __forceinline__ void load_step(const uint4* mrow, const void* lrow, int64_t u_first, int64_t stride,
+                                          int64_t u_hi, uint32_t (&bits)[StepShape<DT>::kUnits],
+                                          uint4 (&raw)[StepShape<DT>::kUnits][StepShape<DT>::kWords]) {
+  constexpr int NU = StepShape<DT>::kUnits, NW = StepShape<DT>::kWords;
+  uint4 mv[NU];
+#pragma unroll
+  for (int j = 0; j < NU; ++j) {
+    const int64_t uu = u_first + j * stride;
+    mv[j] = uu < u_hi ? __ldg(mrow + uu) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int j = 0; j < NU; ++j) bits[j] = unit_kept_bits(mv[j]);
+  const uint4* lp = static_cast<const uint4*>(lrow);
+#pragma unroll
+  for (int j = 0; j < NU; ++j) {
+    const int64_t uu = u_first + j * stride;
+#pragma unroll
+    for (int q = 0; q < NW; ++q) raw[j][q] = bits[j] != 0u ? __ldg(lp + uu * NW + q) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ void widen_unit(const uint4 (&raw)[StepShape<DT>::kWords], float (&x)[kUnit]) {
+  if constexpr (DT == QRITA_DTYPE_F32) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      x[4 * q] = __uint_as_float(raw[q].x);
+      x[4 * q + 1] = __uint_as_float(raw[q].y);
+      x[4 * q + 2] = __uint_as_float(raw[q].z);
+      x[4 * q + 3] = __uint_as_float(raw[q].w);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[8 * q + 2 * i] = __uint_as_float(w[i] << 16);
+        x[8 * q + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
 template <int DT>
 __global__ void __launch_bounds__(kOutThreads) ids_kernel_vec(const void* logits, int64_t V, const int32_t* k,
                                                               int32_t kmax, const uint8_t* mask, int32_t* out_ids) {
@@ -366,26 +422,34 @@ __global__ void __launch_bounds__(kOutThreads) ids_kernel_vec(const void* logits
   const uint32_t n = ok ? min(total, static_cast<uint32_t>(kmax)) : 0u;
   uint32_t np2 = 1;
   while (np2 < n) np2 <<= 1;
-  // pass 2: the first n kept ids with their order keys, in id order
+  // pass 2: the first n kept ids with their order keys, in id order (units
+  // ub + NU lane + j, every load of a step in flight together)
   if (ok && wbase < n) {
+    constexpr int NU = StepShape<DT>::kUnits, NW = StepShape<DT>::kWords;
     uint32_t run = wbase;
-    for (int64_t ub = u_lo; ub < u_hi && run < n; ub += 32) {
-      const int64_t u = ub + lane;
-      const uint32_t bits = u < u_hi ? unit_kept_bits(__ldg(mrow + u)) : 0u;
-      uint32_t step = 0;
-      uint32_t pos = run + warp_excl_u32(__popc(bits), &step);
-      if (bits != 0u && pos < n) {
-        float x[kUnit];
-        unit_logits<DT>(lrow, u, x);
-        uint32_t b = bits;
-        while (b != 0u && pos < n) {
-          const int e = __ffs(b) - 1;
-          b &= b - 1u;
-          float xe = x[0];
+    for (int64_t ub = u_lo; ub < u_hi && run < n; ub += 32 * NU) {
+      uint32_t bits[NU];
+      uint4 raw[NU][NW];
+      load_step<DT>(mrow, lrow, ub + NU * lane, 1, u_hi, bits, raw);
+      uint32_t c = 0;
 #pragma unroll
-          for (int q = 1; q < kUnit; ++q) xe = (q == e) ? x[q] : xe;
-          const uint32_t key = f2key(xe);
-          keys[pos++] = (static_cast<unsigned long long>(~key) << 32) | static_cast<uint32_t>(u * kUnit + e);
+      for (int j = 0; j < NU; ++j) c += __popc(bits[j]);
+      uint32_t step = 0;
+      uint32_t pos = run + warp_excl_u32(c, &step);
+#pragma unroll
+      for (int j = 0; j < NU; ++j) {
+        if (bits[j] != 0u) {
+          const int64_t uu = ub + NU * lane + j;
+          float x[kUnit];
+          widen_unit<DT>(raw[j], x);
+#pragma unroll
+          for (int e = 0; e < kUnit; ++e) {
+            if (((bits[j] >> e) & 1u) && pos < n) {
+              const uint32_t key = f2key(x[e]);
+              keys[pos] = (static_cast<unsigned long long>(~key) << 32) | static_cast<uint32_t>(uu * kUnit + e);
+            }
+            pos += (bits[j] >> e) & 1u;
+          }
         }
       }
       run += step;
@@ -413,62 +477,82 @@ __global__ void __launch_bounds__(kOutThreads) ids_kernel_vec(const void* logits
     orow[i] = static_cast<uint32_t>(i) < n ? static_cast<int32_t>(keys[i] & 0xFFFFFFFFull) : -1;
 }
 
-constexpr int kLaneUnits = 4;  // units a lane takes per step (loads in flight)
+// Candidate lists, vector form: a row is split over a cluster of C CTAs
+// (contiguous runs of units, rank order = id order), merged through
+// distributed shared memory, in two passes over the row: (1) the kept count
+// and the largest kept logit; (2) in id order, the ids and their fixed-point
+// weights (written as floats up to cap), and each CTA's mass. Then the one
+// warp whose mass range holds the draw's target walks its run again to find
+// the token, and the written weights are divided by the total.
+struct alignas(16) CandPub {  // what one CTA publishes to its cluster
+  unsigned long long mass;
+  uint32_t cnt;
+  float mx;
+};
 
-// Candidate lists, vector form, in two passes over the row: (1) the kept
-// count and the largest kept logit; (2) in id order, the ids and their
-// fixed-point weights (written as floats up to cap), and each warp's mass.
-// Then the one warp whose mass range holds the draw's target walks its run
-// again to find the token, and the written weights are divided by the total.
 template <int DT>
-__global__ void __launch_bounds__(kOutThreads, 4) cand_kernel_vec(const void* logits, int64_t V, const uint8_t* mask,
+__global__ void __launch_bounds__(kOutThreads, 3) cand_kernel_vec(const void* logits, int64_t V, const uint8_t* mask,
                                                                   int32_t cap, int32_t* out_ids, float* out_probs,
                                                                   int32_t* out_count, const float* u,
                                                                   int32_t* out_sample) {
+  constexpr int NU = StepShape<DT>::kUnits, NW = StepShape<DT>::kWords;
   __shared__ uint32_t warp_slots[kOutWarps];
   __shared__ unsigned long long warp_slots64[kOutWarps];
   __shared__ float warp_max[kOutWarps];
-  __shared__ int32_t sample_at;
-  const int64_t r = blockIdx.x;
+  __shared__ CandPub pub;
+  uint32_t C;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
+  const uint32_t cr = cluster_rank();
+  const int64_t r = blockIdx.x / C;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t nu = V / kUnit;
   const uint4* mrow = reinterpret_cast<const uint4*>(mask + r * V);
   const void* lrow = static_cast<const unsigned char*>(logits) + r * V * (DT == QRITA_DTYPE_F32 ? 4 : 2);
-  int64_t u_lo, u_hi;
-  warp_units(nu, u_lo, u_hi);
-  // pass 1: kept count and largest kept logit (units u_lo + lane + 32 j)
+  // this CTA's run of units, then its warp's
+  const int64_t per_cta = (nu + C - 1) / C;
+  const int64_t c_lo = min(nu, static_cast<int64_t>(cr) * per_cta), c_hi = min(nu, c_lo + per_cta);
+  const int64_t per_w = (c_hi - c_lo + kOutWarps - 1) / kOutWarps;
+  const int64_t u_lo = min(c_hi, c_lo + warp * per_w), u_hi = min(c_hi, u_lo + per_w);
+  // pass 1: kept count and largest kept logit (units ub + lane + 32 j)
   uint32_t cnt = 0;
   float m = -INFINITY;
-  for (int64_t ub = u_lo; ub < u_hi; ub += 32 * kLaneUnits) {
-    uint32_t bits[kLaneUnits];
+  for (int64_t ub = u_lo; ub < u_hi; ub += 32 * NU) {
+    uint32_t bits[NU];
+    uint4 raw[NU][NW];
+    load_step<DT>(mrow, lrow, ub + lane, 32, u_hi, bits, raw);
 #pragma unroll
-    for (int j = 0; j < kLaneUnits; ++j) {
-      const int64_t uu = ub + lane + 32 * j;
-      bits[j] = uu < u_hi ? unit_kept_bits(__ldg(mrow + uu)) : 0u;
-    }
+    for (int j = 0; j < NU; ++j) {
+      cnt += __popc(bits[j]);
+      float x[kUnit];
+      widen_unit<DT>(raw[j], x);
 #pragma unroll
-    for (int j = 0; j < kLaneUnits; ++j) {
-      if (bits[j] != 0u) {
-        cnt += __popc(bits[j]);
-        float x[kUnit];
-        unit_logits<DT>(lrow, ub + lane + 32 * j, x);
-#pragma unroll
-        for (int e = 0; e < kUnit; ++e) m = ((bits[j] >> e) & 1u) ? fmaxf(m, x[e]) : m;
-      }
+      for (int e = 0; e < kUnit; ++e) m = ((bits[j] >> e) & 1u) ? fmaxf(m, x[e]) : m;
     }
   }
   cnt = __reduce_add_sync(kFullMask, cnt);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, o));
   if (lane == 0) warp_max[warp] = m;
-  uint32_t total = 0;
-  const uint32_t wbase = warps_excl<uint32_t>(cnt, warp_slots, &total);  // (its barriers publish warp_max)
-  float rm = -INFINITY;
-  for (int w = 0; w < kOutWarps; ++w) rm = fmaxf(rm, *reinterpret_cast<volatile float*>(&warp_max[w]));
+  uint32_t cta_cnt = 0;
+  const uint32_t wbase = warps_excl<uint32_t>(cnt, warp_slots, &cta_cnt);  // (its barriers publish warp_max)
   if (tid == 0) {
-    out_count[r] = static_cast<int32_t>(total);
-    sample_at = -1;
+    float cm = -INFINITY;
+    for (int w = 0; w < kOutWarps; ++w) cm = fmaxf(cm, *reinterpret_cast<volatile float*>(&warp_max[w]));
+    pub.cnt = cta_cnt;
+    pub.mx = cm;
+    if (cr == 0u && out_sample != nullptr) out_sample[r] = -1;  // a draw below overwrites it
   }
+  cluster_sync_all();  // every CTA's count and max are published
+  uint32_t total = 0, cbase = 0;
+  float rm = -INFINITY;
+  for (uint32_t q = 0; q < C; ++q) {
+    const uint32_t a = map_rank(smem_u32(&pub), q);
+    const uint32_t n = ld_dsmem_u32(a + offsetof(CandPub, cnt));
+    total += n;
+    cbase += q < cr ? n : 0u;
+    rm = fmaxf(rm, ld_dsmem_f32(a + offsetof(CandPub, mx)));
+  }
+  if (cr == 0u && tid == 0) out_count[r] = static_cast<int32_t>(total);
   const bool m_neginf = rm == -INFINITY;  // every kept logit is -inf: equal weights
   const float scale = exp2f(static_cast<float>(62 - (32 - __clz(static_cast<uint32_t>(V)))));
   auto wfx = [&](float x) -> unsigned long long {
@@ -476,33 +560,26 @@ __global__ void __launch_bounds__(kOutThreads, 4) cand_kernel_vec(const void* lo
     if (!m_neginf) asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(w) : "f"((x - rm) * 1.4426950408889634f));
     return round_u64(w * scale);
   };
-  // the kept weights of lane-contiguous units ub + kLaneUnits * lane + j, in
-  // id order; fn(id, w) per kept id
-  auto lane_units = [&](int64_t ub, uint32_t (&bits)[kLaneUnits]) {
-#pragma unroll
-    for (int j = 0; j < kLaneUnits; ++j) {
-      const int64_t uu = ub + kLaneUnits * lane + j;
-      bits[j] = uu < u_hi ? unit_kept_bits(__ldg(mrow + uu)) : 0u;
-    }
-  };
-  // pass 2: ids and weights in id order, this warp's mass
+  // pass 2: ids and weights in id order (units ub + NU lane + j), this
+  // warp's mass
   unsigned long long wmass = 0ull;
   {
-    uint32_t run = wbase;
-    for (int64_t ub = u_lo; ub < u_hi; ub += 32 * kLaneUnits) {
-      uint32_t bits[kLaneUnits];
-      lane_units(ub, bits);
+    uint32_t run = cbase + wbase;
+    for (int64_t ub = u_lo; ub < u_hi; ub += 32 * NU) {
+      uint32_t bits[NU];
+      uint4 raw[NU][NW];
+      load_step<DT>(mrow, lrow, ub + NU * lane, 1, u_hi, bits, raw);
       uint32_t c = 0;
 #pragma unroll
-      for (int j = 0; j < kLaneUnits; ++j) c += __popc(bits[j]);
+      for (int j = 0; j < NU; ++j) c += __popc(bits[j]);
       uint32_t step_n = 0;
       uint32_t pos = run + warp_excl_u32(c, &step_n);
 #pragma unroll
-      for (int j = 0; j < kLaneUnits; ++j) {
+      for (int j = 0; j < NU; ++j) {
         if (bits[j] != 0u) {
-          const int64_t uu = ub + kLaneUnits * lane + j;
+          const int64_t uu = ub + NU * lane + j;
           float x[kUnit];
-          unit_logits<DT>(lrow, uu, x);
+          widen_unit<DT>(raw[j], x);
 #pragma unroll
           for (int e = 0; e < kUnit; ++e) {
             if ((bits[j] >> e) & 1u) {
@@ -522,9 +599,19 @@ __global__ void __launch_bounds__(kOutThreads, 4) cand_kernel_vec(const void* lo
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wmass += __shfl_xor_sync(kFullMask, wmass, o);
-  unsigned long long z = 0ull;
-  const unsigned long long mbase = warps_excl<unsigned long long>(wmass, warp_slots64, &z);
-  // (the barriers inside also order pass 2's writes before the division)
+  unsigned long long cta_mass = 0ull;
+  const unsigned long long wmbase = warps_excl<unsigned long long>(wmass, warp_slots64, &cta_mass);
+  if (tid == 0) pub.mass = cta_mass;
+  cluster_sync_all();  // every CTA's mass is published (and its writes done)
+  unsigned long long z = 0ull, mcbase = 0ull;
+  for (uint32_t q = 0; q < C; ++q) {
+    const uint32_t a = map_rank(smem_u32(&pub), q) + offsetof(CandPub, mass);
+    const unsigned long long v = static_cast<unsigned long long>(ld_dsmem_u32(a)) |
+                                 (static_cast<unsigned long long>(ld_dsmem_u32(a + 4u)) << 32);
+    z += v;
+    mcbase += q < cr ? v : 0ull;
+  }
+  const unsigned long long mbase = mcbase + wmbase;
   const bool draw = u != nullptr && out_sample != nullptr && total > 0u;
   if (draw) {
     const float uf = u[r];
@@ -533,36 +620,37 @@ __global__ void __launch_bounds__(kOutThreads, 4) cand_kernel_vec(const void* lo
     // the warp whose mass range holds the target walks its run again
     if (mbase <= target && target < mbase + wmass) {
       unsigned long long acc = mbase;
-      for (int64_t ub = u_lo; ub < u_hi; ub += 32 * kLaneUnits) {
-        uint32_t bits[kLaneUnits];
-        lane_units(ub, bits);
+      for (int64_t ub = u_lo; ub < u_hi; ub += 32 * NU) {
+        uint32_t bits[NU];
+        uint4 raw[NU][NW];
+        load_step<DT>(mrow, lrow, ub + NU * lane, 1, u_hi, bits, raw);
         unsigned long long lm = 0ull;
 #pragma unroll
-        for (int j = 0; j < kLaneUnits; ++j) {
-          if (bits[j] != 0u) {
-            float x[kUnit];
-            unit_logits<DT>(lrow, ub + kLaneUnits * lane + j, x);
+        for (int j = 0; j < NU; ++j) {
+          float x[kUnit];
+          widen_unit<DT>(raw[j], x);
 #pragma unroll
-            for (int e = 0; e < kUnit; ++e)
-              if ((bits[j] >> e) & 1u) lm += wfx(x[e]);
-          }
+          for (int e = 0; e < kUnit; ++e)
+            if ((bits[j] >> e) & 1u) lm += wfx(x[e]);
         }
         unsigned long long step_m = 0ull;
         unsigned long long a = acc + warp_excl_u64(lm, &step_m);
         if (a <= target && target < a + lm) {
+          // this lane holds the token: walk its kept ids again (reloaded:
+          // one lane of the row does this)
+          for (int j = 0; j < NU; ++j) {
+            const int64_t uu = ub + NU * lane + j;
+            if (uu >= u_hi) break;
+            const uint32_t bj = unit_kept_bits(__ldg(mrow + uu));
+            if (bj == 0u) continue;
+            float x[kUnit];
+            unit_logits<DT>(lrow, uu, x);
 #pragma unroll
-          for (int j = 0; j < kLaneUnits; ++j) {
-            if (bits[j] != 0u) {
-              const int64_t uu = ub + kLaneUnits * lane + j;
-              float x[kUnit];
-              unit_logits<DT>(lrow, uu, x);
-#pragma unroll
-              for (int e = 0; e < kUnit; ++e) {
-                if ((bits[j] >> e) & 1u) {
-                  const unsigned long long w = wfx(x[e]);
-                  if (a <= target && target < a + w) sample_at = static_cast<int32_t>(uu * kUnit + e);
-                  a += w;
-                }
+            for (int e = 0; e < kUnit; ++e) {
+              if ((bj >> e) & 1u) {
+                const unsigned long long w = wfx(x[e]);
+                if (a <= target && target < a + w) out_sample[r] = static_cast<int32_t>(uu * kUnit + e);
+                a += w;
               }
             }
           }
@@ -572,12 +660,12 @@ __global__ void __launch_bounds__(kOutThreads, 4) cand_kernel_vec(const void* lo
       }
     }
   }
+  // this CTA's written weights to probabilities
   const float zf = static_cast<float>(z);
-  const uint32_t nw = min(total, static_cast<uint32_t>(cap));
-  for (uint32_t i = tid; i < nw; i += kOutThreads) out_probs[r * cap + i] = out_probs[r * cap + i] / zf;
-  __syncthreads();
-  if (draw && tid == 0) out_sample[r] = *reinterpret_cast<volatile int32_t*>(&sample_at);
-  if (!draw && out_sample != nullptr && tid == 0) out_sample[r] = -1;
+  const uint32_t w_lo = min(cbase, static_cast<uint32_t>(cap));
+  const uint32_t w_hi = min(cbase + cta_cnt, static_cast<uint32_t>(cap));
+  for (uint32_t i = w_lo + tid; i < w_hi; i += kOutThreads) out_probs[r * cap + i] = out_probs[r * cap + i] / zf;
+  cluster_sync_all();  // no CTA leaves while another may read its published values
 }
 
 // The last kept id of the row (for a target past every cumulative sum).
@@ -646,25 +734,43 @@ int launch_candidates(const void* logits, int dtype, int64_t B, int64_t V, const
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool vec = vec_rows(logits, mask, V);
   const unsigned g = static_cast<unsigned>(B);
-  if (dtype == QRITA_DTYPE_F32) {
-    if (vec)
-      cand_kernel_vec<QRITA_DTYPE_F32><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count, u,
-                                                                  out_sample);
+  cudaError_t e = cudaSuccess;
+  if (vec) {
+    // rows of at least 8192 units per CTA split over a cluster (a dense row
+    // is the longest work of the launch), up to 4 CTAs
+    const int64_t nu = V / kUnit;
+    unsigned C = 1;
+    while (C < 4 && nu / (2 * C) >= 512) C *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g * C, 1, 1);
+    cfg.blockDim = dim3(kOutThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dtype == QRITA_DTYPE_F32)
+      e = cudaLaunchKernelEx(&cfg, cand_kernel_vec<QRITA_DTYPE_F32>, logits, V, mask, cap, out_ids, out_probs, out_count,
+                             u, out_sample);
     else
-      cand_kernel<QRITA_DTYPE_F32><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count, u,
-                                                              out_sample);
+      e = cudaLaunchKernelEx(&cfg, cand_kernel_vec<QRITA_DTYPE_BF16>, logits, V, mask, cap, out_ids, out_probs,
+                             out_count, u, out_sample);
+  } else if (dtype == QRITA_DTYPE_F32) {
+    cand_kernel<QRITA_DTYPE_F32><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count, u,
+                                                            out_sample);
   } else {
-    if (vec)
-      cand_kernel_vec<QRITA_DTYPE_BF16><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count,
-                                                                   u, out_sample);
-    else
-      cand_kernel<QRITA_DTYPE_BF16><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count, u,
-                                                               out_sample);
+    cand_kernel<QRITA_DTYPE_BF16><<<g, kOutThreads, 0, st>>>(logits, V, mask, cap, out_ids, out_probs, out_count, u,
+                                                             out_sample);
   }
-  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return static_cast<int>(e);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
   if (u != nullptr && out_sample != nullptr) {
-    last_kept_kernel<<<static_cast<unsigned>(B), kOutThreads, 0, st>>>(V, mask, out_sample);
+    last_kept_kernel<<<g, kOutThreads, 0, st>>>(V, mask, out_sample);
     e = cudaGetLastError();
   }
   return static_cast<int>(e);
