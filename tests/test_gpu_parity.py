@@ -346,6 +346,11 @@ def test_key_window_places_bf16_top_p_rows(dev, cl):
     kw = (info["path"] & q.PATH_KEYHIST) != 0
     assert kw[p_only].all()
     assert (info["passes"][p_only] == 1).all()
+    # |Z_t|, read off the window's bins and the rare logits, is the count of
+    # logits >= t
+    for r in np.nonzero(p_only)[0]:
+        x = widen(logits[r], w.dtype)
+        assert info["survivors"][r] == int(np.count_nonzero(x >= np.float32(info["threshold"][r]))), r
 
 
 @pytest.mark.parametrize("case", ["above_window", "huge_tie_group", "negative_logits"])
@@ -487,7 +492,7 @@ def test_deterministic_across_calls(dev):
 def test_row_info_matches_cpu_restatements(dev):
     import top_selection_row_gb300 as q
 
-    for n in (2, 3, 4):
+    for n in (2, 3, 4, 5):
         w = WORKLOADS[n]
         logits, k, p = workload(n, 16)
         got, st, info = run_gpu(logits, w.dtype, k, p, dev)

@@ -3548,19 +3548,31 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     // key-window rows: counts of the window's keys; every other logit weighed
     // (shift m_ref) into the sum outside the window, and apart above it
     F2 kw_out = {0.f, 0.f}, kw_top = {0.f, 0.f}, kw_gap = {0.f, 0.f};
-    uint32_t kw_ca = 0, kw_cb = 0, kw_ge_t = 0;
+    // (kw_ge_t: this thread's survivors x >= t among the rare logits; the
+    // window's are read off its bins after the pass)
+    uint32_t kw_ca = 0, kw_cb = 0, kw_ge_t = 0, kw_kt = 0;
     if constexpr (DT == QRITA_DTYPE_BF16) {
       if (kw) {
         uint32_t* kwh = reinterpret_cast<uint32_t*>(c.lists);
         const uint32_t top_off = kwin.bot_span + kwin.blob_len;
         const uint32_t top_end = top_off + kwin.top_span;
         float po = 0.f, pa = 0.f, pg = 0.f;  // partials of the current piece
+        // order keys of both halves of a packed word: x ^ 0xFFFF for negative
+        // halves, x ^ 0x8000 for the others (-0 keeps its own key; zeros lie
+        // in the gap)
+        auto keys2 = [](uint32_t w) -> uint32_t {
+          const uint32_t sgn = (w >> 15) & 0x00010001u;
+          return w ^ ((sgn * 0x7FFFu) | 0x80008000u);
+        };
+        // x >= t exactly when key(x) >= the key of the smallest bf16 >= t
+        kw_kt = keys2(t2 & 0xFFFFu) & 0xFFFFu;
         // logits outside the bins (below the window, in the gap, above it:
         // rare) are weighed one by one; k: the 16-bit order key of raw h
         auto kw_rare = [&](uint32_t k, uint32_t h) {
           const uint32_t d = k - kwin.lo0;  // wraps for keys below the window
           const float w = exp_shifted(__uint_as_float(h << 16), m_ref);
           po += w;
+          kw_ge_t += k >= kw_kt ? 1u : 0u;
           if (k >= kwin.lo0) {
             if (d >= top_end) {
               pa += w;
@@ -3571,20 +3583,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
             }
           }
         };
-        // order keys of both halves of a packed word: x ^ 0xFFFF for negative
-        // halves, x ^ 0x8000 for the others (-0 keeps its own key; zeros lie
-        // in the gap)
-        auto keys2 = [](uint32_t w) -> uint32_t {
-          const uint32_t sgn = (w >> 15) & 0x00010001u;
-          return w ^ ((sgn * 0x7FFFu) | 0x80008000u);
-        };
         // one key: counted in its bin (predicated, no branch), or marked rare
         const uint32_t kwh_s = smem_u32(kwh);
         auto kw_key = [&](uint32_t k) -> bool {
           const uint32_t d = k - kwin.lo0;
-          const bool in_bot = d < kwin.bot_span;
-          const bool in = in_bot || d - top_off < kwin.top_span;
-          red_inc_shared_at_if(kwh_s + 4u * (in_bot ? d : (in ? d - kwin.blob_len : 0u)), in);
+          const uint32_t dt = d - top_off;
+          const bool ib = d < kwin.bot_span, it = dt < kwin.top_span;
+          const bool in = ib | it;
+          red_inc_shared_at_if(kwh_s + 4u * (ib ? d : dt + kwin.bot_span), in);
           return in;
         };
         auto kw_unit = [&](const uint4 u) {
@@ -3614,7 +3620,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   const uint4 u = v[j];
                   vmax2 = bf2_max_nan(vmax2, bf2_max_nan(bf2_max_nan(u.x, u.y), bf2_max_nan(u.z, u.w)));
                   vmin2 = bf2_min(vmin2, bf2_min(bf2_min(u.x, u.y), bf2_min(u.z, u.w)));
-                  kw_ge_t += __popc(bf16_unit_bits(u, t2));
                   kw_unit(u);
                 }
               }
@@ -3627,7 +3632,6 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               if (valid) {
                 vmax = fmax_nan(vmax, x);
                 vmin = fminf(vmin, x);
-                kw_ge_t += x >= t ? 1u : 0u;
                 const uint32_t h = __float_as_uint(x) >> 16;
                 const uint32_t k = keys2(h) & 0xFFFFu;
                 if (!kw_key(k)) kw_rare(k, h);
@@ -3678,7 +3682,14 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     uint32_t kw_ca_cta = 0, kw_cb_cta = 0;
     if (kw) {
       // survivors (x >= t) are counted, none is in the own list (the merge
-      // sees an overflow); the count above the window goes to the merge
+      // sees an overflow); the count above the window goes to the merge.
+      // The window's survivors: its bins at or above t's key (a bin is one
+      // key; the bins are complete: a block barrier has passed)
+      {
+        const uint32_t* kwh = reinterpret_cast<const uint32_t*>(c.lists);
+        for (uint32_t b = tid; b < kw_nb; b += kThreads)
+          if (window_key(kwin, b) >= kw_kt) kw_ge_t += kwh[b];
+      }
       const uint32_t wg = __reduce_add_sync(kFull, kw_ge_t), wa = __reduce_add_sync(kFull, kw_ca);
       const uint32_t wb = __reduce_add_sync(kFull, kw_cb);
 #pragma unroll
