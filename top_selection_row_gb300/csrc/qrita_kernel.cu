@@ -1622,13 +1622,12 @@ __device__ void own_columns_streamed(Ctx<DT>& c, uint32_t cn) {
 // (no stream is in flight) and copied back to the warp's segment. Left in
 // columns when a warp holds more than the staging gives it.
 template <int DT>
-__device__ void own_columns_to_segments(Ctx<DT>& c, uint32_t cn) {
+__device__ void own_columns_to_segments(Ctx<DT>& c) {
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr uint32_t kStage = kRingBytes / 8 / kWarps;  // entries per warp
-  const uint32_t colcap = c.ocap / kThreads;
   const uint32_t segcap = c.ocap / kWarps;
-  const uint32_t n = min(cn, colcap);
+  const uint32_t n = vld(F.col_n[tid]);  // (at most the column capacity)
   uint32_t incl = n;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -3657,7 +3656,10 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     c.zero_fill_done = zfill;
     if (col) {
       own_columns_streamed<DT>(c, cn);
-      own_columns_to_segments<DT>(c, cn);
+      // bf16 rows place their boundaries with the key histogram, which reads
+      // the columns as they are; the others (or a histogram that gives way)
+      // convert them for the search
+      if (!(DT == QRITA_DTYPE_BF16 && (P.flags & QRITA_FLAG_NO_KEY_HIST) == 0u)) own_columns_to_segments<DT>(c);
     } else {
       own_segments_streamed<DT>(c, trunc ? wn : 0u);
     }
@@ -3926,6 +3928,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       const uint32_t kh_top = DT == QRITA_DTYPE_BF16 ? key16_of(row_max) : 0u;
       const bool kh = DT == QRITA_DTYPE_BF16 && hit && (P.flags & QRITA_FLAG_NO_KEY_HIST) == 0u &&
                       kh_top >= kh_base && kh_top - kh_base < static_cast<uint32_t>(kKeyHistBins);
+      // columns left for the key histogram become segments for a search
+      if (!kh && vld(F.col_mode) != 0u) own_columns_to_segments<DT>(c);
       if (kh) {
         const KeyHist h = keyhist_select<DT>(c, target, p_on, pr, kh_base, kh_top - kh_base + 1u);
         path |= QRITA_PATH_KEYHIST;
