@@ -242,14 +242,17 @@ __global__ void __launch_bounds__(kOutThreads) cand_kernel(const void* logits, i
 // ---------------------------------------------------------------------------
 constexpr int kUnit = 16;  // elements per unit
 
-// Kept bits of one unit of 16 mask bytes: bit e for byte e nonzero.
+// Kept bits of one unit of 16 mask bytes: bit e for byte e nonzero. A byte
+// is nonzero exactly when its low seven bits plus 0x7F carry into bit 7 or
+// its own bit 7 is set; the four bit-7 flags of a word are then gathered by
+// one multiply (bytes 0..3 to bits 0..3).
 __device__ __forceinline__ uint32_t unit_kept_bits(const uint4 m) {
+  if ((m.x | m.y | m.z | m.w) == 0u) return 0u;  // (most units of a sparse mask)
   const uint32_t w[4] = {m.x, m.y, m.z, m.w};
   uint32_t bits = 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    // one bit per nonzero byte (bytes 0..3 to bits 0..3)
-    const uint32_t nz = __vcmpne4(w[i], 0u) & 0x01010101u;
+    const uint32_t nz = ((((w[i] & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w[i]) >> 7) & 0x01010101u;
     bits |= ((nz * 0x01020408u) >> 24) << (4 * i);
   }
   return bits;
@@ -335,6 +338,9 @@ __device__ __forceinline__ T warps_excl(T v, T* slots, T* total) {
   return base;
 }
 
+// Steps of pass 2 whose masses a warp of the candidate kernel records.
+constexpr int kCandSteps = 32;
+
 // Units a lane takes per step, and the 16-byte words of one unit's logits:
 // every load of a step (its masks, then the logits of its units that keep
 // anything, predicated) is issued before any result is used.
@@ -393,8 +399,9 @@ __device__ __forceinline__ void widen_unit(const uint4 (&raw)[StepShape<DT>::kWo
 template <int DT>
 __global__ void __launch_bounds__(kOutThreads) ids_kernel_vec(const void* logits, int64_t V, const int32_t* k,
                                                               int32_t kmax, const uint8_t* mask, int32_t* out_ids) {
+  constexpr int NU = StepShape<DT>::kUnits, NW = StepShape<DT>::kWords;
   extern __shared__ __align__(16) unsigned long long keys[];  // [pow2 >= kmax]
-  __shared__ uint32_t warp_slots[kOutWarps];
+  __shared__ uint32_t fill;
   const int64_t r = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
   const int32_t kr = k[r];
@@ -405,56 +412,45 @@ __global__ void __launch_bounds__(kOutThreads) ids_kernel_vec(const void* logits
   const void* lrow = static_cast<const unsigned char*>(logits) + r * V * (DT == QRITA_DTYPE_F32 ? 4 : 2);
   int64_t u_lo, u_hi;
   warp_units(nu, u_lo, u_hi);
-  // pass 1: this warp's kept count (four units a lane in flight)
-  uint32_t cnt = 0;
+  if (tid == 0) fill = 0u;
+  __syncthreads();
+  // one pass: every kept id with its order key, in any order (the sort
+  // orders them), a lane claiming its slots with one shared atomic; the mask
+  // is the row's top-k mask, so it keeps min(k, V) <= kmax ids
   if (ok) {
-    for (int64_t ub = u_lo + lane; ub < u_hi; ub += 128) {
-      uint4 mv[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) mv[j] = ub + 32 * j < u_hi ? __ldg(mrow + ub + 32 * j) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) cnt += __popc(unit_kept_bits(mv[j]));
-    }
-  }
-  cnt = __reduce_add_sync(kFullMask, cnt);
-  uint32_t total = 0;
-  const uint32_t wbase = warps_excl<uint32_t>(cnt, warp_slots, &total);
-  const uint32_t n = ok ? min(total, static_cast<uint32_t>(kmax)) : 0u;
-  uint32_t np2 = 1;
-  while (np2 < n) np2 <<= 1;
-  // pass 2: the first n kept ids with their order keys, in id order (units
-  // ub + NU lane + j, every load of a step in flight together)
-  if (ok && wbase < n) {
-    constexpr int NU = StepShape<DT>::kUnits, NW = StepShape<DT>::kWords;
-    uint32_t run = wbase;
-    for (int64_t ub = u_lo; ub < u_hi && run < n; ub += 32 * NU) {
+    for (int64_t ub = u_lo; ub < u_hi; ub += 32 * NU) {
       uint32_t bits[NU];
       uint4 raw[NU][NW];
-      load_step<DT>(mrow, lrow, ub + NU * lane, 1, u_hi, bits, raw);
+      load_step<DT>(mrow, lrow, ub + lane, 32, u_hi, bits, raw);
       uint32_t c = 0;
 #pragma unroll
       for (int j = 0; j < NU; ++j) c += __popc(bits[j]);
-      uint32_t step = 0;
-      uint32_t pos = run + warp_excl_u32(c, &step);
+      if (c == 0u) continue;
+      uint32_t slot = atomicAdd(&fill, c);
 #pragma unroll
       for (int j = 0; j < NU; ++j) {
         if (bits[j] != 0u) {
-          const int64_t uu = ub + NU * lane + j;
+          const int64_t uu = ub + lane + 32 * j;
           float x[kUnit];
           widen_unit<DT>(raw[j], x);
 #pragma unroll
           for (int e = 0; e < kUnit; ++e) {
-            if (((bits[j] >> e) & 1u) && pos < n) {
-              const uint32_t key = f2key(x[e]);
-              keys[pos] = (static_cast<unsigned long long>(~key) << 32) | static_cast<uint32_t>(uu * kUnit + e);
+            if ((bits[j] >> e) & 1u) {
+              if (slot < static_cast<uint32_t>(kmax)) {
+                const uint32_t key = f2key(x[e]);
+                keys[slot] = (static_cast<unsigned long long>(~key) << 32) | static_cast<uint32_t>(uu * kUnit + e);
+              }
+              ++slot;
             }
-            pos += (bits[j] >> e) & 1u;
           }
         }
       }
-      run += step;
     }
   }
+  __syncthreads();
+  const uint32_t n = ok ? min(*reinterpret_cast<volatile uint32_t*>(&fill), static_cast<uint32_t>(kmax)) : 0u;
+  uint32_t np2 = 1;
+  while (np2 < n) np2 <<= 1;
   for (uint32_t i = n + tid; i < np2; i += kOutThreads) keys[i] = ~0ull;  // padding sorts last
   __syncthreads();
   // bitonic sort, ascending
@@ -500,6 +496,9 @@ __global__ void __launch_bounds__(kOutThreads, 3) cand_kernel_vec(const void* lo
   __shared__ unsigned long long warp_slots64[kOutWarps];
   __shared__ float warp_max[kOutWarps];
   __shared__ CandPub pub;
+  // each warp's mass per step of pass 2 (its first kCandSteps steps), so the
+  // draw recomputes one step instead of walking the warp's whole run
+  __shared__ unsigned long long step_mass[kOutWarps][kCandSteps];
   uint32_t C;
   asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(C));
   const uint32_t cr = cluster_rank();
@@ -522,6 +521,7 @@ __global__ void __launch_bounds__(kOutThreads, 3) cand_kernel_vec(const void* lo
     load_step<DT>(mrow, lrow, ub + lane, 32, u_hi, bits, raw);
 #pragma unroll
     for (int j = 0; j < NU; ++j) {
+      if (bits[j] == 0u) continue;
       cnt += __popc(bits[j]);
       float x[kUnit];
       widen_unit<DT>(raw[j], x);
@@ -561,11 +561,13 @@ __global__ void __launch_bounds__(kOutThreads, 3) cand_kernel_vec(const void* lo
     return round_u64(w * scale);
   };
   // pass 2: ids and weights in id order (units ub + NU lane + j), this
-  // warp's mass
+  // warp's mass, and its mass per step
   unsigned long long wmass = 0ull;
   {
     uint32_t run = cbase + wbase;
-    for (int64_t ub = u_lo; ub < u_hi; ub += 32 * NU) {
+    int step = 0;
+    for (int64_t ub = u_lo; ub < u_hi; ub += 32 * NU, ++step) {
+      const unsigned long long before = wmass;
       uint32_t bits[NU];
       uint4 raw[NU][NW];
       load_step<DT>(mrow, lrow, ub + NU * lane, 1, u_hi, bits, raw);
@@ -595,8 +597,15 @@ __global__ void __launch_bounds__(kOutThreads, 3) cand_kernel_vec(const void* lo
         }
       }
       run += step_n;
+      if (step < kCandSteps) {
+        unsigned long long sm = wmass - before;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(kFullMask, sm, o);
+        if (lane == 0) step_mass[warp][step] = sm;
+      }
     }
   }
+  const int64_t n_steps = (u_hi - u_lo + 32 * NU - 1) / (32 * NU);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wmass += __shfl_xor_sync(kFullMask, wmass, o);
   unsigned long long cta_mass = 0ull;
@@ -617,10 +626,20 @@ __global__ void __launch_bounds__(kOutThreads, 3) cand_kernel_vec(const void* lo
     const float uf = u[r];
     const F2 t = f2_mul(f2_from_u64(z), uf);
     const unsigned long long target = uf > 0.f ? f2_to_u64(t) : 0ull;
-    // the warp whose mass range holds the target walks its run again
+    // the warp whose mass range holds the target finds the step that holds
+    // it from its step masses and recomputes that step alone (a run of more
+    // than kCandSteps steps walks on from the last recorded one)
     if (mbase <= target && target < mbase + wmass) {
       unsigned long long acc = mbase;
-      for (int64_t ub = u_lo; ub < u_hi; ub += 32 * NU) {
+      int64_t ub0 = u_lo;
+      const int rec = n_steps < kCandSteps ? static_cast<int>(n_steps) : kCandSteps;
+      for (int q = 0; q < rec; ++q) {
+        const unsigned long long sm = *reinterpret_cast<volatile unsigned long long*>(&step_mass[warp][q]);
+        if (target < acc + sm || q == rec - 1) break;  // (warp-uniform)
+        acc += sm;
+        ub0 += 32 * NU;
+      }
+      for (int64_t ub = ub0; ub < u_hi; ub += 32 * NU) {
         uint32_t bits[NU];
         uint4 raw[NU][NW];
         load_step<DT>(mrow, lrow, ub + NU * lane, 1, u_hi, bits, raw);
