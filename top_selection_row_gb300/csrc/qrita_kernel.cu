@@ -20,8 +20,8 @@
 //   --  one cluster merge through distributed shared memory;
 //   A5  hit: the survivors stay in the CTAs' own lists; else a second
 //       truncation at an order statistic of a larger sample (top-k), one
-//       pass that extracts the bins around the boundary (binned top-p rows),
-//       or distributed narrowing passes over the chunk (one 256-bin pass,
+//       pass over the one-byte bin codes that lists the boundary's bin
+//       (binned top-p rows), or distributed narrowing passes over the chunk (one 256-bin pass,
 //       then two quaternary levels per cluster merge) until the range that
 //       holds the boundary fits the own lists, from which it is extracted;
 //   A6  the pivot search over the own lists of the cluster (64 bins a round,
@@ -282,10 +282,10 @@ enum : int {
   // fixed-point masses
   BX_TARGET = 0, BX_MLO, BX_MHI,
   // float pairs
-  BP_ZR = 0, BP_MR, BP_MLO, BP_MHI, BP_TOTAL, BP_GAP,
+  BP_ZR = 0, BP_MR, BP_MLO, BP_MHI, BP_TOTAL, BP_GAP, BP_PHA,
 };
 static_assert(BU_S2S < static_cast<int>(sizeof(Bcast::u) / sizeof(uint32_t)), "every uint slot fits the broadcast block");
-static_assert(BP_GAP < static_cast<int>(sizeof(Bcast::pr) / sizeof(float) / 2), "every pair slot fits the broadcast block");
+static_assert(BP_PHA < static_cast<int>(sizeof(Bcast::pr) / sizeof(float) / 2), "every pair slot fits the broadcast block");
 
 __device__ __forceinline__ void put_pair(Bcast& b, int i, F2 v) {
   b.pr[2 * i] = v.hi;
@@ -1319,41 +1319,29 @@ __device__ void extract_range(Ctx<DT>& c, const Range& R) {
 // ---------------------------------------------------------------------------
 // Top-p rows binned by the streaming pass (top-p alone, far more survivors
 // than the lists hold): the streaming pass also counts and weighs the
-// survivors in kHistBins value bins of [t, m_ref] (bin(x) = trunc((x - t) nb /
-// (m_ref - t)), a monotone function of x, so bins are value intervals; the
-// survivors above m_ref are totalled apart). The weights there are fp32
-// exp(x - m_ref) in 32-bit fixed point: approximate, they only choose the
-// bins around the boundary. One more pass (split_pass) then keeps every
-// element above the chosen bins, extracts the bins' elements to the own
-// list and weighs both exactly in the search's fixed point; the search runs
-// on the list when the exact masses confirm the bracket.
-// List-region layout while the streaming pass runs: per-warp counts at 0,
-// per-warp masses at kWarps * kHistBins * 4; the CTA's totals at kPhTotOff
-// (counts, 64-bit masses, then the count and fp32 mass above m_ref).
+// survivors in kPhBins value bins of [t, ph_hi] (bin(x) = trunc((x - t) nb /
+// (ph_hi - t)), a monotone function of x, so bins are value intervals; the
+// survivors above ph_hi are totalled apart, in compensated fp32). A bin's
+// weights are fp32 exp(x - m_ref) (at most 1 there) in fixed point, summed as
+// two 32-bit halves per warp: exact integer sums, the same in any order. The
+// pass also writes a code byte per logit in place of its mask byte: 0 below
+// t, 1 + bin in the bins, kPhCodeAbove above ph_hi. After the merge the bin
+// that holds the boundary is exact; one pass over the chunk's code bytes
+// (code_pass: 1 byte a logit, from L2) then writes the final mask byte of
+// every logit outside that bin and extracts the bin's logits to the own
+// list, weighed exactly in the search's fixed point; the search runs on the
+// list when the masses confirm the bracket.
+// List-region layout while the streaming pass runs: the high halves of the
+// per-warp masses at 0, the low halves after them (kWarps * kHistBins words
+// each); the CTA's totals at kPhTotOff (64-bit masses, then the count above
+// ph_hi and its compensated fp32 mass).
 // ---------------------------------------------------------------------------
 constexpr int kHistBins = 256;
 static_assert(kHistBins == kThreads, "one thread per histogram bin");
+constexpr int kPhBins = kHistBins - 2;      // bins of the first pass: codes 1 .. kPhBins
+constexpr uint32_t kPhCodeAbove = 255u;     // code of a survivor above ph_hi (0: below t)
 constexpr int kPhTotOff = 2 * kWarps * kHistBins * 4;
-constexpr int kPhAboveOff = kPhTotOff + kHistBins * 4 + kHistBins * 8;
-
-// Block-wide inclusive suffix sum of one float per thread (thread b, bin b).
-template <int DT>
-__device__ __forceinline__ float bin_suffix_sum_f(Ctx<DT>& c, float v) {
-  Fixed& F = *c.F;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_down_sync(kFull, incl, o);
-    if (lane + o < 32) incl += y;
-  }
-  if (lane == 0) F.redf[warp][2] = incl;
-  __syncthreads();
-  float above = 0.f;
-  for (int w = warp + 1; w < kWarps; ++w) above += vld(F.redf[w][2]);
-  __syncthreads();
-  return incl + above;
-}
+constexpr int kPhAboveOff = kPhTotOff + kHistBins * 8;
 
 // Largest key k in [a, b] with bin(k) <= g, given bin(a) <= g; bin is
 // monotone in the key. A 32-way search by each warp (every lane returns it).
@@ -1378,123 +1366,116 @@ __device__ __forceinline__ uint32_t last_key_in_bins(uint32_t a, uint32_t b, int
 template <int DT>
 __device__ void own_segments_streamed(Ctx<DT>& c, uint32_t wn);
 
-// The pass after the first-pass histogram: elements above hi (keys) are kept
-// (mask 1), those in (lo, hi] go to this warp's segment of the own list (mask
-// 0 until the search decides), the rest are dropped; the kept and the listed
-// are weighed exactly. Returns this CTA's count and mass above hi and the
-// list's mass (every thread); the own list's segments are published.
+// The pass after the first-pass bins: one pass over the chunk's code bytes
+// (the streaming pass wrote them in place of the mask bytes). A code above
+// [c_lo, c_hi] becomes 1, one below it 0; a logit whose code lies in the
+// range is reloaded from the row into this warp's segment of the own list,
+// a lane claiming its slot with one shared atomic, and its byte becomes 0
+// until the search decides. Publishes the own list's segments and returns
+// this thread's count of logits above the range.
 template <int DT>
-__device__ void split_pass(Ctx<DT>& c, uint32_t lo, uint32_t hi, uint32_t& c_above,
-                           unsigned long long& m_above, unsigned long long& m_in) {
-  constexpr int E = Ctx<DT>::E;
+__device__ uint32_t code_pass(Ctx<DT>& c, uint32_t c_lo, uint32_t c_hi) {
+  constexpr int S = Ctx<DT>::S;
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float scale = c.fix_scale;
   const uint32_t segcap = c.ocap / kWarps;
   const uint32_t seg_base = static_cast<uint32_t>(warp) * segcap;
-  uint32_t wn = 0;
-  uint32_t ca = 0;
-  // the mass above hi is one constant offset of the search that follows, so
-  // it is summed in compensated fp32 (a unit's partial at a time); the list's
-  // mass must equal what the search sums over the list: exact fixed point,
-  // summed over the list once it is complete
-  F2 ma = {0.f, 0.f};
-  unsigned long long mi = 0ull;
-  const uintptr_t mbp = reinterpret_cast<uintptr_t>(c.gmask + c.head_n);
-  const bool vec_ok = (mbp % E) == 0;
-  // key(x) > q as a float comparison, x > pivot_f(q), for keys at or above
-  // -inf's; a bound below it holds every element
-  const bool lo_all = lo < kKeyNegInf, hi_all = hi < kKeyNegInf;
-  const float lo_f = lo_all ? -INFINITY : pivot_f(lo), hi_f = hi_all ? -INFINITY : pivot_f(hi);
-  stream_pieces<DT>(
-      c,
-      [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
-        float xs[kPieceThreadUnits][E];
-        uint32_t bits[kPieceThreadUnits];
+  if (lane == 0) F.seg_n[warp] = 0u;
+  __syncthreads();  // (also: every code byte of the chunk is written)
+  uint8_t* m = c.gmask;
+  const int n = c.n;
+  // the final byte of logit i with code `code` (a logit in the range gets
+  // its slot and index now, its value after the pass)
+  auto one = [&](uint32_t code, int i) -> uint32_t {
+    if (code >= c_lo && code <= c_hi) {
+      const uint32_t pos = atomicAdd(&F.seg_n[warp], 1u);
+      if (pos < segcap) c.own_idx[seg_base + pos] = static_cast<uint32_t>(i);
+      return 0u;
+    }
+    return code > c_hi ? 1u : 0u;
+  };
+  // the four final bytes of a word of codes at byte offset i0. A word
+  // without a code in the range (no byte equal to c_lo ... c_hi; this pass
+  // runs with c_lo == c_hi) takes four byte compares at once: b > c_hi
+  // exactly when b + (255 - c_hi) carries out of the byte, the carry being
+  // the majority of the two top bits and the carry into bit 7
+  const uint32_t cc4 = c_lo * 0x01010101u;
+  const uint32_t d4 = (255u - c_hi) * 0x01010101u;
+  const uint32_t d_low = d4 & 0x7F7F7F7Fu, d_top = d4 & 0x80808080u;
+  auto word = [&](uint32_t v, int i0) -> uint32_t {
+    const uint32_t t = v ^ cc4;
+    if (c_lo != c_hi || ((t - 0x01010101u) & ~t & 0x80808080u) != 0u) {
+      uint32_t out = 0u;
 #pragma unroll
-        for (int j = 0; j < kPieceThreadUnits; ++j) {
-          unpack<DT>(v[j], xs[j]);
-          bits[j] = 0u;
-          if (j * kThreads + tid < n) {
-            uint32_t keep = 0u;  // bit e: element e is above hi
-            float pa = 0.f;
+      for (int b = 0; b < 4; ++b) out |= one((v >> (8 * b)) & 0xFFu, i0 + b) << (8 * b);
+      return out;
+    }
+    const uint32_t low = (v & 0x7F7F7F7Fu) + d_low;
+    const uint32_t carry = (v & d_top) | ((v | d_top) & low);
+    return (carry >> 7) & 0x01010101u;
+  };
+  // bytes to the first 16-byte boundary, then 16-byte vectors (four of them
+  // a thread in flight: the loads do not wait on the stores before them),
+  // then the last bytes
+  const int head = min(static_cast<int>((16u - static_cast<uint32_t>(reinterpret_cast<uintptr_t>(m) & 15u)) & 15u), n);
+  const int nv = (n - head) / 16;
+  const int tail0 = head + 16 * nv;
+  uint32_t above = 0;
+  if (tid < head) {
+    const uint32_t b = one(m[tid], tid);
+    m[tid] = static_cast<uint8_t>(b);
+    above += b;
+  }
+  uint4* mv = reinterpret_cast<uint4*>(m + head);
+  constexpr int kV = 4;
+  for (int vb = 0; vb < nv; vb += kV * kThreads) {
+    uint4 v[kV];
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-              const float x = xs[j][e];
-              const bool above = hi_all || x > hi_f;
-              const bool in = !above && (lo_all || x > lo_f);
-              const float w = weight(x, c.m, c.m_neginf);
-              ca += above ? 1u : 0u;
-              pa += above ? w : 0.f;
-              keep |= above ? (1u << e) : 0u;
-              bits[j] |= in ? (1u << e) : 0u;
-            }
-            f2_add(ma, pa);
-            // one mask byte per element (bit e of keep -> byte e)
-            uint8_t* dst = c.gmask + c.head_n + static_cast<size_t>(u0 + j * kThreads + tid) * E;
-            const uint32_t w0 = (keep & 1u) | ((keep & 2u) << 7) | ((keep & 4u) << 14) | ((keep & 8u) << 21);
-            if (vec_ok) {
-              if constexpr (E == 4) {
-                *reinterpret_cast<uint32_t*>(dst) = w0;
-              } else {
-                const uint32_t k1 = keep >> 4;
-                const uint32_t w1 = (k1 & 1u) | ((k1 & 2u) << 7) | ((k1 & 4u) << 14) | ((k1 & 8u) << 21);
-                *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
-              }
-            } else {
+    for (int q = 0; q < kV; ++q) {
+      const int iv = vb + q * kThreads + tid;
+      v[q] = iv < nv ? mv[iv] : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-              for (int e = 0; e < E; ++e) dst[e] = static_cast<uint8_t>((keep >> e) & 1u);
-            }
-          }
-        }
-        append_piece<DT>(c, wn, seg_base, segcap, xs, bits, u0);
-      },
-      [&](float x, uint32_t idx, bool valid) {
-        uint32_t bits = 0;
-        if (valid) {
-          const uint32_t k = f2key(x);
-          const bool above = k > hi;
-          const bool in = !above && k > lo;
-          ca += above ? 1u : 0u;
-          if (above) f2_add(ma, weight(x, c.m, c.m_neginf));
-          bits = in ? 1u : 0u;
-          c.gmask[idx] = above ? 1 : 0;
-        }
-        const float xs[1] = {x};
-        seg_append<1>(wn, c.own_val, c.own_idx, seg_base, segcap, xs, idx, bits);
-      },
-      false);
+    for (int q = 0; q < kV; ++q) {
+      const int iv = vb + q * kThreads + tid;
+      if (iv < nv) {
+        const int i0 = head + 16 * iv;
+        const uint4 o = make_uint4(word(v[q].x, i0), word(v[q].y, i0 + 4), word(v[q].z, i0 + 8), word(v[q].w, i0 + 12));
+        mv[iv] = o;
+        above += __popc(o.x) + __popc(o.y) + __popc(o.z) + __popc(o.w);  // (bytes are 0 or 1)
+      }
+    }
+  }
+  if (tid < n - tail0) {
+    const uint32_t b = one(m[tail0 + tid], tail0 + tid);
+    m[tail0 + tid] = static_cast<uint8_t>(b);
+    above += b;
+  }
+  __syncthreads();
+  // the listed logits' values, loaded together (four a lane in flight)
+  const uint32_t wn = vld(F.seg_n[warp]);
+  const uint32_t ns = min(wn, segcap);
+  for (uint32_t k0 = 0; k0 < ns; k0 += 128u) {
+    uint32_t ix[4];
+    float x[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t k = k0 + static_cast<uint32_t>(q * 32 + lane);
+      ix[q] = k < ns ? c.own_idx[seg_base + k] : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) x[q] = load_elem<DT>(c.gx + static_cast<size_t>(ix[q]) * S);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t k = k0 + static_cast<uint32_t>(q * 32 + lane);
+      if (k < ns) c.own_val[seg_base + k] = x[q];
+    }
+  }
   own_segments_streamed<DT>(c, wn);
-  // the list's exact mass (entries past a full segment are lost: the caller
-  // then does not use it)
-  own_for(c, [&](float x, uint32_t) { mi += round_u64(weight(x, c.m, c.m_neginf) * scale); });
-  ca = __reduce_add_sync(kFull, ca);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    ma = f2_merge(ma, f2_make(__shfl_xor_sync(kFull, ma.hi, o), __shfl_xor_sync(kFull, ma.lo, o)));
-  mi = warp_sum_u64(mi);
-  if (lane == 0) {
-    F.lred[0][warp][0].cnt = ca;
-    F.redf[warp][6] = ma.hi;
-    F.redf[warp][7] = ma.lo;
-    F.lred[0][warp][1].mass = mi;
-  }
-  __syncthreads();
-  uint32_t tc = 0;
-  F2 tma = {0.f, 0.f};
-  unsigned long long tmi = 0ull;
-  for (int w = 0; w < kWarps; ++w) {
-    tc += vld(F.lred[0][w][0].cnt);
-    tma = f2_merge(tma, f2_make(vld(F.redf[w][6]), vld(F.redf[w][7])));
-    tmi += vld(F.lred[0][w][1].mass);
-  }
-  c_above = tc;
-  m_above = f2_to_u64(f2_mul(tma, scale));
-  m_in = tmi;
-  __syncthreads();
+  return above;
 }
 
-// Cluster merge after split_pass: F.rank_n[r] (list entries of rank r),
+// Cluster merge after the pass that lists a range: F.rank_n[r] (list entries of rank r),
 // F.bc.u[BU_S2] (row list entries), F.bc.u[BU_OVF2] (a list overflowed),
 // F.bc.u[BU_CHI] (row count above hi), F.bc.x[BX_MHI] / [BX_MLO] (row mass
 // above hi / of the lists).
@@ -3320,21 +3301,31 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     F.bp_bins[tid] = 0u;
   }
   // top-p alone with far more expected survivors than the lists hold: the
-  // streaming pass also bins the survivors in [t, m_ref] (see split_pass)
-  // (bins over [t, ph_hi]; ph_hi = min(m_ref, mu + 4 sigma), so an outlier in
-  // the sample does not widen them; weights there are at most 1)
-  float ph_inv_w = 0.f, ph_scale = 0.f, ph_hi = 0.f;
+  // streaming pass also bins the survivors in [t, ph_hi] (see code_pass)
+  // (ph_hi = min(m_ref, mu + 4 sigma), so an outlier in the sample does not
+  // widen them; weights there are at most 1)
+  float ph_inv_w = 0.f, ph_hi = 0.f, ph_sc = 0.f, ph_lsc = 0.f, ph_ilsc = 0.f;
+  int ph_sbits = 0, ph_lbits = 0;
   bool ph = false;
   if (p_only && trunc && sigma > 0.f && isfinite(m_ref) && (P.flags & QRITA_FLAG_FORCE_FALLBACK) == 0u) {
     const float expect = static_cast<float>(V) * normcdff((mu - t) / sigma);
     ph_hi = fminf(m_ref, fmaf(kClipSigmas, sigma, mu));
-    ph_inv_w = static_cast<float>(kHistBins) / (ph_hi - t);
+    ph_inv_w = static_cast<float>(kPhBins) / (ph_hi - t);
     ph = ph_hi > t && expect > 0.9f * static_cast<float>(c.ocap) * static_cast<float>(c.C) && isfinite(ph_inv_w) &&
          ph_inv_w > 0.f;
-    // 32-bit bin masses per warp: a warp bins at most chunk / kWarps + 32
-    // elements (the same scale in every CTA of the row)
+    // fixed-point bin masses per warp, in two 32-bit halves: a warp bins at
+    // most chunk / kWarps + 32 logits (2^pw at most), so a low half of
+    // 31 - pw bits and a high half of ph_sbits - (31 - pw) bits both sum
+    // without overflow when ph_sbits <= 63 - 2 pw (the same scale in every
+    // CTA of the row)
     const uint32_t per_warp = static_cast<uint32_t>(P.chunk) / kWarps + 32u;
-    ph_scale = exp2f(static_cast<float>(__clz(per_warp)));
+    const int pw = 32 - __clz(per_warp);
+    ph_lbits = 31 - pw;
+    ph_sbits = min(36, 63 - 2 * pw);
+    ph_sc = exp2f(static_cast<float>(ph_sbits));
+    ph_lsc = exp2f(static_cast<float>(ph_lbits));
+    ph_ilsc = exp2f(static_cast<float>(-ph_lbits));
+    ph = ph && ph_sbits >= 20;  // (chunks of millions of logits narrow instead)
   }
   // bf16 rows of that kind count a window of 16-bit keys instead (exact
   // bins: see kw_select); the window reaches kKwHeadroom keys above the
@@ -3407,22 +3398,29 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       }
       ++cn;
     };
-    uint32_t* ph_cnt = reinterpret_cast<uint32_t*>(c.lists) + warp * kHistBins;
-    uint32_t* ph_mass = ph_cnt + kWarps * kHistBins;
-    const uint32_t ph_cnt_s = smem_u32(ph_cnt), ph_mass_s = smem_u32(ph_mass);
+    const uint32_t ph_hi_s = smem_u32(reinterpret_cast<uint32_t*>(c.lists) + warp * kHistBins);
+    const uint32_t ph_lo_s = ph_hi_s + kWarps * kHistBins * 4;
     uint32_t ph_n = 0, ph_ac = 0;  // survivors; those above ph_hi
-    float ph_am = 0.f;             // and the latter's weight (shift m_ref)
-    auto ph_bin = [&](float x, float w) {
+    F2 ph_am = {0.f, 0.f};         // and the latter's weight (shift m_ref)
+    // a survivor's bin (its weight w <= 1 as round(w 2^sbits), in a high and
+    // a low half) and its code byte
+    auto ph_bin = [&](float x, float w) -> uint32_t {
       ++ph_n;
       if (x <= ph_hi) {
         int b = static_cast<int>((x - t) * ph_inv_w);
-        b = b > kHistBins - 1 ? kHistBins - 1 : b;
-        red_add_shared_at(ph_cnt_s + 4u * static_cast<uint32_t>(b), 1u);
-        red_add_shared_at(ph_mass_s + 4u * static_cast<uint32_t>(b), __float2uint_rn(w * ph_scale));
-      } else {
-        ++ph_ac;
-        ph_am += w;
+        b = b > kPhBins - 1 ? kPhBins - 1 : b;
+        const float v = w * ph_sc;                 // exact scaling
+        const float hf = truncf(v * ph_ilsc);       // v / 2^L, rounded down
+        const uint32_t hi = static_cast<uint32_t>(hf);
+        const uint32_t lo = __float2uint_rn(fmaf(-hf, ph_lsc, v));  // exact remainder, rounded
+        const uint32_t off = 4u * static_cast<uint32_t>(b);
+        red_add_shared_at(ph_hi_s + off, hi);
+        red_add_shared_at(ph_lo_s + off, lo);
+        return 1u + static_cast<uint32_t>(b);
       }
+      ++ph_ac;
+      f2_add(ph_am, w);
+      return kPhCodeAbove;
     };
     auto streaming_pass = [&](auto po, auto cm, auto hc, auto zf) {
       constexpr bool PO = decltype(po)::value;
@@ -3472,6 +3470,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               bits[j] = 0u;
               if (j * kThreads + tid < n) {
                 if constexpr (!PO && ZF) zero_unit(u0 + j * kThreads + tid);
+                uint32_t cw[E / 4] = {};  // code bytes (PH)
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
                   const float x = xs[j][e];
@@ -3484,8 +3483,21 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                     zu += w;
                     mu_ += surv ? w : 0.f;
                     if constexpr (PH) {
-                      if (surv) ph_bin(x, w);
+                      const uint32_t code = surv ? ph_bin(x, w) : 0u;
+                      cw[e >> 2] |= code << (8 * (e & 3));
                     }
+                  }
+                }
+                if constexpr (PH) {
+                  // the unit's code bytes in place of its mask bytes (read
+                  // back by code_pass, which writes the final bytes)
+                  uint8_t* dst = c.gmask + c.head_n + static_cast<size_t>(u0 + j * kThreads + tid) * E;
+                  if (zvec) {
+                    if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = cw[0];
+                    else *reinterpret_cast<uint2*>(dst) = make_uint2(cw[0], cw[E / 4 - 1]);
+                  } else {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) dst[e] = static_cast<uint8_t>(cw[e >> 2] >> (8 * (e & 3)));
                   }
                 }
               }
@@ -3530,9 +3542,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                 const float w = exp_shifted(x, m_ref);
                 f2_add(zs, w);
                 f2_add(ms, surv ? w : 0.f);
-                if constexpr (PH) {
-                  if (surv) ph_bin(x, w);
-                }
+                if constexpr (PH) c.gmask[idx] = static_cast<uint8_t>(surv ? ph_bin(x, w) : 0u);
               }
             }
             const float xs[1] = {x};
@@ -3726,38 +3736,40 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       // this CTA's bin totals and its survivors above m_ref, read by the
       // other CTAs of the row after the merge; the survivors are counted
       // (none is in the own list: the merge sees an overflow)
-      uint32_t* tc = reinterpret_cast<uint32_t*>(c.lists + kPhTotOff);
-      unsigned long long* tm = reinterpret_cast<unsigned long long*>(c.lists + kPhTotOff + kHistBins * 4);
+      unsigned long long* tm = reinterpret_cast<unsigned long long*>(c.lists + kPhTotOff);
       uint32_t* ta = reinterpret_cast<uint32_t*>(c.lists + kPhAboveOff);
       const uint32_t* h = reinterpret_cast<const uint32_t*>(c.lists);
-      uint32_t sc = 0;
-      unsigned long long sm = 0ull;
+      // bin tid: the fixed-point mass hi 2^L + lo summed over the warps (exact)
+      unsigned long long sh = 0ull, sl = 0ull;
       for (int w = 0; w < kWarps; ++w) {
-        sc += vld(h[w * kHistBins + tid]);
-        sm += vld(h[(kWarps + w) * kHistBins + tid]);
+        sh += vld(h[w * kHistBins + tid]);
+        sl += vld(h[(kWarps + w) * kHistBins + tid]);
       }
-      tc[tid] = sc;
-      tm[tid] = sm;
+      tm[tid] = (sh << ph_lbits) + sl;
       const uint32_t wnn = __reduce_add_sync(kFull, ph_n), wac = __reduce_add_sync(kFull, ph_ac);
-      const float wam = warp_sum_f(ph_am);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+        ph_am = f2_merge(ph_am, f2_make(__shfl_xor_sync(kFull, ph_am.hi, o), __shfl_xor_sync(kFull, ph_am.lo, o)));
       if (lane == 0) {
         F.redu[warp][0] = wnn;
         F.redu[warp][1] = wac;
-        F.redf[warp][7] = wam;
+        F.redf[warp][6] = ph_am.hi;
+        F.redf[warp][7] = ph_am.lo;
       }
       __syncthreads();
       if (tid == 0) {
         uint32_t a = 0, b = 0;
-        float m2 = 0.f;
+        F2 m2 = {0.f, 0.f};
         for (int w = 0; w < kWarps; ++w) {
           a += vld(F.redu[w][0]);
           b += vld(F.redu[w][1]);
-          m2 += vld(F.redf[w][7]);
+          m2 = f2_merge(m2, f2_make(vld(F.redf[w][6]), vld(F.redf[w][7])));
         }
         F.own_n = a;
         F.seg_ovf = 1u;
         ta[0] = b;
-        ta[1] = __float_as_uint(m2);
+        ta[1] = __float_as_uint(m2.hi);
+        ta[2] = __float_as_uint(m2.lo);
       }
       __syncthreads();
     }
@@ -4238,90 +4250,108 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                                 f2_ge(Mm, f2_mul(f2_mul(Zm, pr), 1.0f + 1e-5f));
           bool ph_done = false;
           if (ph && mass_hit) {
-            // the first pass's bins: row totals of bin tid (approximate mass,
-            // shift m_ref) and of the survivors above m_ref
-            const uint32_t* tc = reinterpret_cast<const uint32_t*>(c.lists + kPhTotOff);
-            const unsigned long long* tm =
-                reinterpret_cast<const unsigned long long*>(c.lists + kPhTotOff + kHistBins * 4);
+            // the first pass's bins, read from every CTA of the row: thread
+            // tid holds bin b = kPhBins - 1 - tid (from the top), its count
+            // and its exact mass moved to the search's fixed point (shift m:
+            // times cf 2^(S - sbits), cf = exp(m_ref - m))
+            const unsigned long long* tm = reinterpret_cast<const unsigned long long*>(c.lists + kPhTotOff);
             const uint32_t* ta = reinterpret_cast<const uint32_t*>(c.lists + kPhAboveOff);
-            float mf = 0.f;
-            for (uint32_t r = 0; r < c.C; ++r) {
-              const uint32_t ab = map_rank(smem_u32(&tm[tid]), r);
-              const unsigned long long v = static_cast<unsigned long long>(ld_dsmem_u32(ab)) |
-                                           (static_cast<unsigned long long>(ld_dsmem_u32(ab + 4u)) << 32);
-              mf += __ull2float_rn(v);
+            const int b_t = kPhBins - 1 - tid;
+            unsigned long long rb = 0ull;
+            if (b_t >= 0) {
+              for (uint32_t r = 0; r < c.C; ++r) {
+                const uint32_t ab = map_rank(smem_u32(&tm[b_t]), r);
+                rb += static_cast<unsigned long long>(ld_dsmem_u32(ab)) |
+                      (static_cast<unsigned long long>(ld_dsmem_u32(ab + 4u)) << 32);
+              }
             }
-            mf *= 1.0f / ph_scale;
+            const float conv = cf * (scale / ph_sc);  // (a power of two times cf)
+            const unsigned long long rm = rb != 0ull ? f2_to_u64(f2_mul(f2_from_u64(rb), conv)) : 0ull;
             if (warp == 0) {
-              uint32_t ac = 0;
-              float am = 0.f;
+              // the survivors above ph_hi: compensated mass (shift m_ref)
+              F2 am = {0.f, 0.f};
               if (lane < static_cast<int>(c.C)) {
-                ac = ld_dsmem_u32(map_rank(smem_u32(&ta[0]), static_cast<uint32_t>(lane)));
-                am = __uint_as_float(ld_dsmem_u32(map_rank(smem_u32(&ta[1]), static_cast<uint32_t>(lane))));
+                am = f2_make(__uint_as_float(ld_dsmem_u32(map_rank(smem_u32(&ta[1]), static_cast<uint32_t>(lane)))),
+                             __uint_as_float(ld_dsmem_u32(map_rank(smem_u32(&ta[2]), static_cast<uint32_t>(lane)))));
               }
-              ac = __reduce_add_sync(kFull, ac);
-              am = warp_sum_f(am);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1)
+                am = f2_merge(am, f2_make(__shfl_xor_sync(kFull, am.hi, o), __shfl_xor_sync(kFull, am.lo, o)));
               if (lane == 0) {
-                F.bc.u[BU_PHAC] = ac;
-                F.bc.f[BF_PHAM] = am;
+                put_pair(F.bc, BP_PHA, am);
+                F.bc.u[BU_NP] = 0xFFFFFFFFu;  // the bin that holds the boundary: none yet
               }
             }
-            const float sfx = bin_suffix_sum_f<DT>(c, mf);  // block barriers inside
-            const float am_row = vld(F.bc.f[BF_PHAM]);
-            const float cum = sfx + am_row;  // mass of bins tid.. and above m_ref
-            const float T = f2_float(f2_mul(Zr, pr));
-            // the largest bin whose mass from the top reaches p Z (approximately),
-            // with one bin of margin on either side
-            const int nb = __syncthreads_count(cum >= T);
-            const int bstar = am_row >= T ? kHistBins : nb - 1;
-            // rank tid's elements in bins [b0, b1] (bin kHistBins: above ph_hi)
-            auto rank_count = [&](int b0, int b1) -> uint32_t {
-              uint32_t cr = 0;
-              const int top = b1 < kHistBins - 1 ? b1 : kHistBins - 1;
-              for (int b = b0; b <= top; ++b) cr += ld_dsmem_u32(map_rank(smem_u32(&tc[b]), static_cast<uint32_t>(tid)));
-              if (b1 >= kHistBins) cr += ld_dsmem_u32(map_rank(smem_u32(&ta[0]), static_cast<uint32_t>(tid)));
-              return cr;
-            };
-            int bl = bstar - 1 < 0 ? 0 : bstar - 1;
-            int bh = bstar + 1;  // >= kHistBins: the range reaches above ph_hi
-            bool fits = __syncthreads_and(tid >= static_cast<int>(c.C) || rank_count(bl, bh) <= c.ocap) != 0;
-            if (!fits && bstar >= 0 && bstar < kHistBins) {
-              // without the margin bins
-              bl = bstar;
-              bh = bstar;
-              fits = __syncthreads_and(tid >= static_cast<int>(c.C) || rank_count(bl, bh) <= c.ocap) != 0;
+            unsigned long long m_bins = 0ull;
+            // mass of the bins above thread tid's (barriers inside)
+            const unsigned long long m_above_b = block_excl_scan_u64(F, rm, &m_bins);
+            const unsigned long long a_row = f2_to_u64(f2_mul(f2_mul(get_pair(F.bc, BP_PHA), cf), scale));
+            const unsigned long long target = f2_to_u64(f2_mul(f2_mul(Zm, pr), scale));
+            // the boundary: among the survivors above ph_hi (code
+            // kPhCodeAbove), or in the one bin where the mass from the top
+            // reaches the target
+            if (tid == 0 && target <= a_row) {
+              F.bc.u[BU_NP] = kPhCodeAbove;
+              F.bc.x[BX_MHI] = 0ull;
             }
+            if (b_t >= 0 && target > a_row) {
+              const unsigned long long above = a_row + m_above_b;
+              if (above < target && target <= above + rm) {
+                F.bc.u[BU_NP] = 1u + static_cast<uint32_t>(b_t);
+                F.bc.x[BX_MHI] = above;
+              }
+            }
+            __syncthreads();
+            const uint32_t code = vld(F.bc.u[BU_NP]);
+            const bool found = code != 0xFFFFFFFFu;
+            const unsigned long long m_above = vld(F.bc.x[BX_MHI]);
             cluster_sync_all();  // every CTA has read the others' totals
-            if (nb > 0 && fits) {
-              // the bins' key range: bin(x) as the streaming pass computed it
+            if (found) {
+              // the code's key range: bin(x) as the streaming pass computed it
               auto bfun = [&](uint32_t k) -> int {
                 const float x = key2f(k);
                 if (!(x >= t)) return -1;
-                if (x > ph_hi) return kHistBins;
+                if (x > ph_hi) return kPhBins;
                 const int b = static_cast<int>((x - t) * ph_inv_w);
-                return b > kHistBins - 1 ? kHistBins - 1 : b;
+                return b > kPhBins - 1 ? kPhBins - 1 : b;
               };
               const uint32_t kt = f2key(t), km = f2key(ph_hi);
-              const uint32_t lo_key = bl == 0 ? kt - 1u : last_key_in_bins(kt, km, bl - 1, bfun);
-              const bool to_top = bh >= kHistBins;
-              const uint32_t hi_key = to_top ? kKeyPosInf : last_key_in_bins(kt, km, bh, bfun);
-              uint32_t ca = 0;
-              unsigned long long ma = 0ull, mi = 0ull;
-              split_pass<DT>(c, lo_key, hi_key, ca, ma, mi);
+              const bool to_top = code == kPhCodeAbove;
+              const int bb = static_cast<int>(code) - 1;
+              const uint32_t lo_key = to_top ? km : (bb == 0 ? kt - 1u : last_key_in_bins(kt, km, bb - 1, bfun));
+              const uint32_t hi_key = to_top ? f2key(row_max) : last_key_in_bins(kt, km, bb, bfun);
+              const uint32_t ca = code_pass<DT>(c, code, code);
               passes += 1u;
-              merge_split<DT>(c, vld(F.own_n), vld(F.seg_ovf), ca, ma, mi);
+              // the list's exact mass (entries past a full segment are lost:
+              // the list then overflowed and is not used)
+              unsigned long long mi = 0ull;
+              own_for(c, [&](float x, uint32_t) { mi += weight_fx(x, c.m, c.m_neginf, scale); });
+              mi = warp_sum_u64(mi);
+              const uint32_t wca = __reduce_add_sync(kFull, ca);
+              if (lane == 0) {
+                F.lred[0][warp][1].mass = mi;
+                F.lred[0][warp][0].cnt = wca;
+              }
+              __syncthreads();
+              unsigned long long tmi = 0ull;
+              uint32_t tca = 0;
+              for (int w = 0; w < kWarps; ++w) {
+                tmi += vld(F.lred[0][w][1].mass);
+                tca += vld(F.lred[0][w][0].cnt);
+              }
+              __syncthreads();
+              merge_split<DT>(c, vld(F.own_n), vld(F.seg_ovf), tca, 0ull, tmi);
+              const uint32_t c_above = vld(F.bc.u[BU_CHI]);
               const uint32_t n_in = vld(F.bc.u[BU_S2]);
               const bool ovf_in = vld(F.bc.u[BU_OVF2]) != 0u;
-              const uint32_t c_above = vld(F.bc.u[BU_CHI]);
-              const unsigned long long m_above = vld(F.bc.x[BX_MHI]), m_in = vld(F.bc.x[BX_MLO]);
-              const unsigned long long target = f2_to_u64(f2_mul(f2_mul(Zm, pr), scale));
+              const unsigned long long m_in = vld(F.bc.x[BX_MLO]);
               // the exact masses confirm the bracket: search the lists (a
               // test flag treats the bracket as missed)
               if (!ovf_in && m_above < target && target <= m_above + m_in &&
                   (P.flags & QRITA_FLAG_HIST_MISS) == 0u) {
                 rank_counts_from<DT>(c, F.rank_n);
                 s.lo = lo_key;
-                s.hi = to_top ? f2key(row_max) : hi_key;
+                s.hi = hi_key;
                 s.c_lo = c_above + n_in;
                 s.c_hi = c_above;
                 s.m_lo = m_above + m_in;
