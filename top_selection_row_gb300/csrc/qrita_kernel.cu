@@ -716,29 +716,65 @@ __device__ __forceinline__ float bf16_bit_value(const uint4 v, int p) {
 // straight from the raw units (only survivors are widened). A lane with
 // survivors claims its slots of the warp's segment with one shared atomic on
 // the warp's running count (F.seg_n[warp], zeroed before the pass): the
-// segment is unordered, so no warp scan is needed.
+// segment is unordered, so no warp scan is needed. The four units' bits are
+// folded into one 32-bit mask (unit j's low halves at bits 4j .. 4j + 3, its
+// high halves at 16 + 4j ..), so a lane walks its survivors in one loop
+// whose trip count is the warp's largest count of the piece; bit p names
+// word p & 15 of the four units (a tree of selects) and its half p >> 4.
+static_assert(kPieceThreadUnits == 4, "four units of 4 + 4 survivor bits fill one 32-bit mask");
 template <int DT>
 __device__ __forceinline__ void append_piece_bf16(Ctx<DT>& c, uint32_t seg_base, uint32_t segcap,
                                                   const uint4 (&v)[kPieceThreadUnits],
                                                   const uint32_t (&bits)[kPieceThreadUnits], int u0) {
   const int tid = threadIdx.x, warp = tid >> 5;
-  uint32_t cnt = 0;
+  uint32_t all = 0u;
 #pragma unroll
-  for (int j = 0; j < kPieceThreadUnits; ++j) cnt += __popc(bits[j]);
-  if (cnt == 0u) return;
-  uint32_t pos = atomicAdd(&c.F->seg_n[warp], cnt);
+  for (int j = 0; j < kPieceThreadUnits; ++j) all |= bits[j] << (4 * j);
+  if (all == 0u) return;
+  uint32_t pos = atomicAdd(&c.F->seg_n[warp], static_cast<uint32_t>(__popc(all)));
+  const uint32_t idx_base = static_cast<uint32_t>(c.head_n + (u0 + tid) * 8);
+  while (all != 0u) {
+    const uint32_t p = static_cast<uint32_t>(__ffs(all) - 1);
+    all &= all - 1u;
+    const bool b0 = (p & 1u) != 0u, b1 = (p & 2u) != 0u, b2 = (p & 4u) != 0u, b3 = (p & 8u) != 0u;
+    uint32_t wj[kPieceThreadUnits];
 #pragma unroll
-  for (int j = 0; j < kPieceThreadUnits; ++j) {
-    uint32_t b = bits[j];
-    const uint32_t idx0 = static_cast<uint32_t>(c.head_n + (u0 + j * kThreads + tid) * 8);
-    while (b != 0u) {
-      const int p = __ffs(b) - 1;
-      b &= b - 1u;
-      if (pos < segcap) {
-        c.own_val[seg_base + pos] = bf16_bit_value(v[j], p);
-        c.own_idx[seg_base + pos] = idx0 + static_cast<uint32_t>(bf16_bit_elem(p));
-      }
-      ++pos;
+    for (int j = 0; j < kPieceThreadUnits; ++j)
+      wj[j] = b1 ? (b0 ? v[j].w : v[j].z) : (b0 ? v[j].y : v[j].x);
+    const uint32_t w = b3 ? (b2 ? wj[3] : wj[2]) : (b2 ? wj[1] : wj[0]);
+    const uint32_t hi = p >> 4;
+    // unit (p >> 2) & 3, element 2 (p & 3) + half
+    const uint32_t idx = idx_base + ((p >> 2) & 3u) * (kThreads * 8u) + (((p & 3u) << 1) | hi);
+    if (pos < segcap) {
+      c.own_val[seg_base + pos] = __uint_as_float(hi ? (w & 0xFFFF0000u) : (w << 16));
+      c.own_idx[seg_base + pos] = idx;
+    }
+    ++pos;
+  }
+}
+
+// The values of this warp's segment entries [0, ns) read back from the row by
+// their indices, eight loads a lane in flight (entries listed by index only;
+// the warp's own index writes are visible after a barrier).
+template <int DT>
+__device__ __forceinline__ void gather_segment_values(Ctx<DT>& c, uint32_t seg_base, uint32_t ns) {
+  constexpr int S = Ctx<DT>::S;
+  constexpr int kG = 8;
+  const int lane = threadIdx.x & 31;
+  for (uint32_t k0 = 0; k0 < ns; k0 += 32u * kG) {
+    uint32_t ix[kG];
+    float x[kG];
+#pragma unroll
+    for (int q = 0; q < kG; ++q) {
+      const uint32_t k = k0 + static_cast<uint32_t>(q * 32 + lane);
+      ix[q] = k < ns ? c.own_idx[seg_base + k] : 0u;
+    }
+#pragma unroll
+    for (int q = 0; q < kG; ++q) x[q] = load_elem<DT>(c.gx + static_cast<size_t>(ix[q]) * S);
+#pragma unroll
+    for (int q = 0; q < kG; ++q) {
+      const uint32_t k = k0 + static_cast<uint32_t>(q * 32 + lane);
+      if (k < ns) c.own_val[seg_base + k] = x[q];
     }
   }
 }
@@ -1452,25 +1488,9 @@ __device__ uint32_t code_pass(Ctx<DT>& c, uint32_t c_lo, uint32_t c_hi) {
     above += b;
   }
   __syncthreads();
-  // the listed logits' values, loaded together (four a lane in flight)
+  // the listed logits' values, loaded together
   const uint32_t wn = vld(F.seg_n[warp]);
-  const uint32_t ns = min(wn, segcap);
-  for (uint32_t k0 = 0; k0 < ns; k0 += 128u) {
-    uint32_t ix[4];
-    float x[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t k = k0 + static_cast<uint32_t>(q * 32 + lane);
-      ix[q] = k < ns ? c.own_idx[seg_base + k] : 0u;
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) x[q] = load_elem<DT>(c.gx + static_cast<size_t>(ix[q]) * S);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t k = k0 + static_cast<uint32_t>(q * 32 + lane);
-      if (k < ns) c.own_val[seg_base + k] = x[q];
-    }
-  }
+  gather_segment_values<DT>(c, seg_base, min(wn, segcap));
   own_segments_streamed<DT>(c, wn);
   return above;
 }
