@@ -498,6 +498,7 @@ struct Ctx {
   float fix_scale;  // fixed-point scale of weights in [0, 1]
   bool zero_fill;       // the chunk's mask is to be zeroed early (by the search tail)
   bool zero_fill_done;  // and it was
+  bool one_fill_done;   // a keep-all row's mask was filled with 1 by the streaming pass
   bool give_up_once;    // test flag: the next bounded copy wait reports that it gave up
   int split;            // bins of a list-search round and of a tail split (64; 4 or 2 by flag)
   int npiv;             // pivots of a narrowing pass (15; 3 or 1 by flag)
@@ -3045,6 +3046,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   c.fix_scale = 0.f;
   c.zero_fill = false;
   c.zero_fill_done = false;
+  c.one_fill_done = false;
 
   const int64_t r = P.heavy_first ? heavy_first_row(P, F, blockIdx.x / P.C) : blockIdx.x / P.C;
   const int32_t V = P.V;
@@ -3400,15 +3402,20 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     // zero the mask later): the emission then only scatters the kept ids from
     // the lists; a row that ends on another path rewrites every byte
     const bool zfill = !p_only && trunc && k_on && c.C == 1u;
+    // keep-all rows on one CTA write their 1s the same way (a row found
+    // non-finite is rewritten by the emission)
+    const bool ofill = keep_all && c.C == 1u;
+    const uint32_t fill_w = ofill ? 0x01010101u : 0u;
+    const uint8_t fill_b = ofill ? 1 : 0;
     const bool zvec = (reinterpret_cast<uintptr_t>(c.gmask + c.head_n) % E) == 0u;
-    auto zero_unit = [&](int u) {
+    auto fill_unit = [&](int u) {
       uint8_t* dst = c.gmask + c.head_n + static_cast<size_t>(u) * E;
       if (zvec) {
-        if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = 0u;
-        else *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
+        if constexpr (E == 4) *reinterpret_cast<uint32_t*>(dst) = fill_w;
+        else *reinterpret_cast<uint2*>(dst) = make_uint2(fill_w, fill_w);
       } else {
 #pragma unroll
-        for (int e = 0; e < E; ++e) dst[e] = 0;
+        for (int e = 0; e < E; ++e) dst[e] = fill_b;
       }
     };
     auto col_put = [&](float x, uint32_t idx) {
@@ -3446,7 +3453,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
       constexpr bool PO = decltype(po)::value;
       constexpr bool COL = decltype(cm)::value;
       constexpr bool PH = decltype(hc)::value;
-      constexpr bool ZF = decltype(zf)::value;  // zero the mask while streaming
+      constexpr bool ZF = decltype(zf)::value;  // fill the mask while streaming (zeros; 1s on keep-all rows)
       stream_pieces<DT>(
           c,
           [&](const uint4 (&v)[kPieceThreadUnits], int u0, int n) {
@@ -3462,7 +3469,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
                   vmax2 = bf2_max_nan(vmax2, bf2_max_nan(bf2_max_nan(u.x, u.y), bf2_max_nan(u.z, u.w)));
                   vmin2 = bf2_min(vmin2, bf2_min(bf2_min(u.x, u.y), bf2_min(u.z, u.w)));
                   if (trunc) bits[j] = bf16_unit_bits(u, t2);
-                  if constexpr (ZF) zero_unit(u0 + j * kThreads + tid);
+                  if constexpr (ZF) fill_unit(u0 + j * kThreads + tid);
                 }
               }
               if constexpr (COL) {
@@ -3489,7 +3496,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               unpack<DT>(v[j], xs[j]);
               bits[j] = 0u;
               if (j * kThreads + tid < n) {
-                if constexpr (!PO && ZF) zero_unit(u0 + j * kThreads + tid);
+                if constexpr (!PO && ZF) fill_unit(u0 + j * kThreads + tid);
                 uint32_t cw[E / 4] = {};  // code bytes (PH)
 #pragma unroll
                 for (int e = 0; e < E; ++e) {
@@ -3557,7 +3564,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
               vmin = fminf(vmin, x);
               const bool surv = trunc && x >= t;
               bits = surv ? 1u : 0u;
-              if constexpr (!PO && ZF) c.gmask[idx] = 0;
+              if constexpr (!PO && ZF) c.gmask[idx] = fill_b;
               if constexpr (PO) {
                 const float w = exp_shifted(x, m_ref);
                 f2_add(zs, w);
@@ -3680,10 +3687,11 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
     else if (p_only) streaming_pass(BoolC<true>{}, BoolC<false>{}, BoolC<false>{}, BoolC<false>{});
     else if (col && zfill) streaming_pass(BoolC<false>{}, BoolC<true>{}, BoolC<false>{}, BoolC<true>{});
     else if (col) streaming_pass(BoolC<false>{}, BoolC<true>{}, BoolC<false>{}, BoolC<false>{});
-    else if (zfill) streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{}, BoolC<true>{});
+    else if (zfill || ofill) streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{}, BoolC<true>{});
     else streaming_pass(BoolC<false>{}, BoolC<false>{}, BoolC<false>{}, BoolC<false>{});
     QRITA_T(2);
     c.zero_fill_done = zfill;
+    c.one_fill_done = ofill;
     if (col) {
       own_columns_streamed<DT>(c, cn);
       // bf16 rows place their boundaries with the key histogram, which reads
@@ -4527,9 +4535,9 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const __grid_consta
   if (kw_emitted) {
     // written
   } else if (sel_all || sel_none || list_emit) {
-    // fill the chunk's mask (unless the search tail zeroed it already), then
-    // scatter the kept ids of the own list
-    if (sel_all || sel_none || !(zero_filled || ph_mask)) fill_mask<DT>(c, sel_all ? 1 : 0);
+    // fill the chunk's mask (unless the streaming pass or the search tail
+    // filled it already), then scatter the kept ids of the own list
+    if (sel_all ? !c.one_fill_done : (sel_none || !(zero_filled || ph_mask))) fill_mask<DT>(c, sel_all ? 1 : 0);
     if (list_emit && !sel_all && !sel_none) {
       __syncthreads();  // the fill is ordered before the scatter
       if (fused_ties) {
