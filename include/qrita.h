@@ -93,9 +93,9 @@ enum {
 #define QRITA_FLAG_FORCE_RETRY 0x8u    /* top-k rows: treat the first truncation as a
                                           miss, so the second truncation runs */
 #define QRITA_FLAG_HIST_MISS 0x10u     /* top-p rows binned by the streaming pass: after
-                                          the pass that extracts the bins, treat their
-                                          bracket as missed, so the narrowing passes run
-                                          (and the mask is written again) */
+                                          the pass that lists the boundary's bin, treat
+                                          its bracket as missed, so the narrowing passes
+                                          run (and the mask is written again) */
 #define QRITA_FLAG_CLUSTER_SHIFT 8     /* bits 8..10: force 2^n CTAs per row (n in 0..4);
                                           0 in these bits and bit 11 clear = automatic */
 #define QRITA_FLAG_CLUSTER_SET 0x800u  /* bit 11: the cluster-size bits are set */
