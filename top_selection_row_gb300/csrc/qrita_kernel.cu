@@ -1679,6 +1679,31 @@ __device__ __forceinline__ void own_for(Ctx<DT>& c, Fn&& fn) {
   for (uint32_t i = static_cast<uint32_t>(lane); i < n; i += 32u) fn(c.own_val[base + i], c.own_idx[base + i]);
 }
 
+// fn(value, index, valid) over this thread's share of the own list, like
+// own_for, but every lane of a warp runs the same number of steps (a lane past
+// its share passes valid = false), so fn may use full-warp collectives.
+template <int DT, typename Fn>
+__device__ __forceinline__ void own_for_warp(Ctx<DT>& c, Fn&& fn) {
+  Fixed& F = *c.F;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (vld(F.col_mode) != 0u) {
+    const uint32_t n = vld(F.col_n[threadIdx.x]);
+    const uint32_t nmax = __reduce_max_sync(kFull, n);
+    for (uint32_t j = 0; j < nmax; ++j) {
+      const bool v = j < n;
+      const uint32_t i = j * kThreads + threadIdx.x;
+      fn(v ? c.own_val[i] : 0.f, v ? c.own_idx[i] : 0u, v);
+    }
+    return;
+  }
+  const uint32_t base = vld(F.seg_base[warp]), n = vld(F.seg_cnt[warp]);
+  for (uint32_t i0 = 0; i0 < n; i0 += 32u) {
+    const uint32_t i = i0 + static_cast<uint32_t>(lane);
+    const bool v = i < n;
+    fn(v ? c.own_val[base + i] : 0.f, v ? c.own_idx[base + i] : 0u, v);
+  }
+}
+
 // Per-rank own-list counts above the search's lo and hi (F.rank_lo,
 // F.rank_hi): n[r] entries of rank r lie above lo, none above hi.
 template <int DT>
@@ -2415,29 +2440,44 @@ __device__ uint32_t tie_index_cut(Ctx<DT>& c, float tau_f, uint32_t keep, bool m
   Fixed& F = *c.F;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // the tie group's indices, compacted into the ring's bytes (no stream is in
-  // flight); a group too large for them is scanned in the own list
+  // flight); a group too large for them is scanned in the own list. Each
+  // warp lists its own in a region of the ring's upper half, counting with
+  // its ballots (no atomics); the regions are then packed in warp order.
   uint32_t* tix = reinterpret_cast<uint32_t*>(const_cast<uint4*>(c.ring_ptr));
-  static_assert(kTieDirect + kThreads <= kTieCap, "the index histogram fits after a small group");
+  static_assert(kTieDirect + kThreads <= kTieCap / 2, "the index histogram fits after a small group");
+  constexpr uint32_t kWarpTies = kTieCap / 2 / kWarps;
+  uint32_t* wreg = tix + kTieCap / 2 + static_cast<uint32_t>(warp) * kWarpTies;
   __syncthreads();  // earlier users of the ring's bytes are done
-  if (tid == 0) F.tail_n = 0u;
-  __syncthreads();
-  own_for(c, [&](float x, uint32_t ix) {
-    if (mark_above && x > tau_f) c.gmask[ix] = 1;
-    const bool eq = x == tau_f;
-    // positions: one shared atomic per warp step
-    const uint32_t am = __activemask();
-    const uint32_t bal = __ballot_sync(am, eq);
-    const int leader = __ffs(bal) - 1;
-    uint32_t wbase = 0;
-    if (lane == leader) wbase = atomicAdd(&F.tail_n, static_cast<uint32_t>(__popc(bal)));
-    wbase = __shfl_sync(am, wbase, leader < 0 ? 0 : leader);
+  // wn: the warp's ties so far (warp-uniform: every lane takes every step)
+  uint32_t wn = 0;
+  own_for_warp(c, [&](float x, uint32_t ix, bool v) {
+    if (v && mark_above && x > tau_f) c.gmask[ix] = 1;
+    const bool eq = v && x == tau_f;
+    const uint32_t bal = __ballot_sync(kFull, eq);
     if (eq) {
-      const uint32_t pos = wbase + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
-      if (pos < kTieCap) tix[pos] = ix;
+      const uint32_t pos = wn + static_cast<uint32_t>(__popc(bal & ((1u << lane) - 1u)));
+      if (pos < kWarpTies) wreg[pos] = ix;
     }
+    wn += static_cast<uint32_t>(__popc(bal));
   });
+  if (lane == 0) F.redu[warp][0] = wn;
   __syncthreads();
-  const uint32_t nt = vld(F.tail_n);
+  uint32_t wbase = 0, nt = 0;
+  bool ovf = false;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const uint32_t n = vld(F.redu[w][0]);
+    wbase += w < warp ? n : 0u;
+    nt += n;
+    ovf = ovf || n > kWarpTies;
+  }
+  if (!ovf)
+    for (uint32_t k = static_cast<uint32_t>(lane); k < wn; k += 32u) tix[wbase + k] = wreg[k];
+  // a warp's overflow leaves the group in the own list only (the count as a
+  // group too large for the ring, for the emission too)
+  if (tid == 0) F.tail_n = ovf ? kTieCap + 1u : nt;
+  __syncthreads();
+  if (ovf) nt = kTieCap + 1u;
   if (nt <= static_cast<uint32_t>(kThreads)) return small_index_cut(F, tix, nt, keep);
   if (nt <= kTieDirect) {
     // a small group: the keep-th smallest index (the (nt + 1 - keep)-th
